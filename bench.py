@@ -1,0 +1,453 @@
+"""Benchmark: one decode step of paged GQA attention over the token pool.
+
+A step is the whole hot path for one batch: the per-step plan (host partition +
+upload), then for every layer the KV append scatter and the split-KV decode
+attention (with its LSE merge). Inputs are seeded synthetic tensors shaped like
+the Qwen3-4B / Qwen3.5 decode workloads (see workloads.py), resident in HBM when
+the timed region starts.
+
+    python bench.py [--config N] [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0). Under torchrun (N > 1) every rank runs an
+independent replica of the step (the path has no exchange step); the time is the
+max over ranks and the value sums all ranks' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged GQA decode attn: HBM GB/s & % of peak; µs/step at batch 8/32/128"
+DEFAULT_CONFIG = 2
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# workload state and the step
+# ---------------------------------------------------------------------------
+
+class StepState:
+    """Device tensors of one decode step for every layer, plus the plan."""
+
+    def __init__(self, wl: workloads.Workload, device="cuda", layers=None,
+                 poison_unreferenced=False):
+        import paged_kv_gqa_tokentokvpool_gb300 as pkv
+        self.pkv = pkv
+        self.wl = wl
+        self.device = torch.device(device)
+        self.layer_ids = list(range(wl.layers)) if layers is None else list(layers)
+        self.q, self.k_pool, self.v_pool, self.k_new, self.v_new = [], [], [], [], []
+        for l in self.layer_ids:
+            t = workloads.layer_tensors(wl, l, device=self.device,
+                                        poison_unreferenced=poison_unreferenced)
+            self.q.append(t.q)
+            self.k_pool.append(t.k_pool)
+            self.v_pool.append(t.v_pool)
+            self.k_new.append(t.k_new)
+            self.v_new.append(t.v_new)
+        B, Hq, D = wl.batch, wl.n_qo_heads, wl.head_dim
+        n = len(self.layer_ids)
+        self.out = [torch.empty(B, Hq, D, dtype=torch.bfloat16, device=self.device) for _ in range(n)]
+        self.lse = [torch.empty(B, Hq, dtype=torch.float32, device=self.device) for _ in range(n)]
+        self.kv_indptr_host = torch.from_numpy(wl.kv_indptr.copy())
+        self.kv_indptr = self.kv_indptr_host.to(self.device)
+        self.kv_indices = torch.from_numpy(wl.kv_indices.copy()).to(self.device)
+        self.slot_ids = torch.from_numpy(wl.append_slots.copy()).to(self.device)
+        self.plan = pkv.paged_decode_plan_create(max(B, 1), max(wl.total_tokens, 1), Hq,
+                                                 wl.n_kv_heads, D)
+        self.launches_per_step = None
+
+    def run(self, attn_events=None):
+        """One decode step on the current stream. attn_events: list to which
+        (start, end) CUDA events around each attention call are appended."""
+        pkv, wl = self.pkv, self.wl
+        stream = torch.cuda.current_stream()
+        pkv.paged_decode_plan(self.plan, self.kv_indptr_host.numpy(), stream=stream)
+        for i in range(len(self.layer_ids)):
+            pkv.kvpool_append(self.k_pool[i], self.v_pool[i], self.slot_ids, self.k_new[i],
+                              self.v_new[i], stream=stream)
+            if attn_events is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            pkv.paged_decode_attn(self.q[i], self.k_pool[i], self.v_pool[i], self.kv_indptr,
+                                  self.kv_indices, wl.batch, wl.n_qo_heads, wl.n_kv_heads,
+                                  wl.head_dim, wl.sm_scale, self.out[i], self.lse[i], self.plan,
+                                  stream=stream)
+            if attn_events is not None:
+                e1.record(stream)
+                attn_events.append((e0, e1))
+        if self.launches_per_step is None:
+            info = self.plan.info()
+            per_layer = (1 if len(wl.append_slots) else 0) + (1 if info["n_units"] else 0) \
+                + (1 if info["n_merges"] else 0)
+            self.launches_per_step = per_layer * len(self.layer_ids)
+
+
+class HostIO:
+    """Pinned host copies of one step's inputs and outputs, for the end-to-end
+    measurement: every step copies q, the new K/V rows and the slot/index arrays
+    host->device, runs the step, and copies out and lse device->host."""
+
+    def __init__(self, st: StepState):
+        self.st = st
+        pin = dict(pin_memory=True)
+        self.q = [t.cpu().pin_memory() for t in st.q]
+        self.k_new = [t.cpu().pin_memory() for t in st.k_new]
+        self.v_new = [t.cpu().pin_memory() for t in st.v_new]
+        self.kv_indices = st.kv_indices.cpu().pin_memory()
+        self.kv_indptr = st.kv_indptr.cpu().pin_memory()
+        self.slot_ids = st.slot_ids.cpu().pin_memory()
+        self.out = [torch.empty(t.shape, dtype=t.dtype, **pin) for t in st.out]
+        self.lse = [torch.empty(t.shape, dtype=t.dtype, **pin) for t in st.lse]
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in
+                             self.q + self.k_new + self.v_new
+                             + [self.kv_indices, self.kv_indptr, self.slot_ids])
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.out + self.lse)
+
+    def run(self):
+        st = self.st
+        for dst, src in zip(st.q, self.q):
+            dst.copy_(src, non_blocking=True)
+        for dst, src in zip(st.k_new, self.k_new):
+            dst.copy_(src, non_blocking=True)
+        for dst, src in zip(st.v_new, self.v_new):
+            dst.copy_(src, non_blocking=True)
+        st.kv_indices.copy_(self.kv_indices, non_blocking=True)
+        st.kv_indptr.copy_(self.kv_indptr, non_blocking=True)
+        st.slot_ids.copy_(self.slot_ids, non_blocking=True)
+        st.run()
+        for dst, src in zip(self.out, st.out):
+            dst.copy_(src, non_blocking=True)
+        for dst, src in zip(self.lse, st.lse):
+            dst.copy_(src, non_blocking=True)
+
+
+def step_bytes(wl: workloads.Workload) -> dict:
+    """Algorithmic HBM bytes of one step: each distinct KV row read once per layer,
+    the slot indices, q, out and lse, and the append's read + write of new rows."""
+    B, Hq, Hkv, D = wl.batch, wl.n_qo_heads, wl.n_kv_heads, wl.head_dim
+    row = Hkv * D * 2  # bytes of one slot's K (or V) for all heads
+    n_unique = int(np.unique(wl.kv_indices).size)
+    N = wl.total_tokens
+    attn = n_unique * 2 * row + N * 4 + (B + 1) * 4 + B * Hq * D * 2 * 2 + B * Hq * 4
+    attn_logical = N * 2 * row + N * 4 + (B + 1) * 4 + B * Hq * D * 2 * 2 + B * Hq * 4
+    n_app = len(wl.append_slots)
+    append = n_app * 2 * row * 2 + n_app * 4
+    return {"attn_per_layer": attn, "attn_logical_per_layer": attn_logical,
+            "append_per_layer": append,
+            "step": wl.layers * (attn + append),
+            "step_logical": wl.layers * (attn_logical + append)}
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "of measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "of fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(st: StepState, budget_s: float = 12.0, max_layers=None):
+    """Time the fp64 oracle on the host cores over a bounded sample of the same
+    step: whole layers (all requests), until ~budget_s of oracle time is spent."""
+    import oracle
+    orc = oracle.default()
+    wl = st.wl
+    threads = orc.max_threads()
+    total_t, total_bytes, layers_done = 0.0, 0, 0
+    per_layer = step_bytes(wl)["attn_per_layer"]
+    uniq, inv = np.unique(wl.kv_indices, return_inverse=True)
+    idx_dev = torch.from_numpy(uniq.astype(np.int64)).to(st.device)
+    compact = inv.astype(np.int32)
+    limit = len(st.layer_ids) if max_layers is None else min(max_layers, len(st.layer_ids))
+    for i in range(limit):
+        k = workloads.bf16_bits(st.k_pool[i].index_select(0, idx_dev))
+        v = workloads.bf16_bits(st.v_pool[i].index_select(0, idx_dev))
+        q = workloads.bf16_bits(st.q[i])
+        t0 = time.perf_counter()
+        orc.decode(q, k, v, wl.kv_indptr, compact, wl.n_qo_heads, wl.n_kv_heads,
+                   wl.head_dim, wl.sm_scale)
+        total_t += time.perf_counter() - t0
+        total_bytes += per_layer
+        layers_done += 1
+        if total_t >= budget_s:
+            break
+    return {"value": total_bytes / total_t / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{layers_done} of {wl.layers} layers of {wl.name} (all {wl.batch} "
+                      f"requests, attention only), fp64 C++ oracle, {total_t:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step is the oracle over one layer of
+    the workload (all requests), on the host cores."""
+    if rank != 0:
+        return 0
+    wl = workloads.config_workload(args.config)
+    import oracle
+    orc = oracle.default()
+    bytes_layer = step_bytes(wl)["attn_per_layer"]
+    t = workloads.layer_tensors(wl, 0, device="cpu")
+    uniq, inv = np.unique(wl.kv_indices, return_inverse=True)
+    k = workloads.bf16_bits(t.k_pool[torch.from_numpy(uniq.astype(np.int64))])
+    v = workloads.bf16_bits(t.v_pool[torch.from_numpy(uniq.astype(np.int64))])
+    q = workloads.bf16_bits(t.q)
+    compact = inv.astype(np.int32)
+
+    def one():
+        orc.decode(q, k, v, wl.kv_indptr, compact, wl.n_qo_heads, wl.n_kv_heads,
+                   wl.head_dim, wl.sm_scale)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    value = bytes_layer * args.steps / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: {wl.description}",
+                       "sample": "one layer (all requests) per step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": orc.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"layer 0 of {wl.layers} of {wl.name}, all "
+                                       f"{wl.batch} requests, per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers of the workload (small profiling "
+                         "captures); the JSON line records it")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+
+    wl = workloads.config_workload(args.config)
+    if args.layers is not None:
+        wl.layers = max(1, min(args.layers, wl.layers))
+        wl.description += f" [first {wl.layers} layers only]"
+    st = StepState(wl)
+    nbytes = step_bytes(wl)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        st.run()
+    barrier()
+    attn_events = []
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    gpu_id = visible[local].strip() if local < len(visible) and visible[local].strip() else str(local)
+    with ClockSampler(gpu_id) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            st.run(attn_events)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = start.elapsed_time(end)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_events]
+    if pg is not None:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # end to end through the public API, host buffers in and out
+    io = HostIO(st)
+    for _ in range(args.warmup):
+        io.run()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        io.run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return 0
+
+    ms_per_step = elapsed_ms / args.steps
+    value = world * nbytes["step"] * args.steps / (elapsed_ms * 1e-3) / 1e9
+    e2e_value = world * nbytes["step"] * args.steps / (e2e_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    attn_avg_ms = statistics.mean(attn_ms)
+    achieved = nbytes["attn_per_layer"] / (attn_avg_ms * 1e-3) / 1e9
+    info = st.plan.info()
+    traffic = _profiled_traffic(args.config)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{wl.name}: {wl.description}", "layers": wl.layers,
+            "batch": wl.batch, "n_qo_heads": wl.n_qo_heads, "n_kv_heads": wl.n_kv_heads,
+            "head_dim": wl.head_dim, "pool_slots": wl.pool_slots,
+            "total_context_tokens": wl.total_tokens, "us_per_step": ms_per_step * 1e3,
+            "hbm_frac_of_peak": value / peak, "peak_gbs": peak, "peak_kind": peak_kind,
+            "effective_logical_gbs": world * nbytes["step_logical"] * args.steps
+            / (elapsed_ms * 1e-3) / 1e9,
+            "plan": {"units": info["n_units"], "merges": info["n_merges"],
+                     "chunk_tokens": info["chunk_tokens"]},
+            "l2": f"inputs larger than L2: each step reads {nbytes['step'] / 1e9:.2f} GB "
+                  f"across {wl.layers} layers' pools (L2 {L2_BYTES / 2**20:.0f} MiB)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "paged_decode_attn (split-KV kernel + LSE merge), "
+                               f"avg of {len(attn_ms)} calls {attn_avg_ms * 1e3:.1f} us, "
+                               f"{nbytes['attn_per_layer'] / 1e6:.1f} MB algorithmic",
+                     "peak_kind": peak_kind},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": io.h2d_bytes,
+                "d2h_bytes_per_step": io.d2h_bytes, "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(st, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def _profiled_traffic(config_no: int):
+    """DRAM bytes per attention call from the committed ncu summary of this
+    workload, if one exists for the current kernels (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d.get(str(config_no))
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,181 @@
+/*
+ * pkv.h — C ABI of the paged GQA decode-attention library (sm_103a, GB300).
+ *
+ * The problem these calls solve is stated in "Agent-Infer: 纯 Rust 编写的高性能 LLM
+ * 推理引擎", section "分页 KV 缓存" (paged KV cache): the KV cache is a token pool
+ * with page size 1 (SGLang's TokenToKVPool), one decode step is batched across all
+ * requests, the attention work plan is built once per step rather than once per
+ * layer, and its buffers are preallocated (same page, section "优化历程", stages 2
+ * and 3). Grouped-query attention with 32 query heads on 8 KV heads at head_dim
+ * 128, and head_dim 256 for the hybrid model's full-attention layers, come from
+ * "Pegainfer: 纯Rust+CUDA构建的LLM推理引擎", sections "1. 注意力机制优化" and
+ * "2. Qwen3.5的混合架构支持".
+ *
+ * Conventions for every call:
+ *  - Pointers are plain device addresses unless a parameter name ends in _host.
+ *    The caller owns every buffer it passes; no call keeps a pointer after it
+ *    returns, except that the device work (kernels, copies) it enqueued on
+ *    `stream` reads and writes them until that work completes.
+ *  - bf16 means IEEE bfloat16 bit patterns (2 bytes, little endian).
+ *  - Layouts are dense row-major:
+ *      pool  (K or V): [pool_slots, n_kv_heads, head_dim] bf16 — one pool row per
+ *                      token slot; one (slot, head) row is head_dim*2 bytes
+ *      q, out        : [batch, n_qo_heads, head_dim] bf16
+ *      lse           : [batch, n_qo_heads] fp32
+ *      kv_indptr     : [batch + 1] int32, kv_indptr[0] = 0, non-decreasing
+ *      kv_indices    : [kv_indptr[batch]] int32 pool slots; request b attends over
+ *                      kv_indices[kv_indptr[b] .. kv_indptr[b+1]) in that order
+ *    Query head h reads KV head h / (n_qo_heads / n_kv_heads).
+ *  - Device pointers to q, pools, new rows and out must be 16-byte aligned.
+ *  - Every call returns PKV_OK (0) or a negative PKV_ERR_* code, and checks its
+ *    arguments on the host before anything is enqueued; on an error nothing is
+ *    enqueued. pkv_last_error() then describes the failure (per thread).
+ *  - No call synchronises the stream or allocates device memory, except
+ *    paged_decode_plan_create / _destroy and the optional debug checks
+ *    (pkv_set_debug_checks), which copy index arrays to the host synchronously.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - Supported shapes: head_dim 128 or 256; n_qo_heads a multiple of n_kv_heads
+ *    with group size G = n_qo_heads / n_kv_heads in {1, 2, 4, 8};
+ *    1 <= n_kv_heads <= 8.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pkv_stream_t; /* same type as cudaStream_t */
+typedef struct pkv_plan pkv_plan;          /* opaque, owned by the library */
+
+enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1, /* null pointer, negative size, misalignment, bad CSR */
+    PKV_ERR_UNSUPPORTED = -2, /* head_dim / group size / head count not supported */
+    PKV_ERR_PLAN = -3,        /* plan missing, too small, or built for other shapes */
+    PKV_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
+    PKV_ERR_INDEX = -5        /* debug checks: slot id out of range / indptr mismatch */
+};
+
+/*
+ * kvpool_append — write this step's new K/V rows into their pool slots.
+ *   k_pool[slot_ids[i], :, :] = k_new[i, :, :]  and  v_pool[...] = v_new[i, :, :]
+ * for i < n. This is the scatter that fills the page-size-1 token pool each decode
+ * step ("Agent-Infer", section "分页 KV 缓存"; the step's scatter is named in
+ * section "优化历程", stage 7).
+ *   k_pool, v_pool : [pool_slots, n_kv_heads, head_dim] bf16, written in place
+ *   slot_ids       : [n] int32 device array; ids must be distinct and in
+ *                    [0, pool_slots) — duplicates leave the row undefined; an
+ *                    out-of-range id is reported (PKV_ERR_INDEX) only when debug
+ *                    checks are on
+ *   k_new, v_new   : [n, n_kv_heads, head_dim] bf16
+ *   n              : number of rows (0 is a no-op)
+ * The copy is bit-exact. Enqueued on `stream`; returns without waiting.
+ */
+int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const void* k_new,
+                  const void* v_new, int64_t n, int n_kv_heads, int head_dim,
+                  int64_t pool_slots, pkv_stream_t stream);
+
+/*
+ * paged_decode_plan_create — allocate a reusable plan for one model shape.
+ * Sizes every buffer once (pinned host staging, device work list, split
+ * workspace) so that no decode step allocates ("Agent-Infer", section "优化历程",
+ * stage 2: preallocated buffers).
+ *   *plan      : receives the new plan
+ *   max_batch  : largest batch any step will use (>= 1)
+ *   max_tokens : largest kv_indptr[batch] any step will use (>= 0)
+ *   n_qo_heads, n_kv_heads, head_dim : the attention shape the plan serves
+ * Uses the current CUDA device; the plan must be used on that device.
+ * Synchronous. Returns PKV_ERR_UNSUPPORTED for shapes outside the supported set.
+ */
+int paged_decode_plan_create(pkv_plan** plan, int max_batch, int64_t max_tokens,
+                             int n_qo_heads, int n_kv_heads, int head_dim);
+
+/*
+ * paged_decode_plan — build this step's work partition, once per decode step.
+ * ("Agent-Infer", section "分页 KV 缓存": the plan runs once per step, not once per
+ * layer; section "优化历程", stage 3.) Splits long contexts into chunks so that
+ * skewed batches fill every SM, and records which requests need a log-sum-exp
+ * merge. The result is copied to the device asynchronously on `stream` from the
+ * plan's pinned staging; every paged_decode_attn call of the step with this
+ * batch reuses it.
+ *   kv_indptr_host : [batch + 1] int32 HOST array, the same values as the device
+ *                    kv_indptr later passed to paged_decode_attn
+ *   batch          : 0 <= batch <= max_batch; kv_indptr_host[batch] <= max_tokens
+ * Before overwriting its staging the call waits (host side) for the previous
+ * step's plan copy to finish. Use the same stream (or order the streams) for the
+ * plan and the attention calls of a step.
+ */
+int paged_decode_plan(pkv_plan* plan, const int32_t* kv_indptr_host, int batch,
+                      pkv_stream_t stream);
+
+/*
+ * paged_decode_attn — batched decode attention over the token pool, once per layer.
+ * For every request b and query head h, with g = h / (n_qo_heads / n_kv_heads) and
+ * idx = kv_indices[kv_indptr[b] .. kv_indptr[b+1]):
+ *   s_j      = sm_scale * dot(q[b,h,:], K[idx_j, g, :])
+ *   lse[b,h] = ln sum_j exp(s_j)                      (natural log, scale included)
+ *   out[b,h] = sum_j exp(s_j - lse[b,h]) * V[idx_j, g, :]
+ * computed with fp32 accumulation and an online softmax; long contexts are split
+ * into chunks whose partial results are merged by log-sum-exp. An empty context
+ * gives out = 0 and lse = -inf.
+ *   q          : [batch, n_qo_heads, head_dim] bf16
+ *   k_pool, v_pool : [pool_slots, n_kv_heads, head_dim] bf16 (read only)
+ *   kv_indptr  : [batch + 1] int32 device array (must equal the plan's host copy)
+ *   kv_indices : int32 device array of pool slots (must be valid slots)
+ *   sm_scale   : the softmax scale (e.g. 1/sqrt(head_dim)), finite
+ *   out        : [batch, n_qo_heads, head_dim] bf16, written (round to nearest even)
+ *   lse        : [batch, n_qo_heads] fp32, written; may be NULL
+ *   plan       : built by paged_decode_plan for this step with the same batch and
+ *                created for the same (n_qo_heads, n_kv_heads, head_dim)
+ * Launches one split-KV kernel and, when any request was split, one merge kernel.
+ */
+int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* kv_indptr, const int32_t* kv_indices, int batch,
+                      int n_qo_heads, int n_kv_heads, int head_dim, float sm_scale,
+                      void* out, float* lse, const pkv_plan* plan, pkv_stream_t stream);
+
+/* paged_decode_plan_destroy — free a plan (waits for its pending copy). NULL is a no-op. */
+void paged_decode_plan_destroy(pkv_plan* plan);
+
+/*
+ * paged_decode_plan_host — the planner alone, on the host, with no CUDA call.
+ * Computes the work list paged_decode_plan would upload, for inspection and tests.
+ *   kv_indptr_host : [batch + 1] int32
+ *   num_sms, ctas_per_sm : the device's SM count and the split kernel's resident
+ *                    CTAs per SM (the plan uses the real values of its device)
+ *   units_out      : [max_units * 4] int32 — per work unit
+ *                    {request b, first token, end token (exclusive), partial slot
+ *                    or -1 when the unit writes out/lse directly}
+ *   merges_out     : [max_merges * 4] int32 — per split request
+ *                    {request b, first partial slot, number of parts, 0}
+ *   n_units, n_merges, chunk_tokens : receive the counts and the chunk length
+ * Returns PKV_ERR_PLAN if the output arrays are too small.
+ */
+int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int num_sms,
+                           int ctas_per_sm, int32_t* units_out, int max_units,
+                           int* n_units, int32_t* merges_out, int max_merges, int* n_merges,
+                           int* chunk_tokens);
+
+/* paged_decode_plan_info — counts of the plan's current step (any out pointer may be NULL). */
+int paged_decode_plan_info(const pkv_plan* plan, int* batch, int* n_units, int* n_merges,
+                           int* chunk_tokens, int* max_units);
+
+/*
+ * pkv_set_debug_checks — when on (nonzero), kvpool_append and paged_decode_attn
+ * also copy slot ids / indptr / indices to the host and check them (range, and
+ * agreement with the plan) before launching; this synchronises the stream.
+ * Off by default. Process-wide.
+ */
+void pkv_set_debug_checks(int on);
+
+/* pkv_last_error — message of the last failed call on this thread ("" if none). */
+const char* pkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

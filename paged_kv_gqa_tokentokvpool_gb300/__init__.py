@@ -1,0 +1,219 @@
+"""Paged GQA decode attention over a page-size-1 token KV pool, for GB300 (sm_103a).
+
+A thin ctypes binding of the C ABI in ``include/pkv.h`` (``libpkv.so``, built
+in-tree by ``build.py``). The functions keep the C names and argument order; they
+only turn torch tensors into pointers and sizes and raise ``PkvError`` on a
+negative return code. Every step of the computation runs in the library's CUDA
+kernels: there is no Python or CPU fallback, and importing this package fails
+if the library has not been built.
+
+Typical decode step (one plan per step, reused by every layer):
+
+    plan = paged_decode_plan_create(max_batch, max_tokens, 32, 8, 128)
+    paged_decode_plan(plan, kv_indptr_cpu)                 # once per step
+    for layer in layers:
+        kvpool_append(k_pool[l], v_pool[l], slot_ids, k_new[l], v_new[l])
+        paged_decode_attn(q[l], k_pool[l], v_pool[l], kv_indptr, kv_indices,
+                          batch, 32, 8, 128, sm_scale, out[l], lse[l], plan)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = -1
+PKV_ERR_UNSUPPORTED = -2
+PKV_ERR_PLAN = -3
+PKV_ERR_CUDA = -4
+PKV_ERR_INDEX = -5
+
+EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
+            "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",
+            "paged_decode_plan_info", "pkv_set_debug_checks", "pkv_last_error")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+        self.message = message
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first (python -m "
+            "paged_kv_gqa_tokentokvpool_gb300.build, or __graft_entry__.build()). "
+            "This package has no CPU fallback.")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.kvpool_append.argtypes = [P, P, P, P, P, I64, I32, I32, I64, P]
+    lib.paged_decode_plan_create.argtypes = [ctypes.POINTER(P), I32, I64, I32, I32, I32]
+    lib.paged_decode_plan.argtypes = [P, P, I32, P]
+    lib.paged_decode_attn.argtypes = [P, P, P, P, P, I32, I32, I32, I32, ctypes.c_float, P, P,
+                                      P, P]
+    lib.paged_decode_plan_destroy.argtypes = [P]
+    lib.paged_decode_plan_destroy.restype = None
+    lib.paged_decode_plan_host.argtypes = [P, I32, I32, I32, P, I32, P, P, I32, P, P]
+    lib.paged_decode_plan_info.argtypes = [P, P, P, P, P, P]
+    lib.pkv_set_debug_checks.argtypes = [I32]
+    lib.pkv_set_debug_checks.restype = None
+    lib.pkv_last_error.argtypes = []
+    lib.pkv_last_error.restype = ctypes.c_char_p
+    for name in ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
+                 "paged_decode_attn", "paged_decode_plan_host", "paged_decode_plan_info"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def pkv_last_error() -> str:
+    return _lib.pkv_last_error().decode()
+
+
+def pkv_set_debug_checks(on: bool) -> None:
+    _lib.pkv_set_debug_checks(1 if on else 0)
+
+
+def _check(rc: int) -> None:
+    if rc != PKV_OK:
+        raise PkvError(rc, pkv_last_error())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return ctypes.c_void_p(t.data_ptr())
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data_as(ctypes.c_void_p)
+    return ctypes.c_void_p(int(t))
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class Plan:
+    """Owns a ``pkv_plan*``; freed by ``paged_decode_plan_destroy`` or on collection."""
+
+    def __init__(self, handle: ctypes.c_void_p, shape):
+        self.handle = handle
+        self.shape = shape
+
+    def info(self) -> dict:
+        vals = [ctypes.c_int() for _ in range(5)]
+        _check(_lib.paged_decode_plan_info(self.handle, *[ctypes.byref(v) for v in vals]))
+        return dict(zip(("batch", "n_units", "n_merges", "chunk_tokens", "max_units"),
+                        (v.value for v in vals)))
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.paged_decode_plan_destroy(self.handle)
+            self.handle = None
+
+
+def kvpool_append(k_pool, v_pool, slot_ids, k_new, v_new, n=None, n_kv_heads=None,
+                  head_dim=None, pool_slots=None, stream=None) -> None:
+    """k_pool[slot_ids[i]] = k_new[i]; v_pool[slot_ids[i]] = v_new[i] (bit-exact)."""
+    _dev(k_pool, torch.bfloat16, "k_pool")
+    _dev(v_pool, torch.bfloat16, "v_pool")
+    _dev(slot_ids, torch.int32, "slot_ids")
+    _dev(k_new, torch.bfloat16, "k_new")
+    _dev(v_new, torch.bfloat16, "v_new")
+    S, hkv, d = k_pool.shape
+    if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape:
+        raise ValueError("pool / new-row shapes disagree")
+    n = slot_ids.numel() if n is None else n
+    _check(_lib.kvpool_append(_ptr(k_pool), _ptr(v_pool), _ptr(slot_ids), _ptr(k_new),
+                              _ptr(v_new), n, hkv if n_kv_heads is None else n_kv_heads,
+                              d if head_dim is None else head_dim,
+                              S if pool_slots is None else pool_slots, _stream(stream)))
+
+
+def paged_decode_plan_create(max_batch: int, max_tokens: int, n_qo_heads: int,
+                             n_kv_heads: int, head_dim: int) -> Plan:
+    h = ctypes.c_void_p()
+    _check(_lib.paged_decode_plan_create(ctypes.byref(h), max_batch, max_tokens, n_qo_heads,
+                                         n_kv_heads, head_dim))
+    return Plan(h, (n_qo_heads, n_kv_heads, head_dim))
+
+
+def _host_indptr(kv_indptr) -> np.ndarray:
+    if isinstance(kv_indptr, torch.Tensor):
+        if kv_indptr.is_cuda:
+            raise TypeError("paged_decode_plan takes the HOST copy of kv_indptr")
+        kv_indptr = kv_indptr.numpy()
+    return np.ascontiguousarray(kv_indptr, dtype=np.int32)
+
+
+def paged_decode_plan(plan: Plan, kv_indptr_host, batch=None, stream=None) -> None:
+    ip = _host_indptr(kv_indptr_host)
+    batch = ip.size - 1 if batch is None else batch
+    plan._indptr_keepalive = ip
+    _check(_lib.paged_decode_plan(plan.handle, _ptr(ip), batch, _stream(stream)))
+
+
+def paged_decode_attn(q, k_pool, v_pool, kv_indptr, kv_indices, batch, n_qo_heads,
+                      n_kv_heads, head_dim, sm_scale, out, lse, plan: Plan,
+                      stream=None) -> None:
+    _dev(q, torch.bfloat16, "q")
+    _dev(k_pool, torch.bfloat16, "k_pool")
+    _dev(v_pool, torch.bfloat16, "v_pool")
+    _dev(kv_indptr, torch.int32, "kv_indptr")
+    _dev(kv_indices, torch.int32, "kv_indices")
+    _dev(out, torch.bfloat16, "out")
+    if lse is not None:
+        _dev(lse, torch.float32, "lse")
+    _check(_lib.paged_decode_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indptr),
+                                  _ptr(kv_indices), batch, n_qo_heads, n_kv_heads, head_dim,
+                                  float(sm_scale), _ptr(out), _ptr(lse), plan.handle,
+                                  _stream(stream)))
+
+
+def paged_decode_plan_destroy(plan: Plan) -> None:
+    if plan.handle:
+        _lib.paged_decode_plan_destroy(plan.handle)
+        plan.handle = None
+
+
+def paged_decode_plan_host(kv_indptr_host, num_sms: int, ctas_per_sm: int,
+                           max_units: int = 1 << 16, max_merges: int = None):
+    """The planner alone (host, no CUDA). Returns (units [n,4], merges [m,4], chunk)."""
+    ip = _host_indptr(kv_indptr_host)
+    batch = ip.size - 1
+    max_merges = max(batch, 1) if max_merges is None else max_merges
+    units = np.zeros((max_units, 4), np.int32)
+    merges = np.zeros((max(max_merges, 1), 4), np.int32)
+    nu, nm, chunk = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(_lib.paged_decode_plan_host(_ptr(ip), batch, num_sms, ctas_per_sm, _ptr(units),
+                                       max_units, ctypes.byref(nu), _ptr(merges), max_merges,
+                                       ctypes.byref(nm), ctypes.byref(chunk)))
+    return units[:nu.value].copy(), merges[:nm.value].copy(), chunk.value

@@ -1,0 +1,301 @@
+// The C ABI (include/pkv.h): argument checks, plan lifetime, launches.
+//
+// Every entry point validates its arguments on the host and returns an error code
+// before enqueuing anything, so a bad call never reaches the GPU. The plan owns
+// the only memory the library allocates, sized once at creation.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+thread_local std::string g_last_error;
+int g_debug_checks = 0;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+}  // namespace
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+void clear_error() { g_last_error.clear(); }
+bool debug_checks() { return g_debug_checks != 0; }
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
+void pkv_set_debug_checks(int on) { g_debug_checks = on ? 1 : 0; }
+
+int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const void* k_new,
+                  const void* v_new, int64_t n, int n_kv_heads, int head_dim,
+                  int64_t pool_slots, pkv_stream_t stream) {
+    clear_error();
+    if (n < 0) return fail(PKV_ERR_INVALID_ARG, "kvpool_append: n = %lld < 0", (long long)n);
+    if (n_kv_heads <= 0 || head_dim <= 0 || pool_slots <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "kvpool_append: n_kv_heads, head_dim, pool_slots must be > 0");
+    const int64_t row_bytes = int64_t(n_kv_heads) * head_dim * 2;
+    if (row_bytes % 16 != 0)
+        return fail(PKV_ERR_UNSUPPORTED, "kvpool_append: row of %lld bytes is not a multiple of 16",
+                    (long long)row_bytes);
+    if (n > pool_slots)
+        return fail(PKV_ERR_INVALID_ARG, "kvpool_append: n = %lld rows exceed pool_slots = %lld",
+                    (long long)n, (long long)pool_slots);
+    if (n == 0) return PKV_OK;
+    if (!k_pool || !v_pool || !slot_ids || !k_new || !v_new)
+        return fail(PKV_ERR_INVALID_ARG, "kvpool_append: NULL pointer argument");
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new))
+        return fail(PKV_ERR_INVALID_ARG, "kvpool_append: pools and new rows must be 16-byte aligned");
+    if (debug_checks()) {
+        std::vector<int32_t> ids(n);
+        cudaError_t e = cudaMemcpyAsync(ids.data(), slot_ids, n * sizeof(int32_t),
+                                        cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "kvpool_append: debug copy of slot_ids");
+        std::vector<int32_t> sorted(ids);
+        std::sort(sorted.begin(), sorted.end());
+        for (int64_t i = 0; i < n; ++i) {
+            if (ids[i] < 0 || ids[i] >= pool_slots)
+                return fail(PKV_ERR_INDEX, "kvpool_append: slot_ids[%lld] = %d outside [0, %lld)",
+                            (long long)i, ids[i], (long long)pool_slots);
+            if (i > 0 && sorted[i] == sorted[i - 1])
+                return fail(PKV_ERR_INDEX, "kvpool_append: slot id %d appears twice", sorted[i]);
+        }
+    }
+    cudaError_t e = launch_append(k_pool, v_pool, slot_ids, k_new, v_new, n,
+                                  static_cast<int>(row_bytes), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvpool_append: launch");
+    return PKV_OK;
+}
+
+int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int num_sms,
+                           int ctas_per_sm, int32_t* units_out, int max_units, int* n_units,
+                           int32_t* merges_out, int max_merges, int* n_merges,
+                           int* chunk_tokens) {
+    clear_error();
+    if (!n_units || !n_merges || !chunk_tokens || (max_units > 0 && !units_out) ||
+        (max_merges > 0 && !merges_out))
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: NULL output");
+    if (num_sms <= 0 || ctas_per_sm <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: num_sms and ctas_per_sm must be > 0");
+    return plan_compute(kv_indptr_host, batch, PlanShape{num_sms, ctas_per_sm},
+                        reinterpret_cast<Unit*>(units_out), max_units,
+                        reinterpret_cast<Merge*>(merges_out), max_merges, n_units, n_merges,
+                        chunk_tokens);
+}
+
+void paged_decode_plan_destroy(pkv_plan* p) {
+    if (p == nullptr) return;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    cudaSetDevice(p->device);
+    if (p->copy_done) {
+        cudaEventSynchronize(p->copy_done);
+        cudaEventDestroy(p->copy_done);
+    }
+    if (p->host_staging) cudaFreeHost(p->host_staging);
+    if (p->dev_meta) cudaFree(p->dev_meta);
+    if (p->ws_o) cudaFree(p->ws_o);
+    if (p->ws_lse) cudaFree(p->ws_lse);
+    if (prev >= 0) cudaSetDevice(prev);
+    delete p;
+}
+
+int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tokens,
+                             int n_qo_heads, int n_kv_heads, int head_dim) {
+    clear_error();
+    if (!out_plan) return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_create: plan is NULL");
+    *out_plan = nullptr;
+    if (max_batch < 1 || max_tokens < 0 || max_tokens >= (int64_t(1) << 31))
+        return fail(PKV_ERR_INVALID_ARG,
+                    "paged_decode_plan_create: need max_batch >= 1 and 0 <= max_tokens < 2^31");
+    if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim))
+        return fail(PKV_ERR_UNSUPPORTED,
+                    "paged_decode_plan_create: unsupported shape (n_qo_heads=%d, n_kv_heads=%d, "
+                    "head_dim=%d); need head_dim 128/256, group 1/2/4/8, n_kv_heads <= 8",
+                    n_qo_heads, n_kv_heads, head_dim);
+    pkv_plan* p = new (std::nothrow) pkv_plan();
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_create: out of host memory");
+    cudaError_t e = cudaGetDevice(&p->device);
+    int sms = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "paged_decode_plan_create: device query");
+    }
+    const int per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim);
+    if (per_sm <= 0) {
+        delete p;
+        return fail(PKV_ERR_CUDA, "paged_decode_plan_create: occupancy query failed");
+    }
+    p->shape = PlanShape{sms, per_sm};
+    p->max_batch = max_batch;
+    p->max_tokens = max_tokens;
+    p->n_qo_heads = n_qo_heads;
+    p->n_kv_heads = n_kv_heads;
+    p->head_dim = head_dim;
+    p->max_units = std::max(plan_target_units(p->shape), max_batch);
+    p->max_merges = max_batch;
+    p->indptr_host.reserve(max_batch + 1);
+    const size_t meta_bytes = sizeof(Unit) * p->max_units + sizeof(Merge) * p->max_merges;
+    const size_t ws_o_bytes = sizeof(float) * size_t(p->max_units) * n_qo_heads * head_dim;
+    const size_t ws_lse_bytes = sizeof(float) * size_t(p->max_units) * n_qo_heads;
+    e = cudaMallocHost(&p->host_staging, meta_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&p->dev_meta, meta_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_o), ws_o_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_lse), ws_lse_bytes);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->copy_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        paged_decode_plan_destroy(p);
+        return cuda_fail(e, "paged_decode_plan_create: allocation");
+    }
+    *out_plan = p;
+    return PKV_OK;
+}
+
+int paged_decode_plan(pkv_plan* p, const int32_t* kv_indptr_host, int batch, pkv_stream_t stream) {
+    clear_error();
+    if (!p) return fail(PKV_ERR_PLAN, "paged_decode_plan: plan is NULL");
+    p->planned = false;
+    if (batch < 0 || batch > p->max_batch)
+        return fail(PKV_ERR_PLAN, "paged_decode_plan: batch %d outside [0, %d]", batch, p->max_batch);
+    if (!kv_indptr_host) return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan: kv_indptr_host is NULL");
+    if (int64_t(kv_indptr_host[batch]) > p->max_tokens)
+        return fail(PKV_ERR_PLAN, "paged_decode_plan: %d tokens exceed the plan's max_tokens %lld",
+                    kv_indptr_host[batch], (long long)p->max_tokens);
+    // The staging buffer may still feed the previous step's copy.
+    if (p->copy_pending) {
+        cudaError_t e = cudaEventSynchronize(p->copy_done);
+        if (e != cudaSuccess) return cuda_fail(e, "paged_decode_plan: waiting for the previous copy");
+        p->copy_pending = false;
+    }
+    int nu = 0, nm = 0, chunk = 0;
+    int rc = plan_compute(kv_indptr_host, batch, p->shape, p->host_units(), p->max_units,
+                          p->host_merges(), p->max_merges, &nu, &nm, &chunk);
+    if (rc != PKV_OK) return rc;
+    // One copy covers the units and, right after the units region, the merges.
+    cudaError_t e = cudaSuccess;
+    if (nu > 0)
+        e = cudaMemcpyAsync(const_cast<Unit*>(p->dev_units()), p->host_units(), sizeof(Unit) * nu,
+                            cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && nm > 0)
+        e = cudaMemcpyAsync(const_cast<Merge*>(p->dev_merges()), p->host_merges(),
+                            sizeof(Merge) * nm, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaEventRecord(p->copy_done, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_plan: upload");
+    p->copy_pending = true;
+    p->batch = batch;
+    p->n_units = nu;
+    p->n_merges = nm;
+    p->chunk_tokens = chunk;
+    p->indptr_host.assign(kv_indptr_host, kv_indptr_host + batch + 1);
+    p->planned = true;
+    return PKV_OK;
+}
+
+int paged_decode_plan_info(const pkv_plan* p, int* batch, int* n_units, int* n_merges,
+                           int* chunk_tokens, int* max_units) {
+    clear_error();
+    if (!p) return fail(PKV_ERR_PLAN, "paged_decode_plan_info: plan is NULL");
+    if (batch) *batch = p->batch;
+    if (n_units) *n_units = p->n_units;
+    if (n_merges) *n_merges = p->n_merges;
+    if (chunk_tokens) *chunk_tokens = p->chunk_tokens;
+    if (max_units) *max_units = p->max_units;
+    return PKV_OK;
+}
+
+int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* kv_indptr, const int32_t* kv_indices, int batch,
+                      int n_qo_heads, int n_kv_heads, int head_dim, float sm_scale, void* out,
+                      float* lse, const pkv_plan* p, pkv_stream_t stream) {
+    clear_error();
+    if (!p) return fail(PKV_ERR_PLAN, "paged_decode_attn: plan is NULL");
+    if (!p->planned) return fail(PKV_ERR_PLAN, "paged_decode_attn: paged_decode_plan was not run");
+    if (n_qo_heads != p->n_qo_heads || n_kv_heads != p->n_kv_heads || head_dim != p->head_dim)
+        return fail(PKV_ERR_PLAN,
+                    "paged_decode_attn: shape (%d, %d, %d) differs from the plan's (%d, %d, %d)",
+                    n_qo_heads, n_kv_heads, head_dim, p->n_qo_heads, p->n_kv_heads, p->head_dim);
+    if (batch != p->batch)
+        return fail(PKV_ERR_PLAN, "paged_decode_attn: batch %d differs from the planned batch %d",
+                    batch, p->batch);
+    if (!std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn: sm_scale not finite");
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_pool || !v_pool || !kv_indptr || !out || (!kv_indices && p->indptr_host[batch] > 0))
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn: NULL pointer argument");
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn: q, pools and out must be 16-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn: lse must be 4-byte aligned");
+    if (debug_checks()) {
+        std::vector<int32_t> ip(batch + 1);
+        cudaError_t e = cudaMemcpyAsync(ip.data(), kv_indptr, ip.size() * sizeof(int32_t),
+                                        cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attn: debug copy of kv_indptr");
+        for (int b = 0; b <= batch; ++b)
+            if (ip[b] != p->indptr_host[b])
+                return fail(PKV_ERR_INDEX, "paged_decode_attn: kv_indptr[%d] = %d but the plan has %d",
+                            b, ip[b], p->indptr_host[b]);
+        const int32_t n = ip[batch];
+        if (n > 0) {
+            std::vector<int32_t> idx(n);
+            e = cudaMemcpyAsync(idx.data(), kv_indices, idx.size() * sizeof(int32_t),
+                                cudaMemcpyDeviceToHost, stream);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attn: debug copy of kv_indices");
+            for (int32_t i = 0; i < n; ++i)
+                if (idx[i] < 0)
+                    return fail(PKV_ERR_INDEX, "paged_decode_attn: kv_indices[%d] = %d < 0", i, idx[i]);
+        }
+    }
+    DecodeArgs a{};
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.kv_indptr = kv_indptr;
+    a.kv_indices = kv_indices;
+    a.units = p->dev_units();
+    a.merges = p->dev_merges();
+    a.n_units = p->n_units;
+    a.n_merges = p->n_merges;
+    a.n_qo_heads = n_qo_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.sm_scale = sm_scale;
+    a.out = out;
+    a.lse = lse;
+    a.ws_o = p->ws_o;
+    a.ws_lse = p->ws_lse;
+    cudaError_t e = launch_decode(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attn: launch");
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// KV append: scatter this step's new K/V rows into their token-pool slots.
+//
+// The pool has page size 1 ("Agent-Infer: 纯 Rust 编写的高性能 LLM 推理引擎", section
+// "分页 KV 缓存"), so a decode step writes exactly one pool row per request and
+// layer: row `slot_ids[i]` of K and of V receives new row i. A row holds all KV
+// heads of one token (n_kv_heads * head_dim bf16, 2 KB for 8 x 128), contiguous in
+// both the source and the pool, so the copy is 16-byte vectors: consecutive
+// threads move consecutive vectors of one row (fully coalesced 2 KB reads and
+// writes), and one grid-stride loop covers K and V. Pure HBM traffic: 2 * n * row
+// bytes read and written, plus 4 bytes of slot id per row.
+#include <cuda_runtime.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+__global__ void __launch_bounds__(256)
+kvpool_append_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                     const int32_t* __restrict__ slot_ids, const uint4* __restrict__ k_new,
+                     const uint4* __restrict__ v_new, int64_t n, int row_vecs) {
+    const int64_t per_pool = n * row_vecs;
+    const int64_t total = 2 * per_pool;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const bool is_v = i >= per_pool;
+        const int64_t j = is_v ? i - per_pool : i;
+        const int64_t row = j / row_vecs;
+        const int64_t col = j - row * row_vecs;
+        const int64_t slot = __ldg(slot_ids + row);
+        const uint4 val = is_v ? __ldg(v_new + j) : __ldg(k_new + j);
+        uint4* dst = is_v ? v_pool : k_pool;
+        dst[slot * row_vecs + col] = val;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_append(void* k_pool, void* v_pool, const int32_t* slot_ids,
+                          const void* k_new, const void* v_new, int64_t n, int row_bytes,
+                          cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    const int row_vecs = row_bytes / 16;
+    const int64_t total = 2 * n * row_vecs;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    // Enough CTAs to fill the GPU several times over; the loop covers the rest.
+    blocks = blocks < 152 * 16 ? blocks : 152 * 16;
+    kvpool_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), slot_ids,
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), n, row_vecs);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,279 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (needs a GPU).
+
+Tolerances (the decode contract): |out - ref| <= 1e-2 + 1e-2 * |ref| elementwise on
+bf16 out, |lse - ref| <= 1e-3 on fp32 lse, and bit-exact pool rows after append.
+Pools are NaN-poisoned outside the listed slots, so any stray read shows up as a
+NaN output. The oracle always works from the generated inputs and applies its own
+append; nothing the CUDA path wrote is fed to it.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+OUT_ATOL, OUT_RTOL, LSE_ATOL = 1e-2, 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_gqa_tokentokvpool_gb300 import build
+    build.build()
+    import paged_kv_gqa_tokentokvpool_gb300 as m
+    return m
+
+
+def bits(t):
+    return workloads.bf16_bits(t)
+
+
+def to_f64(t_bf16):
+    return t_bf16.float().double().cpu().numpy()
+
+
+def assert_parity(out, lse, ref_out, ref_lse, what=""):
+    out = np.asarray(out, np.float64)
+    lse = np.asarray(lse, np.float64)
+    assert out.shape == ref_out.shape and lse.shape == ref_lse.shape
+    empty = np.isneginf(ref_lse)
+    assert np.all(np.isneginf(lse[empty])), f"{what}: empty contexts need lse = -inf"
+    assert np.all(out[empty] == 0), f"{what}: empty contexts need out = 0"
+    assert np.all(np.isfinite(out)), f"{what}: non-finite out (stray read of a poisoned slot?)"
+    assert np.all(np.isfinite(lse[~empty])), f"{what}: non-finite lse"
+    err = np.abs(out - ref_out)
+    bad = err > OUT_ATOL + OUT_RTOL * np.abs(ref_out)
+    assert not bad.any(), (f"{what}: out mismatch at {np.argwhere(bad)[:5].tolist()}, "
+                           f"max err {err.max():.3g}")
+    lerr = np.abs(lse[~empty] - ref_lse[~empty])
+    assert lerr.size == 0 or lerr.max() <= LSE_ATOL, f"{what}: lse max err {lerr.max():.3g}"
+
+
+def oracle_reference(wl, t, layer_pools=None):
+    """Oracle out/lse for one layer from generated (pre-append) tensors."""
+    k_bits = bits(t.k_pool) if layer_pools is None else layer_pools[0]
+    v_bits = bits(t.v_pool) if layer_pools is None else layer_pools[1]
+    k_after = oracle.append(k_bits, wl.append_slots, bits(t.k_new))
+    v_after = oracle.append(v_bits, wl.append_slots, bits(t.v_new))
+    return oracle.decode(bits(t.q), k_after, v_after, wl.kv_indptr, wl.kv_indices,
+                         wl.n_qo_heads, wl.n_kv_heads, wl.head_dim, wl.sm_scale)
+
+
+def run_small(pkv, wl, layer=0, debug=False):
+    """Append + plan + attention for one layer of a small workload; returns GPU
+    results, generated tensors and the GPU pools after append."""
+    t = workloads.layer_tensors(wl, layer, device="cpu", poison_unreferenced=True)
+    dev = torch.device("cuda")
+    k_pool, v_pool = t.k_pool.to(dev), t.v_pool.to(dev)
+    q = t.q.to(dev)
+    out = torch.full((wl.batch, wl.n_qo_heads, wl.head_dim), float("nan"),
+                     dtype=torch.bfloat16, device=dev)
+    lse = torch.full((wl.batch, wl.n_qo_heads), float("nan"), dtype=torch.float32, device=dev)
+    indptr = torch.from_numpy(wl.kv_indptr).to(dev)
+    indices = torch.from_numpy(wl.kv_indices).to(dev)
+    if indices.numel() == 0:
+        indices = torch.zeros(1, dtype=torch.int32, device=dev)
+    slots = torch.from_numpy(wl.append_slots).to(dev)
+    pkv.pkv_set_debug_checks(debug)
+    try:
+        pkv.kvpool_append(k_pool, v_pool, slots, t.k_new.to(dev), t.v_new.to(dev))
+        plan = pkv.paged_decode_plan_create(max(wl.batch, 1), max(wl.total_tokens, 1),
+                                            wl.n_qo_heads, wl.n_kv_heads, wl.head_dim)
+        pkv.paged_decode_plan(plan, wl.kv_indptr)
+        pkv.paged_decode_attn(q, k_pool, v_pool, indptr, indices, wl.batch, wl.n_qo_heads,
+                              wl.n_kv_heads, wl.head_dim, wl.sm_scale, out, lse, plan)
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    return out, lse, t, k_pool, v_pool, plan
+
+
+SMALL_CASES = [
+    # (lengths, Hq, Hkv, D)
+    ([1], 32, 8, 128),
+    ([0], 32, 8, 128),
+    ([0, 1, 0, 2, 3], 32, 8, 128),
+    ([17, 300, 1000, 5, 64, 65, 31, 33], 32, 8, 128),
+    ([4097], 32, 8, 128),
+    ([20000, 7, 3000], 32, 8, 128),
+    ([1, 255, 256, 257, 12345], 16, 4, 256),
+    ([9000, 0, 40], 16, 4, 256),
+    ([100, 2000], 8, 8, 128),
+    ([100, 2000], 16, 8, 128),
+    ([100, 5000], 64, 8, 128),
+    ([77, 3001], 8, 1, 256),
+    ([513] * 40, 32, 8, 128),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL_CASES)))
+def test_decode_small_cases(pkv, case):
+    lengths, hq, hkv, d = SMALL_CASES[case]
+    wl = workloads.scattered_workload(lengths, n_qo_heads=hq, n_kv_heads=hkv, head_dim=d,
+                                      seed=100 + case, k_scale=1.0)
+    out, lse, t, *_ = run_small(pkv, wl, debug=(case % 2 == 0))
+    ref_out, ref_lse = oracle_reference(wl, t)
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what=f"case {case}")
+
+
+def test_append_bit_exact(pkv):
+    wl = workloads.scattered_workload([3, 0, 700, 1, 64] * 7, seed=7)
+    out, lse, t, k_pool, v_pool, _ = run_small(pkv, wl)
+    want_k = oracle.append(bits(t.k_pool), wl.append_slots, bits(t.k_new))
+    want_v = oracle.append(bits(t.v_pool), wl.append_slots, bits(t.v_new))
+    assert np.array_equal(bits(k_pool), want_k)
+    assert np.array_equal(bits(v_pool), want_v)
+
+
+def test_append_zero_rows_is_noop(pkv):
+    dev = torch.device("cuda")
+    pool = torch.randn(64, 8, 128, device=dev).to(torch.bfloat16)
+    before = pool.clone()
+    empty_rows = torch.empty(0, 8, 128, dtype=torch.bfloat16, device=dev)
+    pkv.kvpool_append(pool, pool, torch.empty(0, dtype=torch.int32, device=dev), empty_rows,
+                      empty_rows)
+    torch.cuda.synchronize()
+    assert torch.equal(pool.view(torch.int16), before.view(torch.int16))
+
+
+def test_plan_reused_across_layers_and_steps(pkv):
+    """One plan per step serves every layer; re-planning with other lengths works."""
+    dev = torch.device("cuda")
+    plan = pkv.paged_decode_plan_create(6, 40000, 32, 8, 128)
+    for step, lengths in enumerate([[5000, 3, 900], [1, 1, 1, 1, 1, 30000], [0, 2048]]):
+        wl = workloads.scattered_workload(lengths, layers=3, seed=200 + step)
+        pkv.paged_decode_plan(plan, wl.kv_indptr)
+        indptr = torch.from_numpy(wl.kv_indptr).to(dev)
+        indices = torch.from_numpy(wl.kv_indices).to(dev)
+        for layer in range(3):
+            t = workloads.layer_tensors(wl, layer, device="cpu", poison_unreferenced=True)
+            kp, vp = t.k_pool.to(dev), t.v_pool.to(dev)
+            slots = torch.from_numpy(wl.append_slots).to(dev)
+            pkv.kvpool_append(kp, vp, slots, t.k_new.to(dev), t.v_new.to(dev))
+            out = torch.empty(wl.batch, 32, 128, dtype=torch.bfloat16, device=dev)
+            lse = torch.empty(wl.batch, 32, dtype=torch.float32, device=dev)
+            pkv.paged_decode_attn(t.q.to(dev), kp, vp, indptr, indices, wl.batch, 32, 8, 128,
+                                  wl.sm_scale, out, lse, plan)
+            torch.cuda.synchronize()
+            ref_out, ref_lse = oracle_reference(wl, t)
+            assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse,
+                          what=f"step {step} layer {layer}")
+
+
+def test_lse_optional(pkv):
+    wl = workloads.scattered_workload([300, 5000], seed=9)
+    t = workloads.layer_tensors(wl, 0, device="cpu")
+    dev = torch.device("cuda")
+    kp, vp = t.k_pool.to(dev), t.v_pool.to(dev)
+    out = torch.empty(2, 32, 128, dtype=torch.bfloat16, device=dev)
+    plan = pkv.paged_decode_plan_create(2, wl.total_tokens, 32, 8, 128)
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    pkv.paged_decode_attn(t.q.to(dev), kp, vp, torch.from_numpy(wl.kv_indptr).to(dev),
+                          torch.from_numpy(wl.kv_indices).to(dev), 2, 32, 8, 128, wl.sm_scale,
+                          out, None, plan)
+    torch.cuda.synchronize()
+    ref_out, _ = oracle.decode(bits(t.q), bits(t.k_pool), bits(t.v_pool), wl.kv_indptr,
+                               wl.kv_indices, 32, 8, 128, wl.sm_scale)
+    got = to_f64(out)
+    assert np.all(np.abs(got - ref_out) <= OUT_ATOL + OUT_RTOL * np.abs(ref_out))
+
+
+def test_errors_do_not_launch(pkv):
+    dev = torch.device("cuda")
+    plan = pkv.paged_decode_plan_create(4, 1000, 32, 8, 128)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode_plan(plan, np.array([0, 10, 5], np.int32))
+    assert e.value.code == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode_plan(plan, np.array([0, 10, 2000], np.int32))
+    assert e.value.code == pkv.PKV_ERR_PLAN
+    pkv.paged_decode_plan(plan, np.array([0, 10, 20], np.int32))
+    q = torch.zeros(3, 32, 128, dtype=torch.bfloat16, device=dev)
+    pool = torch.zeros(64, 8, 128, dtype=torch.bfloat16, device=dev)
+    ip = torch.tensor([0, 10, 20, 20], dtype=torch.int32, device=dev)
+    idx = torch.arange(20, dtype=torch.int32, device=dev)
+    out = torch.zeros(3, 32, 128, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(pkv.PkvError) as e:  # batch differs from the plan's
+        pkv.paged_decode_attn(q, pool, pool, ip, idx, 3, 32, 8, 128, 0.1, out, None, plan)
+    assert e.value.code == pkv.PKV_ERR_PLAN
+    with pytest.raises(pkv.PkvError) as e:  # shape differs from the plan's
+        pkv.paged_decode_attn(q[:2], pool, pool, ip[:3], idx, 2, 16, 8, 128, 0.1, out, None, plan)
+    assert e.value.code == pkv.PKV_ERR_PLAN
+    # debug checks catch an indptr that disagrees with the plan and a bad slot
+    pkv.pkv_set_debug_checks(True)
+    try:
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.paged_decode_attn(q[:2], pool, pool, torch.tensor([0, 10, 19], dtype=torch.int32,
+                                  device=dev), idx, 2, 32, 8, 128, 0.1, out, None, plan)
+        assert e.value.code == pkv.PKV_ERR_INDEX
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.kvpool_append(pool, pool, torch.tensor([3, 64], dtype=torch.int32, device=dev),
+                              pool[:2], pool[:2])
+        assert e.value.code == pkv.PKV_ERR_INDEX
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.kvpool_append(pool, pool, torch.tensor([3, 3], dtype=torch.int32, device=dev),
+                              pool[:2], pool[:2])
+        assert e.value.code == pkv.PKV_ERR_INDEX
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0), "a rejected call must not have launched"
+
+
+# ---------------------------------------------------------------------------
+# the benchmark's five workloads at full size, in the benchmark's launch setup
+# ---------------------------------------------------------------------------
+
+FULL = {1: None, 2: None, 3: [0, 35], 4: [0, 7], 5: None}
+
+
+@pytest.mark.parametrize("config_no", sorted(FULL))
+def test_full_size_config(pkv, config_no):
+    import bench
+    wl = workloads.config_workload(config_no)
+    st = bench.StepState(wl, layers=FULL[config_no], poison_unreferenced=True)
+    uniq, inv = np.unique(wl.kv_indices, return_inverse=True)
+    compact = inv.astype(np.int32)
+    uniq_dev = torch.from_numpy(uniq.astype(np.int64)).cuda()
+    # the appended slots' positions in the compacted pool
+    pos = {int(s): i for i, s in enumerate(uniq)}
+    app_compact = np.array([pos[int(s)] for s in wl.append_slots], np.int32)
+    before = []
+    for i in range(len(st.layer_ids)):
+        before.append((bits(st.k_pool[i].index_select(0, uniq_dev)),
+                       bits(st.v_pool[i].index_select(0, uniq_dev))))
+    st.run()
+    torch.cuda.synchronize()
+    for i, layer in enumerate(st.layer_ids):
+        kb, vb = before[i]
+        k_after = oracle.append(kb, app_compact, bits(st.k_new[i]))
+        v_after = oracle.append(vb, app_compact, bits(st.v_new[i]))
+        # append: bit-exact on every listed row (appended and untouched alike)
+        assert np.array_equal(bits(st.k_pool[i].index_select(0, uniq_dev)), k_after)
+        assert np.array_equal(bits(st.v_pool[i].index_select(0, uniq_dev)), v_after)
+        ref_out, ref_lse = oracle.decode(bits(st.q[i]), k_after, v_after, wl.kv_indptr, compact,
+                                         wl.n_qo_heads, wl.n_kv_heads, wl.head_dim, wl.sm_scale)
+        assert_parity(to_f64(st.out[i]), st.lse[i].cpu().numpy(), ref_out, ref_lse,
+                      what=f"config {config_no} layer {layer}")
+        # loose statistical sanity of the generator scaling: E[lse] ~ ln L + sigma^2/2
+        sigma2 = wl.k_scale ** 2
+        expect = np.log(wl.lengths)[:, None] + sigma2 / 2
+        assert abs(float(np.mean(ref_lse - expect))) < 0.2
+
+
+def test_end_to_end_host_path_matches_device_path(pkv):
+    import bench
+    wl = workloads.config_workload(2)
+    st = bench.StepState(wl, layers=[0, 1])
+    st.run()
+    torch.cuda.synchronize()
+    dev_out = [o.clone() for o in st.out]
+    io = bench.HostIO(st)
+    io.run()
+    torch.cuda.synchronize()
+    for a, b in zip(io.out, dev_out):
+        assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
