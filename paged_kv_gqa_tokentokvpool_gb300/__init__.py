@@ -4,8 +4,8 @@ A thin ctypes binding of the C ABI in ``include/pkv.h`` (``libpkv.so``, built
 in-tree by ``build.py``). The functions keep the C names and argument order; they
 only turn torch tensors into pointers and sizes and raise ``PkvError`` on a
 negative return code. Every step of the computation runs in the library's CUDA
-kernels: there is no Python or CPU fallback, and importing this package fails
-if the library has not been built.
+kernels: there is no Python or CPU fallback, and the first call raises
+ImportError if the library has not been built.
 
 Typical decode step (one plan per step, reused by every layer):
 
@@ -73,19 +73,23 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-_lib = _load()
+_lib = None
 
 
 def library() -> ctypes.CDLL:
+    """The loaded libpkv.so (loaded on first use; ImportError if it was not built)."""
+    global _lib
+    if _lib is None:
+        _lib = _load()
     return _lib
 
 
 def pkv_last_error() -> str:
-    return _lib.pkv_last_error().decode()
+    return library().pkv_last_error().decode()
 
 
 def pkv_set_debug_checks(on: bool) -> None:
-    _lib.pkv_set_debug_checks(1 if on else 0)
+    library().pkv_set_debug_checks(1 if on else 0)
 
 
 def _check(rc: int) -> None:
@@ -130,7 +134,7 @@ class Plan:
 
     def info(self) -> dict:
         vals = [ctypes.c_int() for _ in range(5)]
-        _check(_lib.paged_decode_plan_info(self.handle, *[ctypes.byref(v) for v in vals]))
+        _check(library().paged_decode_plan_info(self.handle, *[ctypes.byref(v) for v in vals]))
         return dict(zip(("batch", "n_units", "n_merges", "chunk_tokens", "max_units"),
                         (v.value for v in vals)))
 
@@ -152,7 +156,7 @@ def kvpool_append(k_pool, v_pool, slot_ids, k_new, v_new, n=None, n_kv_heads=Non
     if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape:
         raise ValueError("pool / new-row shapes disagree")
     n = slot_ids.numel() if n is None else n
-    _check(_lib.kvpool_append(_ptr(k_pool), _ptr(v_pool), _ptr(slot_ids), _ptr(k_new),
+    _check(library().kvpool_append(_ptr(k_pool), _ptr(v_pool), _ptr(slot_ids), _ptr(k_new),
                               _ptr(v_new), n, hkv if n_kv_heads is None else n_kv_heads,
                               d if head_dim is None else head_dim,
                               S if pool_slots is None else pool_slots, _stream(stream)))
@@ -161,7 +165,7 @@ def kvpool_append(k_pool, v_pool, slot_ids, k_new, v_new, n=None, n_kv_heads=Non
 def paged_decode_plan_create(max_batch: int, max_tokens: int, n_qo_heads: int,
                              n_kv_heads: int, head_dim: int) -> Plan:
     h = ctypes.c_void_p()
-    _check(_lib.paged_decode_plan_create(ctypes.byref(h), max_batch, max_tokens, n_qo_heads,
+    _check(library().paged_decode_plan_create(ctypes.byref(h), max_batch, max_tokens, n_qo_heads,
                                          n_kv_heads, head_dim))
     return Plan(h, (n_qo_heads, n_kv_heads, head_dim))
 
@@ -178,7 +182,7 @@ def paged_decode_plan(plan: Plan, kv_indptr_host, batch=None, stream=None) -> No
     ip = _host_indptr(kv_indptr_host)
     batch = ip.size - 1 if batch is None else batch
     plan._indptr_keepalive = ip
-    _check(_lib.paged_decode_plan(plan.handle, _ptr(ip), batch, _stream(stream)))
+    _check(library().paged_decode_plan(plan.handle, _ptr(ip), batch, _stream(stream)))
 
 
 def paged_decode_attn(q, k_pool, v_pool, kv_indptr, kv_indices, batch, n_qo_heads,
@@ -192,7 +196,7 @@ def paged_decode_attn(q, k_pool, v_pool, kv_indptr, kv_indices, batch, n_qo_head
     _dev(out, torch.bfloat16, "out")
     if lse is not None:
         _dev(lse, torch.float32, "lse")
-    _check(_lib.paged_decode_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indptr),
+    _check(library().paged_decode_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indptr),
                                   _ptr(kv_indices), batch, n_qo_heads, n_kv_heads, head_dim,
                                   float(sm_scale), _ptr(out), _ptr(lse), plan.handle,
                                   _stream(stream)))
@@ -200,7 +204,7 @@ def paged_decode_attn(q, k_pool, v_pool, kv_indptr, kv_indices, batch, n_qo_head
 
 def paged_decode_plan_destroy(plan: Plan) -> None:
     if plan.handle:
-        _lib.paged_decode_plan_destroy(plan.handle)
+        library().paged_decode_plan_destroy(plan.handle)
         plan.handle = None
 
 
@@ -213,7 +217,7 @@ def paged_decode_plan_host(kv_indptr_host, num_sms: int, ctas_per_sm: int,
     units = np.zeros((max_units, 4), np.int32)
     merges = np.zeros((max(max_merges, 1), 4), np.int32)
     nu, nm, chunk = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    _check(_lib.paged_decode_plan_host(_ptr(ip), batch, num_sms, ctas_per_sm, _ptr(units),
+    _check(library().paged_decode_plan_host(_ptr(ip), batch, num_sms, ctas_per_sm, _ptr(units),
                                        max_units, ctypes.byref(nu), _ptr(merges), max_merges,
                                        ctypes.byref(nm), ctypes.byref(chunk)))
     return units[:nu.value].copy(), merges[:nm.value].copy(), chunk.value
