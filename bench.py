@@ -95,8 +95,7 @@ class StepState:
                 attn_events.append((e0, e1))
         if self.launches_per_step is None:
             info = self.plan.info()
-            per_layer = (1 if len(wl.append_slots) else 0) + (1 if info["n_units"] else 0) \
-                + (1 if info["n_merges"] else 0)
+            per_layer = (1 if len(wl.append_slots) else 0) + (1 if info["n_ctas"] else 0)
             self.launches_per_step = per_layer * len(self.layer_ids)
 
 
@@ -413,14 +412,14 @@ def main(argv=None):
             "effective_logical_gbs": world * nbytes["step_logical"] * args.steps
             / (elapsed_ms * 1e-3) / 1e9,
             "plan": {"units": info["n_units"], "merges": info["n_merges"],
-                     "chunk_tokens": info["chunk_tokens"]},
+                     "chunk_tokens": info["chunk_tokens"], "ctas": info["n_ctas"]},
             "l2": f"inputs larger than L2: each step reads {nbytes['step'] / 1e9:.2f} GB "
                   f"across {wl.layers} layers' pools (L2 {L2_BYTES / 2**20:.0f} MiB)",
             "parallelism": f"replicas x{world}",
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "paged_decode_attn (split-KV kernel + LSE merge), "
+                     "kernel": "paged_decode_attn (split-KV kernel, LSE merge fused), "
                                f"avg of {len(attn_ms)} calls {attn_avg_ms * 1e3:.1f} us, "
                                f"{nbytes['attn_per_layer'] / 1e6:.1f} MB algorithmic",
                      "peak_kind": peak_kind},

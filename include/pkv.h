@@ -130,7 +130,8 @@ int paged_decode_plan(pkv_plan* plan, const int32_t* kv_indptr_host, int batch,
  *   lse        : [batch, n_qo_heads] fp32, written; may be NULL
  *   plan       : built by paged_decode_plan for this step with the same batch and
  *                created for the same (n_qo_heads, n_kv_heads, head_dim)
- * Launches one split-KV kernel and, when any request was split, one merge kernel.
+ * Launches one kernel. Contexts that the plan split are merged inside it by the
+ * CTA that finishes a context's last part. A plan serves one stream at a time.
  */
 int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
                       const int32_t* kv_indptr, const int32_t* kv_indices, int batch,
@@ -143,25 +144,40 @@ void paged_decode_plan_destroy(pkv_plan* plan);
 /*
  * paged_decode_plan_host — the planner alone, on the host, with no CUDA call.
  * Computes the work list paged_decode_plan would upload, for inspection and tests.
+ * The work of one layer is every (request, KV-head group) pair, a group being
+ * min(n_kv_heads, 512 / head_dim) consecutive KV heads; contexts longer than the
+ * chosen chunk are cut into near-equal token ranges, and the units are spread
+ * over `ctas` persistent CTAs longest first.
  *   kv_indptr_host : [batch + 1] int32
- *   num_sms, ctas_per_sm : the device's SM count and the split kernel's resident
- *                    CTAs per SM (the plan uses the real values of its device)
- *   units_out      : [max_units * 4] int32 — per work unit
- *                    {request b, first token, end token (exclusive), partial slot
- *                    or -1 when the unit writes out/lse directly}
- *   merges_out     : [max_merges * 4] int32 — per split request
- *                    {request b, first partial slot, number of parts, 0}
- *   n_units, n_merges, chunk_tokens : receive the counts and the chunk length
- * Returns PKV_ERR_PLAN if the output arrays are too small.
+ *   n_kv_heads, head_dim : the attention shape
+ *   ctas           : persistent CTAs (SMs x resident CTAs per SM on the device)
+ *   units_out      : [max_units * 8] int32 — per unit {request b, head group,
+ *                    first token, end token (exclusive), partial slot or -1 when
+ *                    the unit writes out/lse directly, merge record or -1, 0, 0},
+ *                    listed CTA by CTA
+ *   cta_begin_out  : [ctas + 1] int32 — CTA c runs units [cta_begin[c], cta_begin[c+1])
+ *   merges_out     : [max_merges * 4] int32 — per split (request, head group)
+ *                    {request b, head group, first partial slot, number of parts}
+ *   counts_out     : [5] int32 — {units, CTAs used, merge records, partial slots,
+ *                    chunk tokens}
+ * Returns PKV_ERR_PLAN if an output array is too small.
  */
-int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int num_sms,
-                           int ctas_per_sm, int32_t* units_out, int max_units,
-                           int* n_units, int32_t* merges_out, int max_merges, int* n_merges,
-                           int* chunk_tokens);
+int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_heads,
+                           int head_dim, int ctas, int32_t* units_out, int max_units,
+                           int32_t* cta_begin_out, int32_t* merges_out, int max_merges,
+                           int32_t* counts_out);
 
 /* paged_decode_plan_info — counts of the plan's current step (any out pointer may be NULL). */
 int paged_decode_plan_info(const pkv_plan* plan, int* batch, int* n_units, int* n_merges,
-                           int* chunk_tokens, int* max_units);
+                           int* chunk_tokens, int* n_ctas);
+
+/*
+ * paged_decode_plan_status — read and clear the plan's device status word
+ * (synchronous). 0: every attention kernel that used the plan completed its
+ * pipeline waits; nonzero: some wait exceeded its bound (1 s) and that launch's
+ * outputs are invalid.
+ */
+int paged_decode_plan_status(pkv_plan* plan, int* status);
 
 /*
  * pkv_set_debug_checks — when on (nonzero), kvpool_append and paged_decode_attn

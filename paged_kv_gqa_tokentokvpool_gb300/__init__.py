@@ -36,7 +36,8 @@ PKV_ERR_INDEX = -5
 
 EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",
-            "paged_decode_plan_info", "pkv_set_debug_checks", "pkv_last_error")
+            "paged_decode_plan_info", "paged_decode_plan_status", "pkv_set_debug_checks",
+            "pkv_last_error")
 
 
 class PkvError(RuntimeError):
@@ -61,14 +62,16 @@ def _load() -> ctypes.CDLL:
                                       P, P]
     lib.paged_decode_plan_destroy.argtypes = [P]
     lib.paged_decode_plan_destroy.restype = None
-    lib.paged_decode_plan_host.argtypes = [P, I32, I32, I32, P, I32, P, P, I32, P, P]
+    lib.paged_decode_plan_host.argtypes = [P, I32, I32, I32, I32, P, I32, P, P, I32, P]
     lib.paged_decode_plan_info.argtypes = [P, P, P, P, P, P]
+    lib.paged_decode_plan_status.argtypes = [P, P]
     lib.pkv_set_debug_checks.argtypes = [I32]
     lib.pkv_set_debug_checks.restype = None
     lib.pkv_last_error.argtypes = []
     lib.pkv_last_error.restype = ctypes.c_char_p
     for name in ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
-                 "paged_decode_attn", "paged_decode_plan_host", "paged_decode_plan_info"):
+                 "paged_decode_attn", "paged_decode_plan_host", "paged_decode_plan_info",
+                 "paged_decode_plan_status"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -135,8 +138,14 @@ class Plan:
     def info(self) -> dict:
         vals = [ctypes.c_int() for _ in range(5)]
         _check(library().paged_decode_plan_info(self.handle, *[ctypes.byref(v) for v in vals]))
-        return dict(zip(("batch", "n_units", "n_merges", "chunk_tokens", "max_units"),
+        return dict(zip(("batch", "n_units", "n_merges", "chunk_tokens", "n_ctas"),
                         (v.value for v in vals)))
+
+    def status(self) -> int:
+        """Read and clear the device status word (0 = every pipeline wait completed)."""
+        v = ctypes.c_int()
+        _check(library().paged_decode_plan_status(self.handle, ctypes.byref(v)))
+        return v.value
 
     def __del__(self):
         if getattr(self, "handle", None) and _lib is not None:
@@ -208,16 +217,25 @@ def paged_decode_plan_destroy(plan: Plan) -> None:
         plan.handle = None
 
 
-def paged_decode_plan_host(kv_indptr_host, num_sms: int, ctas_per_sm: int,
-                           max_units: int = 1 << 16, max_merges: int = None):
-    """The planner alone (host, no CUDA). Returns (units [n,4], merges [m,4], chunk)."""
+def paged_decode_plan_host(kv_indptr_host, n_kv_heads: int, head_dim: int, ctas: int,
+                           max_units: int = None, max_merges: int = None):
+    """The planner alone (host, no CUDA).
+
+    Returns dict(units [n, 8], cta_begin [c + 1], merges [m, 4], partials, chunk)."""
     ip = _host_indptr(kv_indptr_host)
     batch = ip.size - 1
-    max_merges = max(batch, 1) if max_merges is None else max_merges
-    units = np.zeros((max_units, 4), np.int32)
+    groups = max(1, n_kv_heads // max(1, min(n_kv_heads, 512 // head_dim)))
+    if max_units is None:
+        max_units = 8 * ctas + max(batch, 1) * groups
+    if max_merges is None:
+        max_merges = max(batch, 1) * groups
+    units = np.zeros((max(max_units, 1), 8), np.int32)
+    cta_begin = np.zeros(ctas + 1, np.int32)
     merges = np.zeros((max(max_merges, 1), 4), np.int32)
-    nu, nm, chunk = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    _check(library().paged_decode_plan_host(_ptr(ip), batch, num_sms, ctas_per_sm, _ptr(units),
-                                       max_units, ctypes.byref(nu), _ptr(merges), max_merges,
-                                       ctypes.byref(nm), ctypes.byref(chunk)))
-    return units[:nu.value].copy(), merges[:nm.value].copy(), chunk.value
+    counts = np.zeros(5, np.int32)
+    _check(library().paged_decode_plan_host(_ptr(ip), batch, n_kv_heads, head_dim, ctas,
+                                            _ptr(units), max_units, _ptr(cta_begin),
+                                            _ptr(merges), max_merges, _ptr(counts)))
+    nu, nc, nm, npart, chunk = (int(x) for x in counts)
+    return {"units": units[:nu].copy(), "cta_begin": cta_begin[:nc + 1].copy(),
+            "merges": merges[:nm].copy(), "partials": npart, "chunk": chunk}

@@ -94,20 +94,31 @@ int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const voi
     return PKV_OK;
 }
 
-int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int num_sms,
-                           int ctas_per_sm, int32_t* units_out, int max_units, int* n_units,
-                           int32_t* merges_out, int max_merges, int* n_merges,
-                           int* chunk_tokens) {
+int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_heads,
+                           int head_dim, int ctas, int32_t* units_out, int max_units,
+                           int32_t* cta_begin_out, int32_t* merges_out, int max_merges,
+                           int32_t* counts_out) {
     clear_error();
-    if (!n_units || !n_merges || !chunk_tokens || (max_units > 0 && !units_out) ||
+    if (!counts_out || (max_units > 0 && !units_out) || !cta_begin_out ||
         (max_merges > 0 && !merges_out))
         return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: NULL output");
-    if (num_sms <= 0 || ctas_per_sm <= 0)
-        return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: num_sms and ctas_per_sm must be > 0");
-    return plan_compute(kv_indptr_host, batch, PlanShape{num_sms, ctas_per_sm},
-                        reinterpret_cast<Unit*>(units_out), max_units,
-                        reinterpret_cast<Merge*>(merges_out), max_merges, n_units, n_merges,
-                        chunk_tokens);
+    if (ctas <= 0 || n_kv_heads <= 0 || head_dim <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: ctas, n_kv_heads, head_dim must be > 0");
+    const int hpg = heads_per_group(n_kv_heads, head_dim);
+    if (hpg < 1 || n_kv_heads % hpg != 0)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_decode_plan_host: %d KV heads do not form groups",
+                    n_kv_heads);
+    PlanCounts c{};
+    int rc = plan_compute(kv_indptr_host, batch, n_kv_heads / hpg, ctas,
+                          PlanLimits{max_units, max_merges}, reinterpret_cast<Unit*>(units_out),
+                          cta_begin_out, reinterpret_cast<Merge*>(merges_out), &c);
+    if (rc != PKV_OK) return rc;
+    counts_out[0] = c.n_units;
+    counts_out[1] = c.n_ctas;
+    counts_out[2] = c.n_merges;
+    counts_out[3] = c.n_partials;
+    counts_out[4] = c.chunk_tokens;
+    return PKV_OK;
 }
 
 void paged_decode_plan_destroy(pkv_plan* p) {
@@ -123,9 +134,15 @@ void paged_decode_plan_destroy(pkv_plan* p) {
     if (p->dev_meta) cudaFree(p->dev_meta);
     if (p->ws_o) cudaFree(p->ws_o);
     if (p->ws_lse) cudaFree(p->ws_lse);
+    if (p->dev_state) cudaFree(p->dev_state);
+    if (p->zero_row) cudaFree(p->zero_row);
     if (prev >= 0) cudaSetDevice(prev);
     delete p;
 }
+
+namespace {
+size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
+}  // namespace
 
 int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tokens,
                              int n_qo_heads, int n_kv_heads, int head_dim) {
@@ -138,39 +155,51 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim))
         return fail(PKV_ERR_UNSUPPORTED,
                     "paged_decode_plan_create: unsupported shape (n_qo_heads=%d, n_kv_heads=%d, "
-                    "head_dim=%d); need head_dim 128/256, group 1/2/4/8, n_kv_heads <= 8",
+                    "head_dim=%d); need head_dim 128/256, group 1/2/4/8, n_kv_heads 1/2/4/8",
                     n_qo_heads, n_kv_heads, head_dim);
     pkv_plan* p = new (std::nothrow) pkv_plan();
     if (!p) return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_create: out of host memory");
     cudaError_t e = cudaGetDevice(&p->device);
-    int sms = 0;
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e != cudaSuccess) {
         delete p;
         return cuda_fail(e, "paged_decode_plan_create: device query");
     }
-    const int per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim);
-    if (per_sm <= 0) {
+    p->ctas_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim);
+    if (p->ctas_per_sm <= 0) {
         delete p;
         return fail(PKV_ERR_CUDA, "paged_decode_plan_create: occupancy query failed");
     }
-    p->shape = PlanShape{sms, per_sm};
+    const int hpg = heads_per_group(n_kv_heads, head_dim);
+    p->ctas = p->num_sms * p->ctas_per_sm;
     p->max_batch = max_batch;
     p->max_tokens = max_tokens;
     p->n_qo_heads = n_qo_heads;
     p->n_kv_heads = n_kv_heads;
     p->head_dim = head_dim;
-    p->max_units = std::max(plan_target_units(p->shape), max_batch);
-    p->max_merges = max_batch;
+    p->n_groups = n_kv_heads / hpg;
+    p->lim.max_units = plan_max_units(p->ctas, max_batch, p->n_groups);
+    p->lim.max_merges = max_batch * p->n_groups;
     p->indptr_host.reserve(max_batch + 1);
-    const size_t meta_bytes = sizeof(Unit) * p->max_units + sizeof(Merge) * p->max_merges;
-    const size_t ws_o_bytes = sizeof(float) * size_t(p->max_units) * n_qo_heads * head_dim;
-    const size_t ws_lse_bytes = sizeof(float) * size_t(p->max_units) * n_qo_heads;
-    e = cudaMallocHost(&p->host_staging, meta_bytes);
-    if (e == cudaSuccess) e = cudaMalloc(&p->dev_meta, meta_bytes);
+    // staging layout: cta_begin[ctas + 1] | merges[max_merges] | units[max_units]
+    p->off_merge = round16(sizeof(int32_t) * (p->ctas + 1));
+    p->off_units = round16(p->off_merge + sizeof(Merge) * p->lim.max_merges);
+    p->meta_bytes = p->off_units + sizeof(Unit) * p->lim.max_units;
+    const int group_q_heads = hpg * (n_qo_heads / n_kv_heads);
+    const size_t ws_o_bytes = sizeof(float) * size_t(p->lim.max_units) * group_q_heads * head_dim;
+    const size_t ws_lse_bytes = sizeof(float) * size_t(p->lim.max_units) * group_q_heads;
+    const size_t state_bytes = sizeof(int) * (size_t(p->lim.max_merges) + 32);
+    e = cudaMallocHost(&p->host_staging, p->meta_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&p->dev_meta, p->meta_bytes);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_o), ws_o_bytes);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_lse), ws_lse_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->dev_state), state_bytes);
+    if (e == cudaSuccess) e = cudaMemset(p->dev_state, 0, state_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&p->zero_row, sizeof(uint16_t) * kHeadGroupElems);
+    if (e == cudaSuccess) e = cudaMemset(p->zero_row, 0, sizeof(uint16_t) * kHeadGroupElems);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->copy_done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         paged_decode_plan_destroy(p);
         return cuda_fail(e, "paged_decode_plan_create: allocation");
@@ -195,39 +224,46 @@ int paged_decode_plan(pkv_plan* p, const int32_t* kv_indptr_host, int batch, pkv
         if (e != cudaSuccess) return cuda_fail(e, "paged_decode_plan: waiting for the previous copy");
         p->copy_pending = false;
     }
-    int nu = 0, nm = 0, chunk = 0;
-    int rc = plan_compute(kv_indptr_host, batch, p->shape, p->host_units(), p->max_units,
-                          p->host_merges(), p->max_merges, &nu, &nm, &chunk);
+    char* st = static_cast<char*>(p->host_staging);
+    PlanCounts c{};
+    int rc = plan_compute(kv_indptr_host, batch, p->n_groups, p->ctas, p->lim,
+                          reinterpret_cast<Unit*>(st + p->off_units),
+                          reinterpret_cast<int32_t*>(st),
+                          reinterpret_cast<Merge*>(st + p->off_merge), &c);
     if (rc != PKV_OK) return rc;
-    // One copy covers the units and, right after the units region, the merges.
-    cudaError_t e = cudaSuccess;
-    if (nu > 0)
-        e = cudaMemcpyAsync(const_cast<Unit*>(p->dev_units()), p->host_units(), sizeof(Unit) * nu,
-                            cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess && nm > 0)
-        e = cudaMemcpyAsync(const_cast<Merge*>(p->dev_merges()), p->host_merges(),
-                            sizeof(Merge) * nm, cudaMemcpyHostToDevice, stream);
+    const size_t bytes = p->off_units + sizeof(Unit) * c.n_units;
+    cudaError_t e = cudaMemcpyAsync(p->dev_meta, st, bytes, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaEventRecord(p->copy_done, stream);
     if (e != cudaSuccess) return cuda_fail(e, "paged_decode_plan: upload");
     p->copy_pending = true;
     p->batch = batch;
-    p->n_units = nu;
-    p->n_merges = nm;
-    p->chunk_tokens = chunk;
+    p->counts = c;
     p->indptr_host.assign(kv_indptr_host, kv_indptr_host + batch + 1);
     p->planned = true;
     return PKV_OK;
 }
 
 int paged_decode_plan_info(const pkv_plan* p, int* batch, int* n_units, int* n_merges,
-                           int* chunk_tokens, int* max_units) {
+                           int* chunk_tokens, int* n_ctas) {
     clear_error();
     if (!p) return fail(PKV_ERR_PLAN, "paged_decode_plan_info: plan is NULL");
     if (batch) *batch = p->batch;
-    if (n_units) *n_units = p->n_units;
-    if (n_merges) *n_merges = p->n_merges;
-    if (chunk_tokens) *chunk_tokens = p->chunk_tokens;
-    if (max_units) *max_units = p->max_units;
+    if (n_units) *n_units = p->counts.n_units;
+    if (n_merges) *n_merges = p->counts.n_merges;
+    if (chunk_tokens) *chunk_tokens = p->counts.chunk_tokens;
+    if (n_ctas) *n_ctas = p->counts.n_ctas;
+    return PKV_OK;
+}
+
+int paged_decode_plan_status(pkv_plan* p, int* status) {
+    clear_error();
+    if (!p || !status) return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_status: NULL argument");
+    int* word = p->dev_state + p->lim.max_merges;
+    int v = 0;
+    cudaError_t e = cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && v != 0) e = cudaMemset(word, 0, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_plan_status: read");
+    *status = v;
     return PKV_OK;
 }
 
@@ -275,16 +311,17 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
                     return fail(PKV_ERR_INDEX, "paged_decode_attn: kv_indices[%d] = %d < 0", i, idx[i]);
         }
     }
+    const char* meta = static_cast<const char*>(p->dev_meta);
     DecodeArgs a{};
     a.q = q;
     a.k_pool = k_pool;
     a.v_pool = v_pool;
     a.kv_indptr = kv_indptr;
     a.kv_indices = kv_indices;
-    a.units = p->dev_units();
-    a.merges = p->dev_merges();
-    a.n_units = p->n_units;
-    a.n_merges = p->n_merges;
+    a.cta_begin = reinterpret_cast<const int32_t*>(meta);
+    a.merges = reinterpret_cast<const Merge*>(meta + p->off_merge);
+    a.units = reinterpret_cast<const Unit*>(meta + p->off_units);
+    a.n_ctas = p->counts.n_ctas;
     a.n_qo_heads = n_qo_heads;
     a.n_kv_heads = n_kv_heads;
     a.head_dim = head_dim;
@@ -293,6 +330,9 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
     a.lse = lse;
     a.ws_o = p->ws_o;
     a.ws_lse = p->ws_lse;
+    a.merge_counters = p->dev_state;
+    a.status = p->dev_state + p->lim.max_merges;
+    a.zero_row = p->zero_row;
     cudaError_t e = launch_decode(a, stream);
     if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attn: launch");
     return PKV_OK;

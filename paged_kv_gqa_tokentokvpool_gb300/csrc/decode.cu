@@ -1,4 +1,4 @@
-// Split-KV paged decode attention with grouped-query heads, and its LSE merge.
+// Split-KV paged decode attention with grouped-query heads and a fused LSE merge.
 //
 // What is computed ("Agent-Infer: 纯 Rust 编写的高性能 LLM 推理引擎", section
 // "分页 KV 缓存": batched decode over a page-size-1 token pool; "Pegainfer:
@@ -8,19 +8,40 @@
 //     out[b,h] = softmax_j(sm_scale * q[b,h] . K[idx_j, g]) . V[idx_j, g]
 //     lse[b,h] = ln sum_j exp(sm_scale * q[b,h] . K[idx_j, g]).
 //
-// Work decomposition: one CTA per work unit of the step's plan (a request and a
-// token range of its slot list), one warp per KV head inside the CTA. A warp keeps
-// the G query heads of its group in registers, so each K/V row it loads serves all
-// G heads; lane i owns head_dim/32 consecutive dimensions, so one (slot, head) row
-// of 256 or 512 bytes is one coalesced 8- or 16-byte-per-lane load. Slot ids are
-// fetched 32 at a time (one per lane) and broadcast with shuffles; rows are loaded
-// U tokens ahead of their use. Scores are reduced across the warp with xor
-// shuffles, then an online softmax in base 2 (scores pre-multiplied by
-// sm_scale * log2 e) rescales the fp32 accumulators. A unit that covers a whole
-// context writes bf16 out and lse; a unit that covers part of one writes its
-// normalised fp32 output and base-2 lse to the plan's workspace, and the merge
-// kernel combines the parts: lse = log2 sum_c 2^lse_c, out = sum_c 2^(lse_c - lse)
-// out_c (the log-sum-exp identity for attention over disjoint parts of a context).
+// Design for sm_103a. The kernel is HBM-bound (about G flops per byte of K/V), so
+// everything serves the gather of scattered pool rows:
+//  * Persistent CTAs (two per SM), each walking the list of work units the
+//    per-step plan gave it. A unit is a token range of one request for one
+//    KV-head group of up to 512 bf16 per token (4 heads at head_dim 128, 2 at
+//    256), so one token's K (or V) row of the group is one contiguous 1 KB run of
+//    the pool.
+//  * Warp specialisation: one producer warp turns slot ids into 1D bulk copies
+//    (cp.async.bulk, the TMA engine) of whole rows into a 3-stage shared-memory
+//    ring of 16-token tiles, signalled by mbarrier transaction counts; lane i
+//    copies token i%16's K (i < 16) or V (i >= 16) row. Four consumer warps take
+//    the tiles. Up to 3 x 32 KB per CTA is in flight, which covers HBM latency
+//    with two CTAs per SM.
+//  * The consumers use the tensor cores for the two small contractions of a GQA
+//    group, so that all G query heads are served by one read of each K/V row and
+//    the instruction count per byte stays far below the issue rate:
+//      S^T[16 tokens x 8 heads]  = K_tile[16 x D] . Q^T[D x 8]     (mma m16n8k16)
+//      O^T[D x 8 heads]         += V_tile^T[D x 16] . P^T[16 x 8]
+//    K and V tiles come from shared memory with ldmatrix (V transposed on the
+//    fly), q stays in registers for the whole unit, and the probabilities move
+//    from the S^T accumulator layout to the P^T operand layout with movmatrix.
+//    Heads beyond G in the 8-wide tile are zero padding.
+//  * Online softmax in base 2 (scores times sm_scale * log2 e), fp32 state per
+//    head; the output accumulators are rescaled only when some running maximum
+//    moved.
+//  * A unit covering a whole context writes bf16 out and lse directly. A unit
+//    covering part of one writes its normalised fp32 output and base-2 lse to the
+//    plan's workspace and bumps the context's arrival counter; the CTA that
+//    arrives last merges all parts by the log-sum-exp identity
+//        lse = log2 sum_c 2^lse_c,   out = sum_c 2^(lse_c - lse) out_c
+//    and resets the counter, so no separate merge launch is needed.
+//  * Every wait on an mbarrier is bounded (1 s); on expiry the kernel sets the
+//    plan's status word, stops, and waits (again bounded) for its own copies in
+//    flight before exiting.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -29,254 +50,546 @@
 namespace pkv {
 namespace {
 
+constexpr int kTile = 16;           // tokens per pipeline stage (one mma M block)
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kStages = 3;
+constexpr int kRowPad = 16;         // bytes between staged rows: conflict-free ldmatrix
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
-__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+// ---------------------------------------------------------------------------
+// PTX wrappers (PTX ISA: mbarrier, cp.async.bulk, ldmatrix, mma, movmatrix)
+// ---------------------------------------------------------------------------
 
-// 2^x with the hardware's approximate exponential unit (ex2.approx, PTX ISA).
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase of `bar` with the given parity. Returns false (and
+// raises the CTA's abort flag and the status word) if it does not complete
+// within kWaitLimitNs, or if another warp of the CTA already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status,
+                                          volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, 1);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// 1D bulk copy global -> shared (TMA), completing `bytes` on mbarrier `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// 2^x on the hardware's approximate exponential unit (ex2.approx, PTX ISA).
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
-template <int VD>
-struct RowVec;
-template <>
-struct RowVec<4> {
-    using T = uint2;
-};
-template <>
-struct RowVec<8> {
-    using T = uint4;
-};
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-// bf16 -> fp32 is exact: the bf16 bits are the upper half of the fp32 bits.
-template <int VD>
-__device__ __forceinline__ void unpack(const typename RowVec<VD>::T& raw, float (&f)[VD]) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw);
-#pragma unroll
-    for (int i = 0; i < VD / 2; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int VD>
-__device__ __forceinline__ typename RowVec<VD>::T pack_bf16(const float (&f)[VD]) {
-    typename RowVec<VD>::T raw;
-    uint32_t* w = reinterpret_cast<uint32_t*>(&raw);
-#pragma unroll
-    for (int i = 0; i < VD / 2; ++i) {
-        __nv_bfloat162 p = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-        w[i] = *reinterpret_cast<uint32_t*>(&p);
-    }
-    return raw;
-}
+// ---------------------------------------------------------------------------
+// kernel
+// ---------------------------------------------------------------------------
 
-template <int D, int G, int U>
-__global__ void __launch_bounds__(256)
-split_kv_decode_kernel(const __nv_bfloat16* __restrict__ q,
-                       const __nv_bfloat16* __restrict__ k_pool,
-                       const __nv_bfloat16* __restrict__ v_pool,
-                       const int32_t* __restrict__ kv_indptr,
-                       const int32_t* __restrict__ kv_indices, const Unit* __restrict__ units,
-                       int n_kv_heads, float scale_log2, __nv_bfloat16* __restrict__ out,
-                       float* __restrict__ lse, float* __restrict__ ws_o,
-                       float* __restrict__ ws_lse) {
-    constexpr int VD = D / 32;
-    using Vec = typename RowVec<VD>::T;
-    const Unit u = units[blockIdx.x];
-    const int kvh = threadIdx.x >> 5;
+template <int D, int G, int WPH>
+struct Cfg {
+    static constexpr int kHeadsPerCta = kConsumerWarps / WPH;   // KV heads of one group
+    static constexpr int kRow = kHeadsPerCta * D * 2;           // bytes of a staged row
+    static constexpr int kRowP = kRow + kRowPad;
+    static constexpr int kStage = 2 * kTile * kRowP;            // K rows then V rows
+    static constexpr int kKSteps = D / 16;                      // k-steps of S^T
+    static constexpr int kMBlocks = D / 16 / WPH;               // O^T dim blocks per warp
+    static constexpr int kDimsPerWarp = D / WPH;
+    static constexpr int kQHeads = kHeadsPerCta * G;            // query heads of a group
+    static constexpr int kBarOffset = kStages * kStage;
+    static constexpr int kSmem = kBarOffset + (2 * kStages + 1) * 8 + 16;
+    static_assert(G >= 1 && G <= 8, "group size");
+    static_assert(kHeadsPerCta * D <= kHeadGroupElems, "head group too wide");
+    static_assert(kMBlocks >= 1, "dims per warp");
+};
+
+struct Shared {
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* cons;       // consumer-warps barrier
+    volatile int* flags;  // [0] abort, [1] this CTA merges the current unit
+};
+
+template <int D, int G, int WPH>
+__device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
+                              int u_end) {
+    using C = Cfg<D, G, WPH>;
     const int lane = threadIdx.x & 31;
-    const int hq = n_kv_heads * G;
-    const int64_t row_elems = int64_t(n_kv_heads) * D;
-    const int64_t ctx0 = kv_indptr[u.b];
-
-    float qf[G][VD];
-    const __nv_bfloat16* qp = q + (int64_t(u.b) * hq + kvh * G) * D + lane * VD;
-#pragma unroll
-    for (int g = 0; g < G; ++g) unpack<VD>(*reinterpret_cast<const Vec*>(qp + g * D), qf[g]);
-
-    float m[G], l[G], o[G][VD];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = neg_inf();
-        l[g] = 0.f;
-#pragma unroll
-        for (int i = 0; i < VD; ++i) o[g][i] = 0.f;
-    }
-
-    const __nv_bfloat16* kp = k_pool + kvh * D + lane * VD;
-    const __nv_bfloat16* vp = v_pool + kvh * D + lane * VD;
-    for (int t0 = u.tok_begin; t0 < u.tok_end; t0 += 32) {
-        const int n = min(32, u.tok_end - t0);
-        const int my_slot = lane < n ? __ldg(kv_indices + ctx0 + t0 + lane) : 0;
-        for (int j = 0; j < n; j += U) {
-            Vec kr[U], vr[U];
-#pragma unroll
-            for (int uu = 0; uu < U; ++uu) {
-                const int64_t slot = __shfl_sync(kFull, my_slot, j + uu);
-                if (j + uu < n) {
-                    kr[uu] = __ldg(reinterpret_cast<const Vec*>(kp + slot * row_elems));
-                    vr[uu] = __ldg(reinterpret_cast<const Vec*>(vp + slot * row_elems));
-                } else {
-                    kr[uu] = Vec{};
-                    vr[uu] = Vec{};
-                }
+    const int tok = lane & (kTile - 1);
+    const bool is_v = lane >= kTile;
+    const char* pool = static_cast<const char*>(is_v ? a.v_pool : a.k_pool);
+    const int64_t slot_bytes = int64_t(a.n_kv_heads) * D * 2;
+    const uint32_t ring = smem_u32(smem) + (is_v ? kTile * C::kRowP : 0) + tok * C::kRowP;
+    int stage = 0;
+    uint32_t empty_parity = 1;  // a fresh barrier reports the phase before it as complete
+    uint32_t fill_parity = 0;
+    uint32_t filled_mask = 0, parity_bits = 0;  // per stage: filled at all / parity of last fill
+    bool aborted = false;
+    for (int u = u_begin; u < u_end && !aborted; ++u) {
+        const Unit un = a.units[u];
+        const int n_tok = un.tok_end - un.tok_begin;
+        const int32_t* idx = a.kv_indices + __ldg(a.kv_indptr + un.b) + un.tok_begin;
+        for (int off = lane * 32; off < n_tok; off += 32 * 32) prefetch_l2(idx + off);
+        const int n_tiles = n_tok > 0 ? (n_tok + kTile - 1) / kTile : 1;
+        const int64_t group_off = int64_t(un.hg) * C::kRow;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int n = min(kTile, n_tok - t * kTile);
+            const int slot = tok < n ? __ldg(idx + t * kTile + tok) : -1;
+            const uint32_t full_bar = smem_u32(&sh.full[stage]);
+            if (lane == 0 && !mbar_wait(smem_u32(&sh.empty[stage]), empty_parity, a.status, sh.flags))
+                sh.flags[0] = 1;
+            __syncwarp();
+            if (sh.flags[0]) {
+                aborted = true;
+                break;
             }
-            float s[U][G];
-#pragma unroll
-            for (int uu = 0; uu < U; ++uu) {
-                float kf[VD];
-                unpack<VD>(kr[uu], kf);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int i = 0; i < VD; ++i) acc = fmaf(qf[g][i], kf[i], acc);
-                    s[uu][g] = acc;
-                }
+            if (lane == 0) mbar_arrive_expect_tx(full_bar, n > 0 ? 2u * kTile * C::kRow : 0u);
+            __syncwarp();
+            if (n > 0) {
+                const void* src = slot >= 0 ? static_cast<const void*>(pool + slot * slot_bytes + group_off)
+                                            : a.zero_row;
+                bulk_g2s(ring + stage * C::kStage, src, C::kRow, full_bar);
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                for (int uu = 0; uu < U; ++uu)
-#pragma unroll
-                    for (int g = 0; g < G; ++g)
-                        s[uu][g] += __shfl_xor_sync(kFull, s[uu][g], off);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float mx = m[g];
-#pragma unroll
-                for (int uu = 0; uu < U; ++uu) {
-                    s[uu][g] = (j + uu < n) ? s[uu][g] * scale_log2 : neg_inf();
-                    mx = fmaxf(mx, s[uu][g]);
-                }
-                const float alpha = ex2(m[g] - mx);
-                m[g] = mx;
-                l[g] *= alpha;
-#pragma unroll
-                for (int i = 0; i < VD; ++i) o[g][i] *= alpha;
-#pragma unroll
-                for (int uu = 0; uu < U; ++uu) {
-                    s[uu][g] = ex2(s[uu][g] - mx);
-                    l[g] += s[uu][g];
-                }
-            }
-#pragma unroll
-            for (int uu = 0; uu < U; ++uu) {
-                float vf[VD];
-                unpack<VD>(vr[uu], vf);
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int i = 0; i < VD; ++i) o[g][i] = fmaf(s[uu][g], vf[i], o[g][i]);
+            filled_mask |= 1u << stage;
+            parity_bits = (parity_bits & ~(1u << stage)) | (fill_parity << stage);
+            if (++stage == kStages) {
+                stage = 0;
+                empty_parity ^= 1;
+                fill_parity ^= 1;
             }
         }
     }
-
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const int h = kvh * G + g;
-        const bool empty = (l[g] == 0.f);
-        const float inv = empty ? 0.f : 1.f / l[g];
-        const float lse2 = empty ? neg_inf() : m[g] + __log2f(l[g]);
-        float r[VD];
-#pragma unroll
-        for (int i = 0; i < VD; ++i) r[i] = o[g][i] * inv;
-        if (u.partial < 0) {
-            const int64_t oh = int64_t(u.b) * hq + h;
-            *reinterpret_cast<Vec*>(out + oh * D + lane * VD) = pack_bf16<VD>(r);
-            if (lse != nullptr && lane == 0) lse[oh] = lse2 * kLn2;
-        } else {
-            const int64_t ph = int64_t(u.partial) * hq + h;
-            float* dst = ws_o + ph * D + lane * VD;
-#pragma unroll
-            for (int i = 0; i < VD; i += 4)
-                *reinterpret_cast<float4*>(dst + i) = make_float4(r[i], r[i + 1], r[i + 2], r[i + 3]);
-            if (lane == 0) ws_lse[ph] = lse2;
-        }
+    // No bulk copy may still be writing this CTA's shared memory when it exits.
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s)
+            if (filled_mask & (1u << s)) {
+                const uint32_t bar = smem_u32(&sh.full[s]);
+                const uint32_t par = (parity_bits >> s) & 1u;
+                if (!mbar_try_wait(bar, par)) {
+                    const unsigned long long t0 = global_ns();
+                    while (!mbar_try_wait(bar, par) && global_ns() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
     }
 }
 
-// One CTA per split request; warp w merges query heads w, w + 4, ...
-template <int D>
-__global__ void __launch_bounds__(128)
-lse_merge_kernel(const Merge* __restrict__ merges, int hq, const float* __restrict__ ws_o,
-                 const float* __restrict__ ws_lse, __nv_bfloat16* __restrict__ out,
-                 float* __restrict__ lse) {
-    constexpr int VD = D / 32;
-    using Vec = typename RowVec<VD>::T;
-    const Merge mg = merges[blockIdx.x];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int h = warp; h < hq; h += blockDim.x / 32) {
+template <int D, int G, int WPH>
+__device__ void merge_parts(const DecodeArgs& a, const Unit& un, int hh, int part, int lane) {
+    using C = Cfg<D, G, WPH>;
+    const Merge mg = a.merges[un.merge];
+    const int hq = a.n_qo_heads;
+    const int kvh = un.hg * C::kHeadsPerCta + hh;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    for (int e = lane * 4; e < G * C::kDimsPerWarp; e += 128) {
+        const int h = e / C::kDimsPerWarp;
+        const int d = part * C::kDimsPerWarp + (e % C::kDimsPerWarp);
+        const int qh = hh * G + h;
+        const float* lse_p = a.ws_lse + int64_t(mg.first) * C::kQHeads + qh;
         float mx = neg_inf();
-        for (int c = 0; c < mg.count; ++c) mx = fmaxf(mx, ws_lse[int64_t(mg.first + c) * hq + h]);
+        for (int c = 0; c < mg.count; ++c) mx = fmaxf(mx, __ldcg(lse_p + int64_t(c) * C::kQHeads));
         float sum = 0.f;
-        for (int c = 0; c < mg.count; ++c) sum += ex2(ws_lse[int64_t(mg.first + c) * hq + h] - mx);
+        for (int c = 0; c < mg.count; ++c) sum += ex2(__ldcg(lse_p + int64_t(c) * C::kQHeads) - mx);
         const float total = mx + __log2f(sum);
-        float acc[VD];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* o_p = a.ws_o + (int64_t(mg.first) * C::kQHeads + qh) * D + d;
+        int c = 0;
+        for (; c + 2 <= mg.count; c += 2) {
+            const float w0 = ex2(__ldcg(lse_p + int64_t(c) * C::kQHeads) - total);
+            const float w1 = ex2(__ldcg(lse_p + int64_t(c + 1) * C::kQHeads) - total);
+            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(o_p + int64_t(c) * C::kQHeads * D));
+            const float4 x1 =
+                __ldcg(reinterpret_cast<const float4*>(o_p + int64_t(c + 1) * C::kQHeads * D));
+            acc.x = fmaf(w0, x0.x, fmaf(w1, x1.x, acc.x));
+            acc.y = fmaf(w0, x0.y, fmaf(w1, x1.y, acc.y));
+            acc.z = fmaf(w0, x0.z, fmaf(w1, x1.z, acc.z));
+            acc.w = fmaf(w0, x0.w, fmaf(w1, x1.w, acc.w));
+        }
+        for (; c < mg.count; ++c) {
+            const float w0 = ex2(__ldcg(lse_p + int64_t(c) * C::kQHeads) - total);
+            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(o_p + int64_t(c) * C::kQHeads * D));
+            acc.x = fmaf(w0, x0.x, acc.x);
+            acc.y = fmaf(w0, x0.y, acc.y);
+            acc.z = fmaf(w0, x0.z, acc.z);
+            acc.w = fmaf(w0, x0.w, acc.w);
+        }
+        const int64_t orow = (int64_t(un.b) * hq + kvh * G + h) * D + d;
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x, acc.y);
+        packed.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(out + orow) = packed;
+        if (a.lse != nullptr && part == 0 && (e % C::kDimsPerWarp) == 0)
+            a.lse[int64_t(un.b) * hq + kvh * G + h] = total * kLn2;
+    }
+}
+
+template <int D, int G, int WPH>
+__device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
+                              int u_end) {
+    using C = Cfg<D, G, WPH>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hh = warp / WPH;    // KV head within the group
+    const int part = warp % WPH;  // which slice of head_dim this warp accumulates
+    const int g = lane >> 2, t4 = lane & 3;
+    const int hq = a.n_qo_heads;
+    const float scale_log2 = a.sm_scale * kLog2e;
+    // ldmatrix row addresses within a stage (see the fragment layouts of mma.m16n8k16):
+    // K tile as the A operand (rows = tokens, k = dims)
+    const uint32_t k_lane = smem_u32(smem) + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowP +
+                            (hh * D + (lane >> 4) * 8) * 2;
+    // V tile, transposed on load, as the A operand (rows = dims, k = tokens)
+    const uint32_t v_lane = smem_u32(smem) + kTile * C::kRowP +
+                            ((lane & 7) + (lane >> 4) * 8) * C::kRowP +
+                            (hh * D + part * C::kDimsPerWarp + ((lane >> 3) & 1) * 8) * 2;
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+    int stage = 0;
+    uint32_t full_parity = 0, cons_parity = 0;
+
+    for (int u = u_begin; u < u_end; ++u) {
+        const Unit un = a.units[u];
+        const int kvh = un.hg * C::kHeadsPerCta + hh;
+        // Q^T as the B operand: lane holds head g, dims 2*t4.. of each k-step
+        uint32_t qb[C::kKSteps][2];
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            q + (int64_t(un.b) * hq + kvh * G + (g < G ? g : 0)) * D + 2 * t4);
 #pragma unroll
-        for (int i = 0; i < VD; ++i) acc[i] = 0.f;
-        for (int c = 0; c < mg.count; ++c) {
-            const int64_t ph = int64_t(mg.first + c) * hq + h;
-            const float w = ex2(ws_lse[ph] - total);
-            const float* src = ws_o + ph * D + lane * VD;
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+            qb[ks][0] = g < G ? __ldg(qrow + ks * 8) : 0u;
+            qb[ks][1] = g < G ? __ldg(qrow + ks * 8 + 4) : 0u;
+        }
+        float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+        float o[C::kMBlocks][4];
 #pragma unroll
-            for (int i = 0; i < VD; i += 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src + i);
-                acc[i] = fmaf(w, x.x, acc[i]);
-                acc[i + 1] = fmaf(w, x.y, acc[i + 1]);
-                acc[i + 2] = fmaf(w, x.z, acc[i + 2]);
-                acc[i + 3] = fmaf(w, x.w, acc[i + 3]);
+        for (int mb = 0; mb < C::kMBlocks; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
+
+        const int n_tok = un.tok_end - un.tok_begin;
+        const int n_tiles = n_tok > 0 ? (n_tok + kTile - 1) / kTile : 1;
+        for (int t = 0; t < n_tiles; ++t) {
+            const bool ok = mbar_wait(smem_u32(&sh.full[stage]), full_parity, a.status, sh.flags);
+            if (!__all_sync(kFull, ok)) return;  // uniform exit: no lane is left in a shuffle
+            const int n = n_tok - t * kTile < kTile ? n_tok - t * kTile : kTile;
+            if (n > 0) {
+                const uint32_t st = stage * C::kStage;
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < C::kKSteps; ++ks) {
+                    uint32_t ka[4];
+                    ldsm_x4(k_lane + st + ks * 32, ka);
+                    mma_bf16(s, ka, qb[ks][0], qb[ks][1]);
+                }
+                // s[0], s[1]: token g, heads 2t4, 2t4+1; s[2], s[3]: token g + 8
+                const float x0 = g < n ? s[0] * scale_log2 : neg_inf();
+                const float x1 = g < n ? s[1] * scale_log2 : neg_inf();
+                const float x2 = g + 8 < n ? s[2] * scale_log2 : neg_inf();
+                const float x3 = g + 8 < n ? s[3] * scale_log2 : neg_inf();
+                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+                m0 = mn0;
+                m1 = mn1;
+                const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
+                const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
+                l0 = fmaf(l0, al0, p0 + p2);
+                l1 = fmaf(l1, al1, p1 + p3);
+                if (__any_sync(kFull, (al0 != 1.f) || (al1 != 1.f))) {
+#pragma unroll
+                    for (int mb = 0; mb < C::kMBlocks; ++mb) {
+                        o[mb][0] *= al0;
+                        o[mb][1] *= al1;
+                        o[mb][2] *= al0;
+                        o[mb][3] *= al1;
+                    }
+                }
+                // P^T operand: tokens 0-7 and 8-15 of the tile, heads in columns
+                const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+                const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+#pragma unroll
+                for (int mb = 0; mb < C::kMBlocks; ++mb) {
+                    uint32_t va[4];
+                    ldsm_x4_trans(v_lane + st + mb * 32, va);
+                    mma_bf16(o[mb], va, pb0, pb1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.empty[stage]));
+            if (++stage == kStages) {
+                stage = 0;
+                full_parity ^= 1;
             }
         }
-        const int64_t oh = int64_t(mg.b) * hq + h;
-        *reinterpret_cast<Vec*>(out + oh * D + lane * VD) = pack_bf16<VD>(acc);
-        if (lse != nullptr && lane == 0) lse[oh] = total * kLn2;
+
+        // ---- epilogue: o[mb][0..3] = (dim 16*mb' + g (+8), heads 2t4, 2t4+1)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(kFull, l0, off);
+            l1 += __shfl_xor_sync(kFull, l1, off);
+        }
+        const float inv0 = l0 == 0.f ? 0.f : 1.f / l0;
+        const float inv1 = l1 == 0.f ? 0.f : 1.f / l1;
+        const float lse0 = l0 == 0.f ? neg_inf() : m0 + __log2f(l0);
+        const float lse1 = l1 == 0.f ? neg_inf() : m1 + __log2f(l1);
+        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+        const int dim0 = part * C::kDimsPerWarp + g;
+        if (un.partial < 0) {
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+            __nv_bfloat16* r0 = out + (int64_t(un.b) * hq + kvh * G + h0) * D + dim0;
+            __nv_bfloat16* r1 = r0 + D;
+#pragma unroll
+            for (int mb = 0; mb < C::kMBlocks; ++mb) {
+                if (h0 < G) {
+                    r0[mb * 16] = __float2bfloat16_rn(o[mb][0] * inv0);
+                    r0[mb * 16 + 8] = __float2bfloat16_rn(o[mb][2] * inv0);
+                }
+                if (h1 < G) {
+                    r1[mb * 16] = __float2bfloat16_rn(o[mb][1] * inv1);
+                    r1[mb * 16 + 8] = __float2bfloat16_rn(o[mb][3] * inv1);
+                }
+            }
+            if (a.lse != nullptr && part == 0 && g == 0) {
+                if (h0 < G) a.lse[int64_t(un.b) * hq + kvh * G + h0] = lse0 * kLn2;
+                if (h1 < G) a.lse[int64_t(un.b) * hq + kvh * G + h1] = lse1 * kLn2;
+            }
+            continue;
+        }
+        // partial result of a split context
+        float* p0r = a.ws_o + (int64_t(un.partial) * C::kQHeads + hh * G + h0) * D + dim0;
+        float* p1r = p0r + D;
+#pragma unroll
+        for (int mb = 0; mb < C::kMBlocks; ++mb) {
+            if (h0 < G) {
+                p0r[mb * 16] = o[mb][0] * inv0;
+                p0r[mb * 16 + 8] = o[mb][2] * inv0;
+            }
+            if (h1 < G) {
+                p1r[mb * 16] = o[mb][1] * inv1;
+                p1r[mb * 16 + 8] = o[mb][3] * inv1;
+            }
+        }
+        if (part == 0 && g == 0) {
+            float* lp = a.ws_lse + int64_t(un.partial) * C::kQHeads + hh * G;
+            if (h0 < G) lp[h0] = lse0;
+            if (h1 < G) lp[h1] = lse1;
+        }
+        // Arrive on the context's counter once all four warps' stores are out;
+        // the last arriving CTA merges.
+        __threadfence();
+        __syncwarp();
+        const uint32_t cons_bar = smem_u32(sh.cons);
+        if (lane == 0) mbar_arrive(cons_bar);
+        if (!__all_sync(kFull, mbar_wait(cons_bar, cons_parity, a.status, sh.flags))) return;
+        cons_parity ^= 1;
+        if (warp == 0 && lane == 0) {
+            const int prev = atomicAdd(a.merge_counters + un.merge, 1);
+            const int last = prev == a.merges[un.merge].count - 1;
+            if (last) a.merge_counters[un.merge] = 0;
+            sh.flags[1] = last;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cons_bar);
+        if (!__all_sync(kFull, mbar_wait(cons_bar, cons_parity, a.status, sh.flags))) return;
+        cons_parity ^= 1;
+        if (sh.flags[1]) {
+            __threadfence();
+            merge_parts<D, G, WPH>(a, un, hh, part, lane);
+        }
     }
 }
 
-template <int D, int G>
-cudaError_t launch_shape(const DecodeArgs& a, cudaStream_t stream) {
-    constexpr int U = 4;
-    if (a.n_units > 0) {
-        split_kv_decode_kernel<D, G, U><<<a.n_units, 32 * a.n_kv_heads, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_pool),
-            static_cast<const __nv_bfloat16*>(a.v_pool), a.kv_indptr, a.kv_indices, a.units,
-            a.n_kv_heads, a.sm_scale * kLog2e, static_cast<__nv_bfloat16*>(a.out), a.lse,
-            a.ws_o, a.ws_lse);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+template <int D, int G, int WPH>
+__global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeArgs a) {
+    using C = Cfg<D, G, WPH>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    Shared sh;
+    sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    sh.empty = sh.full + kStages;
+    sh.cons = sh.empty + kStages;
+    sh.flags = reinterpret_cast<volatile int*>(sh.cons + 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), 1);
+            mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
+        }
+        mbar_init(smem_u32(sh.cons), kConsumerWarps);
+        sh.flags[0] = 0;
+        sh.flags[1] = 0;
+        fence_mbar_init();
     }
-    if (a.n_merges > 0) {
-        lse_merge_kernel<D><<<a.n_merges, 128, 0, stream>>>(
-            a.merges, a.n_qo_heads, a.ws_o, a.ws_lse, static_cast<__nv_bfloat16*>(a.out), a.lse);
-        return cudaGetLastError();
-    }
-    return cudaSuccess;
+    __syncthreads();
+    const int u_begin = a.cta_begin[blockIdx.x];
+    const int u_end = a.cta_begin[blockIdx.x + 1];
+    if ((threadIdx.x >> 5) == kConsumerWarps)
+        producer_warp<D, G, WPH>(a, smem, sh, u_begin, u_end);
+    else
+        consumer_warp<D, G, WPH>(a, smem, sh, u_begin, u_end);
 }
 
-template <int D, int G>
-int occupancy_shape(int n_kv_heads) {
+template <int D, int G, int WPH>
+cudaError_t prepare() {
+    // Raise the dynamic shared memory limit once per instance.
+    static cudaError_t status = cudaFuncSetAttribute(
+        paged_decode_kernel<D, G, WPH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        Cfg<D, G, WPH>::kSmem);
+    return status;
+}
+
+template <int D, int G, int WPH>
+int occupancy() {
+    if (prepare<D, G, WPH>() != cudaSuccess) return 0;
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_kv_decode_kernel<D, G, 4>,
-                                                      32 * n_kv_heads, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_kernel<D, G, WPH>,
+                                                      kThreads, Cfg<D, G, WPH>::kSmem) != cudaSuccess)
         return 0;
     return blocks;
 }
 
-#define PKV_DISPATCH(D_, FN, ...)                         \
-    switch (G) {                                          \
-        case 1: return FN<D_, 1>(__VA_ARGS__);            \
-        case 2: return FN<D_, 2>(__VA_ARGS__);            \
-        case 4: return FN<D_, 4>(__VA_ARGS__);            \
-        case 8: return FN<D_, 8>(__VA_ARGS__);            \
-        default: break;                                   \
+template <int D, int G, int WPH>
+cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
+    cudaError_t e = prepare<D, G, WPH>();
+    if (e != cudaSuccess) return e;
+    if (a.n_ctas == 0) return cudaSuccess;
+    paged_decode_kernel<D, G, WPH><<<a.n_ctas, kThreads, Cfg<D, G, WPH>::kSmem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// Calls FN<D, G, WPH>(args...) for the runtime shape.
+template <template <int, int, int> class FN, typename... Args>
+auto dispatch(int head_dim, int group, int wph, Args&&... args)
+    -> decltype(FN<128, 1, 1>::run(args...)) {
+#define PKV_G(D_, W_)                                          \
+    switch (group) {                                           \
+        case 1: return FN<D_, 1, W_>::run(args...);            \
+        case 2: return FN<D_, 2, W_>::run(args...);            \
+        case 4: return FN<D_, 4, W_>::run(args...);            \
+        case 8: return FN<D_, 8, W_>::run(args...);            \
+        default: break;                                        \
     }
+    if (head_dim == 128) {
+        if (wph == 1) { PKV_G(128, 1) }
+        if (wph == 2) { PKV_G(128, 2) }
+        if (wph == 4) { PKV_G(128, 4) }
+    } else if (head_dim == 256) {
+        if (wph == 2) { PKV_G(256, 2) }
+        if (wph == 4) { PKV_G(256, 4) }
+    }
+#undef PKV_G
+    return FN<128, 1, 1>::unsupported();
+}
+
+template <int D, int G, int WPH>
+struct OccupancyFn {
+    static int run() { return occupancy<D, G, WPH>(); }
+    static int unsupported() { return 0; }
+};
+template <int D, int G, int WPH>
+struct LaunchFn {
+    static cudaError_t run(const DecodeArgs& a, cudaStream_t s) { return launch<D, G, WPH>(a, s); }
+    static cudaError_t unsupported() { return cudaErrorInvalidValue; }
+};
+
+int warps_per_head(int n_kv_heads, int head_dim) {
+    return kConsumerWarps / heads_per_group(n_kv_heads, head_dim);
+}
 
 }  // namespace
 
@@ -285,28 +598,19 @@ bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim) {
     const int G = n_qo_heads / n_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return false;
     if (head_dim != 128 && head_dim != 256) return false;
-    return n_kv_heads <= 8;
+    return n_kv_heads == 1 || n_kv_heads == 2 || n_kv_heads == 4 || n_kv_heads == 8;
 }
 
 int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim) {
     if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim)) return 0;
-    const int G = n_qo_heads / n_kv_heads;
-    if (head_dim == 128) {
-        PKV_DISPATCH(128, occupancy_shape, n_kv_heads)
-    } else {
-        PKV_DISPATCH(256, occupancy_shape, n_kv_heads)
-    }
-    return 0;
+    return dispatch<OccupancyFn>(head_dim, n_qo_heads / n_kv_heads,
+                                 warps_per_head(n_kv_heads, head_dim));
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-    const int G = a.n_qo_heads / a.n_kv_heads;
-    if (a.head_dim == 128) {
-        PKV_DISPATCH(128, launch_shape, a, stream)
-    } else {
-        PKV_DISPATCH(256, launch_shape, a, stream)
-    }
-    return cudaErrorInvalidValue;
+    const cudaError_t e = dispatch<LaunchFn>(a.head_dim, a.n_qo_heads / a.n_kv_heads,
+                                             warps_per_head(a.n_kv_heads, a.head_dim), a, stream);
+    return e;
 }
 
 }  // namespace pkv

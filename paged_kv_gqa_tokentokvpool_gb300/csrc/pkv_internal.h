@@ -15,39 +15,52 @@ int fail(int code, const char* fmt, ...);  // records the message, returns code
 void clear_error();
 bool debug_checks();
 
+// ---- shapes ----------------------------------------------------------------
+// A CTA of the decode kernel serves one KV-head group: the first
+// kHeadGroupElems / head_dim KV heads (or all of them, if fewer). One token's K
+// (or V) row of a group is then at most kHeadGroupElems bf16 = 1 KB, one bulk copy.
+constexpr int kHeadGroupElems = 512;
+inline int heads_per_group(int n_kv_heads, int head_dim) {
+    const int cap = kHeadGroupElems / head_dim;
+    return n_kv_heads < cap ? n_kv_heads : cap;
+}
+
 // ---- plan ----------------------------------------------------------------
-// One work unit of the split-KV kernel: tokens [tok_begin, tok_end) of request b,
-// all KV heads. partial < 0: the unit covers the whole context and writes out/lse;
-// otherwise it writes partial slot `partial` of the workspace.
+// One work unit of the decode kernel: tokens [tok_begin, tok_end) of request b's
+// slot list, KV-head group hg. partial < 0: the unit covers the whole context and
+// writes out/lse; otherwise it writes partial slot `partial` of the workspace and
+// takes part in merge record `merge`.
 struct Unit {
-    int32_t b, tok_begin, tok_end, partial;
+    int32_t b, hg, tok_begin, tok_end, partial, merge, pad0, pad1;
 };
-// One split request: its parts occupy partial slots [first, first + count).
+// One split (request, head group): its parts occupy partial slots
+// [first, first + count).
 struct Merge {
-    int32_t b, first, count, pad;
+    int32_t b, hg, first, count;
 };
-static_assert(sizeof(Unit) == 16 && sizeof(Merge) == 16, "16-byte plan records");
+static_assert(sizeof(Unit) == 32 && sizeof(Merge) == 16, "plan record sizes");
 
-struct PlanShape {
-    int num_sms;
-    int ctas_per_sm;
+// Contexts up to this many tokens are never split.
+constexpr int kMinChunkTokens = 64;
+// Chunk lengths are multiples of this many tokens (one pipeline tile).
+constexpr int kChunkQuantum = 16;
+// The planner keeps the unit count within this many units per CTA (plus one
+// unit per (request, head group)), which bounds the plan's buffers.
+constexpr int kMaxUnitsPerCta = 8;
+
+struct PlanLimits {
+    int max_units;
+    int max_merges;
+};
+struct PlanCounts {
+    int n_units, n_ctas, n_merges, n_partials, chunk_tokens;
 };
 
-// Tokens below which a context is never split: a split costs one fp32 partial
-// (n_qo_heads * head_dim * 4 bytes written and read back) and is only worth it
-// when the chunk it creates reads much more than that.
-constexpr int kMinChunkTokens = 256;
-// Chunk lengths are multiples of this many tokens.
-constexpr int kChunkQuantum = 64;
-// Work units the planner aims for, per resident CTA slot of the device.
-constexpr int kWavesTarget = 4;
-
-int plan_target_units(const PlanShape& s);
-// Pure host planner. Returns PKV_OK or PKV_ERR_PLAN (arrays too small) /
-// PKV_ERR_INVALID_ARG (bad indptr).
-int plan_compute(const int32_t* indptr, int batch, const PlanShape& shape, Unit* units,
-                 int max_units, Merge* merges, int max_merges, int* n_units, int* n_merges,
-                 int* chunk_tokens);
+int plan_max_units(int ctas, int max_batch, int n_groups);
+// Pure host planner. units[max_units], cta_begin[ctas + 1], merges[max_merges].
+// Returns PKV_OK, PKV_ERR_PLAN (capacity) or PKV_ERR_INVALID_ARG (bad indptr).
+int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, const PlanLimits& lim,
+                 Unit* units, int* cta_begin, Merge* merges, PlanCounts* out);
 
 // ---- kernels -------------------------------------------------------------
 struct DecodeArgs {
@@ -57,21 +70,24 @@ struct DecodeArgs {
     const int32_t* kv_indptr;
     const int32_t* kv_indices;
     const Unit* units;
+    const int32_t* cta_begin;
     const Merge* merges;
-    int n_units;
-    int n_merges;
+    int n_ctas;
     int n_qo_heads;
     int n_kv_heads;
     int head_dim;
     float sm_scale;
     void* out;
     float* lse;
-    float* ws_o;    // [max_units, n_qo_heads, head_dim] fp32 partial outputs
-    float* ws_lse;  // [max_units, n_qo_heads] fp32 partial lse (base 2)
+    float* ws_o;          // [max partials, group q heads, head_dim] fp32 partial outputs
+    float* ws_lse;        // [max partials, group q heads] fp32 partial lse (base 2)
+    int* merge_counters;  // [max merges], zero between launches
+    int* status;          // device status word (nonzero: a wait timed out)
+    const void* zero_row; // kHeadGroupElems bf16 zeros (tile padding)
 };
 
 bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim);
-// Resident CTAs per SM of the split kernel for this shape (0 on error).
+// Resident CTAs per SM of the decode kernel for this shape (0 on error).
 int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
@@ -83,26 +99,24 @@ cudaError_t launch_append(void* k_pool, void* v_pool, const int32_t* slot_ids,
 
 struct pkv_plan {
     int device = 0;
-    pkv::PlanShape shape{};
+    int num_sms = 0, ctas_per_sm = 0, ctas = 0;
     int max_batch = 0;
     int64_t max_tokens = 0;
-    int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0;
-    int max_units = 0, max_merges = 0;
-    void* host_staging = nullptr;  // pinned: units[max_units] then merges[max_merges]
-    void* dev_meta = nullptr;      // device copy of the same
+    int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0, n_groups = 0;
+    pkv::PlanLimits lim{};
+    size_t meta_bytes = 0;
+    void* host_staging = nullptr;  // pinned: cta_begin, then merges, then units
+    void* dev_meta = nullptr;      // device copy of the same (used prefix uploaded per step)
     float* ws_o = nullptr;
     float* ws_lse = nullptr;
+    int* dev_state = nullptr;      // merge counters [max_merges], status word, padding
+    void* zero_row = nullptr;
     cudaEvent_t copy_done = nullptr;
     bool copy_pending = false;
     // the current step
     bool planned = false;
-    int batch = 0, n_units = 0, n_merges = 0, chunk_tokens = 0;
+    int batch = 0;
+    pkv::PlanCounts counts{};
+    size_t off_merge = 0, off_units = 0;  // byte offsets of the regions in the staging
     std::vector<int32_t> indptr_host;
-
-    pkv::Unit* host_units() { return static_cast<pkv::Unit*>(host_staging); }
-    pkv::Merge* host_merges() { return reinterpret_cast<pkv::Merge*>(host_units() + max_units); }
-    const pkv::Unit* dev_units() const { return static_cast<const pkv::Unit*>(dev_meta); }
-    const pkv::Merge* dev_merges() const {
-        return reinterpret_cast<const pkv::Merge*>(dev_units() + max_units);
-    }
 };

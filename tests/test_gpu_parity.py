@@ -107,6 +107,10 @@ SMALL_CASES = [
     ([100, 5000], 64, 8, 128),
     ([77, 3001], 8, 1, 256),
     ([513] * 40, 32, 8, 128),
+    (list(range(0, 3000, 15)), 32, 8, 128),
+    ([131072], 32, 8, 128),
+    ([60000, 1, 16, 17, 15], 16, 2, 256),
+    ([3000, 70], 4, 4, 128),
 ]
 
 
@@ -115,9 +119,10 @@ def test_decode_small_cases(pkv, case):
     lengths, hq, hkv, d = SMALL_CASES[case]
     wl = workloads.scattered_workload(lengths, n_qo_heads=hq, n_kv_heads=hkv, head_dim=d,
                                       seed=100 + case, k_scale=1.0)
-    out, lse, t, *_ = run_small(pkv, wl, debug=(case % 2 == 0))
+    out, lse, t, _, _, plan = run_small(pkv, wl, debug=(case % 2 == 0))
     ref_out, ref_lse = oracle_reference(wl, t)
     assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what=f"case {case}")
+    assert plan.status() == 0
 
 
 def test_append_bit_exact(pkv):
@@ -263,6 +268,7 @@ def test_full_size_config(pkv, config_no):
         sigma2 = wl.k_scale ** 2
         expect = np.log(wl.lengths)[:, None] + sigma2 / 2
         assert abs(float(np.mean(ref_lse - expect))) < 0.2
+    assert st.plan.status() == 0
 
 
 def test_end_to_end_host_path_matches_device_path(pkv):

@@ -63,7 +63,8 @@ def test_errors_are_reported_before_any_launch(pkv):
         assert lib.kvpool_append(mis, p, p, p, p, 1, 8, 128, 16, None) == pkv.PKV_ERR_INVALID_ARG
     # unsupported shapes are rejected by plan creation before touching the device
     h = ctypes.c_void_p()
-    for hq, hkv, d in [(32, 8, 64), (30, 8, 128), (48, 4, 128), (32, 16, 128), (32, 0, 128)]:
+    for hq, hkv, d in [(32, 8, 64), (30, 8, 128), (48, 4, 128), (32, 16, 128), (32, 0, 128),
+                       (24, 6, 128), (48, 3, 256)]:
         rc = lib.paged_decode_plan_create(ctypes.byref(h), 8, 1000, hq, hkv, d)
         assert rc == pkv.PKV_ERR_UNSUPPORTED, (hq, hkv, d, rc)
     assert lib.paged_decode_plan_create(ctypes.byref(h), 0, 1000, 32, 8, 128) == pkv.PKV_ERR_INVALID_ARG
@@ -75,41 +76,47 @@ def test_errors_are_reported_before_any_launch(pkv):
     lib.paged_decode_plan_destroy(None)  # no-op
 
 
-def check_plan(indptr, units, merges, chunk, cap):
+def check_plan(indptr, n_kv_heads, head_dim, ctas, plan):
     indptr = np.asarray(indptr, np.int64)
     B = indptr.size - 1
     lengths = np.diff(indptr)
-    covered = [np.zeros(L, np.int32) for L in lengths]
-    partial_owner = {}
-    direct = set()
-    for b, t0, t1, part in units:
-        assert 0 <= b < B and 0 <= t0 <= t1 <= lengths[b]
-        assert t1 - t0 <= max(chunk, lengths[b] if part < 0 else chunk)
-        covered[b][t0:t1] += 1
+    hpg = min(n_kv_heads, 512 // head_dim)
+    groups = n_kv_heads // hpg
+    units, cta_begin, merges, chunk = plan["units"], plan["cta_begin"], plan["merges"], plan["chunk"]
+    n = len(units)
+    assert cta_begin[0] == 0 and cta_begin[-1] == n
+    assert np.all(np.diff(cta_begin) > 0), "every launched CTA has work"
+    assert len(cta_begin) - 1 <= ctas
+    covered = {(b, g): np.zeros(lengths[b], np.int32) for b in range(B) for g in range(groups)}
+    direct, parts_seen = set(), {}
+    for b, hg, t0, t1, part, merge, _, _ in units:
+        assert 0 <= b < B and 0 <= hg < groups and 0 <= t0 <= t1 <= lengths[b]
+        covered[(b, hg)][t0:t1] += 1
         if part < 0:
-            assert (t0, t1) == (0, lengths[b]), "a direct unit covers its whole context"
-            assert b not in direct
-            direct.add(b)
+            assert (t0, t1) == (0, lengths[b]) and merge == -1
+            assert (b, hg) not in direct
+            direct.add((b, hg))
         else:
-            assert part not in partial_owner
-            partial_owner[part] = (b, t0, t1)
-    for b in range(B):
-        assert np.all(covered[b] == 1), f"request {b}: tokens not covered exactly once"
+            assert part not in parts_seen and t1 > t0
+            assert t1 - t0 <= chunk
+            parts_seen[part] = (b, hg, t0, t1, merge)
+    for key, cov in covered.items():
+        assert np.all(cov == 1), f"{key}: tokens not covered exactly once"
     merged = set()
-    for b, first, count, _ in merges:
-        assert count >= 2 and b not in merged and b not in direct
-        merged.add(b)
-        parts = [partial_owner[first + c] for c in range(count)]
-        assert all(pb == b for pb, _, _ in parts)
-        assert sum(t1 - t0 for _, t0, t1 in parts) == lengths[b]
-        assert all(t1 > t0 for _, t0, t1 in parts), "split parts are non-empty"
-    assert merged | direct == set(range(B))
-    assert len(partial_owner) == sum(int(c) for _, _, c, _ in merges)
-    if len(partial_owner):
-        assert set(partial_owner) == set(range(len(partial_owner)))
-    sizes = [t1 - t0 for _, t0, t1, _ in units]
-    assert sizes == sorted(sizes, reverse=True), "units are listed longest first"
-    assert len(units) <= max(cap, B)
+    for m, (b, hg, first, count) in enumerate(merges):
+        assert count >= 2 and (b, hg) not in merged and (b, hg) not in direct
+        merged.add((b, hg))
+        ps = [parts_seen[first + c] for c in range(count)]
+        assert all(pb == b and ph == hg and pm == m for pb, ph, _, _, pm in ps)
+        assert sum(t1 - t0 for _, _, t0, t1, _ in ps) == lengths[b]
+    assert merged | direct == set(covered)
+    assert len(parts_seen) == plan["partials"] == sum(int(c) for *_, c in merges)
+    if parts_seen:
+        assert set(parts_seen) == set(range(len(parts_seen)))
+    assert n <= 8 * ctas + B * groups
+
+
+SHAPES = [(8, 128), (4, 256), (2, 128), (1, 256), (8, 256)]
 
 
 @pytest.mark.parametrize("seed", range(12))
@@ -126,42 +133,48 @@ def test_planner_covers_every_token_once(pkv, seed):
     else:
         lengths = np.full(B, int(rng.integers(1, 70000)))
     indptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
-    sms, per_sm = 152, int(rng.integers(1, 5))
-    units, merges, chunk = pkv.paged_decode_plan_host(indptr, sms, per_sm)
-    check_plan(indptr, units, merges, chunk, sms * per_sm * 4)
-    assert chunk >= 1
-    if lengths.max() > 256:
-        assert chunk >= 256 and chunk % 64 == 0
+    hkv, d = SHAPES[seed % len(SHAPES)]
+    ctas = 152 * int(rng.integers(1, 3))
+    plan = pkv.paged_decode_plan_host(indptr, hkv, d, ctas)
+    check_plan(indptr, hkv, d, ctas, plan)
+    if lengths.max() > 64:
+        assert plan["chunk"] >= 64
+        assert plan["chunk"] % 16 == 0 or plan["chunk"] == lengths.max()
 
 
 def test_planner_edge_cases(pkv):
     # empty batch
-    u, m, c = pkv.paged_decode_plan_host(np.zeros(1, np.int32), 152, 2)
-    assert len(u) == 0 and len(m) == 0
-    # all contexts empty: one (empty) direct unit per request
-    u, m, c = pkv.paged_decode_plan_host(np.zeros(5, np.int32), 152, 2)
-    assert len(u) == 4 and all(t0 == t1 == 0 and p == -1 for _, t0, t1, p in u)
-    # a single huge context is split across the whole device
-    u, m, c = pkv.paged_decode_plan_host(np.array([0, 131072], np.int32), 152, 2)
-    assert len(m) == 1 and 152 <= len(u) <= 152 * 2 * 4
-    check_plan([0, 131072], u, m, c, 152 * 8)
-    # skewed batch like the 128-request long-context workload
+    p = pkv.paged_decode_plan_host(np.zeros(1, np.int32), 8, 128, 304)
+    assert len(p["units"]) == 0 and len(p["merges"]) == 0
+    # all contexts empty: one (empty) direct unit per (request, head group)
+    p = pkv.paged_decode_plan_host(np.zeros(5, np.int32), 8, 128, 304)
+    assert len(p["units"]) == 8 and all(u[2] == u[3] == 0 and u[4] == -1 for u in p["units"])
+    check_plan(np.zeros(5, np.int32), 8, 128, 304, p)
+    # a single huge context is spread over the whole device
+    p = pkv.paged_decode_plan_host(np.array([0, 131072], np.int32), 8, 128, 304)
+    check_plan([0, 131072], 8, 128, 304, p)
+    assert len(p["merges"]) == 2 and len(p["cta_begin"]) - 1 >= 152
+    # the skewed 128-request long-context batch
     rng = np.random.default_rng(5)
     L = np.rint(np.exp(rng.uniform(np.log(128), np.log(32768), 127))).astype(np.int64)
     L = np.append(L, 131072)
     ip = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
-    u, m, c = pkv.paged_decode_plan_host(ip, 152, 2)
-    check_plan(ip, u, m, c, 152 * 8)
-    assert max(t1 - t0 for _, t0, t1, _ in u) <= c
+    p = pkv.paged_decode_plan_host(ip, 8, 128, 304)
+    check_plan(ip, 8, 128, 304, p)
+    assert len(p["cta_begin"]) - 1 == 304
+    # load balance: the busiest CTA holds at most ~20% more tokens than average
+    loads = [int((p["units"][a:b, 3] - p["units"][a:b, 2]).sum())
+             for a, b in zip(p["cta_begin"][:-1], p["cta_begin"][1:])]
+    assert max(loads) <= 1.2 * (2 * L.sum() / 304)
 
 
 def test_planner_rejects_bad_input(pkv):
     with pytest.raises(pkv.PkvError) as e:
-        pkv.paged_decode_plan_host(np.array([0, 5, 3], np.int32), 152, 2)
+        pkv.paged_decode_plan_host(np.array([0, 5, 3], np.int32), 8, 128, 304)
     assert e.value.code == pkv.PKV_ERR_INVALID_ARG
     with pytest.raises(pkv.PkvError) as e:
-        pkv.paged_decode_plan_host(np.array([1, 5], np.int32), 152, 2)
+        pkv.paged_decode_plan_host(np.array([1, 5], np.int32), 8, 128, 304)
     assert e.value.code == pkv.PKV_ERR_INVALID_ARG
     with pytest.raises(pkv.PkvError) as e:
-        pkv.paged_decode_plan_host(np.array([0, 100000], np.int32), 152, 2, max_units=3)
+        pkv.paged_decode_plan_host(np.array([0, 100000], np.int32), 8, 128, 304, max_units=1)
     assert e.value.code == pkv.PKV_ERR_PLAN
