@@ -145,9 +145,9 @@ void paged_decode_plan_destroy(pkv_plan* plan);
  * paged_decode_plan_host — the planner alone, on the host, with no CUDA call.
  * Computes the work list paged_decode_plan would upload, for inspection and tests.
  * The work of one layer is every (request, KV-head group) pair, a group being
- * min(n_kv_heads, 512 / head_dim) consecutive KV heads; contexts longer than the
- * chosen chunk are cut into near-equal token ranges, and the units are spread
- * over `ctas` persistent CTAs longest first.
+ * min(n_kv_heads, 512 / head_dim) consecutive KV heads. The pairs are laid end to
+ * end and cut into `ctas` ranges of equal token count (fewer for a small step);
+ * a context is split only where a range boundary falls inside it.
  *   kv_indptr_host : [batch + 1] int32
  *   n_kv_heads, head_dim : the attention shape
  *   ctas           : persistent CTAs (SMs x resident CTAs per SM on the device)
@@ -155,11 +155,12 @@ void paged_decode_plan_destroy(pkv_plan* plan);
  *                    first token, end token (exclusive), partial slot or -1 when
  *                    the unit writes out/lse directly, merge record or -1, 0, 0},
  *                    listed CTA by CTA
- *   cta_begin_out  : [ctas + 1] int32 — CTA c runs units [cta_begin[c], cta_begin[c+1])
+ *   cta_begin_out  : [ctas + 1] int32 — CTA c runs units [cta_begin[c], cta_begin[c+1]);
+ *                    every CTA of the grid has an entry (possibly an empty range)
  *   merges_out     : [max_merges * 4] int32 — per split (request, head group)
  *                    {request b, head group, first partial slot, number of parts}
- *   counts_out     : [5] int32 — {units, CTAs used, merge records, partial slots,
- *                    chunk tokens}
+ *   counts_out     : [5] int32 — {units, CTAs with work, merge records, partial
+ *                    slots, tokens per CTA range}
  * Returns PKV_ERR_PLAN if an output array is too small.
  */
 int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_heads,

@@ -226,7 +226,7 @@ def paged_decode_plan_host(kv_indptr_host, n_kv_heads: int, head_dim: int, ctas:
     batch = ip.size - 1
     groups = max(1, n_kv_heads // max(1, min(n_kv_heads, 512 // head_dim)))
     if max_units is None:
-        max_units = 8 * ctas + max(batch, 1) * groups
+        max_units = 2 * ctas + max(batch, 1) * groups
     if max_merges is None:
         max_merges = max(batch, 1) * groups
     units = np.zeros((max(max_units, 1), 8), np.int32)
@@ -237,5 +237,5 @@ def paged_decode_plan_host(kv_indptr_host, n_kv_heads: int, head_dim: int, ctas:
                                             _ptr(units), max_units, _ptr(cta_begin),
                                             _ptr(merges), max_merges, _ptr(counts)))
     nu, nc, nm, npart, chunk = (int(x) for x in counts)
-    return {"units": units[:nu].copy(), "cta_begin": cta_begin[:nc + 1].copy(),
+    return {"units": units[:nu].copy(), "cta_begin": cta_begin.copy(), "ctas_used": nc,
             "merges": merges[:nm].copy(), "partials": npart, "chunk": chunk}

@@ -321,7 +321,7 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
     a.cta_begin = reinterpret_cast<const int32_t*>(meta);
     a.merges = reinterpret_cast<const Merge*>(meta + p->off_merge);
     a.units = reinterpret_cast<const Unit*>(meta + p->off_units);
-    a.n_ctas = p->counts.n_ctas;
+    a.n_ctas = p->ctas;
     a.n_qo_heads = n_qo_heads;
     a.n_kv_heads = n_kv_heads;
     a.head_dim = head_dim;

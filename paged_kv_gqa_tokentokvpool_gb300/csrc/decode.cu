@@ -221,14 +221,30 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     uint32_t fill_parity = 0;
     uint32_t filled_mask = 0, parity_bits = 0;  // per stage: filled at all / parity of last fill
     bool aborted = false;
+    // The next unit's descriptor and slot-list base are loaded one unit ahead, and
+    // its slot ids are prefetched into L2 once the current unit's first tile is
+    // on its way.
+    Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
+    int64_t next_base = u_begin < u_end ? int64_t(__ldg(a.kv_indptr + next.b)) + next.tok_begin : 0;
     for (int u = u_begin; u < u_end && !aborted; ++u) {
-        const Unit un = a.units[u];
+        const Unit un = next;
+        const int32_t* idx = a.kv_indices + next_base;
+        if (u + 1 < u_end) {
+            next = a.units[u + 1];
+            next_base = int64_t(__ldg(a.kv_indptr + next.b)) + next.tok_begin;
+        }
         const int n_tok = un.tok_end - un.tok_begin;
-        const int32_t* idx = a.kv_indices + __ldg(a.kv_indptr + un.b) + un.tok_begin;
-        for (int off = lane * 32; off < n_tok; off += 32 * 32) prefetch_l2(idx + off);
         const int n_tiles = n_tok > 0 ? (n_tok + kTile - 1) / kTile : 1;
         const int64_t group_off = int64_t(un.hg) * C::kRow;
+        for (int off = 32 * (lane + 1); off < n_tok; off += 32 * 32) prefetch_l2(idx + off);
         for (int t = 0; t < n_tiles; ++t) {
+            if (t == 1 || (n_tiles == 1 && u + 1 < u_end)) {
+                if (u + 1 < u_end) {
+                    const int32_t* nidx = a.kv_indices + next_base;
+                    for (int off = 32 * lane; off < next.tok_end - next.tok_begin; off += 32 * 32)
+                        prefetch_l2(nidx + off);
+                }
+            }
             const int n = min(kTile, n_tok - t * kTile);
             const int slot = tok < n ? __ldg(idx + t * kTile + tok) : -1;
             const uint32_t full_bar = smem_u32(&sh.full[stage]);
@@ -271,51 +287,79 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
 }
 
 template <int D, int G, int WPH>
+__device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit& un, int hh, int g,
+                                                 int t4, uint32_t (&qf)[Cfg<D, G, WPH>::kKSteps][2]) {
+    using C = Cfg<D, G, WPH>;
+    const int kvh = un.hg * C::kHeadsPerCta + hh;
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(
+        static_cast<const __nv_bfloat16*>(a.q) +
+        (int64_t(un.b) * a.n_qo_heads + kvh * G + (g < G ? g : 0)) * D + 2 * t4);
+#pragma unroll
+    for (int ks = 0; ks < C::kKSteps; ++ks) {
+        qf[ks][0] = g < G ? __ldg(row + ks * 8) : 0u;
+        qf[ks][1] = g < G ? __ldg(row + ks * 8 + 4) : 0u;
+    }
+}
+
+// Log-sum-exp merge of all parts of one split (request, head group), run by the
+// CTA that finished its last part. Warp (hh, part) merges the G query heads of
+// KV head hh over its slice of head_dim; lane l handles float4 v = l + 32 i of
+// that [G x dims] block. Partial results live in L2 (just written by other SMs),
+// so the loads are independent and unrolled over parts.
+template <int D, int G, int WPH>
 __device__ void merge_parts(const DecodeArgs& a, const Unit& un, int hh, int part, int lane) {
     using C = Cfg<D, G, WPH>;
+    constexpr int kVec = G * C::kDimsPerWarp / 4;
+    constexpr int kPerLane = (kVec + 31) / 32;
     const Merge mg = a.merges[un.merge];
+    const int P = mg.count;
     const int hq = a.n_qo_heads;
     const int kvh = un.hg * C::kHeadsPerCta + hh;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    for (int e = lane * 4; e < G * C::kDimsPerWarp; e += 128) {
-        const int h = e / C::kDimsPerWarp;
-        const int d = part * C::kDimsPerWarp + (e % C::kDimsPerWarp);
-        const int qh = hh * G + h;
-        const float* lse_p = a.ws_lse + int64_t(mg.first) * C::kQHeads + qh;
+    const float* lse_base = a.ws_lse + int64_t(mg.first) * C::kQHeads + hh * G;
+    const float* o_base = a.ws_o + (int64_t(mg.first) * C::kQHeads + hh * G) * D;
+    int hsel[kPerLane], dsel[kPerLane];
+    float total[kPerLane];
+    float4 acc[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int v = lane + 32 * i;
+        const int e = 4 * (v < kVec ? v : 0);
+        hsel[i] = e / C::kDimsPerWarp;
+        dsel[i] = part * C::kDimsPerWarp + e % C::kDimsPerWarp;
+        const float* lp = lse_base + hsel[i];
         float mx = neg_inf();
-        for (int c = 0; c < mg.count; ++c) mx = fmaxf(mx, __ldcg(lse_p + int64_t(c) * C::kQHeads));
+#pragma unroll 8
+        for (int c = 0; c < P; ++c) mx = fmaxf(mx, __ldcg(lp + int64_t(c) * C::kQHeads));
         float sum = 0.f;
-        for (int c = 0; c < mg.count; ++c) sum += ex2(__ldcg(lse_p + int64_t(c) * C::kQHeads) - mx);
-        const float total = mx + __log2f(sum);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* o_p = a.ws_o + (int64_t(mg.first) * C::kQHeads + qh) * D + d;
-        int c = 0;
-        for (; c + 2 <= mg.count; c += 2) {
-            const float w0 = ex2(__ldcg(lse_p + int64_t(c) * C::kQHeads) - total);
-            const float w1 = ex2(__ldcg(lse_p + int64_t(c + 1) * C::kQHeads) - total);
-            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(o_p + int64_t(c) * C::kQHeads * D));
-            const float4 x1 =
-                __ldcg(reinterpret_cast<const float4*>(o_p + int64_t(c + 1) * C::kQHeads * D));
-            acc.x = fmaf(w0, x0.x, fmaf(w1, x1.x, acc.x));
-            acc.y = fmaf(w0, x0.y, fmaf(w1, x1.y, acc.y));
-            acc.z = fmaf(w0, x0.z, fmaf(w1, x1.z, acc.z));
-            acc.w = fmaf(w0, x0.w, fmaf(w1, x1.w, acc.w));
+#pragma unroll 8
+        for (int c = 0; c < P; ++c) sum += ex2(__ldcg(lp + int64_t(c) * C::kQHeads) - mx);
+        total[i] = mx + __log2f(sum);
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 4
+    for (int c = 0; c < P; ++c) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int64_t row = int64_t(c) * C::kQHeads + hsel[i];
+            const float w = ex2(__ldcg(lse_base + row) - total[i]);
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(o_base + row * D + dsel[i]));
+            acc[i].x = fmaf(w, x.x, acc[i].x);
+            acc[i].y = fmaf(w, x.y, acc[i].y);
+            acc[i].z = fmaf(w, x.z, acc[i].z);
+            acc[i].w = fmaf(w, x.w, acc[i].w);
         }
-        for (; c < mg.count; ++c) {
-            const float w0 = ex2(__ldcg(lse_p + int64_t(c) * C::kQHeads) - total);
-            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(o_p + int64_t(c) * C::kQHeads * D));
-            acc.x = fmaf(w0, x0.x, acc.x);
-            acc.y = fmaf(w0, x0.y, acc.y);
-            acc.z = fmaf(w0, x0.z, acc.z);
-            acc.w = fmaf(w0, x0.w, acc.w);
-        }
-        const int64_t orow = (int64_t(un.b) * hq + kvh * G + h) * D + d;
+    }
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        if (lane + 32 * i >= kVec) continue;
+        const int64_t orow = (int64_t(un.b) * hq + kvh * G + hsel[i]) * D + dsel[i];
         uint2 packed;
-        packed.x = pack_bf16x2(acc.x, acc.y);
-        packed.y = pack_bf16x2(acc.z, acc.w);
+        packed.x = pack_bf16x2(acc[i].x, acc[i].y);
+        packed.y = pack_bf16x2(acc[i].z, acc[i].w);
         *reinterpret_cast<uint2*>(out + orow) = packed;
-        if (a.lse != nullptr && part == 0 && (e % C::kDimsPerWarp) == 0)
-            a.lse[int64_t(un.b) * hq + kvh * G + h] = total * kLn2;
+        if (a.lse != nullptr && dsel[i] == 0)
+            a.lse[int64_t(un.b) * hq + kvh * G + hsel[i]] = total[i] * kLn2;
     }
 }
 
@@ -337,21 +381,25 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     const uint32_t v_lane = smem_u32(smem) + kTile * C::kRowP +
                             ((lane & 7) + (lane >> 4) * 8) * C::kRowP +
                             (hh * D + part * C::kDimsPerWarp + ((lane >> 3) & 1) * 8) * 2;
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
     int stage = 0;
     uint32_t full_parity = 0, cons_parity = 0;
 
+    // Q^T as the B operand: lane holds head g, dims 2*t4.. of each k-step. The
+    // next unit's fragments are loaded while the current unit streams.
+    uint32_t qb[C::kKSteps][2], qn[C::kKSteps][2];
+    Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
+    if (u_begin < u_end) load_q_fragments<D, G, WPH>(a, next, hh, g, t4, qn);
     for (int u = u_begin; u < u_end; ++u) {
-        const Unit un = a.units[u];
+        const Unit un = next;
         const int kvh = un.hg * C::kHeadsPerCta + hh;
-        // Q^T as the B operand: lane holds head g, dims 2*t4.. of each k-step
-        uint32_t qb[C::kKSteps][2];
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            q + (int64_t(un.b) * hq + kvh * G + (g < G ? g : 0)) * D + 2 * t4);
 #pragma unroll
         for (int ks = 0; ks < C::kKSteps; ++ks) {
-            qb[ks][0] = g < G ? __ldg(qrow + ks * 8) : 0u;
-            qb[ks][1] = g < G ? __ldg(qrow + ks * 8 + 4) : 0u;
+            qb[ks][0] = qn[ks][0];
+            qb[ks][1] = qn[ks][1];
+        }
+        if (u + 1 < u_end) {
+            next = a.units[u + 1];
+            load_q_fragments<D, G, WPH>(a, next, hh, g, t4, qn);
         }
         float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
         float o[C::kMBlocks][4];

@@ -40,13 +40,8 @@ struct Merge {
 };
 static_assert(sizeof(Unit) == 32 && sizeof(Merge) == 16, "plan record sizes");
 
-// Contexts up to this many tokens are never split.
+// No CTA's token range is planned shorter than this (small steps use fewer CTAs).
 constexpr int kMinChunkTokens = 64;
-// Chunk lengths are multiples of this many tokens (one pipeline tile).
-constexpr int kChunkQuantum = 16;
-// The planner keeps the unit count within this many units per CTA (plus one
-// unit per (request, head group)), which bounds the plan's buffers.
-constexpr int kMaxUnitsPerCta = 8;
 
 struct PlanLimits {
     int max_units;
@@ -57,7 +52,8 @@ struct PlanCounts {
 };
 
 int plan_max_units(int ctas, int max_batch, int n_groups);
-// Pure host planner. units[max_units], cta_begin[ctas + 1], merges[max_merges].
+// Pure host planner. units[max_units], cta_begin[ctas + 1] (every CTA of the grid
+// gets an entry; unused ones an empty range), merges[max_merges].
 // Returns PKV_OK, PKV_ERR_PLAN (capacity) or PKV_ERR_INVALID_ARG (bad indptr).
 int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, const PlanLimits& lim,
                  Unit* units, int* cta_begin, Merge* merges, PlanCounts* out);
@@ -72,7 +68,7 @@ struct DecodeArgs {
     const Unit* units;
     const int32_t* cta_begin;
     const Merge* merges;
-    int n_ctas;
+    int n_ctas;           // grid size: every CTA of the plan (some may have no units)
     int n_qo_heads;
     int n_kv_heads;
     int head_dim;

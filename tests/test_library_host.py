@@ -85,8 +85,9 @@ def check_plan(indptr, n_kv_heads, head_dim, ctas, plan):
     units, cta_begin, merges, chunk = plan["units"], plan["cta_begin"], plan["merges"], plan["chunk"]
     n = len(units)
     assert cta_begin[0] == 0 and cta_begin[-1] == n
-    assert np.all(np.diff(cta_begin) > 0), "every launched CTA has work"
-    assert len(cta_begin) - 1 <= ctas
+    assert np.all(np.diff(cta_begin) >= 0)
+    assert len(cta_begin) - 1 == ctas, "every CTA of the grid has an entry"
+    assert plan["ctas_used"] <= ctas
     covered = {(b, g): np.zeros(lengths[b], np.int32) for b in range(B) for g in range(groups)}
     direct, parts_seen = set(), {}
     for b, hg, t0, t1, part, merge, _, _ in units:
@@ -98,7 +99,7 @@ def check_plan(indptr, n_kv_heads, head_dim, ctas, plan):
             direct.add((b, hg))
         else:
             assert part not in parts_seen and t1 > t0
-            assert t1 - t0 <= chunk
+            assert t1 - t0 <= chunk + 32
             parts_seen[part] = (b, hg, t0, t1, merge)
     for key, cov in covered.items():
         assert np.all(cov == 1), f"{key}: tokens not covered exactly once"
@@ -113,7 +114,11 @@ def check_plan(indptr, n_kv_heads, head_dim, ctas, plan):
     assert len(parts_seen) == plan["partials"] == sum(int(c) for *_, c in merges)
     if parts_seen:
         assert set(parts_seen) == set(range(len(parts_seen)))
-    assert n <= 8 * ctas + B * groups
+    assert n <= 2 * ctas + B * groups
+    # each CTA streams about the same number of tokens (ranges snap by <= 32 tokens)
+    loads = [int((units[a:b, 3] - units[a:b, 2]).sum()) for a, b in zip(cta_begin[:-1], cta_begin[1:])]
+    if lengths.sum() >= 64 * ctas:
+        assert max(loads) <= chunk * 1.25 + 1
 
 
 SHAPES = [(8, 128), (4, 256), (2, 128), (1, 256), (8, 256)]
@@ -137,9 +142,8 @@ def test_planner_covers_every_token_once(pkv, seed):
     ctas = 152 * int(rng.integers(1, 3))
     plan = pkv.paged_decode_plan_host(indptr, hkv, d, ctas)
     check_plan(indptr, hkv, d, ctas, plan)
-    if lengths.max() > 64:
+    if lengths.sum() * (hkv // min(hkv, 512 // d)) >= 64:
         assert plan["chunk"] >= 64
-        assert plan["chunk"] % 16 == 0 or plan["chunk"] == lengths.max()
 
 
 def test_planner_edge_cases(pkv):
@@ -153,7 +157,11 @@ def test_planner_edge_cases(pkv):
     # a single huge context is spread over the whole device
     p = pkv.paged_decode_plan_host(np.array([0, 131072], np.int32), 8, 128, 304)
     check_plan([0, 131072], 8, 128, 304, p)
-    assert len(p["merges"]) == 2 and len(p["cta_begin"]) - 1 >= 152
+    assert len(p["merges"]) == 2 and p["ctas_used"] == 304
+    # a tiny step uses few CTAs, none with less than 64 tokens
+    p = pkv.paged_decode_plan_host(np.array([0, 100, 130], np.int32), 8, 128, 304)
+    check_plan([0, 100, 130], 8, 128, 304, p)
+    assert p["ctas_used"] == 260 // 64
     # the skewed 128-request long-context batch
     rng = np.random.default_rng(5)
     L = np.rint(np.exp(rng.uniform(np.log(128), np.log(32768), 127))).astype(np.int64)
@@ -161,11 +169,9 @@ def test_planner_edge_cases(pkv):
     ip = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
     p = pkv.paged_decode_plan_host(ip, 8, 128, 304)
     check_plan(ip, 8, 128, 304, p)
-    assert len(p["cta_begin"]) - 1 == 304
-    # load balance: the busiest CTA holds at most ~20% more tokens than average
-    loads = [int((p["units"][a:b, 3] - p["units"][a:b, 2]).sum())
-             for a, b in zip(p["cta_begin"][:-1], p["cta_begin"][1:])]
-    assert max(loads) <= 1.2 * (2 * L.sum() / 304)
+    assert p["ctas_used"] == 304
+    # a split context has few parts (range boundaries only)
+    assert max(m[3] for m in p["merges"]) <= 2 * 131072 // (2 * L.sum() // 304) + 2
 
 
 def test_planner_rejects_bad_input(pkv):
