@@ -145,16 +145,18 @@ void paged_decode_plan_destroy(pkv_plan* plan);
  * paged_decode_plan_host — the planner alone, on the host, with no CUDA call.
  * Computes the work list paged_decode_plan would upload, for inspection and tests.
  * The work of one layer is every (request, KV-head group) pair, a group being
- * min(n_kv_heads, 512 / head_dim) consecutive KV heads. The pairs are laid end to
- * end and cut into `ctas` ranges of equal token count (fewer for a small step);
- * a context is split only where a range boundary falls inside it.
+ * heads_per_cta consecutive KV heads. The pairs are laid end to end and cut into
+ * `ctas` ranges of equal token count (fewer for a small step); a context is split
+ * only where a range boundary falls inside it.
  *   kv_indptr_host : [batch + 1] int32
  *   n_kv_heads, head_dim : the attention shape
+ *   heads_per_cta  : KV heads per group: 1, 2 or 4, at most 512 / head_dim and
+ *                    dividing n_kv_heads; 0 = the largest allowed
  *   ctas           : persistent CTAs (SMs x resident CTAs per SM on the device)
  *   units_out      : [max_units * 8] int32 — per unit {request b, head group,
  *                    first token, end token (exclusive), partial slot or -1 when
- *                    the unit writes out/lse directly, merge record or -1, 0, 0},
- *                    listed CTA by CTA
+ *                    the unit writes out/lse directly, merge record or -1,
+ *                    kv_indptr[b] + first token, 0}, listed CTA by CTA
  *   cta_begin_out  : [ctas + 1] int32 — CTA c runs units [cta_begin[c], cta_begin[c+1]);
  *                    every CTA of the grid has an entry (possibly an empty range)
  *   merges_out     : [max_merges * 4] int32 — per split (request, head group)
@@ -164,7 +166,8 @@ void paged_decode_plan_destroy(pkv_plan* plan);
  * Returns PKV_ERR_PLAN if an output array is too small.
  */
 int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_heads,
-                           int head_dim, int ctas, int32_t* units_out, int max_units,
+                           int head_dim, int heads_per_cta, int ctas, int32_t* units_out,
+                           int max_units,
                            int32_t* cta_begin_out, int32_t* merges_out, int max_merges,
                            int32_t* counts_out);
 

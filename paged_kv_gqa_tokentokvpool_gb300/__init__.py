@@ -62,7 +62,7 @@ def _load() -> ctypes.CDLL:
                                       P, P]
     lib.paged_decode_plan_destroy.argtypes = [P]
     lib.paged_decode_plan_destroy.restype = None
-    lib.paged_decode_plan_host.argtypes = [P, I32, I32, I32, I32, P, I32, P, P, I32, P]
+    lib.paged_decode_plan_host.argtypes = [P, I32, I32, I32, I32, I32, P, I32, P, P, I32, P]
     lib.paged_decode_plan_info.argtypes = [P, P, P, P, P, P]
     lib.paged_decode_plan_status.argtypes = [P, P]
     lib.pkv_set_debug_checks.argtypes = [I32]
@@ -218,13 +218,14 @@ def paged_decode_plan_destroy(plan: Plan) -> None:
 
 
 def paged_decode_plan_host(kv_indptr_host, n_kv_heads: int, head_dim: int, ctas: int,
-                           max_units: int = None, max_merges: int = None):
+                           heads_per_cta: int = 0, max_units: int = None, max_merges: int = None):
     """The planner alone (host, no CUDA).
 
     Returns dict(units [n, 8], cta_begin [c + 1], merges [m, 4], partials, chunk)."""
     ip = _host_indptr(kv_indptr_host)
     batch = ip.size - 1
-    groups = max(1, n_kv_heads // max(1, min(n_kv_heads, 512 // head_dim)))
+    hpc = heads_per_cta or min(n_kv_heads, 512 // head_dim)
+    groups = max(1, n_kv_heads // max(1, hpc))
     if max_units is None:
         max_units = 2 * ctas + max(batch, 1) * groups
     if max_merges is None:
@@ -233,7 +234,8 @@ def paged_decode_plan_host(kv_indptr_host, n_kv_heads: int, head_dim: int, ctas:
     cta_begin = np.zeros(ctas + 1, np.int32)
     merges = np.zeros((max(max_merges, 1), 4), np.int32)
     counts = np.zeros(5, np.int32)
-    _check(library().paged_decode_plan_host(_ptr(ip), batch, n_kv_heads, head_dim, ctas,
+    _check(library().paged_decode_plan_host(_ptr(ip), batch, n_kv_heads, head_dim,
+                                            heads_per_cta, ctas,
                                             _ptr(units), max_units, _ptr(cta_begin),
                                             _ptr(merges), max_merges, _ptr(counts)))
     nu, nc, nm, npart, chunk = (int(x) for x in counts)

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -95,7 +96,8 @@ int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const voi
 }
 
 int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_heads,
-                           int head_dim, int ctas, int32_t* units_out, int max_units,
+                           int head_dim, int heads_per_cta, int ctas, int32_t* units_out,
+                           int max_units,
                            int32_t* cta_begin_out, int32_t* merges_out, int max_merges,
                            int32_t* counts_out) {
     clear_error();
@@ -104,10 +106,11 @@ int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_he
         return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: NULL output");
     if (ctas <= 0 || n_kv_heads <= 0 || head_dim <= 0)
         return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: ctas, n_kv_heads, head_dim must be > 0");
-    const int hpg = heads_per_group(n_kv_heads, head_dim);
-    if (hpg < 1 || n_kv_heads % hpg != 0)
-        return fail(PKV_ERR_UNSUPPORTED, "paged_decode_plan_host: %d KV heads do not form groups",
-                    n_kv_heads);
+    const int hpg = heads_per_cta > 0 ? heads_per_cta : heads_per_group(n_kv_heads, head_dim);
+    if (hpg < 1 || hpg > heads_per_group(n_kv_heads, head_dim) || n_kv_heads % hpg != 0)
+        return fail(PKV_ERR_UNSUPPORTED,
+                    "paged_decode_plan_host: %d KV heads per group do not fit %d heads of dim %d",
+                    hpg, n_kv_heads, head_dim);
     PlanCounts c{};
     int rc = plan_compute(kv_indptr_host, batch, n_kv_heads / hpg, ctas,
                           PlanLimits{max_units, max_merges}, reinterpret_cast<Unit*>(units_out),
@@ -166,12 +169,20 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
         delete p;
         return cuda_fail(e, "paged_decode_plan_create: device query");
     }
-    p->ctas_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim);
+    // KV heads per CTA group: the largest the shape allows, unless the
+    // PKV_HEADS_PER_CTA environment variable (1, 2 or 4) asks for fewer.
+    int hpg = heads_per_group(n_kv_heads, head_dim);
+    if (const char* env = std::getenv("PKV_HEADS_PER_CTA")) {
+        const int want = std::atoi(env);
+        if ((want == 1 || want == 2 || want == 4) && want <= hpg && n_kv_heads % want == 0)
+            hpg = want;
+    }
+    p->heads_per_cta = hpg;
+    p->ctas_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg);
     if (p->ctas_per_sm <= 0) {
         delete p;
         return fail(PKV_ERR_CUDA, "paged_decode_plan_create: occupancy query failed");
     }
-    const int hpg = heads_per_group(n_kv_heads, head_dim);
     p->ctas = p->num_sms * p->ctas_per_sm;
     p->max_batch = max_batch;
     p->max_tokens = max_tokens;
@@ -322,6 +333,7 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
     a.merges = reinterpret_cast<const Merge*>(meta + p->off_merge);
     a.units = reinterpret_cast<const Unit*>(meta + p->off_units);
     a.n_ctas = p->ctas;
+    a.heads_per_cta = p->heads_per_cta;
     a.n_qo_heads = n_qo_heads;
     a.n_kv_heads = n_kv_heads;
     a.head_dim = head_dim;

@@ -182,12 +182,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // kernel
 // ---------------------------------------------------------------------------
 
+// Shapes of one instance: head_dim D, GQA group G, WPH consumer warps per KV
+// head (so 4 / WPH KV heads per CTA). A pipeline stage holds kSub 16-token
+// sub-tiles of K rows and of V rows of the CTA's kHeadsPerCta heads; kSub is
+// chosen so that every stage carries 16 x kHeadGroupElems bf16 of K and as much
+// of V (32 KB, plus row padding) whatever the head count.
 template <int D, int G, int WPH>
 struct Cfg {
     static constexpr int kHeadsPerCta = kConsumerWarps / WPH;   // KV heads of one group
     static constexpr int kRow = kHeadsPerCta * D * 2;           // bytes of a staged row
     static constexpr int kRowP = kRow + kRowPad;
-    static constexpr int kStage = 2 * kTile * kRowP;            // K rows then V rows
+    static constexpr int kSub = kHeadGroupElems / (kHeadsPerCta * D);  // sub-tiles per stage
+    static constexpr int kStageTokens = kTile * kSub;
+    static constexpr int kStage = 2 * kStageTokens * kRowP;     // K rows then V rows
+    static constexpr uint32_t kStageTx = 2u * kStageTokens * kRow;
     static constexpr int kKSteps = D / 16;                      // k-steps of S^T
     static constexpr int kMBlocks = D / 16 / WPH;               // O^T dim blocks per warp
     static constexpr int kDimsPerWarp = D / WPH;
@@ -195,7 +203,7 @@ struct Cfg {
     static constexpr int kBarOffset = kStages * kStage;
     static constexpr int kSmem = kBarOffset + (2 * kStages + 1) * 8 + 16;
     static_assert(G >= 1 && G <= 8, "group size");
-    static_assert(kHeadsPerCta * D <= kHeadGroupElems, "head group too wide");
+    static_assert(kHeadsPerCta * D * kSub == kHeadGroupElems, "stage budget");
     static_assert(kMBlocks >= 1, "dims per warp");
 };
 
@@ -206,6 +214,8 @@ struct Shared {
     volatile int* flags;  // [0] abort, [1] this CTA merges the current unit
 };
 
+// Producer warp: lane l copies, for every sub-tile j of a stage, token
+// (l % 16) + 16 j's K row (l < 16) or V row (l >= 16) of the CTA's head group.
 template <int D, int G, int WPH>
 __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
@@ -215,38 +225,34 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     const bool is_v = lane >= kTile;
     const char* pool = static_cast<const char*>(is_v ? a.v_pool : a.k_pool);
     const int64_t slot_bytes = int64_t(a.n_kv_heads) * D * 2;
-    const uint32_t ring = smem_u32(smem) + (is_v ? kTile * C::kRowP : 0) + tok * C::kRowP;
+    const uint32_t ring = smem_u32(smem) + (is_v ? C::kStageTokens * C::kRowP : 0) + tok * C::kRowP;
     int stage = 0;
     uint32_t empty_parity = 1;  // a fresh barrier reports the phase before it as complete
     uint32_t fill_parity = 0;
     uint32_t filled_mask = 0, parity_bits = 0;  // per stage: filled at all / parity of last fill
     bool aborted = false;
-    // The next unit's descriptor and slot-list base are loaded one unit ahead, and
-    // its slot ids are prefetched into L2 once the current unit's first tile is
-    // on its way.
+    // The next unit's descriptor is loaded one unit ahead, and its slot ids are
+    // prefetched into L2 once the current unit's first stage is on its way.
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
-    int64_t next_base = u_begin < u_end ? int64_t(__ldg(a.kv_indptr + next.b)) + next.tok_begin : 0;
     for (int u = u_begin; u < u_end && !aborted; ++u) {
         const Unit un = next;
-        const int32_t* idx = a.kv_indices + next_base;
-        if (u + 1 < u_end) {
-            next = a.units[u + 1];
-            next_base = int64_t(__ldg(a.kv_indptr + next.b)) + next.tok_begin;
-        }
+        if (u + 1 < u_end) next = a.units[u + 1];
+        const int32_t* idx = a.kv_indices + un.idx_begin;
         const int n_tok = un.tok_end - un.tok_begin;
-        const int n_tiles = n_tok > 0 ? (n_tok + kTile - 1) / kTile : 1;
+        const int n_stages = n_tok > 0 ? (n_tok + C::kStageTokens - 1) / C::kStageTokens : 1;
         const int64_t group_off = int64_t(un.hg) * C::kRow;
         for (int off = 32 * (lane + 1); off < n_tok; off += 32 * 32) prefetch_l2(idx + off);
-        for (int t = 0; t < n_tiles; ++t) {
-            if (t == 1 || (n_tiles == 1 && u + 1 < u_end)) {
-                if (u + 1 < u_end) {
-                    const int32_t* nidx = a.kv_indices + next_base;
-                    for (int off = 32 * lane; off < next.tok_end - next.tok_begin; off += 32 * 32)
-                        prefetch_l2(nidx + off);
-                }
+        for (int t = 0; t < n_stages; ++t) {
+            if (t == (n_stages > 1 ? 1 : 0) && u + 1 < u_end) {
+                const int32_t* nidx = a.kv_indices + next.idx_begin;
+                for (int off = 32 * lane; off < next.tok_end - next.tok_begin; off += 32 * 32)
+                    prefetch_l2(nidx + off);
             }
-            const int n = min(kTile, n_tok - t * kTile);
-            const int slot = tok < n ? __ldg(idx + t * kTile + tok) : -1;
+            const int n = min(C::kStageTokens, n_tok - t * C::kStageTokens);
+            int slot[C::kSub];
+#pragma unroll
+            for (int j = 0; j < C::kSub; ++j)
+                slot[j] = tok + kTile * j < n ? __ldg(idx + t * C::kStageTokens + tok + kTile * j) : -1;
             const uint32_t full_bar = smem_u32(&sh.full[stage]);
             if (lane == 0 && !mbar_wait(smem_u32(&sh.empty[stage]), empty_parity, a.status, sh.flags))
                 sh.flags[0] = 1;
@@ -255,12 +261,16 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                 aborted = true;
                 break;
             }
-            if (lane == 0) mbar_arrive_expect_tx(full_bar, n > 0 ? 2u * kTile * C::kRow : 0u);
+            if (lane == 0) mbar_arrive_expect_tx(full_bar, n > 0 ? C::kStageTx : 0u);
             __syncwarp();
             if (n > 0) {
-                const void* src = slot >= 0 ? static_cast<const void*>(pool + slot * slot_bytes + group_off)
-                                            : a.zero_row;
-                bulk_g2s(ring + stage * C::kStage, src, C::kRow, full_bar);
+#pragma unroll
+                for (int j = 0; j < C::kSub; ++j) {
+                    const void* src = slot[j] >= 0
+                                          ? static_cast<const void*>(pool + slot[j] * slot_bytes + group_off)
+                                          : a.zero_row;
+                    bulk_g2s(ring + stage * C::kStage + j * kTile * C::kRowP, src, C::kRow, full_bar);
+                }
             }
             filled_mask |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (fill_parity << stage);
@@ -303,9 +313,11 @@ __device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit
 
 // Log-sum-exp merge of all parts of one split (request, head group), run by the
 // CTA that finished its last part. Warp (hh, part) merges the G query heads of
-// KV head hh over its slice of head_dim; lane l handles float4 v = l + 32 i of
-// that [G x dims] block. Partial results live in L2 (just written by other SMs),
-// so the loads are independent and unrolled over parts.
+// KV head hh over its slice of head_dim. First the merged lse of each head:
+// lanes take parts c = lane, lane + 32, ... with an online max/sum, then a warp
+// reduction. Then lane l accumulates float4 v = l + 32 i of the [G x dims] block
+// over all parts. Partial results sit in L2 (just written by other SMs); every
+// load is independent, so they are batched by unrolling.
 template <int D, int G, int WPH>
 __device__ void merge_parts(const DecodeArgs& a, const Unit& un, int hh, int part, int lane) {
     using C = Cfg<D, G, WPH>;
@@ -317,8 +329,42 @@ __device__ void merge_parts(const DecodeArgs& a, const Unit& un, int hh, int par
     const int kvh = un.hg * C::kHeadsPerCta + hh;
     const float* lse_base = a.ws_lse + int64_t(mg.first) * C::kQHeads + hh * G;
     const float* o_base = a.ws_o + (int64_t(mg.first) * C::kQHeads + hh * G) * D;
+
+    float total[G];
+    {
+        float m[G], s[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            m[h] = neg_inf();
+            s[h] = 0.f;
+        }
+        for (int c = lane; c < P; c += 32) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float x = __ldcg(lse_base + int64_t(c) * C::kQHeads + h);
+                const float mn = fmaxf(m[h], x);
+                s[h] = (m[h] == neg_inf() ? 0.f : s[h] * ex2(m[h] - mn)) + ex2(x - mn);
+                m[h] = mn;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float mo = __shfl_xor_sync(kFull, m[h], off);
+                const float so = __shfl_xor_sync(kFull, s[h], off);
+                const float mn = fmaxf(m[h], mo);
+                const float a0 = m[h] == neg_inf() ? 0.f : s[h] * ex2(m[h] - mn);
+                const float a1 = mo == neg_inf() ? 0.f : so * ex2(mo - mn);
+                s[h] = a0 + a1;
+                m[h] = mn;
+            }
+            total[h] = m[h] + __log2f(s[h]);
+        }
+    }
+
     int hsel[kPerLane], dsel[kPerLane];
-    float total[kPerLane];
+    float tsel[kPerLane];
     float4 acc[kPerLane];
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
@@ -326,14 +372,10 @@ __device__ void merge_parts(const DecodeArgs& a, const Unit& un, int hh, int par
         const int e = 4 * (v < kVec ? v : 0);
         hsel[i] = e / C::kDimsPerWarp;
         dsel[i] = part * C::kDimsPerWarp + e % C::kDimsPerWarp;
-        const float* lp = lse_base + hsel[i];
-        float mx = neg_inf();
-#pragma unroll 8
-        for (int c = 0; c < P; ++c) mx = fmaxf(mx, __ldcg(lp + int64_t(c) * C::kQHeads));
-        float sum = 0.f;
-#pragma unroll 8
-        for (int c = 0; c < P; ++c) sum += ex2(__ldcg(lp + int64_t(c) * C::kQHeads) - mx);
-        total[i] = mx + __log2f(sum);
+        tsel[i] = total[0];
+#pragma unroll
+        for (int h = 1; h < G; ++h)
+            if (hsel[i] == h) tsel[i] = total[h];
         acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll 4
@@ -341,7 +383,7 @@ __device__ void merge_parts(const DecodeArgs& a, const Unit& un, int hh, int par
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i) {
             const int64_t row = int64_t(c) * C::kQHeads + hsel[i];
-            const float w = ex2(__ldcg(lse_base + row) - total[i]);
+            const float w = ex2(__ldcg(lse_base + row) - tsel[i]);
             const float4 x = __ldcg(reinterpret_cast<const float4*>(o_base + row * D + dsel[i]));
             acc[i].x = fmaf(w, x.x, acc[i].x);
             acc[i].y = fmaf(w, x.y, acc[i].y);
@@ -359,7 +401,7 @@ __device__ void merge_parts(const DecodeArgs& a, const Unit& un, int hh, int par
         packed.y = pack_bf16x2(acc[i].z, acc[i].w);
         *reinterpret_cast<uint2*>(out + orow) = packed;
         if (a.lse != nullptr && dsel[i] == 0)
-            a.lse[int64_t(un.b) * hq + kvh * G + hsel[i]] = total[i] * kLn2;
+            a.lse[int64_t(un.b) * hq + kvh * G + hsel[i]] = tsel[i] * kLn2;
     }
 }
 
@@ -378,7 +420,7 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     const uint32_t k_lane = smem_u32(smem) + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowP +
                             (hh * D + (lane >> 4) * 8) * 2;
     // V tile, transposed on load, as the A operand (rows = dims, k = tokens)
-    const uint32_t v_lane = smem_u32(smem) + kTile * C::kRowP +
+    const uint32_t v_lane = smem_u32(smem) + C::kStageTokens * C::kRowP +
                             ((lane & 7) + (lane >> 4) * 8) * C::kRowP +
                             (hh * D + part * C::kDimsPerWarp + ((lane >> 3) & 1) * 8) * 2;
     int stage = 0;
@@ -407,13 +449,16 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
         for (int mb = 0; mb < C::kMBlocks; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
 
         const int n_tok = un.tok_end - un.tok_begin;
-        const int n_tiles = n_tok > 0 ? (n_tok + kTile - 1) / kTile : 1;
-        for (int t = 0; t < n_tiles; ++t) {
+        const int n_stages = n_tok > 0 ? (n_tok + C::kStageTokens - 1) / C::kStageTokens : 1;
+        for (int t = 0; t < n_stages; ++t) {
             const bool ok = mbar_wait(smem_u32(&sh.full[stage]), full_parity, a.status, sh.flags);
             if (!__all_sync(kFull, ok)) return;  // uniform exit: no lane is left in a shuffle
-            const int n = n_tok - t * kTile < kTile ? n_tok - t * kTile : kTile;
-            if (n > 0) {
-                const uint32_t st = stage * C::kStage;
+            const int n_stage = n_tok - t * C::kStageTokens;
+#pragma unroll
+            for (int j = 0; j < C::kSub; ++j) {
+                const int n = n_stage - j * kTile;  // valid rows of this sub-tile (if > 0)
+                if (n <= 0) break;
+                const uint32_t st = stage * C::kStage + j * kTile * C::kRowP;
                 float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < C::kKSteps; ++ks) {
@@ -449,7 +494,7 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                         o[mb][3] *= al1;
                     }
                 }
-                // P^T operand: tokens 0-7 and 8-15 of the tile, heads in columns
+                // P^T operand: tokens 0-7 and 8-15 of the sub-tile, heads in columns
                 const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
                 const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
 #pragma unroll
@@ -635,9 +680,7 @@ struct LaunchFn {
     static cudaError_t unsupported() { return cudaErrorInvalidValue; }
 };
 
-int warps_per_head(int n_kv_heads, int head_dim) {
-    return kConsumerWarps / heads_per_group(n_kv_heads, head_dim);
-}
+int warps_per_head(int heads_per_cta) { return kConsumerWarps / heads_per_cta; }
 
 }  // namespace
 
@@ -649,16 +692,17 @@ bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim) {
     return n_kv_heads == 1 || n_kv_heads == 2 || n_kv_heads == 4 || n_kv_heads == 8;
 }
 
-int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim) {
+int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta) {
     if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim)) return 0;
-    return dispatch<OccupancyFn>(head_dim, n_qo_heads / n_kv_heads,
-                                 warps_per_head(n_kv_heads, head_dim));
+    if (heads_per_cta < 1 || heads_per_cta > heads_per_group(n_kv_heads, head_dim) ||
+        n_kv_heads % heads_per_cta != 0)
+        return 0;
+    return dispatch<OccupancyFn>(head_dim, n_qo_heads / n_kv_heads, warps_per_head(heads_per_cta));
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-    const cudaError_t e = dispatch<LaunchFn>(a.head_dim, a.n_qo_heads / a.n_kv_heads,
-                                             warps_per_head(a.n_kv_heads, a.head_dim), a, stream);
-    return e;
+    return dispatch<LaunchFn>(a.head_dim, a.n_qo_heads / a.n_kv_heads,
+                              warps_per_head(a.heads_per_cta), a, stream);
 }
 
 }  // namespace pkv

@@ -16,9 +16,11 @@ void clear_error();
 bool debug_checks();
 
 // ---- shapes ----------------------------------------------------------------
-// A CTA of the decode kernel serves one KV-head group: the first
-// kHeadGroupElems / head_dim KV heads (or all of them, if fewer). One token's K
-// (or V) row of a group is then at most kHeadGroupElems bf16 = 1 KB, one bulk copy.
+// A CTA of the decode kernel serves one KV-head group of 1, 2 or 4 consecutive
+// KV heads, at most kHeadGroupElems / head_dim of them, so that one token's K (or
+// V) row of a group is at most kHeadGroupElems bf16 = 1 KB, one bulk copy.
+// heads_per_group() is the largest group the shape allows; a plan may use fewer
+// heads per group (smaller partial results when contexts are split).
 constexpr int kHeadGroupElems = 512;
 inline int heads_per_group(int n_kv_heads, int head_dim) {
     const int cap = kHeadGroupElems / head_dim;
@@ -27,11 +29,12 @@ inline int heads_per_group(int n_kv_heads, int head_dim) {
 
 // ---- plan ----------------------------------------------------------------
 // One work unit of the decode kernel: tokens [tok_begin, tok_end) of request b's
-// slot list, KV-head group hg. partial < 0: the unit covers the whole context and
-// writes out/lse; otherwise it writes partial slot `partial` of the workspace and
-// takes part in merge record `merge`.
+// slot list, KV-head group hg; idx_begin = kv_indptr[b] + tok_begin is where the
+// unit's slot ids start in kv_indices. partial < 0: the unit covers the whole
+// context and writes out/lse; otherwise it writes partial slot `partial` of the
+// workspace and takes part in merge record `merge`.
 struct Unit {
-    int32_t b, hg, tok_begin, tok_end, partial, merge, pad0, pad1;
+    int32_t b, hg, tok_begin, tok_end, partial, merge, idx_begin, pad;
 };
 // One split (request, head group): its parts occupy partial slots
 // [first, first + count).
@@ -69,6 +72,7 @@ struct DecodeArgs {
     const int32_t* cta_begin;
     const Merge* merges;
     int n_ctas;           // grid size: every CTA of the plan (some may have no units)
+    int heads_per_cta;    // KV heads of one group
     int n_qo_heads;
     int n_kv_heads;
     int head_dim;
@@ -84,7 +88,7 @@ struct DecodeArgs {
 
 bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim);
 // Resident CTAs per SM of the decode kernel for this shape (0 on error).
-int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim);
+int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_append(void* k_pool, void* v_pool, const int32_t* slot_ids,
@@ -98,7 +102,7 @@ struct pkv_plan {
     int num_sms = 0, ctas_per_sm = 0, ctas = 0;
     int max_batch = 0;
     int64_t max_tokens = 0;
-    int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0, n_groups = 0;
+    int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0, n_groups = 0, heads_per_cta = 0;
     pkv::PlanLimits lim{};
     size_t meta_bytes = 0;
     void* host_staging = nullptr;  // pinned: cta_begin, then merges, then units

@@ -131,8 +131,10 @@ int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, const
     for (int u = 0; u < n_units; ++u) {
         const Piece& pc = pieces[u];  // pieces of an item appear in token order
         const int m = merge_of[pc.item];
-        all[u] = Unit{pc.item / n_groups, pc.item % n_groups, static_cast<int32_t>(pc.t0),
-                      static_cast<int32_t>(pc.t1), m >= 0 ? next_slot[pc.item]++ : -1, m, 0, 0};
+        const int b = pc.item / n_groups;
+        all[u] = Unit{b, pc.item % n_groups, static_cast<int32_t>(pc.t0),
+                      static_cast<int32_t>(pc.t1), m >= 0 ? next_slot[pc.item]++ : -1, m,
+                      static_cast<int32_t>(indptr[b] + pc.t0), 0};
     }
 
     // 3. per-CTA lists: split pieces first, then whole items

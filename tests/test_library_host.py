@@ -76,11 +76,11 @@ def test_errors_are_reported_before_any_launch(pkv):
     lib.paged_decode_plan_destroy(None)  # no-op
 
 
-def check_plan(indptr, n_kv_heads, head_dim, ctas, plan):
+def check_plan(indptr, n_kv_heads, head_dim, ctas, plan, hpc=0):
     indptr = np.asarray(indptr, np.int64)
     B = indptr.size - 1
     lengths = np.diff(indptr)
-    hpg = min(n_kv_heads, 512 // head_dim)
+    hpg = hpc or min(n_kv_heads, 512 // head_dim)
     groups = n_kv_heads // hpg
     units, cta_begin, merges, chunk = plan["units"], plan["cta_begin"], plan["merges"], plan["chunk"]
     n = len(units)
@@ -90,8 +90,9 @@ def check_plan(indptr, n_kv_heads, head_dim, ctas, plan):
     assert plan["ctas_used"] <= ctas
     covered = {(b, g): np.zeros(lengths[b], np.int32) for b in range(B) for g in range(groups)}
     direct, parts_seen = set(), {}
-    for b, hg, t0, t1, part, merge, _, _ in units:
+    for b, hg, t0, t1, part, merge, idx_begin, _ in units:
         assert 0 <= b < B and 0 <= hg < groups and 0 <= t0 <= t1 <= lengths[b]
+        assert idx_begin == indptr[b] + t0
         covered[(b, hg)][t0:t1] += 1
         if part < 0:
             assert (t0, t1) == (0, lengths[b]) and merge == -1
@@ -140,9 +141,10 @@ def test_planner_covers_every_token_once(pkv, seed):
     indptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
     hkv, d = SHAPES[seed % len(SHAPES)]
     ctas = 152 * int(rng.integers(1, 3))
-    plan = pkv.paged_decode_plan_host(indptr, hkv, d, ctas)
-    check_plan(indptr, hkv, d, ctas, plan)
-    if lengths.sum() * (hkv // min(hkv, 512 // d)) >= 64:
+    hpc = [0, 1, 2][seed % 3] if min(hkv, 512 // d) >= 2 else 0
+    plan = pkv.paged_decode_plan_host(indptr, hkv, d, ctas, heads_per_cta=hpc)
+    check_plan(indptr, hkv, d, ctas, plan, hpc)
+    if lengths.sum() * (hkv // (hpc or min(hkv, 512 // d))) >= 64:
         assert plan["chunk"] >= 64
 
 
@@ -184,3 +186,6 @@ def test_planner_rejects_bad_input(pkv):
     with pytest.raises(pkv.PkvError) as e:
         pkv.paged_decode_plan_host(np.array([0, 100000], np.int32), 8, 128, 304, max_units=1)
     assert e.value.code == pkv.PKV_ERR_PLAN
+    with pytest.raises(pkv.PkvError) as e:  # 4 heads of dim 256 do not fit a 1 KB row
+        pkv.paged_decode_plan_host(np.array([0, 10], np.int32), 4, 256, 304, heads_per_cta=4)
+    assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
