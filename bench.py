@@ -72,13 +72,14 @@ class StepState:
         self.plan = pkv.paged_decode_plan_create(max(B, 1), max(wl.total_tokens, 1), Hq,
                                                  wl.n_kv_heads, D)
         self.launches_per_step = None
+        self.graph = None
 
-    def run(self, attn_events=None):
-        """One decode step on the current stream. attn_events: list to which
-        (start, end) CUDA events around each attention call are appended."""
+    def layers(self, attn_events=None):
+        """Every layer's KV append and decode attention, on the current stream.
+        attn_events: list to which (start, end) CUDA events around each attention
+        call are appended."""
         pkv, wl = self.pkv, self.wl
         stream = torch.cuda.current_stream()
-        pkv.paged_decode_plan(self.plan, self.kv_indptr_host.numpy(), stream=stream)
         for i in range(len(self.layer_ids)):
             pkv.kvpool_append(self.k_pool[i], self.v_pool[i], self.slot_ids, self.k_new[i],
                               self.v_new[i], stream=stream)
@@ -93,10 +94,34 @@ class StepState:
             if attn_events is not None:
                 e1.record(stream)
                 attn_events.append((e0, e1))
+
+    def run(self, attn_events=None):
+        """One decode step: the per-step plan (host partition + upload), then every
+        layer's append and attention -- replayed from the captured CUDA graph when
+        there is one (and no per-call events are asked for)."""
+        pkv = self.pkv
+        stream = torch.cuda.current_stream()
+        pkv.paged_decode_plan(self.plan, self.kv_indptr_host.numpy(), stream=stream)
+        if self.graph is not None and attn_events is None:
+            self.graph.replay()
+        else:
+            self.layers(attn_events)
         if self.launches_per_step is None:
             info = self.plan.info()
-            per_layer = (1 if len(wl.append_slots) else 0) + (1 if info["n_ctas"] else 0)
+            per_layer = (1 if len(self.wl.append_slots) else 0) + 1
             self.launches_per_step = per_layer * len(self.layer_ids)
+
+    def capture(self):
+        """Capture the layer loop (every layer's append + attention launch) into
+        one CUDA graph; the plan stays outside it, so each step re-plans on the
+        host and uploads into the plan's fixed device buffers before the replay."""
+        self.run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.layers()
+        torch.cuda.synchronize()
+        self.graph = g
 
 
 class HostIO:
@@ -314,6 +339,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every layer eagerly instead of replaying a CUDA graph")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers of the workload (small profiling "
                          "captures); the JSON line records it")
@@ -336,6 +363,8 @@ def main(argv=None):
         wl.layers = max(1, min(args.layers, wl.layers))
         wl.description += f" [first {wl.layers} layers only]"
     st = StepState(wl)
+    if not args.no_graph:
+        st.capture()
     nbytes = step_bytes(wl)
     stream = torch.cuda.current_stream()
 
@@ -355,11 +384,16 @@ def main(argv=None):
     with ClockSampler(gpu_id) as clocks:
         start.record(stream)
         for _ in range(args.steps):
-            st.run(attn_events)
+            st.run()
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
     elapsed_ms = start.elapsed_time(end)
+    # The attention calls alone, each bracketed by CUDA events on its stream
+    # (eager launches: an event between two kernels also ends their overlap).
+    for _ in range(args.steps):
+        st.run(attn_events)
+    torch.cuda.synchronize()
     attn_ms = [a.elapsed_time(b) for a, b in attn_events]
     if pg is not None:
         t = torch.tensor([elapsed_ms], device="cuda")
@@ -416,11 +450,13 @@ def main(argv=None):
             "l2": f"inputs larger than L2: each step reads {nbytes['step'] / 1e9:.2f} GB "
                   f"across {wl.layers} layers' pools (L2 {L2_BYTES / 2**20:.0f} MiB)",
             "parallelism": f"replicas x{world}",
+            "launch": "eager" if args.no_graph else "cuda graph of the layer loop per step; plan on host",
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "paged_decode_attn (split-KV kernel, LSE merge fused), "
-                               f"avg of {len(attn_ms)} calls {attn_avg_ms * 1e3:.1f} us, "
+                               f"avg of {len(attn_ms)} event-timed eager calls "
+                               f"{attn_avg_ms * 1e3:.1f} us, "
                                f"{nbytes['attn_per_layer'] / 1e6:.1f} MB algorithmic",
                      "peak_kind": peak_kind},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": io.h2d_bytes,

@@ -44,6 +44,14 @@ int fail(int code, const char* fmt, ...) {
 void clear_error() { g_last_error.clear(); }
 bool debug_checks() { return g_debug_checks != 0; }
 
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* env = std::getenv("PKV_PDL");
+        return !(env && env[0] == '0');
+    }();
+    return on;
+}
+
 }  // namespace pkv
 
 using namespace pkv;

@@ -19,6 +19,11 @@ __global__ void __launch_bounds__(256)
 kvpool_append_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
                      const int32_t* __restrict__ slot_ids, const uint4* __restrict__ k_new,
                      const uint4* __restrict__ v_new, int64_t n, int row_vecs) {
+    // Launched with programmatic stream serialisation: let the next kernel be
+    // scheduled now, but touch nothing until the previous kernel has finished
+    // (its readers of the pool, or its producers of the new rows).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t per_pool = n * row_vecs;
     const int64_t total = 2 * per_pool;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
@@ -44,12 +49,28 @@ cudaError_t launch_append(void* k_pool, void* v_pool, const int32_t* slot_ids,
     const int64_t total = 2 * n * row_vecs;
     const int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
-    // Enough CTAs to fill the GPU several times over; the loop covers the rest.
-    blocks = blocks < 152 * 16 ? blocks : 152 * 16;
-    kvpool_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), slot_ids,
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), n, row_vecs);
-    return cudaGetLastError();
+    // At most one CTA per SM: with PDL they can all be resident (and waiting)
+    // next to the previous kernel's CTAs; the loop covers the rest.
+    static int sms_of[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (sms_of[dev] == 0 &&
+        cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms_of[dev] = 152;
+    blocks = blocks < sms_of[dev] ? blocks : sms_of[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kvpool_append_kernel, static_cast<uint4*>(k_pool),
+                              static_cast<uint4*>(v_pool), slot_ids,
+                              static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                              n, row_vecs);
 }
 
 }  // namespace pkv

@@ -132,6 +132,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Programmatic dependent launch (PTX griddepcontrol): let the next kernel on the
+// stream be scheduled now / wait until the previous kernel's results are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -234,6 +241,7 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     // The next unit's descriptor is loaded one unit ahead, and its slot ids are
     // prefetched into L2 once the current unit's first stage is on its way.
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
+    pdl_wait();  // slot ids and pools may come from the previous kernel
     for (int u = u_begin; u < u_end && !aborted; ++u) {
         const Unit un = next;
         if (u + 1 < u_end) next = a.units[u + 1];
@@ -430,6 +438,7 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     // next unit's fragments are loaded while the current unit streams.
     uint32_t qb[C::kKSteps][2], qn[C::kKSteps][2];
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
+    pdl_wait();  // q may come from the previous kernel
     if (u_begin < u_end) load_q_fragments<D, G, WPH>(a, next, hh, g, t4, qn);
     for (int u = u_begin; u < u_end; ++u) {
         const Unit un = next;
@@ -609,6 +618,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeA
         fence_mbar_init();
     }
     __syncthreads();
+    // Only plan data (uploaded before the previous kernel ran) is read before
+    // each role's pdl_wait(), so the next kernel may be scheduled right away.
+    pdl_launch_dependents();
     const int u_begin = a.cta_begin[blockIdx.x];
     const int u_end = a.cta_begin[blockIdx.x + 1];
     if ((threadIdx.x >> 5) == kConsumerWarps)
@@ -641,8 +653,17 @@ cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e = prepare<D, G, WPH>();
     if (e != cudaSuccess) return e;
     if (a.n_ctas == 0) return cudaSuccess;
-    paged_decode_kernel<D, G, WPH><<<a.n_ctas, kThreads, Cfg<D, G, WPH>::kSmem, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.n_ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<D, G, WPH>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, WPH>, a);
 }
 
 // Calls FN<D, G, WPH>(args...) for the runtime shape.

@@ -10,6 +10,13 @@
 
 namespace pkv {
 
+// ---- launches -----------------------------------------------------------
+// Kernels are launched with programmatic stream serialisation (PDL) unless the
+// environment variable PKV_PDL is "0": a kernel may then be scheduled while its
+// predecessor on the stream is still running, and does only plan reads and
+// barrier set-up before its griddepcontrol.wait.
+bool pdl_enabled();
+
 // ---- errors -------------------------------------------------------------
 int fail(int code, const char* fmt, ...);  // records the message, returns code
 void clear_error();

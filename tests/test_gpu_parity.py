@@ -283,3 +283,66 @@ def test_end_to_end_host_path_matches_device_path(pkv):
     torch.cuda.synchronize()
     for a, b in zip(io.out, dev_out):
         assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
+
+
+def test_graph_replay_after_replanning(pkv):
+    """A CUDA graph of the layer loop stays valid when the next step re-plans with
+    other context lengths: the grid is fixed and the kernel reads the plan from
+    the plan's own device buffers."""
+    dev = torch.device("cuda")
+    B, layers, S = 4, 2, 1 << 16
+    steps = [[3000, 17, 0, 9000], [1, 20000, 513, 64], [700, 700, 700, 700]]
+    max_tokens = max(sum(s) for s in steps)
+    plan = pkv.paged_decode_plan_create(B, max_tokens, 32, 8, 128)
+    q = torch.empty(layers, B, 32, 128, dtype=torch.bfloat16, device=dev)
+    kp = torch.empty(layers, S, 8, 128, dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    kn = torch.empty(layers, B, 8, 128, dtype=torch.bfloat16, device=dev)
+    vn = torch.empty_like(kn)
+    out = torch.empty(layers, B, 32, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(layers, B, 32, dtype=torch.float32, device=dev)
+    indptr = torch.zeros(B + 1, dtype=torch.int32, device=dev)
+    indices = torch.zeros(max_tokens, dtype=torch.int32, device=dev)
+    slots = torch.zeros(B, dtype=torch.int32, device=dev)
+    graph = None
+    for step, lengths in enumerate(steps):
+        wl = workloads.scattered_workload(lengths, pool_slots=S, layers=layers, seed=300 + step)
+        tens = [workloads.layer_tensors(wl, l, device="cpu") for l in range(layers)]
+        nonempty = [b for b in range(B) if lengths[b] > 0]
+        for l, t in enumerate(tens):
+            q[l].copy_(t.q)
+            kp[l].copy_(t.k_pool)
+            vp[l].copy_(t.v_pool)
+            kn[l].zero_()
+            vn[l].zero_()
+            kn[l][nonempty] = t.k_new.to(dev)
+            vn[l][nonempty] = t.v_new.to(dev)
+        unused = np.setdiff1d(np.arange(S), wl.kv_indices)[:B].astype(np.int32)
+        app = unused.copy()  # rows of empty requests land on slots nobody lists
+        app[nonempty] = wl.append_slots
+        slots.copy_(torch.from_numpy(app))
+        indptr.copy_(torch.from_numpy(wl.kv_indptr))
+        indices[:wl.total_tokens].copy_(torch.from_numpy(wl.kv_indices))
+        pkv.paged_decode_plan(plan, wl.kv_indptr)
+        if graph is None:
+            def body():
+                for l in range(layers):
+                    pkv.kvpool_append(kp[l], vp[l], slots, kn[l], vn[l])
+                    pkv.paged_decode_attn(q[l], kp[l], vp[l], indptr, indices, B, 32, 8, 128,
+                                          wl.sm_scale, out[l], lse[l], plan)
+            body()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                body()
+            # the capture did not run the body; make it run from a fresh pool state
+            for l, t in enumerate(tens):
+                kp[l].copy_(t.k_pool)
+                vp[l].copy_(t.v_pool)
+        graph.replay()
+        torch.cuda.synchronize()
+        for l, t in enumerate(tens):
+            ref_out, ref_lse = oracle_reference(wl, t)
+            assert_parity(to_f64(out[l]), lse[l].cpu().numpy(), ref_out, ref_lse,
+                          what=f"graph step {step} layer {l}")
+    assert plan.status() == 0
