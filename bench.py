@@ -108,7 +108,8 @@ class StepState:
             self.layers(attn_events)
         if self.launches_per_step is None:
             info = self.plan.info()
-            per_layer = (1 if len(self.wl.append_slots) else 0) + 1
+            # append, decode kernel, merge kernel (launched even when nothing is split)
+            per_layer = (1 if len(self.wl.append_slots) else 0) + 2
             self.launches_per_step = per_layer * len(self.layer_ids)
 
     def capture(self):
@@ -195,54 +196,100 @@ def measured_hbm_peak():
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the GPU's SM clock and clock-event (throttle) reasons while the
+    timed region runs: NVML through ctypes, polled from a thread every ~2 ms
+    (falls back to nvidia-smi at 200 ms if NVML cannot be loaded). Read only."""
 
-    def __init__(self, gpu_id: str):
-        self.proc = None
-        self.gpu_id = gpu_id
+    REASONS = {0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.samples = []
+        self.max_mhz = None
+        self._stop = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        props = torch.cuda.get_device_properties(self.device_index)
+        handle = ctypes.c_void_p()
+        uuid = getattr(props, "uuid", None)
+        ok = False
+        if uuid is not None:
+            text = str(uuid)
+            if not text.startswith("GPU-"):
+                text = "GPU-" + text
+            ok = lib.nvmlDeviceGetHandleByUUID(text.encode(), ctypes.byref(handle)) == 0
+        if not ok:
+            raise RuntimeError("no NVML handle for the device")
+        return lib, handle
 
     def __enter__(self):
+        import threading
+        self._stop = threading.Event()
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+            import ctypes
+            lib, handle = self._nvml()
+            clk = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(clk)) == 0:
+                self.max_mhz = clk.value
+            reasons = ctypes.c_ulonglong()
+
+            def poll():
+                while not self._stop.is_set():
+                    c = ctypes.c_uint()
+                    if lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(c)) == 0:
+                        r = ctypes.c_ulonglong(0)
+                        lib.nvmlDeviceGetCurrentClocksEventReasons(handle, ctypes.byref(r))
+                        self.samples.append((c.value, r.value))
+                    self._stop.wait(0.002)
+
+            self._thread = threading.Thread(target=poll, daemon=True)
+            self._thread.start()
+            self._mode = "nvml"
+        except Exception:
+            self._mode = "smi"
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.device_index}",
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._mode == "nvml":
+            self._thread.join(timeout=2)
+        else:
+            self._proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                out, _ = self._proc.communicate(timeout=5)
             except Exception:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                self._proc.kill()
+                out, _ = self._proc.communicate()
+            for line in out.splitlines():
+                parts = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append((float(parts[0]), int(parts[2], 16)))
+                    self.max_mhz = float(parts[1])
+                except (ValueError, IndexError):
+                    pass
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in getattr(self, "lines", []):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "samples": 0, "source": self._mode}
+        mhz = [m for m, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted(name for bit, name in self.REASONS.items() if bits & bit)
+        return {"sm_mhz": statistics.median(mhz), "sm_min_mhz": min(mhz),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(mhz),
+                "source": self._mode}
 
 
 def cpu_baseline(st: StepState, budget_s: float = 12.0, max_layers=None):
@@ -379,9 +426,7 @@ def main(argv=None):
     attn_events = []
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
-    gpu_id = visible[local].strip() if local < len(visible) and visible[local].strip() else str(local)
-    with ClockSampler(gpu_id) as clocks:
+    with ClockSampler(local) as clocks:
         start.record(stream)
         for _ in range(args.steps):
             st.run()

@@ -201,14 +201,15 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     p->lim.max_units = plan_max_units(p->ctas, max_batch, p->n_groups);
     p->lim.max_merges = max_batch * p->n_groups;
     p->indptr_host.reserve(max_batch + 1);
-    // staging layout: cta_begin[ctas + 1] | merges[max_merges] | units[max_units]
-    p->off_merge = round16(sizeof(int32_t) * (p->ctas + 1));
+    // staging layout: header[4] | cta_begin[ctas + 1] | merges[max_merges] | units[max_units]
+    p->off_cta = 16;
+    p->off_merge = round16(p->off_cta + sizeof(int32_t) * (p->ctas + 1));
     p->off_units = round16(p->off_merge + sizeof(Merge) * p->lim.max_merges);
     p->meta_bytes = p->off_units + sizeof(Unit) * p->lim.max_units;
     const int group_q_heads = hpg * (n_qo_heads / n_kv_heads);
     const size_t ws_o_bytes = sizeof(float) * size_t(p->lim.max_units) * group_q_heads * head_dim;
     const size_t ws_lse_bytes = sizeof(float) * size_t(p->lim.max_units) * group_q_heads;
-    const size_t state_bytes = sizeof(int) * (size_t(p->lim.max_merges) + 32);
+    const size_t state_bytes = sizeof(int) * 32;
     e = cudaMallocHost(&p->host_staging, p->meta_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&p->dev_meta, p->meta_bytes);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_o), ws_o_bytes);
@@ -247,9 +248,13 @@ int paged_decode_plan(pkv_plan* p, const int32_t* kv_indptr_host, int batch, pkv
     PlanCounts c{};
     int rc = plan_compute(kv_indptr_host, batch, p->n_groups, p->ctas, p->lim,
                           reinterpret_cast<Unit*>(st + p->off_units),
-                          reinterpret_cast<int32_t*>(st),
+                          reinterpret_cast<int32_t*>(st + p->off_cta),
                           reinterpret_cast<Merge*>(st + p->off_merge), &c);
     if (rc != PKV_OK) return rc;
+    int32_t* header = reinterpret_cast<int32_t*>(st);
+    header[0] = c.n_merges;
+    header[1] = c.n_partials;
+    header[2] = header[3] = 0;
     const size_t bytes = p->off_units + sizeof(Unit) * c.n_units;
     cudaError_t e = cudaMemcpyAsync(p->dev_meta, st, bytes, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaEventRecord(p->copy_done, stream);
@@ -277,7 +282,7 @@ int paged_decode_plan_info(const pkv_plan* p, int* batch, int* n_units, int* n_m
 int paged_decode_plan_status(pkv_plan* p, int* status) {
     clear_error();
     if (!p || !status) return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_status: NULL argument");
-    int* word = p->dev_state + p->lim.max_merges;
+    int* word = p->dev_state;
     int v = 0;
     cudaError_t e = cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && v != 0) e = cudaMemset(word, 0, sizeof v);
@@ -337,7 +342,8 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
     a.v_pool = v_pool;
     a.kv_indptr = kv_indptr;
     a.kv_indices = kv_indices;
-    a.cta_begin = reinterpret_cast<const int32_t*>(meta);
+    a.meta_header = reinterpret_cast<const int32_t*>(meta);
+    a.cta_begin = reinterpret_cast<const int32_t*>(meta + p->off_cta);
     a.merges = reinterpret_cast<const Merge*>(meta + p->off_merge);
     a.units = reinterpret_cast<const Unit*>(meta + p->off_units);
     a.n_ctas = p->ctas;
@@ -350,8 +356,8 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
     a.lse = lse;
     a.ws_o = p->ws_o;
     a.ws_lse = p->ws_lse;
-    a.merge_counters = p->dev_state;
-    a.status = p->dev_state + p->lim.max_merges;
+    a.merge_ctas = p->num_sms;
+    a.status = p->dev_state;
     a.zero_row = p->zero_row;
     cudaError_t e = launch_decode(a, stream);
     if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attn: launch");

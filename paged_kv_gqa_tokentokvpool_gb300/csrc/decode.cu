@@ -35,10 +35,10 @@
 //    moved.
 //  * A unit covering a whole context writes bf16 out and lse directly. A unit
 //    covering part of one writes its normalised fp32 output and base-2 lse to the
-//    plan's workspace and bumps the context's arrival counter; the CTA that
-//    arrives last merges all parts by the log-sum-exp identity
+//    plan's workspace; a second, small kernel merges the parts of every split
+//    context by the log-sum-exp identity
 //        lse = log2 sum_c 2^lse_c,   out = sum_c 2^(lse_c - lse) out_c
-//    and resets the counter, so no separate merge launch is needed.
+//    with one warp per (context, query head), all parts' loads in flight at once.
 //  * Every wait on an mbarrier is bounded (1 s); on expiry the kernel sets the
 //    plan's status word, stops, and waits (again bounded) for its own copies in
 //    flight before exiting.
@@ -208,7 +208,7 @@ struct Cfg {
     static constexpr int kDimsPerWarp = D / WPH;
     static constexpr int kQHeads = kHeadsPerCta * G;            // query heads of a group
     static constexpr int kBarOffset = kStages * kStage;
-    static constexpr int kSmem = kBarOffset + (2 * kStages + 1) * 8 + 16;
+    static constexpr int kSmem = kBarOffset + 2 * kStages * 8 + 16;
     static_assert(G >= 1 && G <= 8, "group size");
     static_assert(kHeadsPerCta * D * kSub == kHeadGroupElems, "stage budget");
     static_assert(kMBlocks >= 1, "dims per warp");
@@ -217,8 +217,7 @@ struct Cfg {
 struct Shared {
     uint64_t* full;
     uint64_t* empty;
-    uint64_t* cons;       // consumer-warps barrier
-    volatile int* flags;  // [0] abort, [1] this CTA merges the current unit
+    volatile int* flags;  // [0] abort
 };
 
 // Producer warp: lane l copies, for every sub-tile j of a stage, token
@@ -319,100 +318,6 @@ __device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit
     }
 }
 
-// Log-sum-exp merge of all parts of one split (request, head group), run by the
-// CTA that finished its last part. Warp (hh, part) merges the G query heads of
-// KV head hh over its slice of head_dim. First the merged lse of each head:
-// lanes take parts c = lane, lane + 32, ... with an online max/sum, then a warp
-// reduction. Then lane l accumulates float4 v = l + 32 i of the [G x dims] block
-// over all parts. Partial results sit in L2 (just written by other SMs); every
-// load is independent, so they are batched by unrolling.
-template <int D, int G, int WPH>
-__device__ void merge_parts(const DecodeArgs& a, const Unit& un, int hh, int part, int lane) {
-    using C = Cfg<D, G, WPH>;
-    constexpr int kVec = G * C::kDimsPerWarp / 4;
-    constexpr int kPerLane = (kVec + 31) / 32;
-    const Merge mg = a.merges[un.merge];
-    const int P = mg.count;
-    const int hq = a.n_qo_heads;
-    const int kvh = un.hg * C::kHeadsPerCta + hh;
-    const float* lse_base = a.ws_lse + int64_t(mg.first) * C::kQHeads + hh * G;
-    const float* o_base = a.ws_o + (int64_t(mg.first) * C::kQHeads + hh * G) * D;
-
-    float total[G];
-    {
-        float m[G], s[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            m[h] = neg_inf();
-            s[h] = 0.f;
-        }
-        for (int c = lane; c < P; c += 32) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float x = __ldcg(lse_base + int64_t(c) * C::kQHeads + h);
-                const float mn = fmaxf(m[h], x);
-                s[h] = (m[h] == neg_inf() ? 0.f : s[h] * ex2(m[h] - mn)) + ex2(x - mn);
-                m[h] = mn;
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float mo = __shfl_xor_sync(kFull, m[h], off);
-                const float so = __shfl_xor_sync(kFull, s[h], off);
-                const float mn = fmaxf(m[h], mo);
-                const float a0 = m[h] == neg_inf() ? 0.f : s[h] * ex2(m[h] - mn);
-                const float a1 = mo == neg_inf() ? 0.f : so * ex2(mo - mn);
-                s[h] = a0 + a1;
-                m[h] = mn;
-            }
-            total[h] = m[h] + __log2f(s[h]);
-        }
-    }
-
-    int hsel[kPerLane], dsel[kPerLane];
-    float tsel[kPerLane];
-    float4 acc[kPerLane];
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-        const int v = lane + 32 * i;
-        const int e = 4 * (v < kVec ? v : 0);
-        hsel[i] = e / C::kDimsPerWarp;
-        dsel[i] = part * C::kDimsPerWarp + e % C::kDimsPerWarp;
-        tsel[i] = total[0];
-#pragma unroll
-        for (int h = 1; h < G; ++h)
-            if (hsel[i] == h) tsel[i] = total[h];
-        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll 4
-    for (int c = 0; c < P; ++c) {
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            const int64_t row = int64_t(c) * C::kQHeads + hsel[i];
-            const float w = ex2(__ldcg(lse_base + row) - tsel[i]);
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(o_base + row * D + dsel[i]));
-            acc[i].x = fmaf(w, x.x, acc[i].x);
-            acc[i].y = fmaf(w, x.y, acc[i].y);
-            acc[i].z = fmaf(w, x.z, acc[i].z);
-            acc[i].w = fmaf(w, x.w, acc[i].w);
-        }
-    }
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-        if (lane + 32 * i >= kVec) continue;
-        const int64_t orow = (int64_t(un.b) * hq + kvh * G + hsel[i]) * D + dsel[i];
-        uint2 packed;
-        packed.x = pack_bf16x2(acc[i].x, acc[i].y);
-        packed.y = pack_bf16x2(acc[i].z, acc[i].w);
-        *reinterpret_cast<uint2*>(out + orow) = packed;
-        if (a.lse != nullptr && dsel[i] == 0)
-            a.lse[int64_t(un.b) * hq + kvh * G + hsel[i]] = tsel[i] * kLn2;
-    }
-}
-
 template <int D, int G, int WPH>
 __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
@@ -432,7 +337,7 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                             ((lane & 7) + (lane >> 4) * 8) * C::kRowP +
                             (hh * D + part * C::kDimsPerWarp + ((lane >> 3) & 1) * 8) * 2;
     int stage = 0;
-    uint32_t full_parity = 0, cons_parity = 0;
+    uint32_t full_parity = 0;
 
     // Q^T as the B operand: lane holds head g, dims 2*t4.. of each k-step. The
     // next unit's fragments are loaded while the current unit streams.
@@ -573,28 +478,6 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             if (h0 < G) lp[h0] = lse0;
             if (h1 < G) lp[h1] = lse1;
         }
-        // Arrive on the context's counter once all four warps' stores are out;
-        // the last arriving CTA merges.
-        __threadfence();
-        __syncwarp();
-        const uint32_t cons_bar = smem_u32(sh.cons);
-        if (lane == 0) mbar_arrive(cons_bar);
-        if (!__all_sync(kFull, mbar_wait(cons_bar, cons_parity, a.status, sh.flags))) return;
-        cons_parity ^= 1;
-        if (warp == 0 && lane == 0) {
-            const int prev = atomicAdd(a.merge_counters + un.merge, 1);
-            const int last = prev == a.merges[un.merge].count - 1;
-            if (last) a.merge_counters[un.merge] = 0;
-            sh.flags[1] = last;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cons_bar);
-        if (!__all_sync(kFull, mbar_wait(cons_bar, cons_parity, a.status, sh.flags))) return;
-        cons_parity ^= 1;
-        if (sh.flags[1]) {
-            __threadfence();
-            merge_parts<D, G, WPH>(a, un, hh, part, lane);
-        }
     }
 }
 
@@ -605,16 +488,13 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeA
     Shared sh;
     sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
     sh.empty = sh.full + kStages;
-    sh.cons = sh.empty + kStages;
-    sh.flags = reinterpret_cast<volatile int*>(sh.cons + 1);
+    sh.flags = reinterpret_cast<volatile int*>(sh.empty + kStages);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
             mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
         }
-        mbar_init(smem_u32(sh.cons), kConsumerWarps);
         sh.flags[0] = 0;
-        sh.flags[1] = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -627,6 +507,98 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeA
         producer_warp<D, G, WPH>(a, smem, sh, u_begin, u_end);
     else
         consumer_warp<D, G, WPH>(a, smem, sh, u_begin, u_end);
+}
+
+// ---------------------------------------------------------------------------
+// LSE merge of split contexts
+// ---------------------------------------------------------------------------
+// One warp per (merge record, query head of the group): lanes first take parts
+// c = lane, lane + 32, ... to form the merged log-sum-exp (online max/sum, then a
+// warp reduction), then every lane owns head_dim/32 consecutive dimensions and
+// sums w_c * out_c over all parts, with w_c = 2^(lse_c - lse) broadcast from the
+// lane that read part c. Launched right after the decode kernel on a fixed grid
+// (warps loop over the work), so the launch does not depend on the step.
+constexpr int kMergeThreads = 128;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // the partial results come from the decode kernel
+    constexpr int kVD = D / 32;  // dims per lane
+    const int lane = threadIdx.x & 31;
+    const int n_merges = a.meta_header[0];
+    const int qheads = a.heads_per_cta * (a.n_qo_heads / a.n_kv_heads);
+    const int G = a.n_qo_heads / a.n_kv_heads;
+    const int items = n_merges * qheads;
+    const int warps = gridDim.x * (kMergeThreads / 32);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    for (int w = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5); w < items; w += warps) {
+        const int m = w / qheads, qh = w % qheads;
+        const Merge mg = a.merges[m];
+        const float* lse_p = a.ws_lse + int64_t(mg.first) * qheads + qh;
+        float mx = neg_inf(), sm = 0.f;
+        for (int c = lane; c < mg.count; c += 32) {
+            const float x = __ldcg(lse_p + int64_t(c) * qheads);
+            const float mn = fmaxf(mx, x);
+            sm = (mx == neg_inf() ? 0.f : sm * ex2(mx - mn)) + ex2(x - mn);
+            mx = mn;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float mo = __shfl_xor_sync(kFull, mx, off);
+            const float so = __shfl_xor_sync(kFull, sm, off);
+            const float mn = fmaxf(mx, mo);
+            sm = (mx == neg_inf() ? 0.f : sm * ex2(mx - mn)) + (mo == neg_inf() ? 0.f : so * ex2(mo - mn));
+            mx = mn;
+        }
+        const float total = mx + __log2f(sm);
+        float acc[kVD];
+#pragma unroll
+        for (int i = 0; i < kVD; ++i) acc[i] = 0.f;
+        const float* o_p = a.ws_o + (int64_t(mg.first) * qheads + qh) * D + lane * kVD;
+        for (int c0 = 0; c0 < mg.count; c0 += 32) {
+            const int c = c0 + lane;
+            const float wl = c < mg.count ? ex2(__ldcg(lse_p + int64_t(c) * qheads) - total) : 0.f;
+            const int n = min(32, mg.count - c0);
+#pragma unroll 8
+            for (int j = 0; j < n; ++j) {
+                const float wj = __shfl_sync(kFull, wl, j);
+                const float* src = o_p + int64_t(c0 + j) * qheads * D;
+#pragma unroll
+                for (int i = 0; i < kVD; i += 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4*>(src + i));
+                    acc[i] = fmaf(wj, x.x, acc[i]);
+                    acc[i + 1] = fmaf(wj, x.y, acc[i + 1]);
+                    acc[i + 2] = fmaf(wj, x.z, acc[i + 2]);
+                    acc[i + 3] = fmaf(wj, x.w, acc[i + 3]);
+                }
+            }
+        }
+        const int h = (mg.hg * a.heads_per_cta) * G + qh;  // query head index
+        __nv_bfloat16* dst = out + (int64_t(mg.b) * a.n_qo_heads + h) * D + lane * kVD;
+#pragma unroll
+        for (int i = 0; i < kVD; i += 4) {
+            uint2 packed;
+            packed.x = pack_bf16x2(acc[i], acc[i + 1]);
+            packed.y = pack_bf16x2(acc[i + 2], acc[i + 3]);
+            *reinterpret_cast<uint2*>(dst + i) = packed;
+        }
+        if (a.lse != nullptr && lane == 0) a.lse[int64_t(mg.b) * a.n_qo_heads + h] = total * kLn2;
+    }
+}
+
+template <int D>
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.merge_ctas);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<D>, a);
 }
 
 template <int D, int G, int WPH>
@@ -722,8 +694,10 @@ int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_p
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-    return dispatch<LaunchFn>(a.head_dim, a.n_qo_heads / a.n_kv_heads,
-                              warps_per_head(a.heads_per_cta), a, stream);
+    cudaError_t e = dispatch<LaunchFn>(a.head_dim, a.n_qo_heads / a.n_kv_heads,
+                                       warps_per_head(a.heads_per_cta), a, stream);
+    if (e != cudaSuccess) return e;
+    return a.head_dim == 128 ? launch_merge<128>(a, stream) : launch_merge<256>(a, stream);
 }
 
 }  // namespace pkv

@@ -88,7 +88,8 @@ struct DecodeArgs {
     float* lse;
     float* ws_o;          // [max partials, group q heads, head_dim] fp32 partial outputs
     float* ws_lse;        // [max partials, group q heads] fp32 partial lse (base 2)
-    int* merge_counters;  // [max merges], zero between launches
+    const int32_t* meta_header;  // device copy of {merge records, partial slots, 0, 0}
+    int merge_ctas;       // grid of the merge kernel (fixed per plan)
     int* status;          // device status word (nonzero: a wait timed out)
     const void* zero_row; // kHeadGroupElems bf16 zeros (tile padding)
 };
@@ -112,11 +113,11 @@ struct pkv_plan {
     int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0, n_groups = 0, heads_per_cta = 0;
     pkv::PlanLimits lim{};
     size_t meta_bytes = 0;
-    void* host_staging = nullptr;  // pinned: cta_begin, then merges, then units
+    void* host_staging = nullptr;  // pinned: header, cta_begin, merges, units
     void* dev_meta = nullptr;      // device copy of the same (used prefix uploaded per step)
     float* ws_o = nullptr;
     float* ws_lse = nullptr;
-    int* dev_state = nullptr;      // merge counters [max_merges], status word, padding
+    int* dev_state = nullptr;      // status word, padding
     void* zero_row = nullptr;
     cudaEvent_t copy_done = nullptr;
     bool copy_pending = false;
@@ -124,6 +125,6 @@ struct pkv_plan {
     bool planned = false;
     int batch = 0;
     pkv::PlanCounts counts{};
-    size_t off_merge = 0, off_units = 0;  // byte offsets of the regions in the staging
+    size_t off_cta = 0, off_merge = 0, off_units = 0;  // byte offsets in the staging
     std::vector<int32_t> indptr_host;
 };
