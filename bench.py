@@ -236,14 +236,15 @@ class ClockSampler:
             clk = ctypes.c_uint()
             if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(clk)) == 0:
                 self.max_mhz = clk.value
-            reasons = ctypes.c_ulonglong()
+            get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
 
             def poll():
                 while not self._stop.is_set():
                     c = ctypes.c_uint()
                     if lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(c)) == 0:
                         r = ctypes.c_ulonglong(0)
-                        lib.nvmlDeviceGetCurrentClocksEventReasons(handle, ctypes.byref(r))
+                        get_reasons(handle, ctypes.byref(r))
                         self.samples.append((c.value, r.value))
                     self._stop.wait(0.002)
 
