@@ -138,6 +138,33 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
                       int n_qo_heads, int n_kv_heads, int head_dim, float sm_scale,
                       void* out, float* lse, const pkv_plan* plan, pkv_stream_t stream);
 
+/*
+ * paged_decode_attn_static — the same attention as paged_decode_attn, for callers
+ * that cannot allocate device memory: an engine that has given all free HBM to
+ * its KV pool, a runtime whose allocator must own every device buffer, or a path
+ * that must not hit cudaMalloc's implicit synchronisation. The paper has no
+ * counterpart; it is an addition of this library.
+ *   Arguments as for paged_decode_attn, plus kv_indptr_host ([batch + 1] int32
+ *   HOST copy of kv_indptr); there is no plan: every call plans the step on the
+ *   host.
+ *   Scratch: the work list, a status word, a zero row and the split workspace live
+ *   in one file-scope __device__ array of 32 MiB that every GPU loading the library
+ *   holds until exit; nothing is allocated. The first call on a device (with that
+ *   device current) looks the array up with cudaGetSymbolAddress; make it before
+ *   any stream capture. Steps needing more than 32 MiB of scratch (or more than
+ *   1024 CTAs, 4096 (request, head group) pairs or 8192 work units) return
+ *   PKV_ERR_PLAN with the size in the message.
+ *   All calls share the array and leave its contents behind (the status word and
+ *   zero row are cleared on every call): calls whose kernels overlap on the GPU
+ *   race. Calls from several host threads are serialised on the host.
+ *   The work list is copied from pageable host memory with cudaMemcpyAsync.
+ */
+int paged_decode_attn_static(const void* q, const void* k_pool, const void* v_pool,
+                             const int32_t* kv_indptr_host, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, int batch, int n_qo_heads,
+                             int n_kv_heads, int head_dim, float sm_scale, void* out,
+                             float* lse, pkv_stream_t stream);
+
 /* paged_decode_plan_destroy — free a plan (waits for its pending copy). NULL is a no-op. */
 void paged_decode_plan_destroy(pkv_plan* plan);
 

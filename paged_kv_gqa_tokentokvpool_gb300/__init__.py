@@ -36,8 +36,8 @@ PKV_ERR_INDEX = -5
 
 EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",
-            "paged_decode_plan_info", "paged_decode_plan_status", "pkv_set_debug_checks",
-            "pkv_last_error")
+            "paged_decode_plan_info", "paged_decode_plan_status", "paged_decode_attn_static",
+            "pkv_set_debug_checks", "pkv_last_error")
 
 
 class PkvError(RuntimeError):
@@ -65,13 +65,15 @@ def _load() -> ctypes.CDLL:
     lib.paged_decode_plan_host.argtypes = [P, I32, I32, I32, I32, I32, P, I32, P, P, I32, P]
     lib.paged_decode_plan_info.argtypes = [P, P, P, P, P, P]
     lib.paged_decode_plan_status.argtypes = [P, P]
+    lib.paged_decode_attn_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32,
+                                             ctypes.c_float, P, P, P]
     lib.pkv_set_debug_checks.argtypes = [I32]
     lib.pkv_set_debug_checks.restype = None
     lib.pkv_last_error.argtypes = []
     lib.pkv_last_error.restype = ctypes.c_char_p
     for name in ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
                  "paged_decode_attn", "paged_decode_plan_host", "paged_decode_plan_info",
-                 "paged_decode_plan_status"):
+                 "paged_decode_plan_status", "paged_decode_attn_static"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -209,6 +211,27 @@ def paged_decode_attn(q, k_pool, v_pool, kv_indptr, kv_indices, batch, n_qo_head
                                   _ptr(kv_indices), batch, n_qo_heads, n_kv_heads, head_dim,
                                   float(sm_scale), _ptr(out), _ptr(lse), plan.handle,
                                   _stream(stream)))
+
+
+def paged_decode_attn_static(q, k_pool, v_pool, kv_indptr_host, kv_indptr, kv_indices, batch,
+                             n_qo_heads, n_kv_heads, head_dim, sm_scale, out, lse,
+                             stream=None) -> None:
+    """paged_decode_attn without a plan and without any device allocation: the
+    step is planned on every call and all scratch lives in the library's static
+    32 MiB device array (see include/pkv.h for the sharing rules)."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(k_pool, torch.bfloat16, "k_pool")
+    _dev(v_pool, torch.bfloat16, "v_pool")
+    _dev(kv_indptr, torch.int32, "kv_indptr")
+    _dev(kv_indices, torch.int32, "kv_indices")
+    _dev(out, torch.bfloat16, "out")
+    if lse is not None:
+        _dev(lse, torch.float32, "lse")
+    ip = _host_indptr(kv_indptr_host)
+    _check(library().paged_decode_attn_static(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(ip), _ptr(kv_indptr), _ptr(kv_indices), batch,
+        n_qo_heads, n_kv_heads, head_dim, float(sm_scale), _ptr(out), _ptr(lse),
+        _stream(stream)))
 
 
 def paged_decode_plan_destroy(plan: Plan) -> None:

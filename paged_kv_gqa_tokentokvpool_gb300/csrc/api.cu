@@ -44,6 +44,16 @@ int fail(int code, const char* fmt, ...) {
 void clear_error() { g_last_error.clear(); }
 bool debug_checks() { return g_debug_checks != 0; }
 
+int choose_heads_per_cta(int n_kv_heads, int head_dim) {
+    int hpg = heads_per_group(n_kv_heads, head_dim);
+    if (const char* env = std::getenv("PKV_HEADS_PER_CTA")) {
+        const int want = std::atoi(env);
+        if ((want == 1 || want == 2 || want == 4) && want <= hpg && n_kv_heads % want == 0)
+            hpg = want;
+    }
+    return hpg;
+}
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char* env = std::getenv("PKV_PDL");
@@ -177,14 +187,7 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
         delete p;
         return cuda_fail(e, "paged_decode_plan_create: device query");
     }
-    // KV heads per CTA group: the largest the shape allows, unless the
-    // PKV_HEADS_PER_CTA environment variable (1, 2 or 4) asks for fewer.
-    int hpg = heads_per_group(n_kv_heads, head_dim);
-    if (const char* env = std::getenv("PKV_HEADS_PER_CTA")) {
-        const int want = std::atoi(env);
-        if ((want == 1 || want == 2 || want == 4) && want <= hpg && n_kv_heads % want == 0)
-            hpg = want;
-    }
+    const int hpg = choose_heads_per_cta(n_kv_heads, head_dim);
     p->heads_per_cta = hpg;
     p->ctas_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg);
     if (p->ctas_per_sm <= 0) {

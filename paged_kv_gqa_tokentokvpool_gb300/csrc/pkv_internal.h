@@ -33,6 +33,9 @@ inline int heads_per_group(int n_kv_heads, int head_dim) {
     const int cap = kHeadGroupElems / head_dim;
     return n_kv_heads < cap ? n_kv_heads : cap;
 }
+// The group size a new plan uses: heads_per_group(), unless the environment
+// variable PKV_HEADS_PER_CTA (1, 2 or 4) asks for a smaller valid one.
+int choose_heads_per_cta(int n_kv_heads, int head_dim);
 
 // ---- plan ----------------------------------------------------------------
 // One work unit of the decode kernel: tokens [tok_begin, tok_end) of request b's
