@@ -46,7 +46,7 @@ class StepState:
     """Device tensors of one decode step for every layer, plus the plan."""
 
     def __init__(self, wl: workloads.Workload, device="cuda", layers=None,
-                 poison_unreferenced=False):
+                 poison_unreferenced=False, fused=None):
         import paged_kv_gqa_tokentokvpool_gb300 as pkv
         self.pkv = pkv
         self.wl = wl
@@ -73,6 +73,10 @@ class StepState:
                                                  wl.n_kv_heads, D)
         self.launches_per_step = None
         self.graph = None
+        # The append runs inside the attention launch when every request has a
+        # newest token that is its last listed slot (the decode steps here).
+        can_fuse = len(wl.append_slots) == wl.batch and wl.batch > 0
+        self.fused = can_fuse if fused is None else (fused and can_fuse)
 
     def layers(self, attn_events=None):
         """Every layer's KV append and decode attention, on the current stream.
@@ -81,16 +85,25 @@ class StepState:
         pkv, wl = self.pkv, self.wl
         stream = torch.cuda.current_stream()
         for i in range(len(self.layer_ids)):
-            pkv.kvpool_append(self.k_pool[i], self.v_pool[i], self.slot_ids, self.k_new[i],
-                              self.v_new[i], stream=stream)
+            if not self.fused:
+                pkv.kvpool_append(self.k_pool[i], self.v_pool[i], self.slot_ids, self.k_new[i],
+                                  self.v_new[i], stream=stream)
             if attn_events is not None:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-            pkv.paged_decode_attn(self.q[i], self.k_pool[i], self.v_pool[i], self.kv_indptr,
-                                  self.kv_indices, wl.batch, wl.n_qo_heads, wl.n_kv_heads,
-                                  wl.head_dim, wl.sm_scale, self.out[i], self.lse[i], self.plan,
-                                  stream=stream)
+            if self.fused:
+                pkv.paged_decode_append_attn(self.q[i], self.k_pool[i], self.v_pool[i],
+                                             self.kv_indptr, self.kv_indices, self.slot_ids,
+                                             self.k_new[i], self.v_new[i], wl.batch,
+                                             wl.n_qo_heads, wl.n_kv_heads, wl.head_dim,
+                                             wl.sm_scale, self.out[i], self.lse[i], self.plan,
+                                             stream=stream)
+            else:
+                pkv.paged_decode_attn(self.q[i], self.k_pool[i], self.v_pool[i], self.kv_indptr,
+                                      self.kv_indices, wl.batch, wl.n_qo_heads, wl.n_kv_heads,
+                                      wl.head_dim, wl.sm_scale, self.out[i], self.lse[i],
+                                      self.plan, stream=stream)
             if attn_events is not None:
                 e1.record(stream)
                 attn_events.append((e0, e1))
@@ -108,8 +121,9 @@ class StepState:
             self.layers(attn_events)
         if self.launches_per_step is None:
             info = self.plan.info()
-            # append, decode kernel, merge kernel (launched even when nothing is split)
-            per_layer = (1 if len(self.wl.append_slots) else 0) + 2
+            # append (unless fused), decode kernel, merge kernel (launched even when
+            # nothing is split)
+            per_layer = (0 if self.fused or not len(self.wl.append_slots) else 1) + 2
             self.launches_per_step = per_layer * len(self.layer_ids)
 
     def capture(self):
@@ -387,6 +401,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--separate-append", action="store_true",
+                    help="run kvpool_append as its own kernel before each attention call")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every layer eagerly instead of replaying a CUDA graph")
     ap.add_argument("--layers", type=int, default=None,
@@ -410,7 +426,7 @@ def main(argv=None):
     if args.layers is not None:
         wl.layers = max(1, min(args.layers, wl.layers))
         wl.description += f" [first {wl.layers} layers only]"
-    st = StepState(wl)
+    st = StepState(wl, fused=not args.separate_append)
     if not args.no_graph:
         st.capture()
     nbytes = step_bytes(wl)
@@ -497,6 +513,7 @@ def main(argv=None):
                   f"across {wl.layers} layers' pools (L2 {L2_BYTES / 2**20:.0f} MiB)",
             "parallelism": f"replicas x{world}",
             "launch": "eager" if args.no_graph else "cuda graph of the layer loop per step; plan on host",
+            "append": "fused into the attention launch" if st.fused else "separate kernel",
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

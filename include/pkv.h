@@ -130,13 +130,36 @@ int paged_decode_plan(pkv_plan* plan, const int32_t* kv_indptr_host, int batch,
  *   lse        : [batch, n_qo_heads] fp32, written; may be NULL
  *   plan       : built by paged_decode_plan for this step with the same batch and
  *                created for the same (n_qo_heads, n_kv_heads, head_dim)
- * Launches one kernel. Contexts that the plan split are merged inside it by the
- * CTA that finishes a context's last part. A plan serves one stream at a time.
+ * Launches the split-KV kernel and then the LSE-merge kernel (the latter exits at
+ * once when no context was split). A plan serves one stream at a time.
  */
 int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
                       const int32_t* kv_indptr, const int32_t* kv_indices, int batch,
                       int n_qo_heads, int n_kv_heads, int head_dim, float sm_scale,
                       void* out, float* lse, const pkv_plan* plan, pkv_stream_t stream);
+
+/*
+ * paged_decode_append_attn — kvpool_append followed by paged_decode_attn, in one
+ * launch (plus the merge kernel): each request's newest K/V row is read straight
+ * from k_new / v_new by the attention kernel, which also writes it to its pool
+ * slot, so the step needs no separate append kernel. The pages' decode step writes
+ * the token's K/V into its pool slot and then attends over the request's slots
+ * ("Agent-Infer", section "分页 KV 缓存"); this call does both.
+ *   slot_ids   : [batch] int32 device array; slot_ids[b] must be request b's LAST
+ *                listed slot, kv_indices[kv_indptr[b+1] - 1], and appear in no
+ *                other request's list (a newly appended token is private)
+ *   k_new, v_new : [batch, n_kv_heads, head_dim] bf16, one new row per request
+ *   pool_slots : rows of each pool (used by the debug checks)
+ *   every request must have a non-empty context (its newest token); other
+ *   arguments as for paged_decode_attn. After the call, k_pool/v_pool hold the new
+ *   rows at slot_ids, bit-exact, and out/lse equal those of append-then-attend.
+ * With debug checks on, the precondition on slot_ids is verified on the host.
+ */
+int paged_decode_append_attn(const void* q, void* k_pool, void* v_pool, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, const int32_t* slot_ids, const void* k_new,
+                             const void* v_new, int batch, int n_qo_heads, int n_kv_heads,
+                             int head_dim, int64_t pool_slots, float sm_scale, void* out,
+                             float* lse, const pkv_plan* plan, pkv_stream_t stream);
 
 /*
  * paged_decode_attn_static — the same attention as paged_decode_attn, for callers

@@ -37,6 +37,7 @@ PKV_ERR_INDEX = -5
 EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",
             "paged_decode_plan_info", "paged_decode_plan_status", "paged_decode_attn_static",
+            "paged_decode_append_attn",
             "pkv_set_debug_checks", "pkv_last_error")
 
 
@@ -67,13 +68,16 @@ def _load() -> ctypes.CDLL:
     lib.paged_decode_plan_status.argtypes = [P, P]
     lib.paged_decode_attn_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32,
                                              ctypes.c_float, P, P, P]
+    lib.paged_decode_append_attn.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I64,
+                                             ctypes.c_float, P, P, P, P]
     lib.pkv_set_debug_checks.argtypes = [I32]
     lib.pkv_set_debug_checks.restype = None
     lib.pkv_last_error.argtypes = []
     lib.pkv_last_error.restype = ctypes.c_char_p
     for name in ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
                  "paged_decode_attn", "paged_decode_plan_host", "paged_decode_plan_info",
-                 "paged_decode_plan_status", "paged_decode_attn_static"):
+                 "paged_decode_plan_status", "paged_decode_attn_static",
+                 "paged_decode_append_attn"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -211,6 +215,24 @@ def paged_decode_attn(q, k_pool, v_pool, kv_indptr, kv_indices, batch, n_qo_head
                                   _ptr(kv_indices), batch, n_qo_heads, n_kv_heads, head_dim,
                                   float(sm_scale), _ptr(out), _ptr(lse), plan.handle,
                                   _stream(stream)))
+
+
+def paged_decode_append_attn(q, k_pool, v_pool, kv_indptr, kv_indices, slot_ids, k_new, v_new,
+                             batch, n_qo_heads, n_kv_heads, head_dim, sm_scale, out, lse,
+                             plan: Plan, stream=None) -> None:
+    """kvpool_append + paged_decode_attn in one launch; slot_ids[b] must be request
+    b's last listed slot (see include/pkv.h)."""
+    for t, name in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"), (k_new, "k_new"),
+                    (v_new, "v_new"), (out, "out")):
+        _dev(t, torch.bfloat16, name)
+    for t, name in ((kv_indptr, "kv_indptr"), (kv_indices, "kv_indices"), (slot_ids, "slot_ids")):
+        _dev(t, torch.int32, name)
+    if lse is not None:
+        _dev(lse, torch.float32, "lse")
+    _check(library().paged_decode_append_attn(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indptr), _ptr(kv_indices), _ptr(slot_ids),
+        _ptr(k_new), _ptr(v_new), batch, n_qo_heads, n_kv_heads, head_dim, k_pool.shape[0],
+        float(sm_scale), _ptr(out), _ptr(lse), plan.handle, _stream(stream)))
 
 
 def paged_decode_attn_static(q, k_pool, v_pool, kv_indptr_host, kv_indptr, kv_indices, batch,

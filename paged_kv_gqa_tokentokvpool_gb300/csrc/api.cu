@@ -294,48 +294,74 @@ int paged_decode_plan_status(pkv_plan* p, int* status) {
     return PKV_OK;
 }
 
-int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
-                      const int32_t* kv_indptr, const int32_t* kv_indices, int batch,
-                      int n_qo_heads, int n_kv_heads, int head_dim, float sm_scale, void* out,
-                      float* lse, const pkv_plan* p, pkv_stream_t stream) {
-    clear_error();
-    if (!p) return fail(PKV_ERR_PLAN, "paged_decode_attn: plan is NULL");
-    if (!p->planned) return fail(PKV_ERR_PLAN, "paged_decode_attn: paged_decode_plan was not run");
+namespace {
+
+// Shared by paged_decode_attn and paged_decode_append_attn: checks against the plan,
+// optional debug checks, then the decode (+ merge) launch.
+int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_pool,
+              const int32_t* kv_indptr, const int32_t* kv_indices, int batch, int n_qo_heads,
+              int n_kv_heads, int head_dim, float sm_scale, void* out, float* lse,
+              const pkv_plan* p, pkv_stream_t stream, const int32_t* slot_ids, const void* k_new,
+              const void* v_new, int64_t pool_slots) {
+    if (!p) return fail(PKV_ERR_PLAN, "%s: plan is NULL", who);
+    if (!p->planned) return fail(PKV_ERR_PLAN, "%s: paged_decode_plan was not run", who);
     if (n_qo_heads != p->n_qo_heads || n_kv_heads != p->n_kv_heads || head_dim != p->head_dim)
-        return fail(PKV_ERR_PLAN,
-                    "paged_decode_attn: shape (%d, %d, %d) differs from the plan's (%d, %d, %d)",
+        return fail(PKV_ERR_PLAN, "%s: shape (%d, %d, %d) differs from the plan's (%d, %d, %d)", who,
                     n_qo_heads, n_kv_heads, head_dim, p->n_qo_heads, p->n_kv_heads, p->head_dim);
     if (batch != p->batch)
-        return fail(PKV_ERR_PLAN, "paged_decode_attn: batch %d differs from the planned batch %d",
-                    batch, p->batch);
-    if (!std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn: sm_scale not finite");
+        return fail(PKV_ERR_PLAN, "%s: batch %d differs from the planned batch %d", who, batch,
+                    p->batch);
+    if (!std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "%s: sm_scale not finite", who);
     if (batch == 0) return PKV_OK;
     if (!q || !k_pool || !v_pool || !kv_indptr || !out || (!kv_indices && p->indptr_host[batch] > 0))
-        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn: NULL pointer argument");
+        return fail(PKV_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
-        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn: q, pools and out must be 16-byte aligned");
+        return fail(PKV_ERR_INVALID_ARG, "%s: q, pools and out must be 16-byte aligned", who);
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
-        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn: lse must be 4-byte aligned");
+        return fail(PKV_ERR_INVALID_ARG, "%s: lse must be 4-byte aligned", who);
+    const bool fused = slot_ids != nullptr;
+    if (fused) {
+        if (!k_new || !v_new) return fail(PKV_ERR_INVALID_ARG, "%s: NULL new rows", who);
+        if (!aligned16(k_new) || !aligned16(v_new))
+            return fail(PKV_ERR_INVALID_ARG, "%s: new rows must be 16-byte aligned", who);
+        for (int b = 0; b < batch; ++b)
+            if (p->indptr_host[b + 1] == p->indptr_host[b])
+                return fail(PKV_ERR_INVALID_ARG,
+                            "%s: request %d has an empty context, so it has no newest token", who, b);
+    }
     if (debug_checks()) {
         std::vector<int32_t> ip(batch + 1);
         cudaError_t e = cudaMemcpyAsync(ip.data(), kv_indptr, ip.size() * sizeof(int32_t),
                                         cudaMemcpyDeviceToHost, stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-        if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attn: debug copy of kv_indptr");
+        if (e != cudaSuccess) return cuda_fail(e, "debug copy of kv_indptr");
         for (int b = 0; b <= batch; ++b)
             if (ip[b] != p->indptr_host[b])
-                return fail(PKV_ERR_INDEX, "paged_decode_attn: kv_indptr[%d] = %d but the plan has %d",
-                            b, ip[b], p->indptr_host[b]);
+                return fail(PKV_ERR_INDEX, "%s: kv_indptr[%d] = %d but the plan has %d", who, b, ip[b],
+                            p->indptr_host[b]);
         const int32_t n = ip[batch];
+        std::vector<int32_t> idx(n > 0 ? n : 0);
         if (n > 0) {
-            std::vector<int32_t> idx(n);
             e = cudaMemcpyAsync(idx.data(), kv_indices, idx.size() * sizeof(int32_t),
                                 cudaMemcpyDeviceToHost, stream);
             if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-            if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attn: debug copy of kv_indices");
+            if (e != cudaSuccess) return cuda_fail(e, "debug copy of kv_indices");
             for (int32_t i = 0; i < n; ++i)
-                if (idx[i] < 0)
-                    return fail(PKV_ERR_INDEX, "paged_decode_attn: kv_indices[%d] = %d < 0", i, idx[i]);
+                if (idx[i] < 0 || (pool_slots > 0 && idx[i] >= pool_slots))
+                    return fail(PKV_ERR_INDEX, "%s: kv_indices[%d] = %d is not a pool slot", who, i,
+                                idx[i]);
+        }
+        if (fused) {
+            std::vector<int32_t> ids(batch);
+            e = cudaMemcpyAsync(ids.data(), slot_ids, ids.size() * sizeof(int32_t),
+                                cudaMemcpyDeviceToHost, stream);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return cuda_fail(e, "debug copy of slot_ids");
+            for (int b = 0; b < batch; ++b)
+                if (ids[b] != idx[ip[b + 1] - 1])
+                    return fail(PKV_ERR_INDEX,
+                                "%s: slot_ids[%d] = %d is not request %d's last listed slot (%d)",
+                                who, b, ids[b], b, idx[ip[b + 1] - 1]);
         }
     }
     const char* meta = static_cast<const char*>(p->dev_meta);
@@ -362,9 +388,38 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
     a.merge_ctas = p->num_sms;
     a.status = p->dev_state;
     a.zero_row = p->zero_row;
+    a.k_new = fused ? k_new : nullptr;
+    a.v_new = fused ? v_new : nullptr;
+    a.slot_ids = fused ? slot_ids : nullptr;
     cudaError_t e = launch_decode(a, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attn: launch");
+    if (e != cudaSuccess) return cuda_fail(e, "launch");
     return PKV_OK;
+}
+
+}  // namespace
+
+int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* kv_indptr, const int32_t* kv_indices, int batch,
+                      int n_qo_heads, int n_kv_heads, int head_dim, float sm_scale, void* out,
+                      float* lse, const pkv_plan* p, pkv_stream_t stream) {
+    clear_error();
+    return attn_impl("paged_decode_attn", q, k_pool, v_pool, kv_indptr, kv_indices, batch,
+                     n_qo_heads, n_kv_heads, head_dim, sm_scale, out, lse, p, stream, nullptr,
+                     nullptr, nullptr, 0);
+}
+
+int paged_decode_append_attn(const void* q, void* k_pool, void* v_pool, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, const int32_t* slot_ids, const void* k_new,
+                             const void* v_new, int batch, int n_qo_heads, int n_kv_heads,
+                             int head_dim, int64_t pool_slots, float sm_scale, void* out,
+                             float* lse, const pkv_plan* p, pkv_stream_t stream) {
+    clear_error();
+    if (!slot_ids) return fail(PKV_ERR_INVALID_ARG, "paged_decode_append_attn: slot_ids is NULL");
+    if (pool_slots <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_append_attn: pool_slots must be > 0");
+    return attn_impl("paged_decode_append_attn", q, k_pool, v_pool, kv_indptr, kv_indices, batch,
+                     n_qo_heads, n_kv_heads, head_dim, sm_scale, out, lse, p, stream, slot_ids,
+                     k_new, v_new, pool_slots);
 }
 
 }  // extern "C"

@@ -230,6 +230,8 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     const int tok = lane & (kTile - 1);
     const bool is_v = lane >= kTile;
     const char* pool = static_cast<const char*>(is_v ? a.v_pool : a.k_pool);
+    const bool fused = a.k_new != nullptr;
+    const char* new_rows = static_cast<const char*>(is_v ? a.v_new : a.k_new);
     const int64_t slot_bytes = int64_t(a.n_kv_heads) * D * 2;
     const uint32_t ring = smem_u32(smem) + (is_v ? C::kStageTokens * C::kRowP : 0) + tok * C::kRowP;
     int stage = 0;
@@ -276,6 +278,9 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                     const void* src = slot[j] >= 0
                                           ? static_cast<const void*>(pool + slot[j] * slot_bytes + group_off)
                                           : a.zero_row;
+                    // fused append: the request's newest token comes from its new row
+                    if (fused && un.tok_begin + t * C::kStageTokens + tok + kTile * j == un.len - 1)
+                        src = new_rows + un.b * slot_bytes + group_off;
                     bulk_g2s(ring + stage * C::kStage + j * kTile * C::kRowP, src, C::kRow, full_bar);
                 }
             }
@@ -315,6 +320,27 @@ __device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit
     for (int ks = 0; ks < C::kKSteps; ++ks) {
         qf[ks][0] = g < G ? __ldg(row + ks * 8) : 0u;
         qf[ks][1] = g < G ? __ldg(row + ks * 8 + 4) : 0u;
+    }
+}
+
+// Fused append: copy this warp's part (head hh, dims of `part`) of the staged new
+// K and V rows of request un.b from shared memory to pool slot slot_ids[un.b].
+template <int D, int G, int WPH>
+__device__ __forceinline__ void store_new_rows(const DecodeArgs& a, const Unit& un,
+                                               const uint8_t* smem, int stage, int row, int hh,
+                                               int part, int lane) {
+    using C = Cfg<D, G, WPH>;
+    constexpr int kBytes = C::kDimsPerWarp * 2;  // bytes of this warp's share of one row
+    const int64_t slot = __ldg(a.slot_ids + un.b);
+    const int64_t dst_off = slot * int64_t(a.n_kv_heads) * D * 2 +
+                            (int64_t(un.hg) * C::kHeadsPerCta + hh) * D * 2 + part * kBytes;
+    const uint8_t* src_row = smem + stage * C::kStage + row * C::kRowP + (hh * D) * 2 + part * kBytes;
+    for (int off = lane * 16; off < 2 * kBytes; off += 32 * 16) {
+        const bool is_v = off >= kBytes;
+        const int o = is_v ? off - kBytes : off;
+        const uint4 v = *reinterpret_cast<const uint4*>(src_row + (is_v ? C::kStageTokens * C::kRowP : 0) + o);
+        char* pool = static_cast<char*>(const_cast<void*>(is_v ? a.v_pool : a.k_pool));
+        *reinterpret_cast<uint4*>(pool + dst_off + o) = v;
     }
 }
 
@@ -368,6 +394,14 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             const bool ok = mbar_wait(smem_u32(&sh.full[stage]), full_parity, a.status, sh.flags);
             if (!__all_sync(kFull, ok)) return;  // uniform exit: no lane is left in a shuffle
             const int n_stage = n_tok - t * C::kStageTokens;
+            // Fused append: the stage holding the request's newest token has its new
+            // K/V rows (copied from k_new / v_new); write this warp's share of them
+            // to the pool slot before the stage is released.
+            if (a.k_new != nullptr) {
+                const int row = un.len - 1 - (un.tok_begin + t * C::kStageTokens);
+                if (row >= 0 && row < n_stage && row < C::kStageTokens)
+                    store_new_rows<D, G, WPH>(a, un, smem, stage, row, hh, part, lane);
+            }
 #pragma unroll
             for (int j = 0; j < C::kSub; ++j) {
                 const int n = n_stage - j * kTile;  // valid rows of this sub-tile (if > 0)

@@ -40,11 +40,12 @@ int choose_heads_per_cta(int n_kv_heads, int head_dim);
 // ---- plan ----------------------------------------------------------------
 // One work unit of the decode kernel: tokens [tok_begin, tok_end) of request b's
 // slot list, KV-head group hg; idx_begin = kv_indptr[b] + tok_begin is where the
-// unit's slot ids start in kv_indices. partial < 0: the unit covers the whole
-// context and writes out/lse; otherwise it writes partial slot `partial` of the
-// workspace and takes part in merge record `merge`.
+// unit's slot ids start in kv_indices, len = the request's context length.
+// partial < 0: the unit covers the whole context and writes out/lse; otherwise it
+// writes partial slot `partial` of the workspace and takes part in merge record
+// `merge`.
 struct Unit {
-    int32_t b, hg, tok_begin, tok_end, partial, merge, idx_begin, pad;
+    int32_t b, hg, tok_begin, tok_end, partial, merge, idx_begin, len;
 };
 // One split (request, head group): its parts occupy partial slots
 // [first, first + count).
@@ -95,6 +96,12 @@ struct DecodeArgs {
     int merge_ctas;       // grid of the merge kernel (fixed per plan)
     int* status;          // device status word (nonzero: a wait timed out)
     const void* zero_row; // kHeadGroupElems bf16 zeros (tile padding)
+    // Fused append (all three set, or all NULL): request b's last listed token is
+    // read from row b of k_new / v_new, and that row is written to pool slot
+    // slot_ids[b] (k_pool / v_pool are then written, despite the const).
+    const void* k_new;
+    const void* v_new;
+    const int32_t* slot_ids;
 };
 
 bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim);

@@ -134,7 +134,8 @@ int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, const
         const int b = pc.item / n_groups;
         all[u] = Unit{b, pc.item % n_groups, static_cast<int32_t>(pc.t0),
                       static_cast<int32_t>(pc.t1), m >= 0 ? next_slot[pc.item]++ : -1, m,
-                      static_cast<int32_t>(indptr[b] + pc.t0), 0};
+                      static_cast<int32_t>(indptr[b] + pc.t0),
+                      static_cast<int32_t>(start[pc.item + 1] - start[pc.item])};
     }
 
     // 3. per-CTA lists: split pieces first, then whole items

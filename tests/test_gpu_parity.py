@@ -236,11 +236,13 @@ def test_errors_do_not_launch(pkv):
 FULL = {1: None, 2: None, 3: [0, 35], 4: [0, 7], 5: None}
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_append", "separate_append"])
 @pytest.mark.parametrize("config_no", sorted(FULL))
-def test_full_size_config(pkv, config_no):
+def test_full_size_config(pkv, config_no, fused):
     import bench
     wl = workloads.config_workload(config_no)
-    st = bench.StepState(wl, layers=FULL[config_no], poison_unreferenced=True)
+    st = bench.StepState(wl, layers=FULL[config_no], poison_unreferenced=True, fused=fused)
+    assert st.fused == fused
     uniq, inv = np.unique(wl.kv_indices, return_inverse=True)
     compact = inv.astype(np.int32)
     uniq_dev = torch.from_numpy(uniq.astype(np.int64)).cuda()
@@ -346,3 +348,78 @@ def test_graph_replay_after_replanning(pkv):
             assert_parity(to_f64(out[l]), lse[l].cpu().numpy(), ref_out, ref_lse,
                           what=f"graph step {step} layer {l}")
     assert plan.status() == 0
+
+
+FUSED_CASES = [
+    ([1], 32, 8, 128),
+    ([1, 2, 3, 17, 300, 1000, 5, 64, 65], 32, 8, 128),
+    ([20000, 7, 3000], 32, 8, 128),
+    ([1, 255, 256, 257, 12345], 16, 4, 256),
+    ([100, 2000], 8, 8, 128),
+    ([100, 5000], 64, 8, 128),
+    ([77, 3001], 8, 1, 256),
+    ([513] * 40, 32, 8, 128),
+]
+
+
+@pytest.mark.parametrize("case", range(len(FUSED_CASES)))
+def test_fused_append_attention(pkv, case):
+    """paged_decode_append_attn == kvpool_append then paged_decode_attn (oracle side:
+    the oracle's append, then the oracle's attention)."""
+    lengths, hq, hkv, d = FUSED_CASES[case]
+    wl = workloads.scattered_workload(lengths, n_qo_heads=hq, n_kv_heads=hkv, head_dim=d,
+                                      seed=400 + case)
+    t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
+    dev = torch.device("cuda")
+    kp, vp = t.k_pool.to(dev), t.v_pool.to(dev)
+    out = torch.full((wl.batch, hq, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((wl.batch, hq), float("nan"), dtype=torch.float32, device=dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, hq, hkv, d)
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    pkv.pkv_set_debug_checks(case % 2 == 0)
+    try:
+        pkv.paged_decode_append_attn(t.q.to(dev), kp, vp, torch.from_numpy(wl.kv_indptr).to(dev),
+                                     torch.from_numpy(wl.kv_indices).to(dev),
+                                     torch.from_numpy(wl.append_slots).to(dev), t.k_new.to(dev),
+                                     t.v_new.to(dev), wl.batch, hq, hkv, d, wl.sm_scale, out, lse,
+                                     plan)
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    k_ref = oracle.append(bits(t.k_pool), wl.append_slots, bits(t.k_new))
+    v_ref = oracle.append(bits(t.v_pool), wl.append_slots, bits(t.v_new))
+    assert np.array_equal(bits(kp), k_ref) and np.array_equal(bits(vp), v_ref)
+    ref_out, ref_lse = oracle.decode(bits(t.q), k_ref, v_ref, wl.kv_indptr, wl.kv_indices, hq,
+                                     hkv, d, wl.sm_scale)
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what=f"fused case {case}")
+    assert plan.status() == 0
+
+
+def test_fused_append_rejects_bad_calls(pkv):
+    dev = torch.device("cuda")
+    wl = workloads.scattered_workload([5, 0, 7], seed=5)
+    plan = pkv.paged_decode_plan_create(3, 12, 32, 8, 128)
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    z = torch.zeros(3, 32, 128, dtype=torch.bfloat16, device=dev)
+    pool = torch.zeros(64, 8, 128, dtype=torch.bfloat16, device=dev)
+    rows = torch.zeros(3, 8, 128, dtype=torch.bfloat16, device=dev)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx = torch.from_numpy(wl.kv_indices).to(dev)
+    slots = torch.zeros(3, dtype=torch.int32, device=dev)
+    with pytest.raises(pkv.PkvError) as e:  # request 1 has no newest token
+        pkv.paged_decode_append_attn(z, pool, pool, ip, idx, slots, rows, rows, 3, 32, 8, 128,
+                                     0.1, z, None, plan)
+    assert e.value.code == pkv.PKV_ERR_INVALID_ARG
+    wl = workloads.scattered_workload([5, 3, 7], pool_slots=64, seed=6)
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx = torch.from_numpy(wl.kv_indices).to(dev)
+    bad = torch.from_numpy(wl.append_slots[::-1].copy()).to(dev)  # not each request's last slot
+    pkv.pkv_set_debug_checks(True)
+    try:
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.paged_decode_append_attn(z, pool, pool, ip, idx, bad, rows, rows, 3, 32, 8, 128,
+                                         0.1, z, None, plan)
+        assert e.value.code == pkv.PKV_ERR_INDEX
+    finally:
+        pkv.pkv_set_debug_checks(False)
