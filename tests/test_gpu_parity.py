@@ -398,7 +398,7 @@ def test_fused_append_attention(pkv, case):
 def test_fused_append_rejects_bad_calls(pkv):
     dev = torch.device("cuda")
     wl = workloads.scattered_workload([5, 0, 7], seed=5)
-    plan = pkv.paged_decode_plan_create(3, 12, 32, 8, 128)
+    plan = pkv.paged_decode_plan_create(3, 20, 32, 8, 128)
     pkv.paged_decode_plan(plan, wl.kv_indptr)
     z = torch.zeros(3, 32, 128, dtype=torch.bfloat16, device=dev)
     pool = torch.zeros(64, 8, 128, dtype=torch.bfloat16, device=dev)
