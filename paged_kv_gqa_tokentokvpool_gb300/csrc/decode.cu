@@ -550,8 +550,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeA
 // c = lane, lane + 32, ... to form the merged log-sum-exp (online max/sum, then a
 // warp reduction), then every lane owns head_dim/32 consecutive dimensions and
 // sums w_c * out_c over all parts, with w_c = 2^(lse_c - lse) broadcast from the
-// lane that read part c. Launched right after the decode kernel on a fixed grid
-// (warps loop over the work), so the launch does not depend on the step.
+// lane that read part c; the parts' loads of a chunk of 16 (8 at head_dim 256)
+// are all issued before any is used. Launched right after the decode kernel on a
+// fixed grid (warps loop over the work), so the launch does not depend on the step.
 constexpr int kMergeThreads = 128;
 
 template <int D>
@@ -590,21 +591,29 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeAr
 #pragma unroll
         for (int i = 0; i < kVD; ++i) acc[i] = 0.f;
         const float* o_p = a.ws_o + (int64_t(mg.first) * qheads + qh) * D + lane * kVD;
-        for (int c0 = 0; c0 < mg.count; c0 += 32) {
-            const int c = c0 + lane;
+        // Parts in chunks of kChunk: every load of a chunk is issued before the first
+        // use, so a chunk costs one round trip to L2.
+        constexpr int kChunk = kVD == 4 ? 16 : 8;
+        for (int c0 = 0; c0 < mg.count; c0 += kChunk) {
+            const int c = c0 + (lane % kChunk);
             const float wl = c < mg.count ? ex2(__ldcg(lse_p + int64_t(c) * qheads) - total) : 0.f;
-            const int n = min(32, mg.count - c0);
-#pragma unroll 8
-            for (int j = 0; j < n; ++j) {
-                const float wj = __shfl_sync(kFull, wl, j);
-                const float* src = o_p + int64_t(c0 + j) * qheads * D;
+            float4 x[kChunk][kVD / 4];
 #pragma unroll
-                for (int i = 0; i < kVD; i += 4) {
-                    const float4 x = __ldcg(reinterpret_cast<const float4*>(src + i));
-                    acc[i] = fmaf(wj, x.x, acc[i]);
-                    acc[i + 1] = fmaf(wj, x.y, acc[i + 1]);
-                    acc[i + 2] = fmaf(wj, x.z, acc[i + 2]);
-                    acc[i + 3] = fmaf(wj, x.w, acc[i + 3]);
+            for (int j = 0; j < kChunk; ++j)
+#pragma unroll
+                for (int i = 0; i < kVD / 4; ++i)
+                    x[j][i] = c0 + j < mg.count
+                                  ? __ldcg(reinterpret_cast<const float4*>(o_p + int64_t(c0 + j) * qheads * D) + i)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+                const float wj = __shfl_sync(kFull, wl, j);
+#pragma unroll
+                for (int i = 0; i < kVD / 4; ++i) {
+                    acc[4 * i] = fmaf(wj, x[j][i].x, acc[4 * i]);
+                    acc[4 * i + 1] = fmaf(wj, x[j][i].y, acc[4 * i + 1]);
+                    acc[4 * i + 2] = fmaf(wj, x[j][i].z, acc[4 * i + 2]);
+                    acc[4 * i + 3] = fmaf(wj, x[j][i].w, acc[4 * i + 3]);
                 }
             }
         }
