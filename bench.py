@@ -46,7 +46,7 @@ class StepState:
     """Device tensors of one decode step for every layer, plus the plan."""
 
     def __init__(self, wl: workloads.Workload, device="cuda", layers=None,
-                 poison_unreferenced=False, fused=None):
+                 poison_unreferenced=False, fused=None, share=True):
         import paged_kv_gqa_tokentokvpool_gb300 as pkv
         self.pkv = pkv
         self.wl = wl
@@ -77,6 +77,15 @@ class StepState:
         # newest token that is its last listed slot (the decode steps here).
         can_fuse = len(wl.append_slots) == wl.batch and wl.batch > 0
         self.fused = can_fuse if fused is None else (fused and can_fuse)
+        # Requests that list the same prefix slots (the prefix-sharing workload) are
+        # described to the planner, which then reads each shared slot once for
+        # several requests.
+        self.sharing = None
+        if share and "prefix_lens" in wl.meta:
+            gs = wl.meta["group_size"]
+            n = len(wl.meta["prefix_lens"])
+            self.sharing = (np.arange(0, gs * n + 1, gs, dtype=np.int32),
+                            np.asarray(wl.meta["prefix_lens"], dtype=np.int32))
 
     def layers(self, attn_events=None):
         """Every layer's KV append and decode attention, on the current stream.
@@ -114,7 +123,11 @@ class StepState:
         there is one (and no per-call events are asked for)."""
         pkv = self.pkv
         stream = torch.cuda.current_stream()
-        pkv.paged_decode_plan(self.plan, self.kv_indptr_host.numpy(), stream=stream)
+        if self.sharing is not None:
+            pkv.paged_decode_plan_shared(self.plan, self.kv_indptr_host.numpy(), self.sharing[0],
+                                         self.sharing[1], stream=stream)
+        else:
+            pkv.paged_decode_plan(self.plan, self.kv_indptr_host.numpy(), stream=stream)
         if self.graph is not None and attn_events is None:
             self.graph.replay()
         else:
@@ -403,6 +416,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--separate-append", action="store_true",
                     help="run kvpool_append as its own kernel before each attention call")
+    ap.add_argument("--no-share", action="store_true",
+                    help="plan the prefix-sharing workload without describing its shared prefixes")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every layer eagerly instead of replaying a CUDA graph")
     ap.add_argument("--layers", type=int, default=None,
@@ -426,7 +441,7 @@ def main(argv=None):
     if args.layers is not None:
         wl.layers = max(1, min(args.layers, wl.layers))
         wl.description += f" [first {wl.layers} layers only]"
-    st = StepState(wl, fused=not args.separate_append)
+    st = StepState(wl, fused=not args.separate_append, share=not args.no_share)
     if not args.no_graph:
         st.capture()
     nbytes = step_bytes(wl)
@@ -514,6 +529,7 @@ def main(argv=None):
             "parallelism": f"replicas x{world}",
             "launch": "eager" if args.no_graph else "cuda graph of the layer loop per step; plan on host",
             "append": "fused into the attention launch" if st.fused else "separate kernel",
+            "shared_prefixes": "described to the planner" if st.sharing is not None else "none",
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -112,6 +112,25 @@ int paged_decode_plan(pkv_plan* plan, const int32_t* kv_indptr_host, int batch,
                       pkv_stream_t stream);
 
 /*
+ * paged_decode_plan_shared — paged_decode_plan for a step in which runs of
+ * consecutive requests list the same first slots (a shared prompt prefix, as the
+ * prefix cache of "Agent-Infer", section "前缀缓存", produces). Requests
+ * [shared_indptr_host[s], shared_indptr_host[s+1]) all list the same
+ * shared_len_host[s] slot ids first, s < n_shared; the runs are disjoint and in
+ * batch order, and every member lists more slots than its shared prefix (its
+ * newest token is private). The attention kernel then reads each shared slot once
+ * for up to 16 / G requests at a time (two 8-row query blocks per KV head) instead
+ * of once per request, and merges each member's prefix and suffix parts by
+ * log-sum-exp. The description is a hint about equal slot ids: results are the
+ * same as with paged_decode_plan (up to fp32 rounding), and for shapes without a
+ * shared-prefix kernel (only head_dim 128 with 4 KV heads per group has one) it is
+ * ignored. Otherwise as paged_decode_plan.
+ */
+int paged_decode_plan_shared(pkv_plan* plan, const int32_t* kv_indptr_host, int batch,
+                             const int32_t* shared_indptr_host, int n_shared,
+                             const int32_t* shared_len_host, pkv_stream_t stream);
+
+/*
  * paged_decode_attn — batched decode attention over the token pool, once per layer.
  * For every request b and query head h, with g = h / (n_qo_heads / n_kv_heads) and
  * idx = kv_indices[kv_indptr[b] .. kv_indptr[b+1]):
@@ -193,33 +212,42 @@ void paged_decode_plan_destroy(pkv_plan* plan);
 
 /*
  * paged_decode_plan_host — the planner alone, on the host, with no CUDA call.
- * Computes the work list paged_decode_plan would upload, for inspection and tests.
- * The work of one layer is every (request, KV-head group) pair, a group being
- * heads_per_cta consecutive KV heads. The pairs are laid end to end and cut into
- * `ctas` ranges of equal token count (fewer for a small step); a context is split
- * only where a range boundary falls inside it.
+ * Computes the work list paged_decode_plan / paged_decode_plan_shared would upload,
+ * for inspection and tests. The work of one layer is a list of items, each a run of
+ * slots of one KV-head group (heads_per_cta consecutive KV heads) attended by one
+ * request, or, for a shared prefix, by up to requests_per_unit requests of a
+ * sharing group; the items are laid end to end and cut into `ctas` ranges of equal
+ * token count (fewer for a small step); a run is split only where a range boundary
+ * falls inside it.
  *   kv_indptr_host : [batch + 1] int32
  *   n_kv_heads, head_dim : the attention shape
  *   heads_per_cta  : KV heads per group: 1, 2 or 4, at most 512 / head_dim and
  *                    dividing n_kv_heads; 0 = the largest allowed
  *   ctas           : persistent CTAs (SMs x resident CTAs per SM on the device)
+ *   shared_indptr_host, n_shared, shared_len_host, requests_per_unit : sharing
+ *                    groups as for paged_decode_plan_shared (n_shared = 0: none)
  *   units_out      : [max_units * 8] int32 — per unit {request b, head group,
- *                    first token, end token (exclusive), partial slot or -1 when
- *                    the unit writes out/lse directly, merge record or -1,
- *                    kv_indptr[b] + first token, 0}, listed CTA by CTA
+ *                    first token, end token (exclusive), first partial slot or -1
+ *                    when the unit writes out/lse directly, requests served,
+ *                    kv_indptr[b] + first token, context length of b or -1 for a
+ *                    shared prefix}, listed CTA by CTA
  *   cta_begin_out  : [ctas + 1] int32 — CTA c runs units [cta_begin[c], cta_begin[c+1]);
  *                    every CTA of the grid has an entry (possibly an empty range)
- *   merges_out     : [max_merges * 4] int32 — per split (request, head group)
- *                    {request b, head group, first partial slot, number of parts}
+ *   merges_out     : [max_merges * 4] int32 — per (request, head group) with partial
+ *                    results {request, head group, first entry in the part list,
+ *                    number of parts}
+ *   part_list_out  : [max_partials] int32 — partial slots named by the merges
  *   counts_out     : [5] int32 — {units, CTAs with work, merge records, partial
  *                    slots, tokens per CTA range}
  * Returns PKV_ERR_PLAN if an output array is too small.
  */
 int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_heads,
-                           int head_dim, int heads_per_cta, int ctas, int32_t* units_out,
-                           int max_units,
-                           int32_t* cta_begin_out, int32_t* merges_out, int max_merges,
-                           int32_t* counts_out);
+                           int head_dim, int heads_per_cta, int ctas,
+                           const int32_t* shared_indptr_host, int n_shared,
+                           const int32_t* shared_len_host, int requests_per_unit,
+                           int32_t* units_out, int max_units, int32_t* cta_begin_out,
+                           int32_t* merges_out, int max_merges, int32_t* part_list_out,
+                           int max_partials, int32_t* counts_out);
 
 /* paged_decode_plan_info — counts of the plan's current step (any out pointer may be NULL). */
 int paged_decode_plan_info(const pkv_plan* plan, int* batch, int* n_units, int* n_merges,

@@ -37,7 +37,7 @@ PKV_ERR_INDEX = -5
 EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",
             "paged_decode_plan_info", "paged_decode_plan_status", "paged_decode_attn_static",
-            "paged_decode_append_attn",
+            "paged_decode_append_attn", "paged_decode_plan_shared",
             "pkv_set_debug_checks", "pkv_last_error")
 
 
@@ -63,7 +63,9 @@ def _load() -> ctypes.CDLL:
                                       P, P]
     lib.paged_decode_plan_destroy.argtypes = [P]
     lib.paged_decode_plan_destroy.restype = None
-    lib.paged_decode_plan_host.argtypes = [P, I32, I32, I32, I32, I32, P, I32, P, P, I32, P]
+    lib.paged_decode_plan_host.argtypes = [P, I32, I32, I32, I32, I32, P, I32, P, I32, P, I32, P,
+                                           P, I32, P, I32, P]
+    lib.paged_decode_plan_shared.argtypes = [P, P, I32, P, I32, P, P]
     lib.paged_decode_plan_info.argtypes = [P, P, P, P, P, P]
     lib.paged_decode_plan_status.argtypes = [P, P]
     lib.paged_decode_attn_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32,
@@ -77,7 +79,7 @@ def _load() -> ctypes.CDLL:
     for name in ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
                  "paged_decode_attn", "paged_decode_plan_host", "paged_decode_plan_info",
                  "paged_decode_plan_status", "paged_decode_attn_static",
-                 "paged_decode_append_attn"):
+                 "paged_decode_append_attn", "paged_decode_plan_shared"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -200,6 +202,19 @@ def paged_decode_plan(plan: Plan, kv_indptr_host, batch=None, stream=None) -> No
     _check(library().paged_decode_plan(plan.handle, _ptr(ip), batch, _stream(stream)))
 
 
+def paged_decode_plan_shared(plan: Plan, kv_indptr_host, shared_indptr_host, shared_len_host,
+                             batch=None, stream=None) -> None:
+    """paged_decode_plan with sharing groups: requests [shared_indptr[s],
+    shared_indptr[s+1]) list the same first shared_len[s] slots."""
+    ip = _host_indptr(kv_indptr_host)
+    sp = np.ascontiguousarray(shared_indptr_host, dtype=np.int32)
+    sl = np.ascontiguousarray(shared_len_host, dtype=np.int32)
+    batch = ip.size - 1 if batch is None else batch
+    plan._indptr_keepalive = (ip, sp, sl)
+    _check(library().paged_decode_plan_shared(plan.handle, _ptr(ip), batch, _ptr(sp),
+                                              max(sp.size - 1, 0), _ptr(sl), _stream(stream)))
+
+
 def paged_decode_attn(q, k_pool, v_pool, kv_indptr, kv_indices, batch, n_qo_heads,
                       n_kv_heads, head_dim, sm_scale, out, lse, plan: Plan,
                       stream=None) -> None:
@@ -263,26 +278,36 @@ def paged_decode_plan_destroy(plan: Plan) -> None:
 
 
 def paged_decode_plan_host(kv_indptr_host, n_kv_heads: int, head_dim: int, ctas: int,
-                           heads_per_cta: int = 0, max_units: int = None, max_merges: int = None):
+                           heads_per_cta: int = 0, shared_indptr=None, shared_len=None,
+                           requests_per_unit: int = 0, max_units: int = None,
+                           max_merges: int = None, max_partials: int = None):
     """The planner alone (host, no CUDA).
 
-    Returns dict(units [n, 8], cta_begin [c + 1], merges [m, 4], partials, chunk)."""
+    Returns dict(units [n, 8], cta_begin [ctas + 1], merges [m, 4], part_list,
+    partials, chunk, ctas_used)."""
     ip = _host_indptr(kv_indptr_host)
     batch = ip.size - 1
     hpc = heads_per_cta or min(n_kv_heads, 512 // head_dim)
     groups = max(1, n_kv_heads // max(1, hpc))
     if max_units is None:
-        max_units = 2 * ctas + max(batch, 1) * groups
+        max_units = 2 * ctas + 2 * max(batch, 1) * groups
     if max_merges is None:
         max_merges = max(batch, 1) * groups
+    if max_partials is None:
+        max_partials = max_units * max(1, requests_per_unit)
+    sp = np.ascontiguousarray(shared_indptr if shared_indptr is not None else [0], np.int32)
+    sl = np.ascontiguousarray(shared_len if shared_len is not None else [0], np.int32)
+    n_shared = sp.size - 1
     units = np.zeros((max(max_units, 1), 8), np.int32)
     cta_begin = np.zeros(ctas + 1, np.int32)
     merges = np.zeros((max(max_merges, 1), 4), np.int32)
+    part_list = np.zeros(max(max_partials, 1), np.int32)
     counts = np.zeros(5, np.int32)
-    _check(library().paged_decode_plan_host(_ptr(ip), batch, n_kv_heads, head_dim,
-                                            heads_per_cta, ctas,
-                                            _ptr(units), max_units, _ptr(cta_begin),
-                                            _ptr(merges), max_merges, _ptr(counts)))
+    _check(library().paged_decode_plan_host(
+        _ptr(ip), batch, n_kv_heads, head_dim, heads_per_cta, ctas, _ptr(sp), n_shared, _ptr(sl),
+        requests_per_unit, _ptr(units), max_units, _ptr(cta_begin), _ptr(merges), max_merges,
+        _ptr(part_list), max_partials, _ptr(counts)))
     nu, nc, nm, npart, chunk = (int(x) for x in counts)
     return {"units": units[:nu].copy(), "cta_begin": cta_begin.copy(), "ctas_used": nc,
-            "merges": merges[:nm].copy(), "partials": npart, "chunk": chunk}
+            "merges": merges[:nm].copy(), "part_list": part_list[:npart].copy(),
+            "partials": npart, "chunk": chunk}

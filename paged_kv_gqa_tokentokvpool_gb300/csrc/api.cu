@@ -113,14 +113,45 @@ int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const voi
     return PKV_OK;
 }
 
+namespace {
+
+// Checks a sharing description against the step's contexts: runs of consecutive
+// requests, each member listing at least len + 1 slots (its newest token stays
+// private). Returns PKV_OK or an error code with the message set.
+int check_sharing(const char* who, const int32_t* kv_indptr_host, int batch,
+                  const int32_t* shared_indptr_host, int n_shared, const int32_t* shared_len_host) {
+    if (n_shared < 0) return fail(PKV_ERR_INVALID_ARG, "%s: n_shared %d < 0", who, n_shared);
+    if (n_shared == 0) return PKV_OK;
+    if (!shared_indptr_host || !shared_len_host)
+        return fail(PKV_ERR_INVALID_ARG, "%s: NULL sharing arrays", who);
+    for (int s = 0; s < n_shared; ++s) {
+        const int m0 = shared_indptr_host[s], m1 = shared_indptr_host[s + 1];
+        if (m0 < 0 || m1 < m0 || m1 > batch)
+            return fail(PKV_ERR_INVALID_ARG, "%s: shared_indptr is not a non-decreasing run in [0, %d]",
+                        who, batch);
+        if (shared_len_host[s] < 0)
+            return fail(PKV_ERR_INVALID_ARG, "%s: shared_len[%d] < 0", who, s);
+        for (int b = m0; b < m1; ++b)
+            if (kv_indptr_host[b + 1] - kv_indptr_host[b] <= shared_len_host[s])
+                return fail(PKV_ERR_INVALID_ARG,
+                            "%s: request %d lists %d slots, not more than its shared prefix of %d",
+                            who, b, kv_indptr_host[b + 1] - kv_indptr_host[b], shared_len_host[s]);
+    }
+    return PKV_OK;
+}
+
+}  // namespace
+
 int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_heads,
-                           int head_dim, int heads_per_cta, int ctas, int32_t* units_out,
-                           int max_units,
-                           int32_t* cta_begin_out, int32_t* merges_out, int max_merges,
-                           int32_t* counts_out) {
+                           int head_dim, int heads_per_cta, int ctas,
+                           const int32_t* shared_indptr_host, int n_shared,
+                           const int32_t* shared_len_host, int requests_per_unit,
+                           int32_t* units_out, int max_units, int32_t* cta_begin_out,
+                           int32_t* merges_out, int max_merges, int32_t* part_list_out,
+                           int max_partials, int32_t* counts_out) {
     clear_error();
     if (!counts_out || (max_units > 0 && !units_out) || !cta_begin_out ||
-        (max_merges > 0 && !merges_out))
+        (max_merges > 0 && !merges_out) || (max_partials > 0 && !part_list_out))
         return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: NULL output");
     if (ctas <= 0 || n_kv_heads <= 0 || head_dim <= 0)
         return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: ctas, n_kv_heads, head_dim must be > 0");
@@ -129,10 +160,18 @@ int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_he
         return fail(PKV_ERR_UNSUPPORTED,
                     "paged_decode_plan_host: %d KV heads per group do not fit %d heads of dim %d",
                     hpg, n_kv_heads, head_dim);
+    if (batch > 0 && !kv_indptr_host)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_host: kv_indptr_host is NULL");
+    int rc = check_sharing("paged_decode_plan_host", kv_indptr_host, batch, shared_indptr_host,
+                           n_shared, shared_len_host);
+    if (rc != PKV_OK) return rc;
+    const PlanSharing sh{shared_indptr_host, shared_len_host, n_shared,
+                         requests_per_unit > 0 ? requests_per_unit : 1};
     PlanCounts c{};
-    int rc = plan_compute(kv_indptr_host, batch, n_kv_heads / hpg, ctas,
-                          PlanLimits{max_units, max_merges}, reinterpret_cast<Unit*>(units_out),
-                          cta_begin_out, reinterpret_cast<Merge*>(merges_out), &c);
+    rc = plan_compute(kv_indptr_host, batch, n_kv_heads / hpg, ctas,
+                      PlanLimits{max_units, max_merges, max_partials}, n_shared > 0 ? &sh : nullptr,
+                      reinterpret_cast<Unit*>(units_out), cta_begin_out,
+                      reinterpret_cast<Merge*>(merges_out), part_list_out, &c);
     if (rc != PKV_OK) return rc;
     counts_out[0] = c.n_units;
     counts_out[1] = c.n_ctas;
@@ -189,7 +228,15 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     }
     const int hpg = choose_heads_per_cta(n_kv_heads, head_dim);
     p->heads_per_cta = hpg;
-    p->ctas_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg);
+    // Shared-prefix units serve 16 / G requests (two 8-row query blocks per KV head)
+    // where a kernel for them exists; both kernels run on the same fixed grid.
+    p->share_rows = decode_has_shared_kernel(n_qo_heads, n_kv_heads, head_dim, hpg)
+                        ? 16 / (n_qo_heads / n_kv_heads)
+                        : 0;
+    p->ctas_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg, 1);
+    if (p->share_rows > 0)
+        p->ctas_per_sm = std::min(p->ctas_per_sm,
+                                  decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg, 2));
     if (p->ctas_per_sm <= 0) {
         delete p;
         return fail(PKV_ERR_CUDA, "paged_decode_plan_create: occupancy query failed");
@@ -203,15 +250,18 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     p->n_groups = n_kv_heads / hpg;
     p->lim.max_units = plan_max_units(p->ctas, max_batch, p->n_groups);
     p->lim.max_merges = max_batch * p->n_groups;
+    p->lim.max_partials = p->lim.max_units * std::max(1, p->share_rows);
     p->indptr_host.reserve(max_batch + 1);
-    // staging layout: header[4] | cta_begin[ctas + 1] | merges[max_merges] | units[max_units]
+    // staging layout: header[4] | cta_begin[ctas + 1] | merges[max_merges] |
+    //                 part_list[max_partials] | units[max_units]
     p->off_cta = 16;
     p->off_merge = round16(p->off_cta + sizeof(int32_t) * (p->ctas + 1));
-    p->off_units = round16(p->off_merge + sizeof(Merge) * p->lim.max_merges);
+    p->off_list = round16(p->off_merge + sizeof(Merge) * p->lim.max_merges);
+    p->off_units = round16(p->off_list + sizeof(int32_t) * p->lim.max_partials);
     p->meta_bytes = p->off_units + sizeof(Unit) * p->lim.max_units;
     const int group_q_heads = hpg * (n_qo_heads / n_kv_heads);
-    const size_t ws_o_bytes = sizeof(float) * size_t(p->lim.max_units) * group_q_heads * head_dim;
-    const size_t ws_lse_bytes = sizeof(float) * size_t(p->lim.max_units) * group_q_heads;
+    const size_t ws_o_bytes = sizeof(float) * size_t(p->lim.max_partials) * group_q_heads * head_dim;
+    const size_t ws_lse_bytes = sizeof(float) * size_t(p->lim.max_partials) * group_q_heads;
     const size_t state_bytes = sizeof(int) * 32;
     e = cudaMallocHost(&p->host_staging, p->meta_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&p->dev_meta, p->meta_bytes);
@@ -231,28 +281,45 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     return PKV_OK;
 }
 
-int paged_decode_plan(pkv_plan* p, const int32_t* kv_indptr_host, int batch, pkv_stream_t stream) {
-    clear_error();
-    if (!p) return fail(PKV_ERR_PLAN, "paged_decode_plan: plan is NULL");
+namespace {
+
+int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int batch,
+              const int32_t* shared_indptr_host, int n_shared, const int32_t* shared_len_host,
+              pkv_stream_t stream) {
+    if (!p) return fail(PKV_ERR_PLAN, "%s: plan is NULL", who);
     p->planned = false;
     if (batch < 0 || batch > p->max_batch)
-        return fail(PKV_ERR_PLAN, "paged_decode_plan: batch %d outside [0, %d]", batch, p->max_batch);
-    if (!kv_indptr_host) return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan: kv_indptr_host is NULL");
+        return fail(PKV_ERR_PLAN, "%s: batch %d outside [0, %d]", who, batch, p->max_batch);
+    if (!kv_indptr_host) return fail(PKV_ERR_INVALID_ARG, "%s: kv_indptr_host is NULL", who);
     if (int64_t(kv_indptr_host[batch]) > p->max_tokens)
-        return fail(PKV_ERR_PLAN, "paged_decode_plan: %d tokens exceed the plan's max_tokens %lld",
+        return fail(PKV_ERR_PLAN, "%s: %d tokens exceed the plan's max_tokens %lld", who,
                     kv_indptr_host[batch], (long long)p->max_tokens);
+    if (kv_indptr_host[0] != 0)
+        return fail(PKV_ERR_INVALID_ARG, "%s: kv_indptr[0] = %d, expected 0", who, kv_indptr_host[0]);
+    for (int b = 0; b < batch; ++b)
+        if (kv_indptr_host[b + 1] < kv_indptr_host[b])
+            return fail(PKV_ERR_INVALID_ARG, "%s: kv_indptr decreases at %d", who, b);
+    int rc = check_sharing(who, kv_indptr_host, batch, shared_indptr_host, n_shared,
+                           shared_len_host);
+    if (rc != PKV_OK) return rc;
+    bool share = false;
+    if (p->share_rows > 0)
+        for (int s = 0; s < n_shared; ++s)
+            share |= shared_len_host[s] > 0 && shared_indptr_host[s + 1] > shared_indptr_host[s];
+    const PlanSharing sh{shared_indptr_host, shared_len_host, n_shared, p->share_rows};
     // The staging buffer may still feed the previous step's copy.
     if (p->copy_pending) {
         cudaError_t e = cudaEventSynchronize(p->copy_done);
-        if (e != cudaSuccess) return cuda_fail(e, "paged_decode_plan: waiting for the previous copy");
+        if (e != cudaSuccess) return cuda_fail(e, "waiting for the previous plan copy");
         p->copy_pending = false;
     }
     char* st = static_cast<char*>(p->host_staging);
     PlanCounts c{};
-    int rc = plan_compute(kv_indptr_host, batch, p->n_groups, p->ctas, p->lim,
-                          reinterpret_cast<Unit*>(st + p->off_units),
-                          reinterpret_cast<int32_t*>(st + p->off_cta),
-                          reinterpret_cast<Merge*>(st + p->off_merge), &c);
+    rc = plan_compute(kv_indptr_host, batch, p->n_groups, p->ctas, p->lim, share ? &sh : nullptr,
+                      reinterpret_cast<Unit*>(st + p->off_units),
+                      reinterpret_cast<int32_t*>(st + p->off_cta),
+                      reinterpret_cast<Merge*>(st + p->off_merge),
+                      reinterpret_cast<int32_t*>(st + p->off_list), &c);
     if (rc != PKV_OK) return rc;
     int32_t* header = reinterpret_cast<int32_t*>(st);
     header[0] = c.n_merges;
@@ -261,13 +328,29 @@ int paged_decode_plan(pkv_plan* p, const int32_t* kv_indptr_host, int batch, pkv
     const size_t bytes = p->off_units + sizeof(Unit) * c.n_units;
     cudaError_t e = cudaMemcpyAsync(p->dev_meta, st, bytes, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaEventRecord(p->copy_done, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_plan: upload");
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
     p->copy_pending = true;
     p->batch = batch;
     p->counts = c;
+    p->n_blocks = share ? 2 : 1;
     p->indptr_host.assign(kv_indptr_host, kv_indptr_host + batch + 1);
     p->planned = true;
     return PKV_OK;
+}
+
+}  // namespace
+
+int paged_decode_plan(pkv_plan* p, const int32_t* kv_indptr_host, int batch, pkv_stream_t stream) {
+    clear_error();
+    return plan_impl("paged_decode_plan", p, kv_indptr_host, batch, nullptr, 0, nullptr, stream);
+}
+
+int paged_decode_plan_shared(pkv_plan* p, const int32_t* kv_indptr_host, int batch,
+                             const int32_t* shared_indptr_host, int n_shared,
+                             const int32_t* shared_len_host, pkv_stream_t stream) {
+    clear_error();
+    return plan_impl("paged_decode_plan_shared", p, kv_indptr_host, batch, shared_indptr_host,
+                     n_shared, shared_len_host, stream);
 }
 
 int paged_decode_plan_info(const pkv_plan* p, int* batch, int* n_units, int* n_merges,
@@ -374,8 +457,10 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
     a.meta_header = reinterpret_cast<const int32_t*>(meta);
     a.cta_begin = reinterpret_cast<const int32_t*>(meta + p->off_cta);
     a.merges = reinterpret_cast<const Merge*>(meta + p->off_merge);
+    a.part_list = reinterpret_cast<const int32_t*>(meta + p->off_list);
     a.units = reinterpret_cast<const Unit*>(meta + p->off_units);
     a.n_ctas = p->ctas;
+    a.n_blocks = p->n_blocks;
     a.heads_per_cta = p->heads_per_cta;
     a.n_qo_heads = n_qo_heads;
     a.n_kv_heads = n_kv_heads;

@@ -38,7 +38,8 @@ constexpr int kMaxMerges = 4096;
 constexpr int kMaxUnits = 8192;
 constexpr size_t kOffCta = 16;
 constexpr size_t kOffMerge = (kOffCta + sizeof(int32_t) * (kMaxCtas + 1) + 255) / 256 * 256;
-constexpr size_t kOffUnits = kOffMerge + sizeof(Merge) * kMaxMerges;
+constexpr size_t kOffList = kOffMerge + sizeof(Merge) * kMaxMerges;
+constexpr size_t kOffUnits = kOffList + sizeof(int32_t) * kMaxUnits;
 constexpr size_t kMetaBytes = (kOffUnits + sizeof(Unit) * kMaxUnits + 255) / 256 * 256;
 // Device layout of the array: work list | status word | zero row | partial lse | partial out
 constexpr size_t kOffStatus = kMetaBytes;
@@ -100,7 +101,7 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     unsigned char* scratch = static_cast<unsigned char*>(g_scratch_addr[dev]);
 
     const int hpc = choose_heads_per_cta(n_kv_heads, head_dim);
-    const int per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpc);
+    const int per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpc, 1);
     if (per_sm <= 0) return fail(PKV_ERR_CUDA, "paged_decode_attn_static: occupancy query failed");
     const int ctas = sms * per_sm;
     if (ctas > kMaxCtas)
@@ -112,12 +113,13 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
                     "paged_decode_attn_static: batch %d x %d head groups exceeds the static maximum "
                     "of %d (request, head group) pairs", batch, n_groups, kMaxMerges);
     PlanCounts c{};
+    const int max_units = std::min(kMaxUnits, plan_max_units(ctas, batch, n_groups));
     int rc = plan_compute(kv_indptr_host, batch, n_groups, ctas,
-                          PlanLimits{std::min(kMaxUnits, plan_max_units(ctas, batch, n_groups)),
-                                     kMaxMerges},
+                          PlanLimits{max_units, kMaxMerges, max_units}, nullptr,
                           reinterpret_cast<Unit*>(g_stage + kOffUnits),
                           reinterpret_cast<int32_t*>(g_stage + kOffCta),
-                          reinterpret_cast<Merge*>(g_stage + kOffMerge), &c);
+                          reinterpret_cast<Merge*>(g_stage + kOffMerge),
+                          reinterpret_cast<int32_t*>(g_stage + kOffList), &c);
     if (rc != PKV_OK) return rc;
     const int qheads = hpc * (n_qo_heads / n_kv_heads);
     const size_t lse_bytes = round256(sizeof(float) * size_t(c.n_partials) * qheads);
@@ -149,6 +151,8 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     a.meta_header = reinterpret_cast<const int32_t*>(scratch);
     a.cta_begin = reinterpret_cast<const int32_t*>(scratch + kOffCta);
     a.merges = reinterpret_cast<const Merge*>(scratch + kOffMerge);
+    a.part_list = reinterpret_cast<const int32_t*>(scratch + kOffList);
+    a.n_blocks = 1;
     a.units = reinterpret_cast<const Unit*>(scratch + kOffUnits);
     a.n_ctas = ctas;
     a.heads_per_cta = hpc;

@@ -194,8 +194,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // sub-tiles of K rows and of V rows of the CTA's kHeadsPerCta heads; kSub is
 // chosen so that every stage carries 16 x kHeadGroupElems bf16 of K and as much
 // of V (32 KB, plus row padding) whatever the head count.
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB = 1>
 struct Cfg {
+    static constexpr int kBlocks = NB;  // 8-row query blocks per KV head (rows of NB*8/G requests)
     static constexpr int kHeadsPerCta = kConsumerWarps / WPH;   // KV heads of one group
     static constexpr int kRow = kHeadsPerCta * D * 2;           // bytes of a staged row
     static constexpr int kRowP = kRow + kRowPad;
@@ -210,6 +211,7 @@ struct Cfg {
     static constexpr int kBarOffset = kStages * kStage;
     static constexpr int kSmem = kBarOffset + 2 * kStages * 8 + 16;
     static_assert(G >= 1 && G <= 8, "group size");
+    static_assert(NB == 1 || NB == 2, "query blocks");
     static_assert(kHeadsPerCta * D * kSub == kHeadGroupElems, "stage budget");
     static_assert(kMBlocks >= 1, "dims per warp");
 };
@@ -222,10 +224,10 @@ struct Shared {
 
 // Producer warp: lane l copies, for every sub-tile j of a stage, token
 // (l % 16) + 16 j's K row (l < 16) or V row (l >= 16) of the CTA's head group.
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB>
 __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
-    using C = Cfg<D, G, WPH>;
+    using C = Cfg<D, G, WPH, NB>;
     const int lane = threadIdx.x & 31;
     const int tok = lane & (kTile - 1);
     const bool is_v = lane >= kTile;
@@ -308,28 +310,38 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     }
 }
 
-template <int D, int G, int WPH>
+// Q^T as the B operand of S^T = K Q^T: query block nb holds the rows 8 nb .. 8 nb + 7
+// of the unit's query set, row r being head r % G of request b + r / G; lane l holds
+// row 8 nb + l / 4, dims 2 (l % 4) .. of each k-step. Rows beyond the unit's
+// requests are zero.
+template <int D, int G, int WPH, int NB>
 __device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit& un, int hh, int g,
-                                                 int t4, uint32_t (&qf)[Cfg<D, G, WPH>::kKSteps][2]) {
-    using C = Cfg<D, G, WPH>;
+                                                 int t4,
+                                                 uint32_t (&qf)[NB][Cfg<D, G, WPH, NB>::kKSteps][2]) {
+    using C = Cfg<D, G, WPH, NB>;
     const int kvh = un.hg * C::kHeadsPerCta + hh;
-    const uint32_t* row = reinterpret_cast<const uint32_t*>(
-        static_cast<const __nv_bfloat16*>(a.q) +
-        (int64_t(un.b) * a.n_qo_heads + kvh * G + (g < G ? g : 0)) * D + 2 * t4);
 #pragma unroll
-    for (int ks = 0; ks < C::kKSteps; ++ks) {
-        qf[ks][0] = g < G ? __ldg(row + ks * 8) : 0u;
-        qf[ks][1] = g < G ? __ldg(row + ks * 8 + 4) : 0u;
+    for (int nb = 0; nb < NB; ++nb) {
+        const int r = 8 * nb + g;
+        const bool valid = r / G < un.nreq;
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(
+            static_cast<const __nv_bfloat16*>(a.q) +
+            (int64_t(un.b + (valid ? r / G : 0)) * a.n_qo_heads + kvh * G + r % G) * D + 2 * t4);
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+            qf[nb][ks][0] = valid ? __ldg(row + ks * 8) : 0u;
+            qf[nb][ks][1] = valid ? __ldg(row + ks * 8 + 4) : 0u;
+        }
     }
 }
 
 // Fused append: copy this warp's part (head hh, dims of `part`) of the staged new
 // K and V rows of request un.b from shared memory to pool slot slot_ids[un.b].
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB>
 __device__ __forceinline__ void store_new_rows(const DecodeArgs& a, const Unit& un,
                                                const uint8_t* smem, int stage, int row, int hh,
                                                int part, int lane) {
-    using C = Cfg<D, G, WPH>;
+    using C = Cfg<D, G, WPH, NB>;
     constexpr int kBytes = C::kDimsPerWarp * 2;  // bytes of this warp's share of one row
     const int64_t slot = __ldg(a.slot_ids + un.b);
     const int64_t dst_off = slot * int64_t(a.n_kv_heads) * D * 2 +
@@ -344,10 +356,10 @@ __device__ __forceinline__ void store_new_rows(const DecodeArgs& a, const Unit& 
     }
 }
 
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB>
 __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
-    using C = Cfg<D, G, WPH>;
+    using C = Cfg<D, G, WPH, NB>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hh = warp / WPH;    // KV head within the group
     const int part = warp % WPH;  // which slice of head_dim this warp accumulates
@@ -365,28 +377,44 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     int stage = 0;
     uint32_t full_parity = 0;
 
-    // Q^T as the B operand: lane holds head g, dims 2*t4.. of each k-step. The
-    // next unit's fragments are loaded while the current unit streams.
-    uint32_t qb[C::kKSteps][2], qn[C::kKSteps][2];
+    // With one query block the next unit's q fragments are loaded while the current
+    // unit streams; with two (shared prefixes) they are loaded at the unit's start.
+    constexpr bool kPrefetchQ = NB == 1;
+    uint32_t qb[NB][C::kKSteps][2], qn[NB][C::kKSteps][2];
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
     pdl_wait();  // q may come from the previous kernel
-    if (u_begin < u_end) load_q_fragments<D, G, WPH>(a, next, hh, g, t4, qn);
+    if constexpr (kPrefetchQ) {
+        if (u_begin < u_end) load_q_fragments<D, G, WPH, NB>(a, next, hh, g, t4, qn);
+    }
     for (int u = u_begin; u < u_end; ++u) {
         const Unit un = next;
         const int kvh = un.hg * C::kHeadsPerCta + hh;
+        if constexpr (kPrefetchQ) {
 #pragma unroll
-        for (int ks = 0; ks < C::kKSteps; ++ks) {
-            qb[ks][0] = qn[ks][0];
-            qb[ks][1] = qn[ks][1];
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int ks = 0; ks < C::kKSteps; ++ks) {
+                    qb[nb][ks][0] = qn[nb][ks][0];
+                    qb[nb][ks][1] = qn[nb][ks][1];
+                }
+        } else {
+            load_q_fragments<D, G, WPH, NB>(a, un, hh, g, t4, qb);
         }
         if (u + 1 < u_end) {
             next = a.units[u + 1];
-            load_q_fragments<D, G, WPH>(a, next, hh, g, t4, qn);
+            if constexpr (kPrefetchQ) load_q_fragments<D, G, WPH, NB>(a, next, hh, g, t4, qn);
         }
-        float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
-        float o[C::kMBlocks][4];
+        // softmax state per query block and column (heads 2 t4, 2 t4 + 1 of the block)
+        float m[NB][2], l[NB][2];
+        float o[NB][C::kMBlocks][4];
 #pragma unroll
-        for (int mb = 0; mb < C::kMBlocks; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
+        for (int nb = 0; nb < NB; ++nb) {
+            m[nb][0] = m[nb][1] = neg_inf();
+            l[nb][0] = l[nb][1] = 0.f;
+#pragma unroll
+            for (int mb = 0; mb < C::kMBlocks; ++mb)
+                o[nb][mb][0] = o[nb][mb][1] = o[nb][mb][2] = o[nb][mb][3] = 0.f;
+        }
 
         const int n_tok = un.tok_end - un.tok_begin;
         const int n_stages = n_tok > 0 ? (n_tok + C::kStageTokens - 1) / C::kStageTokens : 1;
@@ -400,56 +428,70 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             if (a.k_new != nullptr) {
                 const int row = un.len - 1 - (un.tok_begin + t * C::kStageTokens);
                 if (row >= 0 && row < n_stage && row < C::kStageTokens)
-                    store_new_rows<D, G, WPH>(a, un, smem, stage, row, hh, part, lane);
+                    store_new_rows<D, G, WPH, NB>(a, un, smem, stage, row, hh, part, lane);
             }
 #pragma unroll
             for (int j = 0; j < C::kSub; ++j) {
                 const int n = n_stage - j * kTile;  // valid rows of this sub-tile (if > 0)
                 if (n <= 0) break;
                 const uint32_t st = stage * C::kStage + j * kTile * C::kRowP;
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
+                float s[NB][4];
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
 #pragma unroll
                 for (int ks = 0; ks < C::kKSteps; ++ks) {
                     uint32_t ka[4];
                     ldsm_x4(k_lane + st + ks * 32, ka);
-                    mma_bf16(s, ka, qb[ks][0], qb[ks][1]);
-                }
-                // s[0], s[1]: token g, heads 2t4, 2t4+1; s[2], s[3]: token g + 8
-                const float x0 = g < n ? s[0] * scale_log2 : neg_inf();
-                const float x1 = g < n ? s[1] * scale_log2 : neg_inf();
-                const float x2 = g + 8 < n ? s[2] * scale_log2 : neg_inf();
-                const float x3 = g + 8 < n ? s[3] * scale_log2 : neg_inf();
-                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+                    for (int nb = 0; nb < NB; ++nb) mma_bf16(s[nb], ka, qb[nb][ks][0], qb[nb][ks][1]);
                 }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-                m0 = mn0;
-                m1 = mn1;
-                const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
-                const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
-                l0 = fmaf(l0, al0, p0 + p2);
-                l1 = fmaf(l1, al1, p1 + p3);
-                if (__any_sync(kFull, (al0 != 1.f) || (al1 != 1.f))) {
+                uint32_t pb[NB][2];
+                bool rescale = false;
+                float al[NB][2];
 #pragma unroll
-                    for (int mb = 0; mb < C::kMBlocks; ++mb) {
-                        o[mb][0] *= al0;
-                        o[mb][1] *= al1;
-                        o[mb][2] *= al0;
-                        o[mb][3] *= al1;
+                for (int nb = 0; nb < NB; ++nb) {
+                    // s[nb][0], [1]: token g, columns 2t4, 2t4+1; [2], [3]: token g + 8
+                    const float x0 = g < n ? s[nb][0] * scale_log2 : neg_inf();
+                    const float x1 = g < n ? s[nb][1] * scale_log2 : neg_inf();
+                    const float x2 = g + 8 < n ? s[nb][2] * scale_log2 : neg_inf();
+                    const float x3 = g + 8 < n ? s[nb][3] * scale_log2 : neg_inf();
+                    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
                     }
+                    const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
+                    al[nb][0] = ex2(m[nb][0] - mn0);
+                    al[nb][1] = ex2(m[nb][1] - mn1);
+                    rescale |= (al[nb][0] != 1.f) || (al[nb][1] != 1.f);
+                    m[nb][0] = mn0;
+                    m[nb][1] = mn1;
+                    const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
+                    const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
+                    l[nb][0] = fmaf(l[nb][0], al[nb][0], p0 + p2);
+                    l[nb][1] = fmaf(l[nb][1], al[nb][1], p1 + p3);
+                    // P^T operand: tokens 0-7 and 8-15 of the sub-tile, rows in columns
+                    pb[nb][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+                    pb[nb][1] = movmatrix_trans(pack_bf16x2(p2, p3));
                 }
-                // P^T operand: tokens 0-7 and 8-15 of the sub-tile, heads in columns
-                const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-                const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+                if (__any_sync(kFull, rescale)) {
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                        for (int mb = 0; mb < C::kMBlocks; ++mb) {
+                            o[nb][mb][0] *= al[nb][0];
+                            o[nb][mb][1] *= al[nb][1];
+                            o[nb][mb][2] *= al[nb][0];
+                            o[nb][mb][3] *= al[nb][1];
+                        }
+                }
 #pragma unroll
                 for (int mb = 0; mb < C::kMBlocks; ++mb) {
                     uint32_t va[4];
                     ldsm_x4_trans(v_lane + st + mb * 32, va);
-                    mma_bf16(o[mb], va, pb0, pb1);
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) mma_bf16(o[nb][mb], va, pb[nb][0], pb[nb][1]);
                 }
             }
             __syncwarp();
@@ -460,64 +502,48 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             }
         }
 
-        // ---- epilogue: o[mb][0..3] = (dim 16*mb' + g (+8), heads 2t4, 2t4+1)
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(kFull, l0, off);
-            l1 += __shfl_xor_sync(kFull, l1, off);
-        }
-        const float inv0 = l0 == 0.f ? 0.f : 1.f / l0;
-        const float inv1 = l1 == 0.f ? 0.f : 1.f / l1;
-        const float lse0 = l0 == 0.f ? neg_inf() : m0 + __log2f(l0);
-        const float lse1 = l1 == 0.f ? neg_inf() : m1 + __log2f(l1);
-        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+        // ---- epilogue: o[nb][mb][0..3] = (dim 16*mb' + g (+8), rows 8nb + 2t4, +1)
         const int dim0 = part * C::kDimsPerWarp + g;
-        if (un.partial < 0) {
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-            __nv_bfloat16* r0 = out + (int64_t(un.b) * hq + kvh * G + h0) * D + dim0;
-            __nv_bfloat16* r1 = r0 + D;
 #pragma unroll
-            for (int mb = 0; mb < C::kMBlocks; ++mb) {
-                if (h0 < G) {
-                    r0[mb * 16] = __float2bfloat16_rn(o[mb][0] * inv0);
-                    r0[mb * 16 + 8] = __float2bfloat16_rn(o[mb][2] * inv0);
-                }
-                if (h1 < G) {
-                    r1[mb * 16] = __float2bfloat16_rn(o[mb][1] * inv1);
-                    r1[mb * 16 + 8] = __float2bfloat16_rn(o[mb][3] * inv1);
-                }
-            }
-            if (a.lse != nullptr && part == 0 && g == 0) {
-                if (h0 < G) a.lse[int64_t(un.b) * hq + kvh * G + h0] = lse0 * kLn2;
-                if (h1 < G) a.lse[int64_t(un.b) * hq + kvh * G + h1] = lse1 * kLn2;
-            }
-            continue;
-        }
-        // partial result of a split context
-        float* p0r = a.ws_o + (int64_t(un.partial) * C::kQHeads + hh * G + h0) * D + dim0;
-        float* p1r = p0r + D;
+        for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
-        for (int mb = 0; mb < C::kMBlocks; ++mb) {
-            if (h0 < G) {
-                p0r[mb * 16] = o[mb][0] * inv0;
-                p0r[mb * 16 + 8] = o[mb][2] * inv0;
+            for (int jc = 0; jc < 2; ++jc) {
+                float lt = l[nb][jc];
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) lt += __shfl_xor_sync(kFull, lt, off);
+                const int r = 8 * nb + 2 * t4 + jc;
+                const int req = r / G, h = r % G;
+                if (req >= un.nreq) continue;
+                const float inv = lt == 0.f ? 0.f : 1.f / lt;
+                const float lse2 = lt == 0.f ? neg_inf() : m[nb][jc] + __log2f(lt);
+                if (un.partial < 0) {
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
+                                         (int64_t(un.b + req) * hq + kvh * G + h) * D + dim0;
+#pragma unroll
+                    for (int mb = 0; mb < C::kMBlocks; ++mb) {
+                        dst[mb * 16] = __float2bfloat16_rn(o[nb][mb][jc] * inv);
+                        dst[mb * 16 + 8] = __float2bfloat16_rn(o[nb][mb][2 + jc] * inv);
+                    }
+                    if (a.lse != nullptr && part == 0 && g == 0)
+                        a.lse[int64_t(un.b + req) * hq + kvh * G + h] = lse2 * kLn2;
+                } else {
+                    const int64_t prow = int64_t(un.partial + req) * C::kQHeads + hh * G + h;
+                    float* dst = a.ws_o + prow * D + dim0;
+#pragma unroll
+                    for (int mb = 0; mb < C::kMBlocks; ++mb) {
+                        dst[mb * 16] = o[nb][mb][jc] * inv;
+                        dst[mb * 16 + 8] = o[nb][mb][2 + jc] * inv;
+                    }
+                    if (part == 0 && g == 0) a.ws_lse[prow] = lse2;
+                }
             }
-            if (h1 < G) {
-                p1r[mb * 16] = o[mb][1] * inv1;
-                p1r[mb * 16 + 8] = o[mb][3] * inv1;
-            }
-        }
-        if (part == 0 && g == 0) {
-            float* lp = a.ws_lse + int64_t(un.partial) * C::kQHeads + hh * G;
-            if (h0 < G) lp[h0] = lse0;
-            if (h1 < G) lp[h1] = lse1;
         }
     }
 }
 
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB>
 __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeArgs a) {
-    using C = Cfg<D, G, WPH>;
+    using C = Cfg<D, G, WPH, NB>;
     extern __shared__ __align__(128) uint8_t smem[];
     Shared sh;
     sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
@@ -538,9 +564,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeA
     const int u_begin = a.cta_begin[blockIdx.x];
     const int u_end = a.cta_begin[blockIdx.x + 1];
     if ((threadIdx.x >> 5) == kConsumerWarps)
-        producer_warp<D, G, WPH>(a, smem, sh, u_begin, u_end);
+        producer_warp<D, G, WPH, NB>(a, smem, sh, u_begin, u_end);
     else
-        consumer_warp<D, G, WPH>(a, smem, sh, u_begin, u_end);
+        consumer_warp<D, G, WPH, NB>(a, smem, sh, u_begin, u_end);
 }
 
 // ---------------------------------------------------------------------------
@@ -570,10 +596,10 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeAr
     for (int w = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5); w < items; w += warps) {
         const int m = w / qheads, qh = w % qheads;
         const Merge mg = a.merges[m];
-        const float* lse_p = a.ws_lse + int64_t(mg.first) * qheads + qh;
+        const int32_t* parts = a.part_list + mg.first;
         float mx = neg_inf(), sm = 0.f;
         for (int c = lane; c < mg.count; c += 32) {
-            const float x = __ldcg(lse_p + int64_t(c) * qheads);
+            const float x = __ldcg(a.ws_lse + int64_t(__ldg(parts + c)) * qheads + qh);
             const float mn = fmaxf(mx, x);
             sm = (mx == neg_inf() ? 0.f : sm * ex2(mx - mn)) + ex2(x - mn);
             mx = mn;
@@ -590,21 +616,27 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeAr
         float acc[kVD];
 #pragma unroll
         for (int i = 0; i < kVD; ++i) acc[i] = 0.f;
-        const float* o_p = a.ws_o + (int64_t(mg.first) * qheads + qh) * D + lane * kVD;
         // Parts in chunks of kChunk: every load of a chunk is issued before the first
         // use, so a chunk costs one round trip to L2.
         constexpr int kChunk = kVD == 4 ? 16 : 8;
         for (int c0 = 0; c0 < mg.count; c0 += kChunk) {
             const int c = c0 + (lane % kChunk);
-            const float wl = c < mg.count ? ex2(__ldcg(lse_p + int64_t(c) * qheads) - total) : 0.f;
+            int slot_l = 0;
+            float wl = 0.f;
+            if (c < mg.count) {
+                slot_l = __ldg(parts + c);
+                wl = ex2(__ldcg(a.ws_lse + int64_t(slot_l) * qheads + qh) - total);
+            }
             float4 x[kChunk][kVD / 4];
 #pragma unroll
-            for (int j = 0; j < kChunk; ++j)
+            for (int j = 0; j < kChunk; ++j) {
+                const int slot = __shfl_sync(kFull, slot_l, j);
+                const float* src = a.ws_o + (int64_t(slot) * qheads + qh) * D + lane * kVD;
 #pragma unroll
                 for (int i = 0; i < kVD / 4; ++i)
-                    x[j][i] = c0 + j < mg.count
-                                  ? __ldcg(reinterpret_cast<const float4*>(o_p + int64_t(c0 + j) * qheads * D) + i)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x[j][i] = c0 + j < mg.count ? __ldcg(reinterpret_cast<const float4*>(src) + i)
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
             for (int j = 0; j < kChunk; ++j) {
                 const float wj = __shfl_sync(kFull, wl, j);
@@ -644,75 +676,83 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, lse_merge_kernel<D>, a);
 }
 
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB>
 cudaError_t prepare() {
     // Raise the dynamic shared memory limit once per instance.
     static cudaError_t status = cudaFuncSetAttribute(
-        paged_decode_kernel<D, G, WPH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        Cfg<D, G, WPH>::kSmem);
+        paged_decode_kernel<D, G, WPH, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        Cfg<D, G, WPH, NB>::kSmem);
     return status;
 }
 
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB>
 int occupancy() {
-    if (prepare<D, G, WPH>() != cudaSuccess) return 0;
+    if (prepare<D, G, WPH, NB>() != cudaSuccess) return 0;
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_kernel<D, G, WPH>,
-                                                      kThreads, Cfg<D, G, WPH>::kSmem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_kernel<D, G, WPH, NB>,
+                                                      kThreads, Cfg<D, G, WPH, NB>::kSmem) !=
+        cudaSuccess)
         return 0;
     return blocks;
 }
 
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB>
 cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
-    cudaError_t e = prepare<D, G, WPH>();
+    cudaError_t e = prepare<D, G, WPH, NB>();
     if (e != cudaSuccess) return e;
     if (a.n_ctas == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.n_ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<D, G, WPH>::kSmem;
+    cfg.dynamicSmemBytes = Cfg<D, G, WPH, NB>::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, WPH>, a);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, WPH, NB>, a);
 }
 
-// Calls FN<D, G, WPH>(args...) for the runtime shape.
-template <template <int, int, int> class FN, typename... Args>
-auto dispatch(int head_dim, int group, int wph, Args&&... args)
-    -> decltype(FN<128, 1, 1>::run(args...)) {
-#define PKV_G(D_, W_)                                          \
+// Calls FN<D, G, WPH, NB>::run(args...) for the runtime shape. Two query blocks
+// exist only at head_dim 128 with one warp per KV head (four heads per CTA).
+template <template <int, int, int, int> class FN, typename... Args>
+auto dispatch(int head_dim, int group, int wph, int nb, Args&&... args)
+    -> decltype(FN<128, 1, 1, 1>::run(args...)) {
+#define PKV_G(D_, W_, NB_)                                     \
     switch (group) {                                           \
-        case 1: return FN<D_, 1, W_>::run(args...);            \
-        case 2: return FN<D_, 2, W_>::run(args...);            \
-        case 4: return FN<D_, 4, W_>::run(args...);            \
-        case 8: return FN<D_, 8, W_>::run(args...);            \
+        case 1: return FN<D_, 1, W_, NB_>::run(args...);       \
+        case 2: return FN<D_, 2, W_, NB_>::run(args...);       \
+        case 4: return FN<D_, 4, W_, NB_>::run(args...);       \
+        case 8: return FN<D_, 8, W_, NB_>::run(args...);       \
         default: break;                                        \
     }
-    if (head_dim == 128) {
-        if (wph == 1) { PKV_G(128, 1) }
-        if (wph == 2) { PKV_G(128, 2) }
-        if (wph == 4) { PKV_G(128, 4) }
-    } else if (head_dim == 256) {
-        if (wph == 2) { PKV_G(256, 2) }
-        if (wph == 4) { PKV_G(256, 4) }
+    if (nb == 1) {
+        if (head_dim == 128) {
+            if (wph == 1) { PKV_G(128, 1, 1) }
+            if (wph == 2) { PKV_G(128, 2, 1) }
+            if (wph == 4) { PKV_G(128, 4, 1) }
+        } else if (head_dim == 256) {
+            if (wph == 2) { PKV_G(256, 2, 1) }
+            if (wph == 4) { PKV_G(256, 4, 1) }
+        }
+    } else if (nb == 2 && head_dim == 128 && wph == 1) {
+        PKV_G(128, 1, 2)
     }
 #undef PKV_G
-    return FN<128, 1, 1>::unsupported();
+    return FN<128, 1, 1, 1>::unsupported();
 }
 
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB>
 struct OccupancyFn {
-    static int run() { return occupancy<D, G, WPH>(); }
+    static int run() { return occupancy<D, G, WPH, NB>(); }
     static int unsupported() { return 0; }
 };
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int NB>
 struct LaunchFn {
-    static cudaError_t run(const DecodeArgs& a, cudaStream_t s) { return launch<D, G, WPH>(a, s); }
+    static cudaError_t run(const DecodeArgs& a, cudaStream_t s) {
+        return launch<D, G, WPH, NB>(a, s);
+    }
     static cudaError_t unsupported() { return cudaErrorInvalidValue; }
 };
 
@@ -728,17 +768,24 @@ bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim) {
     return n_kv_heads == 1 || n_kv_heads == 2 || n_kv_heads == 4 || n_kv_heads == 8;
 }
 
-int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta) {
+bool decode_has_shared_kernel(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta) {
+    return decode_shape_supported(n_qo_heads, n_kv_heads, head_dim) && head_dim == 128 &&
+           heads_per_cta == kConsumerWarps;
+}
+
+int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta,
+                       int n_blocks) {
     if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim)) return 0;
     if (heads_per_cta < 1 || heads_per_cta > heads_per_group(n_kv_heads, head_dim) ||
         n_kv_heads % heads_per_cta != 0)
         return 0;
-    return dispatch<OccupancyFn>(head_dim, n_qo_heads / n_kv_heads, warps_per_head(heads_per_cta));
+    return dispatch<OccupancyFn>(head_dim, n_qo_heads / n_kv_heads, warps_per_head(heads_per_cta),
+                                 n_blocks);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e = dispatch<LaunchFn>(a.head_dim, a.n_qo_heads / a.n_kv_heads,
-                                       warps_per_head(a.heads_per_cta), a, stream);
+                                       warps_per_head(a.heads_per_cta), a.n_blocks, a, stream);
     if (e != cudaSuccess) return e;
     return a.head_dim == 128 ? launch_merge<128>(a, stream) : launch_merge<256>(a, stream);
 }

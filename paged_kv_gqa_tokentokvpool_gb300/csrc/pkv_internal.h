@@ -38,17 +38,18 @@ inline int heads_per_group(int n_kv_heads, int head_dim) {
 int choose_heads_per_cta(int n_kv_heads, int head_dim);
 
 // ---- plan ----------------------------------------------------------------
-// One work unit of the decode kernel: tokens [tok_begin, tok_end) of request b's
-// slot list, KV-head group hg; idx_begin = kv_indptr[b] + tok_begin is where the
-// unit's slot ids start in kv_indices, len = the request's context length.
-// partial < 0: the unit covers the whole context and writes out/lse; otherwise it
-// writes partial slot `partial` of the workspace and takes part in merge record
-// `merge`.
+// One work unit of the decode kernel: tokens [tok_begin, tok_end) of the slot list
+// of request b, KV-head group hg, attended for the nreq requests b .. b+nreq-1
+// (nreq > 1 only for a prefix those requests share); idx_begin = kv_indptr[b] +
+// tok_begin is where the unit's slot ids start in kv_indices, and len is request
+// b's context length (-1 for a shared prefix), which tells the fused append which
+// token is the newest. partial < 0: the unit covers a whole context and writes
+// out/lse; otherwise request b+r writes partial slot partial + r of the workspace.
 struct Unit {
-    int32_t b, hg, tok_begin, tok_end, partial, merge, idx_begin, len;
+    int32_t b, hg, tok_begin, tok_end, partial, nreq, idx_begin, len;
 };
-// One split (request, head group): its parts occupy partial slots
-// [first, first + count).
+// One (request, head group) whose result is merged from partial results: the
+// slots part_list[first .. first + count).
 struct Merge {
     int32_t b, hg, first, count;
 };
@@ -60,17 +61,29 @@ constexpr int kMinChunkTokens = 64;
 struct PlanLimits {
     int max_units;
     int max_merges;
+    int max_partials;
 };
 struct PlanCounts {
     int n_units, n_ctas, n_merges, n_partials, chunk_tokens;
 };
+// Runs of consecutive requests that list the same first len[s] slots: requests
+// [indptr[s], indptr[s+1]) share len[s] slots; prefix units serve up to
+// requests_per_unit of them at once.
+struct PlanSharing {
+    const int32_t* indptr;
+    const int32_t* len;
+    int n;
+    int requests_per_unit;
+};
 
 int plan_max_units(int ctas, int max_batch, int n_groups);
 // Pure host planner. units[max_units], cta_begin[ctas + 1] (every CTA of the grid
-// gets an entry; unused ones an empty range), merges[max_merges].
+// gets an entry; unused ones an empty range), merges[max_merges],
+// part_list[max_partials]. sharing may be NULL.
 // Returns PKV_OK, PKV_ERR_PLAN (capacity) or PKV_ERR_INVALID_ARG (bad indptr).
 int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, const PlanLimits& lim,
-                 Unit* units, int* cta_begin, Merge* merges, PlanCounts* out);
+                 const PlanSharing* sharing, Unit* units, int* cta_begin, Merge* merges,
+                 int32_t* part_list, PlanCounts* out);
 
 // ---- kernels -------------------------------------------------------------
 struct DecodeArgs {
@@ -82,7 +95,9 @@ struct DecodeArgs {
     const Unit* units;
     const int32_t* cta_begin;
     const Merge* merges;
+    const int32_t* part_list;  // partial slots of the merge records
     int n_ctas;           // grid size: every CTA of the plan (some may have no units)
+    int n_blocks;         // 8-row query blocks per KV head in a unit (1, or 2 with sharing)
     int heads_per_cta;    // KV heads of one group
     int n_qo_heads;
     int n_kv_heads;
@@ -106,7 +121,11 @@ struct DecodeArgs {
 
 bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim);
 // Resident CTAs per SM of the decode kernel for this shape (0 on error).
-int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta);
+int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta,
+                       int n_blocks);
+// Whether a kernel with two query blocks per KV head (shared-prefix units of
+// 16 / G requests) exists for this shape.
+bool decode_has_shared_kernel(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_append(void* k_pool, void* v_pool, const int32_t* slot_ids,
@@ -123,7 +142,7 @@ struct pkv_plan {
     int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0, n_groups = 0, heads_per_cta = 0;
     pkv::PlanLimits lim{};
     size_t meta_bytes = 0;
-    void* host_staging = nullptr;  // pinned: header, cta_begin, merges, units
+    void* host_staging = nullptr;  // pinned: header, cta_begin, merges, part list, units
     void* dev_meta = nullptr;      // device copy of the same (used prefix uploaded per step)
     float* ws_o = nullptr;
     float* ws_lse = nullptr;
@@ -135,6 +154,8 @@ struct pkv_plan {
     bool planned = false;
     int batch = 0;
     pkv::PlanCounts counts{};
-    size_t off_cta = 0, off_merge = 0, off_units = 0;  // byte offsets in the staging
+    size_t off_cta = 0, off_merge = 0, off_list = 0, off_units = 0;  // offsets in the staging
+    int share_rows = 0;  // requests per shared-prefix unit (0: this shape has no such kernel)
+    int n_blocks = 1;    // query blocks of the current step's kernel
     std::vector<int32_t> indptr_host;
 };

@@ -243,6 +243,7 @@ def test_full_size_config(pkv, config_no, fused):
     wl = workloads.config_workload(config_no)
     st = bench.StepState(wl, layers=FULL[config_no], poison_unreferenced=True, fused=fused)
     assert st.fused == fused
+    assert (st.sharing is not None) == (config_no == 3)
     uniq, inv = np.unique(wl.kv_indices, return_inverse=True)
     compact = inv.astype(np.int32)
     uniq_dev = torch.from_numpy(uniq.astype(np.int64)).cuda()
@@ -423,3 +424,50 @@ def test_fused_append_rejects_bad_calls(pkv):
         assert e.value.code == pkv.PKV_ERR_INDEX
     finally:
         pkv.pkv_set_debug_checks(False)
+
+
+SHARED_CASES = [
+    # (prefix lengths, group size, suffix lengths, Hq, Hkv, D)
+    ([300], 4, [5, 1, 700, 64], 32, 8, 128),
+    ([3000, 17], 5, [1, 2, 3, 400, 9000, 16, 17, 1, 2, 3], 32, 8, 128),
+    ([5000], 8, [64] * 8, 32, 8, 128),
+    ([777, 2048], 3, [100, 1, 50, 3000, 2, 8], 64, 8, 128),
+    ([4100], 9, list(range(1, 10)), 16, 8, 128),
+    ([1000], 17, [1] * 17, 8, 8, 128),
+    ([2500], 4, [1, 90, 300, 2], 16, 4, 256),
+]
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["attn", "append_attn"])
+@pytest.mark.parametrize("case", range(len(SHARED_CASES)))
+def test_shared_prefix_plan(pkv, case, fused):
+    """paged_decode_plan_shared: prefix units serve several requests; results must
+    equal the oracle's (which knows nothing about sharing)."""
+    prefixes, gsize, suffixes, hq, hkv, d = SHARED_CASES[case]
+    wl = workloads.prefix_shared_workload(prefixes, suffixes, gsize, n_qo_heads=hq,
+                                          n_kv_heads=hkv, head_dim=d, seed=500 + case)
+    t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
+    dev = torch.device("cuda")
+    kp, vp = t.k_pool.to(dev), t.v_pool.to(dev)
+    out = torch.full((wl.batch, hq, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((wl.batch, hq), float("nan"), dtype=torch.float32, device=dev)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx = torch.from_numpy(wl.kv_indices).to(dev)
+    slots = torch.from_numpy(wl.append_slots).to(dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, hq, hkv, d)
+    shared_indptr = np.arange(0, gsize * len(prefixes) + 1, gsize, dtype=np.int32)
+    pkv.paged_decode_plan_shared(plan, wl.kv_indptr, shared_indptr, np.array(prefixes, np.int32))
+    if fused:
+        pkv.paged_decode_append_attn(t.q.to(dev), kp, vp, ip, idx, slots, t.k_new.to(dev),
+                                     t.v_new.to(dev), wl.batch, hq, hkv, d, wl.sm_scale, out, lse,
+                                     plan)
+    else:
+        pkv.kvpool_append(kp, vp, slots, t.k_new.to(dev), t.v_new.to(dev))
+        pkv.paged_decode_attn(t.q.to(dev), kp, vp, ip, idx, wl.batch, hq, hkv, d, wl.sm_scale,
+                              out, lse, plan)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle_reference(wl, t)
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what=f"shared case {case}")
+    assert plan.status() == 0
+    if d == 128 and hkv == 8:
+        assert plan.info()["n_merges"] >= wl.batch  # every member merged its parts

@@ -76,50 +76,120 @@ def test_errors_are_reported_before_any_launch(pkv):
     lib.paged_decode_plan_destroy(None)  # no-op
 
 
-def check_plan(indptr, n_kv_heads, head_dim, ctas, plan, hpc=0):
+def check_plan(indptr, n_kv_heads, head_dim, ctas, plan, hpc=0, shared=None):
+    """Every (request, head group, token) is attended exactly once; units, partial
+    slots and merge records are consistent. shared = (shared_indptr, shared_len)."""
     indptr = np.asarray(indptr, np.int64)
     B = indptr.size - 1
     lengths = np.diff(indptr)
     hpg = hpc or min(n_kv_heads, 512 // head_dim)
     groups = n_kv_heads // hpg
     units, cta_begin, merges, chunk = plan["units"], plan["cta_begin"], plan["merges"], plan["chunk"]
+    part_list = plan["part_list"]
     n = len(units)
     assert cta_begin[0] == 0 and cta_begin[-1] == n
     assert np.all(np.diff(cta_begin) >= 0)
     assert len(cta_begin) - 1 == ctas, "every CTA of the grid has an entry"
     assert plan["ctas_used"] <= ctas
+    prefix = np.zeros(B, np.int64)
+    if shared is not None:
+        sp, sl = shared
+        for s in range(len(sp) - 1):
+            prefix[sp[s]:sp[s + 1]] = sl[s]
     covered = {(b, g): np.zeros(lengths[b], np.int32) for b in range(B) for g in range(groups)}
-    direct, parts_seen = set(), {}
-    for b, hg, t0, t1, part, merge, idx_begin, _ in units:
-        assert 0 <= b < B and 0 <= hg < groups and 0 <= t0 <= t1 <= lengths[b]
+    direct, slot_owner = set(), {}
+    for b, hg, t0, t1, part, nreq, idx_begin, length in units:
+        assert 0 <= b and b + nreq <= B and nreq >= 1 and 0 <= hg < groups and 0 <= t0 <= t1
         assert idx_begin == indptr[b] + t0
-        covered[(b, hg)][t0:t1] += 1
+        if nreq > 1 or length == -1:  # a shared prefix
+            assert length == -1 and part >= 0
+            for r in range(nreq):
+                assert t1 <= prefix[b + r], "prefix unit beyond the shared prefix"
+        else:
+            assert length == lengths[b] and t1 <= lengths[b]
+        for r in range(nreq):
+            covered[(b + r, hg)][t0:t1] += 1
         if part < 0:
-            assert (t0, t1) == (0, lengths[b]) and merge == -1
+            assert nreq == 1 and (t0, t1) == (0, lengths[b])
             assert (b, hg) not in direct
             direct.add((b, hg))
         else:
-            assert part not in parts_seen and t1 > t0
-            assert t1 - t0 <= chunk + 32
-            parts_seen[part] = (b, hg, t0, t1, merge)
+            for r in range(nreq):
+                assert part + r not in slot_owner
+                slot_owner[part + r] = (b + r, hg, t0, t1)
+            assert t1 > t0
     for key, cov in covered.items():
         assert np.all(cov == 1), f"{key}: tokens not covered exactly once"
     merged = set()
-    for m, (b, hg, first, count) in enumerate(merges):
-        assert count >= 2 and (b, hg) not in merged and (b, hg) not in direct
+    for b, hg, first, count in merges:
+        assert count >= 1 and (b, hg) not in merged and (b, hg) not in direct
         merged.add((b, hg))
-        ps = [parts_seen[first + c] for c in range(count)]
-        assert all(pb == b and ph == hg and pm == m for pb, ph, _, _, pm in ps)
-        assert sum(t1 - t0 for _, _, t0, t1, _ in ps) == lengths[b]
+        ps = [slot_owner[part_list[first + c]] for c in range(count)]
+        assert all(pb == b and ph == hg for pb, ph, _, _ in ps)
+        assert sum(t1 - t0 for _, _, t0, t1 in ps) == lengths[b]
     assert merged | direct == set(covered)
-    assert len(parts_seen) == plan["partials"] == sum(int(c) for *_, c in merges)
-    if parts_seen:
-        assert set(parts_seen) == set(range(len(parts_seen)))
-    assert n <= 2 * ctas + B * groups
+    assert len(slot_owner) == plan["partials"] == sum(int(c) for *_, c in merges)
+    assert sorted(part_list.tolist()) == list(range(plan["partials"]))
+    assert n <= 2 * ctas + 2 * B * groups
     # each CTA streams about the same number of tokens (ranges snap by <= 32 tokens)
     loads = [int((units[a:b, 3] - units[a:b, 2]).sum()) for a, b in zip(cta_begin[:-1], cta_begin[1:])]
-    if lengths.sum() >= 64 * ctas:
+    if lengths.sum() >= 64 * ctas and shared is None:
         assert max(loads) <= chunk * 1.25 + 1
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_planner_with_shared_prefixes(pkv, seed):
+    rng = np.random.default_rng(100 + seed)
+    n_groups = int(rng.integers(1, 6))
+    sizes = rng.integers(1, 10, n_groups)
+    singles = rng.integers(0, 4, n_groups + 1)
+    lengths, sp, sl = [], [], []
+    for gi in range(n_groups):
+        lengths += list(rng.integers(0, 3000, singles[gi]))
+        P = int(rng.integers(0, 5000))
+        sp.append(len(lengths))
+        sl.append(P)
+        lengths += list(P + rng.integers(1, 2000, sizes[gi]))
+        sp.append(len(lengths))
+    lengths += list(rng.integers(0, 3000, singles[-1]))
+    # runs are given as [start, end) pairs collapsed into an indptr of groups
+    starts, ends = sp[0::2], sp[1::2]
+    shared_indptr, shared_len = [], []
+    for s_, e_, P in zip(starts, ends, sl):
+        shared_indptr.append((s_, e_, P))
+    indptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    # the C API takes consecutive runs: build one run per group, with standalone
+    # requests between runs expressed as runs of length 0 shared slots
+    sp_arr, sl_arr = [0], []
+    cursor = 0
+    for s_, e_, P in shared_indptr:
+        if s_ > cursor:
+            sp_arr.append(s_)
+            sl_arr.append(0)
+        sp_arr.append(e_)
+        sl_arr.append(P)
+        cursor = e_
+    if sp_arr[0] != 0 or len(sp_arr) < 2:
+        pass
+    rpu = [2, 4, 8, 16][seed % 4]
+    ctas = 304
+    plan = pkv.paged_decode_plan_host(indptr, 8, 128, ctas, shared_indptr=sp_arr, shared_len=sl_arr,
+                                      requests_per_unit=rpu)
+    check_plan(indptr, 8, 128, ctas, plan, shared=(np.array(sp_arr), np.array(sl_arr)))
+    # a prefix unit serves at most requests_per_unit requests
+    assert plan["units"][:, 5].max() <= rpu
+
+
+def test_planner_rejects_bad_sharing(pkv):
+    indptr = np.array([0, 100, 150, 300], np.int32)
+    with pytest.raises(pkv.PkvError) as e:  # shared prefix as long as a member's context
+        pkv.paged_decode_plan_host(indptr, 8, 128, 304, shared_indptr=[0, 2], shared_len=[50],
+                                   requests_per_unit=4)
+    assert e.value.code == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:  # run beyond the batch
+        pkv.paged_decode_plan_host(indptr, 8, 128, 304, shared_indptr=[1, 5], shared_len=[10],
+                                   requests_per_unit=4)
+    assert e.value.code == pkv.PKV_ERR_INVALID_ARG
 
 
 SHAPES = [(8, 128), (4, 256), (2, 128), (1, 256), (8, 256)]
