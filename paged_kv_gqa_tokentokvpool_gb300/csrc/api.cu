@@ -241,6 +241,12 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
         delete p;
         return fail(PKV_ERR_CUDA, "paged_decode_plan_create: occupancy query failed");
     }
+    // Tuning knob: PKV_CTAS_PER_SM (>= 1) launches fewer persistent CTAs per SM
+    // than fit (longer ranges, fewer split contexts).
+    if (const char* env = std::getenv("PKV_CTAS_PER_SM")) {
+        const int want = std::atoi(env);
+        if (want >= 1 && want < p->ctas_per_sm) p->ctas_per_sm = want;
+    }
     p->ctas = p->num_sms * p->ctas_per_sm;
     p->max_batch = max_batch;
     p->max_tokens = max_tokens;
