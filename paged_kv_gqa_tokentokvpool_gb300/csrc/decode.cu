@@ -584,7 +584,6 @@ constexpr int kMergeThreads = 128;
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeArgs a) {
     pdl_launch_dependents();
-    pdl_wait();  // the partial results come from the decode kernel
     constexpr int kVD = D / 32;  // dims per lane
     const int lane = threadIdx.x & 31;
     const int n_merges = a.meta_header[0];
@@ -593,13 +592,24 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeAr
     const int items = n_merges * qheads;
     const int warps = gridDim.x * (kMergeThreads / 32);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    for (int w = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5); w < items; w += warps) {
-        const int m = w / qheads, qh = w % qheads;
-        const Merge mg = a.merges[m];
+    // The merge record and the slots of its first 32 parts are plan data: read them
+    // before waiting for the decode kernel, so only the partial results are loaded
+    // after it.
+    int w = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
+    Merge mg{};
+    int slot_l = 0;  // slot of part `lane` (parts < 32)
+    if (w < items) {
+        mg = a.merges[w / qheads];
+        if (lane < mg.count) slot_l = __ldg(a.part_list + mg.first + lane);
+    }
+    pdl_wait();  // the partial results come from the decode kernel
+    for (; w < items; w += warps) {
+        const int qh = w % qheads;
         const int32_t* parts = a.part_list + mg.first;
         float mx = neg_inf(), sm = 0.f;
         for (int c = lane; c < mg.count; c += 32) {
-            const float x = __ldcg(a.ws_lse + int64_t(__ldg(parts + c)) * qheads + qh);
+            const int slot = c < 32 ? slot_l : __ldg(parts + c);
+            const float x = __ldcg(a.ws_lse + int64_t(slot) * qheads + qh);
             const float mn = fmaxf(mx, x);
             sm = (mx == neg_inf() ? 0.f : sm * ex2(mx - mn)) + ex2(x - mn);
             mx = mn;
@@ -621,16 +631,17 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeAr
         constexpr int kChunk = kVD == 4 ? 16 : 8;
         for (int c0 = 0; c0 < mg.count; c0 += kChunk) {
             const int c = c0 + (lane % kChunk);
-            int slot_l = 0;
+            const int from_lane = __shfl_sync(kFull, slot_l, c & 31);  // every lane shuffles
+            int slot_c = 0;
             float wl = 0.f;
             if (c < mg.count) {
-                slot_l = __ldg(parts + c);
-                wl = ex2(__ldcg(a.ws_lse + int64_t(slot_l) * qheads + qh) - total);
+                slot_c = c < 32 ? from_lane : __ldg(parts + c);
+                wl = ex2(__ldcg(a.ws_lse + int64_t(slot_c) * qheads + qh) - total);
             }
             float4 x[kChunk][kVD / 4];
 #pragma unroll
             for (int j = 0; j < kChunk; ++j) {
-                const int slot = __shfl_sync(kFull, slot_l, j);
+                const int slot = __shfl_sync(kFull, slot_c, j);
                 const float* src = a.ws_o + (int64_t(slot) * qheads + qh) * D + lane * kVD;
 #pragma unroll
                 for (int i = 0; i < kVD / 4; ++i)
@@ -659,6 +670,11 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeAr
             *reinterpret_cast<uint2*>(dst + i) = packed;
         }
         if (a.lse != nullptr && lane == 0) a.lse[int64_t(mg.b) * a.n_qo_heads + h] = total * kLn2;
+        // next item of this warp
+        if (w + warps < items) {
+            mg = a.merges[(w + warps) / qheads];
+            slot_l = lane < mg.count ? __ldg(a.part_list + mg.first + lane) : 0;
+        }
     }
 }
 
