@@ -552,15 +552,23 @@ def main(argv=None):
 
 
 def _profiled_traffic(config_no: int):
-    """DRAM bytes per attention call from the committed ncu summary of this
-    workload, if one exists for the current kernels (else None)."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per attention call from the committed ncu summary of this workload
+    (profiles/traffic.txt), if it was taken on the current decode-kernel source;
+    else None."""
+    import hashlib
+    src = os.path.join(ROOT, "paged_kv_gqa_tokentokvpool_gb300", "csrc", "decode.cu")
     try:
-        with open(p) as f:
-            d = json.load(f)
-        return d.get(str(config_no))
-    except Exception:
-        return None
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and not line.startswith("#") and parts[0] == str(config_no) \
+                        and sha.startswith(parts[1]):
+                    return int(parts[2])
+    except OSError:
+        pass
+    return None
 
 
 if __name__ == "__main__":
