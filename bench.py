@@ -355,6 +355,21 @@ def cpu_baseline(st: StepState, budget_s: float = 12.0, max_layers=None):
 # main
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest of every rank's x (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_gbs(world: int, bytes_per_step: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput of `world` replicas that each ran `steps` steps in (at
+    most) elapsed_ms: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_step * steps / (elapsed_ms * 1e-3) / 1e9
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -465,17 +480,13 @@ def main(argv=None):
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    elapsed_ms = start.elapsed_time(end)
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), pg, "cuda")
     # The attention calls alone, each bracketed by CUDA events on its stream
     # (eager launches: an event between two kernels also ends their overlap).
     for _ in range(args.steps):
         st.run(attn_events)
     torch.cuda.synchronize()
     attn_ms = [a.elapsed_time(b) for a, b in attn_events]
-    if pg is not None:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
 
     # end to end through the public API, host buffers in and out
     io = HostIO(st)
@@ -490,11 +501,7 @@ def main(argv=None):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, "cuda")
 
     if rank != 0:
         if pg is not None:
@@ -502,8 +509,8 @@ def main(argv=None):
         return 0
 
     ms_per_step = elapsed_ms / args.steps
-    value = world * nbytes["step"] * args.steps / (elapsed_ms * 1e-3) / 1e9
-    e2e_value = world * nbytes["step"] * args.steps / (e2e_ms * 1e-3) / 1e9
+    value = replica_gbs(world, nbytes["step"], args.steps, elapsed_ms)
+    e2e_value = replica_gbs(world, nbytes["step"], args.steps, e2e_ms)
     peak, peak_kind = measured_hbm_peak()
     attn_avg_ms = statistics.mean(attn_ms)
     achieved = nbytes["attn_per_layer"] / (attn_avg_ms * 1e-3) / 1e9
