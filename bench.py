@@ -370,6 +370,40 @@ def replica_gbs(world: int, bytes_per_step: int, steps: int, elapsed_ms: float) 
     return world * bytes_per_step * steps / (elapsed_ms * 1e-3) / 1e9
 
 
+def run_tier_bench(args):
+    """Bandwidth of the host KV tier: offload and prefetch of scattered rows of the
+    workload's pool between HBM and pinned host memory (NVLink-C2C on GB300)."""
+    import paged_kv_gqa_tokentokvpool_gb300 as pkv
+    wl = workloads.config_workload(args.config)
+    dev = torch.device("cuda")
+    rows = min(wl.total_tokens, 1 << 18)
+    t = workloads.layer_tensors(wl, 0, device=dev)
+    kh = torch.empty(rows, wl.n_kv_heads, wl.head_dim, dtype=torch.bfloat16).pin_memory()
+    vh = torch.empty_like(kh).pin_memory()
+    rng = np.random.default_rng(7)
+    dev_slots = torch.from_numpy(wl.kv_indices[:rows].copy()).to(dev)
+    host_slots = torch.from_numpy(rng.permutation(rows).astype(np.int32)).to(dev)
+    row_bytes = 2 * wl.n_kv_heads * wl.head_dim * 2
+    res = {}
+    for name, fn in (("offload", pkv.kvpool_offload), ("prefetch", pkv.kvpool_prefetch)):
+        for _ in range(args.warmup):
+            fn(t.k_pool, t.v_pool, dev_slots, kh, vh, host_slots)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn(t.k_pool, t.v_pool, dev_slots, kh, vh, host_slots)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        res[name] = {"us_per_call": ms * 1e3, "gbs_over_link": rows * row_bytes / (ms * 1e-3) / 1e9}
+    print(json.dumps({"metric": "host KV tier: scattered row moves HBM <-> pinned host memory",
+                      "unit": "GB/s", "rows": rows, "row_bytes": row_bytes,
+                      "workload": f"{wl.name}: {wl.description}", **res}), flush=True)
+    return 0
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -431,6 +465,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--separate-append", action="store_true",
                     help="run kvpool_append as its own kernel before each attention call")
+    ap.add_argument("--tier-bench", action="store_true",
+                    help="measure the host KV tier (offload / prefetch) instead of the step")
     ap.add_argument("--no-share", action="store_true",
                     help="plan the prefix-sharing workload without describing its shared prefixes")
     ap.add_argument("--no-graph", action="store_true",
@@ -444,6 +480,8 @@ def main(argv=None):
     world, rank, local = _dist()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.tier_bench:
+        return run_tier_bench(args)
 
     torch.cuda.set_device(local)
     pg = None

@@ -79,6 +79,29 @@ int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const voi
                   int64_t pool_slots, pkv_stream_t stream);
 
 /*
+ * kvpool_offload / kvpool_prefetch — the host KV tier: move pool rows between HBM
+ * and pinned host memory. When HBM is full, older KV rows move to CPU memory and are
+ * prefetched back when a request needs them again ("Agent-Infer", section "CPU 卸载").
+ *   offload : k_host[host_slots[i]] = k_pool[dev_slots[i]]   (and V), i < n
+ *   prefetch: k_pool[dev_slots[i]]  = k_host[host_slots[i]]  (and V)
+ *   k_pool, v_pool : [pool_slots, n_kv_heads, head_dim] bf16 device pools
+ *   k_host, v_host : [host_slots_cap, n_kv_heads, head_dim] bf16 in PINNED host memory
+ *                    (cudaHostAlloc / a pinned torch tensor), read and written by the
+ *                    GPU directly (NVLink-C2C on GB300); pageable memory is rejected
+ *                    with PKV_ERR_INVALID_ARG before any launch
+ *   dev_slots, host_slots : [n] int32 device arrays; destinations must be distinct
+ *                    (checked, with ranges, only when debug checks are on)
+ * Bit-exact copies; enqueued on `stream` (a side stream lets them overlap attention of
+ * other layers). The caller points the requests' kv_indices at the prefetched slots.
+ */
+int kvpool_offload(const void* k_pool, const void* v_pool, const int32_t* dev_slots, void* k_host,
+                   void* v_host, const int32_t* host_slots, int64_t n, int n_kv_heads,
+                   int head_dim, int64_t pool_slots, int64_t host_slots_cap, pkv_stream_t stream);
+int kvpool_prefetch(void* k_pool, void* v_pool, const int32_t* dev_slots, const void* k_host,
+                    const void* v_host, const int32_t* host_slots, int64_t n, int n_kv_heads,
+                    int head_dim, int64_t pool_slots, int64_t host_slots_cap, pkv_stream_t stream);
+
+/*
  * paged_decode_plan_create — allocate a reusable plan for one model shape.
  * Sizes every buffer once (pinned host staging, device work list, split
  * workspace) so that no decode step allocates ("Agent-Infer", section "优化历程",

@@ -37,7 +37,8 @@ PKV_ERR_INDEX = -5
 EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",
             "paged_decode_plan_info", "paged_decode_plan_status", "paged_decode_attn_static",
-            "paged_decode_append_attn", "paged_decode_plan_shared",
+            "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
+            "kvpool_prefetch",
             "pkv_set_debug_checks", "pkv_last_error")
 
 
@@ -66,6 +67,8 @@ def _load() -> ctypes.CDLL:
     lib.paged_decode_plan_host.argtypes = [P, I32, I32, I32, I32, I32, P, I32, P, I32, P, I32, P,
                                            P, I32, P, I32, P]
     lib.paged_decode_plan_shared.argtypes = [P, P, I32, P, I32, P, P]
+    lib.kvpool_offload.argtypes = [P, P, P, P, P, P, I64, I32, I32, I64, I64, P]
+    lib.kvpool_prefetch.argtypes = [P, P, P, P, P, P, I64, I32, I32, I64, I64, P]
     lib.paged_decode_plan_info.argtypes = [P, P, P, P, P, P]
     lib.paged_decode_plan_status.argtypes = [P, P]
     lib.paged_decode_attn_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32,
@@ -79,7 +82,8 @@ def _load() -> ctypes.CDLL:
     for name in ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
                  "paged_decode_attn", "paged_decode_plan_host", "paged_decode_plan_info",
                  "paged_decode_plan_status", "paged_decode_attn_static",
-                 "paged_decode_append_attn", "paged_decode_plan_shared"):
+                 "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
+                 "kvpool_prefetch"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -177,6 +181,42 @@ def kvpool_append(k_pool, v_pool, slot_ids, k_new, v_new, n=None, n_kv_heads=Non
                               _ptr(v_new), n, hkv if n_kv_heads is None else n_kv_heads,
                               d if head_dim is None else head_dim,
                               S if pool_slots is None else pool_slots, _stream(stream)))
+
+
+def _host_pool(t, name):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a (pinned) CPU tensor")
+    if t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous bf16 tensor")
+    return t
+
+
+def kvpool_offload(k_pool, v_pool, dev_slots, k_host, v_host, host_slots, stream=None) -> None:
+    """k_host[host_slots[i]] = k_pool[dev_slots[i]] (and V); host pools pinned."""
+    _dev(k_pool, torch.bfloat16, "k_pool")
+    _dev(v_pool, torch.bfloat16, "v_pool")
+    _dev(dev_slots, torch.int32, "dev_slots")
+    _dev(host_slots, torch.int32, "host_slots")
+    _host_pool(k_host, "k_host")
+    _host_pool(v_host, "v_host")
+    S, hkv, d = k_pool.shape
+    _check(library().kvpool_offload(_ptr(k_pool), _ptr(v_pool), _ptr(dev_slots), _ptr(k_host),
+                                    _ptr(v_host), _ptr(host_slots), dev_slots.numel(), hkv, d, S,
+                                    k_host.shape[0], _stream(stream)))
+
+
+def kvpool_prefetch(k_pool, v_pool, dev_slots, k_host, v_host, host_slots, stream=None) -> None:
+    """k_pool[dev_slots[i]] = k_host[host_slots[i]] (and V); host pools pinned."""
+    _dev(k_pool, torch.bfloat16, "k_pool")
+    _dev(v_pool, torch.bfloat16, "v_pool")
+    _dev(dev_slots, torch.int32, "dev_slots")
+    _dev(host_slots, torch.int32, "host_slots")
+    _host_pool(k_host, "k_host")
+    _host_pool(v_host, "v_host")
+    S, hkv, d = k_pool.shape
+    _check(library().kvpool_prefetch(_ptr(k_pool), _ptr(v_pool), _ptr(dev_slots), _ptr(k_host),
+                                     _ptr(v_host), _ptr(host_slots), dev_slots.numel(), hkv, d, S,
+                                     k_host.shape[0], _stream(stream)))
 
 
 def paged_decode_plan_create(max_batch: int, max_tokens: int, n_qo_heads: int,

@@ -115,6 +115,112 @@ int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const voi
 
 namespace {
 
+// GPU-visible address of a pool argument: device memory (want_host = false) or
+// pinned host memory mapped into the GPU's address space (want_host = true).
+// Pageable or unknown memory is rejected here, so it never reaches a kernel.
+int gpu_address(const char* who, const char* name, const void* p, bool want_host, void** out) {
+    cudaPointerAttributes attr{};
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PKV_ERR_INVALID_ARG, "%s: %s is not memory CUDA knows (%s)", who, name,
+                    cudaGetErrorString(e));
+    }
+    if (want_host) {
+        if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr)
+            return fail(PKV_ERR_INVALID_ARG,
+                        "%s: %s must be pinned host memory mapped for the GPU (cudaHostAlloc, "
+                        "or a pinned torch tensor)", who, name);
+        *out = attr.devicePointer;
+    } else {
+        if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+            return fail(PKV_ERR_INVALID_ARG, "%s: %s must be device memory", who, name);
+        *out = const_cast<void*>(p);
+    }
+    return PKV_OK;
+}
+
+int check_slots(const char* who, const char* name, const int32_t* slots, int64_t n, int64_t cap,
+                bool distinct, cudaStream_t stream) {
+    std::vector<int32_t> ids(n);
+    cudaError_t e = cudaMemcpyAsync(ids.data(), slots, n * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                    stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "debug copy of slot ids");
+    for (int64_t i = 0; i < n; ++i)
+        if (ids[i] < 0 || ids[i] >= cap)
+            return fail(PKV_ERR_INDEX, "%s: %s[%lld] = %d outside [0, %lld)", who, name, (long long)i,
+                        ids[i], (long long)cap);
+    if (distinct) {
+        std::sort(ids.begin(), ids.end());
+        for (int64_t i = 1; i < n; ++i)
+            if (ids[i] == ids[i - 1])
+                return fail(PKV_ERR_INDEX, "%s: %s repeats slot %d", who, name, ids[i]);
+    }
+    return PKV_OK;
+}
+
+// Shared by kvpool_offload and kvpool_prefetch: dst[dst_slots] = src[src_slots].
+int tier_copy(const char* who, bool to_host, const void* k_dev, const void* v_dev,
+              const int32_t* dev_slots, const void* k_host, const void* v_host,
+              const int32_t* host_slots, int64_t n, int n_kv_heads, int head_dim,
+              int64_t pool_slots, int64_t host_slots_cap, pkv_stream_t stream) {
+    if (n < 0) return fail(PKV_ERR_INVALID_ARG, "%s: n = %lld < 0", who, (long long)n);
+    if (n_kv_heads <= 0 || head_dim <= 0 || pool_slots <= 0 || host_slots_cap <= 0)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "%s: n_kv_heads, head_dim, pool_slots, host_slots_cap must be > 0", who);
+    const int64_t row_bytes = int64_t(n_kv_heads) * head_dim * 2;
+    if (row_bytes % 16 != 0)
+        return fail(PKV_ERR_UNSUPPORTED, "%s: row of %lld bytes is not a multiple of 16", who,
+                    (long long)row_bytes);
+    if (n == 0) return PKV_OK;
+    if (!k_dev || !v_dev || !dev_slots || !k_host || !v_host || !host_slots)
+        return fail(PKV_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
+    if (!aligned16(k_dev) || !aligned16(v_dev) || !aligned16(k_host) || !aligned16(v_host))
+        return fail(PKV_ERR_INVALID_ARG, "%s: pools must be 16-byte aligned", who);
+    void *kd = nullptr, *vd = nullptr, *kh = nullptr, *vh = nullptr;
+    int rc = gpu_address(who, "k_pool", k_dev, false, &kd);
+    if (rc == PKV_OK) rc = gpu_address(who, "v_pool", v_dev, false, &vd);
+    if (rc == PKV_OK) rc = gpu_address(who, "k_host", k_host, true, &kh);
+    if (rc == PKV_OK) rc = gpu_address(who, "v_host", v_host, true, &vh);
+    if (rc != PKV_OK) return rc;
+    if (!aligned16(kh) || !aligned16(vh))
+        return fail(PKV_ERR_INVALID_ARG, "%s: host pools must be 16-byte aligned", who);
+    if (debug_checks()) {
+        rc = check_slots(who, "dev_slots", dev_slots, n, pool_slots, !to_host, stream);
+        if (rc == PKV_OK)
+            rc = check_slots(who, "host_slots", host_slots, n, host_slots_cap, to_host, stream);
+        if (rc != PKV_OK) return rc;
+    }
+    cudaError_t e = to_host
+                        ? launch_tier_copy(kd, vd, dev_slots, kh, vh, host_slots, n,
+                                           static_cast<int>(row_bytes), stream)
+                        : launch_tier_copy(kh, vh, host_slots, kd, vd, dev_slots, n,
+                                           static_cast<int>(row_bytes), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launch");
+    return PKV_OK;
+}
+
+}  // namespace
+
+int kvpool_offload(const void* k_pool, const void* v_pool, const int32_t* dev_slots, void* k_host,
+                   void* v_host, const int32_t* host_slots, int64_t n, int n_kv_heads,
+                   int head_dim, int64_t pool_slots, int64_t host_slots_cap, pkv_stream_t stream) {
+    clear_error();
+    return tier_copy("kvpool_offload", true, k_pool, v_pool, dev_slots, k_host, v_host,
+                     host_slots, n, n_kv_heads, head_dim, pool_slots, host_slots_cap, stream);
+}
+
+int kvpool_prefetch(void* k_pool, void* v_pool, const int32_t* dev_slots, const void* k_host,
+                    const void* v_host, const int32_t* host_slots, int64_t n, int n_kv_heads,
+                    int head_dim, int64_t pool_slots, int64_t host_slots_cap, pkv_stream_t stream) {
+    clear_error();
+    return tier_copy("kvpool_prefetch", false, k_pool, v_pool, dev_slots, k_host, v_host,
+                     host_slots, n, n_kv_heads, head_dim, pool_slots, host_slots_cap, stream);
+}
+
+namespace {
+
 // Checks a sharing description against the step's contexts: runs of consecutive
 // requests, each member listing at least len + 1 slots (its newest token stays
 // private). Returns PKV_OK or an error code with the message set.

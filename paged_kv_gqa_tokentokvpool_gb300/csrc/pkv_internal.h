@@ -128,6 +128,12 @@ int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_p
 bool decode_has_shared_kernel(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// Row scatter between two pools (either may be pinned host memory mapped for the GPU):
+// dst[dst_slots[i]] = src[src_slots[i]] for K and V, i < n.
+cudaError_t launch_tier_copy(const void* k_src, const void* v_src, const int32_t* src_slots,
+                             void* k_dst, void* v_dst, const int32_t* dst_slots, int64_t n,
+                             int row_bytes, cudaStream_t stream);
+
 cudaError_t launch_append(void* k_pool, void* v_pool, const int32_t* slot_ids,
                           const void* k_new, const void* v_new, int64_t n, int row_bytes,
                           cudaStream_t stream);

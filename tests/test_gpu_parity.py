@@ -471,3 +471,84 @@ def test_shared_prefix_plan(pkv, case, fused):
     assert plan.status() == 0
     if d == 128 and hkv == 8:
         assert plan.info()["n_merges"] >= wl.batch  # every member merged its parts
+
+
+def test_host_tier_round_trip_then_attention(pkv):
+    """kvpool_offload + kvpool_prefetch are bit-exact row moves through pinned host
+    memory; attention over the prefetched slots equals the oracle on the original."""
+    dev = torch.device("cuda")
+    wl = workloads.scattered_workload([3000, 700, 12000], seed=41)
+    t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
+    kp, vp = t.k_pool.to(dev), t.v_pool.to(dev)
+    # the cold part of each context: its first half
+    cold = np.concatenate([wl.kv_indices[wl.kv_indptr[b]:wl.kv_indptr[b] + wl.lengths[b] // 2]
+                           for b in range(wl.batch)]).astype(np.int32)
+    n = cold.size
+    H = n + 100
+    kh = torch.zeros(H, 8, 128, dtype=torch.bfloat16).pin_memory()
+    vh = torch.zeros(H, 8, 128, dtype=torch.bfloat16).pin_memory()
+    host_slots = np.random.default_rng(3).permutation(H)[:n].astype(np.int32)
+    pkv.pkv_set_debug_checks(True)
+    try:
+        pkv.kvpool_offload(kp, vp, torch.from_numpy(cold).to(dev), kh, vh,
+                           torch.from_numpy(host_slots).to(dev))
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(kh)[host_slots], bits(t.k_pool)[cold])
+        assert np.array_equal(bits(vh)[host_slots], bits(t.v_pool)[cold])
+        # the device copies are gone (NaN); the rows come back to fresh slots
+        kp.view(torch.int16)[torch.from_numpy(cold).long().to(dev)] = workloads.BF16_NAN_BITS
+        vp.view(torch.int16)[torch.from_numpy(cold).long().to(dev)] = workloads.BF16_NAN_BITS
+        free = np.setdiff1d(np.arange(wl.pool_slots), wl.kv_indices)[:n].astype(np.int32)
+        pkv.kvpool_prefetch(kp, vp, torch.from_numpy(free).to(dev), kh, vh,
+                            torch.from_numpy(host_slots).to(dev))
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    assert np.array_equal(bits(kp)[free], bits(t.k_pool)[cold])
+    assert np.array_equal(bits(vp)[free], bits(t.v_pool)[cold])
+    remap = dict(zip(cold.tolist(), free.tolist()))
+    new_indices = np.array([remap.get(int(s), int(s)) for s in wl.kv_indices], np.int32)
+    # attention over the remapped lists (no append here: pools as generated)
+    out = torch.empty(wl.batch, 32, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(wl.batch, 32, dtype=torch.float32, device=dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, 32, 8, 128)
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    k_ref = bits(t.k_pool).copy()
+    v_ref = bits(t.v_pool).copy()
+    # the appended slots were never filled here: give them their generated new rows
+    k_ref = oracle.append(k_ref, wl.append_slots, bits(t.k_new))
+    v_ref = oracle.append(v_ref, wl.append_slots, bits(t.v_new))
+    kp.view(torch.int16)[torch.from_numpy(wl.append_slots).long().to(dev)] = \
+        torch.from_numpy(bits(t.k_new).view(np.int16)).to(dev)
+    vp.view(torch.int16)[torch.from_numpy(wl.append_slots).long().to(dev)] = \
+        torch.from_numpy(bits(t.v_new).view(np.int16)).to(dev)
+    pkv.paged_decode_attn(t.q.to(dev), kp, vp, torch.from_numpy(wl.kv_indptr).to(dev),
+                          torch.from_numpy(new_indices).to(dev), wl.batch, 32, 8, 128, wl.sm_scale,
+                          out, lse, plan)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.decode(bits(t.q), k_ref, v_ref, wl.kv_indptr, wl.kv_indices, 32, 8,
+                                     128, wl.sm_scale)
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what="after prefetch")
+
+
+def test_host_tier_rejects_pageable_and_duplicate_destinations(pkv):
+    dev = torch.device("cuda")
+    kp = torch.zeros(64, 8, 128, dtype=torch.bfloat16, device=dev)
+    pageable = torch.zeros(16, 8, 128, dtype=torch.bfloat16)
+    slots = torch.arange(4, dtype=torch.int32, device=dev)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.kvpool_offload(kp, kp, slots, pageable, pageable, slots)
+    assert e.value.code == pkv.PKV_ERR_INVALID_ARG
+    pinned = torch.zeros(16, 8, 128, dtype=torch.bfloat16).pin_memory()
+    pkv.pkv_set_debug_checks(True)
+    try:
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.kvpool_prefetch(kp, kp, torch.tensor([1, 1], dtype=torch.int32, device=dev),
+                                pinned, pinned, torch.tensor([0, 1], dtype=torch.int32, device=dev))
+        assert e.value.code == pkv.PKV_ERR_INDEX
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.kvpool_offload(kp, kp, slots, pinned, pinned,
+                               torch.tensor([0, 1, 2, 16], dtype=torch.int32, device=dev))
+        assert e.value.code == pkv.PKV_ERR_INDEX
+    finally:
+        pkv.pkv_set_debug_checks(False)
