@@ -33,26 +33,26 @@ kv_tier_copy_kernel(const uint4* __restrict__ k_src, const uint4* __restrict__ v
     for (int64_t base = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; base < total;
          base += stride * kTierUnroll) {
         uint4 val[kTierUnroll];
-        int64_t dst_index[kTierUnroll];
+        int64_t dst_index[kTierUnroll];  // -1: nothing to store
+        bool dst_v[kTierUnroll];
 #pragma unroll
         for (int u = 0; u < kTierUnroll; ++u) {  // all loads first
             const int64_t i = base + u * stride;
             dst_index[u] = -1;
+            dst_v[u] = false;
             if (i < total) {
                 const bool is_v = i >= per_pool;
                 const int64_t j = is_v ? i - per_pool : i;
                 const int64_t row = j / row_vecs, col = j - row * row_vecs;
                 const int64_t s = __ldg(src_slots + row), d = __ldg(dst_slots + row);
                 val[u] = (is_v ? v_src : k_src)[s * row_vecs + col];
-                dst_index[u] = (is_v ? per_pool : 0) + d * row_vecs + col;
+                dst_index[u] = d * row_vecs + col;
+                dst_v[u] = is_v;
             }
         }
 #pragma unroll
-        for (int u = 0; u < kTierUnroll; ++u) {
-            if (dst_index[u] < 0) continue;
-            const bool is_v = dst_index[u] >= per_pool;
-            (is_v ? v_dst : k_dst)[is_v ? dst_index[u] - per_pool : dst_index[u]] = val[u];
-        }
+        for (int u = 0; u < kTierUnroll; ++u)
+            if (dst_index[u] >= 0) (dst_v[u] ? v_dst : k_dst)[dst_index[u]] = val[u];
     }
 }
 
