@@ -20,7 +20,8 @@
 //    ring of 16-token tiles, signalled by mbarrier transaction counts; lane i
 //    copies token i%16's K (i < 16) or V (i >= 16) row. Four consumer warps take
 //    the tiles. Up to 3 x 32 KB per CTA is in flight, which covers HBM latency
-//    with two CTAs per SM.
+//    with two CTAs per SM. Rows read once carry an L2 evict-first policy; rows of
+//    a shared prefix, which the group's other prefix units read again, evict-last.
 //  * The consumers use the tensor cores for the two small contractions of a GQA
 //    group, so that all G query heads are served by one read of each K/V row and
 //    the instruction count per byte stays far below the issue rate:
@@ -139,6 +140,29 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Same, with an L2 cache policy (createpolicy) for the source lines.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// L2 policies: rows read once are evicted first; rows of a shared prefix, which the
+// other prefix units of the same group read again, are kept.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -236,6 +260,8 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     const char* new_rows = static_cast<const char*>(is_v ? a.v_new : a.k_new);
     const int64_t slot_bytes = int64_t(a.n_kv_heads) * D * 2;
     const uint32_t ring = smem_u32(smem) + (is_v ? C::kStageTokens * C::kRowP : 0) + tok * C::kRowP;
+    const uint64_t stream_policy = policy_evict_first();
+    const uint64_t shared_policy = policy_evict_last();
     int stage = 0;
     uint32_t empty_parity = 1;  // a fresh barrier reports the phase before it as complete
     uint32_t fill_parity = 0;
@@ -283,7 +309,8 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                     // fused append: the request's newest token comes from its new row
                     if (fused && un.tok_begin + t * C::kStageTokens + tok + kTile * j == un.len - 1)
                         src = new_rows + un.b * slot_bytes + group_off;
-                    bulk_g2s(ring + stage * C::kStage + j * kTile * C::kRowP, src, C::kRow, full_bar);
+                    bulk_g2s_hint(ring + stage * C::kStage + j * kTile * C::kRowP, src, C::kRow,
+                                  full_bar, un.nreq > 1 ? shared_policy : stream_policy);
                 }
             }
             filled_mask |= 1u << stage;
