@@ -46,7 +46,7 @@ class StepState:
     """Device tensors of one decode step for every layer, plus the plan."""
 
     def __init__(self, wl: workloads.Workload, device="cuda", layers=None,
-                 poison_unreferenced=False, fused=None, share=True):
+                 poison_unreferenced=False, fused=None, share=True, early=True):
         import paged_kv_gqa_tokentokvpool_gb300 as pkv
         self.pkv = pkv
         self.wl = wl
@@ -77,6 +77,14 @@ class StepState:
         # newest token that is its last listed slot (the decode steps here).
         can_fuse = len(wl.append_slots) == wl.batch and wl.batch > 0
         self.fused = can_fuse if fused is None else (fused and can_fuse)
+        # With the append fused, every row a layer reads was written before the
+        # step's plan upload (earlier steps, or inputs copied in before the plan),
+        # so the attention kernel may start gathering before the kernel ahead of it
+        # has finished (PKV_PLAN_EARLY_GATHER). A separate append kernel after the
+        # plan would break that promise.
+        self.early = bool(early and self.fused)
+        if self.early:
+            self.plan.set_flags(pkv.PKV_PLAN_EARLY_GATHER)
         # Requests that list the same prefix slots (the prefix-sharing workload) are
         # described to the planner, which then reads each shared slot once for
         # several requests.
@@ -469,6 +477,9 @@ def main(argv=None):
                     help="measure the host KV tier (offload / prefetch) instead of the step")
     ap.add_argument("--no-share", action="store_true",
                     help="plan the prefix-sharing workload without describing its shared prefixes")
+    ap.add_argument("--no-early", action="store_true",
+                    help="do not let the attention kernel gather before the previous kernel "
+                         "completes (PKV_PLAN_EARLY_GATHER off)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every layer eagerly instead of replaying a CUDA graph")
     ap.add_argument("--layers", type=int, default=None,
@@ -494,7 +505,8 @@ def main(argv=None):
     if args.layers is not None:
         wl.layers = max(1, min(args.layers, wl.layers))
         wl.description += f" [first {wl.layers} layers only]"
-    st = StepState(wl, fused=not args.separate_append, share=not args.no_share)
+    st = StepState(wl, fused=not args.separate_append, share=not args.no_share,
+                   early=not args.no_early)
     if not args.no_graph:
         st.capture()
     nbytes = step_bytes(wl)
@@ -575,6 +587,7 @@ def main(argv=None):
             "launch": "eager" if args.no_graph else "cuda graph of the layer loop per step; plan on host",
             "append": "fused into the attention launch" if st.fused else "separate kernel",
             "shared_prefixes": "described to the planner" if st.sharing is not None else "none",
+            "early_gather": st.early,
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -142,7 +142,7 @@ int paged_decode_plan(pkv_plan* plan, const int32_t* kv_indptr_host, int batch,
  * shared_len_host[s] slot ids first, s < n_shared; the runs are disjoint and in
  * batch order, and every member lists more slots than its shared prefix (its
  * newest token is private). The attention kernel then reads each shared slot once
- * for up to 16 / G requests at a time (two 8-row query blocks per KV head) instead
+ * for up to 16 / G requests at a time (16 query rows per KV head) instead
  * of once per request, and merges each member's prefix and suffix parts by
  * log-sum-exp. The description is a hint about equal slot ids: results are the
  * same as with paged_decode_plan (up to fp32 rounding), and for shapes without a
@@ -252,8 +252,9 @@ void paged_decode_plan_destroy(pkv_plan* plan);
  *   units_out      : [max_units * 8] int32 — per unit {request b, head group,
  *                    first token, end token (exclusive), first partial slot or -1
  *                    when the unit writes out/lse directly, requests served,
- *                    kv_indptr[b] + first token, context length of b or -1 for a
- *                    shared prefix}, listed CTA by CTA
+ *                    kv_indptr[b] + first token, context length of b, or for a
+ *                    shared prefix -2 when other units of its sharing group read
+ *                    the same slots and -1 when none does}, listed CTA by CTA
  *   cta_begin_out  : [ctas + 1] int32 — CTA c runs units [cta_begin[c], cta_begin[c+1]);
  *                    every CTA of the grid has an entry (possibly an empty range)
  *   merges_out     : [max_merges * 4] int32 — per (request, head group) with partial
@@ -275,6 +276,32 @@ int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_he
 /* paged_decode_plan_info — counts of the plan's current step (any out pointer may be NULL). */
 int paged_decode_plan_info(const pkv_plan* plan, int* batch, int* n_units, int* n_merges,
                            int* chunk_tokens, int* n_ctas);
+
+/* Flags for paged_decode_plan_set_flags. */
+#define PKV_PLAN_EARLY_GATHER 1u
+
+/*
+ * paged_decode_plan_set_flags — options for the attention calls that use `plan`
+ * (this library's own; the pages have no counterpart). Replaces the plan's flags.
+ *   PKV_PLAN_EARLY_GATHER: the caller promises that kv_indices and every K/V pool
+ *     row that the step's attention calls read were written by work enqueued on
+ *     the stream before this step's paged_decode_plan / paged_decode_plan_shared
+ *     call, and that nothing writes them between that call and the step's last
+ *     attention call. Exempt are the newest rows that paged_decode_append_attn
+ *     takes from k_new / v_new and writes itself. The attention kernel then starts
+ *     loading those rows as soon as it is scheduled, while the kernel before it on
+ *     the stream may still run (programmatic dependent launch); the work after the
+ *     plan's host-to-device copy has all started after the writes completed. q,
+ *     k_new, v_new and the newest rows are still read only after the previous
+ *     kernel has completed. This fits a step whose pool was filled by earlier
+ *     steps and whose new token is appended by paged_decode_append_attn. It does
+ *     not fit a step that calls kvpool_append or kvpool_prefetch after the plan.
+ *     Off by default; a broken promise gives stale rows, not an error.
+ *   flags : a bitwise OR of PKV_PLAN_* values (0 = none)
+ * Returns PKV_ERR_PLAN for a NULL plan and PKV_ERR_INVALID_ARG for unknown bits.
+ * Takes effect for attention calls enqueued after it returns.
+ */
+int paged_decode_plan_set_flags(pkv_plan* plan, unsigned flags);
 
 /*
  * paged_decode_plan_status — read and clear the plan's device status word

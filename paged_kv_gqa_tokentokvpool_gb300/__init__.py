@@ -33,12 +33,13 @@ PKV_ERR_UNSUPPORTED = -2
 PKV_ERR_PLAN = -3
 PKV_ERR_CUDA = -4
 PKV_ERR_INDEX = -5
+PKV_PLAN_EARLY_GATHER = 1
 
 EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",
             "paged_decode_plan_info", "paged_decode_plan_status", "paged_decode_attn_static",
             "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
-            "kvpool_prefetch",
+            "kvpool_prefetch", "paged_decode_plan_set_flags",
             "pkv_set_debug_checks", "pkv_last_error")
 
 
@@ -71,6 +72,7 @@ def _load() -> ctypes.CDLL:
     lib.kvpool_prefetch.argtypes = [P, P, P, P, P, P, I64, I32, I32, I64, I64, P]
     lib.paged_decode_plan_info.argtypes = [P, P, P, P, P, P]
     lib.paged_decode_plan_status.argtypes = [P, P]
+    lib.paged_decode_plan_set_flags.argtypes = [P, ctypes.c_uint]
     lib.paged_decode_attn_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32,
                                              ctypes.c_float, P, P, P]
     lib.paged_decode_append_attn.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I64,
@@ -83,7 +85,7 @@ def _load() -> ctypes.CDLL:
                  "paged_decode_attn", "paged_decode_plan_host", "paged_decode_plan_info",
                  "paged_decode_plan_status", "paged_decode_attn_static",
                  "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
-                 "kvpool_prefetch"):
+                 "kvpool_prefetch", "paged_decode_plan_set_flags"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -158,6 +160,10 @@ class Plan:
         v = ctypes.c_int()
         _check(library().paged_decode_plan_status(self.handle, ctypes.byref(v)))
         return v.value
+
+    def set_flags(self, flags: int) -> None:
+        """paged_decode_plan_set_flags (e.g. PKV_PLAN_EARLY_GATHER)."""
+        paged_decode_plan_set_flags(self, flags)
 
     def __del__(self):
         if getattr(self, "handle", None) and _lib is not None:
@@ -309,6 +315,12 @@ def paged_decode_attn_static(q, k_pool, v_pool, kv_indptr_host, kv_indptr, kv_in
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(ip), _ptr(kv_indptr), _ptr(kv_indices), batch,
         n_qo_heads, n_kv_heads, head_dim, float(sm_scale), _ptr(out), _ptr(lse),
         _stream(stream)))
+
+
+def paged_decode_plan_set_flags(plan: Plan, flags: int) -> None:
+    """Options of the attention calls that use the plan (PKV_PLAN_* bits)."""
+    _check(library().paged_decode_plan_set_flags(plan.handle if plan is not None else None,
+                                                 int(flags)))
 
 
 def paged_decode_plan_destroy(plan: Plan) -> None:

@@ -54,6 +54,14 @@ int choose_heads_per_cta(int n_kv_heads, int head_dim) {
     return hpg;
 }
 
+int shared_row_blocks() {
+    static const int rb = [] {
+        const char* env = std::getenv("PKV_SHARED_ROW_BLOCKS");
+        return env && std::atoi(env) == 2 ? 2 : 1;
+    }();
+    return rb;
+}
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char* env = std::getenv("PKV_PDL");
@@ -334,15 +342,14 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     }
     const int hpg = choose_heads_per_cta(n_kv_heads, head_dim);
     p->heads_per_cta = hpg;
-    // Shared-prefix units serve 16 / G requests (two 8-row query blocks per KV head)
-    // where a kernel for them exists; both kernels run on the same fixed grid.
-    p->share_rows = decode_has_shared_kernel(n_qo_heads, n_kv_heads, head_dim, hpg)
-                        ? 16 / (n_qo_heads / n_kv_heads)
+    p->ctas_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg, false);
+    // Shared-prefix units serve 16 x (row blocks) / G requests where a kernel for
+    // them exists; it runs on its own fixed grid.
+    const int shared_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg, true);
+    p->share_rows = shared_per_sm > 0
+                        ? decode_shared_rows(n_qo_heads, n_kv_heads, head_dim, hpg) /
+                              (n_qo_heads / n_kv_heads)
                         : 0;
-    p->ctas_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg, 1);
-    if (p->share_rows > 0)
-        p->ctas_per_sm = std::min(p->ctas_per_sm,
-                                  decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg, 2));
     if (p->ctas_per_sm <= 0) {
         delete p;
         return fail(PKV_ERR_CUDA, "paged_decode_plan_create: occupancy query failed");
@@ -354,24 +361,32 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
         if (want >= 1 && want < p->ctas_per_sm) p->ctas_per_sm = want;
     }
     p->ctas = p->num_sms * p->ctas_per_sm;
+    p->ctas_shared = p->share_rows > 0 ? p->num_sms * shared_per_sm : 0;
+    p->ctas_max = std::max(p->ctas, p->ctas_shared);
     p->max_batch = max_batch;
     p->max_tokens = max_tokens;
     p->n_qo_heads = n_qo_heads;
     p->n_kv_heads = n_kv_heads;
     p->head_dim = head_dim;
     p->n_groups = n_kv_heads / hpg;
-    p->lim.max_units = plan_max_units(p->ctas, max_batch, p->n_groups);
+    p->lim.max_units = plan_max_units(p->ctas_max, max_batch, p->n_groups);
     p->lim.max_merges = max_batch * p->n_groups;
     p->lim.max_partials = p->lim.max_units * std::max(1, p->share_rows);
     p->indptr_host.reserve(max_batch + 1);
     // staging layout: header[4] | cta_begin[ctas + 1] | merges[max_merges] |
     //                 part_list[max_partials] | units[max_units]
     p->off_cta = 16;
-    p->off_merge = round16(p->off_cta + sizeof(int32_t) * (p->ctas + 1));
+    p->off_merge = round16(p->off_cta + sizeof(int32_t) * (p->ctas_max + 1));
     p->off_list = round16(p->off_merge + sizeof(Merge) * p->lim.max_merges);
     p->off_units = round16(p->off_list + sizeof(int32_t) * p->lim.max_partials);
     p->meta_bytes = p->off_units + sizeof(Unit) * p->lim.max_units;
     const int group_q_heads = hpg * (n_qo_heads / n_kv_heads);
+    // The merge kernel runs one warp per (merged context, query head of its group),
+    // four warps a CTA: enough CTAs for the largest step to need one pass, up to
+    // four per SM.
+    const int64_t merge_warps = int64_t(p->lim.max_merges) * group_q_heads;
+    p->merge_ctas = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>((merge_warps + 3) / 4, int64_t(p->num_sms) * 4)));
     const size_t ws_o_bytes = sizeof(float) * size_t(p->lim.max_partials) * group_q_heads * head_dim;
     const size_t ws_lse_bytes = sizeof(float) * size_t(p->lim.max_partials) * group_q_heads;
     const size_t state_bytes = sizeof(int) * 32;
@@ -427,7 +442,8 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
     }
     char* st = static_cast<char*>(p->host_staging);
     PlanCounts c{};
-    rc = plan_compute(kv_indptr_host, batch, p->n_groups, p->ctas, p->lim, share ? &sh : nullptr,
+    const int ctas = share ? p->ctas_shared : p->ctas;
+    rc = plan_compute(kv_indptr_host, batch, p->n_groups, ctas, p->lim, share ? &sh : nullptr,
                       reinterpret_cast<Unit*>(st + p->off_units),
                       reinterpret_cast<int32_t*>(st + p->off_cta),
                       reinterpret_cast<Merge*>(st + p->off_merge),
@@ -444,7 +460,8 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
     p->copy_pending = true;
     p->batch = batch;
     p->counts = c;
-    p->n_blocks = share ? 2 : 1;
+    p->shared = share;
+    p->launch_ctas = ctas;
     p->indptr_host.assign(kv_indptr_host, kv_indptr_host + batch + 1);
     p->planned = true;
     return PKV_OK;
@@ -474,6 +491,16 @@ int paged_decode_plan_info(const pkv_plan* p, int* batch, int* n_units, int* n_m
     if (n_merges) *n_merges = p->counts.n_merges;
     if (chunk_tokens) *chunk_tokens = p->counts.chunk_tokens;
     if (n_ctas) *n_ctas = p->counts.n_ctas;
+    return PKV_OK;
+}
+
+int paged_decode_plan_set_flags(pkv_plan* p, unsigned flags) {
+    clear_error();
+    if (!p) return fail(PKV_ERR_PLAN, "paged_decode_plan_set_flags: plan is NULL");
+    if (flags & ~PKV_PLAN_EARLY_GATHER)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_set_flags: unknown flags 0x%x",
+                    flags & ~PKV_PLAN_EARLY_GATHER);
+    p->flags = flags;
     return PKV_OK;
 }
 
@@ -571,8 +598,9 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
     a.merges = reinterpret_cast<const Merge*>(meta + p->off_merge);
     a.part_list = reinterpret_cast<const int32_t*>(meta + p->off_list);
     a.units = reinterpret_cast<const Unit*>(meta + p->off_units);
-    a.n_ctas = p->ctas;
-    a.n_blocks = p->n_blocks;
+    a.n_ctas = p->launch_ctas;
+    a.shared = p->shared;
+    a.early = (p->flags & PKV_PLAN_EARLY_GATHER) != 0;
     a.heads_per_cta = p->heads_per_cta;
     a.n_qo_heads = n_qo_heads;
     a.n_kv_heads = n_kv_heads;
@@ -582,7 +610,7 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
     a.lse = lse;
     a.ws_o = p->ws_o;
     a.ws_lse = p->ws_lse;
-    a.merge_ctas = p->num_sms;
+    a.merge_ctas = p->merge_ctas;
     a.status = p->dev_state;
     a.zero_row = p->zero_row;
     a.k_new = fused ? k_new : nullptr;

@@ -101,7 +101,7 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     unsigned char* scratch = static_cast<unsigned char*>(g_scratch_addr[dev]);
 
     const int hpc = choose_heads_per_cta(n_kv_heads, head_dim);
-    const int per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpc, 1);
+    const int per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpc, false);
     if (per_sm <= 0) return fail(PKV_ERR_CUDA, "paged_decode_attn_static: occupancy query failed");
     const int ctas = sms * per_sm;
     if (ctas > kMaxCtas)
@@ -152,7 +152,8 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     a.cta_begin = reinterpret_cast<const int32_t*>(scratch + kOffCta);
     a.merges = reinterpret_cast<const Merge*>(scratch + kOffMerge);
     a.part_list = reinterpret_cast<const int32_t*>(scratch + kOffList);
-    a.n_blocks = 1;
+    a.shared = false;
+    a.early = false;
     a.units = reinterpret_cast<const Unit*>(scratch + kOffUnits);
     a.n_ctas = ctas;
     a.heads_per_cta = hpc;

@@ -20,8 +20,14 @@
 //    ring of 16-token tiles, signalled by mbarrier transaction counts; lane i
 //    copies token i%16's K (i < 16) or V (i >= 16) row. Four consumer warps take
 //    the tiles. Up to 3 x 32 KB per CTA is in flight, which covers HBM latency
-//    with two CTAs per SM. Rows read once carry an L2 evict-first policy; rows of
-//    a shared prefix, which the group's other prefix units read again, evict-last.
+//    with two CTAs per SM. The slot ids themselves travel kStages + 1 stages
+//    ahead of the copies (cp.async into a small shared ring), so no stage waits a
+//    round trip for its ids. Rows read once carry an L2 evict-first policy; rows
+//    of a shared prefix, which the group's other prefix units read again,
+//    evict-last.
+//  * Programmatic dependent launch: the plan is read before waiting for the
+//    previous kernel; with PKV_PLAN_EARLY_GATHER the slot ids and old pool rows
+//    are too, so a layer's ring fills while the kernel ahead of it finishes.
 //  * The consumers use the tensor cores for the two small contractions of a GQA
 //    group, so that all G query heads are served by one read of each K/V row and
 //    the instruction count per byte stays far below the issue rate:
@@ -52,9 +58,7 @@ namespace pkv {
 namespace {
 
 constexpr int kTile = 16;           // tokens per pipeline stage (one mma M block)
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kStages = 3;
+constexpr int kGroupWarps = 4;      // consumer warps that cover one head group's rows of q
 constexpr int kRowPad = 16;         // bytes between staged rows: conflict-free ldmatrix
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -123,16 +127,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
     }
 }
 
-// 1D bulk copy global -> shared (TMA), completing `bytes` on mbarrier `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 // Programmatic dependent launch (PTX griddepcontrol): let the next kernel on the
 // stream be scheduled now / wait until the previous kernel's results are visible.
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -140,7 +134,8 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Same, with an L2 cache policy (createpolicy) for the source lines.
+// 1D bulk copy global -> shared (TMA), completing `bytes` on mbarrier `bar`, with an
+// L2 cache policy (createpolicy) for the source lines.
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar, uint64_t policy) {
     asm volatile(
@@ -161,6 +156,18 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// 4-byte asynchronous copy global -> shared (cp.async), completed by commit/wait groups.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
@@ -214,14 +221,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------
 
 // Shapes of one instance: head_dim D, GQA group G, WPH consumer warps per KV
-// head (so 4 / WPH KV heads per CTA). A pipeline stage holds kSub 16-token
+// head (so 4 / WPH KV heads per CTA), NB 8-row query blocks per warp and RB row
+// blocks of warps. A unit's query rows (row r = head r % G of its request r / G)
+// are dealt to RB sets of four warps, 8 NB rows each: RB = 1 serves 8 NB / G
+// requests per unit with two CTAs per SM; RB = 2 doubles the warps and the ring
+// and runs one CTA per SM, so each K/V row staged in shared memory serves
+// 16 NB / G requests (measured slower: one CTA per SM leaves half its warps idle
+// on units of one request). A pipeline stage holds kSub 16-token
 // sub-tiles of K rows and of V rows of the CTA's kHeadsPerCta heads; kSub is
 // chosen so that every stage carries 16 x kHeadGroupElems bf16 of K and as much
 // of V (32 KB, plus row padding) whatever the head count.
-template <int D, int G, int WPH, int NB = 1>
+template <int D, int G, int WPH, int NB = 1, int RB = 1>
 struct Cfg {
-    static constexpr int kBlocks = NB;  // 8-row query blocks per KV head (rows of NB*8/G requests)
-    static constexpr int kHeadsPerCta = kConsumerWarps / WPH;   // KV heads of one group
+    static constexpr int kConsumerWarps = kGroupWarps * RB;
+    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
+    static constexpr int kStages = 3 * RB;                      // 32 KB stages in flight
+    static constexpr int kMinBlocks = 2 / RB;                   // resident CTAs per SM
+    static constexpr int kWarpRows = 8 * NB;                    // query rows of one warp
+    static constexpr int kHeadsPerCta = kGroupWarps / WPH;      // KV heads of one group
     static constexpr int kRow = kHeadsPerCta * D * 2;           // bytes of a staged row
     static constexpr int kRowP = kRow + kRowPad;
     static constexpr int kSub = kHeadGroupElems / (kHeadsPerCta * D);  // sub-tiles per stage
@@ -232,10 +249,13 @@ struct Cfg {
     static constexpr int kMBlocks = D / 16 / WPH;               // O^T dim blocks per warp
     static constexpr int kDimsPerWarp = D / WPH;
     static constexpr int kQHeads = kHeadsPerCta * G;            // query heads of a group
+    static constexpr int kAhead = kStages + 1;                  // stages of slot ids in flight
     static constexpr int kBarOffset = kStages * kStage;
-    static constexpr int kSmem = kBarOffset + 2 * kStages * 8 + 16;
+    static constexpr int kIdxOffset = kBarOffset + 2 * kStages * 8 + 16;
+    static constexpr int kSmem = kIdxOffset + kAhead * kStageTokens * 4;
     static_assert(G >= 1 && G <= 8, "group size");
     static_assert(NB == 1 || NB == 2, "query blocks");
+    static_assert(RB == 1 || RB == 2, "row blocks");
     static_assert(kHeadsPerCta * D * kSub == kHeadGroupElems, "stage budget");
     static_assert(kMBlocks >= 1, "dims per warp");
 };
@@ -246,12 +266,47 @@ struct Shared {
     volatile int* flags;  // [0] abort
 };
 
+__device__ __forceinline__ int unit_stages(const Unit& un, int stage_tokens) {
+    const int n_tok = un.tok_end - un.tok_begin;
+    return n_tok > 0 ? (n_tok + stage_tokens - 1) / stage_tokens : 1;
+}
+
+// The slot ids of the stages ahead of the copies: the producer walks the CTA's
+// stages twice, once here to start the slot-id loads (cp.async into a shared-memory
+// ring of kAhead stages) and kAhead stages later to issue the row copies, so a
+// stage's copies never wait a round trip for its slot ids.
+struct SlotFetch {
+    int u, t, n_stages;  // next stage to fetch: stage t of unit u
+    Unit un;
+    int pos;             // its place in the ring
+};
+
+template <class C>
+__device__ __forceinline__ void fetch_slot_ids(const DecodeArgs& a, SlotFetch& f, int u_end,
+                                               int lane, uint32_t ring) {
+    if (f.u < u_end) {
+        const int n = min(C::kStageTokens, (f.un.tok_end - f.un.tok_begin) - f.t * C::kStageTokens);
+        const int32_t* idx = a.kv_indices + f.un.idx_begin + f.t * C::kStageTokens;
+        const uint32_t dst = ring + f.pos * C::kStageTokens * 4;
+        for (int i = lane; i < n; i += 32) cp_async4(dst + 4 * i, idx + i);
+        if (++f.t == f.n_stages) {
+            f.t = 0;
+            if (++f.u < u_end) {
+                f.un = a.units[f.u];
+                f.n_stages = unit_stages(f.un, C::kStageTokens);
+            }
+        }
+    }
+    cp_async_commit();  // one group per stage (empty past the end)
+    if (++f.pos == C::kAhead) f.pos = 0;
+}
+
 // Producer warp: lane l copies, for every sub-tile j of a stage, token
 // (l % 16) + 16 j's K row (l < 16) or V row (l >= 16) of the CTA's head group.
-template <int D, int G, int WPH, int NB>
+template <int D, int G, int WPH, int NB, int RB>
 __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
-    using C = Cfg<D, G, WPH, NB>;
+    using C = Cfg<D, G, WPH, NB, RB>;
     const int lane = threadIdx.x & 31;
     const int tok = lane & (kTile - 1);
     const bool is_v = lane >= kTile;
@@ -260,6 +315,8 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     const char* new_rows = static_cast<const char*>(is_v ? a.v_new : a.k_new);
     const int64_t slot_bytes = int64_t(a.n_kv_heads) * D * 2;
     const uint32_t ring = smem_u32(smem) + (is_v ? C::kStageTokens * C::kRowP : 0) + tok * C::kRowP;
+    const uint32_t id_ring = smem_u32(smem) + C::kIdxOffset;
+    const int32_t* id_ring_ptr = reinterpret_cast<const int32_t*>(smem + C::kIdxOffset);
     const uint64_t stream_policy = policy_evict_first();
     const uint64_t shared_policy = policy_evict_last();
     int stage = 0;
@@ -270,13 +327,26 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     // The next unit's descriptor is loaded one unit ahead, and its slot ids are
     // prefetched into L2 once the current unit's first stage is on its way.
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
-    pdl_wait();  // slot ids and pools may come from the previous kernel
+    // Slot ids and pool rows may come from the previous kernel: wait for it, after
+    // warming L2 with the first unit's slot ids (prefetches are hints, not reads).
+    // With early gather they were final before the step's plan upload, so the
+    // loads start at once and only the fused append's new rows wait.
+    bool waited = !a.early;
+    if (u_begin < u_end)
+        for (int off = 32 * lane; off < next.tok_end - next.tok_begin && off < 32 * 32 * 4;
+             off += 32 * 32)
+            prefetch_l2(a.kv_indices + next.idx_begin + off);
+    if (waited) pdl_wait();
+    SlotFetch f{u_begin, 0, u_begin < u_end ? unit_stages(next, C::kStageTokens) : 0, next, 0};
+#pragma unroll 1
+    for (int i = 0; i < C::kAhead; ++i) fetch_slot_ids<C>(a, f, u_end, lane, id_ring);
+    int pos = 0;  // ring place of the stage being issued
     for (int u = u_begin; u < u_end && !aborted; ++u) {
         const Unit un = next;
         if (u + 1 < u_end) next = a.units[u + 1];
         const int32_t* idx = a.kv_indices + un.idx_begin;
         const int n_tok = un.tok_end - un.tok_begin;
-        const int n_stages = n_tok > 0 ? (n_tok + C::kStageTokens - 1) / C::kStageTokens : 1;
+        const int n_stages = unit_stages(un, C::kStageTokens);
         const int64_t group_off = int64_t(un.hg) * C::kRow;
         for (int off = 32 * (lane + 1); off < n_tok; off += 32 * 32) prefetch_l2(idx + off);
         for (int t = 0; t < n_stages; ++t) {
@@ -286,10 +356,6 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                     prefetch_l2(nidx + off);
             }
             const int n = min(C::kStageTokens, n_tok - t * C::kStageTokens);
-            int slot[C::kSub];
-#pragma unroll
-            for (int j = 0; j < C::kSub; ++j)
-                slot[j] = tok + kTile * j < n ? __ldg(idx + t * C::kStageTokens + tok + kTile * j) : -1;
             const uint32_t full_bar = smem_u32(&sh.full[stage]);
             if (lane == 0 && !mbar_wait(smem_u32(&sh.empty[stage]), empty_parity, a.status, sh.flags))
                 sh.flags[0] = 1;
@@ -297,6 +363,20 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             if (sh.flags[0]) {
                 aborted = true;
                 break;
+            }
+            // this stage's slot ids (the oldest group in flight) have landed
+            cp_async_wait<C::kAhead - 1>();
+            __syncwarp();
+            int slot[C::kSub];
+#pragma unroll
+            for (int j = 0; j < C::kSub; ++j)
+                slot[j] = tok + kTile * j < n ? id_ring_ptr[pos * C::kStageTokens + tok + kTile * j] : -1;
+            __syncwarp();  // every lane has read its ids before the place is refilled below
+            // k_new / v_new may come from the previous kernel
+            const int first = un.tok_begin + t * C::kStageTokens;
+            if (!waited && fused && un.len - 1 >= first && un.len - 1 < first + n) {
+                pdl_wait();
+                waited = true;
             }
             if (lane == 0) mbar_arrive_expect_tx(full_bar, n > 0 ? C::kStageTx : 0u);
             __syncwarp();
@@ -307,24 +387,28 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                                           ? static_cast<const void*>(pool + slot[j] * slot_bytes + group_off)
                                           : a.zero_row;
                     // fused append: the request's newest token comes from its new row
-                    if (fused && un.tok_begin + t * C::kStageTokens + tok + kTile * j == un.len - 1)
+                    if (fused && first + tok + kTile * j == un.len - 1)
                         src = new_rows + un.b * slot_bytes + group_off;
                     bulk_g2s_hint(ring + stage * C::kStage + j * kTile * C::kRowP, src, C::kRow,
-                                  full_bar, un.nreq > 1 ? shared_policy : stream_policy);
+                                  full_bar, un.len == -2 ? shared_policy : stream_policy);
                 }
             }
+            fetch_slot_ids<C>(a, f, u_end, lane, id_ring);  // refills place `pos`
+            if (++pos == C::kAhead) pos = 0;
             filled_mask |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (fill_parity << stage);
-            if (++stage == kStages) {
+            if (++stage == C::kStages) {
                 stage = 0;
                 empty_parity ^= 1;
                 fill_parity ^= 1;
             }
         }
     }
-    // No bulk copy may still be writing this CTA's shared memory when it exits.
+    // No copy (bulk or slot-id) may still be writing this CTA's shared memory when
+    // it exits.
+    cp_async_wait<0>();
     if (lane == 0) {
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < C::kStages; ++s)
             if (filled_mask & (1u << s)) {
                 const uint32_t bar = smem_u32(&sh.full[s]);
                 const uint32_t par = (parity_bits >> s) & 1u;
@@ -337,19 +421,19 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     }
 }
 
-// Q^T as the B operand of S^T = K Q^T: query block nb holds the rows 8 nb .. 8 nb + 7
-// of the unit's query set, row r being head r % G of request b + r / G; lane l holds
-// row 8 nb + l / 4, dims 2 (l % 4) .. of each k-step. Rows beyond the unit's
-// requests are zero.
-template <int D, int G, int WPH, int NB>
-__device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit& un, int hh, int g,
-                                                 int t4,
-                                                 uint32_t (&qf)[NB][Cfg<D, G, WPH, NB>::kKSteps][2]) {
-    using C = Cfg<D, G, WPH, NB>;
+// Q^T as the B operand of S^T = K Q^T: query block nb of a warp with row base r0
+// holds the rows r0 + 8 nb .. r0 + 8 nb + 7 of the unit's query set, row r being
+// head r % G of request b + r / G; lane l holds row r0 + 8 nb + l / 4, dims
+// 2 (l % 4) .. of each k-step. Rows beyond the unit's requests are zero.
+template <int D, int G, int WPH, int NB, int RB>
+__device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit& un, int hh, int r0,
+                                                 int g, int t4,
+                                                 uint32_t (&qf)[NB][Cfg<D, G, WPH, NB, RB>::kKSteps][2]) {
+    using C = Cfg<D, G, WPH, NB, RB>;
     const int kvh = un.hg * C::kHeadsPerCta + hh;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-        const int r = 8 * nb + g;
+        const int r = r0 + 8 * nb + g;
         const bool valid = r / G < un.nreq;
         const uint32_t* row = reinterpret_cast<const uint32_t*>(
             static_cast<const __nv_bfloat16*>(a.q) +
@@ -364,11 +448,11 @@ __device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit
 
 // Fused append: copy this warp's part (head hh, dims of `part`) of the staged new
 // K and V rows of request un.b from shared memory to pool slot slot_ids[un.b].
-template <int D, int G, int WPH, int NB>
+template <int D, int G, int WPH, int NB, int RB>
 __device__ __forceinline__ void store_new_rows(const DecodeArgs& a, const Unit& un,
                                                const uint8_t* smem, int stage, int row, int hh,
                                                int part, int lane) {
-    using C = Cfg<D, G, WPH, NB>;
+    using C = Cfg<D, G, WPH, NB, RB>;
     constexpr int kBytes = C::kDimsPerWarp * 2;  // bytes of this warp's share of one row
     const int64_t slot = __ldg(a.slot_ids + un.b);
     const int64_t dst_off = slot * int64_t(a.n_kv_heads) * D * 2 +
@@ -383,13 +467,15 @@ __device__ __forceinline__ void store_new_rows(const DecodeArgs& a, const Unit& 
     }
 }
 
-template <int D, int G, int WPH, int NB>
+template <int D, int G, int WPH, int NB, int RB>
 __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
-    using C = Cfg<D, G, WPH, NB>;
+    using C = Cfg<D, G, WPH, NB, RB>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hh = warp / WPH;    // KV head within the group
-    const int part = warp % WPH;  // which slice of head_dim this warp accumulates
+    const int wg = warp % kGroupWarps;
+    const int hh = wg / WPH;      // KV head within the group
+    const int part = wg % WPH;    // which slice of head_dim this warp accumulates
+    const int r0 = (warp / kGroupWarps) * C::kWarpRows;  // first query row of this warp
     const int g = lane >> 2, t4 = lane & 3;
     const int hq = a.n_qo_heads;
     const float scale_log2 = a.sm_scale * kLog2e;
@@ -409,9 +495,16 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     constexpr bool kPrefetchQ = NB == 1;
     uint32_t qb[NB][C::kKSteps][2], qn[NB][C::kKSteps][2];
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
+    // Warm L2 with the first unit's q rows (a hint, safe before the wait): lane l
+    // touches query row r0 + l of this warp's KV head.
+    if (u_begin < u_end && lane < C::kWarpRows && (r0 + lane) / G < next.nreq) {
+        const int kvh = next.hg * C::kHeadsPerCta + hh;
+        prefetch_l2(static_cast<const __nv_bfloat16*>(a.q) +
+                    (int64_t(next.b + (r0 + lane) / G) * a.n_qo_heads + kvh * G + (r0 + lane) % G) * D);
+    }
     pdl_wait();  // q may come from the previous kernel
     if constexpr (kPrefetchQ) {
-        if (u_begin < u_end) load_q_fragments<D, G, WPH, NB>(a, next, hh, g, t4, qn);
+        if (u_begin < u_end) load_q_fragments<D, G, WPH, NB, RB>(a, next, hh, r0, g, t4, qn);
     }
     for (int u = u_begin; u < u_end; ++u) {
         const Unit un = next;
@@ -425,12 +518,14 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                     qb[nb][ks][1] = qn[nb][ks][1];
                 }
         } else {
-            load_q_fragments<D, G, WPH, NB>(a, un, hh, g, t4, qb);
+            load_q_fragments<D, G, WPH, NB, RB>(a, un, hh, r0, g, t4, qb);
         }
         if (u + 1 < u_end) {
             next = a.units[u + 1];
-            if constexpr (kPrefetchQ) load_q_fragments<D, G, WPH, NB>(a, next, hh, g, t4, qn);
+            if constexpr (kPrefetchQ) load_q_fragments<D, G, WPH, NB, RB>(a, next, hh, r0, g, t4, qn);
         }
+        // A warp whose rows are all beyond the unit's requests only passes the stages on.
+        const bool active = r0 / G < un.nreq;
         // softmax state per query block and column (heads 2 t4, 2 t4 + 1 of the block)
         float m[NB][2], l[NB][2];
         float o[NB][C::kMBlocks][4];
@@ -450,16 +545,16 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             if (!__all_sync(kFull, ok)) return;  // uniform exit: no lane is left in a shuffle
             const int n_stage = n_tok - t * C::kStageTokens;
             // Fused append: the stage holding the request's newest token has its new
-            // K/V rows (copied from k_new / v_new); write this warp's share of them
-            // to the pool slot before the stage is released.
-            if (a.k_new != nullptr) {
+            // K/V rows (copied from k_new / v_new); the first row block's warps write
+            // their share of them to the pool slot before the stage is released.
+            if (a.k_new != nullptr && r0 == 0) {
                 const int row = un.len - 1 - (un.tok_begin + t * C::kStageTokens);
                 if (row >= 0 && row < n_stage && row < C::kStageTokens)
-                    store_new_rows<D, G, WPH, NB>(a, un, smem, stage, row, hh, part, lane);
+                    store_new_rows<D, G, WPH, NB, RB>(a, un, smem, stage, row, hh, part, lane);
             }
 #pragma unroll
             for (int j = 0; j < C::kSub; ++j) {
-                const int n = n_stage - j * kTile;  // valid rows of this sub-tile (if > 0)
+                const int n = active ? n_stage - j * kTile : 0;  // valid rows of this sub-tile
                 if (n <= 0) break;
                 const uint32_t st = stage * C::kStage + j * kTile * C::kRowP;
                 float s[NB][4];
@@ -523,13 +618,14 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh.empty[stage]));
-            if (++stage == kStages) {
+            if (++stage == C::kStages) {
                 stage = 0;
                 full_parity ^= 1;
             }
         }
 
-        // ---- epilogue: o[nb][mb][0..3] = (dim 16*mb' + g (+8), rows 8nb + 2t4, +1)
+        // ---- epilogue: o[nb][mb][0..3] = (dim 16*mb' + g (+8), rows r0 + 8nb + 2t4, +1)
+        if (!active) continue;
         const int dim0 = part * C::kDimsPerWarp + g;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
@@ -538,7 +634,7 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                 float lt = l[nb][jc];
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) lt += __shfl_xor_sync(kFull, lt, off);
-                const int r = 8 * nb + 2 * t4 + jc;
+                const int r = r0 + 8 * nb + 2 * t4 + jc;
                 const int req = r / G, h = r % G;
                 if (req >= un.nreq) continue;
                 const float inv = lt == 0.f ? 0.f : 1.f / lt;
@@ -568,18 +664,19 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     }
 }
 
-template <int D, int G, int WPH, int NB>
-__global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeArgs a) {
-    using C = Cfg<D, G, WPH, NB>;
+template <int D, int G, int WPH, int NB, int RB>
+__global__ void __launch_bounds__(Cfg<D, G, WPH, NB, RB>::kThreads, Cfg<D, G, WPH, NB, RB>::kMinBlocks)
+    paged_decode_kernel(const DecodeArgs a) {
+    using C = Cfg<D, G, WPH, NB, RB>;
     extern __shared__ __align__(128) uint8_t smem[];
     Shared sh;
     sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-    sh.empty = sh.full + kStages;
-    sh.flags = reinterpret_cast<volatile int*>(sh.empty + kStages);
+    sh.empty = sh.full + C::kStages;
+    sh.flags = reinterpret_cast<volatile int*>(sh.empty + C::kStages);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
-            mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
+            mbar_init(smem_u32(&sh.empty[s]), C::kConsumerWarps);
         }
         sh.flags[0] = 0;
         fence_mbar_init();
@@ -590,10 +687,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeA
     pdl_launch_dependents();
     const int u_begin = a.cta_begin[blockIdx.x];
     const int u_end = a.cta_begin[blockIdx.x + 1];
-    if ((threadIdx.x >> 5) == kConsumerWarps)
-        producer_warp<D, G, WPH, NB>(a, smem, sh, u_begin, u_end);
+    if ((threadIdx.x >> 5) == C::kConsumerWarps)
+        producer_warp<D, G, WPH, NB, RB>(a, smem, sh, u_begin, u_end);
     else
-        consumer_warp<D, G, WPH, NB>(a, smem, sh, u_begin, u_end);
+        consumer_warp<D, G, WPH, NB, RB>(a, smem, sh, u_begin, u_end);
 }
 
 // ---------------------------------------------------------------------------
@@ -608,8 +705,30 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_kernel(const DecodeA
 // fixed grid (warps loop over the work), so the launch does not depend on the step.
 constexpr int kMergeThreads = 128;
 
+// Issue the loads of parts c0 .. c0 + kChunk - 1 of one merged context's query
+// head: lane l receives dims l * D / 32 .. of every part (zeros past the count).
+template <int D, int kChunk>
+__device__ __forceinline__ void merge_load_chunk(const DecodeArgs& a, const int32_t* parts,
+                                                 int count, int c0, int slot_l, int qheads,
+                                                 int qh, int lane,
+                                                 float4 (&x)[kChunk][D / 128]) {
+    constexpr int kVD = D / 32;
+    const int c = c0 + (lane % kChunk);
+    const int from_lane = __shfl_sync(kFull, slot_l, c & 31);  // every lane shuffles
+    const int slot_c = c < count ? (c < 32 ? from_lane : __ldg(parts + c)) : 0;
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+        const int slot = __shfl_sync(kFull, slot_c, j);
+        const float* src = a.ws_o + (int64_t(slot) * qheads + qh) * D + lane * kVD;
+#pragma unroll
+        for (int i = 0; i < kVD / 4; ++i)
+            x[j][i] = c0 + j < count ? __ldcg(reinterpret_cast<const float4*>(src) + i)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kMergeThreads, 4) lse_merge_kernel(const DecodeArgs a) {
     pdl_launch_dependents();
     constexpr int kVD = D / 32;  // dims per lane
     const int lane = threadIdx.x & 31;
@@ -630,15 +749,22 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeAr
         if (lane < mg.count) slot_l = __ldg(a.part_list + mg.first + lane);
     }
     pdl_wait();  // the partial results come from the decode kernel
+    // Parts in chunks of kChunk: every load of a chunk is issued before the first
+    // use, so a chunk costs one round trip to L2; the first chunk's outputs are
+    // issued together with the log-sum-exp pass, which does not need them.
+    constexpr int kChunk = kVD == 4 ? 16 : 8;
     for (; w < items; w += warps) {
         const int qh = w % qheads;
         const int32_t* parts = a.part_list + mg.first;
-        float mx = neg_inf(), sm = 0.f;
+        float4 x[kChunk][kVD / 4];
+        merge_load_chunk<D, kChunk>(a, parts, mg.count, 0, slot_l, qheads, qh, lane, x);
+        float mx = neg_inf(), sm = 0.f, lse_l = neg_inf();  // lse_l: part `lane`'s lse
         for (int c = lane; c < mg.count; c += 32) {
             const int slot = c < 32 ? slot_l : __ldg(parts + c);
-            const float x = __ldcg(a.ws_lse + int64_t(slot) * qheads + qh);
-            const float mn = fmaxf(mx, x);
-            sm = (mx == neg_inf() ? 0.f : sm * ex2(mx - mn)) + ex2(x - mn);
+            const float xl = __ldcg(a.ws_lse + int64_t(slot) * qheads + qh);
+            if (c < 32) lse_l = xl;
+            const float mn = fmaxf(mx, xl);
+            sm = (mx == neg_inf() ? 0.f : sm * ex2(mx - mn)) + ex2(xl - mn);
             mx = mn;
         }
 #pragma unroll
@@ -653,28 +779,16 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeAr
         float acc[kVD];
 #pragma unroll
         for (int i = 0; i < kVD; ++i) acc[i] = 0.f;
-        // Parts in chunks of kChunk: every load of a chunk is issued before the first
-        // use, so a chunk costs one round trip to L2.
-        constexpr int kChunk = kVD == 4 ? 16 : 8;
         for (int c0 = 0; c0 < mg.count; c0 += kChunk) {
+            if (c0 > 0) merge_load_chunk<D, kChunk>(a, parts, mg.count, c0, slot_l, qheads, qh, lane, x);
+            // weight of part c0 + lane % kChunk (lse from the pass above for parts < 32)
             const int c = c0 + (lane % kChunk);
-            const int from_lane = __shfl_sync(kFull, slot_l, c & 31);  // every lane shuffles
-            int slot_c = 0;
+            const float from_lane = __shfl_sync(kFull, lse_l, c & 31);
             float wl = 0.f;
-            if (c < mg.count) {
-                slot_c = c < 32 ? from_lane : __ldg(parts + c);
-                wl = ex2(__ldcg(a.ws_lse + int64_t(slot_c) * qheads + qh) - total);
-            }
-            float4 x[kChunk][kVD / 4];
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) {
-                const int slot = __shfl_sync(kFull, slot_c, j);
-                const float* src = a.ws_o + (int64_t(slot) * qheads + qh) * D + lane * kVD;
-#pragma unroll
-                for (int i = 0; i < kVD / 4; ++i)
-                    x[j][i] = c0 + j < mg.count ? __ldcg(reinterpret_cast<const float4*>(src) + i)
-                                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            if (c < mg.count)
+                wl = ex2((c < 32 ? from_lane
+                                 : __ldcg(a.ws_lse + int64_t(__ldg(parts + c)) * qheads + qh)) -
+                         total);
 #pragma unroll
             for (int j = 0; j < kChunk; ++j) {
                 const float wj = __shfl_sync(kFull, wl, j);
@@ -719,87 +833,95 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, lse_merge_kernel<D>, a);
 }
 
-template <int D, int G, int WPH, int NB>
+template <int D, int G, int WPH, int NB, int RB>
 cudaError_t prepare() {
     // Raise the dynamic shared memory limit once per instance.
     static cudaError_t status = cudaFuncSetAttribute(
-        paged_decode_kernel<D, G, WPH, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        Cfg<D, G, WPH, NB>::kSmem);
+        paged_decode_kernel<D, G, WPH, NB, RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        Cfg<D, G, WPH, NB, RB>::kSmem);
     return status;
 }
 
-template <int D, int G, int WPH, int NB>
+template <int D, int G, int WPH, int NB, int RB>
 int occupancy() {
-    if (prepare<D, G, WPH, NB>() != cudaSuccess) return 0;
+    using C = Cfg<D, G, WPH, NB, RB>;
+    if (prepare<D, G, WPH, NB, RB>() != cudaSuccess) return 0;
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_kernel<D, G, WPH, NB>,
-                                                      kThreads, Cfg<D, G, WPH, NB>::kSmem) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_kernel<D, G, WPH, NB, RB>,
+                                                      C::kThreads, C::kSmem) != cudaSuccess)
         return 0;
     return blocks;
 }
 
-template <int D, int G, int WPH, int NB>
+template <int D, int G, int WPH, int NB, int RB>
 cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
-    cudaError_t e = prepare<D, G, WPH, NB>();
+    using C = Cfg<D, G, WPH, NB, RB>;
+    cudaError_t e = prepare<D, G, WPH, NB, RB>();
     if (e != cudaSuccess) return e;
     if (a.n_ctas == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.n_ctas);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<D, G, WPH, NB>::kSmem;
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, WPH, NB>, a);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, WPH, NB, RB>, a);
 }
 
-// Calls FN<D, G, WPH, NB>::run(args...) for the runtime shape. Two query blocks
-// exist only at head_dim 128 with one warp per KV head (four heads per CTA).
-template <template <int, int, int, int> class FN, typename... Args>
-auto dispatch(int head_dim, int group, int wph, int nb, Args&&... args)
-    -> decltype(FN<128, 1, 1, 1>::run(args...)) {
-#define PKV_G(D_, W_, NB_)                                     \
-    switch (group) {                                           \
-        case 1: return FN<D_, 1, W_, NB_>::run(args...);       \
-        case 2: return FN<D_, 2, W_, NB_>::run(args...);       \
-        case 4: return FN<D_, 4, W_, NB_>::run(args...);       \
-        case 8: return FN<D_, 8, W_, NB_>::run(args...);       \
-        default: break;                                        \
+// Calls FN<D, G, WPH, NB, RB>::run(args...) for the runtime shape. `shared`
+// selects the shared-prefix instance (two query blocks per warp, two row blocks
+// of warps), which exists only at head_dim 128 with one warp per KV head.
+template <template <int, int, int, int, int> class FN, typename... Args>
+auto dispatch(int head_dim, int group, int wph, bool shared, Args&&... args)
+    -> decltype(FN<128, 1, 1, 1, 1>::run(args...)) {
+#define PKV_G(D_, W_, NB_, RB_)                                     \
+    switch (group) {                                                \
+        case 1: return FN<D_, 1, W_, NB_, RB_>::run(args...);       \
+        case 2: return FN<D_, 2, W_, NB_, RB_>::run(args...);       \
+        case 4: return FN<D_, 4, W_, NB_, RB_>::run(args...);       \
+        case 8: return FN<D_, 8, W_, NB_, RB_>::run(args...);       \
+        default: break;                                             \
     }
-    if (nb == 1) {
+    if (!shared) {
         if (head_dim == 128) {
-            if (wph == 1) { PKV_G(128, 1, 1) }
-            if (wph == 2) { PKV_G(128, 2, 1) }
-            if (wph == 4) { PKV_G(128, 4, 1) }
+            if (wph == 1) { PKV_G(128, 1, 1, 1) }
+            if (wph == 2) { PKV_G(128, 2, 1, 1) }
+            if (wph == 4) { PKV_G(128, 4, 1, 1) }
         } else if (head_dim == 256) {
-            if (wph == 2) { PKV_G(256, 2, 1) }
-            if (wph == 4) { PKV_G(256, 4, 1) }
+            if (wph == 2) { PKV_G(256, 2, 1, 1) }
+            if (wph == 4) { PKV_G(256, 4, 1, 1) }
         }
-    } else if (nb == 2 && head_dim == 128 && wph == 1) {
-        PKV_G(128, 1, 2)
+    } else if (head_dim == 128 && wph == 1) {
+        if (shared_row_blocks() == 2) { PKV_G(128, 1, 2, 2) }
+        PKV_G(128, 1, 2, 1)
     }
 #undef PKV_G
-    return FN<128, 1, 1, 1>::unsupported();
+    return FN<128, 1, 1, 1, 1>::unsupported();
 }
 
-template <int D, int G, int WPH, int NB>
+template <int D, int G, int WPH, int NB, int RB>
 struct OccupancyFn {
-    static int run() { return occupancy<D, G, WPH, NB>(); }
+    static int run() { return occupancy<D, G, WPH, NB, RB>(); }
     static int unsupported() { return 0; }
 };
-template <int D, int G, int WPH, int NB>
+template <int D, int G, int WPH, int NB, int RB>
 struct LaunchFn {
     static cudaError_t run(const DecodeArgs& a, cudaStream_t s) {
-        return launch<D, G, WPH, NB>(a, s);
+        return launch<D, G, WPH, NB, RB>(a, s);
     }
     static cudaError_t unsupported() { return cudaErrorInvalidValue; }
 };
+template <int D, int G, int WPH, int NB, int RB>
+struct RowsFn {
+    static int run() { return Cfg<D, G, WPH, NB, RB>::kWarpRows * RB; }
+    static int unsupported() { return 0; }
+};
 
-int warps_per_head(int heads_per_cta) { return kConsumerWarps / heads_per_cta; }
+int warps_per_head(int heads_per_cta) { return kGroupWarps / heads_per_cta; }
 
 }  // namespace
 
@@ -811,24 +933,26 @@ bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim) {
     return n_kv_heads == 1 || n_kv_heads == 2 || n_kv_heads == 4 || n_kv_heads == 8;
 }
 
-bool decode_has_shared_kernel(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta) {
-    return decode_shape_supported(n_qo_heads, n_kv_heads, head_dim) && head_dim == 128 &&
-           heads_per_cta == kConsumerWarps;
+int decode_shared_rows(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta) {
+    if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim) || heads_per_cta < 1 ||
+        kGroupWarps % heads_per_cta != 0)
+        return 0;
+    return dispatch<RowsFn>(head_dim, n_qo_heads / n_kv_heads, warps_per_head(heads_per_cta), true);
 }
 
 int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta,
-                       int n_blocks) {
+                       bool shared) {
     if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim)) return 0;
     if (heads_per_cta < 1 || heads_per_cta > heads_per_group(n_kv_heads, head_dim) ||
         n_kv_heads % heads_per_cta != 0)
         return 0;
     return dispatch<OccupancyFn>(head_dim, n_qo_heads / n_kv_heads, warps_per_head(heads_per_cta),
-                                 n_blocks);
+                                 shared);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e = dispatch<LaunchFn>(a.head_dim, a.n_qo_heads / a.n_kv_heads,
-                                       warps_per_head(a.heads_per_cta), a.n_blocks, a, stream);
+                                       warps_per_head(a.heads_per_cta), a.shared, a, stream);
     if (e != cudaSuccess) return e;
     return a.head_dim == 128 ? launch_merge<128>(a, stream) : launch_merge<256>(a, stream);
 }

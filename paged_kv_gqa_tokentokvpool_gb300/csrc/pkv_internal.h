@@ -16,6 +16,10 @@ namespace pkv {
 // predecessor on the stream is still running, and does only plan reads and
 // barrier set-up before its griddepcontrol.wait.
 bool pdl_enabled();
+// Row blocks of the shared-prefix kernel: 1 (16 query rows per KV head, two CTAs
+// per SM; default, the faster on GB300) or 2 (32 rows, one CTA per SM); tuning
+// knob PKV_SHARED_ROW_BLOCKS, read once.
+int shared_row_blocks();
 
 // ---- errors -------------------------------------------------------------
 int fail(int code, const char* fmt, ...);  // records the message, returns code
@@ -42,8 +46,9 @@ int choose_heads_per_cta(int n_kv_heads, int head_dim);
 // of request b, KV-head group hg, attended for the nreq requests b .. b+nreq-1
 // (nreq > 1 only for a prefix those requests share); idx_begin = kv_indptr[b] +
 // tok_begin is where the unit's slot ids start in kv_indices, and len is request
-// b's context length (-1 for a shared prefix), which tells the fused append which
-// token is the newest. partial < 0: the unit covers a whole context and writes
+// b's context length, which tells the fused append which token is the newest (for
+// a shared prefix: -2 if other units of the sharing group read the same slots, so
+// their rows should stay in L2, else -1). partial < 0: the unit covers a whole context and writes
 // out/lse; otherwise request b+r writes partial slot partial + r of the workspace.
 struct Unit {
     int32_t b, hg, tok_begin, tok_end, partial, nreq, idx_begin, len;
@@ -97,7 +102,9 @@ struct DecodeArgs {
     const Merge* merges;
     const int32_t* part_list;  // partial slots of the merge records
     int n_ctas;           // grid size: every CTA of the plan (some may have no units)
-    int n_blocks;         // 8-row query blocks per KV head in a unit (1, or 2 with sharing)
+    bool shared;          // the shared-prefix kernel (prefix units of several requests)
+    bool early;           // slot ids and old pool rows may be loaded before the
+                          // previous kernel completes (PKV_PLAN_EARLY_GATHER)
     int heads_per_cta;    // KV heads of one group
     int n_qo_heads;
     int n_kv_heads;
@@ -120,12 +127,13 @@ struct DecodeArgs {
 };
 
 bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim);
-// Resident CTAs per SM of the decode kernel for this shape (0 on error).
+// Resident CTAs per SM of the decode kernel (plain or shared-prefix instance)
+// for this shape (0 on error or when no such instance exists).
 int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta,
-                       int n_blocks);
-// Whether a kernel with two query blocks per KV head (shared-prefix units of
-// 16 / G requests) exists for this shape.
-bool decode_has_shared_kernel(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta);
+                       bool shared);
+// Query rows per KV head that one unit of the shared-prefix kernel serves (so
+// rows / G requests of a sharing group), or 0 when this shape has no such kernel.
+int decode_shared_rows(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // Row scatter between two pools (either may be pinned host memory mapped for the GPU):
@@ -142,7 +150,9 @@ cudaError_t launch_append(void* k_pool, void* v_pool, const int32_t* slot_ids,
 
 struct pkv_plan {
     int device = 0;
-    int num_sms = 0, ctas_per_sm = 0, ctas = 0;
+    // persistent CTAs of the plain and of the shared-prefix kernel (the staging is
+    // sized for the larger grid)
+    int num_sms = 0, ctas_per_sm = 0, ctas = 0, ctas_shared = 0, ctas_max = 0;
     int max_batch = 0;
     int64_t max_tokens = 0;
     int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0, n_groups = 0, heads_per_cta = 0;
@@ -162,6 +172,9 @@ struct pkv_plan {
     pkv::PlanCounts counts{};
     size_t off_cta = 0, off_merge = 0, off_list = 0, off_units = 0;  // offsets in the staging
     int share_rows = 0;  // requests per shared-prefix unit (0: this shape has no such kernel)
-    int n_blocks = 1;    // query blocks of the current step's kernel
+    int merge_ctas = 0;  // grid of the merge kernel
+    unsigned flags = 0;  // PKV_PLAN_* options
+    bool shared = false; // the current step runs the shared-prefix kernel
+    int launch_ctas = 0; // grid of the current step's decode kernel
     std::vector<int32_t> indptr_host;
 };

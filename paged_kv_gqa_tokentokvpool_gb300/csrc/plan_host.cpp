@@ -50,7 +50,7 @@ struct Item {
     int32_t hg;       // KV-head group
     int32_t tok0;     // first token within the request's slot list
     int32_t len;      // tokens
-    int32_t req_len;  // context length of the request (-1 for a prefix item)
+    int32_t req_len;  // context length of the request (-1 / -2 for a prefix item)
     int32_t idx0;     // kv_indptr[b] + tok0
     bool partial;     // its pieces always write partial results (prefix, suffix)
 };
@@ -86,10 +86,13 @@ int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, const
         if (sharing && s < sharing->n && sharing->indptr[s] == b && sharing->len[s] > 0) {
             const int m1 = sharing->indptr[s + 1];
             const int32_t P = sharing->len[s];
+            // -2 marks a prefix that other items of the group read again (the
+            // kernel then asks L2 to keep its rows), -1 one read by this item only
+            const int32_t tag = m1 - b > sharing->requests_per_unit ? -2 : -1;
             for (int c0 = b; c0 < m1; c0 += sharing->requests_per_unit) {
                 const int nreq = std::min(sharing->requests_per_unit, m1 - c0);
                 for (int g = 0; g < n_groups; ++g)
-                    items.push_back(Item{c0, nreq, g, 0, P, -1, indptr[c0], true});
+                    items.push_back(Item{c0, nreq, g, 0, P, tag, indptr[c0], true});
             }
             for (int m = b; m < m1; ++m)
                 for (int g = 0; g < n_groups; ++g)

@@ -351,6 +351,97 @@ def test_graph_replay_after_replanning(pkv):
     assert plan.status() == 0
 
 
+@pytest.mark.parametrize("shared", [False, True], ids=["plain", "shared_prefix"])
+def test_early_gather_graph_steps(pkv, shared):
+    """PKV_PLAN_EARLY_GATHER with the fused append, layer loop in a CUDA graph,
+    re-planned every step: each step's rows are written before its plan upload, as
+    the flag requires. Results equal the oracle's and, bit for bit, those of the
+    same plan without the flag."""
+    dev = torch.device("cuda")
+    layers = 3
+    if shared:
+        wls = [workloads.prefix_shared_workload([1500, 40], [3, 700, 1, 90, 2000, 5, 17, 64], 4,
+                                                pool_slots=1 << 15, layers=layers, seed=700 + i)
+               for i in range(2)]
+    else:
+        wls = [workloads.scattered_workload(l, pool_slots=1 << 15, layers=layers, seed=700 + i)
+               for i, l in enumerate([[3000, 17, 1, 9000], [1, 20000, 513, 64]])]
+    B = wls[0].batch
+    max_tokens = max(w.total_tokens for w in wls)
+    S = wls[0].pool_slots
+    q = torch.empty(layers, B, 32, 128, dtype=torch.bfloat16, device=dev)
+    kp = torch.empty(layers, S, 8, 128, dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    kn = torch.empty(layers, B, 8, 128, dtype=torch.bfloat16, device=dev)
+    vn = torch.empty_like(kn)
+    out = torch.empty(layers, B, 32, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(layers, B, 32, dtype=torch.float32, device=dev)
+    indptr = torch.zeros(B + 1, dtype=torch.int32, device=dev)
+    indices = torch.zeros(max_tokens, dtype=torch.int32, device=dev)
+    slots = torch.zeros(B, dtype=torch.int32, device=dev)
+    plans = {}
+    for early in (True, False):
+        plans[early] = pkv.paged_decode_plan_create(B, max_tokens, 32, 8, 128)
+        if early:
+            plans[early].set_flags(pkv.PKV_PLAN_EARLY_GATHER)
+
+    def plan_step(plan, wl):
+        if shared:
+            gs = wl.meta["group_size"]
+            sp = np.arange(0, B + 1, gs, dtype=np.int32)
+            pkv.paged_decode_plan_shared(plan, wl.kv_indptr, sp,
+                                         np.array(wl.meta["prefix_lens"], np.int32))
+        else:
+            pkv.paged_decode_plan(plan, wl.kv_indptr)
+
+    def body(plan):
+        for l in range(layers):
+            pkv.paged_decode_append_attn(q[l], kp[l], vp[l], indptr, indices, slots, kn[l], vn[l],
+                                         B, 32, 8, 128, wls[0].sm_scale, out[l], lse[l], plan)
+
+    results = {}
+    for early in (True, False):
+        graph = None
+        for step, wl in enumerate(wls):
+            tens = [workloads.layer_tensors(wl, l, device="cpu") for l in range(layers)]
+
+            def load_inputs():
+                for l, t in enumerate(tens):  # every row written before the plan upload
+                    q[l].copy_(t.q)
+                    kp[l].copy_(t.k_pool)
+                    vp[l].copy_(t.v_pool)
+                    kn[l].copy_(t.k_new)
+                    vn[l].copy_(t.v_new)
+                slots.copy_(torch.from_numpy(wl.append_slots))
+                indptr.copy_(torch.from_numpy(wl.kv_indptr))
+                indices[:wl.total_tokens].copy_(torch.from_numpy(wl.kv_indices))
+
+            load_inputs()
+            plan_step(plans[early], wl)
+            if graph is None:
+                body(plans[early])
+                torch.cuda.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    body(plans[early])
+                load_inputs()
+                plan_step(plans[early], wl)
+            graph.replay()
+            torch.cuda.synchronize()
+            for l, t in enumerate(tens):
+                ref_out, ref_lse = oracle_reference(wl, t)
+                assert_parity(to_f64(out[l]), lse[l].cpu().numpy(), ref_out, ref_lse,
+                              what=f"early={early} step {step} layer {l}")
+                k_after = oracle.append(bits(t.k_pool), wl.append_slots, bits(t.k_new))
+                assert np.array_equal(bits(kp[l]), k_after)
+            results[(early, step)] = (out.clone(), lse.clone())
+        assert plans[early].status() == 0
+    for step in range(len(wls)):
+        assert torch.equal(results[(True, step)][0].view(torch.int16),
+                           results[(False, step)][0].view(torch.int16))
+        assert torch.equal(results[(True, step)][1], results[(False, step)][1])
+
+
 FUSED_CASES = [
     ([1], 32, 8, 128),
     ([1, 2, 3, 17, 300, 1000, 5, 64, 65], 32, 8, 128),
@@ -435,6 +526,12 @@ SHARED_CASES = [
     ([4100], 9, list(range(1, 10)), 16, 8, 128),
     ([1000], 17, [1] * 17, 8, 8, 128),
     ([2500], 4, [1, 90, 300, 2], 16, 4, 256),
+    # runs longer than one prefix unit (32 / G requests): several units read the prefix
+    ([2000], 12, [3, 1, 800, 64, 5, 17, 2, 100, 1, 9, 33, 250], 32, 8, 128),
+    ([600, 1500], 9, [1 + 37 * i for i in range(18)], 64, 8, 128),
+    ([900], 40, [1 + (7 * i) % 50 for i in range(40)], 8, 8, 128),
+    ([1200], 20, [2 + 11 * i for i in range(20)], 16, 8, 128),
+    ([3333], 10, [1 + 91 * i for i in range(10)], 16, 4, 128),
 ]
 
 

@@ -73,12 +73,22 @@ def test_errors_are_reported_before_any_launch(pkv):
     assert lib.paged_decode_plan(None, p, 1, None) == pkv.PKV_ERR_PLAN
     assert lib.paged_decode_attn(p, p, p, p, p, 1, 32, 8, 128, ctypes.c_float(0.1), p, p, None,
                                  None) == pkv.PKV_ERR_PLAN
+    assert lib.paged_decode_plan_set_flags(None, pkv.PKV_PLAN_EARLY_GATHER) == pkv.PKV_ERR_PLAN
     lib.paged_decode_plan_destroy(None)  # no-op
 
 
-def check_plan(indptr, n_kv_heads, head_dim, ctas, plan, hpc=0, shared=None):
+def test_header_constants_match_the_binding(pkv):
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    flags = dict(re.findall(r"#define\s+(PKV_PLAN_\w+)\s+(\d+)u", text))
+    assert flags == {"PKV_PLAN_EARLY_GATHER": str(pkv.PKV_PLAN_EARLY_GATHER)}
+    codes = dict(re.findall(r"(PKV_(?:OK|ERR_\w+))\s*=\s*(-?\d+)", text))
+    assert codes and all(getattr(pkv, k) == int(v) for k, v in codes.items())
+
+
+def check_plan(indptr, n_kv_heads, head_dim, ctas, plan, hpc=0, shared=None, rpu=None):
     """Every (request, head group, token) is attended exactly once; units, partial
-    slots and merge records are consistent. shared = (shared_indptr, shared_len)."""
+    slots and merge records are consistent. shared = (shared_indptr, shared_len),
+    rpu = requests per shared-prefix unit."""
     indptr = np.asarray(indptr, np.int64)
     B = indptr.size - 1
     lengths = np.diff(indptr)
@@ -92,17 +102,21 @@ def check_plan(indptr, n_kv_heads, head_dim, ctas, plan, hpc=0, shared=None):
     assert len(cta_begin) - 1 == ctas, "every CTA of the grid has an entry"
     assert plan["ctas_used"] <= ctas
     prefix = np.zeros(B, np.int64)
+    run_size = np.ones(B, np.int64)  # members of the sharing run of each request
     if shared is not None:
         sp, sl = shared
         for s in range(len(sp) - 1):
             prefix[sp[s]:sp[s + 1]] = sl[s]
+            run_size[sp[s]:sp[s + 1]] = sp[s + 1] - sp[s]
     covered = {(b, g): np.zeros(lengths[b], np.int32) for b in range(B) for g in range(groups)}
     direct, slot_owner = set(), {}
     for b, hg, t0, t1, part, nreq, idx_begin, length in units:
         assert 0 <= b and b + nreq <= B and nreq >= 1 and 0 <= hg < groups and 0 <= t0 <= t1
         assert idx_begin == indptr[b] + t0
-        if nreq > 1 or length == -1:  # a shared prefix
-            assert length == -1 and part >= 0
+        if nreq > 1 or length < 0:  # a shared prefix
+            assert length in (-1, -2) and part >= 0
+            if rpu is not None:  # -2: other units of the run read the same slots
+                assert length == (-2 if run_size[b] > rpu else -1)
             for r in range(nreq):
                 assert t1 <= prefix[b + r], "prefix unit beyond the shared prefix"
         else:
@@ -175,7 +189,7 @@ def test_planner_with_shared_prefixes(pkv, seed):
     ctas = 304
     plan = pkv.paged_decode_plan_host(indptr, 8, 128, ctas, shared_indptr=sp_arr, shared_len=sl_arr,
                                       requests_per_unit=rpu)
-    check_plan(indptr, 8, 128, ctas, plan, shared=(np.array(sp_arr), np.array(sl_arr)))
+    check_plan(indptr, 8, 128, ctas, plan, shared=(np.array(sp_arr), np.array(sl_arr)), rpu=rpu)
     # a prefix unit serves at most requests_per_unit requests
     assert plan["units"][:, 5].max() <= rpu
 
