@@ -53,6 +53,9 @@ class OracleLib:
         lib.oracle_decode.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64,
                                       ctypes.c_float, P, P, ctypes.c_int]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_prefill.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64,
+                                       ctypes.c_float, P, P, ctypes.c_int]
+        lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_append.argtypes = [P, P, P, I64, I64, I64]
         lib.oracle_append.restype = ctypes.c_int
         lib.oracle_lse_merge.argtypes = [P, P, I64, I64, I64, P, P]
@@ -90,6 +93,37 @@ class OracleLib:
                                     int(n_threads))
         if rc != 0:
             raise ValueError("oracle_decode: bad arguments")
+        return out, lse
+
+    def prefill(self, q_bits, k_pool_bits, v_pool_bits, qo_indptr, kv_indptr, kv_indices,
+                n_qo_heads, n_kv_heads, head_dim, sm_scale, n_threads: int = 0):
+        """Causal chunked-prefill attention in fp64.
+
+        q_bits: [NQ, Hq, D] uint16 (NQ = qo_indptr[-1]); request b's chunk is rows
+        qo_indptr[b] .. qo_indptr[b+1], its newest C_b tokens, at list positions
+        L_b - C_b .. L_b - 1. Returns (out [NQ, Hq, D] float64, lse [NQ, Hq] float64).
+        """
+        q = _c(q_bits, np.uint16)
+        k = _c(k_pool_bits, np.uint16)
+        v = _c(v_pool_bits, np.uint16)
+        qo = _c(qo_indptr, np.int32)
+        indptr = _c(kv_indptr, np.int32)
+        indices = _c(kv_indices, np.int32)
+        B = indptr.size - 1
+        assert qo.size == B + 1
+        NQ = int(qo[-1]) if B >= 0 and qo.size else 0
+        S = k.size // (n_kv_heads * head_dim)
+        assert q.size == NQ * n_qo_heads * head_dim and v.size == k.size
+        if indices.size == 0:
+            indices = np.zeros(1, np.int32)
+        out = np.empty((NQ, n_qo_heads, head_dim), np.float64)
+        lse = np.empty((NQ, n_qo_heads), np.float64)
+        rc = self.lib.oracle_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(qo), _ptr(indptr),
+                                     _ptr(indices), B, n_qo_heads, n_kv_heads, head_dim, S,
+                                     float(np.float32(sm_scale)), _ptr(out), _ptr(lse),
+                                     int(n_threads))
+        if rc != 0:
+            raise ValueError("oracle_prefill: bad arguments")
         return out, lse
 
     def append(self, pool_bits, slot_ids, rows_bits):
@@ -144,6 +178,10 @@ def max_threads() -> int:
 
 def decode(*args, **kwargs):
     return default().decode(*args, **kwargs)
+
+
+def prefill(*args, **kwargs):
+    return default().prefill(*args, **kwargs)
 
 
 def append(*args, **kwargs):

@@ -26,6 +26,13 @@
 //    the identity that lets a context be split: lse = ln sum_c exp(lse_c) and
 //    out = sum_c exp(lse_c - lse) * out_c.
 //  * The append is a row copy: pool[slot_ids[i]] = rows[i].
+//  * Chunked prefill over the same pool ("Agent-Infer", section "连续批处理"
+//    (continuous batching): long prefills are cut into chunks of 512 tokens, 64
+//    while decodes are running, so decode steps can run between chunks). Reading
+//    taken: a chunk holds the request's newest C tokens, already appended, so its
+//    slot list has L >= C entries and query token i of the chunk (i < C) sits at
+//    position p = L - C + i; it attends causally to list entries 0 .. p, with the
+//    same softmax definition as above.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -111,6 +118,82 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_p
                 const double p = std::exp(s[j] - l);
                 const uint16_t* v = v_pool + (int64_t(kv_indices[begin + j]) * n_kv_heads + g) * head_dim;
                 for (int64_t d = 0; d < head_dim; ++d) o[d] += p * widen_bf16(v[d]);
+            }
+        }
+    }
+    return 0;
+}
+
+// Causal attention of prefill chunks over their requests' slot lists.
+//   q      : [qo_indptr[batch], n_qo_heads, head_dim] bf16 bit patterns; request b's
+//            chunk is rows qo_indptr[b] .. qo_indptr[b+1]
+//   k_pool, v_pool, kv_indptr, kv_indices : as for oracle_decode; request b lists
+//            L_b = kv_indptr[b+1] - kv_indptr[b] >= C_b = qo_indptr[b+1] - qo_indptr[b]
+//   out    : [qo_indptr[batch], n_qo_heads, head_dim] fp64; lse : [qo_indptr[batch], n_qo_heads]
+// Query row i of request b (chunk index c = i - qo_indptr[b]) is at position
+// p = L_b - C_b + c and attends list entries 0 .. p.
+// Returns 0, or -1 on a bad argument.
+int oracle_prefill(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                   const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+                   int64_t batch, int64_t n_qo_heads, int64_t n_kv_heads, int64_t head_dim,
+                   int64_t pool_slots, float sm_scale, double* out, double* lse, int n_threads) {
+    if (batch < 0 || n_kv_heads <= 0 || n_qo_heads % n_kv_heads != 0 || head_dim <= 0)
+        return -1;
+    if (kv_indptr[0] != 0 || qo_indptr[0] != 0) return -1;
+    for (int64_t b = 0; b < batch; ++b) {
+        if (kv_indptr[b + 1] < kv_indptr[b] || qo_indptr[b + 1] < qo_indptr[b]) return -1;
+        if (qo_indptr[b + 1] - qo_indptr[b] > kv_indptr[b + 1] - kv_indptr[b]) return -1;
+    }
+    for (int64_t i = 0; i < kv_indptr[batch]; ++i) {
+        if (kv_indices[i] < 0 || kv_indices[i] >= pool_slots) return -1;
+    }
+    const int64_t G = n_qo_heads / n_kv_heads;
+    const double scale = static_cast<double>(sm_scale);
+    const int64_t rows = int64_t(qo_indptr[batch]) * n_qo_heads;
+    // request of every query row
+    std::vector<int64_t> req(qo_indptr[batch]);
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t i = qo_indptr[b]; i < qo_indptr[b + 1]; ++i) req[i] = b;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel
+#endif
+    {
+        std::vector<double> qd(head_dim), s;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t ih = 0; ih < rows; ++ih) {
+            const int64_t i = ih / n_qo_heads;
+            const int64_t kv_head = (ih % n_qo_heads) / G;
+            const int64_t b = req[i];
+            const int64_t first = kv_indptr[b];
+            const int64_t L = kv_indptr[b + 1] - first;
+            const int64_t C = qo_indptr[b + 1] - qo_indptr[b];
+            const int64_t pos = L - C + (i - qo_indptr[b]);  // position of this query
+            const int64_t n_seen = pos + 1;                  // entries 0 .. pos
+            double* orow = out + ih * head_dim;
+            for (int64_t d = 0; d < head_dim; ++d) {
+                qd[d] = widen_bf16(q[ih * head_dim + d]);
+                orow[d] = 0.0;
+            }
+            s.assign(n_seen, 0.0);
+            double smax = -std::numeric_limits<double>::infinity();
+            for (int64_t j = 0; j < n_seen; ++j) {
+                const int64_t row = int64_t(kv_indices[first + j]) * n_kv_heads + kv_head;
+                double qk = 0.0;
+                for (int64_t d = 0; d < head_dim; ++d) qk += qd[d] * widen_bf16(k_pool[row * head_dim + d]);
+                s[j] = qk * scale;
+                smax = std::fmax(smax, s[j]);
+            }
+            double denom = 0.0;
+            for (int64_t j = 0; j < n_seen; ++j) denom += std::exp(s[j] - smax);
+            const double log_denom = smax + std::log(denom);
+            lse[ih] = log_denom;
+            for (int64_t j = 0; j < n_seen; ++j) {
+                const int64_t row = int64_t(kv_indices[first + j]) * n_kv_heads + kv_head;
+                const double w = std::exp(s[j] - log_denom);
+                for (int64_t d = 0; d < head_dim; ++d) orow[d] += w * widen_bf16(v_pool[row * head_dim + d]);
             }
         }
     }

@@ -14,7 +14,14 @@ AssertionError when the oracle disagrees with:
     section "分页 KV 缓存"), splitting a context and merging the halves by
     log-sum-exp, equal queries in a GQA group, Hq = Hkv reducing to MHA;
   * the mean of lse over many N(0,1) heads (ln L + sigma^2 / 2);
-  * numpy's scatter for the append.
+  * numpy's scatter for the append;
+  * for chunked prefill (causal attention of a request's newest C tokens over its
+    L listed slots, "Agent-Infer", section "连续批处理"): torch's fp64
+    scaled_dot_product_attention with an explicit causal mask, a brute-force
+    loop on a tiny case, the first token of a chunk with no prefix (out = its V
+    row), causality (rows after a query's position do not matter to it, the row
+    at it does), a chunk cut in two giving the same rows, and chunks of one token
+    reducing to decode.
 The mutation test plants mistakes in copies of the oracle and checks that some
 pin fails for each.
 """
@@ -263,6 +270,144 @@ def pin_append(orc, seed=9):
     assert np.array_equal(orc.append(pool, np.zeros(0, np.int32), rows[:0]), pool)
 
 
+# ---------------------------------------------------------------------------
+# chunked prefill
+# ---------------------------------------------------------------------------
+
+def prefill_case(rng, chunks, contexts, hq, hkv, d, extra_slots=5):
+    """Request b lists contexts[b] slots; its newest chunks[b] tokens are the chunk."""
+    assert all(0 <= c <= l for c, l in zip(chunks, contexts))
+    n = sum(contexts)
+    S = n + extra_slots
+    indices = rng.permutation(S)[:n].astype(np.int32)
+    kv_indptr = np.concatenate([[0], np.cumsum(contexts)]).astype(np.int32)
+    qo_indptr = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = bf16_bits_of(rng.standard_normal((int(qo_indptr[-1]), hq, d)))
+    k = bf16_bits_of(rng.standard_normal((S, hkv, d)))
+    v = bf16_bits_of(rng.standard_normal((S, hkv, d)))
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    return q, k, v, qo_indptr, kv_indptr, indices, scale
+
+
+def sdpa_prefill_reference(q, k, v, qo_indptr, kv_indptr, indices, hq, hkv, d, scale):
+    """Dense fp64 causal attention per request by torch's library routines, with the
+    mask built from positions: query c of a chunk of C over L entries sees j <= L-C+c."""
+    G = hq // hkv
+    NQ = int(qo_indptr[-1])
+    out = np.zeros((NQ, hq, d))
+    lse = np.zeros((NQ, hq))
+    qd, kd, vd = widen(q), widen(k), widen(v)
+    for b in range(len(kv_indptr) - 1):
+        C = int(qo_indptr[b + 1] - qo_indptr[b])
+        if C == 0:
+            continue
+        idx = indices[kv_indptr[b]:kv_indptr[b + 1]]
+        L = idx.size
+        Q = torch.from_numpy(qd[qo_indptr[b]:qo_indptr[b + 1]]).permute(1, 0, 2)[None]
+        K = torch.from_numpy(kd[idx]).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+        V = torch.from_numpy(vd[idx]).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+        allowed = torch.arange(L)[None, :] <= (L - C + torch.arange(C))[:, None]
+        o = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=allowed,
+                                                             scale=float(scale))
+        out[qo_indptr[b]:qo_indptr[b + 1]] = o[0].permute(1, 0, 2).numpy()
+        scores = (Q @ K.transpose(-1, -2))[0] * float(scale)
+        scores = scores.masked_fill(~allowed[None], float("-inf"))
+        lse[qo_indptr[b]:qo_indptr[b + 1]] = torch.logsumexp(scores, dim=-1).T.numpy()
+    return out, lse
+
+
+def pin_prefill_sdpa(orc, seed=21):
+    rng = np.random.default_rng(seed)
+    for chunks, contexts, hq, hkv, d in [
+        ([5, 1, 0, 7], [9, 6, 4, 7], 8, 2, 16),     # prefix + chunk, one token, none, no prefix
+        ([16, 3], [40, 3], 4, 4, 8),                 # G = 1
+        ([6], [11], 16, 2, 32),                      # G = 8
+    ]:
+        q, k, v, qo, kvp, idx, scale = prefill_case(rng, chunks, contexts, hq, hkv, d)
+        out, lse = orc.prefill(q, k, v, qo, kvp, idx, hq, hkv, d, scale)
+        ro, rl = sdpa_prefill_reference(q, k, v, qo, kvp, idx, hq, hkv, d, scale)
+        _close(out, ro, 1e-12, 1e-12, what="prefill vs sdpa out")
+        _close(lse, rl, 1e-12, 1e-12, what="prefill vs sdpa lse")
+
+
+def pin_prefill_brute_force(orc):
+    """Two query tokens over three listed slots, one KV head shared by two query
+    heads, head_dim 4: the definition written out with math.exp."""
+    rng = np.random.default_rng(31)
+    q, k, v, qo, kvp, idx, scale = prefill_case(rng, [2], [3], 2, 1, 4, extra_slots=2)
+    out, lse = orc.prefill(q, k, v, qo, kvp, idx, 2, 1, 4, scale)
+    qd, kd, vd = widen(q), widen(k), widen(v)
+    for c in range(2):
+        pos = 3 - 2 + c
+        for h in range(2):
+            s = [scale * sum(qd[c, h, t] * kd[idx[j], 0, t] for t in range(4))
+                 for j in range(pos + 1)]
+            m = max(s)
+            tot = sum(math.exp(x - m) for x in s)
+            want_lse = m + math.log(tot)
+            assert abs(lse[c, h] - want_lse) < 1e-12, (c, h)
+            for t in range(4):
+                want = sum(math.exp(s[j] - want_lse) * vd[idx[j], 0, t] for j in range(pos + 1))
+                assert abs(out[c, h, t] - want) < 1e-12, (c, h, t)
+
+
+def pin_prefill_first_token(orc):
+    """A chunk with no prefix (C = L): its first query sees only entry 0."""
+    rng = np.random.default_rng(32)
+    q, k, v, qo, kvp, idx, scale = prefill_case(rng, [4], [4], 4, 2, 8)
+    out, lse = orc.prefill(q, k, v, qo, kvp, idx, 4, 2, 8, scale)
+    qd, kd, vd = widen(q), widen(k), widen(v)
+    for h in range(4):
+        g = h // 2
+        assert np.array_equal(out[0, h], vd[idx[0], g]), h
+        s0 = scale * float(np.dot(qd[0, h], kd[idx[0], g]))
+        assert abs(lse[0, h] - s0) < 1e-12
+
+
+def pin_prefill_causality(orc, seed=33):
+    """Rows after a query's position do not change its result; the row at it does."""
+    rng = np.random.default_rng(seed)
+    chunks, contexts = [3], [8]
+    q, k, v, qo, kvp, idx, scale = prefill_case(rng, chunks, contexts, 4, 2, 8)
+    base_o, base_l = orc.prefill(q, k, v, qo, kvp, idx, 4, 2, 8, scale)
+    pos0 = 8 - 3  # position of the chunk's first query
+    k2, v2 = k.copy(), v.copy()
+    for j in range(pos0 + 1, 8):
+        k2[idx[j]] = bf16_bits_of(rng.standard_normal(k.shape[1:]) * 3)
+        v2[idx[j]] = bf16_bits_of(rng.standard_normal(v.shape[1:]) * 3)
+    o2, l2 = orc.prefill(q, k2, v2, qo, kvp, idx, 4, 2, 8, scale)
+    assert np.array_equal(o2[0], base_o[0]) and np.array_equal(l2[0], base_l[0])
+    assert not np.allclose(o2[1:], base_o[1:]), "later queries see those rows"
+    v3 = v.copy()
+    v3[idx[pos0]] = bf16_bits_of(rng.standard_normal(v.shape[1:]) * 3)
+    o3, _ = orc.prefill(q, k, v3, qo, kvp, idx, 4, 2, 8, scale)
+    assert not np.allclose(o3[0], base_o[0]), "a query sees the row at its own position"
+
+
+def pin_prefill_chunk_cut(orc, seed=34):
+    """Cutting a chunk in two gives the same rows: the last C2 queries of a chunk of
+    C over L entries equal a chunk of C2 over the same L entries."""
+    rng = np.random.default_rng(seed)
+    q, k, v, qo, kvp, idx, scale = prefill_case(rng, [9], [20], 8, 2, 16)
+    full_o, full_l = orc.prefill(q, k, v, qo, kvp, idx, 8, 2, 16, scale)
+    tail_o, tail_l = orc.prefill(q[5:], k, v, np.array([0, 4], np.int32), kvp, idx, 8, 2, 16,
+                                 scale)
+    assert np.array_equal(tail_o, full_o[5:]) and np.array_equal(tail_l, full_l[5:])
+
+
+def pin_prefill_one_token_chunks(orc, seed=35):
+    """Chunks of one token are decode (whose own pins hold on the decode oracle)."""
+    rng = np.random.default_rng(seed)
+    q, k, v, qo, kvp, idx, scale = prefill_case(rng, [1, 1, 1], [5, 1, 12], 8, 2, 16)
+    po, pl = orc.prefill(q, k, v, qo, kvp, idx, 8, 2, 16, scale)
+    do, dl = orc.decode(q, k, v, kvp, idx, 8, 2, 16, scale)
+    assert np.array_equal(po, do) or np.allclose(po, do, rtol=1e-14, atol=1e-14)
+    assert np.allclose(pl, dl, rtol=1e-14, atol=1e-14)
+
+
+PREFILL_PINS = [pin_prefill_sdpa, pin_prefill_brute_force, pin_prefill_first_token,
+                pin_prefill_causality, pin_prefill_chunk_cut, pin_prefill_one_token_chunks]
+
 ALL_PINS = [pin_golden, pin_sdpa, pin_single_token, pin_zero_query, pin_identical_v,
             pin_permutation, pin_split_merge, pin_gqa_equal_queries, pin_empty,
-            pin_lse_statistics, pin_append]
+            pin_lse_statistics, pin_append] + PREFILL_PINS

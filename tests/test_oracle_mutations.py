@@ -31,6 +31,18 @@ MUTANTS = {
     "append_wrong_row": ("rows + i * row_elems,", "rows + ((i + 1) % n) * row_elems,"),
     "widen_truncates": ("uint32_t w = static_cast<uint32_t>(bits) << 16;",
                         "uint32_t w = static_cast<uint32_t>(bits & 0xFFFE) << 16;"),
+    "prefill_position_ignores_prefix": ("const int64_t pos = L - C + (i - qo_indptr[b]);",
+                                        "const int64_t pos = (i - qo_indptr[b]);"),
+    "prefill_excludes_own_token": ("const int64_t n_seen = pos + 1;", "const int64_t n_seen = pos;"),
+    "prefill_sees_next_token": ("const int64_t n_seen = pos + 1;",
+                                "const int64_t n_seen = pos + 2 < L ? pos + 2 : L;"),
+    "prefill_group_modulo": ("const int64_t kv_head = (ih % n_qo_heads) / G;",
+                             "const int64_t kv_head = (ih % n_qo_heads) % n_kv_heads;"),
+    "prefill_drop_scale": ("s[j] = qk * scale;", "s[j] = qk;"),
+    "prefill_v_reads_k": ("orow[d] += w * widen_bf16(v_pool[row * head_dim + d]);",
+                          "orow[d] += w * widen_bf16(k_pool[row * head_dim + d]);"),
+    "prefill_weights_vs_max": ("const double w = std::exp(s[j] - log_denom);",
+                               "const double w = std::exp(s[j] - smax);"),
     "query_head_offset": ("qd[d] = widen_bf16(q[bh * head_dim + d]);",
                           "qd[d] = widen_bf16(q[(b * n_qo_heads + (h ^ 1) % n_qo_heads) * head_dim + d]);"),
 }

@@ -30,3 +30,11 @@ def test_thread_count_does_not_change_results(oracle_mod):
     a = oracle_mod.decode(q, k, v, indptr, indices, 32, 8, 128, scale, n_threads=1)
     b = oracle_mod.decode(q, k, v, indptr, indices, 32, 8, 128, scale, n_threads=4)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_prefill_rejects_chunk_longer_than_context(oracle_mod):
+    rng = np.random.default_rng(3)
+    q, k, v, qo, kvp, idx, scale = P.prefill_case(rng, [2], [2], 2, 1, 4)
+    with pytest.raises(ValueError):
+        oracle_mod.prefill(q, k, v, np.array([0, 2], np.int32), np.array([0, 1], np.int32),
+                           idx[:1], 2, 1, 4, scale)
