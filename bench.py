@@ -35,6 +35,7 @@ import workloads  # noqa: E402
 METRIC = "paged GQA decode attn: HBM GB/s & % of peak; µs/step at batch 8/32/128"
 DEFAULT_CONFIG = 2
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -412,6 +413,126 @@ def run_tier_bench(args):
     return 0
 
 
+def measured_tensor_peak():
+    """Sustained dense bf16 rate (a kernel timed inside a long step)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "of measured (sustained)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS_SUSTAINED, "of fallback (sustained)"
+
+
+class PrefillState:
+    """Device tensors of one chunked-prefill step for every layer, plus the plan.
+    A layer is kvpool_append of the chunks' rows, then paged_prefill_attn."""
+
+    def __init__(self, pw: workloads.PrefillWorkload, device="cuda", layers=None):
+        import paged_kv_gqa_tokentokvpool_gb300 as pkv
+        self.pkv, self.pw = pkv, pw
+        dev = torch.device(device)
+        self.layer_ids = list(range(pw.layers)) if layers is None else list(layers)
+        self.t = [workloads.prefill_tensors(pw, l, device=dev) for l in self.layer_ids]
+        self.out = [torch.empty(pw.total_q, pw.n_qo_heads, pw.head_dim, dtype=torch.bfloat16,
+                                device=dev) for _ in self.layer_ids]
+        self.lse = [torch.empty(pw.total_q, pw.n_qo_heads, dtype=torch.float32, device=dev)
+                    for _ in self.layer_ids]
+        self.qo = torch.from_numpy(pw.qo_indptr).to(dev)
+        self.kv = torch.from_numpy(pw.kv_indptr).to(dev)
+        self.idx = torch.from_numpy(pw.kv_indices).to(dev)
+        self.slots = torch.from_numpy(pw.chunk_slots).to(dev)
+        self.plan = pkv.paged_prefill_plan_create(pw.batch, pw.total_q, pw.n_qo_heads,
+                                                  pw.n_kv_heads, pw.head_dim)
+        self.graph = None
+
+    def layers(self, events=None):
+        pkv, pw = self.pkv, self.pw
+        stream = torch.cuda.current_stream()
+        for i in range(len(self.layer_ids)):
+            q, kp, vp, kn, vn = self.t[i]
+            pkv.kvpool_append(kp, vp, self.slots, kn, vn, stream=stream)
+            if events is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            pkv.paged_prefill_attn(q, kp, vp, self.qo, self.kv, self.idx, pw.batch,
+                                   pw.n_qo_heads, pw.n_kv_heads, pw.head_dim, pw.sm_scale,
+                                   self.out[i], self.lse[i], self.plan, stream=stream)
+            if events is not None:
+                e1.record(stream)
+                events.append((e0, e1))
+
+    def run(self, events=None):
+        self.pkv.paged_prefill_plan(self.plan, self.pw.qo_indptr, self.pw.kv_indptr,
+                                    stream=torch.cuda.current_stream())
+        if self.graph is not None and events is None:
+            self.graph.replay()
+        else:
+            self.layers(events)
+
+    def capture(self):
+        self.run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.layers()
+        torch.cuda.synchronize()
+        self.graph = g
+
+
+def run_prefill_bench(args):
+    """Chunked prefill (the pages' 512- and 64-token chunks): useful causal
+    attention FLOP/s of the step, and of the attention kernel alone against the
+    tensor roofline."""
+    pw = workloads.prefill_config(args.prefill)
+    if args.layers is not None:
+        pw.layers = max(1, min(args.layers, pw.layers))
+    st = PrefillState(pw)
+    st.capture()
+    stream = torch.cuda.current_stream()
+    # causal attention: per query head and attended pair, 2 D flops for q.k and 2 D for p.v
+    flops_layer = 4.0 * pw.head_dim * pw.n_qo_heads * pw.attended_pairs()
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            st.run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    events = []
+    for _ in range(args.steps):
+        st.run(events)
+    torch.cuda.synchronize()
+    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in events]))
+    peak, peak_kind = measured_tensor_peak()
+    step_tflops = flops_layer * pw.layers / (ms * 1e-3) / 1e12
+    attn_tflops = flops_layer / (attn_ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "chunked-prefill attention over the token pool: useful causal TFLOP/s",
+        "value": step_tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{pw.name}: {pw.description}", "layers": pw.layers,
+                   "batch": pw.batch, "query_tokens": pw.total_q,
+                   "context_tokens": pw.total_tokens, "attended_pairs": pw.attended_pairs(),
+                   "flops_per_layer": flops_layer,
+                   "launch": "cuda graph of the layer loop (append + attention per layer)"},
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak,
+                     "unit": "TFLOP/s", "frac": attn_tflops / peak, "traffic": None,
+                     "kernel": f"paged_prefill_attn, avg of {len(events)} event-timed eager "
+                               f"calls {attn_ms * 1e3:.1f} us, mma.sync m16n8k16",
+                     "peak_kind": peak_kind},
+        "clocks": clocks.summary(),
+    }), flush=True)
+    return 0
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -475,6 +596,8 @@ def main(argv=None):
                     help="run kvpool_append as its own kernel before each attention call")
     ap.add_argument("--tier-bench", action="store_true",
                     help="measure the host KV tier (offload / prefetch) instead of the step")
+    ap.add_argument("--prefill", type=int, default=None, choices=[1, 2, 3],
+                    help="measure a chunked-prefill workload instead of the decode step")
     ap.add_argument("--no-share", action="store_true",
                     help="plan the prefix-sharing workload without describing its shared prefixes")
     ap.add_argument("--no-early", action="store_true",
@@ -493,6 +616,8 @@ def main(argv=None):
         return run_reference(args, world, rank)
     if args.tier_bench:
         return run_tier_bench(args)
+    if args.prefill is not None:
+        return run_prefill_bench(args)
 
     torch.cuda.set_device(local)
     pg = None

@@ -277,6 +277,69 @@ int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_he
 int paged_decode_plan_info(const pkv_plan* plan, int* batch, int* n_units, int* n_merges,
                            int* chunk_tokens, int* n_ctas);
 
+/*
+ * ---------------------------------------------------------------------------
+ * Chunked prefill over the same pool
+ * ---------------------------------------------------------------------------
+ * "Agent-Infer", section "连续批处理" (continuous batching): long prefills are cut
+ * into chunks (512 tokens by default, 64 while decodes are running) so that decode
+ * steps run between them. A chunk is a request's newest C tokens. Their K/V rows
+ * are already in the pool (kvpool_append) and their slots are the last C entries of
+ * the request's slot list of L >= C entries. Query c of the chunk (c < C) sits at
+ * list position p = L - C + c and attends causally to entries 0 .. p:
+ *   s_j      = sm_scale * dot(q[i,h,:], K[idx_j, g, :]),   j <= p
+ *   lse[i,h] = ln sum_{j<=p} exp(s_j)
+ *   out[i,h] = sum_{j<=p} exp(s_j - lse[i,h]) * V[idx_j, g, :]
+ * with i = qo_indptr[b] + c and g = h / (n_qo_heads / n_kv_heads).
+ */
+typedef struct pkv_prefill_plan pkv_prefill_plan; /* opaque, library-owned */
+
+/*
+ * paged_prefill_plan_create — allocate a reusable prefill plan for one shape.
+ *   max_batch    : largest batch of any step (>= 1)
+ *   max_q_tokens : largest qo_indptr[batch] of any step (>= 0)
+ *   n_qo_heads, n_kv_heads, head_dim : head_dim 128 or 256; group size
+ *                  n_qo_heads / n_kv_heads in {1, 2, 4, 8}
+ * Uses the current device. Synchronous. PKV_ERR_UNSUPPORTED for other shapes.
+ */
+int paged_prefill_plan_create(pkv_prefill_plan** plan, int max_batch, int64_t max_q_tokens,
+                              int n_qo_heads, int n_kv_heads, int head_dim);
+
+/*
+ * paged_prefill_plan — the step's work list, once per prefill step (reused by every
+ * layer). Cuts every chunk into tiles of 64 / G query tokens per KV head and orders
+ * the tiles longest causal range first. Uploaded asynchronously on `stream` from
+ * pinned staging; waits on the host for the previous step's upload first.
+ *   qo_indptr_host : [batch + 1] int32 HOST copy of the chunk offsets (qo_indptr[0] = 0,
+ *                    non-decreasing, qo_indptr[batch] <= max_q_tokens)
+ *   kv_indptr_host : [batch + 1] int32 HOST copy of the slot-list offsets; every
+ *                    request lists at least as many slots as its chunk has tokens
+ * Returns PKV_ERR_INVALID_ARG for bad offsets, PKV_ERR_PLAN if batch > max_batch.
+ */
+int paged_prefill_plan(pkv_prefill_plan* plan, const int32_t* qo_indptr_host,
+                       const int32_t* kv_indptr_host, int batch, pkv_stream_t stream);
+
+/*
+ * paged_prefill_attn — causal attention of the planned chunks, once per layer.
+ *   q          : [qo_indptr[batch], n_qo_heads, head_dim] bf16
+ *   k_pool, v_pool, kv_indices : as for paged_decode_attn (the chunk's rows appended)
+ *   qo_indptr, kv_indptr : [batch + 1] int32 device arrays equal to the plan's host
+ *                copies (checked against them when debug checks are on)
+ *   out        : [qo_indptr[batch], n_qo_heads, head_dim] bf16, written
+ *   lse        : [qo_indptr[batch], n_qo_heads] fp32 natural-log lse, or NULL
+ *   plan       : built by paged_prefill_plan for this step, same shape
+ * One kernel launch (none when the step has no query tokens). fp32 accumulation
+ * and an online softmax; q, pools and out must be 16-byte aligned.
+ */
+int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
+                       const int32_t* qo_indptr, const int32_t* kv_indptr,
+                       const int32_t* kv_indices, int batch, int n_qo_heads, int n_kv_heads,
+                       int head_dim, float sm_scale, void* out, float* lse,
+                       const pkv_prefill_plan* plan, pkv_stream_t stream);
+
+/* paged_prefill_plan_destroy — free a prefill plan (waits for its pending upload). NULL is a no-op. */
+void paged_prefill_plan_destroy(pkv_prefill_plan* plan);
+
 /* Flags for paged_decode_plan_set_flags. */
 #define PKV_PLAN_EARLY_GATHER 1u
 

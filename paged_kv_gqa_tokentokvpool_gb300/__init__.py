@@ -39,7 +39,8 @@ EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",
             "paged_decode_plan_info", "paged_decode_plan_status", "paged_decode_attn_static",
             "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
-            "kvpool_prefetch", "paged_decode_plan_set_flags",
+            "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
+            "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_destroy",
             "pkv_set_debug_checks", "pkv_last_error")
 
 
@@ -73,6 +74,12 @@ def _load() -> ctypes.CDLL:
     lib.paged_decode_plan_info.argtypes = [P, P, P, P, P, P]
     lib.paged_decode_plan_status.argtypes = [P, P]
     lib.paged_decode_plan_set_flags.argtypes = [P, ctypes.c_uint]
+    lib.paged_prefill_plan_create.argtypes = [ctypes.POINTER(P), I32, I64, I32, I32, I32]
+    lib.paged_prefill_plan.argtypes = [P, P, P, I32, P]
+    lib.paged_prefill_attn.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, ctypes.c_float,
+                                       P, P, P, P]
+    lib.paged_prefill_plan_destroy.argtypes = [P]
+    lib.paged_prefill_plan_destroy.restype = None
     lib.paged_decode_attn_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32,
                                              ctypes.c_float, P, P, P]
     lib.paged_decode_append_attn.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I64,
@@ -85,7 +92,8 @@ def _load() -> ctypes.CDLL:
                  "paged_decode_attn", "paged_decode_plan_host", "paged_decode_plan_info",
                  "paged_decode_plan_status", "paged_decode_attn_static",
                  "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
-                 "kvpool_prefetch", "paged_decode_plan_set_flags"):
+                 "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
+                 "paged_prefill_plan", "paged_prefill_attn"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -236,7 +244,7 @@ def paged_decode_plan_create(max_batch: int, max_tokens: int, n_qo_heads: int,
 def _host_indptr(kv_indptr) -> np.ndarray:
     if isinstance(kv_indptr, torch.Tensor):
         if kv_indptr.is_cuda:
-            raise TypeError("paged_decode_plan takes the HOST copy of kv_indptr")
+            raise TypeError("plans take HOST copies of the offset arrays")
         kv_indptr = kv_indptr.numpy()
     return np.ascontiguousarray(kv_indptr, dtype=np.int32)
 
@@ -321,6 +329,61 @@ def paged_decode_plan_set_flags(plan: Plan, flags: int) -> None:
     """Options of the attention calls that use the plan (PKV_PLAN_* bits)."""
     _check(library().paged_decode_plan_set_flags(plan.handle if plan is not None else None,
                                                  int(flags)))
+
+
+class PrefillPlan:
+    """Owns a ``pkv_prefill_plan*``; freed by ``paged_prefill_plan_destroy`` or on collection."""
+
+    def __init__(self, handle: ctypes.c_void_p, shape):
+        self.handle = handle
+        self.shape = shape
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.paged_prefill_plan_destroy(self.handle)
+            self.handle = None
+
+
+def paged_prefill_plan_create(max_batch: int, max_q_tokens: int, n_qo_heads: int,
+                              n_kv_heads: int, head_dim: int) -> PrefillPlan:
+    h = ctypes.c_void_p()
+    _check(library().paged_prefill_plan_create(ctypes.byref(h), max_batch, max_q_tokens,
+                                               n_qo_heads, n_kv_heads, head_dim))
+    return PrefillPlan(h, (n_qo_heads, n_kv_heads, head_dim))
+
+
+def paged_prefill_plan(plan: PrefillPlan, qo_indptr_host, kv_indptr_host, batch=None,
+                       stream=None) -> None:
+    """The step's prefill work list from HOST copies of the chunk and slot-list offsets."""
+    qo = _host_indptr(qo_indptr_host)
+    kv = _host_indptr(kv_indptr_host)
+    batch = kv.size - 1 if batch is None else batch
+    plan._indptr_keepalive = (qo, kv)
+    _check(library().paged_prefill_plan(plan.handle, _ptr(qo), _ptr(kv), batch,
+                                        _stream(stream)))
+
+
+def paged_prefill_attn(q, k_pool, v_pool, qo_indptr, kv_indptr, kv_indices, batch, n_qo_heads,
+                       n_kv_heads, head_dim, sm_scale, out, lse, plan: PrefillPlan,
+                       stream=None) -> None:
+    """Causal attention of the planned chunks: q/out [qo_indptr[batch], Hq, D] bf16."""
+    for t, name in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"), (out, "out")):
+        _dev(t, torch.bfloat16, name)
+    for t, name in ((qo_indptr, "qo_indptr"), (kv_indptr, "kv_indptr"),
+                    (kv_indices, "kv_indices")):
+        _dev(t, torch.int32, name)
+    if lse is not None:
+        _dev(lse, torch.float32, "lse")
+    _check(library().paged_prefill_attn(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices),
+        batch, n_qo_heads, n_kv_heads, head_dim, float(sm_scale), _ptr(out), _ptr(lse),
+        plan.handle, _stream(stream)))
+
+
+def paged_prefill_plan_destroy(plan: PrefillPlan) -> None:
+    if plan.handle:
+        library().paged_prefill_plan_destroy(plan.handle)
+        plan.handle = None
 
 
 def paged_decode_plan_destroy(plan: Plan) -> None:

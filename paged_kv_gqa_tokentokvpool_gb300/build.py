@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "pkv")
 LIB_PATH = os.path.join(HERE, "libpkv.so")
-SOURCES = ["api.cu", "append.cu", "decode.cu", "plan_host.cpp", "attn_static.cu", "tier.cu"]
+SOURCES = ["api.cu", "append.cu", "decode.cu", "plan_host.cpp", "attn_static.cu", "tier.cu",
+           "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,589 @@
+// Chunked-prefill attention over the page-size-1 token pool.
+//
+// What is computed ("Agent-Infer: 纯 Rust 编写的高性能 LLM 推理引擎", section
+// "连续批处理": long prefills run in chunks of 512 tokens, 64 while decodes are
+// running, between decode steps; the pool is the same TokenToKVPool as for decode,
+// section "分页 KV 缓存"): a chunk is a request's newest C tokens, already appended,
+// so they are the last C of its L listed slots. Query c of the chunk sits at list
+// position p = L - C + c and attends causally to entries 0 .. p:
+//     out[i,h] = softmax_{j<=p}(sm_scale * q[i,h] . K[idx_j, g]) . V[idx_j, g]
+//     lse[i,h] = ln sum_{j<=p} exp(sm_scale * q[i,h] . K[idx_j, g])
+// with g = h / G (grouped-query attention, "Pegainfer: 纯Rust+CUDA构建的LLM推理引擎",
+// section "1. 注意力机制优化").
+//
+// Design for sm_103a. Unlike decode, every K/V row here serves the 64 / G query
+// tokens of a tile times G heads, so the work is a dense contraction per KV head:
+//  * One CTA per work unit (request, KV head, tile of 64 / G chunk tokens): its 64
+//    query rows (token, head) are four 16-row warp tiles. The plan orders units
+//    longest causal range first, so the grid drains evenly.
+//  * The unit's q rows are staged once in shared memory; the request's slot rows
+//    of that KV head stream through a ring of 32-token K/V tiles gathered with
+//    16-byte cp.async (each thread copies whole 16-byte pieces of scattered pool
+//    rows; a stage's slot ids are loaded one iteration ahead of its copies).
+//  * Tensor cores, FlashAttention-2 orientation: per warp and tile
+//      S[16 x 32] = Q[16 x D] K^T    and    O[16 x D] += P[16 x 32] V[32 x D]
+//    with mma.sync m16n8k16 (bf16, fp32 accumulate). K fragments come by
+//    ldmatrix, V by ldmatrix.trans, and the probabilities pass from the S
+//    accumulators to the A operand of P V in registers.
+//  * Online softmax in base 2 with fp32 state per row; the causal mask compares
+//    each token's list position with the row's query position, and the ring
+//    stops at the unit's last query position.
+//  * No spin-waits: the ring is cp.async groups and CTA barriers.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <new>
+#include <vector>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kPfWarps = 4;
+constexpr int kPfThreads = 32 * kPfWarps;
+constexpr int kPfRows = 16 * kPfWarps;  // query rows (token, head) per CTA
+constexpr int kPfKvTile = 32;           // KV tokens per ring stage
+constexpr int kPfPad = 8;               // bf16 padding per shared row: conflict-free ldmatrix
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// One work unit: query tokens q_row0 .. q_row0 + n_q - 1 (rows of q/out) of request
+// b, KV head g; the request's slot list starts at kv_begin, the unit's first query
+// sits at list position pos0, and its queries together see entries 0 .. n_kv - 1.
+struct PfUnit {
+    int32_t b, g, q_row0, n_q, kv_begin, pos0, n_kv, pad;
+};
+static_assert(sizeof(PfUnit) == 32, "unit record");
+
+struct PfArgs {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* kv_indices;
+    const PfUnit* units;
+    int n_qo_heads;
+    int n_kv_heads;
+    float scale_log2;  // sm_scale * log2(e)
+    void* out;
+    float* lse;
+};
+
+template <int D, int G>
+struct PfCfg {
+    static constexpr int kStages = D == 128 ? 3 : 2;   // 2 CTAs per SM at D = 256
+    static constexpr int kPitch = D + kPfPad;          // shared row pitch (bf16)
+    static constexpr int kQBytes = kPfRows * kPitch * 2;
+    static constexpr int kKvBytes = kPfKvTile * kPitch * 2;  // K (or V) of one stage
+    static constexpr int kStageBytes = 2 * kKvBytes;
+    static constexpr int kSmem = kQBytes + kStages * kStageBytes;
+    static constexpr int kChunks = D / 8;                  // 16-byte pieces per row
+    static constexpr int kPieces = kPfKvTile * kChunks / kPfThreads;  // per thread, K (or V)
+    static constexpr int kKSteps = D / 16;
+    static constexpr int kNT = kPfKvTile / 8;              // 8-token column tiles of S
+    static constexpr int kDT = D / 8;                      // 8-dim column tiles of O
+    static_assert(kPieces * kPfThreads == kPfKvTile * kChunks, "ring pieces");
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (PTX ISA: cp.async, ldmatrix, mma, griddepcontrol, ex2)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async copy; with valid = false nothing is read and the 16 bytes are zero.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float minus_inf() { return __int_as_float(0xff800000); }
+
+// ---------------------------------------------------------------------------
+// kernel
+// ---------------------------------------------------------------------------
+
+// Slot ids of the pieces this thread copies for KV tile `tile` (-1 past the range).
+template <int D, int G>
+__device__ __forceinline__ void load_tile_slots(const PfArgs& a, const PfUnit& un, int tile,
+                                                int (&slot)[PfCfg<D, G>::kPieces]) {
+    using C = PfCfg<D, G>;
+#pragma unroll
+    for (int i = 0; i < C::kPieces; ++i) {
+        const int tok = (threadIdx.x + i * kPfThreads) / C::kChunks;
+        const int j = tile * kPfKvTile + tok;
+        slot[i] = j < un.n_kv ? __ldg(a.kv_indices + un.kv_begin + j) : -1;
+    }
+}
+
+// Issue the cp.async copies of KV tile pieces into ring stage `st` (tokens past the
+// unit's range are zero-filled).
+template <int D, int G>
+__device__ __forceinline__ void issue_tile(const PfArgs& a, const PfUnit& un, uint8_t* smem,
+                                           int st, const int (&slot)[PfCfg<D, G>::kPieces]) {
+    using C = PfCfg<D, G>;
+    const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_pool);
+    const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_pool);
+    uint8_t* sk = smem + C::kQBytes + st * C::kStageBytes;
+    uint8_t* sv = sk + C::kKvBytes;
+#pragma unroll
+    for (int i = 0; i < C::kPieces; ++i) {
+        const int c = threadIdx.x + i * kPfThreads;
+        const int tok = c / C::kChunks, part = c % C::kChunks;
+        const bool valid = slot[i] >= 0;
+        const int64_t off = (int64_t(valid ? slot[i] : 0) * a.n_kv_heads + un.g) * D + part * 8;
+        const int soff = (tok * C::kPitch + part * 8) * 2;
+        cp_async16(smem_addr(sk + soff), kp + off, valid);
+        cp_async16(smem_addr(sv + soff), vp + off, valid);
+    }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs a) {
+    using C = PfCfg<D, G>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const PfUnit un = a.units[blockIdx.x];  // plan data: read before the wait
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    // q, the pools and their indices may come from the previous kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- the unit's q rows (row r: chunk token r / G, head r % G) -> shared memory
+    {
+        const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+        for (int c = tid; c < kPfRows * C::kChunks; c += kPfThreads) {
+            const int r = c / C::kChunks, part = c % C::kChunks;
+            const int t = r / G, h = r % G;
+            const bool valid = t < un.n_q;
+            const int64_t off =
+                (int64_t(un.q_row0 + (valid ? t : 0)) * a.n_qo_heads + un.g * G + h) * D + part * 8;
+            cp_async16(smem_addr(smem + (r * C::kPitch + part * 8) * 2), q + off, valid);
+        }
+    }
+    // ---- ring prologue: tiles 0 .. kStages - 2, and the slot ids of the next one
+    const int n_tiles = (un.n_kv + kPfKvTile - 1) / kPfKvTile;
+    int slot[C::kPieces];
+#pragma unroll
+    for (int s = 0; s < C::kStages - 1; ++s) {
+        if (s < n_tiles) {
+            load_tile_slots<D, G>(a, un, s, slot);
+            issue_tile<D, G>(a, un, smem, s, slot);
+        }
+        cp_commit();  // one group per tile (the first also holds q)
+    }
+    if (C::kStages - 1 < n_tiles) load_tile_slots<D, G>(a, un, C::kStages - 1, slot);
+
+    // per lane: rows lo = 16 warp + g8 and hi = lo + 8 of the unit's 64
+    const int r_lo = 16 * warp + g8, r_hi = r_lo + 8;
+    const int pos_lo = un.pos0 + r_lo / G, pos_hi = un.pos0 + r_hi / G;
+    float m_lo = minus_inf(), m_hi = minus_inf(), l_lo = 0.f, l_hi = 0.f;
+    float o[C::kDT][4];
+#pragma unroll
+    for (int dt = 0; dt < C::kDT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+
+    // ldmatrix lane addresses
+    const uint32_t q_addr = smem_addr(smem) +
+                            ((16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1)) * C::kPitch +
+                             8 * (lane >> 4)) * 2;
+    const int mi = lane >> 3;
+    const uint32_t k_off = ((8 * (mi >> 1) + (lane & 7)) * C::kPitch + 8 * (mi & 1)) * 2;
+    const uint32_t v_off = ((8 * (mi & 1) + (lane & 7)) * C::kPitch + 8 * (mi >> 1)) * 2;
+
+    for (int n = 0; n < n_tiles; ++n) {
+        // copies of tile n + kStages - 1 (slot ids loaded last iteration), then the
+        // slot ids of the tile after it
+        const int ahead = n + C::kStages - 1;
+        if (ahead < n_tiles) issue_tile<D, G>(a, un, smem, ahead % C::kStages, slot);
+        cp_commit();
+        if (ahead + 1 < n_tiles) load_tile_slots<D, G>(a, un, ahead + 1, slot);
+        cp_wait<C::kStages - 1>();  // tile n (and q) have landed for this thread
+        __syncthreads();            // ... and for every thread
+
+        const int st = n % C::kStages;
+        const uint32_t sk = smem_addr(smem) + C::kQBytes + st * C::kStageBytes;
+        const uint32_t sv = sk + C::kKvBytes;
+        // S = Q K^T for this warp's 16 rows and the tile's 32 tokens
+        float s[C::kNT][4];
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+            uint32_t qa[4];
+            ldsm4(q_addr + ks * 32, qa);
+#pragma unroll
+            for (int np = 0; np < C::kNT / 2; ++np) {
+                uint32_t kb[4];
+                ldsm4(sk + k_off + (16 * np * C::kPitch + 16 * ks) * 2, kb);
+                mma16816(s[2 * np], qa, kb[0], kb[1]);
+                mma16816(s[2 * np + 1], qa, kb[2], kb[3]);
+            }
+        }
+        // causal mask and online softmax (base 2); token j of the tile is list
+        // position n * 32 + 8 nt + 2 t4 (+1); c[0..1] are row lo, c[2..3] row hi
+        const int j0 = n * kPfKvTile + 2 * t4;
+        float mx_lo = minus_inf(), mx_hi = minus_inf();
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) {
+            const int j = j0 + 8 * nt;
+            s[nt][0] = j <= pos_lo ? s[nt][0] * a.scale_log2 : minus_inf();
+            s[nt][1] = j + 1 <= pos_lo ? s[nt][1] * a.scale_log2 : minus_inf();
+            s[nt][2] = j <= pos_hi ? s[nt][2] * a.scale_log2 : minus_inf();
+            s[nt][3] = j + 1 <= pos_hi ? s[nt][3] * a.scale_log2 : minus_inf();
+            mx_lo = fmaxf(mx_lo, fmaxf(s[nt][0], s[nt][1]));
+            mx_hi = fmaxf(mx_hi, fmaxf(s[nt][2], s[nt][3]));
+        }
+#pragma unroll
+        for (int off = 1; off < 4; off <<= 1) {
+            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(kFullMask, mx_lo, off));
+            mx_hi = fmaxf(mx_hi, __shfl_xor_sync(kFullMask, mx_hi, off));
+        }
+        // every row sees list entry 0 in tile 0, so the maxima are finite from then on
+        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+        const float al_lo = exp2_approx(m_lo - mn_lo), al_hi = exp2_approx(m_hi - mn_hi);
+        m_lo = mn_lo;
+        m_hi = mn_hi;
+        float sum_lo = 0.f, sum_hi = 0.f;
+        uint32_t pa[C::kNT / 2][4];
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) {
+            const float p0 = exp2_approx(s[nt][0] - mn_lo), p1 = exp2_approx(s[nt][1] - mn_lo);
+            const float p2 = exp2_approx(s[nt][2] - mn_hi), p3 = exp2_approx(s[nt][3] - mn_hi);
+            sum_lo += p0 + p1;
+            sum_hi += p2 + p3;
+            // S accumulators of column tiles 2k, 2k+1 form the A operand of k-step k
+            pa[nt >> 1][(nt & 1) * 2] = pack2(p0, p1);
+            pa[nt >> 1][(nt & 1) * 2 + 1] = pack2(p2, p3);
+        }
+        l_lo = fmaf(l_lo, al_lo, sum_lo);
+        l_hi = fmaf(l_hi, al_hi, sum_hi);
+#pragma unroll
+        for (int dt = 0; dt < C::kDT; ++dt) {
+            o[dt][0] *= al_lo;
+            o[dt][1] *= al_lo;
+            o[dt][2] *= al_hi;
+            o[dt][3] *= al_hi;
+        }
+        // O += P V
+#pragma unroll
+        for (int kk = 0; kk < C::kNT / 2; ++kk) {
+#pragma unroll
+            for (int dp = 0; dp < C::kDT / 2; ++dp) {
+                uint32_t vb[4];
+                ldsm4_t(sv + v_off + (16 * kk * C::kPitch + 16 * dp) * 2, vb);
+                mma16816(o[2 * dp], pa[kk], vb[0], vb[1]);
+                mma16816(o[2 * dp + 1], pa[kk], vb[2], vb[3]);
+            }
+        }
+        __syncthreads();  // the stage is read before the next iteration refills it
+    }
+    cp_wait<0>();
+
+    // ---- epilogue: rows lo / hi of this lane
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        l_lo += __shfl_xor_sync(kFullMask, l_lo, off);
+        l_hi += __shfl_xor_sync(kFullMask, l_hi, off);
+    }
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = half ? r_hi : r_lo;
+        const int t = r / G, h = r % G;
+        if (t >= un.n_q) continue;
+        const float lt = half ? l_hi : l_lo;
+        const float inv = 1.f / lt;
+        const int64_t row = int64_t(un.q_row0 + t) * a.n_qo_heads + un.g * G + h;
+        __nv_bfloat16* dst = out + row * D + 2 * t4;
+#pragma unroll
+        for (int dt = 0; dt < C::kDT; ++dt)
+            *reinterpret_cast<uint32_t*>(dst + 8 * dt) =
+                pack2(o[dt][2 * half] * inv, o[dt][2 * half + 1] * inv);
+        if (a.lse != nullptr && t4 == 0) a.lse[row] = ((half ? m_hi : m_lo) + __log2f(lt)) * kLn2;
+    }
+}
+
+template <int D, int G>
+cudaError_t launch_prefill(const PfArgs& a, int n_units, cudaStream_t stream) {
+    using C = PfCfg<D, G>;
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        paged_prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (attr != cudaSuccess) return attr;
+    if (n_units == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_units);
+    cfg.blockDim = dim3(kPfThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, G>, a);
+}
+
+cudaError_t launch_prefill_any(const PfArgs& a, int head_dim, int group, int n_units,
+                               cudaStream_t stream) {
+#define PKV_PF(D_)                                                  \
+    switch (group) {                                                \
+        case 1: return launch_prefill<D_, 1>(a, n_units, stream);   \
+        case 2: return launch_prefill<D_, 2>(a, n_units, stream);   \
+        case 4: return launch_prefill<D_, 4>(a, n_units, stream);   \
+        case 8: return launch_prefill<D_, 8>(a, n_units, stream);   \
+        default: break;                                             \
+    }
+    if (head_dim == 128) { PKV_PF(128) }
+    if (head_dim == 256) { PKV_PF(256) }
+#undef PKV_PF
+    return cudaErrorInvalidValue;
+}
+
+bool prefill_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim) {
+    if (n_kv_heads <= 0 || n_qo_heads <= 0 || n_qo_heads % n_kv_heads != 0) return false;
+    const int G = n_qo_heads / n_kv_heads;
+    return (G == 1 || G == 2 || G == 4 || G == 8) && (head_dim == 128 || head_dim == 256);
+}
+
+int pf_cuda_fail(cudaError_t e, const char* what) {
+    return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+}  // namespace
+}  // namespace pkv
+
+struct pkv_prefill_plan {
+    int device = 0;
+    int max_batch = 0;
+    int64_t max_q_tokens = 0;
+    int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0;
+    int tile_tokens = 0;  // query tokens per unit: 64 / G
+    int max_units = 0;
+    pkv::PfUnit* host_units = nullptr;  // pinned staging
+    pkv::PfUnit* dev_units = nullptr;
+    cudaEvent_t copy_done = nullptr;
+    bool copy_pending = false;
+    bool planned = false;
+    int batch = 0;
+    int n_units = 0;
+    std::vector<int32_t> qo_host, kv_host;  // the step's offsets (debug checks)
+};
+
+using namespace pkv;
+
+extern "C" {
+
+int paged_prefill_plan_create(pkv_prefill_plan** out_plan, int max_batch, int64_t max_q_tokens,
+                              int n_qo_heads, int n_kv_heads, int head_dim) {
+    clear_error();
+    if (!out_plan) return fail(PKV_ERR_INVALID_ARG, "paged_prefill_plan_create: plan is NULL");
+    *out_plan = nullptr;
+    if (max_batch < 1 || max_q_tokens < 0 || max_q_tokens > INT32_MAX)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "paged_prefill_plan_create: need max_batch >= 1 and 0 <= max_q_tokens < 2^31");
+    if (!prefill_shape_supported(n_qo_heads, n_kv_heads, head_dim))
+        return fail(PKV_ERR_UNSUPPORTED,
+                    "paged_prefill_plan_create: unsupported shape (n_qo_heads=%d, n_kv_heads=%d, "
+                    "head_dim=%d); need head_dim 128/256 and group 1/2/4/8",
+                    n_qo_heads, n_kv_heads, head_dim);
+    pkv_prefill_plan* p = new (std::nothrow) pkv_prefill_plan();
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "paged_prefill_plan_create: out of host memory");
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e != cudaSuccess) {
+        delete p;
+        return pf_cuda_fail(e, "paged_prefill_plan_create: device query");
+    }
+    p->max_batch = max_batch;
+    p->max_q_tokens = max_q_tokens;
+    p->n_qo_heads = n_qo_heads;
+    p->n_kv_heads = n_kv_heads;
+    p->head_dim = head_dim;
+    p->tile_tokens = kPfRows / (n_qo_heads / n_kv_heads);
+    const int64_t units = (max_q_tokens / p->tile_tokens + max_batch) * int64_t(n_kv_heads);
+    if (units > INT32_MAX / 2) {
+        delete p;
+        return fail(PKV_ERR_INVALID_ARG, "paged_prefill_plan_create: too many work units");
+    }
+    p->max_units = static_cast<int>(units);
+    e = cudaMallocHost(reinterpret_cast<void**>(&p->host_units), sizeof(PfUnit) * size_t(units));
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->dev_units), sizeof(PfUnit) * size_t(units));
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->copy_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        paged_prefill_plan_destroy(p);
+        return pf_cuda_fail(e, "paged_prefill_plan_create: allocation");
+    }
+    *out_plan = p;
+    return PKV_OK;
+}
+
+void paged_prefill_plan_destroy(pkv_prefill_plan* p) {
+    if (p == nullptr) return;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    cudaSetDevice(p->device);
+    if (p->copy_done) {
+        cudaEventSynchronize(p->copy_done);
+        cudaEventDestroy(p->copy_done);
+    }
+    if (p->host_units) cudaFreeHost(p->host_units);
+    if (p->dev_units) cudaFree(p->dev_units);
+    if (prev >= 0) cudaSetDevice(prev);
+    delete p;
+}
+
+int paged_prefill_plan(pkv_prefill_plan* p, const int32_t* qo_indptr_host,
+                       const int32_t* kv_indptr_host, int batch, pkv_stream_t stream) {
+    clear_error();
+    const char* who = "paged_prefill_plan";
+    if (!p) return fail(PKV_ERR_PLAN, "%s: plan is NULL", who);
+    p->planned = false;
+    if (batch < 0 || batch > p->max_batch)
+        return fail(PKV_ERR_PLAN, "%s: batch %d outside [0, %d]", who, batch, p->max_batch);
+    if (!qo_indptr_host || !kv_indptr_host)
+        return fail(PKV_ERR_INVALID_ARG, "%s: NULL offsets", who);
+    if (qo_indptr_host[0] != 0 || kv_indptr_host[0] != 0)
+        return fail(PKV_ERR_INVALID_ARG, "%s: offsets must start at 0", who);
+    for (int b = 0; b < batch; ++b) {
+        const int C = qo_indptr_host[b + 1] - qo_indptr_host[b];
+        const int L = kv_indptr_host[b + 1] - kv_indptr_host[b];
+        if (C < 0 || L < 0)
+            return fail(PKV_ERR_INVALID_ARG, "%s: offsets decrease at request %d", who, b);
+        if (C > L)
+            return fail(PKV_ERR_INVALID_ARG,
+                        "%s: request %d has a chunk of %d tokens but lists only %d slots", who, b,
+                        C, L);
+    }
+    if (int64_t(qo_indptr_host[batch]) > p->max_q_tokens)
+        return fail(PKV_ERR_PLAN, "%s: %d query tokens exceed the plan's max_q_tokens %lld", who,
+                    qo_indptr_host[batch], (long long)p->max_q_tokens);
+    if (p->copy_pending) {  // the staging may still feed the previous step's copy
+        cudaError_t e = cudaEventSynchronize(p->copy_done);
+        if (e != cudaSuccess) return pf_cuda_fail(e, "waiting for the previous prefill plan copy");
+        p->copy_pending = false;
+    }
+    int n = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int C = qo_indptr_host[b + 1] - qo_indptr_host[b];
+        const int L = kv_indptr_host[b + 1] - kv_indptr_host[b];
+        for (int t0 = 0; t0 < C; t0 += p->tile_tokens) {
+            const int n_q = std::min(p->tile_tokens, C - t0);
+            const int pos0 = L - C + t0;
+            for (int g = 0; g < p->n_kv_heads; ++g) {
+                if (n >= p->max_units)
+                    return fail(PKV_ERR_PLAN, "%s: more work units than the plan holds (%d)", who,
+                                p->max_units);
+                p->host_units[n++] = PfUnit{b, g, qo_indptr_host[b] + t0, n_q,
+                                            kv_indptr_host[b], pos0, pos0 + n_q, 0};
+            }
+        }
+    }
+    // longest causal range first: the grid's last CTAs are the short ones
+    std::stable_sort(p->host_units, p->host_units + n,
+                     [](const PfUnit& x, const PfUnit& y) { return x.n_kv > y.n_kv; });
+    if (n > 0) {
+        cudaError_t e = cudaMemcpyAsync(p->dev_units, p->host_units, sizeof(PfUnit) * size_t(n),
+                                        cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaEventRecord(p->copy_done, stream);
+        if (e != cudaSuccess) return pf_cuda_fail(e, "prefill plan upload");
+        p->copy_pending = true;
+    }
+    p->batch = batch;
+    p->n_units = n;
+    p->qo_host.assign(qo_indptr_host, qo_indptr_host + batch + 1);
+    p->kv_host.assign(kv_indptr_host, kv_indptr_host + batch + 1);
+    p->planned = true;
+    return PKV_OK;
+}
+
+int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
+                       const int32_t* qo_indptr, const int32_t* kv_indptr,
+                       const int32_t* kv_indices, int batch, int n_qo_heads, int n_kv_heads,
+                       int head_dim, float sm_scale, void* out, float* lse,
+                       const pkv_prefill_plan* p, pkv_stream_t stream) {
+    clear_error();
+    const char* who = "paged_prefill_attn";
+    if (!p || !p->planned) return fail(PKV_ERR_PLAN, "%s: plan is NULL or not planned", who);
+    if (batch != p->batch)
+        return fail(PKV_ERR_PLAN, "%s: batch %d differs from the plan's %d", who, batch, p->batch);
+    if (n_qo_heads != p->n_qo_heads || n_kv_heads != p->n_kv_heads || head_dim != p->head_dim)
+        return fail(PKV_ERR_PLAN, "%s: shape differs from the plan's", who);
+    if (!std::isfinite(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "%s: sm_scale not finite", who);
+    if (p->n_units == 0) return PKV_OK;
+    if (!q || !k_pool || !v_pool || !qo_indptr || !kv_indptr || !kv_indices || !out)
+        return fail(PKV_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
+    const auto aligned16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return fail(PKV_ERR_INVALID_ARG, "%s: q, pools and out must be 16-byte aligned", who);
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(PKV_ERR_INVALID_ARG, "%s: lse must be 4-byte aligned", who);
+    if (debug_checks()) {
+        std::vector<int32_t> qo(batch + 1), kv(batch + 1);
+        cudaError_t e = cudaMemcpyAsync(qo.data(), qo_indptr, qo.size() * 4, cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(kv.data(), kv_indptr, kv.size() * 4, cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return pf_cuda_fail(e, "paged_prefill_attn: debug copy of offsets");
+        if (qo != p->qo_host || kv != p->kv_host)
+            return fail(PKV_ERR_INDEX, "%s: device offsets differ from the plan's host copies", who);
+    }
+    PfArgs a{};
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.kv_indices = kv_indices;
+    a.units = p->dev_units;
+    a.n_qo_heads = n_qo_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.scale_log2 = sm_scale * kLog2e;
+    a.out = out;
+    a.lse = lse;
+    const cudaError_t e =
+        launch_prefill_any(a, head_dim, n_qo_heads / n_kv_heads, p->n_units, stream);
+    if (e != cudaSuccess) return pf_cuda_fail(e, "paged_prefill_attn: launch");
+    return PKV_OK;
+}
+
+}  // extern "C"

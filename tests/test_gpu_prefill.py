@@ -1,0 +1,179 @@
+"""Chunked-prefill attention on the GPU against the fp64 oracle (parity tests).
+
+Every case follows a prefill step's flow: the chunk's K/V rows are appended to the
+pool with kvpool_append, the step is planned (paged_prefill_plan) and the chunk
+attends causally over its request's slot list (paged_prefill_attn). Pool slots no
+request lists hold bf16 NaN, and so do the chunk's slots before the append, so a
+stray or early read shows as NaN. Tolerances are those of the decode parity tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from test_gpu_parity import assert_parity, bits, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_gqa_tokentokvpool_gb300 import build
+    build.build()
+    import paged_kv_gqa_tokentokvpool_gb300 as m
+    return m
+
+
+def run_prefill(pkv, pw, layer=0, debug=False):
+    """GPU out/lse of one layer of a prefill workload, and the pools after the append."""
+    q, kp, vp, kn, vn = workloads.prefill_tensors(pw, layer, device="cpu",
+                                                  poison_unreferenced=True)
+    dev = torch.device("cuda")
+    B, Hq, Hkv, D, NQ = pw.batch, pw.n_qo_heads, pw.n_kv_heads, pw.head_dim, pw.total_q
+    kp_d, vp_d = kp.to(dev), vp.to(dev)
+    slots = torch.from_numpy(pw.chunk_slots).to(dev)
+    if NQ:
+        pkv.kvpool_append(kp_d, vp_d, slots, kn.to(dev), vn.to(dev))
+    plan = pkv.paged_prefill_plan_create(max(B, 1), max(NQ, 1), Hq, Hkv, D)
+    pkv.paged_prefill_plan(plan, pw.qo_indptr, pw.kv_indptr)
+    out = torch.full((max(NQ, 1), Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((max(NQ, 1), Hq), float("nan"), dtype=torch.float32, device=dev)
+    idx = torch.from_numpy(pw.kv_indices if pw.kv_indices.size else np.zeros(1, np.int32)).to(dev)
+    pkv.pkv_set_debug_checks(debug)
+    try:
+        pkv.paged_prefill_attn(q.to(dev) if NQ else out, kp_d, vp_d,
+                               torch.from_numpy(pw.qo_indptr).to(dev),
+                               torch.from_numpy(pw.kv_indptr).to(dev), idx, B, Hq, Hkv, D,
+                               pw.sm_scale, out, lse, plan)
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    torch.cuda.synchronize()
+    return out[:NQ], lse[:NQ], (q, kp, vp, kn, vn), (kp_d, vp_d)
+
+
+def oracle_prefill(pw, tensors, rows=None):
+    """Oracle out/lse (all chunk rows) from the generated pre-append tensors."""
+    q, kp, vp, kn, vn = tensors
+    k_after = oracle.append(bits(kp), pw.chunk_slots, bits(kn))
+    v_after = oracle.append(bits(vp), pw.chunk_slots, bits(vn))
+    return oracle.prefill(bits(q), k_after, v_after, pw.qo_indptr, pw.kv_indptr, pw.kv_indices,
+                          pw.n_qo_heads, pw.n_kv_heads, pw.head_dim, pw.sm_scale)
+
+
+PREFILL_CASES = [
+    # (chunks, contexts, Hq, Hkv, D)
+    ([64], [64], 32, 8, 128),                            # whole prompt, no prefix
+    ([512, 64, 1, 0, 100], [700, 64, 3000, 5, 100], 32, 8, 128),
+    ([17, 33], [40, 200], 8, 8, 128),                    # G = 1
+    ([9, 70], [9, 500], 16, 8, 128),                     # G = 2
+    ([13, 5], [100, 5], 64, 8, 128),                     # G = 8
+    ([1, 1, 1], [5, 1, 300], 32, 8, 128),                # one-token chunks
+    ([64, 31], [1000, 31], 16, 4, 256),                  # head_dim 256, G = 4
+    ([8, 3], [40, 8], 8, 1, 256),                        # head_dim 256, G = 8, one KV head
+    ([40], [40], 4, 4, 256),                             # head_dim 256, G = 1
+    ([200, 7], [4000, 2500], 16, 2, 128),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL_CASES)))
+def test_prefill_small_cases(pkv, case):
+    chunks, contexts, hq, hkv, d = PREFILL_CASES[case]
+    pw = workloads.prefill_workload(chunks, contexts, n_qo_heads=hq, n_kv_heads=hkv,
+                                    head_dim=d, seed=900 + case)
+    out, lse, tensors, (kp_d, _) = run_prefill(pkv, pw, debug=True)
+    ref_out, ref_lse = oracle_prefill(pw, tensors)
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what=f"prefill case {case}")
+    # the append wrote the chunk's rows bit-exactly
+    k_after = oracle.append(bits(tensors[1]), pw.chunk_slots, bits(tensors[3]))
+    assert np.array_equal(bits(kp_d), k_after)
+
+
+def test_prefill_plan_reused_across_layers(pkv):
+    """One plan serves every layer of the step (different q and pools per layer)."""
+    pw = workloads.prefill_workload([100, 37], [300, 37], layers=3, seed=77)
+    dev = torch.device("cuda")
+    plan = pkv.paged_prefill_plan_create(2, pw.total_q, 32, 8, 128)
+    pkv.paged_prefill_plan(plan, pw.qo_indptr, pw.kv_indptr)
+    qo = torch.from_numpy(pw.qo_indptr).to(dev)
+    kv = torch.from_numpy(pw.kv_indptr).to(dev)
+    idx = torch.from_numpy(pw.kv_indices).to(dev)
+    for layer in range(3):
+        q, kp, vp, kn, vn = workloads.prefill_tensors(pw, layer, poison_unreferenced=True)
+        kp_d, vp_d = kp.to(dev), vp.to(dev)
+        pkv.kvpool_append(kp_d, vp_d, torch.from_numpy(pw.chunk_slots).to(dev), kn.to(dev),
+                          vn.to(dev))
+        out = torch.empty(pw.total_q, 32, 128, dtype=torch.bfloat16, device=dev)
+        pkv.paged_prefill_attn(q.to(dev), kp_d, vp_d, qo, kv, idx, 2, 32, 8, 128, pw.sm_scale,
+                               out, None, plan)
+        torch.cuda.synchronize()
+        ref_out, ref_lse = oracle_prefill(pw, (q, kp, vp, kn, vn))
+        assert_parity(to_f64(out), ref_lse, ref_out, ref_lse, what=f"layer {layer}")
+
+
+def test_prefill_rejects_bad_calls(pkv):
+    plan = pkv.paged_prefill_plan_create(4, 1000, 32, 8, 128)
+    with pytest.raises(pkv.PkvError) as e:  # chunk longer than the slot list
+        pkv.paged_prefill_plan(plan, np.array([0, 10], np.int32), np.array([0, 9], np.int32))
+    assert e.value.code == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:  # more query tokens than the plan holds
+        pkv.paged_prefill_plan(plan, np.array([0, 1001], np.int32), np.array([0, 2000], np.int32))
+    assert e.value.code == pkv.PKV_ERR_PLAN
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_prefill_plan_create(4, 1000, 30, 8, 128)
+    assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
+    pkv.paged_prefill_plan(plan, np.array([0, 5, 9], np.int32), np.array([0, 50, 60], np.int32))
+    dev = torch.device("cuda")
+    z = torch.zeros(16, 32, 128, dtype=torch.bfloat16, device=dev)
+    pool = torch.zeros(64, 8, 128, dtype=torch.bfloat16, device=dev)
+    ip = torch.zeros(3, dtype=torch.int32, device=dev)
+    with pytest.raises(pkv.PkvError) as e:  # batch differs from the plan's
+        pkv.paged_prefill_attn(z, pool, pool, ip, ip, ip, 3, 32, 8, 128, 0.1, z, None, plan)
+    assert e.value.code == pkv.PKV_ERR_PLAN
+    with pytest.raises(pkv.PkvError) as e:  # shape differs from the plan's
+        pkv.paged_prefill_attn(z, pool, pool, ip, ip, ip, 2, 16, 8, 128, 0.1, z, None, plan)
+    assert e.value.code == pkv.PKV_ERR_PLAN
+    pkv.pkv_set_debug_checks(True)
+    try:  # device offsets that disagree with the plan's host copies
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.paged_prefill_attn(z, pool, pool, ip, ip, ip, 2, 32, 8, 128, 0.1, z, None, plan)
+        assert e.value.code == pkv.PKV_ERR_INDEX
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    torch.cuda.synchronize()
+    assert torch.all(z == 0), "a rejected call must not have launched"
+
+
+def test_prefill_empty_step(pkv):
+    pw = workloads.prefill_workload([0, 0], [5, 0], seed=3)
+    out, lse, _, _ = run_prefill(pkv, pw)
+    assert out.numel() == 0
+
+
+@pytest.mark.parametrize("config_no", [1, 3])
+def test_prefill_full_size_sampled(pkv, config_no):
+    """The benchmark's prefill workloads at full size (layer 0): every row of the
+    smallest request's chunk, and the first and last 16 rows of every other chunk
+    (by causality, the first rows need only the list up to their positions and
+    the last rows only a shorter chunk over the whole list)."""
+    pw = workloads.prefill_config(config_no)
+    out, lse, tensors, _ = run_prefill(pkv, pw)
+    q, kp, vp, kn, vn = tensors
+    k_after = oracle.append(bits(kp), pw.chunk_slots, bits(kn))
+    v_after = oracle.append(bits(vp), pw.chunk_slots, bits(vn))
+    qb = bits(q)
+    smallest = int(np.argmin(pw.contexts))
+    for b in range(pw.batch):
+        C, L = int(pw.chunks[b]), int(pw.contexts[b])
+        q0, k0 = int(pw.qo_indptr[b]), int(pw.kv_indptr[b])
+        idx = pw.kv_indices[k0:k0 + L]
+        pieces = [(0, C)] if (b == smallest and config_no == 1) else [(0, 16), (C - 16, C)]
+        for c0, c1 in pieces:
+            # rows c0 .. c1 of the chunk: a chunk of c1 - c0 tokens over the first
+            # L - C + c1 list entries
+            ref_o, ref_l = oracle.prefill(qb[q0 + c0:q0 + c1], k_after, v_after,
+                                          np.array([0, c1 - c0], np.int32),
+                                          np.array([0, L - C + c1], np.int32), idx[:L - C + c1],
+                                          pw.n_qo_heads, pw.n_kv_heads, pw.head_dim, pw.sm_scale)
+            assert_parity(to_f64(out[q0 + c0:q0 + c1]), lse[q0 + c0:q0 + c1].cpu().numpy(),
+                          ref_o, ref_l, what=f"prefill config {config_no} request {b} rows {c0}-{c1}")

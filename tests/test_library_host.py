@@ -74,6 +74,16 @@ def test_errors_are_reported_before_any_launch(pkv):
     assert lib.paged_decode_attn(p, p, p, p, p, 1, 32, 8, 128, ctypes.c_float(0.1), p, p, None,
                                  None) == pkv.PKV_ERR_PLAN
     assert lib.paged_decode_plan_set_flags(None, pkv.PKV_PLAN_EARLY_GATHER) == pkv.PKV_ERR_PLAN
+    # chunked prefill: shapes and sizes are checked before the device is touched
+    for hq, hkv, d in [(32, 8, 64), (30, 8, 128), (48, 4, 128), (32, 0, 128)]:
+        rc = lib.paged_prefill_plan_create(ctypes.byref(h), 8, 1000, hq, hkv, d)
+        assert rc == pkv.PKV_ERR_UNSUPPORTED, (hq, hkv, d, rc)
+    assert lib.paged_prefill_plan_create(ctypes.byref(h), 0, 1000, 32, 8, 128) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.paged_prefill_plan_create(None, 8, 1000, 32, 8, 128) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.paged_prefill_plan(None, p, p, 1, None) == pkv.PKV_ERR_PLAN
+    assert lib.paged_prefill_attn(p, p, p, p, p, p, 1, 32, 8, 128, ctypes.c_float(0.1), p, p,
+                                  None, None) == pkv.PKV_ERR_PLAN
+    lib.paged_prefill_plan_destroy(None)  # no-op
     lib.paged_decode_plan_destroy(None)  # no-op
 
 

@@ -254,3 +254,137 @@ def layer_tensors(wl: Workload, layer: int, device="cpu", poison_unreferenced=Fa
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bf16 bit patterns of a tensor as a host uint16 array (no arithmetic)."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill ("Agent-Infer", section "连续批处理": chunks of 512 tokens, 64
+# while decodes are running)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class PrefillWorkload:
+    name: str
+    layers: int
+    batch: int
+    n_qo_heads: int
+    n_kv_heads: int
+    head_dim: int
+    pool_slots: int
+    sm_scale: float
+    k_scale: float
+    seed: int
+    chunks: np.ndarray         # [batch] int64, query tokens of each chunk
+    contexts: np.ndarray       # [batch] int64, listed slots incl. the chunk's own
+    qo_indptr: np.ndarray      # [batch + 1] int32
+    kv_indptr: np.ndarray      # [batch + 1] int32
+    kv_indices: np.ndarray     # [N] int32
+    chunk_slots: np.ndarray    # [qo_indptr[-1]] int32: the slot of every chunk token
+    description: str = ""
+
+    @property
+    def total_q(self) -> int:
+        return int(self.qo_indptr[-1])
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.kv_indptr[-1])
+
+    def attended_pairs(self) -> int:
+        """Sum over chunk tokens of the list entries each attends (causal)."""
+        c, l = self.chunks.astype(np.int64), self.contexts.astype(np.int64)
+        return int(np.sum(c * (l - c) + c * (c + 1) // 2))
+
+
+def prefill_workload(chunks, contexts, *, n_qo_heads=32, n_kv_heads=8, head_dim=128,
+                     pool_slots=None, layers=1, k_scale=1.0, seed=0, name="prefill",
+                     description="") -> PrefillWorkload:
+    """Requests whose newest chunks[b] tokens are a prefill chunk: each lists
+    contexts[b] >= chunks[b] scattered slots, the chunk's slots last."""
+    chunks = np.asarray([int(x) for x in chunks], dtype=np.int64)
+    contexts = np.asarray([int(x) for x in contexts], dtype=np.int64)
+    assert chunks.size == contexts.size and np.all((0 <= chunks) & (chunks <= contexts))
+    need = int(contexts.sum())
+    if pool_slots is None:
+        pool_slots = max(16, 2 * need)
+    if need > pool_slots:
+        raise ValueError("pool too small for the requested contexts")
+    rng = np.random.default_rng(seed)
+    perm = rng.permutation(pool_slots)
+    lists, off = [], 0
+    for L in contexts:
+        lists.append(perm[off:off + L])
+        off += int(L)
+    kv_indptr = np.zeros(chunks.size + 1, dtype=np.int64)
+    kv_indptr[1:] = np.cumsum(contexts)
+    qo_indptr = np.zeros(chunks.size + 1, dtype=np.int64)
+    qo_indptr[1:] = np.cumsum(chunks)
+    if kv_indptr[-1] >= 2**31:
+        raise ValueError("total context exceeds int32 CSR range")
+    indices = (np.concatenate(lists) if lists else np.zeros(0)).astype(np.int32)
+    chunk_slots = (np.concatenate([lst[len(lst) - c:] for lst, c in zip(lists, chunks)])
+                   if lists else np.zeros(0)).astype(np.int32)
+    return PrefillWorkload(name=name, layers=layers, batch=int(chunks.size),
+                           n_qo_heads=n_qo_heads, n_kv_heads=n_kv_heads, head_dim=head_dim,
+                           pool_slots=pool_slots, sm_scale=_sm_scale(head_dim), k_scale=k_scale,
+                           seed=seed, chunks=chunks, contexts=contexts,
+                           qo_indptr=qo_indptr.astype(np.int32),
+                           kv_indptr=kv_indptr.astype(np.int32), kv_indices=indices,
+                           chunk_slots=chunk_slots, description=description)
+
+
+PREFILL_DESCRIPTIONS = {
+    1: "chunked prefill, Qwen3-4B shape: 36 layers, 4 requests x 512-token chunks at "
+       "contexts U[512,8192], 32Q/8KV, head_dim 128, 65536-slot pools",
+    2: "chunked prefill beside decodes: 36 layers, 8 requests x 64-token chunks at contexts "
+       "U[64,16384], 32Q/8KV, head_dim 128, 2^18-slot pools",
+    3: "chunked prefill, hybrid full-attention layers: 8 layers, 4 requests x 512-token chunks "
+       "at contexts U[512,32768], 16Q/4KV, head_dim 256, K scaled 0.5, 2^18-slot pools",
+}
+
+
+def prefill_config(no: int) -> PrefillWorkload:
+    """The chunked-prefill workloads (seed 2000 + no)."""
+    seed = 2000 + no
+    rng = np.random.default_rng(seed)
+    desc = PREFILL_DESCRIPTIONS[no]
+    if no == 1:
+        ctx = rng.integers(512, 8192, size=4, endpoint=True)
+        return prefill_workload([512] * 4, ctx, pool_slots=65536, layers=36, seed=seed,
+                                name="pf1", description=desc)
+    if no == 2:
+        ctx = rng.integers(64, 16384, size=8, endpoint=True)
+        return prefill_workload([64] * 8, ctx, pool_slots=1 << 18, layers=36, seed=seed,
+                                name="pf2", description=desc)
+    if no == 3:
+        ctx = rng.integers(512, 32768, size=4, endpoint=True)
+        return prefill_workload([512] * 4, ctx, n_qo_heads=16, n_kv_heads=4, head_dim=256,
+                                pool_slots=1 << 18, layers=8, k_scale=0.5, seed=seed,
+                                name="pf3", description=desc)
+    raise ValueError(f"unknown prefill config {no}")
+
+
+def prefill_tensors(pw: PrefillWorkload, layer: int, device="cpu", poison_unreferenced=False):
+    """Seeded tensors of one layer: (q [NQ, Hq, D], k_pool, v_pool before the chunk's
+    append, k_new, v_new [NQ, Hkv, D] the chunk's rows). With ``poison_unreferenced``
+    unlisted slots and the chunk's own slots (before the append) hold bf16 NaN."""
+    device = torch.device(device)
+    gen = _gen(device, pw.seed * 1000 + layer)
+    NQ, Hq, Hkv, D, S = pw.total_q, pw.n_qo_heads, pw.n_kv_heads, pw.head_dim, pw.pool_slots
+    q = torch.empty(NQ, Hq, D, dtype=torch.bfloat16, device=device)
+    _fill_normal_bf16(q, gen)
+    k_new = torch.empty(NQ, Hkv, D, dtype=torch.bfloat16, device=device)
+    v_new = torch.empty(NQ, Hkv, D, dtype=torch.bfloat16, device=device)
+    _fill_normal_bf16(k_new, gen, pw.k_scale)
+    _fill_normal_bf16(v_new, gen)
+    k_pool = torch.empty(S, Hkv, D, dtype=torch.bfloat16, device=device)
+    v_pool = torch.empty(S, Hkv, D, dtype=torch.bfloat16, device=device)
+    _fill_normal_bf16(k_pool, gen, pw.k_scale)
+    _fill_normal_bf16(v_pool, gen)
+    if poison_unreferenced:
+        keep = torch.zeros(S, dtype=torch.bool, device=device)
+        keep[torch.as_tensor(pw.kv_indices, dtype=torch.int64, device=device)] = True
+        keep[torch.as_tensor(pw.chunk_slots, dtype=torch.int64, device=device)] = False
+        nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16, device=device)
+        k_pool.view(torch.int16)[~keep] = nan
+        v_pool.view(torch.int16)[~keep] = nan
+    return q, k_pool, v_pool, k_new, v_new
