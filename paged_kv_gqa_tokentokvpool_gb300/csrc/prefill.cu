@@ -16,7 +16,8 @@
 //  * One CTA per work unit (request, KV head, tile of 64 / G chunk tokens): its 64
 //    query rows (token, head) are four 16-row warp tiles. The plan orders units
 //    longest causal range first, so the grid drains evenly.
-//  * The unit's q rows are staged once in shared memory; the request's slot rows
+//  * The unit's q rows are staged once in shared memory and then held as mma
+//    fragments in registers for the whole unit; the request's slot rows
 //    of that KV head stream through a ring of 32-token K/V tiles gathered with
 //    16-byte cp.async (each thread copies whole 16-byte pieces of scattered pool
 //    rows; a stage's slot ids are loaded one iteration ahead of its copies).
@@ -233,6 +234,8 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
     const uint32_t k_off = ((8 * (mi >> 1) + (lane & 7)) * C::kPitch + 8 * (mi & 1)) * 2;
     const uint32_t v_off = ((8 * (mi & 1) + (lane & 7)) * C::kPitch + 8 * (mi >> 1)) * 2;
 
+    uint32_t qf[C::kKSteps][4];  // this warp's q rows as A fragments, loaded once
+    bool q_loaded = false;
     for (int n = 0; n < n_tiles; ++n) {
         // copies of tile n + kStages - 1 (slot ids loaded last iteration), then the
         // slot ids of the tile after it
@@ -242,6 +245,11 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
         if (ahead + 1 < n_tiles) load_tile_slots<D, G>(a, un, ahead + 1, slot);
         cp_wait<C::kStages - 1>();  // tile n (and q) have landed for this thread
         __syncthreads();            // ... and for every thread
+        if (!q_loaded) {
+#pragma unroll
+            for (int ks = 0; ks < C::kKSteps; ++ks) ldsm4(q_addr + ks * 32, qf[ks]);
+            q_loaded = true;
+        }
 
         const int st = n % C::kStages;
         const uint32_t sk = smem_addr(smem) + C::kQBytes + st * C::kStageBytes;
@@ -252,14 +260,12 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
         for (int nt = 0; nt < C::kNT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < C::kKSteps; ++ks) {
-            uint32_t qa[4];
-            ldsm4(q_addr + ks * 32, qa);
 #pragma unroll
             for (int np = 0; np < C::kNT / 2; ++np) {
                 uint32_t kb[4];
                 ldsm4(sk + k_off + (16 * np * C::kPitch + 16 * ks) * 2, kb);
-                mma16816(s[2 * np], qa, kb[0], kb[1]);
-                mma16816(s[2 * np + 1], qa, kb[2], kb[3]);
+                mma16816(s[2 * np], qf[ks], kb[0], kb[1]);
+                mma16816(s[2 * np + 1], qf[ks], kb[2], kb[3]);
             }
         }
         // causal mask and online softmax (base 2); token j of the tile is list
