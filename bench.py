@@ -512,6 +512,7 @@ def run_prefill_bench(args):
     attn_ms = float(np.mean([a.elapsed_time(b) for a, b in events]))
     peak, peak_kind = measured_tensor_peak()
     step_tflops = flops_layer * pw.layers / (ms * 1e-3) / 1e12
+    cpu = None if args.no_cpu_baseline else prefill_cpu_baseline(pw, args.cpu_budget)
     attn_tflops = flops_layer / (attn_ms * 1e-3) / 1e12
     print(json.dumps({
         "metric": "chunked-prefill attention over the token pool: useful causal TFLOP/s",
@@ -529,8 +530,38 @@ def run_prefill_bench(args):
                                f"calls {attn_ms * 1e3:.1f} us, mma.sync m16n8k16",
                      "peak_kind": peak_kind},
         "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
     }), flush=True)
     return 0
+
+
+def prefill_cpu_baseline(pw: workloads.PrefillWorkload, budget_s: float):
+    """The fp64 oracle on the host cores over a bounded sample of the same step:
+    whole requests of layer 0, one at a time, until about budget_s seconds."""
+    import oracle
+    orc = oracle.default()
+    q, kp, vp, kn, vn = workloads.prefill_tensors(pw, 0, device="cpu")
+    kb = orc.append(workloads.bf16_bits(kp), pw.chunk_slots, workloads.bf16_bits(kn))
+    vb = orc.append(workloads.bf16_bits(vp), pw.chunk_slots, workloads.bf16_bits(vn))
+    qb = workloads.bf16_bits(q)
+    flops = 0.0
+    done = 0
+    t0 = time.perf_counter()
+    for b in np.argsort(pw.contexts):  # shortest first, so the sample is not empty
+        C, L = int(pw.chunks[b]), int(pw.contexts[b])
+        q0, k0 = int(pw.qo_indptr[b]), int(pw.kv_indptr[b])
+        orc.prefill(qb[q0:q0 + C], kb, vb, np.array([0, C], np.int32),
+                    np.array([0, L], np.int32), pw.kv_indices[k0:k0 + L], pw.n_qo_heads,
+                    pw.n_kv_heads, pw.head_dim, pw.sm_scale)
+        flops += 4.0 * pw.head_dim * pw.n_qo_heads * (C * (L - C) + C * (C + 1) // 2)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": orc.max_threads(),
+            "kind": "oracle",
+            "sample": f"{done} of {pw.batch} requests of layer 0 (shortest first), fp64 C++ "
+                      f"oracle, {el:.1f} s"}
 
 
 def _dist():

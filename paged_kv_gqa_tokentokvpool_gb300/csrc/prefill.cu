@@ -52,13 +52,24 @@ constexpr unsigned kFullMask = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// One work unit: query tokens q_row0 .. q_row0 + n_q - 1 (rows of q/out) of request
-// b, KV head g; the request's slot list starts at kv_begin, the unit's first query
-// sits at list position pos0, and its queries together see entries 0 .. n_kv - 1.
+// One work unit: query tokens q_row0 .. q_row0 + n_q - 1 (rows of q/out) of one
+// request, KV head g, over list entries kv_lo .. kv_hi - 1 of the request's slot
+// list (which starts at kv_begin in kv_indices). The unit's first query sits at list
+// position pos0. part < 0: the unit covers every entry its queries see and writes
+// out/lse; otherwise it is one piece of a split range, kv_lo <= pos0 and kv_lo a
+// multiple of the ring tile, and writes its 64 rows' normalised fp32 output and
+// base-2 lse to workspace block `part`.
 struct PfUnit {
-    int32_t b, g, q_row0, n_q, kv_begin, pos0, n_kv, pad;
+    int32_t part, g, q_row0, n_q, kv_begin, pos0, kv_lo, kv_hi;
 };
 static_assert(sizeof(PfUnit) == 32, "unit record");
+
+// The pieces of one split unit: workspace blocks first .. first + count - 1, for
+// query tokens q_row0 .. q_row0 + n_q - 1 and KV head g.
+struct PfMerge {
+    int32_t q_row0, n_q, g, first, count, pad0, pad1, pad2;
+};
+static_assert(sizeof(PfMerge) == 32, "merge record");
 
 struct PfArgs {
     const void* q;
@@ -71,6 +82,10 @@ struct PfArgs {
     float scale_log2;  // sm_scale * log2(e)
     void* out;
     float* lse;
+    float* ws_o;       // [blocks, 64, head_dim] partial outputs of split units
+    float* ws_lse;     // [blocks, 64] their base-2 lse
+    const PfMerge* merges;
+    int n_merges;
 };
 
 template <int D, int G>
@@ -156,7 +171,7 @@ __device__ __forceinline__ void load_tile_slots(const PfArgs& a, const PfUnit& u
     for (int i = 0; i < C::kPieces; ++i) {
         const int tok = (threadIdx.x + i * kPfThreads) / C::kChunks;
         const int j = tile * kPfKvTile + tok;
-        slot[i] = j < un.n_kv ? __ldg(a.kv_indices + un.kv_begin + j) : -1;
+        slot[i] = j < un.kv_hi ? __ldg(a.kv_indices + un.kv_begin + j) : -1;
     }
 }
 
@@ -205,18 +220,20 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
             cp_async16(smem_addr(smem + (r * C::kPitch + part * 8) * 2), q + off, valid);
         }
     }
-    // ---- ring prologue: tiles 0 .. kStages - 2, and the slot ids of the next one
-    const int n_tiles = (un.n_kv + kPfKvTile - 1) / kPfKvTile;
+    // ---- ring prologue: the range's tiles 0 .. kStages - 2, and the slot ids of the
+    // next one (ring index i holds list tile t0 + i)
+    const int t0 = un.kv_lo / kPfKvTile;
+    const int n_tiles = (un.kv_hi + kPfKvTile - 1) / kPfKvTile - t0;
     int slot[C::kPieces];
 #pragma unroll
     for (int s = 0; s < C::kStages - 1; ++s) {
         if (s < n_tiles) {
-            load_tile_slots<D, G>(a, un, s, slot);
+            load_tile_slots<D, G>(a, un, t0 + s, slot);
             issue_tile<D, G>(a, un, smem, s, slot);
         }
         cp_commit();  // one group per tile (the first also holds q)
     }
-    if (C::kStages - 1 < n_tiles) load_tile_slots<D, G>(a, un, C::kStages - 1, slot);
+    if (C::kStages - 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + C::kStages - 1, slot);
 
     // per lane: rows lo = 16 warp + g8 and hi = lo + 8 of the unit's 64
     const int r_lo = 16 * warp + g8, r_hi = r_lo + 8;
@@ -242,7 +259,7 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
         const int ahead = n + C::kStages - 1;
         if (ahead < n_tiles) issue_tile<D, G>(a, un, smem, ahead % C::kStages, slot);
         cp_commit();
-        if (ahead + 1 < n_tiles) load_tile_slots<D, G>(a, un, ahead + 1, slot);
+        if (ahead + 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + ahead + 1, slot);
         cp_wait<C::kStages - 1>();  // tile n (and q) have landed for this thread
         __syncthreads();            // ... and for every thread
         if (!q_loaded) {
@@ -269,8 +286,8 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
             }
         }
         // causal mask and online softmax (base 2); token j of the tile is list
-        // position n * 32 + 8 nt + 2 t4 (+1); c[0..1] are row lo, c[2..3] row hi
-        const int j0 = n * kPfKvTile + 2 * t4;
+        // position (t0 + n) * 32 + 8 nt + 2 t4 (+1); c[0..1] are row lo, c[2..3] row hi
+        const int j0 = (t0 + n) * kPfKvTile + 2 * t4;
         float mx_lo = minus_inf(), mx_hi = minus_inf();
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) {
@@ -287,7 +304,8 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
             mx_lo = fmaxf(mx_lo, __shfl_xor_sync(kFullMask, mx_lo, off));
             mx_hi = fmaxf(mx_hi, __shfl_xor_sync(kFullMask, mx_hi, off));
         }
-        // every row sees list entry 0 in tile 0, so the maxima are finite from then on
+        // every row sees the range's first entry (kv_lo <= pos0), so the maxima are
+        // finite from the range's first tile on
         const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
         const float al_lo = exp2_approx(m_lo - mn_lo), al_hi = exp2_approx(m_hi - mn_hi);
         m_lo = mn_lo;
@@ -342,51 +360,162 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
         if (t >= un.n_q) continue;
         const float lt = half ? l_hi : l_lo;
         const float inv = 1.f / lt;
+        const float lse2 = (half ? m_hi : m_lo) + __log2f(lt);
+        if (un.part >= 0) {  // a piece of a split range: fp32 partial result
+            const int64_t wrow = int64_t(un.part) * kPfRows + r;
+            float* dst = a.ws_o + wrow * D + 2 * t4;
+#pragma unroll
+            for (int dt = 0; dt < C::kDT; ++dt)
+                *reinterpret_cast<float2*>(dst + 8 * dt) =
+                    make_float2(o[dt][2 * half] * inv, o[dt][2 * half + 1] * inv);
+            if (t4 == 0) a.ws_lse[wrow] = lse2;
+            continue;
+        }
         const int64_t row = int64_t(un.q_row0 + t) * a.n_qo_heads + un.g * G + h;
         __nv_bfloat16* dst = out + row * D + 2 * t4;
 #pragma unroll
         for (int dt = 0; dt < C::kDT; ++dt)
             *reinterpret_cast<uint32_t*>(dst + 8 * dt) =
                 pack2(o[dt][2 * half] * inv, o[dt][2 * half + 1] * inv);
-        if (a.lse != nullptr && t4 == 0) a.lse[row] = ((half ? m_hi : m_lo) + __log2f(lt)) * kLn2;
+        if (a.lse != nullptr && t4 == 0) a.lse[row] = lse2 * kLn2;
     }
 }
 
+// Log-sum-exp merge of split units: one warp per (merge record, row of its 64),
+// lanes over head_dim, every piece's loads issued before any is used:
+//     lse = log2 sum_c 2^lse_c,   out = sum_c 2^(lse_c - lse) out_c
+constexpr int kPfMergeWarps = 4;
+constexpr int kPfMaxPieces = 16;  // pieces per split unit (the planner's cap)
+
 template <int D, int G>
-cudaError_t launch_prefill(const PfArgs& a, int n_units, cudaStream_t stream) {
-    using C = PfCfg<D, G>;
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        paged_prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (attr != cudaSuccess) return attr;
-    if (n_units == 0) return cudaSuccess;
+__global__ void __launch_bounds__(32 * kPfMergeWarps) prefill_merge_kernel(const PfArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    constexpr int kVD = D / 32;  // dims per lane
+    const int lane = threadIdx.x & 31;
+    const int w = blockIdx.x * kPfMergeWarps + (threadIdx.x >> 5);
+    if (w >= a.n_merges * kPfRows) return;
+    const PfMerge mg = a.merges[w / kPfRows];  // plan data
+    const int r = w % kPfRows, t = r / G, h = r % G;
+    if (t >= mg.n_q) return;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the pieces come from the kernel before
+    float x[kPfMaxPieces][kVD], xl[kPfMaxPieces];
+#pragma unroll
+    for (int c = 0; c < kPfMaxPieces; ++c) {
+        if (c < mg.count) {
+            const int64_t wrow = int64_t(mg.first + c) * kPfRows + r;
+            xl[c] = __ldcg(a.ws_lse + wrow);
+#pragma unroll
+            for (int i = 0; i < kVD; i += 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_o + wrow * D + lane * kVD + i));
+                x[c][i] = v.x;
+                x[c][i + 1] = v.y;
+                x[c][i + 2] = v.z;
+                x[c][i + 3] = v.w;
+            }
+        }
+    }
+    float mx = minus_inf();
+#pragma unroll
+    for (int c = 0; c < kPfMaxPieces; ++c)
+        if (c < mg.count) mx = fmaxf(mx, xl[c]);
+    float sum = 0.f, acc[kVD];
+#pragma unroll
+    for (int i = 0; i < kVD; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < kPfMaxPieces; ++c) {
+        if (c < mg.count) {
+            const float wgt = exp2_approx(xl[c] - mx);
+            sum += wgt;
+#pragma unroll
+            for (int i = 0; i < kVD; ++i) acc[i] = fmaf(wgt, x[c][i], acc[i]);
+        }
+    }
+    const float inv = 1.f / sum;
+    const int64_t row = int64_t(mg.q_row0 + t) * a.n_qo_heads + mg.g * G + h;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + row * D + lane * kVD;
+#pragma unroll
+    for (int i = 0; i < kVD; i += 2)
+        *reinterpret_cast<uint32_t*>(dst + i) = pack2(acc[i] * inv, acc[i + 1] * inv);
+    if (a.lse != nullptr && lane == 0) a.lse[row] = (mx + __log2f(sum)) * kLn2;
+}
+
+template <int D, int G>
+cudaError_t prefill_prepare() {
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(paged_prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PfCfg<D, G>::kSmem);
+    return attr;
+}
+
+// Resident CTAs per SM of the prefill kernel (0 on error).
+template <int D, int G>
+int prefill_occupancy() {
+    if (prefill_prepare<D, G>() != cudaSuccess) return 0;
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_prefill_kernel<D, G>,
+                                                      kPfThreads, PfCfg<D, G>::kSmem) != cudaSuccess)
+        return 0;
+    return blocks;
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, const PfArgs& a,
+                       cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_units);
-    cfg.blockDim = dim3(kPfThreads);
-    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, G>, a);
+    void* args[] = {const_cast<PfArgs*>(&a)};
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-cudaError_t launch_prefill_any(const PfArgs& a, int head_dim, int group, int n_units,
-                               cudaStream_t stream) {
-#define PKV_PF(D_)                                                  \
-    switch (group) {                                                \
-        case 1: return launch_prefill<D_, 1>(a, n_units, stream);   \
-        case 2: return launch_prefill<D_, 2>(a, n_units, stream);   \
-        case 4: return launch_prefill<D_, 4>(a, n_units, stream);   \
-        case 8: return launch_prefill<D_, 8>(a, n_units, stream);   \
-        default: break;                                             \
+template <int D, int G>
+cudaError_t launch_prefill(const PfArgs& a, int n_units, cudaStream_t stream) {
+    cudaError_t e = prefill_prepare<D, G>();
+    if (e != cudaSuccess || n_units == 0) return e;
+    e = launch_pdl(reinterpret_cast<const void*>(&paged_prefill_kernel<D, G>), dim3(n_units),
+                   dim3(kPfThreads), PfCfg<D, G>::kSmem, a, stream);
+    if (e != cudaSuccess || a.n_merges == 0) return e;
+    const int warps = a.n_merges * kPfRows;
+    return launch_pdl(reinterpret_cast<const void*>(&prefill_merge_kernel<D, G>),
+                      dim3((warps + kPfMergeWarps - 1) / kPfMergeWarps), dim3(32 * kPfMergeWarps),
+                      0, a, stream);
+}
+
+// Calls FN<D, G>::run(args...) for the runtime shape.
+template <template <int, int> class FN, typename... Args>
+auto prefill_dispatch(int head_dim, int group, Args&&... args) -> decltype(FN<128, 1>::run(args...)) {
+#define PKV_PF(D_)                                          \
+    switch (group) {                                        \
+        case 1: return FN<D_, 1>::run(args...);             \
+        case 2: return FN<D_, 2>::run(args...);             \
+        case 4: return FN<D_, 4>::run(args...);             \
+        case 8: return FN<D_, 8>::run(args...);             \
+        default: break;                                     \
     }
     if (head_dim == 128) { PKV_PF(128) }
     if (head_dim == 256) { PKV_PF(256) }
 #undef PKV_PF
-    return cudaErrorInvalidValue;
+    return FN<128, 1>::unsupported();
 }
+
+template <int D, int G>
+struct PfLaunchFn {
+    static cudaError_t run(const PfArgs& a, int n_units, cudaStream_t s) {
+        return launch_prefill<D, G>(a, n_units, s);
+    }
+    static cudaError_t unsupported() { return cudaErrorInvalidValue; }
+};
+template <int D, int G>
+struct PfOccupancyFn {
+    static int run() { return prefill_occupancy<D, G>(); }
+    static int unsupported() { return 0; }
+};
 
 bool prefill_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim) {
     if (n_kv_heads <= 0 || n_qo_heads <= 0 || n_qo_heads % n_kv_heads != 0) return false;
@@ -407,9 +536,17 @@ struct pkv_prefill_plan {
     int64_t max_q_tokens = 0;
     int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0;
     int tile_tokens = 0;  // query tokens per unit: 64 / G
-    int max_units = 0;
+    int max_units = 0;    // capacity of the unit list (tiles plus split pieces)
+    int split_target = 0; // a step with fewer tile units than this splits long ranges
+    int max_blocks = 0;   // workspace blocks of 64 rows (pieces of split units)
+    int max_merges = 0;
     pkv::PfUnit* host_units = nullptr;  // pinned staging
     pkv::PfUnit* dev_units = nullptr;
+    pkv::PfMerge* host_merges = nullptr;
+    pkv::PfMerge* dev_merges = nullptr;
+    float* ws_o = nullptr;
+    float* ws_lse = nullptr;
+    int n_merges = 0;
     cudaEvent_t copy_done = nullptr;
     bool copy_pending = false;
     bool planned = false;
@@ -448,14 +585,34 @@ int paged_prefill_plan_create(pkv_prefill_plan** out_plan, int max_batch, int64_
     p->n_kv_heads = n_kv_heads;
     p->head_dim = head_dim;
     p->tile_tokens = kPfRows / (n_qo_heads / n_kv_heads);
-    const int64_t units = (max_q_tokens / p->tile_tokens + max_batch) * int64_t(n_kv_heads);
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    const int per_sm = prefill_dispatch<PfOccupancyFn>(head_dim, n_qo_heads / n_kv_heads);
+    if (e != cudaSuccess || per_sm <= 0) {
+        delete p;
+        return fail(PKV_ERR_CUDA, "paged_prefill_plan_create: device or occupancy query failed");
+    }
+    // Steps with fewer tile units than two waves of the grid split long causal
+    // ranges into pieces; a split step has at most 2 x target pieces.
+    p->split_target = 2 * sms * per_sm;
+    p->max_merges = p->split_target;
+    p->max_blocks = 2 * p->split_target;
+    const int64_t units = (max_q_tokens / p->tile_tokens + max_batch) * int64_t(n_kv_heads) +
+                          p->max_blocks;
     if (units > INT32_MAX / 2) {
         delete p;
         return fail(PKV_ERR_INVALID_ARG, "paged_prefill_plan_create: too many work units");
     }
     p->max_units = static_cast<int>(units);
+    const size_t rows = size_t(p->max_blocks) * kPfRows;
     e = cudaMallocHost(reinterpret_cast<void**>(&p->host_units), sizeof(PfUnit) * size_t(units));
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->dev_units), sizeof(PfUnit) * size_t(units));
+    if (e == cudaSuccess)
+        e = cudaMallocHost(reinterpret_cast<void**>(&p->host_merges), sizeof(PfMerge) * size_t(p->max_merges));
+    if (e == cudaSuccess)
+        e = cudaMalloc(reinterpret_cast<void**>(&p->dev_merges), sizeof(PfMerge) * size_t(p->max_merges));
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_o), sizeof(float) * rows * head_dim);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_lse), sizeof(float) * rows);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->copy_done, cudaEventDisableTiming);
     if (e != cudaSuccess) {
         paged_prefill_plan_destroy(p);
@@ -476,6 +633,10 @@ void paged_prefill_plan_destroy(pkv_prefill_plan* p) {
     }
     if (p->host_units) cudaFreeHost(p->host_units);
     if (p->dev_units) cudaFree(p->dev_units);
+    if (p->host_merges) cudaFreeHost(p->host_merges);
+    if (p->dev_merges) cudaFree(p->dev_merges);
+    if (p->ws_o) cudaFree(p->ws_o);
+    if (p->ws_lse) cudaFree(p->ws_lse);
     if (prev >= 0) cudaSetDevice(prev);
     delete p;
 }
@@ -510,7 +671,10 @@ int paged_prefill_plan(pkv_prefill_plan* p, const int32_t* qo_indptr_host,
         if (e != cudaSuccess) return pf_cuda_fail(e, "waiting for the previous prefill plan copy");
         p->copy_pending = false;
     }
-    int n = 0;
+    // 1. one unit per (request, tile of chunk tokens, KV head), over every list
+    //    entry its queries see
+    std::vector<PfUnit> tiles;
+    int64_t total_tiles = 0;
     for (int b = 0; b < batch; ++b) {
         const int C = qo_indptr_host[b + 1] - qo_indptr_host[b];
         const int L = kv_indptr_host[b + 1] - kv_indptr_host[b];
@@ -518,26 +682,64 @@ int paged_prefill_plan(pkv_prefill_plan* p, const int32_t* qo_indptr_host,
             const int n_q = std::min(p->tile_tokens, C - t0);
             const int pos0 = L - C + t0;
             for (int g = 0; g < p->n_kv_heads; ++g) {
-                if (n >= p->max_units)
-                    return fail(PKV_ERR_PLAN, "%s: more work units than the plan holds (%d)", who,
-                                p->max_units);
-                p->host_units[n++] = PfUnit{b, g, qo_indptr_host[b] + t0, n_q,
-                                            kv_indptr_host[b], pos0, pos0 + n_q, 0};
+                tiles.push_back(PfUnit{-1, g, qo_indptr_host[b] + t0, n_q, kv_indptr_host[b],
+                                       pos0, 0, pos0 + n_q});
+                total_tiles += (pos0 + n_q + kPfKvTile - 1) / kPfKvTile;
             }
         }
     }
-    // longest causal range first: the grid's last CTAs are the short ones
-    std::stable_sort(p->host_units, p->host_units + n,
-                     [](const PfUnit& x, const PfUnit& y) { return x.n_kv > y.n_kv; });
+    // 2. Too few units for two waves of the grid: cut each long range at ring-tile
+    //    boundaries below its first query's position (every query then sees every
+    //    entry of every piece but the last), into pieces of about equal length;
+    //    each piece writes a partial result that the merge kernel combines.
+    int n = 0, n_blocks = 0, n_merges = 0;
+    const bool split = int64_t(tiles.size()) < p->split_target && total_tiles > 0;
+    const int64_t piece_tiles =
+        std::max<int64_t>(8, (total_tiles + p->split_target - 1) / p->split_target);
+    for (const PfUnit& u : tiles) {
+        int cuts = 0;  // split points at multiples of step * kPfKvTile, all <= pos0
+        int64_t step = piece_tiles;
+        if (split) {
+            cuts = static_cast<int>(u.pos0 / (step * kPfKvTile));
+            if (cuts > kPfMaxPieces - 1) {
+                step = (u.pos0 / kPfKvTile + kPfMaxPieces - 1) / (kPfMaxPieces - 1);
+                cuts = static_cast<int>(u.pos0 / (step * kPfKvTile));
+                cuts = std::min(cuts, kPfMaxPieces - 1);
+            }
+        }
+        if (n + cuts + 1 > p->max_units || n_blocks + (cuts ? cuts + 1 : 0) > p->max_blocks ||
+            (cuts && n_merges >= p->max_merges))
+            return fail(PKV_ERR_PLAN, "%s: more work than the plan holds", who);
+        if (cuts == 0) {
+            p->host_units[n++] = u;
+            continue;
+        }
+        p->host_merges[n_merges++] = PfMerge{u.q_row0, u.n_q, u.g, n_blocks, cuts + 1, 0, 0, 0};
+        for (int c = 0; c <= cuts; ++c) {
+            PfUnit piece = u;
+            piece.part = n_blocks++;
+            piece.kv_lo = static_cast<int32_t>(c * step * kPfKvTile);
+            piece.kv_hi = c == cuts ? u.kv_hi : static_cast<int32_t>((c + 1) * step * kPfKvTile);
+            p->host_units[n++] = piece;
+        }
+    }
+    // 3. longest range first: the grid's last CTAs are the short ones
+    std::stable_sort(p->host_units, p->host_units + n, [](const PfUnit& x, const PfUnit& y) {
+        return x.kv_hi - x.kv_lo > y.kv_hi - y.kv_lo;
+    });
     if (n > 0) {
         cudaError_t e = cudaMemcpyAsync(p->dev_units, p->host_units, sizeof(PfUnit) * size_t(n),
                                         cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess && n_merges > 0)
+            e = cudaMemcpyAsync(p->dev_merges, p->host_merges, sizeof(PfMerge) * size_t(n_merges),
+                                cudaMemcpyHostToDevice, stream);
         if (e == cudaSuccess) e = cudaEventRecord(p->copy_done, stream);
         if (e != cudaSuccess) return pf_cuda_fail(e, "prefill plan upload");
         p->copy_pending = true;
     }
     p->batch = batch;
     p->n_units = n;
+    p->n_merges = n_merges;
     p->qo_host.assign(qo_indptr_host, qo_indptr_host + batch + 1);
     p->kv_host.assign(kv_indptr_host, kv_indptr_host + batch + 1);
     p->planned = true;
@@ -586,8 +788,12 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
     a.scale_log2 = sm_scale * kLog2e;
     a.out = out;
     a.lse = lse;
-    const cudaError_t e =
-        launch_prefill_any(a, head_dim, n_qo_heads / n_kv_heads, p->n_units, stream);
+    a.ws_o = p->ws_o;
+    a.ws_lse = p->ws_lse;
+    a.merges = p->dev_merges;
+    a.n_merges = p->n_merges;
+    const cudaError_t e = prefill_dispatch<PfLaunchFn>(head_dim, n_qo_heads / n_kv_heads, a,
+                                                       p->n_units, stream);
     if (e != cudaSuccess) return pf_cuda_fail(e, "paged_prefill_attn: launch");
     return PKV_OK;
 }
