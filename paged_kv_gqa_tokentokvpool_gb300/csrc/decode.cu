@@ -728,7 +728,7 @@ __device__ __forceinline__ void merge_load_chunk(const DecodeArgs& a, const int3
 }
 
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads, 4) lse_merge_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kMergeThreads, 2) lse_merge_kernel(const DecodeArgs a) {
     pdl_launch_dependents();
     constexpr int kVD = D / 32;  // dims per lane
     const int lane = threadIdx.x & 31;
@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) lse_merge_kernel(const Decod
     // Parts in chunks of kChunk: every load of a chunk is issued before the first
     // use, so a chunk costs one round trip to L2; the first chunk's outputs are
     // issued together with the log-sum-exp pass, which does not need them.
-    constexpr int kChunk = kVD == 4 ? 16 : 8;
+    constexpr int kChunk = kVD == 4 ? 32 : 16;
     for (; w < items; w += warps) {
         const int qh = w % qheads;
         const int32_t* parts = a.part_list + mg.first;
