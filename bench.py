@@ -53,19 +53,32 @@ class StepState:
         self.wl = wl
         self.device = torch.device(device)
         self.layer_ids = list(range(wl.layers)) if layers is None else list(layers)
-        self.q, self.k_pool, self.v_pool, self.k_new, self.v_new = [], [], [], [], []
-        for l in self.layer_ids:
+        # Every layer's q, new rows, out and lse live in one stacked buffer each
+        # (the per-layer tensors are views), so a step's host transfers are a few
+        # large copies; the pools are separate allocations per layer.
+        B, Hq, Hkv, D = wl.batch, wl.n_qo_heads, wl.n_kv_heads, wl.head_dim
+        n = len(self.layer_ids)
+        n_app = len(wl.append_slots)
+        bf16 = dict(dtype=torch.bfloat16, device=self.device)
+        self.q_all = torch.empty(n, B, Hq, D, **bf16)
+        self.k_new_all = torch.empty(n, n_app, Hkv, D, **bf16)
+        self.v_new_all = torch.empty(n, n_app, Hkv, D, **bf16)
+        self.out_all = torch.empty(n, B, Hq, D, **bf16)
+        self.lse_all = torch.empty(n, B, Hq, dtype=torch.float32, device=self.device)
+        self.k_pool, self.v_pool = [], []
+        for i, l in enumerate(self.layer_ids):
             t = workloads.layer_tensors(wl, l, device=self.device,
                                         poison_unreferenced=poison_unreferenced)
-            self.q.append(t.q)
+            self.q_all[i].copy_(t.q)
+            self.k_new_all[i].copy_(t.k_new)
+            self.v_new_all[i].copy_(t.v_new)
             self.k_pool.append(t.k_pool)
             self.v_pool.append(t.v_pool)
-            self.k_new.append(t.k_new)
-            self.v_new.append(t.v_new)
-        B, Hq, D = wl.batch, wl.n_qo_heads, wl.head_dim
-        n = len(self.layer_ids)
-        self.out = [torch.empty(B, Hq, D, dtype=torch.bfloat16, device=self.device) for _ in range(n)]
-        self.lse = [torch.empty(B, Hq, dtype=torch.float32, device=self.device) for _ in range(n)]
+        self.q = list(self.q_all.unbind(0))
+        self.k_new = list(self.k_new_all.unbind(0))
+        self.v_new = list(self.v_new_all.unbind(0))
+        self.out = list(self.out_all.unbind(0))
+        self.lse = list(self.lse_all.unbind(0))
         self.kv_indptr_host = torch.from_numpy(wl.kv_indptr.copy())
         self.kv_indptr = self.kv_indptr_host.to(self.device)
         self.kv_indices = torch.from_numpy(wl.kv_indices.copy()).to(self.device)
@@ -164,40 +177,26 @@ class StepState:
 class HostIO:
     """Pinned host copies of one step's inputs and outputs, for the end-to-end
     measurement: every step copies q, the new K/V rows and the slot/index arrays
-    host->device, runs the step, and copies out and lse device->host."""
+    host->device, runs the step, and copies out and lse device->host. Each stacked
+    array (all layers) is one copy."""
 
     def __init__(self, st: StepState):
         self.st = st
-        pin = dict(pin_memory=True)
-        self.q = [t.cpu().pin_memory() for t in st.q]
-        self.k_new = [t.cpu().pin_memory() for t in st.k_new]
-        self.v_new = [t.cpu().pin_memory() for t in st.v_new]
-        self.kv_indices = st.kv_indices.cpu().pin_memory()
-        self.kv_indptr = st.kv_indptr.cpu().pin_memory()
-        self.slot_ids = st.slot_ids.cpu().pin_memory()
-        self.out = [torch.empty(t.shape, dtype=t.dtype, **pin) for t in st.out]
-        self.lse = [torch.empty(t.shape, dtype=t.dtype, **pin) for t in st.lse]
-        self.h2d_bytes = sum(t.numel() * t.element_size() for t in
-                             self.q + self.k_new + self.v_new
-                             + [self.kv_indices, self.kv_indptr, self.slot_ids])
-        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.out + self.lse)
+        self.ins = [(dev, dev.cpu().pin_memory()) for dev in
+                    (st.q_all, st.k_new_all, st.v_new_all, st.kv_indices, st.kv_indptr,
+                     st.slot_ids)]
+        self.outs = [(dev, torch.empty(dev.shape, dtype=dev.dtype, pin_memory=True))
+                     for dev in (st.out_all, st.lse_all)]
+        self.out = list(self.outs[0][1].unbind(0))
+        self.h2d_bytes = sum(h.numel() * h.element_size() for _, h in self.ins)
+        self.d2h_bytes = sum(h.numel() * h.element_size() for _, h in self.outs)
 
     def run(self):
-        st = self.st
-        for dst, src in zip(st.q, self.q):
-            dst.copy_(src, non_blocking=True)
-        for dst, src in zip(st.k_new, self.k_new):
-            dst.copy_(src, non_blocking=True)
-        for dst, src in zip(st.v_new, self.v_new):
-            dst.copy_(src, non_blocking=True)
-        st.kv_indices.copy_(self.kv_indices, non_blocking=True)
-        st.kv_indptr.copy_(self.kv_indptr, non_blocking=True)
-        st.slot_ids.copy_(self.slot_ids, non_blocking=True)
-        st.run()
-        for dst, src in zip(self.out, st.out):
-            dst.copy_(src, non_blocking=True)
-        for dst, src in zip(self.lse, st.lse):
-            dst.copy_(src, non_blocking=True)
+        for dev, host in self.ins:
+            dev.copy_(host, non_blocking=True)
+        self.st.run()
+        for dev, host in self.outs:
+            host.copy_(dev, non_blocking=True)
 
 
 def step_bytes(wl: workloads.Workload) -> dict:
