@@ -764,15 +764,22 @@ def main(argv=None):
     return 0
 
 
+def kernel_source_sha() -> str:
+    """sha256 of the decode kernel's sources: csrc/decode.cu, then csrc/ptx.cuh."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("decode.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_gqa_tokentokvpool_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _profiled_traffic(config_no: int):
     """DRAM bytes per attention call from the committed ncu summary of this workload
-    (profiles/traffic.txt), if it was taken on the current decode-kernel source;
-    else None."""
-    import hashlib
-    src = os.path.join(ROOT, "paged_kv_gqa_tokentokvpool_gb300", "csrc", "decode.cu")
+    (profiles/traffic.txt), if it was taken on the current decode-kernel source
+    (csrc/decode.cu followed by csrc/ptx.cuh, hashed together); else None."""
+    sha = kernel_source_sha()
     try:
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
         with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             for line in f:
                 parts = line.split()

@@ -39,9 +39,12 @@
 #include <vector>
 
 #include "pkv_internal.h"
+#include "ptx.cuh"
 
 namespace pkv {
 namespace {
+
+using namespace ptx;
 
 constexpr int kPfWarps = 4;
 constexpr int kPfThreads = 32 * kPfWarps;
@@ -105,60 +108,6 @@ struct PfCfg {
 };
 
 // ---------------------------------------------------------------------------
-// PTX wrappers (PTX ISA: cp.async, ldmatrix, mma, griddepcontrol, ex2)
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// 16-byte async copy; with valid = false nothing is read and the 16 bytes are zero.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ float exp2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float minus_inf() { return __int_as_float(0xff800000); }
-
-// ---------------------------------------------------------------------------
 // kernel
 // ---------------------------------------------------------------------------
 
@@ -192,8 +141,8 @@ __device__ __forceinline__ void issue_tile(const PfArgs& a, const PfUnit& un, ui
         const bool valid = slot[i] >= 0;
         const int64_t off = (int64_t(valid ? slot[i] : 0) * a.n_kv_heads + un.g) * D + part * 8;
         const int soff = (tok * C::kPitch + part * 8) * 2;
-        cp_async16(smem_addr(sk + soff), kp + off, valid);
-        cp_async16(smem_addr(sv + soff), vp + off, valid);
+        cp_async16(smem_u32(sk + soff), kp + off, valid);
+        cp_async16(smem_u32(sv + soff), vp + off, valid);
     }
 }
 
@@ -201,12 +150,12 @@ template <int D, int G>
 __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs a) {
     using C = PfCfg<D, G>;
     extern __shared__ __align__(128) uint8_t smem[];
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_launch_dependents();
     const PfUnit un = a.units[blockIdx.x];  // plan data: read before the wait
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g8 = lane >> 2, t4 = lane & 3;
     // q, the pools and their indices may come from the previous kernel
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
 
     // ---- the unit's q rows (row r: chunk token r / G, head r % G) -> shared memory
     {
@@ -217,7 +166,7 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
             const bool valid = t < un.n_q;
             const int64_t off =
                 (int64_t(un.q_row0 + (valid ? t : 0)) * a.n_qo_heads + un.g * G + h) * D + part * 8;
-            cp_async16(smem_addr(smem + (r * C::kPitch + part * 8) * 2), q + off, valid);
+            cp_async16(smem_u32(smem + (r * C::kPitch + part * 8) * 2), q + off, valid);
         }
     }
     // ---- ring prologue: the range's tiles 0 .. kStages - 2, and the slot ids of the
@@ -231,20 +180,20 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
             load_tile_slots<D, G>(a, un, t0 + s, slot);
             issue_tile<D, G>(a, un, smem, s, slot);
         }
-        cp_commit();  // one group per tile (the first also holds q)
+        cp_async_commit();  // one group per tile (the first also holds q)
     }
     if (C::kStages - 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + C::kStages - 1, slot);
 
     // per lane: rows lo = 16 warp + g8 and hi = lo + 8 of the unit's 64
     const int r_lo = 16 * warp + g8, r_hi = r_lo + 8;
     const int pos_lo = un.pos0 + r_lo / G, pos_hi = un.pos0 + r_hi / G;
-    float m_lo = minus_inf(), m_hi = minus_inf(), l_lo = 0.f, l_hi = 0.f;
+    float m_lo = neg_inf(), m_hi = neg_inf(), l_lo = 0.f, l_hi = 0.f;
     float o[C::kDT][4];
 #pragma unroll
     for (int dt = 0; dt < C::kDT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
 
     // ldmatrix lane addresses
-    const uint32_t q_addr = smem_addr(smem) +
+    const uint32_t q_addr = smem_u32(smem) +
                             ((16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1)) * C::kPitch +
                              8 * (lane >> 4)) * 2;
     const int mi = lane >> 3;
@@ -258,18 +207,18 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
         // slot ids of the tile after it
         const int ahead = n + C::kStages - 1;
         if (ahead < n_tiles) issue_tile<D, G>(a, un, smem, ahead % C::kStages, slot);
-        cp_commit();
+        cp_async_commit();
         if (ahead + 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + ahead + 1, slot);
-        cp_wait<C::kStages - 1>();  // tile n (and q) have landed for this thread
+        cp_async_wait<C::kStages - 1>();  // tile n (and q) have landed for this thread
         __syncthreads();            // ... and for every thread
         if (!q_loaded) {
 #pragma unroll
-            for (int ks = 0; ks < C::kKSteps; ++ks) ldsm4(q_addr + ks * 32, qf[ks]);
+            for (int ks = 0; ks < C::kKSteps; ++ks) ldsm_x4(q_addr + ks * 32, qf[ks]);
             q_loaded = true;
         }
 
         const int st = n % C::kStages;
-        const uint32_t sk = smem_addr(smem) + C::kQBytes + st * C::kStageBytes;
+        const uint32_t sk = smem_u32(smem) + C::kQBytes + st * C::kStageBytes;
         const uint32_t sv = sk + C::kKvBytes;
         // S = Q K^T for this warp's 16 rows and the tile's 32 tokens
         float s[C::kNT][4];
@@ -280,22 +229,22 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
 #pragma unroll
             for (int np = 0; np < C::kNT / 2; ++np) {
                 uint32_t kb[4];
-                ldsm4(sk + k_off + (16 * np * C::kPitch + 16 * ks) * 2, kb);
-                mma16816(s[2 * np], qf[ks], kb[0], kb[1]);
-                mma16816(s[2 * np + 1], qf[ks], kb[2], kb[3]);
+                ldsm_x4(sk + k_off + (16 * np * C::kPitch + 16 * ks) * 2, kb);
+                mma_bf16(s[2 * np], qf[ks], kb[0], kb[1]);
+                mma_bf16(s[2 * np + 1], qf[ks], kb[2], kb[3]);
             }
         }
         // causal mask and online softmax (base 2); token j of the tile is list
         // position (t0 + n) * 32 + 8 nt + 2 t4 (+1); c[0..1] are row lo, c[2..3] row hi
         const int j0 = (t0 + n) * kPfKvTile + 2 * t4;
-        float mx_lo = minus_inf(), mx_hi = minus_inf();
+        float mx_lo = neg_inf(), mx_hi = neg_inf();
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) {
             const int j = j0 + 8 * nt;
-            s[nt][0] = j <= pos_lo ? s[nt][0] * a.scale_log2 : minus_inf();
-            s[nt][1] = j + 1 <= pos_lo ? s[nt][1] * a.scale_log2 : minus_inf();
-            s[nt][2] = j <= pos_hi ? s[nt][2] * a.scale_log2 : minus_inf();
-            s[nt][3] = j + 1 <= pos_hi ? s[nt][3] * a.scale_log2 : minus_inf();
+            s[nt][0] = j <= pos_lo ? s[nt][0] * a.scale_log2 : neg_inf();
+            s[nt][1] = j + 1 <= pos_lo ? s[nt][1] * a.scale_log2 : neg_inf();
+            s[nt][2] = j <= pos_hi ? s[nt][2] * a.scale_log2 : neg_inf();
+            s[nt][3] = j + 1 <= pos_hi ? s[nt][3] * a.scale_log2 : neg_inf();
             mx_lo = fmaxf(mx_lo, fmaxf(s[nt][0], s[nt][1]));
             mx_hi = fmaxf(mx_hi, fmaxf(s[nt][2], s[nt][3]));
         }
@@ -307,20 +256,20 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
         // every row sees the range's first entry (kv_lo <= pos0), so the maxima are
         // finite from the range's first tile on
         const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-        const float al_lo = exp2_approx(m_lo - mn_lo), al_hi = exp2_approx(m_hi - mn_hi);
+        const float al_lo = ex2(m_lo - mn_lo), al_hi = ex2(m_hi - mn_hi);
         m_lo = mn_lo;
         m_hi = mn_hi;
         float sum_lo = 0.f, sum_hi = 0.f;
         uint32_t pa[C::kNT / 2][4];
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) {
-            const float p0 = exp2_approx(s[nt][0] - mn_lo), p1 = exp2_approx(s[nt][1] - mn_lo);
-            const float p2 = exp2_approx(s[nt][2] - mn_hi), p3 = exp2_approx(s[nt][3] - mn_hi);
+            const float p0 = ex2(s[nt][0] - mn_lo), p1 = ex2(s[nt][1] - mn_lo);
+            const float p2 = ex2(s[nt][2] - mn_hi), p3 = ex2(s[nt][3] - mn_hi);
             sum_lo += p0 + p1;
             sum_hi += p2 + p3;
             // S accumulators of column tiles 2k, 2k+1 form the A operand of k-step k
-            pa[nt >> 1][(nt & 1) * 2] = pack2(p0, p1);
-            pa[nt >> 1][(nt & 1) * 2 + 1] = pack2(p2, p3);
+            pa[nt >> 1][(nt & 1) * 2] = pack_bf16x2(p0, p1);
+            pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
         }
         l_lo = fmaf(l_lo, al_lo, sum_lo);
         l_hi = fmaf(l_hi, al_hi, sum_hi);
@@ -337,14 +286,14 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
 #pragma unroll
             for (int dp = 0; dp < C::kDT / 2; ++dp) {
                 uint32_t vb[4];
-                ldsm4_t(sv + v_off + (16 * kk * C::kPitch + 16 * dp) * 2, vb);
-                mma16816(o[2 * dp], pa[kk], vb[0], vb[1]);
-                mma16816(o[2 * dp + 1], pa[kk], vb[2], vb[3]);
+                ldsm_x4_trans(sv + v_off + (16 * kk * C::kPitch + 16 * dp) * 2, vb);
+                mma_bf16(o[2 * dp], pa[kk], vb[0], vb[1]);
+                mma_bf16(o[2 * dp + 1], pa[kk], vb[2], vb[3]);
             }
         }
         __syncthreads();  // the stage is read before the next iteration refills it
     }
-    cp_wait<0>();
+    cp_async_wait<0>();
 
     // ---- epilogue: rows lo / hi of this lane
 #pragma unroll
@@ -376,7 +325,7 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs 
 #pragma unroll
         for (int dt = 0; dt < C::kDT; ++dt)
             *reinterpret_cast<uint32_t*>(dst + 8 * dt) =
-                pack2(o[dt][2 * half] * inv, o[dt][2 * half + 1] * inv);
+                pack_bf16x2(o[dt][2 * half] * inv, o[dt][2 * half + 1] * inv);
         if (a.lse != nullptr && t4 == 0) a.lse[row] = lse2 * kLn2;
     }
 }
@@ -389,7 +338,7 @@ constexpr int kPfMaxPieces = 16;  // pieces per split unit (the planner's cap)
 
 template <int D, int G>
 __global__ void __launch_bounds__(32 * kPfMergeWarps) prefill_merge_kernel(const PfArgs a) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_launch_dependents();
     constexpr int kVD = D / 32;  // dims per lane
     const int lane = threadIdx.x & 31;
     const int w = blockIdx.x * kPfMergeWarps + (threadIdx.x >> 5);
@@ -397,7 +346,7 @@ __global__ void __launch_bounds__(32 * kPfMergeWarps) prefill_merge_kernel(const
     const PfMerge mg = a.merges[w / kPfRows];  // plan data
     const int r = w % kPfRows, t = r / G, h = r % G;
     if (t >= mg.n_q) return;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the pieces come from the kernel before
+    pdl_wait();  // the pieces come from the kernel before
     float x[kPfMaxPieces][kVD], xl[kPfMaxPieces];
 #pragma unroll
     for (int c = 0; c < kPfMaxPieces; ++c) {
@@ -414,7 +363,7 @@ __global__ void __launch_bounds__(32 * kPfMergeWarps) prefill_merge_kernel(const
             }
         }
     }
-    float mx = minus_inf();
+    float mx = neg_inf();
 #pragma unroll
     for (int c = 0; c < kPfMaxPieces; ++c)
         if (c < mg.count) mx = fmaxf(mx, xl[c]);
@@ -424,7 +373,7 @@ __global__ void __launch_bounds__(32 * kPfMergeWarps) prefill_merge_kernel(const
 #pragma unroll
     for (int c = 0; c < kPfMaxPieces; ++c) {
         if (c < mg.count) {
-            const float wgt = exp2_approx(xl[c] - mx);
+            const float wgt = ex2(xl[c] - mx);
             sum += wgt;
 #pragma unroll
             for (int i = 0; i < kVD; ++i) acc[i] = fmaf(wgt, x[c][i], acc[i]);
@@ -435,7 +384,7 @@ __global__ void __launch_bounds__(32 * kPfMergeWarps) prefill_merge_kernel(const
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + row * D + lane * kVD;
 #pragma unroll
     for (int i = 0; i < kVD; i += 2)
-        *reinterpret_cast<uint32_t*>(dst + i) = pack2(acc[i] * inv, acc[i + 1] * inv);
+        *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
     if (a.lse != nullptr && lane == 0) a.lse[row] = (mx + __log2f(sum)) * kLn2;
 }
 
