@@ -746,7 +746,7 @@ def main(argv=None):
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "paged_decode_attn (split-KV kernel, LSE merge fused), "
+                     "kernel": "paged_decode_attn (split-KV decode kernel + LSE merge kernel), "
                                f"avg of {len(attn_ms)} event-timed eager calls "
                                f"{attn_avg_ms * 1e3:.1f} us, "
                                f"{nbytes['attn_per_layer'] / 1e6:.1f} MB algorithmic",

@@ -72,7 +72,9 @@ PREFILL_CASES = [
     ([64, 31], [1000, 31], 16, 4, 256),                  # head_dim 256, G = 4
     ([8, 3], [40, 8], 8, 1, 256),                        # head_dim 256, G = 8, one KV head
     ([40], [40], 4, 4, 256),                             # head_dim 256, G = 1
-    ([200, 7], [4000, 2500], 16, 2, 128),
+    ([200, 7], [4000, 2500], 16, 2, 128),                # G = 8, long ranges split
+    ([300, 5], [5000, 3000], 16, 4, 256),                # head_dim 256, long ranges split
+    ([100], [6000], 8, 8, 128),                          # G = 1, long range split
 ]
 
 
