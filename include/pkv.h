@@ -382,6 +382,17 @@ int paged_decode_plan_status(pkv_plan* plan, int* status);
  */
 void pkv_set_debug_checks(int on);
 
+/*
+ * pkv_inject_stall — failure injection for tests of the bounded waits (this
+ * library's own; the pages have no counterpart). The next n_launches attention
+ * launches (paged_decode_attn / paged_decode_append_attn, any thread) run with a
+ * producer that issues no copies. Every pipeline wait of such a launch expires
+ * after its bound (1 s), the launch ends without a fault or a hang, and the plan's
+ * status word reads nonzero (paged_decode_plan_status); its outputs are invalid.
+ * Later launches are unaffected. 0 cancels. Process-wide.
+ */
+void pkv_inject_stall(int n_launches);
+
 /* pkv_last_error — message of the last failed call on this thread ("" if none). */
 const char* pkv_last_error(void);
 

@@ -41,7 +41,7 @@ EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
             "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
             "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_destroy",
-            "pkv_set_debug_checks", "pkv_last_error")
+            "pkv_set_debug_checks", "pkv_inject_stall", "pkv_last_error")
 
 
 class PkvError(RuntimeError):
@@ -86,6 +86,8 @@ def _load() -> ctypes.CDLL:
                                              ctypes.c_float, P, P, P, P]
     lib.pkv_set_debug_checks.argtypes = [I32]
     lib.pkv_set_debug_checks.restype = None
+    lib.pkv_inject_stall.argtypes = [I32]
+    lib.pkv_inject_stall.restype = None
     lib.pkv_last_error.argtypes = []
     lib.pkv_last_error.restype = ctypes.c_char_p
     for name in ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
@@ -115,6 +117,12 @@ def pkv_last_error() -> str:
 
 def pkv_set_debug_checks(on: bool) -> None:
     library().pkv_set_debug_checks(1 if on else 0)
+
+
+def pkv_inject_stall(n_launches: int) -> None:
+    """The next n attention launches withhold their copies: their bounded waits
+    expire and the plan's status word is set (failure-detection tests)."""
+    library().pkv_inject_stall(int(n_launches))
 
 
 def _check(rc: int) -> None:

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -22,6 +23,7 @@ namespace {
 
 thread_local std::string g_last_error;
 int g_debug_checks = 0;
+std::atomic<int> g_stalls_to_inject{0};  // pkv_inject_stall
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -79,6 +81,8 @@ extern "C" {
 const char* pkv_last_error(void) { return g_last_error.c_str(); }
 
 void pkv_set_debug_checks(int on) { g_debug_checks = on ? 1 : 0; }
+
+void pkv_inject_stall(int n_launches) { g_stalls_to_inject.store(n_launches > 0 ? n_launches : 0); }
 
 int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const void* k_new,
                   const void* v_new, int64_t n, int n_kv_heads, int head_dim,
@@ -601,6 +605,10 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
     a.n_ctas = p->launch_ctas;
     a.shared = p->shared;
     a.early = (p->flags & PKV_PLAN_EARLY_GATHER) != 0;
+    int stalls = g_stalls_to_inject.load();
+    while (stalls > 0 && !g_stalls_to_inject.compare_exchange_weak(stalls, stalls - 1)) {
+    }
+    a.withhold = stalls > 0;
     a.heads_per_cta = p->heads_per_cta;
     a.n_qo_heads = n_qo_heads;
     a.n_kv_heads = n_kv_heads;

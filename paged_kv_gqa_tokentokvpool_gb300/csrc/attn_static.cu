@@ -154,6 +154,7 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     a.part_list = reinterpret_cast<const int32_t*>(scratch + kOffList);
     a.shared = false;
     a.early = false;
+    a.withhold = false;
     a.units = reinterpret_cast<const Unit*>(scratch + kOffUnits);
     a.n_ctas = ctas;
     a.heads_per_cta = hpc;

@@ -206,6 +206,7 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     bool aborted = false;
     // The next unit's descriptor is loaded one unit ahead, and its slot ids are
     // prefetched into L2 once the current unit's first stage is on its way.
+    if (a.withhold) return;  // injected stall: the consumers' waits expire (bounded)
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
     // Slot ids and pool rows may come from the previous kernel: wait for it, after
     // warming L2 with the first unit's slot ids (prefetches are hints, not reads).

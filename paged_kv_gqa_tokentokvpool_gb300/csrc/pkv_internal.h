@@ -105,6 +105,8 @@ struct DecodeArgs {
     bool shared;          // the shared-prefix kernel (prefix units of several requests)
     bool early;           // slot ids and old pool rows may be loaded before the
                           // previous kernel completes (PKV_PLAN_EARLY_GATHER)
+    bool withhold;        // injected stall (pkv_inject_stall): the producer issues no
+                          // copies, so every pipeline wait of the launch expires
     int heads_per_cta;    // KV heads of one group
     int n_qo_heads;
     int n_kv_heads;
