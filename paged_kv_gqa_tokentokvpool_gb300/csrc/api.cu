@@ -595,7 +595,6 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
     a.q = q;
     a.k_pool = k_pool;
     a.v_pool = v_pool;
-    a.kv_indptr = kv_indptr;
     a.kv_indices = kv_indices;
     a.meta_header = reinterpret_cast<const int32_t*>(meta);
     a.cta_begin = reinterpret_cast<const int32_t*>(meta + p->off_cta);

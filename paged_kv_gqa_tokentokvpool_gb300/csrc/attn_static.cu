@@ -146,7 +146,6 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     a.q = q;
     a.k_pool = k_pool;
     a.v_pool = v_pool;
-    a.kv_indptr = kv_indptr;
     a.kv_indices = kv_indices;
     a.meta_header = reinterpret_cast<const int32_t*>(scratch);
     a.cta_begin = reinterpret_cast<const int32_t*>(scratch + kOffCta);

@@ -1,4 +1,5 @@
-// Split-KV paged decode attention with grouped-query heads and a fused LSE merge.
+// Split-KV paged decode attention with grouped-query heads, and the LSE merge of
+// split contexts.
 //
 // What is computed ("Agent-Infer: 纯 Rust 编写的高性能 LLM 推理引擎", section
 // "分页 KV 缓存": batched decode over a page-size-1 token pool; "Pegainfer:
@@ -754,8 +755,9 @@ cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 // Calls FN<D, G, WPH, NB, RB>::run(args...) for the runtime shape. `shared`
-// selects the shared-prefix instance (two query blocks per warp, two row blocks
-// of warps), which exists only at head_dim 128 with one warp per KV head.
+// selects the shared-prefix instance (two query blocks per warp; two row blocks of
+// warps as well under PKV_SHARED_ROW_BLOCKS=2), which exists only at head_dim 128
+// with one warp per KV head.
 template <template <int, int, int, int, int> class FN, typename... Args>
 auto dispatch(int head_dim, int group, int wph, bool shared, Args&&... args)
     -> decltype(FN<128, 1, 1, 1, 1>::run(args...)) {

@@ -95,7 +95,6 @@ struct DecodeArgs {
     const void* q;
     const void* k_pool;
     const void* v_pool;
-    const int32_t* kv_indptr;
     const int32_t* kv_indices;
     const Unit* units;
     const int32_t* cta_begin;
