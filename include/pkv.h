@@ -337,6 +337,24 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
                        int head_dim, float sm_scale, void* out, float* lse,
                        const pkv_prefill_plan* plan, pkv_stream_t stream);
 
+/*
+ * paged_prefill_plan_host — the prefill planner alone, on the host, with no CUDA call
+ * (for inspection and tests). Same offset checks as paged_prefill_plan.
+ *   split_target : a step with fewer tile units than this has its long ranges split
+ *                  (paged_prefill_plan uses two waves of the device's grid); 0 = never
+ *   units_out    : [max_units * 8] int32 — per unit {workspace block or -1, KV head,
+ *                  first query row, query rows, kv_indptr[b], list position of the
+ *                  first query, first list entry, end list entry (exclusive)}
+ *   merges_out   : [max_merges * 8] int32 — per split unit {first query row, query rows,
+ *                  KV head, first workspace block, blocks, 0, 0, 0}
+ *   counts_out   : [3] int32 — {units, merge records, workspace blocks}
+ * Returns PKV_ERR_PLAN if an output array is too small.
+ */
+int paged_prefill_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
+                            int batch, int n_qo_heads, int n_kv_heads, int head_dim,
+                            int split_target, int32_t* units_out, int max_units,
+                            int32_t* merges_out, int max_merges, int32_t* counts_out);
+
 /* paged_prefill_plan_destroy — free a prefill plan (waits for its pending upload). NULL is a no-op. */
 void paged_prefill_plan_destroy(pkv_prefill_plan* plan);
 

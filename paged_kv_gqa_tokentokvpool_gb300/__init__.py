@@ -41,6 +41,7 @@ EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
             "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
             "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_destroy",
+            "paged_prefill_plan_host",
             "pkv_set_debug_checks", "pkv_inject_stall", "pkv_last_error")
 
 
@@ -78,6 +79,7 @@ def _load() -> ctypes.CDLL:
     lib.paged_prefill_plan.argtypes = [P, P, P, I32, P]
     lib.paged_prefill_attn.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, ctypes.c_float,
                                        P, P, P, P]
+    lib.paged_prefill_plan_host.argtypes = [P, P, I32, I32, I32, I32, I32, P, I32, P, I32, P]
     lib.paged_prefill_plan_destroy.argtypes = [P]
     lib.paged_prefill_plan_destroy.restype = None
     lib.paged_decode_attn_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32,
@@ -95,7 +97,7 @@ def _load() -> ctypes.CDLL:
                  "paged_decode_plan_status", "paged_decode_attn_static",
                  "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
                  "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
-                 "paged_prefill_plan", "paged_prefill_attn"):
+                 "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_host"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -386,6 +388,30 @@ def paged_prefill_attn(q, k_pool, v_pool, qo_indptr, kv_indptr, kv_indices, batc
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices),
         batch, n_qo_heads, n_kv_heads, head_dim, float(sm_scale), _ptr(out), _ptr(lse),
         plan.handle, _stream(stream)))
+
+
+def paged_prefill_plan_host(qo_indptr_host, kv_indptr_host, n_qo_heads: int, n_kv_heads: int,
+                            head_dim: int, split_target: int, max_units: int = None,
+                            max_merges: int = None) -> dict:
+    """The prefill planner on the host (no CUDA call). Returns dict(units [n, 8],
+    merges [m, 8], blocks) with the record layouts of include/pkv.h."""
+    qo = _host_indptr(qo_indptr_host)
+    kv = _host_indptr(kv_indptr_host)
+    batch = kv.size - 1
+    G = n_qo_heads // max(n_kv_heads, 1)
+    tile = 64 // max(G, 1)
+    if max_units is None:
+        max_units = (int(qo[-1]) // max(tile, 1) + batch) * n_kv_heads + 2 * max(split_target, 0) + 1
+    if max_merges is None:
+        max_merges = max(split_target, 0) + 1
+    units = np.zeros((max(max_units, 1), 8), np.int32)
+    merges = np.zeros((max(max_merges, 1), 8), np.int32)
+    counts = np.zeros(3, np.int32)
+    _check(library().paged_prefill_plan_host(_ptr(qo), _ptr(kv), batch, n_qo_heads, n_kv_heads,
+                                             head_dim, split_target, _ptr(units), max_units,
+                                             _ptr(merges), max_merges, _ptr(counts)))
+    nu, nm, nb = (int(x) for x in counts)
+    return {"units": units[:nu].copy(), "merges": merges[:nm].copy(), "blocks": nb}
 
 
 def paged_prefill_plan_destroy(plan: PrefillPlan) -> None:

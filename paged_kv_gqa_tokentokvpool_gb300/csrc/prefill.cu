@@ -476,6 +476,89 @@ int pf_cuda_fail(cudaError_t e, const char* what) {
     return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+struct PfPlanCounts {
+    int n_units, n_merges, n_blocks;
+};
+
+// The prefill planner (host only, no CUDA call): checks the offsets and fills
+// units[0 .. n_units) and merges[0 .. n_merges).
+//  1. one unit per (request, tile of tile_tokens chunk tokens, KV head), over every
+//     list entry its queries see;
+//  2. with fewer such units than split_target, each long range is cut at ring-tile
+//     boundaries at or below its first query's position (every query then sees
+//     every entry of every piece but the last) into at most kPfMaxPieces pieces of
+//     about equal length; each piece writes workspace block `part`, and a merge
+//     record names the unit's consecutive blocks;
+//  3. units are listed longest range first.
+int prefill_plan_compute(const char* who, const int32_t* qo, const int32_t* kv, int batch,
+                         int tile_tokens, int n_kv_heads, int split_target, PfUnit* units,
+                         int max_units, PfMerge* merges, int max_merges, int max_blocks,
+                         PfPlanCounts* out) {
+    if (batch > 0 && (qo[0] != 0 || kv[0] != 0))
+        return fail(PKV_ERR_INVALID_ARG, "%s: offsets must start at 0", who);
+    for (int b = 0; b < batch; ++b) {
+        const int C = qo[b + 1] - qo[b];
+        const int L = kv[b + 1] - kv[b];
+        if (C < 0 || L < 0)
+            return fail(PKV_ERR_INVALID_ARG, "%s: offsets decrease at request %d", who, b);
+        if (C > L)
+            return fail(PKV_ERR_INVALID_ARG,
+                        "%s: request %d has a chunk of %d tokens but lists only %d slots", who, b,
+                        C, L);
+    }
+    std::vector<PfUnit> tiles;
+    int64_t total_tiles = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int C = qo[b + 1] - qo[b];
+        const int L = kv[b + 1] - kv[b];
+        for (int t0 = 0; t0 < C; t0 += tile_tokens) {
+            const int n_q = std::min(tile_tokens, C - t0);
+            const int pos0 = L - C + t0;
+            for (int g = 0; g < n_kv_heads; ++g) {
+                tiles.push_back(PfUnit{-1, g, qo[b] + t0, n_q, kv[b], pos0, 0, pos0 + n_q});
+                total_tiles += (pos0 + n_q + kPfKvTile - 1) / kPfKvTile;
+            }
+        }
+    }
+    int n = 0, n_blocks = 0, n_merges = 0;
+    const bool split = int64_t(tiles.size()) < split_target && total_tiles > 0;
+    const int64_t piece_tiles =
+        split ? std::max<int64_t>(8, (total_tiles + split_target - 1) / split_target) : 1;
+    for (const PfUnit& u : tiles) {
+        int cuts = 0;  // split points at multiples of step * kPfKvTile, all <= pos0
+        int64_t step = piece_tiles;
+        if (split) {
+            cuts = static_cast<int>(u.pos0 / (step * kPfKvTile));
+            if (cuts > kPfMaxPieces - 1) {
+                step = (u.pos0 / kPfKvTile + kPfMaxPieces - 1) / (kPfMaxPieces - 1);
+                cuts = std::min(static_cast<int>(u.pos0 / (step * kPfKvTile)), kPfMaxPieces - 1);
+            }
+        }
+        if (n + cuts + 1 > max_units || n_blocks + (cuts ? cuts + 1 : 0) > max_blocks ||
+            (cuts && n_merges >= max_merges))
+            return fail(PKV_ERR_PLAN, "%s: more work than the plan holds", who);
+        if (cuts == 0) {
+            units[n++] = u;
+            continue;
+        }
+        merges[n_merges++] = PfMerge{u.q_row0, u.n_q, u.g, n_blocks, cuts + 1, 0, 0, 0};
+        for (int c = 0; c <= cuts; ++c) {
+            PfUnit piece = u;
+            piece.part = n_blocks++;
+            piece.kv_lo = static_cast<int32_t>(c * step * kPfKvTile);
+            piece.kv_hi = c == cuts ? u.kv_hi : static_cast<int32_t>((c + 1) * step * kPfKvTile);
+            units[n++] = piece;
+        }
+    }
+    std::stable_sort(units, units + n, [](const PfUnit& x, const PfUnit& y) {
+        return x.kv_hi - x.kv_lo > y.kv_hi - y.kv_lo;
+    });
+    out->n_units = n;
+    out->n_merges = n_merges;
+    out->n_blocks = n_blocks;
+    return PKV_OK;
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -600,19 +683,8 @@ int paged_prefill_plan(pkv_prefill_plan* p, const int32_t* qo_indptr_host,
         return fail(PKV_ERR_PLAN, "%s: batch %d outside [0, %d]", who, batch, p->max_batch);
     if (!qo_indptr_host || !kv_indptr_host)
         return fail(PKV_ERR_INVALID_ARG, "%s: NULL offsets", who);
-    if (qo_indptr_host[0] != 0 || kv_indptr_host[0] != 0)
-        return fail(PKV_ERR_INVALID_ARG, "%s: offsets must start at 0", who);
-    for (int b = 0; b < batch; ++b) {
-        const int C = qo_indptr_host[b + 1] - qo_indptr_host[b];
-        const int L = kv_indptr_host[b + 1] - kv_indptr_host[b];
-        if (C < 0 || L < 0)
-            return fail(PKV_ERR_INVALID_ARG, "%s: offsets decrease at request %d", who, b);
-        if (C > L)
-            return fail(PKV_ERR_INVALID_ARG,
-                        "%s: request %d has a chunk of %d tokens but lists only %d slots", who, b,
-                        C, L);
-    }
-    if (int64_t(qo_indptr_host[batch]) > p->max_q_tokens)
+    if (qo_indptr_host[0] == 0 && batch >= 0 &&
+        int64_t(qo_indptr_host[batch]) > p->max_q_tokens)
         return fail(PKV_ERR_PLAN, "%s: %d query tokens exceed the plan's max_q_tokens %lld", who,
                     qo_indptr_host[batch], (long long)p->max_q_tokens);
     if (p->copy_pending) {  // the staging may still feed the previous step's copy
@@ -620,78 +692,52 @@ int paged_prefill_plan(pkv_prefill_plan* p, const int32_t* qo_indptr_host,
         if (e != cudaSuccess) return pf_cuda_fail(e, "waiting for the previous prefill plan copy");
         p->copy_pending = false;
     }
-    // 1. one unit per (request, tile of chunk tokens, KV head), over every list
-    //    entry its queries see
-    std::vector<PfUnit> tiles;
-    int64_t total_tiles = 0;
-    for (int b = 0; b < batch; ++b) {
-        const int C = qo_indptr_host[b + 1] - qo_indptr_host[b];
-        const int L = kv_indptr_host[b + 1] - kv_indptr_host[b];
-        for (int t0 = 0; t0 < C; t0 += p->tile_tokens) {
-            const int n_q = std::min(p->tile_tokens, C - t0);
-            const int pos0 = L - C + t0;
-            for (int g = 0; g < p->n_kv_heads; ++g) {
-                tiles.push_back(PfUnit{-1, g, qo_indptr_host[b] + t0, n_q, kv_indptr_host[b],
-                                       pos0, 0, pos0 + n_q});
-                total_tiles += (pos0 + n_q + kPfKvTile - 1) / kPfKvTile;
-            }
-        }
-    }
-    // 2. Too few units for two waves of the grid: cut each long range at ring-tile
-    //    boundaries below its first query's position (every query then sees every
-    //    entry of every piece but the last), into pieces of about equal length;
-    //    each piece writes a partial result that the merge kernel combines.
-    int n = 0, n_blocks = 0, n_merges = 0;
-    const bool split = int64_t(tiles.size()) < p->split_target && total_tiles > 0;
-    const int64_t piece_tiles =
-        std::max<int64_t>(8, (total_tiles + p->split_target - 1) / p->split_target);
-    for (const PfUnit& u : tiles) {
-        int cuts = 0;  // split points at multiples of step * kPfKvTile, all <= pos0
-        int64_t step = piece_tiles;
-        if (split) {
-            cuts = static_cast<int>(u.pos0 / (step * kPfKvTile));
-            if (cuts > kPfMaxPieces - 1) {
-                step = (u.pos0 / kPfKvTile + kPfMaxPieces - 1) / (kPfMaxPieces - 1);
-                cuts = static_cast<int>(u.pos0 / (step * kPfKvTile));
-                cuts = std::min(cuts, kPfMaxPieces - 1);
-            }
-        }
-        if (n + cuts + 1 > p->max_units || n_blocks + (cuts ? cuts + 1 : 0) > p->max_blocks ||
-            (cuts && n_merges >= p->max_merges))
-            return fail(PKV_ERR_PLAN, "%s: more work than the plan holds", who);
-        if (cuts == 0) {
-            p->host_units[n++] = u;
-            continue;
-        }
-        p->host_merges[n_merges++] = PfMerge{u.q_row0, u.n_q, u.g, n_blocks, cuts + 1, 0, 0, 0};
-        for (int c = 0; c <= cuts; ++c) {
-            PfUnit piece = u;
-            piece.part = n_blocks++;
-            piece.kv_lo = static_cast<int32_t>(c * step * kPfKvTile);
-            piece.kv_hi = c == cuts ? u.kv_hi : static_cast<int32_t>((c + 1) * step * kPfKvTile);
-            p->host_units[n++] = piece;
-        }
-    }
-    // 3. longest range first: the grid's last CTAs are the short ones
-    std::stable_sort(p->host_units, p->host_units + n, [](const PfUnit& x, const PfUnit& y) {
-        return x.kv_hi - x.kv_lo > y.kv_hi - y.kv_lo;
-    });
-    if (n > 0) {
-        cudaError_t e = cudaMemcpyAsync(p->dev_units, p->host_units, sizeof(PfUnit) * size_t(n),
+    PfPlanCounts c{};
+    const int rc = prefill_plan_compute(who, qo_indptr_host, kv_indptr_host, batch,
+                                        p->tile_tokens, p->n_kv_heads, p->split_target,
+                                        p->host_units, p->max_units, p->host_merges,
+                                        p->max_merges, p->max_blocks, &c);
+    if (rc != PKV_OK) return rc;
+    if (c.n_units > 0) {
+        cudaError_t e = cudaMemcpyAsync(p->dev_units, p->host_units,
+                                        sizeof(PfUnit) * size_t(c.n_units),
                                         cudaMemcpyHostToDevice, stream);
-        if (e == cudaSuccess && n_merges > 0)
-            e = cudaMemcpyAsync(p->dev_merges, p->host_merges, sizeof(PfMerge) * size_t(n_merges),
+        if (e == cudaSuccess && c.n_merges > 0)
+            e = cudaMemcpyAsync(p->dev_merges, p->host_merges, sizeof(PfMerge) * size_t(c.n_merges),
                                 cudaMemcpyHostToDevice, stream);
         if (e == cudaSuccess) e = cudaEventRecord(p->copy_done, stream);
         if (e != cudaSuccess) return pf_cuda_fail(e, "prefill plan upload");
         p->copy_pending = true;
     }
     p->batch = batch;
-    p->n_units = n;
-    p->n_merges = n_merges;
+    p->n_units = c.n_units;
+    p->n_merges = c.n_merges;
     p->qo_host.assign(qo_indptr_host, qo_indptr_host + batch + 1);
     p->kv_host.assign(kv_indptr_host, kv_indptr_host + batch + 1);
     p->planned = true;
+    return PKV_OK;
+}
+
+int paged_prefill_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
+                            int batch, int n_qo_heads, int n_kv_heads, int head_dim,
+                            int split_target, int32_t* units_out, int max_units,
+                            int32_t* merges_out, int max_merges, int32_t* counts_out) {
+    clear_error();
+    const char* who = "paged_prefill_plan_host";
+    if (!prefill_shape_supported(n_qo_heads, n_kv_heads, head_dim))
+        return fail(PKV_ERR_UNSUPPORTED, "%s: unsupported shape", who);
+    if (!qo_indptr_host || !kv_indptr_host || !counts_out || (max_units > 0 && !units_out) ||
+        (max_merges > 0 && !merges_out) || batch < 0 || max_units < 0 || max_merges < 0)
+        return fail(PKV_ERR_INVALID_ARG, "%s: NULL or negative argument", who);
+    PfPlanCounts c{};
+    const int rc = prefill_plan_compute(
+        who, qo_indptr_host, kv_indptr_host, batch, kPfRows / (n_qo_heads / n_kv_heads),
+        n_kv_heads, split_target, reinterpret_cast<PfUnit*>(units_out), max_units,
+        reinterpret_cast<PfMerge*>(merges_out), max_merges, 2 * std::max(split_target, 0), &c);
+    if (rc != PKV_OK) return rc;
+    counts_out[0] = c.n_units;
+    counts_out[1] = c.n_merges;
+    counts_out[2] = c.n_blocks;
     return PKV_OK;
 }
 

@@ -283,3 +283,87 @@ def test_planner_rejects_bad_input(pkv):
     with pytest.raises(pkv.PkvError) as e:  # 4 heads of dim 256 do not fit a 1 KB row
         pkv.paged_decode_plan_host(np.array([0, 10], np.int32), 4, 256, 304, heads_per_cta=4)
     assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# the chunked-prefill planner (host only)
+# ---------------------------------------------------------------------------
+
+def check_prefill_plan(qo, kv, hq, hkv, plan, split_target):
+    """Every (query row, KV head) is planned exactly once; split units' pieces
+    partition their range at ring-tile cuts at or below the first query's position."""
+    qo, kv = np.asarray(qo, np.int64), np.asarray(kv, np.int64)
+    G = hq // hkv
+    tile = 64 // G
+    units, merges = plan["units"], plan["merges"]
+    covered = np.zeros((int(qo[-1]), hkv), np.int32)
+    req_of_row = np.repeat(np.arange(len(qo) - 1), np.diff(qo))
+    lengths = [int(x) for x in units[:, 7] - units[:, 6]]
+    assert lengths == sorted(lengths, reverse=True), "longest range first"
+    by_block = {}
+    for part, g, q_row0, n_q, kv_begin, pos0, kv_lo, kv_hi in units:
+        assert 1 <= n_q <= tile and 0 <= g < hkv
+        b = req_of_row[q_row0]
+        C, L = qo[b + 1] - qo[b], kv[b + 1] - kv[b]
+        t0 = q_row0 - qo[b]
+        assert t0 % tile == 0 and kv_begin == kv[b] and pos0 == L - C + t0
+        assert 0 <= kv_lo < kv_hi <= pos0 + n_q
+        if part < 0:
+            assert kv_lo == 0 and kv_hi == pos0 + n_q
+            covered[q_row0:q_row0 + n_q, g] += 1
+        else:
+            assert part not in by_block
+            by_block[part] = (q_row0, n_q, g, pos0, kv_lo, kv_hi)
+    assert sorted(by_block) == list(range(plan["blocks"]))
+    for q_row0, n_q, g, first, count, *_ in merges:
+        assert 2 <= count <= 16
+        pieces = [by_block[first + c] for c in range(count)]
+        assert all(p[:3] == (q_row0, n_q, g) for p in pieces)
+        pos0 = pieces[0][3]
+        ranges = sorted((p[4], p[5]) for p in pieces)
+        assert ranges[0][0] == 0 and ranges[-1][1] == pos0 + n_q
+        for (lo, hi), (lo2, _) in zip(ranges, ranges[1:]):
+            assert hi == lo2 and hi % 32 == 0 and hi <= pos0, "cut on a tile edge at or below pos0"
+        covered[q_row0:q_row0 + n_q, g] += 1
+    assert np.all(covered == 1)
+    n_tile_units = sum(-(-int(qo[b + 1] - qo[b]) // tile) for b in range(len(qo) - 1)) * hkv
+    if n_tile_units >= split_target:
+        assert len(merges) == 0, "enough units: no split"
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_prefill_planner_properties(pkv, seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 12))
+    chunks = rng.choice([0, 1, 17, 64, 300, 512], B)
+    contexts = chunks + rng.integers(0, [20000, 3000, 50][seed % 3], B)
+    qo = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    kv = np.concatenate([[0], np.cumsum(contexts)]).astype(np.int32)
+    hq, hkv, d = [(32, 8, 128), (16, 4, 256), (8, 8, 128), (64, 8, 128)][seed % 4]
+    for target in (0, 100, 912, 100000):
+        plan = pkv.paged_prefill_plan_host(qo, kv, hq, hkv, d, target)
+        check_prefill_plan(qo, kv, hq, hkv, plan, target)
+
+
+def test_prefill_planner_splits_a_short_step(pkv):
+    # 8 requests x 64-token chunks over long contexts: far fewer units than the target
+    qo = np.arange(0, 9 * 64, 64, dtype=np.int32)
+    kv = np.concatenate([[0], np.cumsum([16000, 9000, 64, 300, 15000, 7000, 2000, 12000])]).astype(np.int32)
+    plan = pkv.paged_prefill_plan_host(qo, kv, 32, 8, 128, 912)
+    check_prefill_plan(qo, kv, 32, 8, plan, 912)
+    assert len(plan["merges"]) > 0 and len(plan["units"]) > 256
+
+
+def test_prefill_planner_rejects_bad_input(pkv):
+    with pytest.raises(pkv.PkvError) as e:  # chunk longer than the slot list
+        pkv.paged_prefill_plan_host(np.array([0, 10], np.int32), np.array([0, 9], np.int32),
+                                    32, 8, 128, 0)
+    assert e.value.code == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_prefill_plan_host(np.array([0, 10], np.int32), np.array([0, 90], np.int32),
+                                    32, 8, 128, 0, max_units=1)
+    assert e.value.code == pkv.PKV_ERR_PLAN
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_prefill_plan_host(np.array([0, 1], np.int32), np.array([0, 9], np.int32),
+                                    30, 8, 128, 0)
+    assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
