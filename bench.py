@@ -37,6 +37,7 @@ DEFAULT_CONFIG = 2
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 L2_BYTES = 129 * 1024 * 1024
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 
 # ---------------------------------------------------------------------------
@@ -676,16 +677,37 @@ def main(argv=None):
         st.run()
     barrier()
     attn_events = []
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        start.record(stream)
+    # A step that reads less than twice the L2 would be timed warm: then each step is
+    # timed on its own, with a write of a buffer larger than L2 between steps.
+    flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=stream.device)
+             if nbytes["step"] < 2 * L2_BYTES else None)
+
+    def timed(fn):
+        if flush is None:
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1)
+        pairs = []
         for _ in range(args.steps):
-            st.run()
-        end.record(stream)
+            flush.fill_(1)
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            fn()
+            t1.record(stream)
+            pairs.append((t0, t1))
         torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in pairs)
+
+    with ClockSampler(local) as clocks:
+        step_ms = timed(st.run)
     barrier()
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), pg, "cuda")
+    elapsed_ms = max_over_ranks(step_ms, pg, "cuda")
     # The attention calls alone, each bracketed by CUDA events on its stream
     # (eager launches: an event between two kernels also ends their overlap).
     for _ in range(args.steps):
@@ -698,15 +720,7 @@ def main(argv=None):
     for _ in range(args.warmup):
         io.run()
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        io.run()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, "cuda")
+    e2e_ms = max_over_ranks(timed(io.run), pg, "cuda")
 
     if rank != 0:
         if pg is not None:
@@ -736,8 +750,12 @@ def main(argv=None):
             / (elapsed_ms * 1e-3) / 1e9,
             "plan": {"units": info["n_units"], "merges": info["n_merges"],
                      "chunk_tokens": info["chunk_tokens"], "ctas": info["n_ctas"]},
-            "l2": f"inputs larger than L2: each step reads {nbytes['step'] / 1e9:.2f} GB "
-                  f"across {wl.layers} layers' pools (L2 {L2_BYTES / 2**20:.0f} MiB)",
+            "l2": (f"inputs larger than L2: each step reads {nbytes['step'] / 1e9:.2f} GB "
+                   f"across {wl.layers} layers' pools (L2 {L2_BYTES / 2**20:.0f} MiB)"
+                   if flush is None else
+                   f"L2 flushed between timed steps (a {2 * L2_BYTES / 2**20:.0f} MiB write); "
+                   f"each step reads {nbytes['step'] / 1e6:.1f} MB"),
+            "hbm_frac_of_nominal": value / NOMINAL_HBM_GBS,
             "parallelism": f"replicas x{world}",
             "launch": "eager" if args.no_graph else "cuda graph of the layer loop per step; plan on host",
             "append": "fused into the attention launch" if st.fused else "separate kernel",

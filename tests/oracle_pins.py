@@ -133,6 +133,30 @@ def pin_sdpa(orc, seed=0):
         _close(lse, rlse, 1e-12, 1e-12, what=f"sdpa lse {lengths},{hq}/{hkv},{d}")
 
 
+def pin_numpy_brute_force(orc, seed=10):
+    """Tiny random cases (B <= 3, L <= 5, head_dim 4 or 8) against the definition
+    written out with numpy, request by request and head by head."""
+    rng = np.random.default_rng(seed)
+    for lengths, hq, hkv, d in [([1, 5, 3], 2, 1, 4), ([4, 2], 4, 2, 8), ([5], 8, 2, 8),
+                                ([3, 0, 2], 2, 2, 4)]:
+        q, k, v, indptr, indices, scale = random_case(rng, lengths, hq, hkv, d)
+        out, lse = orc.decode(q, k, v, indptr, indices, hq, hkv, d, scale)
+        qd, kd, vd = widen(q), widen(k), widen(v)
+        G = hq // hkv
+        for b in range(len(lengths)):
+            idx = indices[indptr[b]:indptr[b + 1]]
+            for h in range(hq):
+                if idx.size == 0:
+                    assert lse[b, h] == -np.inf and np.all(out[b, h] == 0)
+                    continue
+                s = np.array([scale * np.dot(qd[b, h], kd[j, h // G]) for j in idx])
+                m = s.max()
+                want_lse = m + np.log(np.exp(s - m).sum())
+                want = (np.exp(s - want_lse)[:, None] * vd[idx, h // G]).sum(axis=0)
+                assert abs(lse[b, h] - want_lse) < 1e-12, (lengths, b, h)
+                assert np.max(np.abs(out[b, h] - want)) < 1e-12, (lengths, b, h)
+
+
 def pin_single_token(orc, seed=1):
     rng = np.random.default_rng(seed)
     hq, hkv, d = 8, 2, 128
@@ -408,6 +432,6 @@ def pin_prefill_one_token_chunks(orc, seed=35):
 PREFILL_PINS = [pin_prefill_sdpa, pin_prefill_brute_force, pin_prefill_first_token,
                 pin_prefill_causality, pin_prefill_chunk_cut, pin_prefill_one_token_chunks]
 
-ALL_PINS = [pin_golden, pin_sdpa, pin_single_token, pin_zero_query, pin_identical_v,
+ALL_PINS = [pin_golden, pin_sdpa, pin_numpy_brute_force, pin_single_token, pin_zero_query, pin_identical_v,
             pin_permutation, pin_split_merge, pin_gqa_equal_queries, pin_empty,
             pin_lse_statistics, pin_append] + PREFILL_PINS
