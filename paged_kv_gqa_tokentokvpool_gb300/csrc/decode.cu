@@ -16,14 +16,16 @@
 //    KV-head group of up to 512 bf16 per token (4 heads at head_dim 128, 2 at
 //    256), so one token's K (or V) row of the group is one contiguous 1 KB run of
 //    the pool.
-//  * Warp specialisation: one producer warp turns slot ids into 1D bulk copies
+//  * Warp specialisation: two producer warps turn slot ids into 1D bulk copies
 //    (cp.async.bulk, the TMA engine) of whole rows into a 3-stage shared-memory
-//    ring of 16-token tiles, signalled by mbarrier transaction counts; lane i
-//    copies token i%16's K (i < 16) or V (i >= 16) row. Four consumer warps take
+//    ring of 16-token tiles, signalled by mbarrier transaction counts; each
+//    stage's 32 row copies (16 K rows, 16 V rows) are shared between them. One
+//    warp alone issues only about 25 bulk copies per microsecond, which at 1 KB
+//    per copy is below the HBM rate of an SM's two CTAs. Four consumer warps take
 //    the tiles. Up to 3 x 32 KB per CTA is in flight, which covers HBM latency
 //    with two CTAs per SM. The slot ids themselves travel kStages + 1 stages
-//    ahead of the copies (cp.async into a small shared ring), so no stage waits a
-//    round trip for its ids. Rows read once carry an L2 evict-first policy; rows
+//    ahead of the copies (cp.async into a small shared ring per producer warp),
+//    so no stage waits a round trip for its ids. Rows read once carry an L2 evict-first policy; rows
 //    of a shared prefix, which the group's other prefix units read again,
 //    evict-last.
 //  * Programmatic dependent launch: the plan is read before waiting for the
@@ -68,6 +70,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr int kProducersPerBlock = 2;  // producer warps per row block of consumer warps
 
 // ---------------------------------------------------------------------------
 // bounded waits (PTX ISA: mbarrier.try_wait, %globaltimer)
@@ -105,18 +108,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
 // head (so 4 / WPH KV heads per CTA), NB 8-row query blocks per warp and RB row
 // blocks of warps. A unit's query rows (row r = head r % G of its request r / G)
 // are dealt to RB sets of four warps, 8 NB rows each: RB = 1 serves 8 NB / G
-// requests per unit with two CTAs per SM; RB = 2 doubles the warps and the ring
-// and runs one CTA per SM, so each K/V row staged in shared memory serves
-// 16 NB / G requests (measured slower: one CTA per SM leaves half its warps idle
-// on units of one request). A pipeline stage holds kSub 16-token
+// requests per unit with two CTAs per SM; RB = 2 doubles the warps and runs one
+// CTA per SM, so each K/V row staged in shared memory serves 16 NB / G requests.
+// Under RB = 2 a unit whose rows fit one row block (a private suffix, say) is
+// dealt by stages instead: set s takes the unit's stages t with t % 2 == s, and
+// set 1 hands its softmax state (m, l, o) to set 0 through shared memory at the
+// unit's end, where set 0 folds the two by the log-sum-exp identity. So no warp
+// idles on a unit of one request. A pipeline stage holds kSub 16-token
 // sub-tiles of K rows and of V rows of the CTA's kHeadsPerCta heads; kSub is
 // chosen so that every stage carries 16 x kHeadGroupElems bf16 of K and as much
 // of V (32 KB, plus row padding) whatever the head count.
 template <int D, int G, int WPH, int NB = 1, int RB = 1>
 struct Cfg {
     static constexpr int kConsumerWarps = kGroupWarps * RB;
-    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
-    static constexpr int kStages = 3 * RB;                      // 32 KB stages in flight
+    static constexpr int kProducerWarps = kProducersPerBlock * RB;  // each issues 1 / P of the copies
+    static constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
+    static constexpr int kStages = RB == 1 ? 3 : 5;             // 32 KB stages in flight
     static constexpr int kMinBlocks = 2 / RB;                   // resident CTAs per SM
     static constexpr int kWarpRows = 8 * NB;                    // query rows of one warp
     static constexpr int kHeadsPerCta = kGroupWarps / WPH;      // KV heads of one group
@@ -132,11 +139,25 @@ struct Cfg {
     static constexpr int kQHeads = kHeadsPerCta * G;            // query heads of a group
     static constexpr int kAhead = kStages + 1;                  // stages of slot ids in flight
     static constexpr int kBarOffset = kStages * kStage;
-    static constexpr int kIdxOffset = kBarOffset + 2 * kStages * 8 + 16;
-    static constexpr int kSmem = kIdxOffset + kAhead * kStageTokens * 4;
+    // hand-over barriers of the stage-dealt units: full and empty per warp of set 1
+    static constexpr int kXBars = RB == 2 ? 2 * kGroupWarps : 0;
+    static constexpr int kIdxOffset = kBarOffset + (2 * kStages + kXBars) * 8 + 16;
+    // hand-over buffer: per warp of set 1, per lane, m and l of its 2 NB columns
+    // and its 4 NB kMBlocks output accumulators, stored [value][lane]
+    static constexpr int kXFloats = NB * (4 + 4 * kMBlocks);
+    // copies of one stage: K then V rows of kStageTokens tokens; copy c is issued by
+    // producer warp c % P, lane (c / P) % 32
+    static constexpr int kCopies = 2 * kStageTokens;
+    static constexpr int kCopiesPerLane = (kCopies / kProducerWarps + 31) / 32;
+    static constexpr int kIdRing = kAhead * kStageTokens * 4;  // slot-id ring of one producer warp
+    static constexpr int kXOffset = (kIdxOffset + kProducerWarps * kIdRing + 15) / 16 * 16;
+    static constexpr int kSmem = kXOffset + (RB == 2 ? kGroupWarps * 32 * kXFloats * 4 : 0);
     static_assert(G >= 1 && G <= 8, "group size");
     static_assert(NB == 1 || NB == 2, "query blocks");
     static_assert(RB == 1 || RB == 2, "row blocks");
+    static_assert(RB == 1 || NB == 2, "two row blocks load q per unit (two query blocks)");
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+    static_assert(kCopies % kProducerWarps == 0, "copies split evenly over the producer warps");
     static_assert(kHeadsPerCta * D * kSub == kHeadGroupElems, "stage budget");
     static_assert(kMBlocks >= 1, "dims per warp");
 };
@@ -144,6 +165,8 @@ struct Cfg {
 struct Shared {
     uint64_t* full;
     uint64_t* empty;
+    uint64_t* xfull;   // [kGroupWarps] set 1's hand-over written (two row blocks only)
+    uint64_t* xempty;  // [kGroupWarps] set 0 has read it
     volatile int* flags;  // [0] abort
 };
 
@@ -182,22 +205,34 @@ __device__ __forceinline__ void fetch_slot_ids(const DecodeArgs& a, SlotFetch& f
     if (++f.pos == C::kAhead) f.pos = 0;
 }
 
-// Producer warp: lane l copies, for every sub-tile j of a stage, token
-// (l % 16) + 16 j's K row (l < 16) or V row (l >= 16) of the CTA's head group.
+// Producer warps: copy c of a stage (c < kStageTokens: token c's K row, else token
+// c - kStageTokens's V row of the CTA's head group) is issued by warp c % P, lane
+// (c / P) % 32, so the P warps share each stage's copies. Each warp arrives on the
+// stage's full barrier with the bytes of its own copies and keeps its own ring of
+// slot ids.
 template <int D, int G, int WPH, int NB, int RB>
 __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
     using C = Cfg<D, G, WPH, NB, RB>;
+    constexpr int P = C::kProducerWarps;
     const int lane = threadIdx.x & 31;
-    const int tok = lane & (kTile - 1);
-    const bool is_v = lane >= kTile;
-    const char* pool = static_cast<const char*>(is_v ? a.v_pool : a.k_pool);
+    const int pw = (threadIdx.x >> 5) - C::kConsumerWarps;  // producer warp index
     const bool fused = a.k_new != nullptr;
-    const char* new_rows = static_cast<const char*>(is_v ? a.v_new : a.k_new);
     const int64_t slot_bytes = int64_t(a.n_kv_heads) * D * 2;
-    const uint32_t ring = smem_u32(smem) + (is_v ? C::kStageTokens * C::kRowP : 0) + tok * C::kRowP;
-    const uint32_t id_ring = smem_u32(smem) + C::kIdxOffset;
-    const int32_t* id_ring_ptr = reinterpret_cast<const int32_t*>(smem + C::kIdxOffset);
+    // this lane's copies: token, K or V, and shared-memory offset within a stage
+    int tok[C::kCopiesPerLane];
+    bool is_v[C::kCopiesPerLane], has[C::kCopiesPerLane];
+    uint32_t dst[C::kCopiesPerLane];
+#pragma unroll
+    for (int i = 0; i < C::kCopiesPerLane; ++i) {
+        const int c = pw + P * (lane + 32 * i);
+        has[i] = c < C::kCopies;
+        is_v[i] = c >= C::kStageTokens;
+        tok[i] = is_v[i] ? c - C::kStageTokens : c;
+        dst[i] = smem_u32(smem) + (is_v[i] ? C::kStageTokens * C::kRowP : 0) + tok[i] * C::kRowP;
+    }
+    const uint32_t id_ring = smem_u32(smem) + C::kIdxOffset + pw * C::kIdRing;
+    const int32_t* id_ring_ptr = reinterpret_cast<const int32_t*>(smem + C::kIdxOffset + pw * C::kIdRing);
     const uint64_t stream_policy = policy_evict_first();
     const uint64_t shared_policy = policy_evict_last();
     int stage = 0;
@@ -205,8 +240,9 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     uint32_t fill_parity = 0;
     uint32_t filled_mask = 0, parity_bits = 0;  // per stage: filled at all / parity of last fill
     bool aborted = false;
-    // The next unit's descriptor is loaded one unit ahead, and its slot ids are
-    // prefetched into L2 once the current unit's first stage is on its way.
+    // The next unit's descriptor is loaded one unit ahead, and (by the first producer
+    // warp) its slot ids are prefetched into L2 once the current unit's first stage
+    // is on its way.
     if (a.withhold) return;  // injected stall: the consumers' waits expire (bounded)
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
     // Slot ids and pool rows may come from the previous kernel: wait for it, after
@@ -214,7 +250,7 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     // With early gather they were final before the step's plan upload, so the
     // loads start at once and only the fused append's new rows wait.
     bool waited = !a.early;
-    if (u_begin < u_end)
+    if (u_begin < u_end && pw == 0)
         for (int off = 32 * lane; off < next.tok_end - next.tok_begin && off < 32 * 32 * 4;
              off += 32 * 32)
             prefetch_l2(a.kv_indices + next.idx_begin + off);
@@ -230,9 +266,11 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
         const int n_tok = un.tok_end - un.tok_begin;
         const int n_stages = unit_stages(un, C::kStageTokens);
         const int64_t group_off = int64_t(un.hg) * C::kRow;
-        for (int off = 32 * (lane + 1); off < n_tok; off += 32 * 32) prefetch_l2(idx + off);
+        const uint64_t policy = un.len == -2 ? shared_policy : stream_policy;
+        if (pw == 0)
+            for (int off = 32 * (lane + 1); off < n_tok; off += 32 * 32) prefetch_l2(idx + off);
         for (int t = 0; t < n_stages; ++t) {
-            if (t == (n_stages > 1 ? 1 : 0) && u + 1 < u_end) {
+            if (pw == 0 && t == (n_stages > 1 ? 1 : 0) && u + 1 < u_end) {
                 const int32_t* nidx = a.kv_indices + next.idx_begin;
                 for (int off = 32 * lane; off < next.tok_end - next.tok_begin; off += 32 * 32)
                     prefetch_l2(nidx + off);
@@ -249,10 +287,10 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             // this stage's slot ids (the oldest group in flight) have landed
             cp_async_wait<C::kAhead - 1>();
             __syncwarp();
-            int slot[C::kSub];
+            int slot[C::kCopiesPerLane];
 #pragma unroll
-            for (int j = 0; j < C::kSub; ++j)
-                slot[j] = tok + kTile * j < n ? id_ring_ptr[pos * C::kStageTokens + tok + kTile * j] : -1;
+            for (int i = 0; i < C::kCopiesPerLane; ++i)
+                slot[i] = has[i] && tok[i] < n ? id_ring_ptr[pos * C::kStageTokens + tok[i]] : -1;
             __syncwarp();  // every lane has read its ids before the place is refilled below
             // k_new / v_new may come from the previous kernel
             const int first = un.tok_begin + t * C::kStageTokens;
@@ -260,19 +298,21 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                 pdl_wait();
                 waited = true;
             }
-            if (lane == 0) mbar_arrive_expect_tx(full_bar, n > 0 ? C::kStageTx : 0u);
+            if (lane == 0) mbar_arrive_expect_tx(full_bar, n > 0 ? C::kStageTx / P : 0u);
             __syncwarp();
             if (n > 0) {
 #pragma unroll
-                for (int j = 0; j < C::kSub; ++j) {
-                    const void* src = slot[j] >= 0
-                                          ? static_cast<const void*>(pool + slot[j] * slot_bytes + group_off)
+                for (int i = 0; i < C::kCopiesPerLane; ++i) {
+                    if (!has[i]) continue;
+                    const char* pool = static_cast<const char*>(is_v[i] ? a.v_pool : a.k_pool);
+                    const void* src = slot[i] >= 0
+                                          ? static_cast<const void*>(pool + slot[i] * slot_bytes + group_off)
                                           : a.zero_row;
                     // fused append: the request's newest token comes from its new row
-                    if (fused && first + tok + kTile * j == un.len - 1)
-                        src = new_rows + un.b * slot_bytes + group_off;
-                    bulk_g2s_hint(ring + stage * C::kStage + j * kTile * C::kRowP, src, C::kRow,
-                                  full_bar, un.len == -2 ? shared_policy : stream_policy);
+                    if (fused && first + tok[i] == un.len - 1)
+                        src = static_cast<const char*>(is_v[i] ? a.v_new : a.k_new) + un.b * slot_bytes +
+                              group_off;
+                    bulk_g2s_hint(dst[i] + stage * C::kStage, src, C::kRow, full_bar, policy);
                 }
             }
             fetch_slot_ids<C>(a, f, u_end, lane, id_ring);  // refills place `pos`
@@ -357,7 +397,7 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     const int wg = warp % kGroupWarps;
     const int hh = wg / WPH;      // KV head within the group
     const int part = wg % WPH;    // which slice of head_dim this warp accumulates
-    const int r0 = (warp / kGroupWarps) * C::kWarpRows;  // first query row of this warp
+    const int rb = warp / kGroupWarps;  // row block (set of four warps)
     const int g = lane >> 2, t4 = lane & 3;
     const int hq = a.n_qo_heads;
     const float scale_log2 = a.sm_scale * kLog2e;
@@ -371,6 +411,11 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                             (hh * D + part * C::kDimsPerWarp + ((lane >> 3) & 1) * 8) * 2;
     int stage = 0;
     uint32_t full_parity = 0;
+    // hand-over of stage-dealt units (two row blocks): set 1 waits for its buffer
+    // to be free (a fresh barrier reports the phase before it as complete), set 0
+    // for it to be written
+    uint32_t x_parity = rb == 1 ? 1u : 0u;
+    float* xbuf = reinterpret_cast<float*>(smem + C::kXOffset) + wg * 32 * C::kXFloats + lane;
 
     // With one query block the next unit's q fragments are loaded while the current
     // unit streams; with two (shared prefixes) they are loaded at the unit's start.
@@ -378,19 +423,24 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     uint32_t qb[NB][C::kKSteps][2], qn[NB][C::kKSteps][2];
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
     // Warm L2 with the first unit's q rows (a hint, safe before the wait): lane l
-    // touches query row r0 + l of this warp's KV head.
-    if (u_begin < u_end && lane < C::kWarpRows && (r0 + lane) / G < next.nreq) {
+    // touches query row rb * kWarpRows + l of this warp's KV head.
+    if (u_begin < u_end && lane < C::kWarpRows && (rb * C::kWarpRows + lane) / G < next.nreq) {
         const int kvh = next.hg * C::kHeadsPerCta + hh;
+        const int r = rb * C::kWarpRows + lane;
         prefetch_l2(static_cast<const __nv_bfloat16*>(a.q) +
-                    (int64_t(next.b + (r0 + lane) / G) * a.n_qo_heads + kvh * G + (r0 + lane) % G) * D);
+                    (int64_t(next.b + r / G) * a.n_qo_heads + kvh * G + r % G) * D);
     }
     pdl_wait();  // q may come from the previous kernel
     if constexpr (kPrefetchQ) {
-        if (u_begin < u_end) load_q_fragments<D, G, WPH, NB, RB>(a, next, hh, r0, g, t4, qn);
+        if (u_begin < u_end) load_q_fragments<D, G, WPH, NB, RB>(a, next, hh, 0, g, t4, qn);
     }
     for (int u = u_begin; u < u_end; ++u) {
         const Unit un = next;
         const int kvh = un.hg * C::kHeadsPerCta + hh;
+        // Two row blocks: a unit whose rows fit one block is dealt by stages (both
+        // sets take rows 0 ..), a larger one by rows.
+        const bool by_stage = RB == 2 && un.nreq * G <= C::kWarpRows;
+        const int r0 = by_stage ? 0 : rb * C::kWarpRows;  // first query row of this warp
         if constexpr (kPrefetchQ) {
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
@@ -426,17 +476,20 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             const bool ok = mbar_wait(smem_u32(&sh.full[stage]), full_parity, a.status, sh.flags);
             if (!__all_sync(kFull, ok)) return;  // uniform exit: no lane is left in a shuffle
             const int n_stage = n_tok - t * C::kStageTokens;
+            // this warp's share of the stage: all of it, or none when dealt to the other set
+            const bool mine = !by_stage || (t & 1) == rb;
             // Fused append: the stage holding the request's newest token has its new
-            // K/V rows (copied from k_new / v_new); the first row block's warps write
-            // their share of them to the pool slot before the stage is released.
-            if (a.k_new != nullptr && r0 == 0) {
+            // K/V rows (copied from k_new / v_new); the warps of the first row block
+            // (or of the set the stage is dealt to) write their share of them to the
+            // pool slot before the stage is released.
+            if (a.k_new != nullptr && (by_stage ? mine : rb == 0)) {
                 const int row = un.len - 1 - (un.tok_begin + t * C::kStageTokens);
                 if (row >= 0 && row < n_stage && row < C::kStageTokens)
                     store_new_rows<D, G, WPH, NB, RB>(a, un, smem, stage, row, hh, part, lane);
             }
 #pragma unroll
             for (int j = 0; j < C::kSub; ++j) {
-                const int n = active ? n_stage - j * kTile : 0;  // valid rows of this sub-tile
+                const int n = active && mine ? n_stage - j * kTile : 0;  // valid rows of this sub-tile
                 if (n <= 0) break;
                 const uint32_t st = stage * C::kStage + j * kTile * C::kRowP;
                 float s[NB][4];
@@ -506,6 +559,53 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             }
         }
 
+        // ---- stage-dealt unit: set 1 hands (m, l, o) to set 0, which folds them in
+        if (by_stage && n_stages > 1) {
+            const bool ok = mbar_wait(smem_u32(rb == 1 ? &sh.xempty[wg] : &sh.xfull[wg]), x_parity,
+                                      a.status, sh.flags);
+            if (!__all_sync(kFull, ok)) return;
+            x_parity ^= 1;
+            if (rb == 1) {
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+                    for (int jc = 0; jc < 2; ++jc) {
+                        xbuf[32 * (2 * nb + jc)] = m[nb][jc];
+                        xbuf[32 * (2 * NB + 2 * nb + jc)] = l[nb][jc];
+                    }
+#pragma unroll
+                    for (int mb = 0; mb < C::kMBlocks; ++mb)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            xbuf[32 * (4 * NB + 4 * (nb * C::kMBlocks + mb) + i)] = o[nb][mb][i];
+                }
+                mbar_arrive(smem_u32(&sh.xfull[wg]));  // each lane releases its own stores
+                continue;
+            }
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                float a0[2], a1[2];
+#pragma unroll
+                for (int jc = 0; jc < 2; ++jc) {
+                    const float m1 = xbuf[32 * (2 * nb + jc)];
+                    const float l1 = xbuf[32 * (2 * NB + 2 * nb + jc)];
+                    const float mn = fmaxf(m[nb][jc], m1);
+                    a0[jc] = m[nb][jc] == neg_inf() ? 0.f : ex2(m[nb][jc] - mn);
+                    a1[jc] = m1 == neg_inf() ? 0.f : ex2(m1 - mn);
+                    l[nb][jc] = l[nb][jc] * a0[jc] + l1 * a1[jc];
+                    m[nb][jc] = mn;
+                }
+#pragma unroll
+                for (int mb = 0; mb < C::kMBlocks; ++mb)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        o[nb][mb][i] = o[nb][mb][i] * a0[i & 1] +
+                                       xbuf[32 * (4 * NB + 4 * (nb * C::kMBlocks + mb) + i)] * a1[i & 1];
+            }
+            mbar_arrive(smem_u32(&sh.xempty[wg]));  // the buffer may be refilled
+        }
+        if (by_stage && rb == 1) continue;  // set 0 writes the unit's results
+
         // ---- epilogue: o[nb][mb][0..3] = (dim 16*mb' + g (+8), rows r0 + 8nb + 2t4, +1)
         if (!active) continue;
         const int dim0 = part * C::kDimsPerWarp + g;
@@ -554,11 +654,17 @@ __global__ void __launch_bounds__(Cfg<D, G, WPH, NB, RB>::kThreads, Cfg<D, G, WP
     Shared sh;
     sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
     sh.empty = sh.full + C::kStages;
-    sh.flags = reinterpret_cast<volatile int*>(sh.empty + C::kStages);
+    sh.xfull = sh.empty + C::kStages;
+    sh.xempty = sh.xfull + C::kXBars / 2;
+    sh.flags = reinterpret_cast<volatile int*>(sh.full + 2 * C::kStages + C::kXBars);
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(&sh.full[s]), 1);
+            mbar_init(smem_u32(&sh.full[s]), C::kProducerWarps);
             mbar_init(smem_u32(&sh.empty[s]), C::kConsumerWarps);
+        }
+        for (int w = 0; w < C::kXBars / 2; ++w) {  // every lane of a warp arrives
+            mbar_init(smem_u32(&sh.xfull[w]), 32);
+            mbar_init(smem_u32(&sh.xempty[w]), 32);
         }
         sh.flags[0] = 0;
         fence_mbar_init();
@@ -569,7 +675,7 @@ __global__ void __launch_bounds__(Cfg<D, G, WPH, NB, RB>::kThreads, Cfg<D, G, WP
     pdl_launch_dependents();
     const int u_begin = a.cta_begin[blockIdx.x];
     const int u_end = a.cta_begin[blockIdx.x + 1];
-    if ((threadIdx.x >> 5) == C::kConsumerWarps)
+    if ((threadIdx.x >> 5) >= C::kConsumerWarps)
         producer_warp<D, G, WPH, NB, RB>(a, smem, sh, u_begin, u_end);
     else
         consumer_warp<D, G, WPH, NB, RB>(a, smem, sh, u_begin, u_end);
