@@ -307,7 +307,7 @@ int paged_prefill_plan_create(pkv_prefill_plan** plan, int max_batch, int64_t ma
 
 /*
  * paged_prefill_plan — the step's work list, once per prefill step (reused by every
- * layer). Cuts every chunk into tiles of 64 / G query tokens per KV head and orders
+ * layer). Cuts every chunk into tiles of 128 / G query tokens per KV head and orders
  * the tiles longest causal range first. Uploaded asynchronously on `stream` from
  * pinned staging; waits on the host for the previous step's upload first.
  *   qo_indptr_host : [batch + 1] int32 HOST copy of the chunk offsets (qo_indptr[0] = 0,
@@ -354,6 +354,14 @@ int paged_prefill_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_ind
                             int batch, int n_qo_heads, int n_kv_heads, int head_dim,
                             int split_target, int32_t* units_out, int max_units,
                             int32_t* merges_out, int max_merges, int32_t* counts_out);
+
+/*
+ * paged_prefill_plan_status — read and clear the prefill plan's device status word
+ * (synchronous). 0: every prefill kernel that used the plan completed its pipeline
+ * waits; nonzero: some wait exceeded its bound (1 s) and that launch's outputs are
+ * invalid.
+ */
+int paged_prefill_plan_status(pkv_prefill_plan* plan, int* status);
 
 /* paged_prefill_plan_destroy — free a prefill plan (waits for its pending upload). NULL is a no-op. */
 void paged_prefill_plan_destroy(pkv_prefill_plan* plan);

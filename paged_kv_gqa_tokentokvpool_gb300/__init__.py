@@ -41,7 +41,7 @@ EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
             "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
             "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_destroy",
-            "paged_prefill_plan_host",
+            "paged_prefill_plan_host", "paged_prefill_plan_status",
             "pkv_set_debug_checks", "pkv_inject_stall", "pkv_last_error")
 
 
@@ -80,6 +80,7 @@ def _load() -> ctypes.CDLL:
     lib.paged_prefill_attn.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, ctypes.c_float,
                                        P, P, P, P]
     lib.paged_prefill_plan_host.argtypes = [P, P, I32, I32, I32, I32, I32, P, I32, P, I32, P]
+    lib.paged_prefill_plan_status.argtypes = [P, P]
     lib.paged_prefill_plan_destroy.argtypes = [P]
     lib.paged_prefill_plan_destroy.restype = None
     lib.paged_decode_attn_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32,
@@ -97,7 +98,8 @@ def _load() -> ctypes.CDLL:
                  "paged_decode_plan_status", "paged_decode_attn_static",
                  "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
                  "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
-                 "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_host"):
+                 "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_host",
+                 "paged_prefill_plan_status"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -347,6 +349,12 @@ class PrefillPlan:
     def __init__(self, handle: ctypes.c_void_p, shape):
         self.handle = handle
         self.shape = shape
+
+    def status(self) -> int:
+        """Read and clear the device status word (0 = every pipeline wait completed)."""
+        v = ctypes.c_int()
+        _check(library().paged_prefill_plan_status(self.handle, ctypes.byref(v)))
+        return v.value
 
     def __del__(self):
         if getattr(self, "handle", None) and _lib is not None:

@@ -11,25 +11,32 @@
 // with g = h / G (grouped-query attention, "Pegainfer: 纯Rust+CUDA构建的LLM推理引擎",
 // section "1. 注意力机制优化").
 //
-// Design for sm_103a. Unlike decode, every K/V row here serves the 64 / G query
-// tokens of a tile times G heads, so the work is a dense contraction per KV head:
-//  * One CTA per work unit (request, KV head, tile of 64 / G chunk tokens): its 64
-//    query rows (token, head) are four 16-row warp tiles. The plan orders units
-//    longest causal range first, so the grid drains evenly.
-//  * The unit's q rows are staged once in shared memory and then held as mma
-//    fragments in registers for the whole unit; the request's slot rows
-//    of that KV head stream through a ring of 32-token K/V tiles gathered with
-//    16-byte cp.async (each thread copies whole 16-byte pieces of scattered pool
-//    rows; a stage's slot ids are loaded one iteration ahead of its copies).
-//  * Tensor cores, FlashAttention-2 orientation: per warp and tile
-//      S[16 x 32] = Q[16 x D] K^T    and    O[16 x D] += P[16 x 32] V[32 x D]
-//    with mma.sync m16n8k16 (bf16, fp32 accumulate). K fragments come by
-//    ldmatrix, V by ldmatrix.trans, and the probabilities pass from the S
-//    accumulators to the A operand of P V in registers.
-//  * Online softmax in base 2 with fp32 state per row; the causal mask compares
-//    each token's list position with the row's query position, and the ring
-//    stops at the unit's last query position.
-//  * No spin-waits: the ring is cp.async groups and CTA barriers.
+// Design for sm_103a. Unlike decode, every K/V row here serves the 128 / G query
+// tokens of a unit times G heads, so the work is a dense contraction per KV head,
+// run on the fifth-generation tensor cores (tcgen05) with accumulators in tensor
+// memory:
+//  * One CTA per work unit (request, KV head, tile of 128 / G chunk tokens): its 128
+//    query rows (row r: token r / G, head r % G) are the M of every MMA. The plan
+//    orders units longest causal range first, so the grid drains evenly.
+//  * Four producer warps gather the unit's q rows once, then the request's slot rows
+//    of that KV head in 64-token K/V tiles, with 16-byte cp.async into a ring of
+//    shared-memory stages, each row stored in the tensor core's 128-byte swizzled
+//    layout (K-major for q and K; V's rows are the same bytes read as an MN-major
+//    operand).
+//  * One thread issues the MMAs: S = Q K^T (128 x 64, K = head_dim) into one of two
+//    TMEM buffers, and O += P V (128 x head_dim, K = 64) into a TMEM accumulator,
+//    each signalled on an mbarrier by tcgen05.commit. S of the next tile is computed
+//    while the softmax works on the current one.
+//  * Four softmax warps own one query row per thread: they read the row of S from
+//    TMEM, apply the causal mask (list position <= the row's query position) and an
+//    online softmax in base 2 with fp32 state, write P as bf16 to shared memory for
+//    the P V product, and rescale O in TMEM when a row's running maximum grows by
+//    more than 2^8 (between rescales the probabilities stay below 2^8, exact enough
+//    for bf16 P and fp32 sums). At the end they read O back, divide by the row sum
+//    and store out and lse.
+//  * Every wait is an mbarrier wait bounded by 1 s; on expiry the CTA records it in
+//    the plan's status word, every role leaves its loop, the MMA and copies in
+//    flight are drained (again bounded) and the tensor memory is freed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,27 +47,34 @@
 
 #include "pkv_internal.h"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 namespace {
 
 using namespace ptx;
 
-constexpr int kPfWarps = 4;
-constexpr int kPfThreads = 32 * kPfWarps;
-constexpr int kPfRows = 16 * kPfWarps;  // query rows (token, head) per CTA
-constexpr int kPfKvTile = 32;           // KV tokens per ring stage
-constexpr int kPfPad = 8;               // bf16 padding per shared row: conflict-free ldmatrix
+constexpr int kPfRows = 128;                // query rows (token, head) per unit: the MMA's M
+constexpr int kPfKvTile = 64;               // KV tokens per ring stage: N of S, K of P V
+constexpr int kPfSoftmaxWarps = 4;          // one thread per query row (TMEM lane)
+constexpr int kPfProducerWarps = 4;
+constexpr int kPfProducerThreads = 32 * kPfProducerWarps;
+constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfProducerWarps;  // also owns the TMEM allocation
+constexpr int kPfThreads = 32 * (kPfMmaWarp + 1);
+constexpr uint32_t kPfTmemCols = 512;
+constexpr int kPfOCol = 256;                // TMEM columns: S buffers at 0 and 64, O from 256
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.f;         // rescale O once a row maximum grows by more
+constexpr unsigned long long kPfWaitNs = 1000000000ull;
 
 // One work unit: query tokens q_row0 .. q_row0 + n_q - 1 (rows of q/out) of one
 // request, KV head g, over list entries kv_lo .. kv_hi - 1 of the request's slot
 // list (which starts at kv_begin in kv_indices). The unit's first query sits at list
 // position pos0. part < 0: the unit covers every entry its queries see and writes
 // out/lse; otherwise it is one piece of a split range, kv_lo <= pos0 and kv_lo a
-// multiple of the ring tile, and writes its 64 rows' normalised fp32 output and
+// multiple of the ring tile, and writes its 128 rows' normalised fp32 output and
 // base-2 lse to workspace block `part`.
 struct PfUnit {
     int32_t part, g, q_row0, n_q, kv_begin, pos0, kv_lo, kv_hi;
@@ -85,252 +99,378 @@ struct PfArgs {
     float scale_log2;  // sm_scale * log2(e)
     void* out;
     float* lse;
-    float* ws_o;       // [blocks, 64, head_dim] partial outputs of split units
-    float* ws_lse;     // [blocks, 64] their base-2 lse
+    float* ws_o;       // [blocks, 128, head_dim] partial outputs of split units
+    float* ws_lse;     // [blocks, 128] their base-2 lse
     const PfMerge* merges;
     int n_merges;
+    int* status;       // nonzero: a wait of some CTA exceeded its bound
 };
 
+// Shared memory of one CTA (offsets from a 1024-byte aligned base). Every operand
+// is stored as 64-element panels of 128-byte rows in the 128-byte swizzled layout:
+// row n of a panel at (n / 8) * 1024 + (n % 8) * 128, its 16-byte chunk c at
+// ((c ^ (n % 8)) * 16).
 template <int D, int G>
 struct PfCfg {
-    static constexpr int kStages = D == 128 ? 3 : 2;   // 2 CTAs per SM at D = 256
-    static constexpr int kPitch = D + kPfPad;          // shared row pitch (bf16)
-    static constexpr int kQBytes = kPfRows * kPitch * 2;
-    static constexpr int kKvBytes = kPfKvTile * kPitch * 2;  // K (or V) of one stage
-    static constexpr int kStageBytes = 2 * kKvBytes;
-    static constexpr int kSmem = kQBytes + kStages * kStageBytes;
-    static constexpr int kChunks = D / 8;                  // 16-byte pieces per row
-    static constexpr int kPieces = kPfKvTile * kChunks / kPfThreads;  // per thread, K (or V)
-    static constexpr int kKSteps = D / 16;
-    static constexpr int kNT = kPfKvTile / 8;              // 8-token column tiles of S
-    static constexpr int kDT = D / 8;                      // 8-dim column tiles of O
-    static_assert(kPieces * kPfThreads == kPfKvTile * kChunks, "ring pieces");
+    static constexpr int kStages = D == 128 ? 4 : 2;
+    static constexpr int kPanels = D / 64;
+    static constexpr int kQPanel = kPfRows * 128;           // bytes of one q panel
+    static constexpr int kKvPanel = kPfKvTile * 128;        // bytes of one K (or V) panel
+    static constexpr int kQBytes = kPanels * kQPanel;
+    static constexpr int kKvBytes = kPanels * kKvPanel;     // K (or V) of one stage
+    static constexpr int kPBytes = kPfRows * kPfKvTile * 2; // one panel
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + kQBytes;
+    static constexpr int kVOff = kKOff + kStages * kKvBytes;
+    static constexpr int kPOff = kVOff + kStages * kKvBytes;
+    static constexpr int kBarOff = kPOff + kPBytes;
+    // mbarriers: kv_full[kStages], kv_empty[kStages], s_full[2], s_empty[2], p_full,
+    // o_done, drain; then the TMEM address and the abort flag
+    static constexpr int kNumBars = 2 * kStages + 7;
+    static constexpr int kTmemOff = kBarOff + 8 * kNumBars;
+    static constexpr int kAbortOff = kTmemOff + 4;
+    static constexpr int kSmem = kAbortOff + 4 + 1024;      // + slack to align the base
+    static constexpr int kChunks = D / 8;                   // 16-byte pieces per row
+    static constexpr int kTilePieces = kPfKvTile * kChunks / kPfProducerThreads;
+    static constexpr int kQPieces = kPfRows * kChunks / kPfProducerThreads;
+    static constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kPfRows, kPfKvTile, false, false);
+    static constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kPfRows, D, false, true);
+    static_assert(kTilePieces * kPfProducerThreads == kPfKvTile * kChunks, "ring pieces");
+    static_assert(kQPieces * kPfProducerThreads == kPfRows * kChunks, "q pieces");
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+    static_assert(2 * kPfKvTile <= kPfOCol && kPfOCol + D <= int(kPfTmemCols), "TMEM columns");
 };
 
-// ---------------------------------------------------------------------------
-// kernel
-// ---------------------------------------------------------------------------
+// Byte offset of 16-byte chunk c of row n in a panel-major swizzled operand whose
+// panels hold `rows` rows.
+__device__ __forceinline__ uint32_t sw128_off(int n, int c, int rows) {
+    return uint32_t((c >> 3) * rows * 128 + (n >> 3) * 1024 + (n & 7) * 128 + (((c & 7) ^ (n & 7)) << 4));
+}
 
-// Slot ids of the pieces this thread copies for KV tile `tile` (-1 past the range).
+__device__ __forceinline__ unsigned long long pf_global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase of `bar` with the given parity; on expiry (or if
+// another thread already gave up) records the failure and returns false.
+__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, int* status,
+                                        volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = pf_global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (pf_global_ns() - t0 > kPfWaitNs) {
+            atomicOr(status, 1);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Slot ids of the rows this producer thread copies for KV tile `tile` (-1 past
+// the range): piece i is token (pt + i * kPfProducerThreads) / kChunks.
 template <int D, int G>
-__device__ __forceinline__ void load_tile_slots(const PfArgs& a, const PfUnit& un, int tile,
-                                                int (&slot)[PfCfg<D, G>::kPieces]) {
+__device__ __forceinline__ void load_tile_slots(const PfArgs& a, const PfUnit& un, int tile, int pt,
+                                                int (&slot)[PfCfg<D, G>::kTilePieces]) {
     using C = PfCfg<D, G>;
 #pragma unroll
-    for (int i = 0; i < C::kPieces; ++i) {
-        const int tok = (threadIdx.x + i * kPfThreads) / C::kChunks;
+    for (int i = 0; i < C::kTilePieces; ++i) {
+        const int tok = (pt + i * kPfProducerThreads) / C::kChunks;
         const int j = tile * kPfKvTile + tok;
         slot[i] = j < un.kv_hi ? __ldg(a.kv_indices + un.kv_begin + j) : -1;
     }
 }
 
-// Issue the cp.async copies of KV tile pieces into ring stage `st` (tokens past the
-// unit's range are zero-filled).
+// cp.async of this thread's pieces of a K/V tile into stage `st` (zero past the range).
 template <int D, int G>
-__device__ __forceinline__ void issue_tile(const PfArgs& a, const PfUnit& un, uint8_t* smem,
-                                           int st, const int (&slot)[PfCfg<D, G>::kPieces]) {
+__device__ __forceinline__ void issue_tile(const PfArgs& a, const PfUnit& un, uint32_t base, int st,
+                                           int pt, const int (&slot)[PfCfg<D, G>::kTilePieces]) {
     using C = PfCfg<D, G>;
     const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_pool);
     const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_pool);
-    uint8_t* sk = smem + C::kQBytes + st * C::kStageBytes;
-    uint8_t* sv = sk + C::kKvBytes;
+    const uint32_t sk = base + C::kKOff + st * C::kKvBytes;
+    const uint32_t sv = base + C::kVOff + st * C::kKvBytes;
 #pragma unroll
-    for (int i = 0; i < C::kPieces; ++i) {
-        const int c = threadIdx.x + i * kPfThreads;
+    for (int i = 0; i < C::kTilePieces; ++i) {
+        const int c = pt + i * kPfProducerThreads;
         const int tok = c / C::kChunks, part = c % C::kChunks;
         const bool valid = slot[i] >= 0;
         const int64_t off = (int64_t(valid ? slot[i] : 0) * a.n_kv_heads + un.g) * D + part * 8;
-        const int soff = (tok * C::kPitch + part * 8) * 2;
-        cp_async16(smem_u32(sk + soff), kp + off, valid);
-        cp_async16(smem_u32(sv + soff), vp + off, valid);
+        const uint32_t so = sw128_off(tok, part, kPfKvTile);
+        cp_async16(sk + so, kp + off, valid);
+        cp_async16(sv + so, vp + off, valid);
     }
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const PfArgs a) {
+__global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfArgs a) {
     using C = PfCfg<D, G>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    pdl_launch_dependents();
-    const PfUnit un = a.units[blockIdx.x];  // plan data: read before the wait
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the swizzled operands need 1024-byte aligned atoms
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+    const uint32_t bars = base + C::kBarOff;
+    const auto kv_full = [&](int s) { return bars + 8u * s; };
+    const auto kv_empty = [&](int s) { return bars + 8u * (C::kStages + s); };
+    const auto s_full = [&](int b) { return bars + 8u * (2 * C::kStages + b); };
+    const auto s_empty = [&](int b) { return bars + 8u * (2 * C::kStages + 2 + b); };
+    const uint32_t p_full = bars + 8u * (2 * C::kStages + 4);
+    const uint32_t o_done = bars + 8u * (2 * C::kStages + 5);
+    const uint32_t drain = bars + 8u * (2 * C::kStages + 6);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g8 = lane >> 2, t4 = lane & 3;
-    // q, the pools and their indices may come from the previous kernel
-    pdl_wait();
 
-    // ---- the unit's q rows (row r: chunk token r / G, head r % G) -> shared memory
-    {
-        const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-        for (int c = tid; c < kPfRows * C::kChunks; c += kPfThreads) {
-            const int r = c / C::kChunks, part = c % C::kChunks;
-            const int t = r / G, h = r % G;
-            const bool valid = t < un.n_q;
-            const int64_t off =
-                (int64_t(un.q_row0 + (valid ? t : 0)) * a.n_qo_heads + un.g * G + h) * D + part * 8;
-            cp_async16(smem_u32(smem + (r * C::kPitch + part * 8) * 2), q + off, valid);
+    if (tid == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(kv_full(s), kPfProducerThreads);
+            mbar_init(kv_empty(s), 1);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(s_full(b), 1);
+            mbar_init(s_empty(b), 32 * kPfSoftmaxWarps);
+        }
+        mbar_init(p_full, 32 * kPfSoftmaxWarps);
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
     }
-    // ---- ring prologue: the range's tiles 0 .. kStages - 2, and the slot ids of the
-    // next one (ring index i holds list tile t0 + i)
+    if (warp == kPfMmaWarp) {  // the whole warp: allocation is .sync.aligned
+        tc::tmem_alloc(base + C::kTmemOff, kPfTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kTmemOff);
+    pdl_launch_dependents();
+    const PfUnit un = a.units[blockIdx.x];  // plan data
     const int t0 = un.kv_lo / kPfKvTile;
     const int n_tiles = (un.kv_hi + kPfKvTile - 1) / kPfKvTile - t0;
-    int slot[C::kPieces];
-#pragma unroll
-    for (int s = 0; s < C::kStages - 1; ++s) {
-        if (s < n_tiles) {
-            load_tile_slots<D, G>(a, un, t0 + s, slot);
-            issue_tile<D, G>(a, un, smem, s, slot);
-        }
-        cp_async_commit();  // one group per tile (the first also holds q)
-    }
-    if (C::kStages - 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + C::kStages - 1, slot);
+    // q, the pools and their indices may come from the previous kernel, and out may
+    // still be read by it
+    pdl_wait();
 
-    // per lane: rows lo = 16 warp + g8 and hi = lo + 8 of the unit's 64
-    const int r_lo = 16 * warp + g8, r_hi = r_lo + 8;
-    const int pos_lo = un.pos0 + r_lo / G, pos_hi = un.pos0 + r_hi / G;
-    float m_lo = neg_inf(), m_hi = neg_inf(), l_lo = 0.f, l_hi = 0.f;
-    float o[C::kDT][4];
-#pragma unroll
-    for (int dt = 0; dt < C::kDT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-
-    // ldmatrix lane addresses
-    const uint32_t q_addr = smem_u32(smem) +
-                            ((16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1)) * C::kPitch +
-                             8 * (lane >> 4)) * 2;
-    const int mi = lane >> 3;
-    const uint32_t k_off = ((8 * (mi >> 1) + (lane & 7)) * C::kPitch + 8 * (mi & 1)) * 2;
-    const uint32_t v_off = ((8 * (mi & 1) + (lane & 7)) * C::kPitch + 8 * (mi >> 1)) * 2;
-
-    uint32_t qf[C::kKSteps][4];  // this warp's q rows as A fragments, loaded once
-    bool q_loaded = false;
-    for (int n = 0; n < n_tiles; ++n) {
-        // copies of tile n + kStages - 1 (slot ids loaded last iteration), then the
-        // slot ids of the tile after it
-        const int ahead = n + C::kStages - 1;
-        if (ahead < n_tiles) issue_tile<D, G>(a, un, smem, ahead % C::kStages, slot);
-        cp_async_commit();
-        if (ahead + 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + ahead + 1, slot);
-        cp_async_wait<C::kStages - 1>();  // tile n (and q) have landed for this thread
-        __syncthreads();            // ... and for every thread
-        if (!q_loaded) {
-#pragma unroll
-            for (int ks = 0; ks < C::kKSteps; ++ks) ldsm_x4(q_addr + ks * 32, qf[ks]);
-            q_loaded = true;
-        }
-
-        const int st = n % C::kStages;
-        const uint32_t sk = smem_u32(smem) + C::kQBytes + st * C::kStageBytes;
-        const uint32_t sv = sk + C::kKvBytes;
-        // S = Q K^T for this warp's 16 rows and the tile's 32 tokens
-        float s[C::kNT][4];
-#pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < C::kKSteps; ++ks) {
-#pragma unroll
-            for (int np = 0; np < C::kNT / 2; ++np) {
-                uint32_t kb[4];
-                ldsm_x4(sk + k_off + (16 * np * C::kPitch + 16 * ks) * 2, kb);
-                mma_bf16(s[2 * np], qf[ks], kb[0], kb[1]);
-                mma_bf16(s[2 * np + 1], qf[ks], kb[2], kb[3]);
+    if (warp >= kPfSoftmaxWarps && warp < kPfMmaWarp) {
+        // ================= producers =================
+        const int pt = tid - 32 * kPfSoftmaxWarps;
+        {   // the unit's q rows (row r: token r / G, head r % G), with tile 0 below
+            const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+#pragma unroll 4
+            for (int i = 0; i < C::kQPieces; ++i) {
+                const int c = pt + i * kPfProducerThreads;
+                const int r = c / C::kChunks, part = c % C::kChunks;
+                const int t = r / G, h = r % G;
+                const bool valid = t < un.n_q;
+                const int64_t off =
+                    (int64_t(un.q_row0 + (valid ? t : 0)) * a.n_qo_heads + un.g * G + h) * D + part * 8;
+                cp_async16(base + C::kQOff + sw128_off(r, part, kPfRows), q + off, valid);
             }
         }
-        // causal mask and online softmax (base 2); token j of the tile is list
-        // position (t0 + n) * 32 + 8 nt + 2 t4 (+1); c[0..1] are row lo, c[2..3] row hi
-        const int j0 = (t0 + n) * kPfKvTile + 2 * t4;
-        float mx_lo = neg_inf(), mx_hi = neg_inf();
-#pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) {
-            const int j = j0 + 8 * nt;
-            s[nt][0] = j <= pos_lo ? s[nt][0] * a.scale_log2 : neg_inf();
-            s[nt][1] = j + 1 <= pos_lo ? s[nt][1] * a.scale_log2 : neg_inf();
-            s[nt][2] = j <= pos_hi ? s[nt][2] * a.scale_log2 : neg_inf();
-            s[nt][3] = j + 1 <= pos_hi ? s[nt][3] * a.scale_log2 : neg_inf();
-            mx_lo = fmaxf(mx_lo, fmaxf(s[nt][0], s[nt][1]));
-            mx_hi = fmaxf(mx_hi, fmaxf(s[nt][2], s[nt][3]));
+        int slot[C::kTilePieces];
+        // prologue: tiles 0 .. kStages - 2 (the first group also holds q)
+#pragma unroll 1
+        for (int s = 0; s < C::kStages - 1; ++s) {
+            if (s < n_tiles) {
+                load_tile_slots<D, G>(a, un, t0 + s, pt, slot);
+                issue_tile<D, G>(a, un, base, s, pt, slot);
+            }
+            cp_async_commit();
         }
-#pragma unroll
-        for (int off = 1; off < 4; off <<= 1) {
-            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(kFullMask, mx_lo, off));
-            mx_hi = fmaxf(mx_hi, __shfl_xor_sync(kFullMask, mx_hi, off));
+        if (C::kStages - 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + C::kStages - 1, pt, slot);
+        bool ok = true;
+        for (int n = 0; n < n_tiles && ok; ++n) {
+            // tile n has landed (later groups may still be in flight): hand it to the
+            // tensor core (generic-proxy writes, read by the async proxy)
+            cp_async_wait<C::kStages - 2>();
+            tc::fence_proxy_async_smem();
+            mbar_arrive(kv_full(n % C::kStages));
+            // refill the stage of tile n - 1 with tile n + kStages - 1 once P V of
+            // tile n - 1 has read it
+            const int ahead = n + C::kStages - 1;
+            if (ahead < n_tiles) {
+                const int st = ahead % C::kStages;
+                ok = pf_wait(kv_empty(st), uint32_t((ahead / C::kStages - 1) & 1), a.status, abort_flag);
+                if (ok) {
+                    issue_tile<D, G>(a, un, base, st, pt, slot);
+                    if (ahead + 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + ahead + 1, pt, slot);
+                }
+            }
+            cp_async_commit();
         }
-        // every row sees the range's first entry (kv_lo <= pos0), so the maxima are
-        // finite from the range's first tile on
-        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-        const float al_lo = ex2(m_lo - mn_lo), al_hi = ex2(m_hi - mn_hi);
-        m_lo = mn_lo;
-        m_hi = mn_hi;
-        float sum_lo = 0.f, sum_hi = 0.f;
-        uint32_t pa[C::kNT / 2][4];
+        cp_async_wait<0>();  // nothing may still write this CTA's shared memory at exit
+    } else if (warp == kPfMmaWarp) {
+        // ================= MMA issuer (one thread) =================
+        if (lane == 0) {
+            const uint32_t o_tmem = tmem + uint32_t(kPfOCol);
+            bool ok = true;
+            const auto pv = [&](int n) {  // O (+)= P V of tile n
+                ok = ok && pf_wait(p_full, uint32_t(n & 1), a.status, abort_flag);
+                if (!ok) return;
+                tc::fence_after_sync();
+                const uint32_t sv = base + C::kVOff + (n % C::kStages) * C::kKvBytes;
 #pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) {
-            const float p0 = ex2(s[nt][0] - mn_lo), p1 = ex2(s[nt][1] - mn_lo);
-            const float p2 = ex2(s[nt][2] - mn_hi), p3 = ex2(s[nt][3] - mn_hi);
-            sum_lo += p0 + p1;
-            sum_hi += p2 + p3;
-            // S accumulators of column tiles 2k, 2k+1 form the A operand of k-step k
-            pa[nt >> 1][(nt & 1) * 2] = pack_bf16x2(p0, p1);
-            pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
-        }
-        l_lo = fmaf(l_lo, al_lo, sum_lo);
-        l_hi = fmaf(l_hi, al_hi, sum_hi);
+                for (int ks = 0; ks < kPfKvTile / 16; ++ks)
+                    tc::mma_bf16_ss(o_tmem, tc::sdesc_sw128(base + C::kPOff + ks * 32, 16, 1024),
+                                    tc::sdesc_sw128(sv + ks * 16 * 128, C::kKvPanel, 1024), C::kIdescO,
+                                    n > 0 || ks > 0);
+                tc::commit(o_done);
+                tc::commit(kv_empty(n % C::kStages));
+            };
+            for (int n = 0; n < n_tiles && ok; ++n) {
+                const int b = n & 1;
+                ok = pf_wait(kv_full(n % C::kStages), uint32_t((n / C::kStages) & 1), a.status, abort_flag);
+                if (ok && n >= 2) ok = pf_wait(s_empty(b), uint32_t((n / 2 - 1) & 1), a.status, abort_flag);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const uint32_t sk = base + C::kKOff + (n % C::kStages) * C::kKvBytes;
 #pragma unroll
-        for (int dt = 0; dt < C::kDT; ++dt) {
-            o[dt][0] *= al_lo;
-            o[dt][1] *= al_lo;
-            o[dt][2] *= al_hi;
-            o[dt][3] *= al_hi;
-        }
-        // O += P V
-#pragma unroll
-        for (int kk = 0; kk < C::kNT / 2; ++kk) {
-#pragma unroll
-            for (int dp = 0; dp < C::kDT / 2; ++dp) {
-                uint32_t vb[4];
-                ldsm_x4_trans(sv + v_off + (16 * kk * C::kPitch + 16 * dp) * 2, vb);
-                mma_bf16(o[2 * dp], pa[kk], vb[0], vb[1]);
-                mma_bf16(o[2 * dp + 1], pa[kk], vb[2], vb[3]);
+                for (int ks = 0; ks < D / 16; ++ks)
+                    tc::mma_bf16_ss(tmem + uint32_t(b * kPfKvTile),
+                                    tc::sdesc_sw128(base + C::kQOff + (ks >> 2) * C::kQPanel + (ks & 3) * 32, 16, 1024),
+                                    tc::sdesc_sw128(sk + (ks >> 2) * C::kKvPanel + (ks & 3) * 32, 16, 1024),
+                                    C::kIdescS, ks > 0);
+                tc::commit(s_full(b));
+                if (n >= 1) pv(n - 1);
+            }
+            if (ok && n_tiles > 0) pv(n_tiles - 1);
+            // every MMA issued has completed before the CTA frees TMEM and exits (this
+            // wait does not stop early for another role's failure)
+            tc::commit(drain);
+            const unsigned long long t_drain = pf_global_ns();
+            while (!mbar_try_wait(drain, 0u) && pf_global_ns() - t_drain < kPfWaitNs) {
             }
         }
-        __syncthreads();  // the stage is read before the next iteration refills it
-    }
-    cp_async_wait<0>();
-
-    // ---- epilogue: rows lo / hi of this lane
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-        l_lo += __shfl_xor_sync(kFullMask, l_lo, off);
-        l_hi += __shfl_xor_sync(kFullMask, l_hi, off);
-    }
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int r = half ? r_hi : r_lo;
+        __syncwarp();
+    } else {
+        // ================= softmax: thread = query row =================
+        const int r = tid;                       // TMEM lane and query row
         const int t = r / G, h = r % G;
-        if (t >= un.n_q) continue;
-        const float lt = half ? l_hi : l_lo;
-        const float inv = 1.f / lt;
-        const float lse2 = (half ? m_hi : m_lo) + __log2f(lt);
-        if (un.part >= 0) {  // a piece of a split range: fp32 partial result
-            const int64_t wrow = int64_t(un.part) * kPfRows + r;
-            float* dst = a.ws_o + wrow * D + 2 * t4;
+        const int qpos = un.pos0 + t;
+        const uint32_t lane_base = uint32_t(32 * warp) << 16;
+        const float sl2 = a.scale_log2;
+        float m = neg_inf(), l = 0.f;
+        bool ok = true;
+        for (int n = 0; n < n_tiles; ++n) {
+            const int b = n & 1;
+            ok = pf_wait(s_full(b), uint32_t((n / 2) & 1), a.status, abort_flag);
+            if (!__all_sync(kFullMask, ok)) { ok = false; break; }
+            tc::fence_after_sync();
+            float x[kPfKvTile];
 #pragma unroll
-            for (int dt = 0; dt < C::kDT; ++dt)
-                *reinterpret_cast<float2*>(dst + 8 * dt) =
-                    make_float2(o[dt][2 * half] * inv, o[dt][2 * half + 1] * inv);
-            if (t4 == 0) a.ws_lse[wrow] = lse2;
-            continue;
+            for (int c = 0; c < kPfKvTile / 32; ++c) {
+                uint32_t v[32];
+                tc::tmem_ld32(tmem + lane_base + uint32_t(b * kPfKvTile + 32 * c), v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(v[i]);
+            }
+            tc::fence_before_sync();
+            mbar_arrive(s_empty(b));  // S buffer b may be overwritten
+            // causal mask: entry e is seen by this row iff e <= qpos and e < kv_hi
+            const int e0 = (t0 + n) * kPfKvTile;
+            const int lim = min(qpos + 1, un.kv_hi) - e0;  // entries 0 .. lim - 1 seen
+            float mx = neg_inf();
+#pragma unroll
+            for (int i = 0; i < kPfKvTile; ++i) {
+                x[i] = i < lim ? x[i] * sl2 : neg_inf();
+                mx = fmaxf(mx, x[i]);
+            }
+            // running maximum: moves when a row's maximum grows by more than 2^8 (the
+            // first tile always sets it: every row sees entry kv_lo)
+            const bool grow = mx > m + kRescaleLog2;
+            const float m_new = grow ? mx : m;
+            const float alpha = grow ? ex2(m - m_new) : 1.f;  // 0 on the first tile
+            m = m_new;
+            float sum = 0.f;
+            uint32_t pk[kPfKvTile / 2];
+#pragma unroll
+            for (int i = 0; i < kPfKvTile; i += 2) {
+                const float p0 = ex2(x[i] - m), p1 = ex2(x[i + 1] - m);
+                sum += p0 + p1;
+                pk[i / 2] = pack_bf16x2(p0, p1);
+            }
+            l = fmaf(l, alpha, sum);
+            // P V of the previous tile has finished: its O may be rescaled and P rewritten
+            if (n > 0) {
+                ok = pf_wait(o_done, uint32_t((n - 1) & 1), a.status, abort_flag);
+                if (!__all_sync(kFullMask, ok)) { ok = false; break; }
+                tc::fence_after_sync();
+                if (__any_sync(kFullMask, grow)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        const uint32_t ta = tmem + lane_base + uint32_t(kPfOCol + 32 * c);
+                        tc::tmem_ld32(ta, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tc::tmem_st32(ta, v);
+                    }
+                    tc::tmem_st_wait();
+                }
+            }
+            // P (bf16) into the swizzled K-major operand, row r
+#pragma unroll
+            for (int c = 0; c < kPfKvTile / 8; ++c) {
+                const uint4 v4 = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                *reinterpret_cast<uint4*>(smem + C::kPOff + sw128_off(r, c, kPfRows)) = v4;
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(p_full);
         }
-        const int64_t row = int64_t(un.q_row0 + t) * a.n_qo_heads + un.g * G + h;
-        __nv_bfloat16* dst = out + row * D + 2 * t4;
+        // ---- epilogue: O of the last tile, divided by the row sum
+        if (ok && n_tiles > 0) {
+            ok = pf_wait(o_done, uint32_t((n_tiles - 1) & 1), a.status, abort_flag);
+            ok = __all_sync(kFullMask, ok);
+        }
+        if (ok && n_tiles > 0) {
+            tc::fence_after_sync();
+            const bool store = t < un.n_q;
+            const float inv = 1.f / l;
+            const float lse2 = m + __log2f(l);
+            const int64_t row = int64_t(un.q_row0 + t) * a.n_qo_heads + un.g * G + h;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tc::tmem_ld32(tmem + lane_base + uint32_t(kPfOCol + 32 * c), v);
+                if (!store) continue;
+                if (un.part >= 0) {  // a piece of a split range: fp32 partial result
+                    float4* dst = reinterpret_cast<float4*>(
+                        a.ws_o + (int64_t(un.part) * kPfRows + r) * D + 32 * c);
 #pragma unroll
-        for (int dt = 0; dt < C::kDT; ++dt)
-            *reinterpret_cast<uint32_t*>(dst + 8 * dt) =
-                pack_bf16x2(o[dt][2 * half] * inv, o[dt][2 * half + 1] * inv);
-        if (a.lse != nullptr && t4 == 0) a.lse[row] = lse2 * kLn2;
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
+                                             __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * D + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
+                                            pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
+                                            pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
+                                            pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
+                }
+            }
+            if (store) {
+                if (un.part >= 0) a.ws_lse[int64_t(un.part) * kPfRows + r] = lse2;
+                else if (a.lse != nullptr) a.lse[row] = lse2 * kLn2;
+            }
+        }
+    }
+    // every role is done with TMEM (and the MMAs have drained): free it
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kPfMmaWarp) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kPfTmemCols);
     }
 }
 
-// Log-sum-exp merge of split units: one warp per (merge record, row of its 64),
+// Log-sum-exp merge of split units: one warp per (merge record, row of its 128),
 // lanes over head_dim, every piece's loads issued before any is used:
 //     lse = log2 sum_c 2^lse_c,   out = sum_c 2^(lse_c - lse) out_c
 constexpr int kPfMergeWarps = 4;
@@ -567,10 +707,10 @@ struct pkv_prefill_plan {
     int max_batch = 0;
     int64_t max_q_tokens = 0;
     int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0;
-    int tile_tokens = 0;  // query tokens per unit: 64 / G
+    int tile_tokens = 0;  // query tokens per unit: 128 / G
     int max_units = 0;    // capacity of the unit list (tiles plus split pieces)
     int split_target = 0; // a step with fewer tile units than this splits long ranges
-    int max_blocks = 0;   // workspace blocks of 64 rows (pieces of split units)
+    int max_blocks = 0;   // workspace blocks of 128 rows (pieces of split units)
     int max_merges = 0;
     pkv::PfUnit* host_units = nullptr;  // pinned staging
     pkv::PfUnit* dev_units = nullptr;
@@ -578,6 +718,7 @@ struct pkv_prefill_plan {
     pkv::PfMerge* dev_merges = nullptr;
     float* ws_o = nullptr;
     float* ws_lse = nullptr;
+    int* dev_status = nullptr;  // nonzero: a bounded wait of some CTA expired
     int n_merges = 0;
     cudaEvent_t copy_done = nullptr;
     bool copy_pending = false;
@@ -645,6 +786,8 @@ int paged_prefill_plan_create(pkv_prefill_plan** out_plan, int max_batch, int64_
         e = cudaMalloc(reinterpret_cast<void**>(&p->dev_merges), sizeof(PfMerge) * size_t(p->max_merges));
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_o), sizeof(float) * rows * head_dim);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_lse), sizeof(float) * rows);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->dev_status), sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(p->dev_status, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->copy_done, cudaEventDisableTiming);
     if (e != cudaSuccess) {
         paged_prefill_plan_destroy(p);
@@ -669,6 +812,7 @@ void paged_prefill_plan_destroy(pkv_prefill_plan* p) {
     if (p->dev_merges) cudaFree(p->dev_merges);
     if (p->ws_o) cudaFree(p->ws_o);
     if (p->ws_lse) cudaFree(p->ws_lse);
+    if (p->dev_status) cudaFree(p->dev_status);
     if (prev >= 0) cudaSetDevice(prev);
     delete p;
 }
@@ -741,6 +885,17 @@ int paged_prefill_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_ind
     return PKV_OK;
 }
 
+int paged_prefill_plan_status(pkv_prefill_plan* p, int* status) {
+    clear_error();
+    if (!p || !status) return fail(PKV_ERR_INVALID_ARG, "paged_prefill_plan_status: NULL argument");
+    int v = 0;
+    cudaError_t e = cudaMemcpy(&v, p->dev_status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && v != 0) e = cudaMemset(p->dev_status, 0, sizeof v);
+    if (e != cudaSuccess) return pf_cuda_fail(e, "paged_prefill_plan_status: read");
+    *status = v;
+    return PKV_OK;
+}
+
 int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
                        const int32_t* qo_indptr, const int32_t* kv_indptr,
                        const int32_t* kv_indices, int batch, int n_qo_heads, int n_kv_heads,
@@ -787,6 +942,7 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
     a.ws_lse = p->ws_lse;
     a.merges = p->dev_merges;
     a.n_merges = p->n_merges;
+    a.status = p->dev_status;
     const cudaError_t e = prefill_dispatch<PfLaunchFn>(head_dim, n_qo_heads / n_kv_heads, a,
                                                        p->n_units, stream);
     if (e != cudaSuccess) return pf_cuda_fail(e, "paged_prefill_attn: launch");

@@ -294,7 +294,7 @@ def check_prefill_plan(qo, kv, hq, hkv, plan, split_target):
     partition their range at ring-tile cuts at or below the first query's position."""
     qo, kv = np.asarray(qo, np.int64), np.asarray(kv, np.int64)
     G = hq // hkv
-    tile = 64 // G
+    tile = 128 // G
     units, merges = plan["units"], plan["merges"]
     covered = np.zeros((int(qo[-1]), hkv), np.int32)
     req_of_row = np.repeat(np.arange(len(qo) - 1), np.diff(qo))
@@ -323,7 +323,7 @@ def check_prefill_plan(qo, kv, hq, hkv, plan, split_target):
         ranges = sorted((p[4], p[5]) for p in pieces)
         assert ranges[0][0] == 0 and ranges[-1][1] == pos0 + n_q
         for (lo, hi), (lo2, _) in zip(ranges, ranges[1:]):
-            assert hi == lo2 and hi % 32 == 0 and hi <= pos0, "cut on a tile edge at or below pos0"
+            assert hi == lo2 and hi % 64 == 0 and hi <= pos0, "cut on a tile edge at or below pos0"
         covered[q_row0:q_row0 + n_q, g] += 1
     assert np.all(covered == 1)
     n_tile_units = sum(-(-int(qo[b + 1] - qo[b]) // tile) for b in range(len(qo) - 1)) * hkv
