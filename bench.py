@@ -515,6 +515,8 @@ def run_prefill_bench(args):
         st.run(events)
     torch.cuda.synchronize()
     attn_ms = float(np.mean([a.elapsed_time(b) for a, b in events]))
+    if st.plan.status() != 0:
+        raise RuntimeError("a prefill pipeline wait exceeded its bound: the timed results are invalid")
     peak, peak_kind = measured_tensor_peak()
     step_tflops = flops_layer * pw.layers / (ms * 1e-3) / 1e12
     cpu = None if args.no_cpu_baseline else prefill_cpu_baseline(pw, args.cpu_budget)
@@ -532,7 +534,7 @@ def run_prefill_bench(args):
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak,
                      "unit": "TFLOP/s", "frac": attn_tflops / peak, "traffic": None,
                      "kernel": f"paged_prefill_attn, avg of {len(events)} event-timed eager "
-                               f"calls {attn_ms * 1e3:.1f} us, mma.sync m16n8k16",
+                               f"calls {attn_ms * 1e3:.1f} us, tcgen05.mma with TMEM accumulators",
                      "peak_kind": peak_kind},
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
@@ -719,6 +721,8 @@ def main(argv=None):
         st.run(attn_events)
     torch.cuda.synchronize()
     attn_ms = [a.elapsed_time(b) for a, b in attn_events]
+    if st.plan.status() != 0:
+        raise RuntimeError("a decode pipeline wait exceeded its bound: the timed results are invalid")
 
     # end to end through the public API, host buffers in and out
     io = HostIO(st)

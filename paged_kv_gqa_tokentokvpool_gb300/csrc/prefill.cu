@@ -55,12 +55,14 @@ namespace {
 using namespace ptx;
 
 constexpr int kPfRows = 128;                // query rows (token, head) per unit: the MMA's M
-constexpr int kPfKvTile = 64;               // KV tokens per ring stage: N of S, K of P V
+constexpr int kPfKvTile = 128;              // planning granularity of KV ranges (split cuts)
 constexpr int kPfSoftmaxWarps = 4;          // one thread per query row (TMEM lane)
 constexpr int kPfProducerWarps = 4;
 constexpr int kPfProducerThreads = 32 * kPfProducerWarps;
+constexpr int kPfHalfThreads = kPfProducerThreads / 2;  // K rows by one half, V rows by the other
 constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfProducerWarps;  // also owns the TMEM allocation
-constexpr int kPfThreads = 32 * (kPfMmaWarp + 1);
+constexpr int kPfRelayWarp = kPfMmaWarp + 1;
+constexpr int kPfThreads = 32 * (kPfRelayWarp + 1);
 constexpr uint32_t kPfTmemCols = 512;
 constexpr int kPfOCol = 256;                // TMEM columns: S buffers at 0 and 64, O from 256
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -112,33 +114,40 @@ struct PfArgs {
 // ((c ^ (n % 8)) * 16).
 template <int D, int G>
 struct PfCfg {
-    static constexpr int kStages = D == 128 ? 4 : 2;
+    // KV tokens per ring stage: the N of S and the K of P V. Each tcgen05.mma costs
+    // its issuing thread about as much time as a 128 x 128 x 16 step takes the
+    // tensor core, so the MMAs are made as large as shared memory allows.
+    static constexpr int kKv = D == 128 ? 128 : 64;
+    static constexpr int kStages = 2;
     static constexpr int kPanels = D / 64;
     static constexpr int kQPanel = kPfRows * 128;           // bytes of one q panel
-    static constexpr int kKvPanel = kPfKvTile * 128;        // bytes of one K (or V) panel
+    static constexpr int kKvPanel = kKv * 128;              // bytes of one K (or V) panel
     static constexpr int kQBytes = kPanels * kQPanel;
     static constexpr int kKvBytes = kPanels * kKvPanel;     // K (or V) of one stage
-    static constexpr int kPBytes = kPfRows * kPfKvTile * 2; // one panel
+    static constexpr int kPQPanel = kPfRows * 128;          // bytes of one P panel
+    static constexpr int kPBytes = kPfRows * kKv * 2;       // one P buffer: kKv / 64 panels
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKvBytes;
     static constexpr int kPOff = kVOff + kStages * kKvBytes;
-    static constexpr int kBarOff = kPOff + kPBytes;
-    // mbarriers: kv_full[kStages], kv_empty[kStages], s_full[2], s_empty[2], p_full,
-    // o_done, drain; then the TMEM address and the abort flag
-    static constexpr int kNumBars = 2 * kStages + 7;
+    static constexpr int kBarOff = kPOff + 2 * kPBytes;       // two P buffers
+    // mbarriers: for K and for V rings each landed / full / empty [kStages];
+    // s_full[2], s_empty[2], p_full[2], o_done[2], drain; then the TMEM address and
+    // the abort flag
+    static constexpr int kNumBars = 6 * kStages + 9;
     static constexpr int kTmemOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemOff + 4;
     static constexpr int kSmem = kAbortOff + 4 + 1024;      // + slack to align the base
     static constexpr int kChunks = D / 8;                   // 16-byte pieces per row
-    static constexpr int kTilePieces = kPfKvTile * kChunks / kPfProducerThreads;
-    static constexpr int kQPieces = kPfRows * kChunks / kPfProducerThreads;
-    static constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kPfRows, kPfKvTile, false, false);
+    static constexpr int kTilePieces = kKv * kChunks / kPfHalfThreads;   // per thread, K or V
+    static constexpr int kQPieces = kPfRows * kChunks / kPfHalfThreads;   // q, by the K half
+    static constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kPfRows, kKv, false, false);
     static constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kPfRows, D, false, true);
-    static_assert(kTilePieces * kPfProducerThreads == kPfKvTile * kChunks, "ring pieces");
-    static_assert(kQPieces * kPfProducerThreads == kPfRows * kChunks, "q pieces");
+    static_assert(kTilePieces * kPfHalfThreads == kKv * kChunks, "ring pieces");
+    static_assert(kPfKvTile % kKv == 0, "split cuts fall on ring tiles");
+    static_assert(kQPieces * kPfHalfThreads == kPfRows * kChunks, "q pieces");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-    static_assert(2 * kPfKvTile <= kPfOCol && kPfOCol + D <= int(kPfTmemCols), "TMEM columns");
+    static_assert(2 * kKv <= kPfOCol && kPfOCol + D <= int(kPfTmemCols), "TMEM columns");
 };
 
 // Byte offset of 16-byte chunk c of row n in a panel-major swizzled operand whose
@@ -170,38 +179,53 @@ __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, int* stat
     }
 }
 
+// Non-blocking test of the phase of `bar` with the given parity.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// One arrival on `bar` once every cp.async this thread issued before has completed
+// (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Slot ids of the rows this producer thread copies for KV tile `tile` (-1 past
-// the range): piece i is token (pt + i * kPfProducerThreads) / kChunks.
+// the range): piece i is token (pt + i * kPfHalfThreads) / kChunks.
 template <int D, int G>
 __device__ __forceinline__ void load_tile_slots(const PfArgs& a, const PfUnit& un, int tile, int pt,
                                                 int (&slot)[PfCfg<D, G>::kTilePieces]) {
     using C = PfCfg<D, G>;
 #pragma unroll
     for (int i = 0; i < C::kTilePieces; ++i) {
-        const int tok = (pt + i * kPfProducerThreads) / C::kChunks;
-        const int j = tile * kPfKvTile + tok;
+        const int tok = (pt + i * kPfHalfThreads) / C::kChunks;
+        const int j = tile * C::kKv + tok;
         slot[i] = j < un.kv_hi ? __ldg(a.kv_indices + un.kv_begin + j) : -1;
     }
 }
 
-// cp.async of this thread's pieces of a K/V tile into stage `st` (zero past the range).
+// cp.async of this thread's pieces of a K (or V) tile from `pool` into the stage at
+// shared address `dst` (zero past the range).
 template <int D, int G>
-__device__ __forceinline__ void issue_tile(const PfArgs& a, const PfUnit& un, uint32_t base, int st,
-                                           int pt, const int (&slot)[PfCfg<D, G>::kTilePieces]) {
+__device__ __forceinline__ void issue_tile(const PfArgs& a, const PfUnit& un, const __nv_bfloat16* pool,
+                                           uint32_t dst, int pt,
+                                           const int (&slot)[PfCfg<D, G>::kTilePieces]) {
     using C = PfCfg<D, G>;
-    const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_pool);
-    const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_pool);
-    const uint32_t sk = base + C::kKOff + st * C::kKvBytes;
-    const uint32_t sv = base + C::kVOff + st * C::kKvBytes;
 #pragma unroll
     for (int i = 0; i < C::kTilePieces; ++i) {
-        const int c = pt + i * kPfProducerThreads;
+        const int c = pt + i * kPfHalfThreads;
         const int tok = c / C::kChunks, part = c % C::kChunks;
         const bool valid = slot[i] >= 0;
         const int64_t off = (int64_t(valid ? slot[i] : 0) * a.n_kv_heads + un.g) * D + part * 8;
-        const uint32_t so = sw128_off(tok, part, kPfKvTile);
-        cp_async16(sk + so, kp + off, valid);
-        cp_async16(sv + so, vp + off, valid);
+        cp_async16(dst + sw128_off(tok, part, C::kKv), pool + off, valid);
     }
 }
 
@@ -214,27 +238,38 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw);
     const uint32_t bars = base + C::kBarOff;
-    const auto kv_full = [&](int s) { return bars + 8u * s; };
-    const auto kv_empty = [&](int s) { return bars + 8u * (C::kStages + s); };
-    const auto s_full = [&](int b) { return bars + 8u * (2 * C::kStages + b); };
-    const auto s_empty = [&](int b) { return bars + 8u * (2 * C::kStages + 2 + b); };
-    const uint32_t p_full = bars + 8u * (2 * C::kStages + 4);
-    const uint32_t o_done = bars + 8u * (2 * C::kStages + 5);
-    const uint32_t drain = bars + 8u * (2 * C::kStages + 6);
+    // ring barriers of K (v = 0) and V (v = 1): landed (the producers' copies are in
+    // shared memory), full (announced to the tensor core), empty (read by it)
+    const auto landed = [&](int v, int s) { return bars + 8u * ((0 + v) * C::kStages + s); };
+    const auto full = [&](int v, int s) { return bars + 8u * ((2 + v) * C::kStages + s); };
+    const auto empty = [&](int v, int s) { return bars + 8u * ((4 + v) * C::kStages + s); };
+    const uint32_t bars2 = bars + 8u * 6 * C::kStages;
+    const auto s_full = [&](int b) { return bars2 + 8u * b; };
+    const auto s_empty = [&](int b) { return bars2 + 8u * (2 + b); };
+    // P of tile n written / P V of tile n done: one barrier per P buffer (tiles of
+    // one parity), so that a barrier's next phase always waits for its reader to
+    // have seen the previous one
+    const auto p_full = [&](int n) { return bars2 + 8u * (4 + (n & 1)); };
+    const auto o_done = [&](int n) { return bars2 + 8u * (6 + (n & 1)); };
+    const uint32_t drain = bars2 + 8u * 8;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(kv_full(s), kPfProducerThreads);
-            mbar_init(kv_empty(s), 1);
-        }
+        for (int v = 0; v < 2; ++v)
+            for (int s = 0; s < C::kStages; ++s) {
+                mbar_init(landed(v, s), kPfHalfThreads);
+                mbar_init(full(v, s), 1);
+                mbar_init(empty(v, s), 1);
+            }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full(b), 1);
             mbar_init(s_empty(b), 32 * kPfSoftmaxWarps);
         }
-        mbar_init(p_full, 32 * kPfSoftmaxWarps);
-        mbar_init(o_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(p_full(b), 32 * kPfSoftmaxWarps);
+            mbar_init(o_done(b), 1);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -249,20 +284,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kTmemOff);
     pdl_launch_dependents();
     const PfUnit un = a.units[blockIdx.x];  // plan data
-    const int t0 = un.kv_lo / kPfKvTile;
-    const int n_tiles = (un.kv_hi + kPfKvTile - 1) / kPfKvTile - t0;
+    const int t0 = un.kv_lo / C::kKv;
+    const int n_tiles = (un.kv_hi + C::kKv - 1) / C::kKv - t0;
     // q, the pools and their indices may come from the previous kernel, and out may
     // still be read by it
     pdl_wait();
 
     if (warp >= kPfSoftmaxWarps && warp < kPfMmaWarp) {
         // ================= producers =================
-        const int pt = tid - 32 * kPfSoftmaxWarps;
-        {   // the unit's q rows (row r: token r / G, head r % G), with tile 0 below
+        // Two halves: one gathers K tiles (and the unit's q rows), the other V tiles.
+        // K tile n goes to K stage n % kStages once S of tile n - kStages has read it,
+        // V tile n once P V of tile n - kStages has, so the next K tiles are not held
+        // back by the P V products. Each thread's arrival on the stage's `landed`
+        // barrier is attached to its copies, so it completes the moment the rows are
+        // in shared memory; the relay warp then announces the stage to the tensor core.
+        const int half = (tid - 32 * kPfSoftmaxWarps) / kPfHalfThreads;  // 0: K, 1: V
+        const int pt = (tid - 32 * kPfSoftmaxWarps) % kPfHalfThreads;
+        if (half == 0) {   // the unit's q rows (row r: token r / G, head r % G), with K tile 0
             const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
 #pragma unroll 4
             for (int i = 0; i < C::kQPieces; ++i) {
-                const int c = pt + i * kPfProducerThreads;
+                const int c = pt + i * kPfHalfThreads;
                 const int r = c / C::kChunks, part = c % C::kChunks;
                 const int t = r / G, h = r % G;
                 const bool valid = t < un.n_q;
@@ -271,78 +313,118 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
                 cp_async16(base + C::kQOff + sw128_off(r, part, kPfRows), q + off, valid);
             }
         }
+        const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(half ? a.v_pool : a.k_pool);
+        const uint32_t ring = base + (half ? C::kVOff : C::kKOff);
         int slot[C::kTilePieces];
-        // prologue: tiles 0 .. kStages - 2 (the first group also holds q)
-#pragma unroll 1
-        for (int s = 0; s < C::kStages - 1; ++s) {
-            if (s < n_tiles) {
-                load_tile_slots<D, G>(a, un, t0 + s, pt, slot);
-                issue_tile<D, G>(a, un, base, s, pt, slot);
-            }
-            cp_async_commit();
-        }
-        if (C::kStages - 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + C::kStages - 1, pt, slot);
-        bool ok = true;
-        for (int n = 0; n < n_tiles && ok; ++n) {
-            // tile n has landed (later groups may still be in flight): hand it to the
-            // tensor core (generic-proxy writes, read by the async proxy)
-            cp_async_wait<C::kStages - 2>();
-            tc::fence_proxy_async_smem();
-            mbar_arrive(kv_full(n % C::kStages));
-            // refill the stage of tile n - 1 with tile n + kStages - 1 once P V of
-            // tile n - 1 has read it
-            const int ahead = n + C::kStages - 1;
-            if (ahead < n_tiles) {
-                const int st = ahead % C::kStages;
-                ok = pf_wait(kv_empty(st), uint32_t((ahead / C::kStages - 1) & 1), a.status, abort_flag);
-                if (ok) {
-                    issue_tile<D, G>(a, un, base, st, pt, slot);
-                    if (ahead + 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + ahead + 1, pt, slot);
-                }
-            }
-            cp_async_commit();
+        load_tile_slots<D, G>(a, un, t0, pt, slot);
+        for (int n = 0; n < n_tiles; ++n) {
+            const int st = n % C::kStages;
+            if (n >= C::kStages &&
+                !pf_wait(empty(half, st), uint32_t((n / C::kStages - 1) & 1), a.status, abort_flag))
+                break;
+            issue_tile<D, G>(a, un, pool, ring + st * C::kKvBytes, pt, slot);
+            cp_async_arrive(landed(half, st));
+            if (n + 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + n + 1, pt, slot);
         }
         cp_async_wait<0>();  // nothing may still write this CTA's shared memory at exit
     } else if (warp == kPfMmaWarp) {
         // ================= MMA issuer (one thread) =================
+        // Two streams of work, each issued as soon as its inputs are ready (polled,
+        // so that neither waits behind the other): S of tile ns once its K/V stage
+        // has landed and the softmax has read the S buffer's previous tile, and P V of
+        // tile npv once the softmax has written its P (and rescaled O).
         if (lane == 0) {
             const uint32_t o_tmem = tmem + uint32_t(kPfOCol);
-            bool ok = true;
-            const auto pv = [&](int n) {  // O (+)= P V of tile n
-                ok = ok && pf_wait(p_full, uint32_t(n & 1), a.status, abort_flag);
-                if (!ok) return;
-                tc::fence_after_sync();
-                const uint32_t sv = base + C::kVOff + (n % C::kStages) * C::kKvBytes;
+            int ns = 0, npv = 0;
+            unsigned idle = 0;
+            unsigned long long t_idle = pf_global_ns();
+            while (npv < n_tiles) {
+                bool progress = false;
+                if (ns < n_tiles && ns < npv + 2 &&
+                    mbar_test(full(0, ns % C::kStages), uint32_t((ns / C::kStages) & 1)) &&
+                    (ns < 2 || mbar_test(s_empty(ns & 1), uint32_t((ns / 2 - 1) & 1)))) {
+                    tc::fence_after_sync();
+                    const uint32_t sk = base + C::kKOff + (ns % C::kStages) * C::kKvBytes;
 #pragma unroll
-                for (int ks = 0; ks < kPfKvTile / 16; ++ks)
-                    tc::mma_bf16_ss(o_tmem, tc::sdesc_sw128(base + C::kPOff + ks * 32, 16, 1024),
-                                    tc::sdesc_sw128(sv + ks * 16 * 128, C::kKvPanel, 1024), C::kIdescO,
-                                    n > 0 || ks > 0);
-                tc::commit(o_done);
-                tc::commit(kv_empty(n % C::kStages));
-            };
-            for (int n = 0; n < n_tiles && ok; ++n) {
-                const int b = n & 1;
-                ok = pf_wait(kv_full(n % C::kStages), uint32_t((n / C::kStages) & 1), a.status, abort_flag);
-                if (ok && n >= 2) ok = pf_wait(s_empty(b), uint32_t((n / 2 - 1) & 1), a.status, abort_flag);
-                if (!ok) break;
-                tc::fence_after_sync();
-                const uint32_t sk = base + C::kKOff + (n % C::kStages) * C::kKvBytes;
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        tc::mma_bf16_ss(tmem + uint32_t((ns & 1) * C::kKv),
+                                        tc::sdesc_sw128(base + C::kQOff + (ks >> 2) * C::kQPanel + (ks & 3) * 32, 16, 1024),
+                                        tc::sdesc_sw128(sk + (ks >> 2) * C::kKvPanel + (ks & 3) * 32, 16, 1024),
+                                        C::kIdescS, ks > 0);
+                    tc::commit(s_full(ns & 1));
+                    tc::commit(empty(0, ns % C::kStages));
+                    ++ns;
+                    progress = true;
+                }
+                if (npv < ns && mbar_test(p_full(npv), uint32_t((npv >> 1) & 1)) &&
+                    mbar_test(full(1, npv % C::kStages), uint32_t((npv / C::kStages) & 1))) {
+                    tc::fence_after_sync();
+                    const uint32_t sv = base + C::kVOff + (npv % C::kStages) * C::kKvBytes;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    tc::mma_bf16_ss(tmem + uint32_t(b * kPfKvTile),
-                                    tc::sdesc_sw128(base + C::kQOff + (ks >> 2) * C::kQPanel + (ks & 3) * 32, 16, 1024),
-                                    tc::sdesc_sw128(sk + (ks >> 2) * C::kKvPanel + (ks & 3) * 32, 16, 1024),
-                                    C::kIdescS, ks > 0);
-                tc::commit(s_full(b));
-                if (n >= 1) pv(n - 1);
+                    for (int ks = 0; ks < C::kKv / 16; ++ks)
+                        tc::mma_bf16_ss(o_tmem,
+                                        tc::sdesc_sw128(base + C::kPOff + (npv & 1) * C::kPBytes +
+                                                            (ks >> 2) * C::kPQPanel + (ks & 3) * 32, 16, 1024),
+                                        tc::sdesc_sw128(sv + ks * 16 * 128, C::kKvPanel, 1024), C::kIdescO,
+                                        npv > 0 || ks > 0);
+                    tc::commit(o_done(npv));
+                    tc::commit(empty(1, npv % C::kStages));
+                    ++npv;
+                    progress = true;
+                }
+                if (progress) {
+                    idle = 0;
+                } else if (++idle % 256 == 0) {  // the clocks are read now and then only
+                    if (idle == 256) t_idle = pf_global_ns();
+                    if (*abort_flag) break;
+                    if (pf_global_ns() - t_idle > kPfWaitNs) {
+                        atomicOr(a.status, 1);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
             }
-            if (ok && n_tiles > 0) pv(n_tiles - 1);
             // every MMA issued has completed before the CTA frees TMEM and exits (this
             // wait does not stop early for another role's failure)
             tc::commit(drain);
             const unsigned long long t_drain = pf_global_ns();
             while (!mbar_try_wait(drain, 0u) && pf_global_ns() - t_drain < kPfWaitNs) {
+            }
+        }
+        __syncwarp();
+    } else if (warp == kPfRelayWarp) {
+        // ================= relay: landed stage -> tensor core =================
+        // The rows came by cp.async (generic proxy); the tensor core reads them
+        // through the async proxy. One thread orders the two (proxy fence) after each
+        // stage has landed, polling the K and V rings in turn (neither waits behind
+        // the other), so that neither the producers nor the MMA thread wait for it.
+        if (lane == 0) {
+            int nr[2] = {0, 0};
+            unsigned idle = 0;
+            unsigned long long t_idle = 0;
+            while (nr[0] < n_tiles || nr[1] < n_tiles) {
+                bool progress = false;
+#pragma unroll
+                for (int v = 0; v < 2; ++v) {
+                    const int n = nr[v];
+                    if (n < n_tiles && mbar_test(landed(v, n % C::kStages), uint32_t((n / C::kStages) & 1))) {
+                        tc::fence_proxy_async_smem();
+                        mbar_arrive(full(v, n % C::kStages));
+                        nr[v] = n + 1;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    idle = 0;
+                } else if (++idle % 256 == 0) {
+                    if (idle == 256) t_idle = pf_global_ns();
+                    if (*abort_flag) break;
+                    if (pf_global_ns() - t_idle > kPfWaitNs) {
+                        atomicOr(a.status, 1);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
             }
         }
         __syncwarp();
@@ -360,46 +442,69 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
             ok = pf_wait(s_full(b), uint32_t((n / 2) & 1), a.status, abort_flag);
             if (!__all_sync(kFullMask, ok)) { ok = false; break; }
             tc::fence_after_sync();
-            float x[kPfKvTile];
+            float x[C::kKv];
 #pragma unroll
-            for (int c = 0; c < kPfKvTile / 32; ++c) {
+            for (int c = 0; c < C::kKv / 32; ++c) {
                 uint32_t v[32];
-                tc::tmem_ld32(tmem + lane_base + uint32_t(b * kPfKvTile + 32 * c), v);
+                tc::tmem_ld32(tmem + lane_base + uint32_t(b * C::kKv + 32 * c), v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(v[i]);
             }
             tc::fence_before_sync();
             mbar_arrive(s_empty(b));  // S buffer b may be overwritten
             // causal mask: entry e is seen by this row iff e <= qpos and e < kv_hi
-            const int e0 = (t0 + n) * kPfKvTile;
+            // (raw scores; sm_scale > 0 is applied in the exponent below)
+            const int e0 = (t0 + n) * C::kKv;
             const int lim = min(qpos + 1, un.kv_hi) - e0;  // entries 0 .. lim - 1 seen
-            float mx = neg_inf();
+            if (lim < C::kKv) {
 #pragma unroll
-            for (int i = 0; i < kPfKvTile; ++i) {
-                x[i] = i < lim ? x[i] * sl2 : neg_inf();
-                mx = fmaxf(mx, x[i]);
+                for (int i = 0; i < C::kKv; ++i) x[i] = i < lim ? x[i] : neg_inf();
             }
-            // running maximum: moves when a row's maximum grows by more than 2^8 (the
-            // first tile always sets it: every row sees entry kv_lo)
+            float mx0 = x[0], mx1 = x[1];
+#pragma unroll
+            for (int i = 2; i < C::kKv; i += 2) {
+                mx0 = fmaxf(mx0, x[i]);
+                mx1 = fmaxf(mx1, x[i + 1]);
+            }
+            const float mx = fmaxf(mx0, mx1) * sl2;
+            // running maximum (base 2, scaled): moves when a row's maximum grows by more
+            // than 2^8 (the first tile always sets it: every row sees entry kv_lo)
             const bool grow = mx > m + kRescaleLog2;
             const float m_new = grow ? mx : m;
             const float alpha = grow ? ex2(m - m_new) : 1.f;  // 0 on the first tile
             m = m_new;
-            float sum = 0.f;
-            uint32_t pk[kPfKvTile / 2];
-#pragma unroll
-            for (int i = 0; i < kPfKvTile; i += 2) {
-                const float p0 = ex2(x[i] - m), p1 = ex2(x[i + 1] - m);
-                sum += p0 + p1;
-                pk[i / 2] = pack_bf16x2(p0, p1);
+            const float neg_m = -m;
+            // P buffer n & 1 was last read by P V of tile n - 2
+            if (n > 1) {
+                ok = pf_wait(o_done(n), uint32_t(((n - 2) >> 1) & 1), a.status, abort_flag);
+                if (!__all_sync(kFullMask, ok)) { ok = false; break; }
             }
-            l = fmaf(l, alpha, sum);
-            // P V of the previous tile has finished: its O may be rescaled and P rewritten
-            if (n > 0) {
-                ok = pf_wait(o_done, uint32_t((n - 1) & 1), a.status, abort_flag);
+            // P = 2^(s * scale - m) as bf16 into the swizzled K-major operand, row r,
+            // 8 entries (one 16-byte chunk) at a time
+            uint8_t* pbuf = smem + C::kPOff + (n & 1) * C::kPBytes;
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < C::kKv / 8; ++c) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float p0 = ex2(fmaf(x[8 * c + 2 * i], sl2, neg_m));
+                    const float p1 = ex2(fmaf(x[8 * c + 2 * i + 1], sl2, neg_m));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                *reinterpret_cast<uint4*>(pbuf + sw128_off(r, c, kPfRows)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            l = fmaf(l, alpha, sum0 + sum1);
+            // a row maximum moved: O (complete up to P V of tile n - 1) is rescaled
+            // before P V of tile n accumulates into it
+            if (n > 0 && __any_sync(kFullMask, grow)) {
+                ok = pf_wait(o_done(n - 1), uint32_t(((n - 1) >> 1) & 1), a.status, abort_flag);
                 if (!__all_sync(kFullMask, ok)) { ok = false; break; }
                 tc::fence_after_sync();
-                if (__any_sync(kFullMask, grow)) {
+                {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
@@ -412,19 +517,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
                     tc::tmem_st_wait();
                 }
             }
-            // P (bf16) into the swizzled K-major operand, row r
-#pragma unroll
-            for (int c = 0; c < kPfKvTile / 8; ++c) {
-                const uint4 v4 = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                *reinterpret_cast<uint4*>(smem + C::kPOff + sw128_off(r, c, kPfRows)) = v4;
-            }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
-            mbar_arrive(p_full);
+            mbar_arrive(p_full(n));
         }
         // ---- epilogue: O of the last tile, divided by the row sum
         if (ok && n_tiles > 0) {
-            ok = pf_wait(o_done, uint32_t((n_tiles - 1) & 1), a.status, abort_flag);
+            ok = pf_wait(o_done(n_tiles - 1), uint32_t(((n_tiles - 1) >> 1) & 1), a.status, abort_flag);
             ok = __all_sync(kFullMask, ok);
         }
         if (ok && n_tiles > 0) {

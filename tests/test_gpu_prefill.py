@@ -49,6 +49,7 @@ def run_prefill(pkv, pw, layer=0, debug=False):
     finally:
         pkv.pkv_set_debug_checks(False)
     torch.cuda.synchronize()
+    assert plan.status() == 0, "a pipeline wait of the prefill kernel expired"
     return out[:NQ], lse[:NQ], (q, kp, vp, kn, vn), (kp_d, vp_d)
 
 
@@ -111,6 +112,7 @@ def test_prefill_plan_reused_across_layers(pkv):
         torch.cuda.synchronize()
         ref_out, ref_lse = oracle_prefill(pw, (q, kp, vp, kn, vn))
         assert_parity(to_f64(out), ref_lse, ref_out, ref_lse, what=f"layer {layer}")
+    assert plan.status() == 0
 
 
 def test_prefill_rejects_bad_calls(pkv):
@@ -179,3 +181,47 @@ def test_prefill_full_size_sampled(pkv, config_no):
                                           pw.n_qo_heads, pw.n_kv_heads, pw.head_dim, pw.sm_scale)
             assert_parity(to_f64(out[q0 + c0:q0 + c1]), lse[q0 + c0:q0 + c1].cpu().numpy(),
                           ref_o, ref_l, what=f"prefill config {config_no} request {b} rows {c0}-{c1}")
+
+
+def test_prefill_graph_replay_steps(pkv):
+    """Several steps of back-to-back layers replayed from a CUDA graph, as the
+    benchmark runs them (64-token chunks over long contexts: split ranges and the
+    merge kernel): every layer's results equal the oracle's and no pipeline wait
+    expires."""
+    pw = workloads.prefill_workload([64, 64, 64], [9000, 3000, 700], layers=3, seed=31)
+    dev = torch.device("cuda")
+    plan = pkv.paged_prefill_plan_create(pw.batch, pw.total_q, 32, 8, 128)
+    qo = torch.from_numpy(pw.qo_indptr).to(dev)
+    kv = torch.from_numpy(pw.kv_indptr).to(dev)
+    idx = torch.from_numpy(pw.kv_indices).to(dev)
+    slots = torch.from_numpy(pw.chunk_slots).to(dev)
+    layers = [workloads.prefill_tensors(pw, l, poison_unreferenced=True) for l in range(3)]
+    dev_t = [tuple(x.to(dev) for x in t) for t in layers]
+    outs = [torch.empty(pw.total_q, 32, 128, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    lses = [torch.empty(pw.total_q, 32, dtype=torch.float32, device=dev) for _ in range(3)]
+
+    def step_layers():
+        for (q, kp, vp, kn, vn), o, l in zip(dev_t, outs, lses):
+            pkv.kvpool_append(kp, vp, slots, kn, vn)
+            pkv.paged_prefill_attn(q, kp, vp, qo, kv, idx, pw.batch, 32, 8, 128, pw.sm_scale, o,
+                                   l, plan)
+
+    pkv.paged_prefill_plan(plan, pw.qo_indptr, pw.kv_indptr)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step_layers()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step_layers()
+    for _ in range(4):
+        pkv.paged_prefill_plan(plan, pw.qo_indptr, pw.kv_indptr)
+        g.replay()
+    torch.cuda.synchronize()
+    assert plan.status() == 0, "a pipeline wait of the prefill kernel expired"
+    for layer in range(3):
+        ref_out, ref_lse = oracle_prefill(pw, layers[layer])
+        assert_parity(to_f64(outs[layer]), lses[layer].cpu().numpy(), ref_out, ref_lse,
+                      what=f"graph layer {layer}")
