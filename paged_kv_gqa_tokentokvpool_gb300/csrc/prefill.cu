@@ -64,7 +64,7 @@ constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfProducerWarps;  // also owns the
 constexpr int kPfRelayWarp = kPfMmaWarp + 1;
 constexpr int kPfThreads = 32 * (kPfRelayWarp + 1);
 constexpr uint32_t kPfTmemCols = 512;
-constexpr int kPfOCol = 256;                // TMEM columns: S buffers at 0 and 64, O from 256
+constexpr int kPfOCol = 256;                // TMEM columns of O: 256 .. 256 + head_dim
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -118,19 +118,19 @@ struct PfCfg {
     // its issuing thread about as much time as a 128 x 128 x 16 step takes the
     // tensor core, so the MMAs are made as large as shared memory allows.
     static constexpr int kKv = D == 128 ? 128 : 64;
-    static constexpr int kStages = 2;
+    static constexpr int kStages = D == 128 ? 3 : 2;
+    // TMEM columns: S buffers at 0 and kKv (fp32), O at kPfOCol, and two P buffers
+    // of kKv / 2 columns (bf16 pairs) at kPCol, the A operand of P V
+    static constexpr int kPCol = D == 128 ? kPfOCol + D : 2 * kKv;
     static constexpr int kPanels = D / 64;
     static constexpr int kQPanel = kPfRows * 128;           // bytes of one q panel
     static constexpr int kKvPanel = kKv * 128;              // bytes of one K (or V) panel
     static constexpr int kQBytes = kPanels * kQPanel;
     static constexpr int kKvBytes = kPanels * kKvPanel;     // K (or V) of one stage
-    static constexpr int kPQPanel = kPfRows * 128;          // bytes of one P panel
-    static constexpr int kPBytes = kPfRows * kKv * 2;       // one P buffer: kKv / 64 panels
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKvBytes;
-    static constexpr int kPOff = kVOff + kStages * kKvBytes;
-    static constexpr int kBarOff = kPOff + 2 * kPBytes;       // two P buffers
+    static constexpr int kBarOff = kVOff + kStages * kKvBytes;
     // mbarriers: for K and for V rings each landed / full / empty [kStages];
     // s_full[2], s_empty[2], p_full[2], o_done[2], drain; then the TMEM address and
     // the abort flag
@@ -148,6 +148,8 @@ struct PfCfg {
     static_assert(kQPieces * kPfHalfThreads == kPfRows * kChunks, "q pieces");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static_assert(2 * kKv <= kPfOCol && kPfOCol + D <= int(kPfTmemCols), "TMEM columns");
+    static_assert(kPCol + kKv <= int(kPfTmemCols) && (kPCol >= kPfOCol + D || kPCol + kKv <= kPfOCol),
+                  "P columns");
 };
 
 // Byte offset of 16-byte chunk c of row n in a panel-major swizzled operand whose
@@ -328,65 +330,82 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
         }
         cp_async_wait<0>();  // nothing may still write this CTA's shared memory at exit
     } else if (warp == kPfMmaWarp) {
-        // ================= MMA issuer (one thread) =================
+        // ================= MMA issuer (one warp, one lane issues) =================
         // Two streams of work, each issued as soon as its inputs are ready (polled,
-        // so that neither waits behind the other): S of tile ns once its K/V stage
-        // has landed and the softmax has read the S buffer's previous tile, and P V of
-        // tile npv once the softmax has written its P (and rescaled O).
-        if (lane == 0) {
-            const uint32_t o_tmem = tmem + uint32_t(kPfOCol);
-            int ns = 0, npv = 0;
-            unsigned idle = 0;
-            unsigned long long t_idle = pf_global_ns();
-            while (npv < n_tiles) {
-                bool progress = false;
-                if (ns < n_tiles && ns < npv + 2 &&
-                    mbar_test(full(0, ns % C::kStages), uint32_t((ns / C::kStages) & 1)) &&
-                    (ns < 2 || mbar_test(s_empty(ns & 1), uint32_t((ns / 2 - 1) & 1)))) {
-                    tc::fence_after_sync();
-                    const uint32_t sk = base + C::kKOff + (ns % C::kStages) * C::kKvBytes;
+        // so that neither waits behind the other): S of tile ns once its K stage has
+        // been announced and the softmax has read the S buffer's previous tile (so S
+        // runs up to two tiles ahead of the softmax), and
+        // P V of tile npv once its P is in TMEM (and O rescaled) and its V stage has
+        // been announced. The whole warp runs the loop with lane 0's view of the
+        // barriers, so the descriptors stay warp-uniform; lane 0 alone issues.
+        const bool leader = lane == 0;
+        const uint32_t o_tmem = tmem + uint32_t(kPfOCol);
+        const uint64_t q_desc = tc::sdesc_sw128(base + C::kQOff, 16, 1024);
+        const uint64_t k_desc = tc::sdesc_sw128(base + C::kKOff, 16, 1024);
+        const uint64_t v_desc = tc::sdesc_sw128(base + C::kVOff, C::kKvPanel, 1024);
+        int ns = 0, npv = 0;
+        unsigned idle = 0;
+        unsigned long long t_idle = 0;
+        while (npv < n_tiles) {
+            bool progress = false;
+            bool go = false;
+            if (leader && ns < n_tiles)
+                go = mbar_test(full(0, ns % C::kStages), uint32_t((ns / C::kStages) & 1)) &&
+                     (ns < 2 || mbar_test(s_empty(ns & 1), uint32_t((ns / 2 - 1) & 1)));
+            if (__shfl_sync(kFullMask, go, 0)) {
+                tc::fence_after_sync();
+                // descriptor start addresses advance in 16-byte units (low bits)
+                const uint64_t kd = k_desc + uint64_t(((ns % C::kStages) * C::kKvBytes) >> 4);
+                const uint32_t s_tmem = tmem + uint32_t((ns & 1) * C::kKv);
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        tc::mma_bf16_ss(tmem + uint32_t((ns & 1) * C::kKv),
-                                        tc::sdesc_sw128(base + C::kQOff + (ks >> 2) * C::kQPanel + (ks & 3) * 32, 16, 1024),
-                                        tc::sdesc_sw128(sk + (ks >> 2) * C::kKvPanel + (ks & 3) * 32, 16, 1024),
-                                        C::kIdescS, ks > 0);
-                    tc::commit(s_full(ns & 1));
-                    tc::commit(empty(0, ns % C::kStages));
-                    ++ns;
-                    progress = true;
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = uint32_t(((ks >> 2) * C::kQPanel + (ks & 3) * 32) >> 4);
+                    const uint32_t koff = uint32_t(((ks >> 2) * C::kKvPanel + (ks & 3) * 32) >> 4);
+                    tc::mma_bf16_ss_if(leader, s_tmem, q_desc + off, kd + koff, C::kIdescS, ks > 0);
                 }
-                if (npv < ns && mbar_test(p_full(npv), uint32_t((npv >> 1) & 1)) &&
-                    mbar_test(full(1, npv % C::kStages), uint32_t((npv / C::kStages) & 1))) {
-                    tc::fence_after_sync();
-                    const uint32_t sv = base + C::kVOff + (npv % C::kStages) * C::kKvBytes;
+                tc::commit_if(leader, s_full(ns & 1));
+                tc::commit_if(leader, empty(0, ns % C::kStages));
+                ++ns;
+                progress = true;
+            }
+            go = false;
+            if (leader && npv < ns)
+                go = mbar_test(p_full(npv), uint32_t((npv >> 1) & 1)) &&
+                     mbar_test(full(1, npv % C::kStages), uint32_t((npv / C::kStages) & 1));
+            if (__shfl_sync(kFullMask, go, 0)) {
+                tc::fence_after_sync();
+                const uint64_t vd = v_desc + uint64_t(((npv % C::kStages) * C::kKvBytes) >> 4);
+                const uint32_t p_tmem = tmem + uint32_t(C::kPCol + (npv & 1) * (C::kKv / 2));
 #pragma unroll
-                    for (int ks = 0; ks < C::kKv / 16; ++ks)
-                        tc::mma_bf16_ss(o_tmem,
-                                        tc::sdesc_sw128(base + C::kPOff + (npv & 1) * C::kPBytes +
-                                                            (ks >> 2) * C::kPQPanel + (ks & 3) * 32, 16, 1024),
-                                        tc::sdesc_sw128(sv + ks * 16 * 128, C::kKvPanel, 1024), C::kIdescO,
-                                        npv > 0 || ks > 0);
-                    tc::commit(o_done(npv));
-                    tc::commit(empty(1, npv % C::kStages));
-                    ++npv;
-                    progress = true;
-                }
-                if (progress) {
-                    idle = 0;
-                } else if (++idle % 256 == 0) {  // the clocks are read now and then only
+                for (int ks = 0; ks < C::kKv / 16; ++ks)
+                    tc::mma_bf16_ts_if(leader, o_tmem, p_tmem + uint32_t(8 * ks),
+                                       vd + uint64_t((ks * 16 * 128) >> 4), C::kIdescO, npv > 0 || ks > 0);
+                tc::commit_if(leader, o_done(npv));
+                tc::commit_if(leader, empty(1, npv % C::kStages));
+                ++npv;
+                progress = true;
+            }
+            if (progress) {
+                idle = 0;
+            } else if (++idle % 256 == 0) {  // the clocks are read now and then only
+                bool stop = false;
+                if (leader) {
                     if (idle == 256) t_idle = pf_global_ns();
-                    if (*abort_flag) break;
-                    if (pf_global_ns() - t_idle > kPfWaitNs) {
+                    if (*abort_flag) {
+                        stop = true;
+                    } else if (pf_global_ns() - t_idle > kPfWaitNs) {
                         atomicOr(a.status, 1);
                         *abort_flag = 1;
-                        break;
+                        stop = true;
                     }
                 }
+                if (__shfl_sync(kFullMask, stop, 0)) break;
             }
-            // every MMA issued has completed before the CTA frees TMEM and exits (this
-            // wait does not stop early for another role's failure)
-            tc::commit(drain);
+        }
+        // every MMA issued has completed before the CTA frees TMEM and exits (this
+        // wait does not stop early for another role's failure)
+        tc::commit_if(leader, drain);
+        if (leader) {
             const unsigned long long t_drain = pf_global_ns();
             while (!mbar_try_wait(drain, 0u) && pf_global_ns() - t_drain < kPfWaitNs) {
             }
@@ -443,12 +462,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
             if (!__all_sync(kFullMask, ok)) { ok = false; break; }
             tc::fence_after_sync();
             float x[C::kKv];
+            {   // the row of S in one load
+                uint32_t v[C::kKv];
+                if constexpr (C::kKv == 128)
+                    tc::tmem_ld128(tmem + lane_base + uint32_t(b * C::kKv), v);
+                else
+                    tc::tmem_ld64(tmem + lane_base + uint32_t(b * C::kKv), v);
 #pragma unroll
-            for (int c = 0; c < C::kKv / 32; ++c) {
-                uint32_t v[32];
-                tc::tmem_ld32(tmem + lane_base + uint32_t(b * C::kKv + 32 * c), v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(v[i]);
+                for (int i = 0; i < C::kKv; ++i) x[i] = __uint_as_float(v[i]);
             }
             tc::fence_before_sync();
             mbar_arrive(s_empty(b));  // S buffer b may be overwritten
@@ -460,13 +481,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
 #pragma unroll
                 for (int i = 0; i < C::kKv; ++i) x[i] = i < lim ? x[i] : neg_inf();
             }
-            float mx0 = x[0], mx1 = x[1];
+            // row maximum: eight independent chains, then a tree
+            float mxv[8];
 #pragma unroll
-            for (int i = 2; i < C::kKv; i += 2) {
-                mx0 = fmaxf(mx0, x[i]);
-                mx1 = fmaxf(mx1, x[i + 1]);
-            }
-            const float mx = fmaxf(mx0, mx1) * sl2;
+            for (int j = 0; j < 8; ++j) mxv[j] = x[j];
+#pragma unroll
+            for (int i = 8; i < C::kKv; i += 8)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) mxv[j] = fmaxf(mxv[j], x[i + j]);
+            const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
+                                   fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7]))) * sl2;
             // running maximum (base 2, scaled): moves when a row's maximum grows by more
             // than 2^8 (the first tile always sets it: every row sees entry kv_lo)
             const bool grow = mx > m + kRescaleLog2;
@@ -474,29 +498,29 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
             const float alpha = grow ? ex2(m - m_new) : 1.f;  // 0 on the first tile
             m = m_new;
             const float neg_m = -m;
-            // P buffer n & 1 was last read by P V of tile n - 2
+            // TMEM P buffer n & 1 was last read by P V of tile n - 2
             if (n > 1) {
                 ok = pf_wait(o_done(n), uint32_t(((n - 2) >> 1) & 1), a.status, abort_flag);
                 if (!__all_sync(kFullMask, ok)) { ok = false; break; }
             }
-            // P = 2^(s * scale - m) as bf16 into the swizzled K-major operand, row r,
-            // 8 entries (one 16-byte chunk) at a time
-            uint8_t* pbuf = smem + C::kPOff + (n & 1) * C::kPBytes;
-            float sum0 = 0.f, sum1 = 0.f;
+            // P = 2^(s * scale - m) as bf16 pairs into this row's TMEM lane (the A
+            // operand of P V), 64 entries (32 columns) at a time
+            const uint32_t p_tmem = tmem + lane_base + uint32_t(C::kPCol + (n & 1) * (C::kKv / 2));
+            float sums[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < C::kKv / 8; ++c) {
-                uint32_t pk[4];
+            for (int c = 0; c < C::kKv / 64; ++c) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float p0 = ex2(fmaf(x[8 * c + 2 * i], sl2, neg_m));
-                    const float p1 = ex2(fmaf(x[8 * c + 2 * i + 1], sl2, neg_m));
-                    sum0 += p0;
-                    sum1 += p1;
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2(fmaf(x[64 * c + 2 * i], sl2, neg_m));
+                    const float p1 = ex2(fmaf(x[64 * c + 2 * i + 1], sl2, neg_m));
+                    sums[(2 * i) & 3] += p0;
+                    sums[(2 * i + 1) & 3] += p1;
                     pk[i] = pack_bf16x2(p0, p1);
                 }
-                *reinterpret_cast<uint4*>(pbuf + sw128_off(r, c, kPfRows)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                tc::tmem_st32(p_tmem + uint32_t(32 * c), pk);
             }
+            const float sum0 = sums[0] + sums[2], sum1 = sums[1] + sums[3];
             l = fmaf(l, alpha, sum0 + sum1);
             // a row maximum moved: O (complete up to P V of tile n - 1) is rescaled
             // before P V of tile n accumulates into it
@@ -517,7 +541,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
                     tc::tmem_st_wait();
                 }
             }
-            tc::fence_proxy_async_smem();
+            tc::tmem_st_wait();
             tc::fence_before_sync();
             mbar_arrive(p_full(n));
         }

@@ -96,6 +96,51 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], one M x N x 16 step with A in tensor memory: row
+// i of A in lane i, its 16 bf16 of the step packed two to a 32-bit column (element
+// 2j in the low half of column j) from the address's column on.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// The same, issued only where `issue` is true: a whole warp executes the statement
+// with warp-uniform operands and one lane issues, so that no branch separates the
+// operands from the instruction.
+__device__ __forceinline__ void mma_bf16_ss_if(bool issue, uint32_t d_tmem, uint64_t a_desc,
+                                               uint64_t b_desc, uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(issue ? 1u : 0u)
+        : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_if(bool issue, uint32_t d_tmem, uint32_t a_tmem,
+                                               uint64_t b_desc, uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(issue ? 1u : 0u)
+        : "memory");
+}
+__device__ __forceinline__ void commit_if(bool issue, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(issue ? 1u : 0u)
+        : "memory");
+}
+
 // The mbarrier at `bar` receives one arrival when every tcgen05 operation this
 // thread issued before has completed.
 __device__ __forceinline__ void commit(uint32_t bar) {
@@ -121,6 +166,41 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
         : PKV_TC_R8(0), PKV_TC_R8(8), PKV_TC_R8(16), PKV_TC_R8(24)
+        : "r"(taddr)
+        : "memory");
+}
+
+// 64 consecutive columns in one instruction (and its wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : PKV_TC_R8(0), PKV_TC_R8(8), PKV_TC_R8(16), PKV_TC_R8(24), PKV_TC_R8(32), PKV_TC_R8(40),
+          PKV_TC_R8(48), PKV_TC_R8(56)
+        : "r"(taddr)
+        : "memory");
+}
+
+// 128 consecutive columns in one instruction (and its wait).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, "
+        "%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
+        "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, "
+        "%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, "
+        "%112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : PKV_TC_R8(0), PKV_TC_R8(8), PKV_TC_R8(16), PKV_TC_R8(24), PKV_TC_R8(32), PKV_TC_R8(40),
+          PKV_TC_R8(48), PKV_TC_R8(56), PKV_TC_R8(64), PKV_TC_R8(72), PKV_TC_R8(80), PKV_TC_R8(88),
+          PKV_TC_R8(96), PKV_TC_R8(104), PKV_TC_R8(112), PKV_TC_R8(120)
         : "r"(taddr)
         : "memory");
 }
