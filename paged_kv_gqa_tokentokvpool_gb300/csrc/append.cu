@@ -6,8 +6,10 @@
 // heads of one token (n_kv_heads * head_dim bf16, 2 KB for 8 x 128), contiguous in
 // both the source and the pool, so the copy is 16-byte vectors: consecutive
 // threads move consecutive vectors of one row (fully coalesced 2 KB reads and
-// writes), and one grid-stride loop covers K and V. Pure HBM traffic: 2 * n * row
-// bytes read and written, plus 4 bytes of slot id per row.
+// writes), and one grid-stride loop covers K and V, each thread loading four
+// vectors before it stores them (a prefill chunk appends thousands of rows, and
+// the loads in flight set the rate). Pure HBM traffic: 2 * n * row bytes read and
+// written, plus 4 bytes of slot id per row.
 #include <cuda_runtime.h>
 
 #include "pkv_internal.h"
@@ -24,18 +26,30 @@ kvpool_append_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
     // (its readers of the pool, or its producers of the new rows).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    constexpr int kUnroll = 4;
     const int64_t per_pool = n * row_vecs;
     const int64_t total = 2 * per_pool;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const bool is_v = i >= per_pool;
-        const int64_t j = is_v ? i - per_pool : i;
-        const int64_t row = j / row_vecs;
-        const int64_t col = j - row * row_vecs;
-        const int64_t slot = __ldg(slot_ids + row);
-        const uint4 val = is_v ? __ldg(v_new + j) : __ldg(k_new + j);
-        uint4* dst = is_v ? v_pool : k_pool;
-        dst[slot * row_vecs + col] = val;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i0 < total;
+         i0 += kUnroll * stride) {
+        uint4 val[kUnroll];
+        int64_t off[kUnroll];  // vector index in its pool; -1: past the end
+        bool to_v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            to_v[u] = i >= per_pool;
+            off[u] = -1;
+            if (i < total) {
+                const int64_t j = to_v[u] ? i - per_pool : i;
+                const int64_t row = j / row_vecs;
+                val[u] = to_v[u] ? __ldg(v_new + j) : __ldg(k_new + j);
+                off[u] = int64_t(__ldg(slot_ids + row)) * row_vecs + (j - row * row_vecs);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (off[u] >= 0) (to_v[u] ? v_pool : k_pool)[off[u]] = val[u];
     }
 }
 
@@ -49,7 +63,7 @@ cudaError_t launch_append(void* k_pool, void* v_pool, const int32_t* slot_ids,
     const int64_t total = 2 * n * row_vecs;
     const int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
-    // At most one CTA per SM: with PDL they can all be resident (and waiting)
+    // At most four CTAs per SM: with PDL they can all be resident (and waiting)
     // next to the previous kernel's CTAs; the loop covers the rest.
     static int sms_of[64] = {0};
     int dev = 0;
@@ -57,7 +71,8 @@ cudaError_t launch_append(void* k_pool, void* v_pool, const int32_t* slot_ids,
     if (sms_of[dev] == 0 &&
         cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms_of[dev] = 152;
-    blocks = blocks < sms_of[dev] ? blocks : sms_of[dev];
+    blocks = (blocks + 3) / 4;  // four vectors per thread and pass
+    blocks = blocks < 4 * sms_of[dev] ? blocks : 4 * sms_of[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(threads);
