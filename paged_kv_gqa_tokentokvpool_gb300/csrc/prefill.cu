@@ -18,25 +18,29 @@
 //  * One CTA per work unit (request, KV head, tile of 128 / G chunk tokens): its 128
 //    query rows (row r: token r / G, head r % G) are the M of every MMA. The plan
 //    orders units longest causal range first, so the grid drains evenly.
-//  * Four producer warps gather the unit's q rows once, then the request's slot rows
-//    of that KV head in 64-token K/V tiles, with 16-byte cp.async into a ring of
-//    shared-memory stages, each row stored in the tensor core's 128-byte swizzled
+//  * Two producer halves (two warps each) gather the unit's q rows once and the
+//    request's slot rows of that KV head in K/V tiles of kKv tokens (128 at head_dim
+//    128, 64 at 256), with 16-byte cp.async into separate K and V rings of
+//    shared-memory stages. Each row is stored in the tensor core's 128-byte swizzled
 //    layout (K-major for q and K; V's rows are the same bytes read as an MN-major
-//    operand).
-//  * One thread issues the MMAs: S = Q K^T (128 x 64, K = head_dim) into one of two
-//    TMEM buffers, and O += P V (128 x head_dim, K = 64) into a TMEM accumulator,
-//    each signalled on an mbarrier by tcgen05.commit. S of the next tile is computed
-//    while the softmax works on the current one.
+//    operand). A thread's arrival on a stage's barrier rides on its copies, and a
+//    relay thread fences the landed stage (generic to async proxy) for the tensor
+//    core.
+//  * An MMA warp issues, from one lane, S = Q K^T (128 x kKv, K = head_dim, operands
+//    in shared memory) into one of two TMEM buffers, and O += P V (128 x head_dim,
+//    K = kKv) with P read from TMEM as the A operand, each signalled on an mbarrier
+//    by tcgen05.commit. S runs up to two tiles ahead of the softmax.
 //  * Four softmax warps own one query row per thread: they read the row of S from
 //    TMEM, apply the causal mask (list position <= the row's query position) and an
-//    online softmax in base 2 with fp32 state, write P as bf16 to shared memory for
-//    the P V product, and rescale O in TMEM when a row's running maximum grows by
-//    more than 2^8 (between rescales the probabilities stay below 2^8, exact enough
-//    for bf16 P and fp32 sums). At the end they read O back, divide by the row sum
-//    and store out and lse.
+//    online softmax in base 2 with fp32 state, write P as bf16 pairs back to TMEM, and
+//    rescale O in TMEM when a row's running maximum grows by more than 2^8 (between
+//    rescales the probabilities stay below 2^8, exact enough for bf16 P and fp32
+//    sums). At the end they read O back, divide by the row sum and store out and lse.
 //  * Every wait is an mbarrier wait bounded by 1 s; on expiry the CTA records it in
 //    the plan's status word, every role leaves its loop, the MMA and copies in
-//    flight are drained (again bounded) and the tensor memory is freed.
+//    flight are drained (again bounded) and the tensor memory is freed. Barriers a
+//    reader could fall two phases behind on are split per buffer, so that no parity
+//    test can alias.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
