@@ -76,6 +76,14 @@ PREFILL_CASES = [
     ([200, 7], [4000, 2500], 16, 2, 128),                # G = 8, long ranges split
     ([300, 5], [5000, 3000], 16, 4, 256),                # head_dim 256, long ranges split
     ([100], [6000], 8, 8, 128),                          # G = 1, long range split
+    # K/V tiles are 128 entries at head_dim 128 and 64 at 256, units 128 / G tokens:
+    # contexts at and around tile edges, chunks one token over a unit
+    ([33, 32, 31], [128, 129, 127], 32, 8, 128),         # G = 4: units of 32 tokens
+    ([17, 16], [256, 255], 64, 8, 128),                  # G = 8: units of 16 tokens
+    ([129, 128], [257, 384], 8, 8, 128),                 # G = 1: units of 128 tokens
+    ([65, 64], [64 + 65, 192], 16, 8, 128),              # G = 2: units of 64 tokens
+    ([33, 1], [65, 63], 16, 4, 256),                     # head_dim 256 around 64-entry tiles
+    ([65, 64], [129, 64], 8, 4, 256),                    # head_dim 256, G = 2
 ]
 
 
