@@ -411,11 +411,12 @@ void pkv_set_debug_checks(int on);
 /*
  * pkv_inject_stall — failure injection for tests of the bounded waits (this
  * library's own; the pages have no counterpart). The next n_launches attention
- * launches (paged_decode_attn / paged_decode_append_attn, any thread) run with a
- * producer that issues no copies. Every pipeline wait of such a launch expires
- * after its bound (1 s), the launch ends without a fault or a hang, and the plan's
- * status word reads nonzero (paged_decode_plan_status); its outputs are invalid.
- * Later launches are unaffected. 0 cancels. Process-wide.
+ * launches (paged_decode_attn / paged_decode_append_attn / paged_prefill_attn, any
+ * thread) run with producers that issue no copies. Every pipeline wait of such a
+ * launch expires after its bound (1 s), the launch ends without a fault or a hang
+ * (the prefill kernel frees its tensor memory on that path too), and the plan's
+ * status word reads nonzero (paged_decode_plan_status / paged_prefill_plan_status);
+ * its outputs are invalid. Later launches are unaffected. 0 cancels. Process-wide.
  */
 void pkv_inject_stall(int n_launches);
 

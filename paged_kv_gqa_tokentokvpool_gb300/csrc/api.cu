@@ -46,6 +46,13 @@ int fail(int code, const char* fmt, ...) {
 void clear_error() { g_last_error.clear(); }
 bool debug_checks() { return g_debug_checks != 0; }
 
+bool take_injected_stall() {
+    int stalls = g_stalls_to_inject.load();
+    while (stalls > 0 && !g_stalls_to_inject.compare_exchange_weak(stalls, stalls - 1)) {
+    }
+    return stalls > 0;
+}
+
 int choose_heads_per_cta(int n_kv_heads, int head_dim) {
     int hpg = heads_per_group(n_kv_heads, head_dim);
     if (const char* env = std::getenv("PKV_HEADS_PER_CTA")) {
@@ -604,10 +611,7 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
     a.n_ctas = p->launch_ctas;
     a.shared = p->shared;
     a.early = (p->flags & PKV_PLAN_EARLY_GATHER) != 0;
-    int stalls = g_stalls_to_inject.load();
-    while (stalls > 0 && !g_stalls_to_inject.compare_exchange_weak(stalls, stalls - 1)) {
-    }
-    a.withhold = stalls > 0;
+    a.withhold = take_injected_stall();
     a.heads_per_cta = p->heads_per_cta;
     a.n_qo_heads = n_qo_heads;
     a.n_kv_heads = n_kv_heads;

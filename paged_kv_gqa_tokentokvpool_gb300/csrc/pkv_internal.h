@@ -25,6 +25,9 @@ int shared_row_blocks();
 int fail(int code, const char* fmt, ...);  // records the message, returns code
 void clear_error();
 bool debug_checks();
+// One injected stall (pkv_inject_stall) for the attention launch being prepared:
+// true if this launch is to withhold its copies (and the count is taken down).
+bool take_injected_stall();
 
 // ---- shapes ----------------------------------------------------------------
 // A CTA of the decode kernel serves one KV-head group of 1, 2 or 4 consecutive

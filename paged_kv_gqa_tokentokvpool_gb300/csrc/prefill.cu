@@ -110,6 +110,7 @@ struct PfArgs {
     const PfMerge* merges;
     int n_merges;
     int* status;       // nonzero: a wait of some CTA exceeded its bound
+    bool withhold;     // injected stall (pkv_inject_stall): the producers issue no copies
 };
 
 // Shared memory of one CTA (offsets from a 1024-byte aligned base). Every operand
@@ -306,7 +307,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
         // in shared memory; the relay warp then announces the stage to the tensor core.
         const int half = (tid - 32 * kPfSoftmaxWarps) / kPfHalfThreads;  // 0: K, 1: V
         const int pt = (tid - 32 * kPfSoftmaxWarps) % kPfHalfThreads;
-        if (half == 0) {   // the unit's q rows (row r: token r / G, head r % G), with K tile 0
+        // an injected stall: no copies, so every wait of the launch expires (bounded)
+        const int n_copy_tiles = a.withhold ? 0 : n_tiles;
+        if (half == 0 && !a.withhold) {   // the unit's q rows (row r: token r / G, head r % G), with K tile 0
             const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
 #pragma unroll 4
             for (int i = 0; i < C::kQPieces; ++i) {
@@ -322,8 +325,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
         const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(half ? a.v_pool : a.k_pool);
         const uint32_t ring = base + (half ? C::kVOff : C::kKOff);
         int slot[C::kTilePieces];
-        load_tile_slots<D, G>(a, un, t0, pt, slot);
-        for (int n = 0; n < n_tiles; ++n) {
+        if (n_copy_tiles > 0) load_tile_slots<D, G>(a, un, t0, pt, slot);
+        for (int n = 0; n < n_copy_tiles; ++n) {
             const int st = n % C::kStages;
             if (n >= C::kStages &&
                 !pf_wait(empty(half, st), uint32_t((n / C::kStages - 1) & 1), a.status, abort_flag))
@@ -1070,6 +1073,7 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
     a.merges = p->dev_merges;
     a.n_merges = p->n_merges;
     a.status = p->dev_status;
+    a.withhold = take_injected_stall();
     const cudaError_t e = prefill_dispatch<PfLaunchFn>(head_dim, n_qo_heads / n_kv_heads, a,
                                                        p->n_units, stream);
     if (e != cudaSuccess) return pf_cuda_fail(e, "paged_prefill_attn: launch");

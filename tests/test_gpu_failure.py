@@ -55,3 +55,43 @@ def test_expired_waits_set_the_status_word_and_the_context_survives(pkv):
     assert plan.status() == 0
     ref_out, ref_lse = oracle_reference(wl, t)
     assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what="after the stall")
+
+
+def test_prefill_expired_waits_set_the_status_word_and_the_context_survives(pkv):
+    """The same for the chunked-prefill kernel (tcgen05, tensor memory): the stalled
+    launch ends by itself, frees its tensor memory on that path (the next launch
+    allocates it again), and the next launch is correct with status 0."""
+    import oracle
+    from test_gpu_parity import bits
+    pw = workloads.prefill_workload([40, 7], [300, 50], seed=62)
+    q, kp, vp, kn, vn = workloads.prefill_tensors(pw, 0, device="cpu", poison_unreferenced=True)
+    dev = torch.device("cuda")
+    kp_d, vp_d = kp.to(dev), vp.to(dev)
+    pkv.kvpool_append(kp_d, vp_d, torch.from_numpy(pw.chunk_slots).to(dev), kn.to(dev), vn.to(dev))
+    plan = pkv.paged_prefill_plan_create(pw.batch, pw.total_q, 32, 8, 128)
+    pkv.paged_prefill_plan(plan, pw.qo_indptr, pw.kv_indptr)
+    args = (q.to(dev), kp_d, vp_d, torch.from_numpy(pw.qo_indptr).to(dev),
+            torch.from_numpy(pw.kv_indptr).to(dev), torch.from_numpy(pw.kv_indices).to(dev),
+            pw.batch, 32, 8, 128, pw.sm_scale)
+    out = torch.zeros(pw.total_q, 32, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros(pw.total_q, 32, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    pkv.pkv_inject_stall(1)
+    try:
+        t0 = time.perf_counter()
+        pkv.paged_prefill_attn(*args, out, lse, plan)
+        torch.cuda.synchronize()  # ends by itself once the bounded waits expire
+        waited = time.perf_counter() - t0
+    finally:
+        pkv.pkv_inject_stall(0)
+    assert plan.status() != 0, "an expired wait must be reported"
+    assert waited > 0.5, "the waits should have run to their bound"
+    pkv.paged_prefill_attn(*args, out, lse, plan)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    ref_out, ref_lse = oracle.prefill(
+        bits(q), oracle.append(bits(kp), pw.chunk_slots, bits(kn)),
+        oracle.append(bits(vp), pw.chunk_slots, bits(vn)), pw.qo_indptr, pw.kv_indptr,
+        pw.kv_indices, 32, 8, 128, pw.sm_scale)
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what="prefill after the stall")
