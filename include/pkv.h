@@ -328,8 +328,12 @@ int paged_prefill_plan(pkv_prefill_plan* plan, const int32_t* qo_indptr_host,
  *   out        : [qo_indptr[batch], n_qo_heads, head_dim] bf16, written
  *   lse        : [qo_indptr[batch], n_qo_heads] fp32 natural-log lse, or NULL
  *   plan       : built by paged_prefill_plan for this step, same shape
- * One kernel launch (none when the step has no query tokens). fp32 accumulation
- * and an online softmax; q, pools and out must be 16-byte aligned.
+ * One kernel launch on the fifth-generation tensor cores (tcgen05, accumulators in
+ * tensor memory; 230 KB of shared memory per CTA, one CTA per SM), plus a merge
+ * kernel when the plan split long ranges; none when the step has no query tokens.
+ * bf16 inputs, fp32 accumulation, probabilities rounded to bf16 for P V, an online
+ * softmax; q, pools and out must be 16-byte aligned. Every pipeline wait is bounded
+ * (1 s); an expired one is reported by paged_prefill_plan_status.
  */
 int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
                        const int32_t* qo_indptr, const int32_t* kv_indptr,
