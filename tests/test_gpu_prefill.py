@@ -162,12 +162,13 @@ def test_prefill_empty_step(pkv):
     assert out.numel() == 0
 
 
-@pytest.mark.parametrize("config_no", [1, 3])
+@pytest.mark.parametrize("config_no", [1, 2, 3])
 def test_prefill_full_size_sampled(pkv, config_no):
     """The benchmark's prefill workloads at full size (layer 0): every row of the
     smallest request's chunk, and the first and last 16 rows of every other chunk
     (by causality, the first rows need only the list up to their positions and
-    the last rows only a shorter chunk over the whole list)."""
+    the last rows only a shorter chunk over the whole list). The 64-token chunks over
+    long contexts (config 2) go through split ranges and the merge kernel."""
     pw = workloads.prefill_config(config_no)
     out, lse, tensors, _ = run_prefill(pkv, pw)
     q, kp, vp, kn, vn = tensors
