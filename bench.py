@@ -412,6 +412,23 @@ def run_tier_bench(args):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / args.steps
         res[name] = {"us_per_call": ms * 1e3, "gbs_over_link": rows * row_bytes / (ms * 1e-3) / 1e9}
+    # the link's rate for the same bytes as one contiguous copy each way (copy engines)
+    host_flat = torch.empty(rows * row_bytes, dtype=torch.uint8).pin_memory()
+    dev_flat = torch.empty(rows * row_bytes, dtype=torch.uint8, device=dev)
+    for name, (dst, src) in (("contiguous_h2d", (dev_flat, host_flat)),
+                             ("contiguous_d2h", (host_flat, dev_flat))):
+        for _ in range(args.warmup):
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        res[name] = {"gbs": rows * row_bytes / (ms * 1e-3) / 1e9}
     print(json.dumps({"metric": "host KV tier: scattered row moves HBM <-> pinned host memory",
                       "unit": "GB/s", "rows": rows, "row_bytes": row_bytes,
                       "workload": f"{wl.name}: {wl.description}", **res}), flush=True)
