@@ -294,6 +294,7 @@ int paged_decode_plan_host(const int32_t* kv_indptr_host, int batch, int n_kv_he
                          requests_per_unit > 0 ? requests_per_unit : 1};
     PlanCounts c{};
     rc = plan_compute(kv_indptr_host, batch, n_kv_heads / hpg, ctas,
+                      decode_stage_tokens(hpg, head_dim),
                       PlanLimits{max_units, max_merges, max_partials}, n_shared > 0 ? &sh : nullptr,
                       reinterpret_cast<Unit*>(units_out), cta_begin_out,
                       reinterpret_cast<Merge*>(merges_out), part_list_out, &c);
@@ -454,7 +455,9 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
     char* st = static_cast<char*>(p->host_staging);
     PlanCounts c{};
     const int ctas = share ? p->ctas_shared : p->ctas;
-    rc = plan_compute(kv_indptr_host, batch, p->n_groups, ctas, p->lim, share ? &sh : nullptr,
+    rc = plan_compute(kv_indptr_host, batch, p->n_groups, ctas,
+                      decode_stage_tokens(p->n_kv_heads / p->n_groups, p->head_dim), p->lim,
+                      share ? &sh : nullptr,
                       reinterpret_cast<Unit*>(st + p->off_units),
                       reinterpret_cast<int32_t*>(st + p->off_cta),
                       reinterpret_cast<Merge*>(st + p->off_merge),

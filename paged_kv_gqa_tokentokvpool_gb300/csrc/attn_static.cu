@@ -114,7 +114,7 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
                     "of %d (request, head group) pairs", batch, n_groups, kMaxMerges);
     PlanCounts c{};
     const int max_units = std::min(kMaxUnits, plan_max_units(ctas, batch, n_groups));
-    int rc = plan_compute(kv_indptr_host, batch, n_groups, ctas,
+    int rc = plan_compute(kv_indptr_host, batch, n_groups, ctas, decode_stage_tokens(hpc, head_dim),
                           PlanLimits{max_units, kMaxMerges, max_units}, nullptr,
                           reinterpret_cast<Unit*>(g_stage + kOffUnits),
                           reinterpret_cast<int32_t*>(g_stage + kOffCta),

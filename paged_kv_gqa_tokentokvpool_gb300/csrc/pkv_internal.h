@@ -63,8 +63,15 @@ struct Merge {
 };
 static_assert(sizeof(Unit) == 32 && sizeof(Merge) == 16, "plan record sizes");
 
-// No CTA's token range is planned shorter than this (small steps use fewer CTAs).
+// No piece of a context split across CTAs is planned shorter than this.
 constexpr int kMinChunkTokens = 64;
+// Tokens of K/V that one decode pipeline stage holds for a head group of hpc heads
+// of head_dim: a stage carries kStageRows rows of kHeadGroupElems bf16 of K and as
+// many of V, so a smaller group takes proportionally more tokens per stage.
+constexpr int kStageRows = 16;
+inline int decode_stage_tokens(int hpc, int head_dim) {
+    return kStageRows * (kHeadGroupElems / (hpc * head_dim));
+}
 
 struct PlanLimits {
     int max_units;
@@ -87,9 +94,11 @@ struct PlanSharing {
 int plan_max_units(int ctas, int max_batch, int n_groups);
 // Pure host planner. units[max_units], cta_begin[ctas + 1] (every CTA of the grid
 // gets an entry; unused ones an empty range), merges[max_merges],
-// part_list[max_partials]. sharing may be NULL.
+// part_list[max_partials]. stage_tokens: decode_stage_tokens() of the plan's head
+// group (the planner's cost model). sharing may be NULL.
 // Returns PKV_OK, PKV_ERR_PLAN (capacity) or PKV_ERR_INVALID_ARG (bad indptr).
-int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, const PlanLimits& lim,
+int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, int stage_tokens,
+                 const PlanLimits& lim,
                  const PlanSharing* sharing, Unit* units, int* cta_begin, Merge* merges,
                  int32_t* part_list, PlanCounts* out);
 

@@ -15,13 +15,16 @@
 // Head groups are independent, so cutting along heads costs nothing, while cutting
 // a run into token ranges costs one fp32 partial result per extra range (per
 // request of the item) plus a log-sum-exp merge. The planner therefore:
-//   1. lays the items end to end and cuts that sequence into `ctas` ranges of equal
-//      token count (fewer if a range would drop below kMinChunkTokens), so every
-//      CTA streams the same number of bytes whatever the mix of lengths, and an
+//   1. lays the items end to end and gives each CTA a contiguous range of that
+//      sequence, costed in tokens as the kernel spends its time: whole pipeline
+//      stages (a ragged last stage costs a full one) plus a fixed cost per unit.
+//      A CTA takes whole items while they fit its budget, then as many whole stages
+//      of the next item as fit, so only an item's last piece has a ragged stage and
+//      no piece of a split item is shorter than kMinChunkTokens;
+//   2. takes the smallest budget for which that greedy fill needs at most `ctas`
+//      CTAs (a bisection over the budget), so the slowest CTA,
+//      which sets the launch's duration, is as fast as the cost model allows. An
 //      item is only split where a range boundary falls inside it;
-//   2. moves each boundary to the nearest item edge when it falls within
-//      min(kSnapTokens, range / 8) tokens of it, so no split creates a sliver of a
-//      unit while the ranges stay within 25% of equal;
 //   3. gives every piece of a split item, and every piece of a prefix or suffix
 //      item, a partial slot per request it serves, and every (request, head group)
 //      with partial results a merge record whose part list names those slots in
@@ -40,10 +43,6 @@ namespace pkv {
 
 namespace {
 
-// A range boundary closer than this to an item edge moves onto the edge (the
-// distance is also capped at an eighth of the range).
-constexpr int64_t kSnapTokens = 32;
-
 struct Item {
     int32_t b;        // (first) request
     int32_t nreq;     // requests served
@@ -55,6 +54,62 @@ struct Item {
     bool partial;     // its pieces always write partial results (prefix, suffix)
 };
 
+
+// Cost of a CTA streaming a piece of t tokens, in tokens: the kernel moves K/V in
+// pipeline stages of stage_tokens tokens, and a ragged last stage takes a whole
+// stage's turn; every unit also pays a fixed cost (its epilogue, the switch of
+// query rows).
+// stage_tokens is a power of two.
+int64_t piece_cost(int64_t t, int64_t stage_tokens, int64_t unit_cost) {
+    return ((t + stage_tokens - 1) & ~(stage_tokens - 1)) + unit_cost;
+}
+
+// Cuts the items, laid end to end, into CTA ranges of cost at most T: each CTA
+// takes the sequence in order, whole items while they fit and then as many whole
+// stages of the next item as fit, so that only an item's last piece has a ragged
+// stage. No piece of a split item is shorter than kMinChunkTokens. Returns the
+// number of CTAs used (writing cut[0 .. used] when cut is not NULL), or
+// max_ctas + 1 once more than max_ctas would be needed or a piece cannot fit an
+// empty CTA.
+int greedy_fill(const std::vector<Item>& items, const std::vector<int64_t>& start, int64_t T,
+                int64_t stage_tokens, int64_t unit_cost, int max_ctas, int64_t* cut) {
+    const int64_t kMin = kMinChunkTokens;
+    int n = 0;              // index of the CTA being filled
+    int64_t budget = T;     // its budget left
+    if (cut) cut[0] = 0;
+    for (size_t k = 0; k < items.size(); ++k) {
+        int64_t r = items[k].len;  // tokens of item k not yet placed
+        while (r > 0) {
+            const int64_t c = piece_cost(r, stage_tokens, unit_cost);
+            if (c <= budget) {
+                budget -= c;
+                break;
+            }
+            // split: whole stages that fit, leaving at least kMin tokens behind
+            int64_t p = budget > unit_cost ? (budget - unit_cost) & ~(stage_tokens - 1) : 0;
+            if (r - p < kMin) p = r >= kMin ? (r - kMin) & ~(stage_tokens - 1) : 0;
+            if (p >= kMin) {
+                r -= p;
+            } else if (budget == T) {
+                return max_ctas + 1;  // not even a minimum piece fits an empty CTA
+            } else {
+                p = 0;
+            }
+            // the range ends here
+            if (++n >= max_ctas) return max_ctas + 1;
+            if (cut) cut[n] = start[k + 1] - r;
+            budget = T;
+        }
+    }
+    if (budget == T && n > 0) {
+        // the last range is empty: the previous cut already ends the sequence
+        if (cut) cut[n] = start[items.size()];
+        return n;
+    }
+    if (cut) cut[n + 1] = start[items.size()];
+    return n + 1;
+}
+
 }  // namespace
 
 int plan_max_units(int ctas, int max_batch, int n_groups) {
@@ -63,7 +118,8 @@ int plan_max_units(int ctas, int max_batch, int n_groups) {
     return 2 * ctas + 2 * max_batch * n_groups;
 }
 
-int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, const PlanLimits& lim,
+int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, int stage_tokens,
+                 const PlanLimits& lim,
                  const PlanSharing* sharing, Unit* units, int* cta_begin, Merge* merges,
                  int32_t* part_list, PlanCounts* out) {
     if (batch < 0) return fail(PKV_ERR_INVALID_ARG, "plan: batch %d < 0", batch);
@@ -110,23 +166,37 @@ int plan_compute(const int32_t* indptr, int batch, int n_groups, int ctas, const
     for (int k = 0; k < n_items; ++k) start[k + 1] = start[k] + items[k].len;
     const int64_t total = start[n_items];
 
-    // 1-2. range boundaries, snapped near item edges; a small step uses fewer CTAs
-    // so that no range is shorter than kMinChunkTokens
-    const int used = static_cast<int>(
-        std::max<int64_t>(1, std::min<int64_t>(ctas, total / kMinChunkTokens)));
-    std::vector<int64_t> cut(used + 1);
+    // 1-2. range boundaries: the smallest budget whose greedy fill needs at most
+    // `ctas` CTAs
+    std::vector<int64_t> cut(size_t(ctas) + 1);
+    const int64_t unit_cost = std::max<int64_t>(1, stage_tokens / 4);
+    int64_t lb = 0;  // sum of the items' costs, unsplit
+    for (int k = 0; k < n_items; ++k)
+        if (items[k].len > 0) lb += piece_cost(items[k].len, stage_tokens, unit_cost);
+    int used = 1;
     cut[0] = 0;
-    cut[used] = total;
-    const int64_t snap = std::min<int64_t>(kSnapTokens, total / used / 8);
-    int k = 0;
-    for (int c = 1; c < used; ++c) {
-        int64_t p = total * c / used;
-        while (k < n_items && start[k + 1] <= p) ++k;  // item k: start[k] <= p < start[k+1]
-        if (k < n_items && p > start[k]) {
-            if (p - start[k] < snap) p = start[k];
-            else if (start[k + 1] - p < snap) p = start[k + 1];
+    cut[1] = total;
+    if (total > 0) {
+        // lo: infeasible, as `ctas` CTAs of a smaller budget than lb / ctas cannot
+        // hold costs that add up to at least lb. hi: feasible; a minimum piece, two
+        // stages and a unit above lb / ctas usually is, else the step doubles (all
+        // items in one CTA, a budget of lb, always are)
+        const int64_t base = (lb + ctas - 1) / ctas;
+        int64_t lo = base - 1, step = kMinChunkTokens + 2 * stage_tokens + unit_cost;
+        int64_t hi = std::min(lb, base + step);
+        while (hi < lb && greedy_fill(items, start, hi, stage_tokens, unit_cost, ctas, nullptr) > ctas) {
+            lo = hi;
+            step *= 2;
+            hi = std::min(lb, base + step);
         }
-        cut[c] = std::max(cut[c - 1], std::min(p, total));
+        while (hi - lo > 1) {
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (greedy_fill(items, start, mid, stage_tokens, unit_cost, ctas, nullptr) <= ctas)
+                hi = mid;
+            else
+                lo = mid;
+        }
+        used = greedy_fill(items, start, hi, stage_tokens, unit_cost, ctas, cut.data());
     }
 
     // pieces: walk every range over the items it touches

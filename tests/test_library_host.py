@@ -155,10 +155,29 @@ def check_plan(indptr, n_kv_heads, head_dim, ctas, plan, hpc=0, shared=None, rpu
     assert len(slot_owner) == plan["partials"] == sum(int(c) for *_, c in merges)
     assert sorted(part_list.tolist()) == list(range(plan["partials"]))
     assert n <= 2 * ctas + 2 * B * groups
-    # each CTA streams about the same number of tokens (ranges snap by <= 32 tokens)
-    loads = [int((units[a:b, 3] - units[a:b, 2]).sum()) for a, b in zip(cta_begin[:-1], cta_begin[1:])]
-    if lengths.sum() >= 64 * ctas and shared is None:
-        assert max(loads) <= chunk * 1.25 + 1
+    # Costed as the kernel spends its time (whole pipeline stages of st tokens plus
+    # a fixed cost per unit), no CTA exceeds the larger of the average cost and the
+    # cost of a context too short to split by more than one CTA's possible slack:
+    # a minimum piece, a stage and a unit.
+    st = 16 * (512 // (hpg * head_dim))
+    uc = max(1, st // 4)
+
+    def cost(t):
+        return -(-int(t) // st) * st + uc if t > 0 else 0
+
+    for b, hg, t0, t1, part, nreq, idx_begin, length in units:
+        if t1 > t0 and part >= 0:
+            # pieces of split contexts start on a stage boundary of their item and
+            # are never shorter than the minimum piece, except an item's whole run
+            start = 0 if (nreq > 1 or length < 0) else int(prefix[b])
+            item_len = (int(prefix[b]) if (nreq > 1 or length < 0) else lengths[b] - start)
+            assert (t0 - start) % st == 0, "a split falls inside a pipeline stage"
+            assert t1 - t0 >= min(64, item_len), "a piece shorter than the minimum"
+    cta_cost = [sum(cost(u[3] - u[2]) for u in units[a:b]) for a, b in zip(cta_begin[:-1], cta_begin[1:])]
+    if shared is None:
+        whole = sum(cost(L) for L in lengths) * groups
+        short = max([cost(L) for L in lengths if L < 2 * 64 + st] + [0])
+        assert max(cta_cost) <= max(whole / ctas, short) + 64 + st + uc
 
 
 @pytest.mark.parametrize("seed", range(8))
@@ -238,8 +257,6 @@ def test_planner_covers_every_token_once(pkv, seed):
     hpc = [0, 1, 2][seed % 3] if min(hkv, 512 // d) >= 2 else 0
     plan = pkv.paged_decode_plan_host(indptr, hkv, d, ctas, heads_per_cta=hpc)
     check_plan(indptr, hkv, d, ctas, plan, hpc)
-    if lengths.sum() * (hkv // (hpc or min(hkv, 512 // d))) >= 64:
-        assert plan["chunk"] >= 64
 
 
 def test_planner_edge_cases(pkv):
@@ -254,10 +271,11 @@ def test_planner_edge_cases(pkv):
     p = pkv.paged_decode_plan_host(np.array([0, 131072], np.int32), 8, 128, 304)
     check_plan([0, 131072], 8, 128, 304, p)
     assert len(p["merges"]) == 2 and p["ctas_used"] == 304
-    # a tiny step uses few CTAs, none with less than 64 tokens
+    # a tiny step: contexts too short for two minimum pieces stay whole, and the
+    # two 30-token ones share a CTA (their stages cost less than the 100-token one's)
     p = pkv.paged_decode_plan_host(np.array([0, 100, 130], np.int32), 8, 128, 304)
     check_plan([0, 100, 130], 8, 128, 304, p)
-    assert p["ctas_used"] == 260 // 64
+    assert p["ctas_used"] == 3 and all(u[4] == -1 for u in p["units"])
     # the skewed 128-request long-context batch
     rng = np.random.default_rng(5)
     L = np.rint(np.exp(rng.uniform(np.log(128), np.log(32768), 127))).astype(np.int64)
