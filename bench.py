@@ -818,10 +818,12 @@ def main(argv=None):
 
 
 def kernel_source_sha() -> str:
-    """sha256 of the decode kernel's sources: csrc/decode.cu, then csrc/ptx.cuh."""
+    """sha256 of the sources that decide a decode call's DRAM traffic: the kernel
+    (csrc/decode.cu, then csrc/ptx.cuh) and the planner that splits the contexts
+    (csrc/plan_host.cpp: the split parts' partial results are part of the traffic)."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("decode.cu", "ptx.cuh"):
+    for name in ("decode.cu", "ptx.cuh", "plan_host.cpp"):
         with open(os.path.join(ROOT, "paged_kv_gqa_tokentokvpool_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -829,8 +831,8 @@ def kernel_source_sha() -> str:
 
 def _profiled_traffic(config_no: int):
     """DRAM bytes per attention call from the committed ncu summary of this workload
-    (profiles/traffic.txt), if it was taken on the current decode-kernel source
-    (csrc/decode.cu followed by csrc/ptx.cuh, hashed together); else None."""
+    (profiles/traffic.txt), if it was taken on the current decode sources (as
+    hashed by kernel_source_sha); else None."""
     sha = kernel_source_sha()
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
