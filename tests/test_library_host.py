@@ -174,9 +174,23 @@ def check_plan(indptr, n_kv_heads, head_dim, ctas, plan, hpc=0, shared=None, rpu
             assert (t0 - start) % st == 0, "a split falls inside a pipeline stage"
             assert t1 - t0 >= min(64, item_len), "a piece shorter than the minimum"
     cta_cost = [sum(cost(u[3] - u[2]) for u in units[a:b]) for a, b in zip(cta_begin[:-1], cta_begin[1:])]
+    # the planner's items: per head group, one per plain request; with shared
+    # prefixes, ceil(run / rpu) prefix items per run and a suffix item per member
+    item_lens = []
     if shared is None:
-        whole = sum(cost(L) for L in lengths) * groups
-        short = max([cost(L) for L in lengths if L < 2 * 64 + st] + [0])
+        item_lens = [int(L) for L in lengths]
+    elif rpu is not None:
+        sp, sl = shared
+        in_run = np.zeros(B, bool)
+        for s in range(len(sp) - 1):
+            if sl[s] > 0 and sp[s + 1] > sp[s]:
+                in_run[sp[s]:sp[s + 1]] = True
+                item_lens += [int(sl[s])] * (-(-(sp[s + 1] - sp[s]) // rpu))
+                item_lens += [int(lengths[m] - sl[s]) for m in range(sp[s], sp[s + 1])]
+        item_lens += [int(lengths[b]) for b in range(B) if not in_run[b]]
+    if item_lens:
+        whole = sum(cost(L) for L in item_lens) * groups
+        short = max([cost(L) for L in item_lens if L < 2 * 64 + st] + [0])
         assert max(cta_cost) <= max(whole / ctas, short) + 64 + st + uc
 
 
