@@ -121,7 +121,10 @@ int paged_decode_plan_create(pkv_plan** plan, int max_batch, int64_t max_tokens,
  * ("Agent-Infer", section "分页 KV 缓存": the plan runs once per step, not once per
  * layer; section "优化历程", stage 3.) Splits long contexts into chunks so that
  * skewed batches fill every SM, and records which requests need a log-sum-exp
- * merge. The result is copied to the device asynchronously on `stream` from the
+ * merge. The persistent CTAs get contiguous ranges of the step's (request, head
+ * group) runs, balanced in the kernel's pipeline stages plus a fixed cost per
+ * piece: the smallest budget that the greedy fill fits into the grid, so the
+ * slowest CTA is as short as that cost model allows. The result is copied to the device asynchronously on `stream` from the
  * plan's pinned staging; every paged_decode_attn call of the step with this
  * batch reuses it.
  *   kv_indptr_host : [batch + 1] int32 HOST array, the same values as the device
