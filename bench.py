@@ -88,6 +88,7 @@ class StepState:
                                                  wl.n_kv_heads, D)
         self.launches_per_step = None
         self.graph = None
+        self.plan_host_s, self.plan_calls = 0.0, 0  # host time of the per-step plan calls
         # The append runs inside the attention launch when every request has a
         # newest token that is its last listed slot (the decode steps here).
         can_fuse = len(wl.append_slots) == wl.batch and wl.batch > 0
@@ -146,11 +147,14 @@ class StepState:
         there is one (and no per-call events are asked for)."""
         pkv = self.pkv
         stream = torch.cuda.current_stream()
+        t0 = time.perf_counter()
         if self.sharing is not None:
             pkv.paged_decode_plan_shared(self.plan, self.kv_indptr_host.numpy(), self.sharing[0],
                                          self.sharing[1], stream=stream)
         else:
             pkv.paged_decode_plan(self.plan, self.kv_indptr_host.numpy(), stream=stream)
+        self.plan_host_s += time.perf_counter() - t0
+        self.plan_calls += 1
         if self.graph is not None and attn_events is None:
             self.graph.replay()
         else:
@@ -781,7 +785,10 @@ def main(argv=None):
             "effective_logical_gbs": world * nbytes["step_logical"] * args.steps
             / (elapsed_ms * 1e-3) / 1e9,
             "plan": {"units": info["n_units"], "merges": info["n_merges"],
-                     "chunk_tokens": info["chunk_tokens"], "ctas": info["n_ctas"]},
+                     "chunk_tokens": info["chunk_tokens"], "ctas": info["n_ctas"],
+                     "host_us_per_step": st.plan_host_s / max(st.plan_calls, 1) * 1e6,
+                     "host_note": "host time of the per-step plan call (partition, staging "
+                                  "and async upload), averaged over every step run"},
             "l2": (f"inputs larger than L2: each step reads {nbytes['step'] / 1e9:.2f} GB "
                    f"across {wl.layers} layers' pools (L2 {L2_BYTES / 2**20:.0f} MiB)"
                    if flush is None else
