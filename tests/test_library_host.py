@@ -399,3 +399,54 @@ def test_prefill_planner_rejects_bad_input(pkv):
         pkv.paged_prefill_plan_host(np.array([0, 1], np.int32), np.array([0, 9], np.int32),
                                     30, 8, 128, 0)
     assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
+
+
+def _fill_count(items, T, st, uc, min_piece=64):
+    """CTAs the documented greedy fill needs at budget T (None when a piece cannot fit
+    an empty CTA): whole items while they fit, then whole stages of the next item,
+    never leaving or taking less than a minimum piece of a split item."""
+    def cost(t):
+        return -(-t // st) * st + uc
+    n, budget = 0, T
+    for length in items:
+        r = length
+        while r > 0:
+            if cost(r) <= budget:
+                budget -= cost(r)
+                break
+            p = (budget - uc) // st * st if budget > uc else 0
+            if r - p < min_piece:
+                p = (r - min_piece) // st * st if r >= min_piece else 0
+            if p >= min_piece:
+                r -= p
+            elif budget == T:
+                return None
+            n += 1
+            budget = T
+    return n + (budget < T)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_planner_budget_is_the_smallest_that_fits(pkv, seed):
+    """No smaller budget than the plan's costliest CTA lets the greedy fill fit the
+    grid: the bisection found the least one."""
+    rng = np.random.default_rng(700 + seed)
+    B = int(rng.integers(1, 40))
+    lengths = rng.integers(0, [300, 3000, 20000][seed % 3], B)
+    ctas = int(rng.integers(1, 64))
+    hkv, d = SHAPES[seed % len(SHAPES)]
+    indptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    plan = pkv.paged_decode_plan_host(indptr, hkv, d, ctas)
+    check_plan(indptr, hkv, d, ctas, plan)
+    hpg = min(hkv, 512 // d)
+    st = 16 * (512 // (hpg * d))
+    uc = max(1, st // 4)
+    units, cb = plan["units"], plan["cta_begin"]
+    costs = [sum(-(-int(u[3] - u[2]) // st) * st + uc for u in units[a:b] if u[3] > u[2])
+             for a, b in zip(cb[:-1], cb[1:])]
+    if max(costs) == 0:
+        return
+    items = [int(L) for L in lengths for _ in range(hkv // hpg)]
+    items = [L for L in items if L > 0]
+    n = _fill_count(items, max(costs) - 1, st, uc)
+    assert n is None or n > ctas, f"budget {max(costs) - 1} fits in {n} of {ctas} CTAs"
