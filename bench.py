@@ -507,32 +507,33 @@ class PrefillState:
         self.graph = g
 
 
-def run_prefill_bench(args):
+def measure_prefill(pf_no: int, steps: int, warmup: int, layers=None, cpu_budget=None):
     """Chunked prefill (the pages' 512- and 64-token chunks): useful causal
     attention FLOP/s of the step, and of the attention kernel alone against the
-    tensor roofline."""
-    pw = workloads.prefill_config(args.prefill)
-    if args.layers is not None:
-        pw.layers = max(1, min(args.layers, pw.layers))
+    tensor roofline. Returns the JSON line as a dict (cpu_baseline only when
+    cpu_budget is given)."""
+    pw = workloads.prefill_config(pf_no)
+    if layers is not None:
+        pw.layers = max(1, min(layers, pw.layers))
     st = PrefillState(pw)
     st.capture()
     stream = torch.cuda.current_stream()
     # causal attention: per query head and attended pair, 2 D flops for q.k and 2 D for p.v
     flops_layer = 4.0 * pw.head_dim * pw.n_qo_heads * pw.attended_pairs()
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         st.run()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clocks:
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             st.run()
         e1.record(stream)
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / steps
     events = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         st.run(events)
     torch.cuda.synchronize()
     attn_ms = float(np.mean([a.elapsed_time(b) for a, b in events]))
@@ -540,12 +541,11 @@ def run_prefill_bench(args):
         raise RuntimeError("a prefill pipeline wait exceeded its bound: the timed results are invalid")
     peak, peak_kind = measured_tensor_peak()
     step_tflops = flops_layer * pw.layers / (ms * 1e-3) / 1e12
-    cpu = None if args.no_cpu_baseline else prefill_cpu_baseline(pw, args.cpu_budget)
     attn_tflops = flops_layer / (attn_ms * 1e-3) / 1e12
-    print(json.dumps({
+    line = {
         "metric": "chunked-prefill attention over the token pool: useful causal TFLOP/s",
-        "value": step_tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+        "value": step_tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": f"{pw.name}: {pw.description}", "layers": pw.layers,
                    "batch": pw.batch, "query_tokens": pw.total_q,
@@ -558,8 +558,18 @@ def run_prefill_bench(args):
                                f"calls {attn_ms * 1e3:.1f} us, tcgen05.mma with TMEM accumulators",
                      "peak_kind": peak_kind},
         "clocks": clocks.summary(),
-        "cpu_baseline": cpu,
-    }), flush=True)
+    }
+    if cpu_budget is not None:
+        line["cpu_baseline"] = prefill_cpu_baseline(pw, cpu_budget)
+    del st
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_prefill_bench(args):
+    line = measure_prefill(args.prefill, args.steps, args.warmup, args.layers,
+                           None if args.no_cpu_baseline else args.cpu_budget)
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -642,52 +652,15 @@ def run_reference(args, world, rank):
     return 0
 
 
-def main(argv=None):
-    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--separate-append", action="store_true",
-                    help="run kvpool_append as its own kernel before each attention call")
-    ap.add_argument("--tier-bench", action="store_true",
-                    help="measure the host KV tier (offload / prefetch) instead of the step")
-    ap.add_argument("--prefill", type=int, default=None, choices=[1, 2, 3],
-                    help="measure a chunked-prefill workload instead of the decode step")
-    ap.add_argument("--no-share", action="store_true",
-                    help="plan the prefix-sharing workload without describing its shared prefixes")
-    ap.add_argument("--no-early", action="store_true",
-                    help="do not let the attention kernel gather before the previous kernel "
-                         "completes (PKV_PLAN_EARLY_GATHER off)")
-    ap.add_argument("--no-graph", action="store_true",
-                    help="launch every layer eagerly instead of replaying a CUDA graph")
-    ap.add_argument("--layers", type=int, default=None,
-                    help="run only the first N layers of the workload (small profiling "
-                         "captures); the JSON line records it")
-    args = ap.parse_args(argv)
-    if args.warmup < 3 and args.impl == "ours":
-        ap.error("--warmup must be >= 3")
-    world, rank, local = _dist()
-    if args.impl == "reference":
-        return run_reference(args, world, rank)
-    if args.tier_bench:
-        return run_tier_bench(args)
-    if args.prefill is not None:
-        return run_prefill_bench(args)
-
-    torch.cuda.set_device(local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-        pg = dist
-
-    wl = workloads.config_workload(args.config)
-    if args.layers is not None:
-        wl.layers = max(1, min(args.layers, wl.layers))
+def measure_decode(config_no: int, args, world=1, pg=None, local=0, cpu_budget=None,
+                   layers=None):
+    """Time one decode workload: K graph-replayed steps (device time, max over
+    ranks), an eager pass that times each attention call alone, and the end-to-end
+    step through the public API with host buffers. Returns the JSON line as a dict
+    (cpu_baseline only when cpu_budget is given)."""
+    wl = workloads.config_workload(config_no)
+    if layers is not None:
+        wl.layers = max(1, min(layers, wl.layers))
         wl.description += f" [first {wl.layers} layers only]"
     st = StepState(wl, fused=not args.separate_append, share=not args.no_share,
                    early=not args.no_early)
@@ -732,13 +705,34 @@ def main(argv=None):
         torch.cuda.synchronize()
         return sum(a.elapsed_time(b) for a, b in pairs)
 
+    st.plan_host_s, st.plan_calls = 0.0, 0
+    st.plan.reset_timing()
     with ClockSampler(local) as clocks:
         step_ms = timed(st.run)
     barrier()
+    plan_timing = st.plan.timing()
+    plan_wall_us = st.plan_host_s / max(st.plan_calls, 1) * 1e6
     elapsed_ms = max_over_ranks(step_ms, pg, "cuda")
+    # The timed loop queues every step at once, so the host runs ahead of the GPU and
+    # each plan call waits for a free staging buffer. Here the host instead waits for
+    # the step two back before planning (it stays two steps ahead): the plan call's
+    # own wait should then be about zero.
+    done = []
+    st.plan.reset_timing()
+    for _ in range(args.steps):
+        if len(done) >= 2:
+            done[-2].synchronize()
+        st.run()
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        done.append(ev)
+    torch.cuda.synchronize()
+    plan_two_ahead = st.plan.timing()
     # The attention calls alone, each bracketed by CUDA events on its stream
     # (eager launches: an event between two kernels also ends their overlap).
     for _ in range(args.steps):
+        if flush is not None:
+            flush.fill_(1)
         st.run(attn_events)
     torch.cuda.synchronize()
     attn_ms = [a.elapsed_time(b) for a, b in attn_events]
@@ -751,11 +745,6 @@ def main(argv=None):
         io.run()
     barrier()
     e2e_ms = max_over_ranks(timed(io.run), pg, "cuda")
-
-    if rank != 0:
-        if pg is not None:
-            pg.destroy_process_group()
-        return 0
 
     ms_per_step = elapsed_ms / args.steps
     value = replica_gbs(world, nbytes["step"], args.steps, elapsed_ms)
@@ -770,7 +759,7 @@ def main(argv=None):
     achieved = nbytes["step"] / n_layers / (layer_ms * 1e-3) / 1e9
     eager_gbs = nbytes["attn_per_layer"] / (attn_avg_ms * 1e-3) / 1e9
     info = st.plan.info()
-    traffic = _profiled_traffic(args.config)
+    traffic = _profiled_traffic(config_no) if layers is None else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -781,20 +770,29 @@ def main(argv=None):
             "batch": wl.batch, "n_qo_heads": wl.n_qo_heads, "n_kv_heads": wl.n_kv_heads,
             "head_dim": wl.head_dim, "pool_slots": wl.pool_slots,
             "total_context_tokens": wl.total_tokens, "us_per_step": ms_per_step * 1e3,
-            "hbm_frac_of_peak": value / peak, "peak_gbs": peak, "peak_kind": peak_kind,
+            "bytes_per_step": nbytes["step"],
+            "hbm_frac_of_peak": value / world / peak, "peak_gbs": peak, "peak_kind": peak_kind,
             "effective_logical_gbs": world * nbytes["step_logical"] * args.steps
             / (elapsed_ms * 1e-3) / 1e9,
             "plan": {"units": info["n_units"], "merges": info["n_merges"],
                      "chunk_tokens": info["chunk_tokens"], "ctas": info["n_ctas"],
-                     "host_us_per_step": st.plan_host_s / max(st.plan_calls, 1) * 1e6,
-                     "host_note": "host time of the per-step plan call (partition, staging "
-                                  "and async upload), averaged over every step run"},
+                     "host_us_per_step": plan_wall_us,
+                     "compute_us_per_step": plan_timing["compute_us"],
+                     "wait_us_per_step": plan_timing["wait_us"],
+                     "wait_us_two_ahead": plan_two_ahead["wait_us"],
+                     "compute_us_two_ahead": plan_two_ahead["compute_us"],
+                     "host_note": "host time of the per-step plan call (wall), of its "
+                                  "partition alone (compute) and of its wait for a free "
+                                  "staging buffer (wait), averaged over the timed steps, "
+                                  "where the host queues every step at once and runs "
+                                  "ahead of the GPU; *_two_ahead: the same with the host "
+                                  "kept two steps ahead of the GPU"},
             "l2": (f"inputs larger than L2: each step reads {nbytes['step'] / 1e9:.2f} GB "
                    f"across {wl.layers} layers' pools (L2 {L2_BYTES / 2**20:.0f} MiB)"
                    if flush is None else
                    f"L2 flushed between timed steps (a {2 * L2_BYTES / 2**20:.0f} MiB write); "
                    f"each step reads {nbytes['step'] / 1e6:.1f} MB"),
-            "hbm_frac_of_nominal": value / NOMINAL_HBM_GBS,
+            "hbm_frac_of_nominal": value / world / NOMINAL_HBM_GBS,
             "parallelism": f"replicas x{world}",
             "launch": "eager" if args.no_graph else "cuda graph of the layer loop per step; plan on host",
             "append": "fused into the attention launch" if st.fused else "separate kernel",
@@ -809,16 +807,109 @@ def main(argv=None):
                                f"{nbytes['step'] / n_layers / 1e6:.1f} MB algorithmic per call",
                      "eager_call": {"us": attn_avg_ms * 1e3, "gbs": eager_gbs,
                                     "note": f"avg of {len(attn_ms)} calls each timed alone with "
-                                            "events (eager launches, no overlap between calls)"},
+                                            "events (eager launches, no overlap between calls"
+                                            + (", L2 flushed before each step)" if flush is not None
+                                               else ")")},
                      "peak_kind": peak_kind},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": io.h2d_bytes,
                 "d2h_bytes_per_step": io.d2h_bytes, "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": st.launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(st, budget_s=args.cpu_budget)
-    print(json.dumps(line), flush=True)
+    if cpu_budget is not None and world == 1:
+        line["cpu_baseline"] = cpu_baseline(st, budget_s=cpu_budget)
+    del io, st
+    torch.cuda.empty_cache()
+    return line
+
+
+def sweep_entry(line: dict) -> dict:
+    """The figures of one workload's bench line that the sweep records."""
+    c, r = line["config"], line["roofline"]
+    e = {"workload": c["workload"], "layers": c["layers"], "batch": c["batch"],
+         "steps": line["steps"], "clocks": line["clocks"]}
+    if line["unit"] == "GB/s":
+        e.update({"us_per_step": c["us_per_step"], "gbs": line["value"],
+                  "frac_of_measured": c["hbm_frac_of_peak"],
+                  "frac_of_nominal": c["hbm_frac_of_nominal"], "peak_kind": c["peak_kind"],
+                  "bytes_per_step": c["bytes_per_step"],
+                  "attn_call_eager_us": r["eager_call"]["us"], "e2e_gbs": line["e2e"]["value"],
+                  "e2e_us_per_step": line["e2e"]["ms_per_step"] * 1e3, "plan": c["plan"],
+                  "l2": c["l2"], "shared_prefixes": c["shared_prefixes"]})
+    else:
+        e.update({"ms_per_step": line["ms_per_step"], "tflops": line["value"],
+                  "attn_call_tflops": r["achieved"], "frac_of_measured_sustained": r["frac"],
+                  "peak_kind": r["peak_kind"]})
+    return e
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--separate-append", action="store_true",
+                    help="run kvpool_append as its own kernel before each attention call")
+    ap.add_argument("--tier-bench", action="store_true",
+                    help="measure the host KV tier (offload / prefetch) instead of the step")
+    ap.add_argument("--prefill", type=int, default=None, choices=[1, 2, 3],
+                    help="measure a chunked-prefill workload instead of the decode step")
+    ap.add_argument("--no-share", action="store_true",
+                    help="plan the prefix-sharing workload without describing its shared prefixes")
+    ap.add_argument("--no-early", action="store_true",
+                    help="do not let the attention kernel gather before the previous kernel "
+                         "completes (PKV_PLAN_EARLY_GATHER off)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every layer eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers of the workload (small profiling "
+                         "captures); the JSON line records it")
+    ap.add_argument("--sweep", dest="sweep", action="store_true", default=None,
+                    help="also time the other decode workloads and the chunked-prefill "
+                         "workloads and record them under config.sweep (default on one GPU "
+                         "for the default workload)")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    if args.tier_bench:
+        return run_tier_bench(args)
+    if args.prefill is not None:
+        return run_prefill_bench(args)
+
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    sweep = args.sweep
+    if sweep is None:
+        sweep = world == 1 and args.config == DEFAULT_CONFIG and args.layers is None
+
+    line = measure_decode(args.config, args, world, pg, local,
+                          None if args.no_cpu_baseline else args.cpu_budget, args.layers)
+    if sweep:
+        # The other decode workloads (batch 1, 32, 16 and 128) and the chunked-prefill
+        # workloads, each timed like the default one, one after the other with the
+        # previous one's memory released.
+        entries = {}
+        for no in (1, 3, 4, 5):
+            if no != args.config:
+                entries[f"cfg{no}"] = sweep_entry(measure_decode(no, args, world, pg, local))
+        for no in (1, 2, 3):
+            entries[f"pf{no}"] = sweep_entry(measure_prefill(no, args.steps, args.warmup))
+        entries[f"cfg{args.config}"] = sweep_entry(line)
+        line["config"]["sweep"] = entries
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
     return 0

@@ -130,9 +130,11 @@ int paged_decode_plan_create(pkv_plan** plan, int max_batch, int64_t max_tokens,
  *   kv_indptr_host : [batch + 1] int32 HOST array, the same values as the device
  *                    kv_indptr later passed to paged_decode_attn
  *   batch          : 0 <= batch <= max_batch; kv_indptr_host[batch] <= max_tokens
- * Before overwriting its staging the call waits (host side) for the previous
- * step's plan copy to finish. Use the same stream (or order the streams) for the
- * plan and the attention calls of a step.
+ * The plan has two pinned staging buffers and fills them in turn, so before
+ * filling one the call waits (host side) only for the upload of the step before
+ * the previous one: the host may run up to two steps ahead of the GPU without
+ * blocking here. Use the same stream (or order the streams) for the plan and the
+ * attention calls of a step.
  */
 int paged_decode_plan(pkv_plan* plan, const int32_t* kv_indptr_host, int batch,
                       pkv_stream_t stream);
@@ -147,10 +149,16 @@ int paged_decode_plan(pkv_plan* plan, const int32_t* kv_indptr_host, int batch,
  * newest token is private). The attention kernel then reads each shared slot once
  * for up to 16 / G requests at a time (16 query rows per KV head) instead
  * of once per request, and merges each member's prefix and suffix parts by
- * log-sum-exp. The description is a hint about equal slot ids: results are the
- * same as with paged_decode_plan (up to fp32 rounding), and for shapes without a
- * shared-prefix kernel (only head_dim 128 with 4 KV heads per group has one) it is
- * ignored. Otherwise as paged_decode_plan.
+ * log-sum-exp.
+ * PRECONDITION: the members of a run list identical slot ids in their first
+ * shared_len_host[s] entries of kv_indices. The kernel reads the shared slots from
+ * the first member's list on behalf of all members, so a description that is not
+ * true of kv_indices gives wrong results for the other members. With debug checks
+ * on (pkv_set_debug_checks), the attention calls that use the plan verify it on
+ * the host and return PKV_ERR_INDEX, launching nothing, when it does not hold.
+ * When it holds, results are those of paged_decode_plan (up to fp32 rounding).
+ * For shapes without a shared-prefix kernel (only head_dim 128 with 4 KV heads
+ * per group has one) the description is not used. Otherwise as paged_decode_plan.
  */
 int paged_decode_plan_shared(pkv_plan* plan, const int32_t* kv_indptr_host, int batch,
                              const int32_t* shared_indptr_host, int n_shared,
@@ -213,25 +221,42 @@ int paged_decode_append_attn(const void* q, void* k_pool, void* v_pool, const in
  * that must not hit cudaMalloc's implicit synchronisation. The paper has no
  * counterpart; it is an addition of this library.
  *   Arguments as for paged_decode_attn, plus kv_indptr_host ([batch + 1] int32
- *   HOST copy of kv_indptr); there is no plan: every call plans the step on the
- *   host.
+ *   HOST copy of kv_indptr, read during the call only); there is no plan: every
+ *   call plans the step on the host.
  *   Scratch: the work list, a status word, a zero row and the split workspace live
  *   in one file-scope __device__ array of 32 MiB that every GPU loading the library
- *   holds until exit; nothing is allocated. The first call on a device (with that
- *   device current) looks the array up with cudaGetSymbolAddress; make it before
- *   any stream capture. Steps needing more than 32 MiB of scratch (or more than
- *   1024 CTAs, 4096 (request, head group) pairs or 8192 work units) return
- *   PKV_ERR_PLAN with the size in the message.
- *   All calls share the array and leave its contents behind (the status word and
- *   zero row are cleared on every call): calls whose kernels overlap on the GPU
- *   race. Calls from several host threads are serialised on the host.
- *   The work list is copied from pageable host memory with cudaMemcpyAsync.
+ *   holds until exit; nothing is allocated. The CUDA driver places the array on a
+ *   device when it loads the library's code there (with lazy module loading, at
+ *   the first call). The first call on a device (with that device current) looks
+ *   the array up with cudaGetSymbolAddress and zeroes its status word and zero row
+ *   on `stream`, waiting for that; make it before any stream capture. Steps needing
+ *   more than 32 MiB of scratch (or more than 1024 CTAs, 4096 (request, head
+ *   group) pairs or 8192 work units) return PKV_ERR_PLAN with the size in the
+ *   message.
+ *   All calls share the array and leave its contents behind: calls whose kernels
+ *   overlap on the GPU race. Calls queued one after another on one stream are
+ *   ordered. Calls from several host threads are serialised on the host.
+ *   The work list is copied from pageable host memory with cudaMemcpyAsync; the
+ *   CUDA runtime may block the host during that copy until it has staged the
+ *   bytes.
+ *   A bounded pipeline wait that runs out (1 s) sets the array's status word,
+ *   which stays set until paged_decode_attn_static_status reads it.
  */
 int paged_decode_attn_static(const void* q, const void* k_pool, const void* v_pool,
                              const int32_t* kv_indptr_host, const int32_t* kv_indptr,
                              const int32_t* kv_indices, int batch, int n_qo_heads,
                              int n_kv_heads, int head_dim, float sm_scale, void* out,
                              float* lse, pkv_stream_t stream);
+
+/*
+ * paged_decode_attn_static_status — wait for `stream` and the device, then read
+ * and clear the status word of paged_decode_attn_static's array on the current
+ * device (this library's own; the paper has no counterpart). *status = 0: every
+ * static call since the last read completed its pipeline waits (or none ran on
+ * this device); nonzero: some wait exceeded its bound and that call's outputs are
+ * invalid. Allocates nothing.
+ */
+int paged_decode_attn_static_status(pkv_stream_t stream, int* status);
 
 /* paged_decode_plan_destroy — free a plan (waits for its pending copy). NULL is a no-op. */
 void paged_decode_plan_destroy(pkv_plan* plan);
@@ -372,6 +397,17 @@ int paged_prefill_plan_status(pkv_prefill_plan* plan, int* status);
 
 /* paged_prefill_plan_destroy — free a prefill plan (waits for its pending upload). NULL is a no-op. */
 void paged_prefill_plan_destroy(pkv_prefill_plan* plan);
+
+/*
+ * paged_decode_plan_host_times — host time spent by the plan's successful
+ * paged_decode_plan / paged_decode_plan_shared calls since the last reset (this
+ * library's own; the pages have no counterpart): in the partition itself
+ * (*compute_us) and waiting for a staging buffer to be free (*wait_us), summed
+ * over *calls calls, in microseconds. reset != 0 zeroes the counters after they
+ * are read. Any out pointer may be NULL. No CUDA call.
+ */
+int paged_decode_plan_host_times(pkv_plan* plan, double* compute_us, double* wait_us,
+                                 int64_t* calls, int reset);
 
 /* Flags for paged_decode_plan_set_flags. */
 #define PKV_PLAN_EARLY_GATHER 1u

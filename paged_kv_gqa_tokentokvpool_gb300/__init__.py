@@ -42,7 +42,9 @@ EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
             "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_destroy",
             "paged_prefill_plan_host", "paged_prefill_plan_status",
-            "pkv_set_debug_checks", "pkv_inject_stall", "pkv_last_error")
+            "paged_decode_plan_host_times", "paged_decode_attn_static_status",
+            "pkv_set_debug_checks", "pkv_inject_stall",
+            "pkv_last_error")
 
 
 class PkvError(RuntimeError):
@@ -75,6 +77,8 @@ def _load() -> ctypes.CDLL:
     lib.paged_decode_plan_info.argtypes = [P, P, P, P, P, P]
     lib.paged_decode_plan_status.argtypes = [P, P]
     lib.paged_decode_plan_set_flags.argtypes = [P, ctypes.c_uint]
+    lib.paged_decode_plan_host_times.argtypes = [P, P, P, P, I32]
+    lib.paged_decode_attn_static_status.argtypes = [P, P]
     lib.paged_prefill_plan_create.argtypes = [ctypes.POINTER(P), I32, I64, I32, I32, I32]
     lib.paged_prefill_plan.argtypes = [P, P, P, I32, P]
     lib.paged_prefill_attn.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, ctypes.c_float,
@@ -99,7 +103,8 @@ def _load() -> ctypes.CDLL:
                  "paged_decode_append_attn", "paged_decode_plan_shared", "kvpool_offload",
                  "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
                  "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_host",
-                 "paged_prefill_plan_status"):
+                 "paged_prefill_plan_status", "paged_decode_plan_host_times",
+                 "paged_decode_attn_static_status"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -184,6 +189,20 @@ class Plan:
     def set_flags(self, flags: int) -> None:
         """paged_decode_plan_set_flags (e.g. PKV_PLAN_EARLY_GATHER)."""
         paged_decode_plan_set_flags(self, flags)
+
+    def timing(self, reset: bool = False) -> dict:
+        """Host time of the plan calls since the last reset (paged_decode_plan_host_times):
+        per call on average, in the partition (compute_us) and waiting for a free
+        staging buffer (wait_us)."""
+        c, w, n = ctypes.c_double(), ctypes.c_double(), ctypes.c_int64()
+        _check(library().paged_decode_plan_host_times(self.handle, ctypes.byref(c),
+                                                      ctypes.byref(w), ctypes.byref(n),
+                                                      1 if reset else 0))
+        calls = max(n.value, 1)
+        return {"compute_us": c.value / calls, "wait_us": w.value / calls, "calls": n.value}
+
+    def reset_timing(self) -> None:
+        self.timing(reset=True)
 
     def __del__(self):
         if getattr(self, "handle", None) and _lib is not None:
@@ -316,12 +335,13 @@ def paged_decode_append_attn(q, k_pool, v_pool, kv_indptr, kv_indices, slot_ids,
         float(sm_scale), _ptr(out), _ptr(lse), plan.handle, _stream(stream)))
 
 
-def paged_decode_attn_static(q, k_pool, v_pool, kv_indptr_host, kv_indptr, kv_indices, batch,
-                             n_qo_heads, n_kv_heads, head_dim, sm_scale, out, lse,
-                             stream=None) -> None:
+def paged_decode_attn_static(q, k_pool, v_pool, kv_indptr_host, kv_indptr, kv_indices,
+                             batch=None, n_qo_heads=None, n_kv_heads=None, head_dim=None,
+                             sm_scale=None, out=None, lse=None, stream=None) -> None:
     """paged_decode_attn without a plan and without any device allocation: the
     step is planned on every call and all scratch lives in the library's static
-    32 MiB device array (see include/pkv.h for the sharing rules)."""
+    32 MiB device array (see include/pkv.h for the sharing rules). batch defaults
+    to the host offsets' length - 1 and may not exceed it."""
     _dev(q, torch.bfloat16, "q")
     _dev(k_pool, torch.bfloat16, "k_pool")
     _dev(v_pool, torch.bfloat16, "v_pool")
@@ -331,10 +351,28 @@ def paged_decode_attn_static(q, k_pool, v_pool, kv_indptr_host, kv_indptr, kv_in
     if lse is not None:
         _dev(lse, torch.float32, "lse")
     ip = _host_indptr(kv_indptr_host)
+    batch = ip.size - 1 if batch is None else int(batch)
+    if batch < 0 or ip.size < batch + 1:
+        raise ValueError(f"kv_indptr_host has {ip.size} entries; batch {batch} needs {batch + 1}")
+    if kv_indptr.numel() < batch + 1:
+        raise ValueError(f"kv_indptr has {kv_indptr.numel()} entries; batch {batch} needs {batch + 1}")
+    S, hkv, d = k_pool.shape
+    n_kv_heads = hkv if n_kv_heads is None else n_kv_heads
+    head_dim = d if head_dim is None else head_dim
+    n_qo_heads = q.shape[1] if n_qo_heads is None else n_qo_heads
+    # ip (the host offsets) is referenced until the call returns
     _check(library().paged_decode_attn_static(
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(ip), _ptr(kv_indptr), _ptr(kv_indices), batch,
         n_qo_heads, n_kv_heads, head_dim, float(sm_scale), _ptr(out), _ptr(lse),
         _stream(stream)))
+
+
+def paged_decode_attn_static_status(stream=None) -> int:
+    """Wait for the stream, then read and clear the status word of the static entry
+    point's array on the current device (0 = every pipeline wait completed)."""
+    v = ctypes.c_int()
+    _check(library().paged_decode_attn_static_status(_stream(stream), ctypes.byref(v)))
+    return v.value
 
 
 def paged_decode_plan_set_flags(plan: Plan, flags: int) -> None:

@@ -7,6 +7,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -51,24 +52,6 @@ bool take_injected_stall() {
     while (stalls > 0 && !g_stalls_to_inject.compare_exchange_weak(stalls, stalls - 1)) {
     }
     return stalls > 0;
-}
-
-int choose_heads_per_cta(int n_kv_heads, int head_dim) {
-    int hpg = heads_per_group(n_kv_heads, head_dim);
-    if (const char* env = std::getenv("PKV_HEADS_PER_CTA")) {
-        const int want = std::atoi(env);
-        if ((want == 1 || want == 2 || want == 4) && want <= hpg && n_kv_heads % want == 0)
-            hpg = want;
-    }
-    return hpg;
-}
-
-int shared_row_blocks() {
-    static const int rb = [] {
-        const char* env = std::getenv("PKV_SHARED_ROW_BLOCKS");
-        return env && std::atoi(env) == 2 ? 2 : 1;
-    }();
-    return rb;
 }
 
 bool pdl_enabled() {
@@ -312,11 +295,13 @@ void paged_decode_plan_destroy(pkv_plan* p) {
     int prev = -1;
     cudaGetDevice(&prev);
     cudaSetDevice(p->device);
-    if (p->copy_done) {
-        cudaEventSynchronize(p->copy_done);
-        cudaEventDestroy(p->copy_done);
+    for (int i = 0; i < 2; ++i) {
+        if (p->copy_done[i]) {
+            cudaEventSynchronize(p->copy_done[i]);
+            cudaEventDestroy(p->copy_done[i]);
+        }
+        if (p->host_staging[i]) cudaFreeHost(p->host_staging[i]);
     }
-    if (p->host_staging) cudaFreeHost(p->host_staging);
     if (p->dev_meta) cudaFree(p->dev_meta);
     if (p->ws_o) cudaFree(p->ws_o);
     if (p->ws_lse) cudaFree(p->ws_lse);
@@ -352,11 +337,11 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
         delete p;
         return cuda_fail(e, "paged_decode_plan_create: device query");
     }
-    const int hpg = choose_heads_per_cta(n_kv_heads, head_dim);
+    const int hpg = heads_per_group(n_kv_heads, head_dim);
     p->heads_per_cta = hpg;
     p->ctas_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg, false);
-    // Shared-prefix units serve 16 x (row blocks) / G requests where a kernel for
-    // them exists; it runs on its own fixed grid.
+    // Shared-prefix units serve 16 / G requests where a kernel for them exists; it
+    // runs on its own fixed grid.
     const int shared_per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpg, true);
     p->share_rows = shared_per_sm > 0
                         ? decode_shared_rows(n_qo_heads, n_kv_heads, head_dim, hpg) /
@@ -365,12 +350,6 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     if (p->ctas_per_sm <= 0) {
         delete p;
         return fail(PKV_ERR_CUDA, "paged_decode_plan_create: occupancy query failed");
-    }
-    // Tuning knob: PKV_CTAS_PER_SM (>= 1) launches fewer persistent CTAs per SM
-    // than fit (longer ranges, fewer split contexts).
-    if (const char* env = std::getenv("PKV_CTAS_PER_SM")) {
-        const int want = std::atoi(env);
-        if (want >= 1 && want < p->ctas_per_sm) p->ctas_per_sm = want;
     }
     p->ctas = p->num_sms * p->ctas_per_sm;
     p->ctas_shared = p->share_rows > 0 ? p->num_sms * shared_per_sm : 0;
@@ -402,7 +381,8 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     const size_t ws_o_bytes = sizeof(float) * size_t(p->lim.max_partials) * group_q_heads * head_dim;
     const size_t ws_lse_bytes = sizeof(float) * size_t(p->lim.max_partials) * group_q_heads;
     const size_t state_bytes = sizeof(int) * 32;
-    e = cudaMallocHost(&p->host_staging, p->meta_bytes);
+    e = cudaMallocHost(&p->host_staging[0], p->meta_bytes);
+    if (e == cudaSuccess) e = cudaMallocHost(&p->host_staging[1], p->meta_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&p->dev_meta, p->meta_bytes);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_o), ws_o_bytes);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->ws_lse), ws_lse_bytes);
@@ -410,7 +390,8 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     if (e == cudaSuccess) e = cudaMemset(p->dev_state, 0, state_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&p->zero_row, sizeof(uint16_t) * kHeadGroupElems);
     if (e == cudaSuccess) e = cudaMemset(p->zero_row, 0, sizeof(uint16_t) * kHeadGroupElems);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->copy_done, cudaEventDisableTiming);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+        e = cudaEventCreateWithFlags(&p->copy_done[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         paged_decode_plan_destroy(p);
@@ -446,13 +427,17 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
         for (int s = 0; s < n_shared; ++s)
             share |= shared_len_host[s] > 0 && shared_indptr_host[s + 1] > shared_indptr_host[s];
     const PlanSharing sh{shared_indptr_host, shared_len_host, n_shared, p->share_rows};
-    // The staging buffer may still feed the previous step's copy.
-    if (p->copy_pending) {
-        cudaError_t e = cudaEventSynchronize(p->copy_done);
-        if (e != cudaSuccess) return cuda_fail(e, "waiting for the previous plan copy");
-        p->copy_pending = false;
+    // The staging buffer this call fills may still feed the upload of the step
+    // before the previous one (the buffers are used in turn).
+    const int sb = p->next_staging;
+    const auto t0 = std::chrono::steady_clock::now();
+    if (p->copy_pending[sb]) {
+        cudaError_t e = cudaEventSynchronize(p->copy_done[sb]);
+        if (e != cudaSuccess) return cuda_fail(e, "waiting for an earlier plan copy");
+        p->copy_pending[sb] = false;
     }
-    char* st = static_cast<char*>(p->host_staging);
+    const auto t1 = std::chrono::steady_clock::now();
+    char* st = static_cast<char*>(p->host_staging[sb]);
     PlanCounts c{};
     const int ctas = share ? p->ctas_shared : p->ctas;
     rc = plan_compute(kv_indptr_host, batch, p->n_groups, ctas,
@@ -463,15 +448,27 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
                       reinterpret_cast<Merge*>(st + p->off_merge),
                       reinterpret_cast<int32_t*>(st + p->off_list), &c);
     if (rc != PKV_OK) return rc;
+    const auto t2 = std::chrono::steady_clock::now();
     int32_t* header = reinterpret_cast<int32_t*>(st);
     header[0] = c.n_merges;
     header[1] = c.n_partials;
     header[2] = header[3] = 0;
     const size_t bytes = p->off_units + sizeof(Unit) * c.n_units;
     cudaError_t e = cudaMemcpyAsync(p->dev_meta, st, bytes, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaEventRecord(p->copy_done, stream);
+    if (e == cudaSuccess) e = cudaEventRecord(p->copy_done[sb], stream);
     if (e != cudaSuccess) return cuda_fail(e, "plan upload");
-    p->copy_pending = true;
+    p->copy_pending[sb] = true;
+    p->next_staging = sb ^ 1;
+    p->wait_ns += std::chrono::duration<double, std::nano>(t1 - t0).count();
+    p->compute_ns += std::chrono::duration<double, std::nano>(t2 - t1).count();
+    ++p->timed_calls;
+    if (share) {
+        p->shared_indptr_host.assign(shared_indptr_host, shared_indptr_host + n_shared + 1);
+        p->shared_len_host.assign(shared_len_host, shared_len_host + n_shared);
+    } else {
+        p->shared_indptr_host.clear();
+        p->shared_len_host.clear();
+    }
     p->batch = batch;
     p->counts = c;
     p->shared = share;
@@ -505,6 +502,20 @@ int paged_decode_plan_info(const pkv_plan* p, int* batch, int* n_units, int* n_m
     if (n_merges) *n_merges = p->counts.n_merges;
     if (chunk_tokens) *chunk_tokens = p->counts.chunk_tokens;
     if (n_ctas) *n_ctas = p->counts.n_ctas;
+    return PKV_OK;
+}
+
+int paged_decode_plan_host_times(pkv_plan* p, double* compute_us, double* wait_us,
+                                 int64_t* calls, int reset) {
+    clear_error();
+    if (!p) return fail(PKV_ERR_PLAN, "paged_decode_plan_host_times: plan is NULL");
+    if (compute_us) *compute_us = p->compute_ns * 1e-3;
+    if (wait_us) *wait_us = p->wait_ns * 1e-3;
+    if (calls) *calls = p->timed_calls;
+    if (reset) {
+        p->compute_ns = p->wait_ns = 0;
+        p->timed_calls = 0;
+    }
     return PKV_OK;
 }
 
@@ -586,6 +597,21 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
                 if (idx[i] < 0 || (pool_slots > 0 && idx[i] >= pool_slots))
                     return fail(PKV_ERR_INDEX, "%s: kv_indices[%d] = %d is not a pool slot", who, i,
                                 idx[i]);
+        }
+        if (p->shared) {
+            // the shared-prefix kernel reads each shared slot once, from the first
+            // member's list, for every member: the members must list the same ids
+            const std::vector<int32_t>& sp = p->shared_indptr_host;
+            const std::vector<int32_t>& sl = p->shared_len_host;
+            for (size_t s = 0; s + 1 < sp.size(); ++s)
+                for (int m = sp[s] + 1; m < sp[s + 1]; ++m)
+                    for (int32_t j = 0; j < sl[s]; ++j)
+                        if (idx[ip[m] + j] != idx[ip[sp[s]] + j])
+                            return fail(PKV_ERR_INDEX,
+                                        "%s: request %d lists slot %d at position %d of its shared "
+                                        "prefix, but request %d (the first of its sharing group) "
+                                        "lists %d there", who, m, idx[ip[m] + j], j, sp[s],
+                                        idx[ip[sp[s]] + j]);
         }
         if (fused) {
             std::vector<int32_t> ids(batch);

@@ -12,11 +12,14 @@
 // process exits.
 //
 // Set-up: the first call on a device (with that device current) looks up the
-// array's device address with cudaGetSymbolAddress and keeps it for later calls;
-// make that first call before any stream capture. Every call shares the one array
-// and leaves its contents behind, so calls whose kernels overlap on the GPU (two
-// streams, or two host threads without ordering) race on it; the host side holds
-// a mutex for the duration of each call.
+// array's device address with cudaGetSymbolAddress, keeps it for later calls, and
+// zeroes the status word and the zero row on the call's stream, waiting for that
+// (the only synchronisation the entry point does); make that first call before any
+// stream capture. Every call shares the one array and leaves its contents behind,
+// so calls whose kernels overlap on the GPU (two streams, or two host threads
+// without ordering) race on it; the host side holds a mutex for the duration of
+// each call. The status word is set by a kernel whose bounded pipeline wait ran
+// out and stays set until paged_decode_attn_static_status reads and clears it.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -96,11 +99,18 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
         if (e != cudaSuccess || ptr == nullptr)
             return fail(PKV_ERR_CUDA, "paged_decode_attn_static: cudaGetSymbolAddress: %s",
                         cudaGetErrorString(e));
+        // the status word and the zero row start at zero; no kernel writes the
+        // zero row, and only paged_decode_attn_static_status clears the status
+        e = cudaMemsetAsync(static_cast<unsigned char*>(ptr) + kOffStatus, 0,
+                            kOffWork - kOffStatus, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess)
+            return fail(PKV_ERR_CUDA, "paged_decode_attn_static: set-up: %s", cudaGetErrorString(e));
         g_scratch_addr[dev] = ptr;
     }
     unsigned char* scratch = static_cast<unsigned char*>(g_scratch_addr[dev]);
 
-    const int hpc = choose_heads_per_cta(n_kv_heads, head_dim);
+    const int hpc = heads_per_group(n_kv_heads, head_dim);
     const int per_sm = decode_ctas_per_sm(n_qo_heads, n_kv_heads, head_dim, hpc, false);
     if (per_sm <= 0) return fail(PKV_ERR_CUDA, "paged_decode_attn_static: occupancy query failed");
     const int ctas = sms * per_sm;
@@ -134,11 +144,11 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     header[2] = header[3] = 0;
 
     // Upload the work list from the (pageable) staging: the copy has read the
-    // staging when cudaMemcpyAsync returns, so the next call may overwrite it.
+    // staging when cudaMemcpyAsync returns, so the next call may overwrite it. The
+    // kernels that follow on the stream start only after this copy has completed,
+    // which orders them after the previous call's kernels on the same stream.
     e = cudaMemcpyAsync(scratch, g_stage, kOffUnits + sizeof(Unit) * c.n_units,
                         cudaMemcpyHostToDevice, stream);
-    // The status word and the zero row must start at zero on every call.
-    if (e == cudaSuccess) e = cudaMemsetAsync(scratch + kOffStatus, 0, kOffWork - kOffStatus, stream);
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "paged_decode_attn_static: upload: %s", cudaGetErrorString(e));
 
@@ -153,7 +163,7 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     a.part_list = reinterpret_cast<const int32_t*>(scratch + kOffList);
     a.shared = false;
     a.early = false;
-    a.withhold = false;
+    a.withhold = take_injected_stall();
     a.units = reinterpret_cast<const Unit*>(scratch + kOffUnits);
     a.n_ctas = ctas;
     a.heads_per_cta = hpc;
@@ -171,5 +181,29 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     e = launch_decode(a, stream);
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "paged_decode_attn_static: launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
+
+extern "C" int paged_decode_attn_static_status(pkv_stream_t stream, int* status) {
+    clear_error();
+    if (!status) return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn_static_status: status is NULL");
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail(PKV_ERR_CUDA, "paged_decode_attn_static_status: device query failed");
+    *status = 0;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "paged_decode_attn_static_status: %s", cudaGetErrorString(e));
+    if (g_scratch_addr[dev] == nullptr) return PKV_OK;  // no call has run on this device
+    int* word = reinterpret_cast<int*>(static_cast<unsigned char*>(g_scratch_addr[dev]) + kOffStatus);
+    int v = 0;
+    e = cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && v != 0) e = cudaMemset(word, 0, sizeof v);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "paged_decode_attn_static_status: %s", cudaGetErrorString(e));
+    *status = v;
     return PKV_OK;
 }

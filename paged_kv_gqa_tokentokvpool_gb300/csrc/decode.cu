@@ -105,26 +105,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
 // ---------------------------------------------------------------------------
 
 // Shapes of one instance: head_dim D, GQA group G, WPH consumer warps per KV
-// head (so 4 / WPH KV heads per CTA), NB 8-row query blocks per warp and RB row
-// blocks of warps. A unit's query rows (row r = head r % G of its request r / G)
-// are dealt to RB sets of four warps, 8 NB rows each: RB = 1 serves 8 NB / G
-// requests per unit with two CTAs per SM; RB = 2 doubles the warps and runs one
-// CTA per SM, so each K/V row staged in shared memory serves 16 NB / G requests.
-// Under RB = 2 a unit whose rows fit one row block (a private suffix, say) is
-// dealt by stages instead: set s takes the unit's stages t with t % 2 == s, and
-// set 1 hands its softmax state (m, l, o) to set 0 through shared memory at the
-// unit's end, where set 0 folds the two by the log-sum-exp identity. So no warp
-// idles on a unit of one request. A pipeline stage holds kSub 16-token
-// sub-tiles of K rows and of V rows of the CTA's kHeadsPerCta heads; kSub is
-// chosen so that every stage carries 16 x kHeadGroupElems bf16 of K and as much
-// of V (32 KB, plus row padding) whatever the head count.
-template <int D, int G, int WPH, int NB = 1, int RB = 1>
+// head (so 4 / WPH KV heads per CTA) and NB 8-row query blocks per warp. A unit's
+// query rows (row r = head r % G of its request r / G) are 8 NB per warp, so a
+// unit serves 8 NB / G requests (NB = 2: the shared-prefix instance). Two CTAs run
+// per SM. A pipeline stage holds kSub 16-token sub-tiles of K rows and of V rows
+// of the CTA's kHeadsPerCta heads; kSub is chosen so that every stage carries
+// 16 x kHeadGroupElems bf16 of K and as much of V (32 KB, plus row padding)
+// whatever the head count.
+template <int D, int G, int WPH, int NB = 1>
 struct Cfg {
-    static constexpr int kConsumerWarps = kGroupWarps * RB;
-    static constexpr int kProducerWarps = kProducersPerBlock * RB;  // each issues 1 / P of the copies
+    static constexpr int kConsumerWarps = kGroupWarps;
+    static constexpr int kProducerWarps = kProducersPerBlock;  // each issues 1 / P of the copies
     static constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
-    static constexpr int kStages = RB == 1 ? 3 : 5;             // 32 KB stages in flight
-    static constexpr int kMinBlocks = 2 / RB;                   // resident CTAs per SM
+    static constexpr int kStages = 3;                           // 32 KB stages in flight
+    static constexpr int kMinBlocks = 2;                        // resident CTAs per SM
     static constexpr int kWarpRows = 8 * NB;                    // query rows of one warp
     static constexpr int kHeadsPerCta = kGroupWarps / WPH;      // KV heads of one group
     static constexpr int kRow = kHeadsPerCta * D * 2;           // bytes of a staged row
@@ -139,23 +133,15 @@ struct Cfg {
     static constexpr int kQHeads = kHeadsPerCta * G;            // query heads of a group
     static constexpr int kAhead = kStages + 1;                  // stages of slot ids in flight
     static constexpr int kBarOffset = kStages * kStage;
-    // hand-over barriers of the stage-dealt units: full and empty per warp of set 1
-    static constexpr int kXBars = RB == 2 ? 2 * kGroupWarps : 0;
-    static constexpr int kIdxOffset = kBarOffset + (2 * kStages + kXBars) * 8 + 16;
-    // hand-over buffer: per warp of set 1, per lane, m and l of its 2 NB columns
-    // and its 4 NB kMBlocks output accumulators, stored [value][lane]
-    static constexpr int kXFloats = NB * (4 + 4 * kMBlocks);
+    static constexpr int kIdxOffset = kBarOffset + 2 * kStages * 8 + 16;
     // copies of one stage: K then V rows of kStageTokens tokens; copy c is issued by
     // producer warp c % P, lane (c / P) % 32
     static constexpr int kCopies = 2 * kStageTokens;
     static constexpr int kCopiesPerLane = (kCopies / kProducerWarps + 31) / 32;
     static constexpr int kIdRing = kAhead * kStageTokens * 4;  // slot-id ring of one producer warp
-    static constexpr int kXOffset = (kIdxOffset + kProducerWarps * kIdRing + 15) / 16 * 16;
-    static constexpr int kSmem = kXOffset + (RB == 2 ? kGroupWarps * 32 * kXFloats * 4 : 0);
+    static constexpr int kSmem = kIdxOffset + kProducerWarps * kIdRing;
     static_assert(G >= 1 && G <= 8, "group size");
     static_assert(NB == 1 || NB == 2, "query blocks");
-    static_assert(RB == 1 || RB == 2, "row blocks");
-    static_assert(RB == 1 || NB == 2, "two row blocks load q per unit (two query blocks)");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static_assert(kCopies % kProducerWarps == 0, "copies split evenly over the producer warps");
     static_assert(kHeadsPerCta * D * kSub == kHeadGroupElems, "stage budget");
@@ -165,8 +151,6 @@ struct Cfg {
 struct Shared {
     uint64_t* full;
     uint64_t* empty;
-    uint64_t* xfull;   // [kGroupWarps] set 1's hand-over written (two row blocks only)
-    uint64_t* xempty;  // [kGroupWarps] set 0 has read it
     volatile int* flags;  // [0] abort
 };
 
@@ -210,10 +194,10 @@ __device__ __forceinline__ void fetch_slot_ids(const DecodeArgs& a, SlotFetch& f
 // (c / P) % 32, so the P warps share each stage's copies. Each warp arrives on the
 // stage's full barrier with the bytes of its own copies and keeps its own ring of
 // slot ids.
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
-    using C = Cfg<D, G, WPH, NB, RB>;
+    using C = Cfg<D, G, WPH, NB>;
     constexpr int P = C::kProducerWarps;
     const int lane = threadIdx.x & 31;
     const int pw = (threadIdx.x >> 5) - C::kConsumerWarps;  // producer warp index
@@ -347,11 +331,11 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
 // holds the rows r0 + 8 nb .. r0 + 8 nb + 7 of the unit's query set, row r being
 // head r % G of request b + r / G; lane l holds row r0 + 8 nb + l / 4, dims
 // 2 (l % 4) .. of each k-step. Rows beyond the unit's requests are zero.
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 __device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit& un, int hh, int r0,
                                                  int g, int t4,
-                                                 uint32_t (&qf)[NB][Cfg<D, G, WPH, NB, RB>::kKSteps][2]) {
-    using C = Cfg<D, G, WPH, NB, RB>;
+                                                 uint32_t (&qf)[NB][Cfg<D, G, WPH, NB>::kKSteps][2]) {
+    using C = Cfg<D, G, WPH, NB>;
     const int kvh = un.hg * C::kHeadsPerCta + hh;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
@@ -370,11 +354,11 @@ __device__ __forceinline__ void load_q_fragments(const DecodeArgs& a, const Unit
 
 // Fused append: copy this warp's part (head hh, dims of `part`) of the staged new
 // K and V rows of request un.b from shared memory to pool slot slot_ids[un.b].
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 __device__ __forceinline__ void store_new_rows(const DecodeArgs& a, const Unit& un,
                                                const uint8_t* smem, int stage, int row, int hh,
                                                int part, int lane) {
-    using C = Cfg<D, G, WPH, NB, RB>;
+    using C = Cfg<D, G, WPH, NB>;
     constexpr int kBytes = C::kDimsPerWarp * 2;  // bytes of this warp's share of one row
     const int64_t slot = __ldg(a.slot_ids + un.b);
     const int64_t dst_off = slot * int64_t(a.n_kv_heads) * D * 2 +
@@ -389,15 +373,13 @@ __device__ __forceinline__ void store_new_rows(const DecodeArgs& a, const Unit& 
     }
 }
 
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
-    using C = Cfg<D, G, WPH, NB, RB>;
+    using C = Cfg<D, G, WPH, NB>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int wg = warp % kGroupWarps;
-    const int hh = wg / WPH;      // KV head within the group
-    const int part = wg % WPH;    // which slice of head_dim this warp accumulates
-    const int rb = warp / kGroupWarps;  // row block (set of four warps)
+    const int hh = warp / WPH;    // KV head within the group
+    const int part = warp % WPH;  // which slice of head_dim this warp accumulates
     const int g = lane >> 2, t4 = lane & 3;
     const int hq = a.n_qo_heads;
     const float scale_log2 = a.sm_scale * kLog2e;
@@ -411,11 +393,6 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                             (hh * D + part * C::kDimsPerWarp + ((lane >> 3) & 1) * 8) * 2;
     int stage = 0;
     uint32_t full_parity = 0;
-    // hand-over of stage-dealt units (two row blocks): set 1 waits for its buffer
-    // to be free (a fresh barrier reports the phase before it as complete), set 0
-    // for it to be written
-    uint32_t x_parity = rb == 1 ? 1u : 0u;
-    float* xbuf = reinterpret_cast<float*>(smem + C::kXOffset) + wg * 32 * C::kXFloats + lane;
 
     // With one query block the next unit's q fragments are loaded while the current
     // unit streams; with two (shared prefixes) they are loaded at the unit's start.
@@ -423,24 +400,21 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     uint32_t qb[NB][C::kKSteps][2], qn[NB][C::kKSteps][2];
     Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
     // Warm L2 with the first unit's q rows (a hint, safe before the wait): lane l
-    // touches query row rb * kWarpRows + l of this warp's KV head.
-    if (u_begin < u_end && lane < C::kWarpRows && (rb * C::kWarpRows + lane) / G < next.nreq) {
+    // touches query row l of this warp's KV head.
+    if (u_begin < u_end && lane < C::kWarpRows && lane / G < next.nreq) {
         const int kvh = next.hg * C::kHeadsPerCta + hh;
-        const int r = rb * C::kWarpRows + lane;
+        const int r = lane;
         prefetch_l2(static_cast<const __nv_bfloat16*>(a.q) +
                     (int64_t(next.b + r / G) * a.n_qo_heads + kvh * G + r % G) * D);
     }
     pdl_wait();  // q may come from the previous kernel
     if constexpr (kPrefetchQ) {
-        if (u_begin < u_end) load_q_fragments<D, G, WPH, NB, RB>(a, next, hh, 0, g, t4, qn);
+        if (u_begin < u_end) load_q_fragments<D, G, WPH, NB>(a, next, hh, 0, g, t4, qn);
     }
     for (int u = u_begin; u < u_end; ++u) {
         const Unit un = next;
         const int kvh = un.hg * C::kHeadsPerCta + hh;
-        // Two row blocks: a unit whose rows fit one block is dealt by stages (both
-        // sets take rows 0 ..), a larger one by rows.
-        const bool by_stage = RB == 2 && un.nreq * G <= C::kWarpRows;
-        const int r0 = by_stage ? 0 : rb * C::kWarpRows;  // first query row of this warp
+        constexpr int r0 = 0;  // first query row of this warp
         if constexpr (kPrefetchQ) {
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
@@ -450,11 +424,11 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                     qb[nb][ks][1] = qn[nb][ks][1];
                 }
         } else {
-            load_q_fragments<D, G, WPH, NB, RB>(a, un, hh, r0, g, t4, qb);
+            load_q_fragments<D, G, WPH, NB>(a, un, hh, r0, g, t4, qb);
         }
         if (u + 1 < u_end) {
             next = a.units[u + 1];
-            if constexpr (kPrefetchQ) load_q_fragments<D, G, WPH, NB, RB>(a, next, hh, r0, g, t4, qn);
+            if constexpr (kPrefetchQ) load_q_fragments<D, G, WPH, NB>(a, next, hh, r0, g, t4, qn);
         }
         // A warp whose rows are all beyond the unit's requests only passes the stages on.
         const bool active = r0 / G < un.nreq;
@@ -476,20 +450,17 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             const bool ok = mbar_wait(smem_u32(&sh.full[stage]), full_parity, a.status, sh.flags);
             if (!__all_sync(kFull, ok)) return;  // uniform exit: no lane is left in a shuffle
             const int n_stage = n_tok - t * C::kStageTokens;
-            // this warp's share of the stage: all of it, or none when dealt to the other set
-            const bool mine = !by_stage || (t & 1) == rb;
             // Fused append: the stage holding the request's newest token has its new
-            // K/V rows (copied from k_new / v_new); the warps of the first row block
-            // (or of the set the stage is dealt to) write their share of them to the
-            // pool slot before the stage is released.
-            if (a.k_new != nullptr && (by_stage ? mine : rb == 0)) {
+            // K/V rows (copied from k_new / v_new); each warp writes its share of them
+            // to the pool slot before the stage is released.
+            if (a.k_new != nullptr) {
                 const int row = un.len - 1 - (un.tok_begin + t * C::kStageTokens);
                 if (row >= 0 && row < n_stage && row < C::kStageTokens)
-                    store_new_rows<D, G, WPH, NB, RB>(a, un, smem, stage, row, hh, part, lane);
+                    store_new_rows<D, G, WPH, NB>(a, un, smem, stage, row, hh, part, lane);
             }
 #pragma unroll
             for (int j = 0; j < C::kSub; ++j) {
-                const int n = active && mine ? n_stage - j * kTile : 0;  // valid rows of this sub-tile
+                const int n = active ? n_stage - j * kTile : 0;  // valid rows of this sub-tile
                 if (n <= 0) break;
                 const uint32_t st = stage * C::kStage + j * kTile * C::kRowP;
                 float s[NB][4];
@@ -559,53 +530,6 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             }
         }
 
-        // ---- stage-dealt unit: set 1 hands (m, l, o) to set 0, which folds them in
-        if (by_stage && n_stages > 1) {
-            const bool ok = mbar_wait(smem_u32(rb == 1 ? &sh.xempty[wg] : &sh.xfull[wg]), x_parity,
-                                      a.status, sh.flags);
-            if (!__all_sync(kFull, ok)) return;
-            x_parity ^= 1;
-            if (rb == 1) {
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-#pragma unroll
-                    for (int jc = 0; jc < 2; ++jc) {
-                        xbuf[32 * (2 * nb + jc)] = m[nb][jc];
-                        xbuf[32 * (2 * NB + 2 * nb + jc)] = l[nb][jc];
-                    }
-#pragma unroll
-                    for (int mb = 0; mb < C::kMBlocks; ++mb)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            xbuf[32 * (4 * NB + 4 * (nb * C::kMBlocks + mb) + i)] = o[nb][mb][i];
-                }
-                mbar_arrive(smem_u32(&sh.xfull[wg]));  // each lane releases its own stores
-                continue;
-            }
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-                float a0[2], a1[2];
-#pragma unroll
-                for (int jc = 0; jc < 2; ++jc) {
-                    const float m1 = xbuf[32 * (2 * nb + jc)];
-                    const float l1 = xbuf[32 * (2 * NB + 2 * nb + jc)];
-                    const float mn = fmaxf(m[nb][jc], m1);
-                    a0[jc] = m[nb][jc] == neg_inf() ? 0.f : ex2(m[nb][jc] - mn);
-                    a1[jc] = m1 == neg_inf() ? 0.f : ex2(m1 - mn);
-                    l[nb][jc] = l[nb][jc] * a0[jc] + l1 * a1[jc];
-                    m[nb][jc] = mn;
-                }
-#pragma unroll
-                for (int mb = 0; mb < C::kMBlocks; ++mb)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        o[nb][mb][i] = o[nb][mb][i] * a0[i & 1] +
-                                       xbuf[32 * (4 * NB + 4 * (nb * C::kMBlocks + mb) + i)] * a1[i & 1];
-            }
-            mbar_arrive(smem_u32(&sh.xempty[wg]));  // the buffer may be refilled
-        }
-        if (by_stage && rb == 1) continue;  // set 0 writes the unit's results
-
         // ---- epilogue: o[nb][mb][0..3] = (dim 16*mb' + g (+8), rows r0 + 8nb + 2t4, +1)
         if (!active) continue;
         const int dim0 = part * C::kDimsPerWarp + g;
@@ -646,25 +570,19 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     }
 }
 
-template <int D, int G, int WPH, int NB, int RB>
-__global__ void __launch_bounds__(Cfg<D, G, WPH, NB, RB>::kThreads, Cfg<D, G, WPH, NB, RB>::kMinBlocks)
+template <int D, int G, int WPH, int NB>
+__global__ void __launch_bounds__(Cfg<D, G, WPH, NB>::kThreads, Cfg<D, G, WPH, NB>::kMinBlocks)
     paged_decode_kernel(const DecodeArgs a) {
-    using C = Cfg<D, G, WPH, NB, RB>;
+    using C = Cfg<D, G, WPH, NB>;
     extern __shared__ __align__(128) uint8_t smem[];
     Shared sh;
     sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
     sh.empty = sh.full + C::kStages;
-    sh.xfull = sh.empty + C::kStages;
-    sh.xempty = sh.xfull + C::kXBars / 2;
-    sh.flags = reinterpret_cast<volatile int*>(sh.full + 2 * C::kStages + C::kXBars);
+    sh.flags = reinterpret_cast<volatile int*>(sh.full + 2 * C::kStages);
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), C::kProducerWarps);
             mbar_init(smem_u32(&sh.empty[s]), C::kConsumerWarps);
-        }
-        for (int w = 0; w < C::kXBars / 2; ++w) {  // every lane of a warp arrives
-            mbar_init(smem_u32(&sh.xfull[w]), 32);
-            mbar_init(smem_u32(&sh.xempty[w]), 32);
         }
         sh.flags[0] = 0;
         fence_mbar_init();
@@ -676,9 +594,9 @@ __global__ void __launch_bounds__(Cfg<D, G, WPH, NB, RB>::kThreads, Cfg<D, G, WP
     const int u_begin = a.cta_begin[blockIdx.x];
     const int u_end = a.cta_begin[blockIdx.x + 1];
     if ((threadIdx.x >> 5) >= C::kConsumerWarps)
-        producer_warp<D, G, WPH, NB, RB>(a, smem, sh, u_begin, u_end);
+        producer_warp<D, G, WPH, NB>(a, smem, sh, u_begin, u_end);
     else
-        consumer_warp<D, G, WPH, NB, RB>(a, smem, sh, u_begin, u_end);
+        consumer_warp<D, G, WPH, NB>(a, smem, sh, u_begin, u_end);
 }
 
 // ---------------------------------------------------------------------------
@@ -821,30 +739,30 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, lse_merge_kernel<D>, a);
 }
 
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 cudaError_t prepare() {
     // Raise the dynamic shared memory limit once per instance.
     static cudaError_t status = cudaFuncSetAttribute(
-        paged_decode_kernel<D, G, WPH, NB, RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        Cfg<D, G, WPH, NB, RB>::kSmem);
+        paged_decode_kernel<D, G, WPH, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        Cfg<D, G, WPH, NB>::kSmem);
     return status;
 }
 
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 int occupancy() {
-    using C = Cfg<D, G, WPH, NB, RB>;
-    if (prepare<D, G, WPH, NB, RB>() != cudaSuccess) return 0;
+    using C = Cfg<D, G, WPH, NB>;
+    if (prepare<D, G, WPH, NB>() != cudaSuccess) return 0;
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_kernel<D, G, WPH, NB, RB>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_kernel<D, G, WPH, NB>,
                                                       C::kThreads, C::kSmem) != cudaSuccess)
         return 0;
     return blocks;
 }
 
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
-    using C = Cfg<D, G, WPH, NB, RB>;
-    cudaError_t e = prepare<D, G, WPH, NB, RB>();
+    using C = Cfg<D, G, WPH, NB>;
+    cudaError_t e = prepare<D, G, WPH, NB>();
     if (e != cudaSuccess) return e;
     if (a.n_ctas == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
@@ -857,56 +775,54 @@ cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, WPH, NB, RB>, a);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, WPH, NB>, a);
 }
 
-// Calls FN<D, G, WPH, NB, RB>::run(args...) for the runtime shape. `shared`
-// selects the shared-prefix instance (two query blocks per warp; two row blocks of
-// warps as well under PKV_SHARED_ROW_BLOCKS=2), which exists only at head_dim 128
-// with one warp per KV head.
-template <template <int, int, int, int, int> class FN, typename... Args>
+// Calls FN<D, G, WPH, NB>::run(args...) for the runtime shape. `shared` selects
+// the shared-prefix instance (two query blocks per warp), which exists only at
+// head_dim 128 with one warp per KV head.
+template <template <int, int, int, int> class FN, typename... Args>
 auto dispatch(int head_dim, int group, int wph, bool shared, Args&&... args)
-    -> decltype(FN<128, 1, 1, 1, 1>::run(args...)) {
-#define PKV_G(D_, W_, NB_, RB_)                                     \
-    switch (group) {                                                \
-        case 1: return FN<D_, 1, W_, NB_, RB_>::run(args...);       \
-        case 2: return FN<D_, 2, W_, NB_, RB_>::run(args...);       \
-        case 4: return FN<D_, 4, W_, NB_, RB_>::run(args...);       \
-        case 8: return FN<D_, 8, W_, NB_, RB_>::run(args...);       \
-        default: break;                                             \
+    -> decltype(FN<128, 1, 1, 1>::run(args...)) {
+#define PKV_G(D_, W_, NB_)                                     \
+    switch (group) {                                           \
+        case 1: return FN<D_, 1, W_, NB_>::run(args...);       \
+        case 2: return FN<D_, 2, W_, NB_>::run(args...);       \
+        case 4: return FN<D_, 4, W_, NB_>::run(args...);       \
+        case 8: return FN<D_, 8, W_, NB_>::run(args...);       \
+        default: break;                                        \
     }
     if (!shared) {
         if (head_dim == 128) {
-            if (wph == 1) { PKV_G(128, 1, 1, 1) }
-            if (wph == 2) { PKV_G(128, 2, 1, 1) }
-            if (wph == 4) { PKV_G(128, 4, 1, 1) }
+            if (wph == 1) { PKV_G(128, 1, 1) }
+            if (wph == 2) { PKV_G(128, 2, 1) }
+            if (wph == 4) { PKV_G(128, 4, 1) }
         } else if (head_dim == 256) {
-            if (wph == 2) { PKV_G(256, 2, 1, 1) }
-            if (wph == 4) { PKV_G(256, 4, 1, 1) }
+            if (wph == 2) { PKV_G(256, 2, 1) }
+            if (wph == 4) { PKV_G(256, 4, 1) }
         }
     } else if (head_dim == 128 && wph == 1) {
-        if (shared_row_blocks() == 2) { PKV_G(128, 1, 2, 2) }
-        PKV_G(128, 1, 2, 1)
+        PKV_G(128, 1, 2)
     }
 #undef PKV_G
-    return FN<128, 1, 1, 1, 1>::unsupported();
+    return FN<128, 1, 1, 1>::unsupported();
 }
 
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 struct OccupancyFn {
-    static int run() { return occupancy<D, G, WPH, NB, RB>(); }
+    static int run() { return occupancy<D, G, WPH, NB>(); }
     static int unsupported() { return 0; }
 };
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 struct LaunchFn {
     static cudaError_t run(const DecodeArgs& a, cudaStream_t s) {
-        return launch<D, G, WPH, NB, RB>(a, s);
+        return launch<D, G, WPH, NB>(a, s);
     }
     static cudaError_t unsupported() { return cudaErrorInvalidValue; }
 };
-template <int D, int G, int WPH, int NB, int RB>
+template <int D, int G, int WPH, int NB>
 struct RowsFn {
-    static int run() { return Cfg<D, G, WPH, NB, RB>::kWarpRows * RB; }
+    static int run() { return Cfg<D, G, WPH, NB>::kWarpRows; }
     static int unsupported() { return 0; }
 };
 

@@ -12,14 +12,11 @@ namespace pkv {
 
 // ---- launches -----------------------------------------------------------
 // Kernels are launched with programmatic stream serialisation (PDL) unless the
-// environment variable PKV_PDL is "0": a kernel may then be scheduled while its
+// environment variable PKV_PDL is "0" (a diagnostic switch: results do not depend
+// on it, only how soon a kernel starts): a kernel may then be scheduled while its
 // predecessor on the stream is still running, and does only plan reads and
 // barrier set-up before its griddepcontrol.wait.
 bool pdl_enabled();
-// Row blocks of the shared-prefix kernel: 1 (16 query rows per KV head, two CTAs
-// per SM; default, the faster on GB300) or 2 (32 rows, one CTA per SM); tuning
-// knob PKV_SHARED_ROW_BLOCKS, read once.
-int shared_row_blocks();
 
 // ---- errors -------------------------------------------------------------
 int fail(int code, const char* fmt, ...);  // records the message, returns code
@@ -33,16 +30,13 @@ bool take_injected_stall();
 // A CTA of the decode kernel serves one KV-head group of 1, 2 or 4 consecutive
 // KV heads, at most kHeadGroupElems / head_dim of them, so that one token's K (or
 // V) row of a group is at most kHeadGroupElems bf16 = 1 KB, one bulk copy.
-// heads_per_group() is the largest group the shape allows; a plan may use fewer
-// heads per group (smaller partial results when contexts are split).
+// heads_per_group() is the largest group the shape allows, the group every plan
+// uses (the host-only planner entry also accepts smaller ones).
 constexpr int kHeadGroupElems = 512;
 inline int heads_per_group(int n_kv_heads, int head_dim) {
     const int cap = kHeadGroupElems / head_dim;
     return n_kv_heads < cap ? n_kv_heads : cap;
 }
-// The group size a new plan uses: heads_per_group(), unless the environment
-// variable PKV_HEADS_PER_CTA (1, 2 or 4) asks for a smaller valid one.
-int choose_heads_per_cta(int n_kv_heads, int head_dim);
 
 // ---- plan ----------------------------------------------------------------
 // One work unit of the decode kernel: tokens [tok_begin, tok_end) of the slot list
@@ -171,14 +165,21 @@ struct pkv_plan {
     int n_qo_heads = 0, n_kv_heads = 0, head_dim = 0, n_groups = 0, heads_per_cta = 0;
     pkv::PlanLimits lim{};
     size_t meta_bytes = 0;
-    void* host_staging = nullptr;  // pinned: header, cta_begin, merges, part list, units
+    // Two pinned staging buffers (header, cta_begin, merges, part list, units), used
+    // in turn: a step's plan call waits only for the upload of the step before the
+    // previous one, so the host may run two steps ahead of the GPU.
+    void* host_staging[2] = {nullptr, nullptr};
+    cudaEvent_t copy_done[2] = {nullptr, nullptr};
+    bool copy_pending[2] = {false, false};
+    int next_staging = 0;          // the buffer the next plan call fills
     void* dev_meta = nullptr;      // device copy of the same (used prefix uploaded per step)
     float* ws_o = nullptr;
     float* ws_lse = nullptr;
     int* dev_state = nullptr;      // status word, padding
     void* zero_row = nullptr;
-    cudaEvent_t copy_done = nullptr;
-    bool copy_pending = false;
+    // host time of the plan calls since the last reset (paged_decode_plan_host_times)
+    double compute_ns = 0, wait_ns = 0;
+    int64_t timed_calls = 0;
     // the current step
     bool planned = false;
     int batch = 0;
@@ -190,4 +191,7 @@ struct pkv_plan {
     bool shared = false; // the current step runs the shared-prefix kernel
     int launch_ctas = 0; // grid of the current step's decode kernel
     std::vector<int32_t> indptr_host;
+    // the current step's sharing description (checked against kv_indices when
+    // debug checks are on and the shared-prefix kernel runs)
+    std::vector<int32_t> shared_indptr_host, shared_len_host;
 };

@@ -111,6 +111,11 @@ SMALL_CASES = [
     ([131072], 32, 8, 128),
     ([60000, 1, 16, 17, 15], 16, 2, 256),
     ([3000, 70], 4, 4, 128),
+    # groups of fewer than four KV heads at head_dim 128 (two and four consumer warps
+    # per head) and of one at head_dim 256
+    ([300, 4000, 1], 4, 2, 128),
+    ([2500, 9, 700], 8, 1, 128),
+    ([5000, 33], 4, 1, 256),
 ]
 
 
@@ -568,6 +573,52 @@ def test_shared_prefix_plan(pkv, case, fused):
     assert plan.status() == 0
     if d == 128 and hkv == 8:
         assert plan.info()["n_merges"] >= wl.batch  # every member merged its parts
+
+
+def test_false_sharing_description_is_rejected_with_debug_checks(pkv):
+    """paged_decode_plan_shared's precondition (members list the same prefix slot
+    ids) is verified by the attention call when debug checks are on: a description
+    that kv_indices does not bear out gives PKV_ERR_INDEX and launches nothing."""
+    wl = workloads.scattered_workload([400, 500, 300, 600], seed=77)  # nothing shared
+    dev = torch.device("cuda")
+    t = workloads.layer_tensors(wl, 0, device=dev)
+    out = torch.full((wl.batch, 32, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((wl.batch, 32), float("nan"), dtype=torch.float32, device=dev)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx = torch.from_numpy(wl.kv_indices).to(dev)
+    slots = torch.from_numpy(wl.append_slots).to(dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, 32, 8, 128)
+    # claims requests 0-3 share their first 200 slots
+    pkv.paged_decode_plan_shared(plan, wl.kv_indptr, np.array([0, 4], np.int32),
+                                 np.array([200], np.int32))
+    pkv.pkv_set_debug_checks(True)
+    try:
+        for fused in (False, True):
+            with pytest.raises(pkv.PkvError) as e:
+                if fused:
+                    pkv.paged_decode_append_attn(t.q, t.k_pool, t.v_pool, ip, idx, slots, t.k_new,
+                                                 t.v_new, wl.batch, 32, 8, 128, wl.sm_scale, out,
+                                                 lse, plan)
+                else:
+                    pkv.paged_decode_attn(t.q, t.k_pool, t.v_pool, ip, idx, wl.batch, 32, 8, 128,
+                                          wl.sm_scale, out, lse, plan)
+            assert e.value.code == pkv.PKV_ERR_INDEX
+            assert "shared" in e.value.message
+        torch.cuda.synchronize()
+        assert torch.isnan(out.float()).all() and torch.isnan(lse).all()  # nothing launched
+        # a true description passes the check: requests 0-1 made to share 100 slots
+        shared = wl.kv_indices.copy()
+        shared[wl.kv_indptr[1]:wl.kv_indptr[1] + 100] = shared[:100]
+        idx2 = torch.from_numpy(shared).to(dev)
+        pkv.paged_decode_plan_shared(plan, wl.kv_indptr, np.array([0, 2], np.int32),
+                                     np.array([100], np.int32))
+        pkv.paged_decode_attn(t.q, t.k_pool, t.v_pool, ip, idx2, wl.batch, 32, 8, 128,
+                              wl.sm_scale, out, lse, plan)
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    assert plan.status() == 0
+    assert torch.isfinite(out.float()).all()
 
 
 def test_host_tier_round_trip_then_attention(pkv):
