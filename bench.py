@@ -388,54 +388,87 @@ def replica_gbs(world: int, bytes_per_step: int, steps: int, elapsed_ms: float) 
     return world * bytes_per_step * steps / (elapsed_ms * 1e-3) / 1e9
 
 
-def run_tier_bench(args):
-    """Bandwidth of the host KV tier: offload and prefetch of scattered rows of the
-    workload's pool between HBM and pinned host memory (NVLink-C2C on GB300)."""
+def measure_tier(config_no: int, steps: int, warmup: int, host_frac: float = 0.1) -> dict:
+    """The host KV tier on a workload's pool (NVLink-C2C on GB300): scattered row moves
+    HBM <-> pinned host memory (kvpool_offload / kvpool_prefetch) against one contiguous
+    copy of the same bytes by the copy engines, and one layer's attention with a
+    fraction of its listed rows read in place from host memory
+    (paged_decode_attn_tiered) against the same call with every row in HBM."""
     import paged_kv_gqa_tokentokvpool_gb300 as pkv
-    wl = workloads.config_workload(args.config)
+    wl = workloads.config_workload(config_no)
     dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
     rows = min(wl.total_tokens, 1 << 18)
     t = workloads.layer_tensors(wl, 0, device=dev)
-    kh = torch.empty(rows, wl.n_kv_heads, wl.head_dim, dtype=torch.bfloat16).pin_memory()
+    Hkv, D = wl.n_kv_heads, wl.head_dim
+    kh = torch.empty(rows, Hkv, D, dtype=torch.bfloat16).pin_memory()
     vh = torch.empty_like(kh).pin_memory()
     rng = np.random.default_rng(7)
     dev_slots = torch.from_numpy(wl.kv_indices[:rows].copy()).to(dev)
     host_slots = torch.from_numpy(rng.permutation(rows).astype(np.int32)).to(dev)
-    row_bytes = 2 * wl.n_kv_heads * wl.head_dim * 2
-    res = {}
-    for name, fn in (("offload", pkv.kvpool_offload), ("prefetch", pkv.kvpool_prefetch)):
-        for _ in range(args.warmup):
-            fn(t.k_pool, t.v_pool, dev_slots, kh, vh, host_slots)
+    row_bytes = 2 * Hkv * D * 2
+
+    def event_ms(fn):
+        for _ in range(warmup):
+            fn()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            fn(t.k_pool, t.v_pool, dev_slots, kh, vh, host_slots)
-        e1.record()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / args.steps
+        return e0.elapsed_time(e1) / steps
+
+    res = {"rows": rows, "row_bytes": row_bytes, "workload": f"{wl.name}: {wl.description}"}
+    for name, fn in (("offload", pkv.kvpool_offload), ("prefetch", pkv.kvpool_prefetch)):
+        ms = event_ms(lambda: fn(t.k_pool, t.v_pool, dev_slots, kh, vh, host_slots))
         res[name] = {"us_per_call": ms * 1e3, "gbs_over_link": rows * row_bytes / (ms * 1e-3) / 1e9}
     # the link's rate for the same bytes as one contiguous copy each way (copy engines)
     host_flat = torch.empty(rows * row_bytes, dtype=torch.uint8).pin_memory()
     dev_flat = torch.empty(rows * row_bytes, dtype=torch.uint8, device=dev)
     for name, (dst, src) in (("contiguous_h2d", (dev_flat, host_flat)),
                              ("contiguous_d2h", (host_flat, dev_flat))):
-        for _ in range(args.warmup):
-            dst.copy_(src, non_blocking=True)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            dst.copy_(src, non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / args.steps
+        ms = event_ms(lambda: dst.copy_(src, non_blocking=True))
         res[name] = {"gbs": rows * row_bytes / (ms * 1e-3) / 1e9}
-    print(json.dumps({"metric": "host KV tier: scattered row moves HBM <-> pinned host memory",
-                      "unit": "GB/s", "rows": rows, "row_bytes": row_bytes,
-                      "workload": f"{wl.name}: {wl.description}", **res}), flush=True)
+    del host_flat, dev_flat, kh, vh
+    # attention over the layer with host_frac of its listed rows in host memory
+    n = wl.total_tokens
+    moved = np.sort(rng.choice(n, size=max(1, int(host_frac * n)), replace=False))
+    moved_slots = torch.from_numpy(wl.kv_indices[moved].astype(np.int64)).to(dev)
+    kh2 = t.k_pool.index_select(0, moved_slots).cpu().pin_memory()
+    vh2 = t.v_pool.index_select(0, moved_slots).cpu().pin_memory()
+    tiered_idx = wl.kv_indices.copy()
+    tiered_idx[moved] = -1 - np.arange(len(moved), dtype=np.int32)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx_dev = torch.from_numpy(wl.kv_indices).to(dev)
+    idx_tier = torch.from_numpy(tiered_idx).to(dev)
+    out = torch.empty(wl.batch, wl.n_qo_heads, D, dtype=torch.bfloat16, device=dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, n, wl.n_qo_heads, Hkv, D)
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    args = (wl.batch, wl.n_qo_heads, Hkv, D, wl.sm_scale, out, None, plan)
+    ms_dev = event_ms(lambda: pkv.paged_decode_attn(t.q, t.k_pool, t.v_pool, ip, idx_dev, *args))
+    ms_tier = event_ms(lambda: pkv.paged_decode_attn_tiered(t.q, t.k_pool, t.v_pool, kh2, vh2, ip,
+                                                            idx_tier, *args))
+    if plan.status() != 0:
+        raise RuntimeError("a decode pipeline wait exceeded its bound: the tier figures are invalid")
+    host_bytes = len(moved) * row_bytes
+    res["attention_in_place"] = {
+        "host_fraction": len(moved) / n, "host_bytes": host_bytes,
+        "us_all_rows_in_hbm": ms_dev * 1e3, "us_with_host_rows": ms_tier * 1e3,
+        "host_gbs": host_bytes / (ms_tier * 1e-3) / 1e9,
+        "note": "one layer's attention (all requests); host rows read over the link in place"}
+    del plan, t
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_tier_bench(args):
+    res = measure_tier(args.config, args.steps, args.warmup)
+    print(json.dumps({"metric": "host KV tier: scattered row moves HBM <-> pinned host memory, "
+                                "and attention reading host rows in place",
+                      "unit": "GB/s", **res}), flush=True)
     return 0
 
 
@@ -906,6 +939,7 @@ def main(argv=None):
                 entries[f"cfg{no}"] = sweep_entry(measure_decode(no, args, world, pg, local))
         for no in (1, 2, 3):
             entries[f"pf{no}"] = sweep_entry(measure_prefill(no, args.steps, args.warmup))
+        entries["tier"] = measure_tier(5, args.steps, args.warmup)
         entries[f"cfg{args.config}"] = sweep_entry(line)
         line["config"]["sweep"] = entries
     if rank == 0:

@@ -192,6 +192,33 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
                       void* out, float* lse, const pkv_plan* plan, pkv_stream_t stream);
 
 /*
+ * paged_decode_attn_tiered — paged_decode_attn over a slot list whose older rows may
+ * sit in the host KV tier. When HBM is full, old KV rows move to CPU memory
+ * ("Agent-Infer", section "CPU 卸载"); kvpool_prefetch brings them back before a
+ * step, while this call reads them where they are: a slot id s >= 0 names row s of
+ * k_pool / v_pool, and s < 0 names row -1 - s of k_host / v_host, which the kernel
+ * reads over NVLink-C2C (16-byte copies into the same shared-memory stages as the
+ * device rows). Results are those of paged_decode_attn over the same rows.
+ *   pool_slots   : rows of k_pool / v_pool
+ *   k_host, v_host : [host_slots, n_kv_heads, head_dim] bf16 in PINNED host memory
+ *                  mapped for the GPU (cudaHostAlloc, a pinned torch tensor); pageable
+ *                  memory is rejected with PKV_ERR_INVALID_ARG before any launch
+ *   host_slots   : rows of each host pool (> 0)
+ *   kv_indices   : entries in [-host_slots, pool_slots) (checked, with debug checks
+ *                  on, as PKV_ERR_INDEX)
+ * Other arguments as for paged_decode_attn. Host rows move at the link's rate (about
+ * 200 GB/s on GB300), some thirty times slower than HBM, so a step spends time in
+ * proportion to its host rows; the plan, built from kv_indptr alone, balances the
+ * CTAs as if every row were in HBM.
+ */
+int paged_decode_attn_tiered(const void* q, const void* k_pool, const void* v_pool,
+                             int64_t pool_slots, const void* k_host, const void* v_host,
+                             int64_t host_slots, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, int batch, int n_qo_heads,
+                             int n_kv_heads, int head_dim, float sm_scale, void* out,
+                             float* lse, const pkv_plan* plan, pkv_stream_t stream);
+
+/*
  * paged_decode_append_attn — kvpool_append followed by paged_decode_attn, in one
  * launch (plus the merge kernel): each request's newest K/V row is read straight
  * from k_new / v_new by the attention kernel, which also writes it to its pool
@@ -411,6 +438,7 @@ int paged_decode_plan_host_times(pkv_plan* plan, double* compute_us, double* wai
 
 /* Flags for paged_decode_plan_set_flags. */
 #define PKV_PLAN_EARLY_GATHER 1u
+#define PKV_PLAN_PERSISTENT 2u
 
 /*
  * paged_decode_plan_set_flags — options for the attention calls that use `plan`
@@ -434,6 +462,13 @@ int paged_decode_plan_host_times(pkv_plan* plan, double* compute_us, double* wai
  * Takes effect for attention calls enqueued after it returns.
  */
 int paged_decode_plan_set_flags(pkv_plan* plan, unsigned flags);
+
+/*
+ * paged_decode_plan_mode — *single_launch = 1 when the plan's steps run in the
+ * single-launch small-step mode (see paged_decode_plan_create), 0 when they run on
+ * the persistent grid with an uploaded work list. No CUDA call.
+ */
+int paged_decode_plan_mode(const pkv_plan* plan, int* single_launch);
 
 /*
  * paged_decode_plan_status — read and clear the plan's device status word

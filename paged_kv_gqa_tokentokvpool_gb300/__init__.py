@@ -34,6 +34,7 @@ PKV_ERR_PLAN = -3
 PKV_ERR_CUDA = -4
 PKV_ERR_INDEX = -5
 PKV_PLAN_EARLY_GATHER = 1
+PKV_PLAN_PERSISTENT = 2
 
 EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",
@@ -43,6 +44,7 @@ EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_destroy",
             "paged_prefill_plan_host", "paged_prefill_plan_status",
             "paged_decode_plan_host_times", "paged_decode_attn_static_status",
+            "paged_decode_attn_tiered", "paged_decode_plan_mode",
             "pkv_set_debug_checks", "pkv_inject_stall",
             "pkv_last_error")
 
@@ -79,6 +81,9 @@ def _load() -> ctypes.CDLL:
     lib.paged_decode_plan_set_flags.argtypes = [P, ctypes.c_uint]
     lib.paged_decode_plan_host_times.argtypes = [P, P, P, P, I32]
     lib.paged_decode_attn_static_status.argtypes = [P, P]
+    lib.paged_decode_plan_mode.argtypes = [P, P]
+    lib.paged_decode_attn_tiered.argtypes = [P, P, P, I64, P, P, I64, P, P, I32, I32, I32, I32,
+                                             ctypes.c_float, P, P, P, P]
     lib.paged_prefill_plan_create.argtypes = [ctypes.POINTER(P), I32, I64, I32, I32, I32]
     lib.paged_prefill_plan.argtypes = [P, P, P, I32, P]
     lib.paged_prefill_attn.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, ctypes.c_float,
@@ -104,7 +109,8 @@ def _load() -> ctypes.CDLL:
                  "kvpool_prefetch", "paged_decode_plan_set_flags", "paged_prefill_plan_create",
                  "paged_prefill_plan", "paged_prefill_attn", "paged_prefill_plan_host",
                  "paged_prefill_plan_status", "paged_decode_plan_host_times",
-                 "paged_decode_attn_static_status"):
+                 "paged_decode_attn_static_status", "paged_decode_attn_tiered",
+                 "paged_decode_plan_mode"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -185,6 +191,13 @@ class Plan:
         v = ctypes.c_int()
         _check(library().paged_decode_plan_status(self.handle, ctypes.byref(v)))
         return v.value
+
+    def single_launch(self) -> bool:
+        """True when the plan's steps run as single launches of the cluster kernel
+        (paged_decode_plan_mode)."""
+        v = ctypes.c_int()
+        _check(library().paged_decode_plan_mode(self.handle, ctypes.byref(v)))
+        return bool(v.value)
 
     def set_flags(self, flags: int) -> None:
         """paged_decode_plan_set_flags (e.g. PKV_PLAN_EARLY_GATHER)."""
@@ -315,6 +328,25 @@ def paged_decode_attn(q, k_pool, v_pool, kv_indptr, kv_indices, batch, n_qo_head
                                   _ptr(kv_indices), batch, n_qo_heads, n_kv_heads, head_dim,
                                   float(sm_scale), _ptr(out), _ptr(lse), plan.handle,
                                   _stream(stream)))
+
+
+def paged_decode_attn_tiered(q, k_pool, v_pool, k_host, v_host, kv_indptr, kv_indices, batch,
+                             n_qo_heads, n_kv_heads, head_dim, sm_scale, out, lse, plan: Plan,
+                             stream=None) -> None:
+    """paged_decode_attn where a slot id s < 0 names row -1 - s of the pinned host pools
+    k_host / v_host, read in place over the host link (see include/pkv.h)."""
+    for t, name in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"), (out, "out")):
+        _dev(t, torch.bfloat16, name)
+    for t, name in ((kv_indptr, "kv_indptr"), (kv_indices, "kv_indices")):
+        _dev(t, torch.int32, name)
+    _host_pool(k_host, "k_host")
+    _host_pool(v_host, "v_host")
+    if lse is not None:
+        _dev(lse, torch.float32, "lse")
+    _check(library().paged_decode_attn_tiered(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(k_host), _ptr(v_host),
+        k_host.shape[0], _ptr(kv_indptr), _ptr(kv_indices), batch, n_qo_heads, n_kv_heads,
+        head_dim, float(sm_scale), _ptr(out), _ptr(lse), plan.handle, _stream(stream)))
 
 
 def paged_decode_append_attn(q, k_pool, v_pool, kv_indptr, kv_indices, slot_ids, k_new, v_new,

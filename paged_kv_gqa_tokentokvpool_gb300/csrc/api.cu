@@ -353,6 +353,15 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     }
     p->ctas = p->num_sms * p->ctas_per_sm;
     p->ctas_shared = p->share_rows > 0 ? p->num_sms * shared_per_sm : 0;
+    // A plan whose every step is small runs its steps as single launches of the
+    // cluster kernel: all (request, head group) clusters resident at once, and a CTA's
+    // share of the longest context the plan allows at most kSmallMaxStages stages.
+    {
+        const int64_t items = int64_t(max_batch) * (n_kv_heads / hpg);
+        const int64_t max_share = int64_t(kSmallCluster) * kSmallMaxStages * decode_stage_tokens(hpg, head_dim);
+        p->small = max_tokens <= max_share &&
+                   items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim);
+    }
     p->ctas_max = std::max(p->ctas, p->ctas_shared);
     p->max_batch = max_batch;
     p->max_tokens = max_tokens;
@@ -422,11 +431,33 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
     int rc = check_sharing(who, kv_indptr_host, batch, shared_indptr_host, n_shared,
                            shared_len_host);
     if (rc != PKV_OK) return rc;
+    const bool small = p->small && !(p->flags & PKV_PLAN_PERSISTENT);
     bool share = false;
-    if (p->share_rows > 0)
+    if (p->share_rows > 0 && !small)
         for (int s = 0; s < n_shared; ++s)
             share |= shared_len_host[s] > 0 && shared_indptr_host[s + 1] > shared_indptr_host[s];
     const PlanSharing sh{shared_indptr_host, shared_len_host, n_shared, p->share_rows};
+    p->step_small = small;
+    if (small) {
+        // nothing to upload: the cluster kernel reads kv_indptr itself
+        const int items = batch * p->n_groups;
+        const int st = decode_stage_tokens(p->n_kv_heads / p->n_groups, p->head_dim);
+        int longest = 0;
+        for (int b = 0; b < batch; ++b)
+            longest = std::max(longest, kv_indptr_host[b + 1] - kv_indptr_host[b]);
+        p->counts = PlanCounts{items * kSmallCluster, items * kSmallCluster, items,
+                               items * kSmallCluster,
+                               ((longest + kSmallCluster - 1) / kSmallCluster + st - 1) / st * st};
+        p->batch = batch;
+        p->shared = false;
+        p->launch_ctas = items * kSmallCluster;
+        p->shared_indptr_host.clear();
+        p->shared_len_host.clear();
+        p->indptr_host.assign(kv_indptr_host, kv_indptr_host + batch + 1);
+        ++p->timed_calls;
+        p->planned = true;
+        return PKV_OK;
+    }
     // The staging buffer this call fills may still feed the upload of the step
     // before the previous one (the buffers are used in turn).
     const int sb = p->next_staging;
@@ -522,10 +553,18 @@ int paged_decode_plan_host_times(pkv_plan* p, double* compute_us, double* wait_u
 int paged_decode_plan_set_flags(pkv_plan* p, unsigned flags) {
     clear_error();
     if (!p) return fail(PKV_ERR_PLAN, "paged_decode_plan_set_flags: plan is NULL");
-    if (flags & ~PKV_PLAN_EARLY_GATHER)
+    constexpr unsigned kKnown = PKV_PLAN_EARLY_GATHER | PKV_PLAN_PERSISTENT;
+    if (flags & ~kKnown)
         return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_set_flags: unknown flags 0x%x",
-                    flags & ~PKV_PLAN_EARLY_GATHER);
+                    flags & ~kKnown);
     p->flags = flags;
+    return PKV_OK;
+}
+
+int paged_decode_plan_mode(const pkv_plan* p, int* single_launch) {
+    clear_error();
+    if (!p || !single_launch) return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_mode: NULL argument");
+    *single_launch = p->small && !(p->flags & PKV_PLAN_PERSISTENT) ? 1 : 0;
     return PKV_OK;
 }
 
@@ -549,7 +588,8 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
               const int32_t* kv_indptr, const int32_t* kv_indices, int batch, int n_qo_heads,
               int n_kv_heads, int head_dim, float sm_scale, void* out, float* lse,
               const pkv_plan* p, pkv_stream_t stream, const int32_t* slot_ids, const void* k_new,
-              const void* v_new, int64_t pool_slots) {
+              const void* v_new, int64_t pool_slots, const void* k_host = nullptr,
+              const void* v_host = nullptr, int64_t host_slots = 0) {
     if (!p) return fail(PKV_ERR_PLAN, "%s: plan is NULL", who);
     if (!p->planned) return fail(PKV_ERR_PLAN, "%s: paged_decode_plan was not run", who);
     if (n_qo_heads != p->n_qo_heads || n_kv_heads != p->n_kv_heads || head_dim != p->head_dim)
@@ -567,6 +607,19 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
         return fail(PKV_ERR_INVALID_ARG, "%s: lse must be 4-byte aligned", who);
     const bool fused = slot_ids != nullptr;
+    const bool tiered = k_host != nullptr;
+    void *kh = nullptr, *vh = nullptr;
+    if (tiered) {
+        if (!v_host || host_slots <= 0)
+            return fail(PKV_ERR_INVALID_ARG, "%s: host pools need v_host and host_slots > 0", who);
+        if (!aligned16(k_host) || !aligned16(v_host))
+            return fail(PKV_ERR_INVALID_ARG, "%s: host pools must be 16-byte aligned", who);
+        int rc = gpu_address(who, "k_host", k_host, true, &kh);
+        if (rc == PKV_OK) rc = gpu_address(who, "v_host", v_host, true, &vh);
+        if (rc != PKV_OK) return rc;
+        if (!aligned16(kh) || !aligned16(vh))
+            return fail(PKV_ERR_INVALID_ARG, "%s: host pools must be 16-byte aligned", who);
+    }
     if (fused) {
         if (!k_new || !v_new) return fail(PKV_ERR_INVALID_ARG, "%s: NULL new rows", who);
         if (!aligned16(k_new) || !aligned16(v_new))
@@ -594,9 +647,9 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
             if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
             if (e != cudaSuccess) return cuda_fail(e, "debug copy of kv_indices");
             for (int32_t i = 0; i < n; ++i)
-                if (idx[i] < 0 || (pool_slots > 0 && idx[i] >= pool_slots))
-                    return fail(PKV_ERR_INDEX, "%s: kv_indices[%d] = %d is not a pool slot", who, i,
-                                idx[i]);
+                if (idx[i] < (tiered ? -host_slots : 0) || (pool_slots > 0 && idx[i] >= pool_slots))
+                    return fail(PKV_ERR_INDEX, "%s: kv_indices[%d] = %d is not a %s slot", who, i,
+                                idx[i], tiered ? "pool or host-pool" : "pool");
         }
         if (p->shared) {
             // the shared-prefix kernel reads each shared slot once, from the first
@@ -656,6 +709,11 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
     a.k_new = fused ? k_new : nullptr;
     a.v_new = fused ? v_new : nullptr;
     a.slot_ids = fused ? slot_ids : nullptr;
+    a.k_host = tiered ? kh : nullptr;
+    a.v_host = tiered ? vh : nullptr;
+    a.small = p->step_small ? 1 : 0;
+    a.batch = batch;
+    a.kv_indptr = kv_indptr;
     cudaError_t e = launch_decode(a, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch");
     return PKV_OK;
@@ -671,6 +729,22 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
     return attn_impl("paged_decode_attn", q, k_pool, v_pool, kv_indptr, kv_indices, batch,
                      n_qo_heads, n_kv_heads, head_dim, sm_scale, out, lse, p, stream, nullptr,
                      nullptr, nullptr, 0);
+}
+
+int paged_decode_attn_tiered(const void* q, const void* k_pool, const void* v_pool,
+                             int64_t pool_slots, const void* k_host, const void* v_host,
+                             int64_t host_slots, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, int batch, int n_qo_heads, int n_kv_heads,
+                             int head_dim, float sm_scale, void* out, float* lse,
+                             const pkv_plan* p, pkv_stream_t stream) {
+    clear_error();
+    if (!k_host || !v_host)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn_tiered: k_host and v_host are required");
+    if (pool_slots <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn_tiered: pool_slots must be > 0");
+    return attn_impl("paged_decode_attn_tiered", q, k_pool, v_pool, kv_indptr, kv_indices, batch,
+                     n_qo_heads, n_kv_heads, head_dim, sm_scale, out, lse, p, stream, nullptr,
+                     nullptr, nullptr, pool_slots, k_host, v_host, host_slots);
 }
 
 int paged_decode_append_attn(const void* q, void* k_pool, void* v_pool, const int32_t* kv_indptr,

@@ -178,6 +178,8 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     a.merge_ctas = sms;
     a.status = reinterpret_cast<int*>(scratch + kOffStatus);
     a.zero_row = scratch + kOffZero;
+    a.k_host = a.v_host = nullptr;
+    a.small = 0;
     e = launch_decode(a, stream);
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "paged_decode_attn_static: launch: %s", cudaGetErrorString(e));

@@ -132,6 +132,11 @@ struct Cfg {
     static constexpr int kDimsPerWarp = D / WPH;
     static constexpr int kQHeads = kHeadsPerCta * G;            // query heads of a group
     static constexpr int kAhead = kStages + 1;                  // stages of slot ids in flight
+    // With early gather, the stages issued before the previous kernel has completed:
+    // one fewer than the ring holds, so the next layer's start loads less of the
+    // memory system while the previous layer's merge runs (measured faster than a
+    // full ring or a single stage on the Qwen3-4B-shaped step)
+    static constexpr int kEarlyStages = kStages - 1;
     static constexpr int kBarOffset = kStages * kStage;
     static constexpr int kIdxOffset = kBarOffset + 2 * kStages * 8 + 16;
     // copies of one stage: K then V rows of kStageTokens tokens; copy c is issued by
@@ -148,10 +153,24 @@ struct Cfg {
     static_assert(kMBlocks >= 1, "dims per warp");
 };
 
+// Shared memory of the single-launch kernel for small steps: Cfg's layout plus a
+// barrier and its one work unit; its partial result is written over the drained
+// ring as [kQHeads][D] fp32, then the kQHeads base-2 lse values.
+template <int D, int G, int WPH>
+struct SmallCfg {
+    using C = Cfg<D, G, WPH, 1>;
+    static constexpr int kOffset = (C::kSmem + 15) / 16 * 16;
+    static constexpr int kSmem = kOffset + 16 + 32;
+    static constexpr int kPartBytes = C::kQHeads * D * 4 + C::kQHeads * 4;
+    static_assert(kPartBytes <= C::kStages * C::kStage, "a partial result fits the ring");
+};
+
 struct Shared {
     uint64_t* full;
     uint64_t* empty;
+    uint64_t* cdone;      // single-launch steps: every consumer warp has consumed its unit
     volatile int* flags;  // [0] abort
+    const Unit* units;    // the CTA's work units (the plan's list, or one built on the device)
 };
 
 __device__ __forceinline__ int unit_stages(const Unit& un, int stage_tokens) {
@@ -171,7 +190,7 @@ struct SlotFetch {
 
 template <class C>
 __device__ __forceinline__ void fetch_slot_ids(const DecodeArgs& a, SlotFetch& f, int u_end,
-                                               int lane, uint32_t ring) {
+                                               int lane, uint32_t ring, const Unit* units) {
     if (f.u < u_end) {
         const int n = min(C::kStageTokens, (f.un.tok_end - f.un.tok_begin) - f.t * C::kStageTokens);
         const int32_t* idx = a.kv_indices + f.un.idx_begin + f.t * C::kStageTokens;
@@ -180,7 +199,7 @@ __device__ __forceinline__ void fetch_slot_ids(const DecodeArgs& a, SlotFetch& f
         if (++f.t == f.n_stages) {
             f.t = 0;
             if (++f.u < u_end) {
-                f.un = a.units[f.u];
+                f.un = units[f.u];
                 f.n_stages = unit_stages(f.un, C::kStageTokens);
             }
         }
@@ -202,6 +221,7 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     const int lane = threadIdx.x & 31;
     const int pw = (threadIdx.x >> 5) - C::kConsumerWarps;  // producer warp index
     const bool fused = a.k_new != nullptr;
+    const bool tiered = a.k_host != nullptr;
     const int64_t slot_bytes = int64_t(a.n_kv_heads) * D * 2;
     // this lane's copies: token, K or V, and shared-memory offset within a stage
     int tok[C::kCopiesPerLane];
@@ -228,7 +248,7 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     // warp) its slot ids are prefetched into L2 once the current unit's first stage
     // is on its way.
     if (a.withhold) return;  // injected stall: the consumers' waits expire (bounded)
-    Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
+    Unit next = u_begin < u_end ? sh.units[u_begin] : Unit{};
     // Slot ids and pool rows may come from the previous kernel: wait for it, after
     // warming L2 with the first unit's slot ids (prefetches are hints, not reads).
     // With early gather they were final before the step's plan upload, so the
@@ -241,11 +261,12 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     if (waited) pdl_wait();
     SlotFetch f{u_begin, 0, u_begin < u_end ? unit_stages(next, C::kStageTokens) : 0, next, 0};
 #pragma unroll 1
-    for (int i = 0; i < C::kAhead; ++i) fetch_slot_ids<C>(a, f, u_end, lane, id_ring);
-    int pos = 0;  // ring place of the stage being issued
+    for (int i = 0; i < C::kAhead; ++i) fetch_slot_ids<C>(a, f, u_end, lane, id_ring, sh.units);
+    int pos = 0;     // ring place of the stage being issued
+    int issued = 0;  // stages issued so far
     for (int u = u_begin; u < u_end && !aborted; ++u) {
         const Unit un = next;
-        if (u + 1 < u_end) next = a.units[u + 1];
+        if (u + 1 < u_end) next = sh.units[u + 1];
         const int32_t* idx = a.kv_indices + un.idx_begin;
         const int n_tok = un.tok_end - un.tok_begin;
         const int n_stages = unit_stages(un, C::kStageTokens);
@@ -271,35 +292,81 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             // this stage's slot ids (the oldest group in flight) have landed
             cp_async_wait<C::kAhead - 1>();
             __syncwarp();
+            // slot id of each copy of this lane; a copy past the stage's tokens pads
+            // the tile with the zero row
             int slot[C::kCopiesPerLane];
+            bool row[C::kCopiesPerLane];
 #pragma unroll
-            for (int i = 0; i < C::kCopiesPerLane; ++i)
-                slot[i] = has[i] && tok[i] < n ? id_ring_ptr[pos * C::kStageTokens + tok[i]] : -1;
+            for (int i = 0; i < C::kCopiesPerLane; ++i) {
+                row[i] = has[i] && tok[i] < n;
+                slot[i] = row[i] ? id_ring_ptr[pos * C::kStageTokens + tok[i]] : 0;
+            }
             __syncwarp();  // every lane has read its ids before the place is refilled below
+            if (!waited && issued == C::kEarlyStages) {
+                pdl_wait();
+                waited = true;
+            }
+            ++issued;
             // k_new / v_new may come from the previous kernel
             const int first = un.tok_begin + t * C::kStageTokens;
             if (!waited && fused && un.len - 1 >= first && un.len - 1 < first + n) {
                 pdl_wait();
                 waited = true;
             }
-            if (lane == 0) mbar_arrive_expect_tx(full_bar, n > 0 ? C::kStageTx / P : 0u);
-            __syncwarp();
-            if (n > 0) {
+            if (!tiered) {
+                if (lane == 0) mbar_arrive_expect_tx(full_bar, n > 0 ? C::kStageTx / P : 0u);
+                __syncwarp();
+                if (n > 0) {
+#pragma unroll
+                    for (int i = 0; i < C::kCopiesPerLane; ++i) {
+                        if (!has[i]) continue;
+                        const char* pool = static_cast<const char*>(is_v[i] ? a.v_pool : a.k_pool);
+                        const void* src = row[i] ? static_cast<const void*>(pool + slot[i] * slot_bytes + group_off)
+                                                 : a.zero_row;
+                        // fused append: the request's newest token comes from its new row
+                        if (fused && first + tok[i] == un.len - 1)
+                            src = static_cast<const char*>(is_v[i] ? a.v_new : a.k_new) + un.b * slot_bytes +
+                                  group_off;
+                        bulk_g2s_hint(dst[i] + stage * C::kStage, src, C::kRow, full_bar, policy);
+                    }
+                }
+            } else {
+                // Host KV tier: a negative slot id -1 - h names row h of the pinned host
+                // pools. Those rows come over NVLink-C2C by 16-byte cp.async from this
+                // lane, whose completion the barrier tracks (one arrival per lane and
+                // stage); the rest are bulk copies counted in transaction bytes.
+                bool host[C::kCopiesPerLane];
+                int n_host = 0;
 #pragma unroll
                 for (int i = 0; i < C::kCopiesPerLane; ++i) {
-                    if (!has[i]) continue;
-                    const char* pool = static_cast<const char*>(is_v[i] ? a.v_pool : a.k_pool);
-                    const void* src = slot[i] >= 0
-                                          ? static_cast<const void*>(pool + slot[i] * slot_bytes + group_off)
-                                          : a.zero_row;
-                    // fused append: the request's newest token comes from its new row
-                    if (fused && first + tok[i] == un.len - 1)
-                        src = static_cast<const char*>(is_v[i] ? a.v_new : a.k_new) + un.b * slot_bytes +
-                              group_off;
-                    bulk_g2s_hint(dst[i] + stage * C::kStage, src, C::kRow, full_bar, policy);
+                    host[i] = n > 0 && row[i] && slot[i] < 0;
+                    n_host += host[i] ? 1 : 0;
                 }
+                const int warp_host = __reduce_add_sync(kFull, n_host);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full_bar, n > 0 ? C::kStageTx / P - uint32_t(warp_host) * C::kRow : 0u);
+                __syncwarp();
+                if (n > 0) {
+#pragma unroll
+                    for (int i = 0; i < C::kCopiesPerLane; ++i) {
+                        if (!has[i]) continue;
+                        if (host[i]) {
+                            const char* src = static_cast<const char*>(is_v[i] ? a.v_host : a.k_host) +
+                                              int64_t(-1 - slot[i]) * slot_bytes + group_off;
+                            const uint32_t d = dst[i] + stage * C::kStage;
+#pragma unroll 8
+                            for (int c = 0; c < C::kRow / 16; ++c) cp_async16(d + 16 * c, src + 16 * c, true);
+                            continue;
+                        }
+                        const char* pool = static_cast<const char*>(is_v[i] ? a.v_pool : a.k_pool);
+                        const void* src = row[i] ? static_cast<const void*>(pool + slot[i] * slot_bytes + group_off)
+                                                 : a.zero_row;
+                        bulk_g2s_hint(dst[i] + stage * C::kStage, src, C::kRow, full_bar, policy);
+                    }
+                }
+                cp_async_arrive_noinc(full_bar);  // fires once this lane's copies have landed
             }
-            fetch_slot_ids<C>(a, f, u_end, lane, id_ring);  // refills place `pos`
+            fetch_slot_ids<C>(a, f, u_end, lane, id_ring, sh.units);  // refills place `pos`
             if (++pos == C::kAhead) pos = 0;
             filled_mask |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (fill_parity << stage);
@@ -373,7 +440,9 @@ __device__ __forceinline__ void store_new_rows(const DecodeArgs& a, const Unit& 
     }
 }
 
-template <int D, int G, int WPH, int NB>
+// kSmall: the single-launch kernel for small steps, whose one unit writes its partial
+// result over the CTA's drained ring for the cluster's merge.
+template <int D, int G, int WPH, int NB, bool kSmall = false>
 __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
     using C = Cfg<D, G, WPH, NB>;
@@ -398,7 +467,7 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
     // unit streams; with two (shared prefixes) they are loaded at the unit's start.
     constexpr bool kPrefetchQ = NB == 1;
     uint32_t qb[NB][C::kKSteps][2], qn[NB][C::kKSteps][2];
-    Unit next = u_begin < u_end ? a.units[u_begin] : Unit{};
+    Unit next = u_begin < u_end ? sh.units[u_begin] : Unit{};
     // Warm L2 with the first unit's q rows (a hint, safe before the wait): lane l
     // touches query row l of this warp's KV head.
     if (u_begin < u_end && lane < C::kWarpRows && lane / G < next.nreq) {
@@ -427,7 +496,7 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             load_q_fragments<D, G, WPH, NB>(a, un, hh, r0, g, t4, qb);
         }
         if (u + 1 < u_end) {
-            next = a.units[u + 1];
+            next = sh.units[u + 1];
             if constexpr (kPrefetchQ) load_q_fragments<D, G, WPH, NB>(a, next, hh, r0, g, t4, qn);
         }
         // A warp whose rows are all beyond the unit's requests only passes the stages on.
@@ -530,6 +599,13 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             }
         }
 
+        if constexpr (kSmall) {
+            // the ring is reused for the partial result once every consumer warp has
+            // consumed its last stage (bounded wait, like every other)
+            if (lane == 0) mbar_arrive(smem_u32(sh.cdone));
+            const bool ok = mbar_wait(smem_u32(sh.cdone), 0, a.status, sh.flags);
+            if (!__all_sync(kFull, ok)) return;
+        }
         // ---- epilogue: o[nb][mb][0..3] = (dim 16*mb' + g (+8), rows r0 + 8nb + 2t4, +1)
         if (!active) continue;
         const int dim0 = part * C::kDimsPerWarp + g;
@@ -556,14 +632,17 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                     if (a.lse != nullptr && part == 0 && g == 0)
                         a.lse[int64_t(un.b + req) * hq + kvh * G + h] = lse2 * kLn2;
                 } else {
-                    const int64_t prow = int64_t(un.partial + req) * C::kQHeads + hh * G + h;
-                    float* dst = a.ws_o + prow * D + dim0;
+                    const int64_t prow = kSmall ? hh * G + h
+                                                : int64_t(un.partial + req) * C::kQHeads + hh * G + h;
+                    float* part_o = kSmall ? reinterpret_cast<float*>(smem) : a.ws_o;
+                    float* part_lse = kSmall ? reinterpret_cast<float*>(smem) + C::kQHeads * D : a.ws_lse;
+                    float* dst = part_o + prow * D + dim0;
 #pragma unroll
                     for (int mb = 0; mb < C::kMBlocks; ++mb) {
                         dst[mb * 16] = o[nb][mb][jc] * inv;
                         dst[mb * 16 + 8] = o[nb][mb][2 + jc] * inv;
                     }
-                    if (part == 0 && g == 0) a.ws_lse[prow] = lse2;
+                    if (part == 0 && g == 0) part_lse[prow] = lse2;
                 }
             }
         }
@@ -578,10 +657,15 @@ __global__ void __launch_bounds__(Cfg<D, G, WPH, NB>::kThreads, Cfg<D, G, WPH, N
     Shared sh;
     sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
     sh.empty = sh.full + C::kStages;
+    sh.cdone = nullptr;
     sh.flags = reinterpret_cast<volatile int*>(sh.full + 2 * C::kStages);
+    sh.units = a.units;
     if (threadIdx.x == 0) {
+        // a stage completes on one arrival per producer warp (plus, with the host KV
+        // tier, one per producer lane for its cp.async copies) and the bulk bytes
+        const uint32_t full_arrivals = C::kProducerWarps * (a.k_host != nullptr ? 33 : 1);
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(&sh.full[s]), C::kProducerWarps);
+            mbar_init(smem_u32(&sh.full[s]), full_arrivals);
             mbar_init(smem_u32(&sh.empty[s]), C::kConsumerWarps);
         }
         sh.flags[0] = 0;
@@ -597,6 +681,152 @@ __global__ void __launch_bounds__(Cfg<D, G, WPH, NB>::kThreads, Cfg<D, G, WPH, N
         producer_warp<D, G, WPH, NB>(a, smem, sh, u_begin, u_end);
     else
         consumer_warp<D, G, WPH, NB>(a, smem, sh, u_begin, u_end);
+}
+
+// ---------------------------------------------------------------------------
+// Small steps in one launch: a thread-block cluster per (request, head group)
+// ---------------------------------------------------------------------------
+// A plan whose capacity is small (a few requests of short contexts, the
+// latency-bound single-request decode) runs each step as one launch with no work
+// list: cluster c serves (request c / groups, head group c % groups), and its CTA of
+// rank r takes the r-th of cs stage-aligned shares of the request's slot list, read
+// from kv_indptr on the device. Every CTA ends with a partial result in its own
+// shared memory; after a cluster barrier the consumer warps of the cluster merge
+// the query heads' parts by the log-sum-exp identity, reading the peers' results
+// through distributed shared memory (ld.shared::cluster), and write out and lse. A
+// second cluster barrier keeps every CTA's shared memory alive until its peers have
+// read it. Every thread reaches both barriers, also after a bounded wait ran out.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+
+template <int D, int G, int WPH>
+__global__ void __launch_bounds__(Cfg<D, G, WPH, 1>::kThreads, 1)
+    paged_decode_small_kernel(const DecodeArgs a) {
+    using C = Cfg<D, G, WPH, 1>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    Shared sh;
+    sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    sh.empty = sh.full + C::kStages;
+    sh.flags = reinterpret_cast<volatile int*>(sh.full + 2 * C::kStages);
+    sh.cdone = reinterpret_cast<uint64_t*>(smem + SmallCfg<D, G, WPH>::kOffset);
+    Unit* unit = reinterpret_cast<Unit*>(smem + SmallCfg<D, G, WPH>::kOffset + 16);
+    sh.units = unit;
+    constexpr int cs = kSmallCluster;
+    const uint32_t rank = cluster_rank();
+    const int item = blockIdx.x / cs;
+    const int n_groups = a.n_kv_heads / C::kHeadsPerCta;
+    const bool has_item = item < a.batch * n_groups;  // the same for the whole cluster
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) {
+        const uint32_t full_arrivals = C::kProducerWarps * (a.k_host != nullptr ? 33 : 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), full_arrivals);
+            mbar_init(smem_u32(&sh.empty[s]), C::kConsumerWarps);
+        }
+        mbar_init(smem_u32(sh.cdone), C::kConsumerWarps);
+        sh.flags[0] = 0;
+        if (has_item) {
+            // with early gather kv_indptr was final before the step's plan call
+            if (!a.early) pdl_wait();
+            const int b = item / n_groups;
+            const int ip0 = a.kv_indptr[b], ip1 = a.kv_indptr[b + 1];
+            const int L = ip1 - ip0;
+            const int st = C::kStageTokens;
+            const int share = ((L + cs - 1) / cs + st - 1) / st * st;
+            const int t0 = min(int(rank) * share, L), t1 = min(t0 + share, L);
+            *unit = Unit{b, item % n_groups, t0, t1, int(rank), 1, ip0 + t0, L};
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int n_units = has_item ? 1 : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= C::kConsumerWarps)
+        producer_warp<D, G, WPH, 1>(a, smem, sh, 0, n_units);
+    else
+        consumer_warp<D, G, WPH, 1, true>(a, smem, sh, 0, n_units);
+    __syncwarp();
+    cluster_sync_all();  // every CTA's partial result is in its shared memory
+    if (has_item && warp < C::kConsumerWarps) {
+        constexpr int kVD = D / 32;  // dims per lane
+        const Unit un = *unit;
+        const uint32_t part_base = smem_u32(smem);
+        for (int qh = int(rank) * C::kConsumerWarps + warp; qh < C::kQHeads;
+             qh += C::kConsumerWarps * cs) {
+            // lane p < cs holds part p's base-2 lse
+            const float lp =
+                lane < cs ? dsmem_ld_f32(dsmem_addr(part_base + (C::kQHeads * D + qh) * 4, lane)) : neg_inf();
+            float4 x[cs][kVD / 4];
+#pragma unroll
+            for (int p = 0; p < cs; ++p)
+#pragma unroll
+                for (int i = 0; i < kVD / 4; ++i)
+                    x[p][i] = dsmem_ld_f32x4(dsmem_addr(part_base + (qh * D + lane * kVD + 4 * i) * 4, p));
+            float mx = lp;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+            const float e = lp == neg_inf() ? 0.f : ex2(lp - mx);
+            float sm = e;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(kFull, sm, off);
+            float acc[kVD];
+#pragma unroll
+            for (int i = 0; i < kVD; ++i) acc[i] = 0.f;
+#pragma unroll
+            for (int p = 0; p < cs; ++p) {
+                const float w = __shfl_sync(kFull, e, p);
+#pragma unroll
+                for (int i = 0; i < kVD / 4; ++i) {
+                    acc[4 * i] = fmaf(w, x[p][i].x, acc[4 * i]);
+                    acc[4 * i + 1] = fmaf(w, x[p][i].y, acc[4 * i + 1]);
+                    acc[4 * i + 2] = fmaf(w, x[p][i].z, acc[4 * i + 2]);
+                    acc[4 * i + 3] = fmaf(w, x[p][i].w, acc[4 * i + 3]);
+                }
+            }
+            const float inv = sm > 0.f ? 1.f / sm : 0.f;
+            const int h = (un.hg * C::kHeadsPerCta) * G + qh;  // query head index
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
+                                 (int64_t(un.b) * a.n_qo_heads + h) * D + lane * kVD;
+#pragma unroll
+            for (int i = 0; i < kVD; i += 4) {
+                uint2 packed;
+                packed.x = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+                packed.y = pack_bf16x2(acc[i + 2] * inv, acc[i + 3] * inv);
+                *reinterpret_cast<uint2*>(dst + i) = packed;
+            }
+            if (a.lse != nullptr && lane == 0)
+                a.lse[int64_t(un.b) * a.n_qo_heads + h] = sm > 0.f ? (mx + __log2f(sm)) * kLn2 : neg_inf();
+        }
+    }
+    __syncwarp();
+    cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
 }
 
 // ---------------------------------------------------------------------------
@@ -778,6 +1008,64 @@ cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, WPH, NB>, a);
 }
 
+template <int D, int G, int WPH>
+cudaError_t prepare_small() {
+    static cudaError_t status = [] {
+        auto k = paged_decode_small_kernel<D, G, WPH>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SmallCfg<D, G, WPH>::kSmem);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return e;
+    }();
+    return status;
+}
+
+template <int D, int G, int WPH>
+cudaLaunchConfig_t small_config(int grid, cudaStream_t stream, cudaLaunchAttribute (&attr)[2]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Cfg<D, G, WPH, 1>::kThreads);
+    cfg.dynamicSmemBytes = SmallCfg<D, G, WPH>::kSmem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSmallCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    return cfg;
+}
+
+// Clusters of the single-launch kernel that fit on the device at once (0: the kernel
+// cannot run, e.g. no 16-CTA clusters).
+template <int D, int G, int WPH>
+int small_clusters() {
+    if (prepare_small<D, G, WPH>() != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = small_config<D, G, WPH>(kSmallCluster, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, paged_decode_small_kernel<D, G, WPH>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int D, int G, int WPH>
+cudaError_t launch_small(const DecodeArgs& a, cudaStream_t stream) {
+    cudaError_t e = prepare_small<D, G, WPH>();
+    if (e != cudaSuccess) return e;
+    if (a.n_ctas == 0) return cudaSuccess;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = small_config<D, G, WPH>(a.n_ctas, stream, attr);
+    return cudaLaunchKernelEx(&cfg, paged_decode_small_kernel<D, G, WPH>, a);
+}
+
 // Calls FN<D, G, WPH, NB>::run(args...) for the runtime shape. `shared` selects
 // the shared-prefix instance (two query blocks per warp), which exists only at
 // head_dim 128 with one warp per KV head.
@@ -821,6 +1109,16 @@ struct LaunchFn {
     static cudaError_t unsupported() { return cudaErrorInvalidValue; }
 };
 template <int D, int G, int WPH, int NB>
+struct SmallClustersFn {
+    static int run() { return NB == 1 ? small_clusters<D, G, WPH>() : 0; }
+    static int unsupported() { return 0; }
+};
+template <int D, int G, int WPH, int NB>
+struct SmallLaunchFn {
+    static cudaError_t run(const DecodeArgs& a, cudaStream_t s) { return launch_small<D, G, WPH>(a, s); }
+    static cudaError_t unsupported() { return cudaErrorInvalidValue; }
+};
+template <int D, int G, int WPH, int NB>
 struct RowsFn {
     static int run() { return Cfg<D, G, WPH, NB>::kWarpRows; }
     static int unsupported() { return 0; }
@@ -855,7 +1153,16 @@ int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_p
                                  shared);
 }
 
+int decode_small_clusters(int n_qo_heads, int n_kv_heads, int head_dim) {
+    if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim)) return 0;
+    const int hpc = heads_per_group(n_kv_heads, head_dim);
+    return dispatch<SmallClustersFn>(head_dim, n_qo_heads / n_kv_heads, warps_per_head(hpc), false);
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.small)
+        return dispatch<SmallLaunchFn>(a.head_dim, a.n_qo_heads / a.n_kv_heads,
+                                       warps_per_head(a.heads_per_cta), false, a, stream);
     cudaError_t e = dispatch<LaunchFn>(a.head_dim, a.n_qo_heads / a.n_kv_heads,
                                        warps_per_head(a.heads_per_cta), a.shared, a, stream);
     if (e != cudaSuccess) return e;

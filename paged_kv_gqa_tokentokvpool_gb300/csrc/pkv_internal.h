@@ -131,6 +131,15 @@ struct DecodeArgs {
     const void* k_new;
     const void* v_new;
     const int32_t* slot_ids;
+    // Host KV tier (both set, or both NULL; never with the fused append): GPU-visible
+    // addresses of pinned host pools; a negative slot id -1 - h names host row h.
+    const void* k_host;
+    const void* v_host;
+    // Single-launch small steps (small != 0): no work list; the kernel reads the step's
+    // kv_indptr ([batch + 1], on the device) and merges split parts in each cluster.
+    int small;
+    int batch;
+    const int32_t* kv_indptr;
 };
 
 bool decode_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim);
@@ -142,6 +151,15 @@ int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_p
 // rows / G requests of a sharing group), or 0 when this shape has no such kernel.
 int decode_shared_rows(int n_qo_heads, int n_kv_heads, int head_dim, int heads_per_cta);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// ---- small steps in one launch ----------------------------------------------
+// CTAs of one thread-block cluster of the single-launch kernel (a non-portable
+// cluster size): each (request, head group) of a small step is split 16 ways.
+constexpr int kSmallCluster = 16;
+// A small-step plan's longest context gives each CTA at most this many stages.
+constexpr int kSmallMaxStages = 8;
+// Clusters of that kernel resident at once for this shape (0: it cannot run here).
+int decode_small_clusters(int n_qo_heads, int n_kv_heads, int head_dim);
 
 // Row scatter between two pools (either may be pinned host memory mapped for the GPU):
 // dst[dst_slots[i]] = src[src_slots[i]] for K and V, i < n.
@@ -190,6 +208,10 @@ struct pkv_plan {
     unsigned flags = 0;  // PKV_PLAN_* options
     bool shared = false; // the current step runs the shared-prefix kernel
     int launch_ctas = 0; // grid of the current step's decode kernel
+    // Small-step mode (fixed at creation): every step runs as one launch of the
+    // cluster kernel, which reads kv_indptr on the device; nothing is uploaded.
+    bool small = false;
+    bool step_small = false;  // the current step runs in that mode
     std::vector<int32_t> indptr_host;
     // the current step's sharing description (checked against kv_indices when
     // debug checks are on and the shared-prefix kernel runs)

@@ -86,6 +86,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
                  "r"(valid ? 16 : 0)
                  : "memory");
 }
+// Arrive on an mbarrier once every cp.async this thread issued so far has landed;
+// the barrier's expected count already includes this arrival (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }

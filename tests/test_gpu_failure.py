@@ -22,8 +22,12 @@ def pkv():
     return m
 
 
-def test_expired_waits_set_the_status_word_and_the_context_survives(pkv):
-    wl = workloads.scattered_workload([3000, 17, 900, 1], seed=61)
+@pytest.mark.parametrize("lengths", [[3000, 17, 900, 1], [500, 17, 900, 1]],
+                         ids=["persistent_grid", "single_launch"])
+def test_expired_waits_set_the_status_word_and_the_context_survives(pkv, lengths):
+    """The second workload's plan is small enough for the single-launch cluster kernel,
+    whose CTAs also meet at cluster barriers after the bounded waits have run out."""
+    wl = workloads.scattered_workload(lengths, seed=61)
     t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
     dev = torch.device("cuda")
     kp, vp = t.k_pool.to(dev), t.v_pool.to(dev)
@@ -32,6 +36,7 @@ def test_expired_waits_set_the_status_word_and_the_context_survives(pkv):
     slots = torch.from_numpy(wl.append_slots).to(dev)
     pkv.kvpool_append(kp, vp, slots, t.k_new.to(dev), t.v_new.to(dev))
     plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, 32, 8, 128)
+    assert plan.single_launch() == (wl.total_tokens <= 2048)
     pkv.paged_decode_plan(plan, wl.kv_indptr)
     q = t.q.to(dev)
     out = torch.zeros(wl.batch, 32, 128, dtype=torch.bfloat16, device=dev)

@@ -679,6 +679,201 @@ def test_host_tier_round_trip_then_attention(pkv):
     assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what="after prefetch")
 
 
+SINGLE_LAUNCH_CASES = [
+    # (lengths, Hq, Hkv, D): plans small enough for the single-launch cluster kernel
+    ([512], 32, 8, 128),
+    ([1], 32, 8, 128),
+    ([0, 5, 1500], 32, 8, 128),
+    ([17, 300, 33], 16, 4, 256),
+    ([2000, 1], 8, 8, 128),      # G = 1
+    ([700, 64], 64, 8, 128),     # G = 8
+    ([100, 2000], 4, 2, 128),    # two KV heads per group
+    ([1000], 8, 1, 256),         # one KV head, G = 8
+]
+
+
+@pytest.mark.parametrize("persistent", [False, True], ids=["single_launch", "persistent"])
+@pytest.mark.parametrize("fused", [False, True], ids=["attn", "append_attn"])
+@pytest.mark.parametrize("case", range(len(SINGLE_LAUNCH_CASES)))
+def test_small_step_modes(pkv, case, fused, persistent):
+    """A small plan runs its steps as one launch of the cluster kernel (slot-list
+    shares per CTA, merged in distributed shared memory); PKV_PLAN_PERSISTENT runs
+    the same step on the persistent grid. Both must equal the oracle."""
+    lengths, hq, hkv, d = SINGLE_LAUNCH_CASES[case]
+    if fused and 0 in lengths:
+        pytest.skip("the fused append needs a newest token in every request")
+    wl = workloads.scattered_workload(lengths, n_qo_heads=hq, n_kv_heads=hkv, head_dim=d,
+                                      seed=700 + case)
+    t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
+    dev = torch.device("cuda")
+    kp, vp = t.k_pool.to(dev), t.v_pool.to(dev)
+    out = torch.full((wl.batch, hq, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((wl.batch, hq), float("nan"), dtype=torch.float32, device=dev)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx = torch.from_numpy(wl.kv_indices if wl.kv_indices.size else np.zeros(1, np.int32)).to(dev)
+    slots = torch.from_numpy(wl.append_slots).to(dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, max(wl.total_tokens, 1), hq, hkv, d)
+    flags = pkv.PKV_PLAN_EARLY_GATHER if fused else 0
+    plan.set_flags(flags | (pkv.PKV_PLAN_PERSISTENT if persistent else 0))
+    assert plan.single_launch() == (not persistent)
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    pkv.pkv_set_debug_checks(True)
+    try:
+        if fused:
+            pkv.paged_decode_append_attn(t.q.to(dev), kp, vp, ip, idx, slots, t.k_new.to(dev),
+                                         t.v_new.to(dev), wl.batch, hq, hkv, d, wl.sm_scale, out,
+                                         lse, plan)
+        else:
+            pkv.kvpool_append(kp, vp, slots, t.k_new.to(dev), t.v_new.to(dev))
+            pkv.paged_decode_attn(t.q.to(dev), kp, vp, ip, idx, wl.batch, hq, hkv, d, wl.sm_scale,
+                                  out, lse, plan)
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    assert plan.status() == 0
+    ref_out, ref_lse = oracle_reference(wl, t)
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse,
+                  what=f"small case {case} fused={fused} persistent={persistent}")
+    k_after = oracle.append(bits(t.k_pool), wl.append_slots, bits(t.k_new))
+    assert np.array_equal(bits(kp), k_after)
+
+
+def test_single_launch_graph_steps(pkv):
+    """Small-step mode under CUDA-graph replay: three layers captured once, replayed
+    for several steps, each step re-planned on the host (nothing uploaded); every
+    layer equals the oracle and no bounded wait expires."""
+    wl = workloads.scattered_workload([300, 1200, 40], layers=3, seed=41)
+    dev = torch.device("cuda")
+    plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, 32, 8, 128)
+    plan.set_flags(pkv.PKV_PLAN_EARLY_GATHER)
+    assert plan.single_launch()
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx = torch.from_numpy(wl.kv_indices).to(dev)
+    slots = torch.from_numpy(wl.append_slots).to(dev)
+    layers = [workloads.layer_tensors(wl, l, poison_unreferenced=True) for l in range(3)]
+    dt = [(t.q.to(dev), t.k_pool.to(dev), t.v_pool.to(dev), t.k_new.to(dev), t.v_new.to(dev))
+          for t in layers]
+    outs = [torch.empty(wl.batch, 32, 128, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    lses = [torch.empty(wl.batch, 32, dtype=torch.float32, device=dev) for _ in range(3)]
+
+    def step_layers():
+        for (q, kp, vp, kn, vn), o, l in zip(dt, outs, lses):
+            pkv.paged_decode_append_attn(q, kp, vp, ip, idx, slots, kn, vn, wl.batch, 32, 8, 128,
+                                         wl.sm_scale, o, l, plan)
+
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step_layers()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step_layers()
+    for _ in range(4):
+        pkv.paged_decode_plan(plan, wl.kv_indptr)
+        g.replay()
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    for layer in range(3):
+        ref_out, ref_lse = oracle_reference(wl, layers[layer])
+        assert_parity(to_f64(outs[layer]), lses[layer].cpu().numpy(), ref_out, ref_lse,
+                      what=f"single-launch graph layer {layer}")
+
+
+TIERED_CASES = [
+    # (lengths, Hq, Hkv, D, fraction of listed rows kept in host memory)
+    ([3000, 17, 900, 5000, 1], 32, 8, 128, 0.4),
+    ([1, 700, 12000, 9], 16, 4, 256, 0.25),
+    ([4097, 2, 300], 8, 1, 128, 1.0),
+    ([20000], 32, 8, 128, 0.05),
+]
+
+
+@pytest.mark.parametrize("case", range(len(TIERED_CASES)))
+def test_tiered_attention_reads_host_rows_in_place(pkv, case):
+    """paged_decode_attn_tiered: lists that mix HBM slots and host slots (-1 - h). The
+    HBM copies of the host-resident rows are NaN, so any read of them from HBM shows;
+    results must equal the oracle on the original placement."""
+    lengths, hq, hkv, d, frac = TIERED_CASES[case]
+    wl = workloads.scattered_workload(lengths, n_qo_heads=hq, n_kv_heads=hkv, head_dim=d,
+                                      seed=610 + case)
+    t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
+    k_bits = oracle.append(bits(t.k_pool), wl.append_slots, bits(t.k_new))
+    v_bits = oracle.append(bits(t.v_pool), wl.append_slots, bits(t.v_new))
+    ref_out, ref_lse = oracle.decode(bits(t.q), k_bits, v_bits, wl.kv_indptr, wl.kv_indices,
+                                     hq, hkv, d, wl.sm_scale)
+    rng = np.random.default_rng(case)
+    n = wl.total_tokens
+    moved = np.sort(rng.choice(n, size=max(1, int(frac * n)), replace=False))
+    host_rows = rng.permutation(len(moved) + 7)[:len(moved)]  # scattered in a larger host pool
+    as_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    k_host = torch.full((len(moved) + 7, hkv, d), float("nan"), dtype=torch.bfloat16).pin_memory()
+    v_host = torch.full((len(moved) + 7, hkv, d), float("nan"), dtype=torch.bfloat16).pin_memory()
+    slots = wl.kv_indices[moved]
+    k_host[torch.from_numpy(host_rows)] = as_bf16(k_bits[slots])
+    v_host[torch.from_numpy(host_rows)] = as_bf16(v_bits[slots])
+    k_dev, v_dev = k_bits.copy(), v_bits.copy()
+    k_dev[slots] = workloads.BF16_NAN_BITS
+    v_dev[slots] = workloads.BF16_NAN_BITS
+    indices = wl.kv_indices.copy()
+    indices[moved] = -1 - host_rows.astype(np.int32)
+    dev = torch.device("cuda")
+    kp, vp = as_bf16(k_dev).to(dev), as_bf16(v_dev).to(dev)
+    out = torch.full((wl.batch, hq, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((wl.batch, hq), float("nan"), dtype=torch.float32, device=dev)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx = torch.from_numpy(indices).to(dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, hq, hkv, d)
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    pkv.pkv_set_debug_checks(True)
+    try:
+        pkv.paged_decode_attn_tiered(t.q.to(dev), kp, vp, k_host, v_host, ip, idx, wl.batch, hq,
+                                     hkv, d, wl.sm_scale, out, lse, plan)
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    assert plan.status() == 0
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what=f"tiered case {case}")
+    # a second call without debug checks (no host synchronisation in between)
+    out2 = torch.full_like(out, float("nan"))
+    pkv.paged_decode_attn_tiered(t.q.to(dev), kp, vp, k_host, v_host, ip, idx, wl.batch, hq, hkv,
+                                 d, wl.sm_scale, out2, None, plan)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, out)
+    assert plan.status() == 0
+
+
+def test_tiered_attention_rejects_bad_host_arguments(pkv):
+    wl = workloads.scattered_workload([50, 60], seed=5)
+    dev = torch.device("cuda")
+    t = workloads.layer_tensors(wl, 0, device=dev)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx_np = wl.kv_indices.copy()
+    idx_np[3] = -20  # host row 19 of a 10-row host pool
+    idx = torch.from_numpy(idx_np).to(dev)
+    out = torch.full((wl.batch, 32, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, 32, 8, 128)
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    pinned = torch.zeros(10, 8, 128, dtype=torch.bfloat16).pin_memory()
+    pageable = torch.zeros(10, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode_attn_tiered(t.q, t.k_pool, t.v_pool, pageable, pageable, ip, idx,
+                                     wl.batch, 32, 8, 128, wl.sm_scale, out, None, plan)
+    assert e.value.code == pkv.PKV_ERR_INVALID_ARG
+    pkv.pkv_set_debug_checks(True)
+    try:
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.paged_decode_attn_tiered(t.q, t.k_pool, t.v_pool, pinned, pinned, ip, idx,
+                                         wl.batch, 32, 8, 128, wl.sm_scale, out, None, plan)
+        assert e.value.code == pkv.PKV_ERR_INDEX
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    torch.cuda.synchronize()
+    assert torch.isnan(out.float()).all()  # nothing launched
+
+
 def test_host_tier_rejects_pageable_and_duplicate_destinations(pkv):
     dev = torch.device("cuda")
     kp = torch.zeros(64, 8, 128, dtype=torch.bfloat16, device=dev)

@@ -165,10 +165,12 @@ def test_prefill_empty_step(pkv):
 @pytest.mark.parametrize("config_no", [1, 2, 3])
 def test_prefill_full_size_sampled(pkv, config_no):
     """The benchmark's prefill workloads at full size (layer 0): every row of the
-    smallest request's chunk, and the first and last 16 rows of every other chunk
-    (by causality, the first rows need only the list up to their positions and
-    the last rows only a shorter chunk over the whole list). The 64-token chunks over
-    long contexts (config 2) go through split ranges and the merge kernel."""
+    chunk of the request with the longest context (every unit of it at the full
+    tile count, and for the 64-token chunks of config 2 its split ranges and their
+    merge), every row of the smallest request's chunk, and the first and last 16
+    rows of every other chunk (by causality, the first rows need only the list up
+    to their positions and the last rows only a shorter chunk over the whole
+    list)."""
     pw = workloads.prefill_config(config_no)
     out, lse, tensors, _ = run_prefill(pkv, pw)
     q, kp, vp, kn, vn = tensors
@@ -176,11 +178,13 @@ def test_prefill_full_size_sampled(pkv, config_no):
     v_after = oracle.append(bits(vp), pw.chunk_slots, bits(vn))
     qb = bits(q)
     smallest = int(np.argmin(pw.contexts))
+    longest = int(np.argmax(pw.contexts))
     for b in range(pw.batch):
         C, L = int(pw.chunks[b]), int(pw.contexts[b])
         q0, k0 = int(pw.qo_indptr[b]), int(pw.kv_indptr[b])
         idx = pw.kv_indices[k0:k0 + L]
-        pieces = [(0, C)] if (b == smallest and config_no == 1) else [(0, 16), (C - 16, C)]
+        whole = b == longest or (b == smallest and config_no == 1)
+        pieces = [(0, C)] if whole else [(0, 16), (C - 16, C)]
         for c0, c1 in pieces:
             # rows c0 .. c1 of the chunk: a chunk of c1 - c0 tokens over the first
             # L - C + c1 list entries
