@@ -112,6 +112,18 @@ int kvpool_prefetch(void* k_pool, void* v_pool, const int32_t* dev_slots, const 
  *   n_qo_heads, n_kv_heads, head_dim : the attention shape the plan serves
  * Uses the current CUDA device; the plan must be used on that device.
  * Synchronous. Returns PKV_ERR_UNSUPPORTED for shapes outside the supported set.
+ *
+ * Small plans (max_batch x KV-head groups within the thread-block clusters the
+ * device holds at once, and max_tokens at most 16 x 8 pipeline stages, 2048 tokens
+ * at head_dim 128 with 8 KV heads) run their steps in single-launch mode, the
+ * latency-bound decode of one or a few requests: paged_decode_plan uploads
+ * nothing, and each attention call is one launch of a cluster kernel in which 16
+ * CTAs split each (request, head group), read kv_indptr on the device, and merge
+ * their parts through distributed shared memory. In this mode each attention
+ * launch carries the step's batch: a CUDA graph of attention calls is valid only
+ * for steps with the batch it was captured with (PKV_PLAN_PERSISTENT keeps the
+ * persistent grid, whose graphs serve any batch). paged_decode_plan_mode reports
+ * the mode.
  */
 int paged_decode_plan_create(pkv_plan** plan, int max_batch, int64_t max_tokens,
                              int n_qo_heads, int n_kv_heads, int head_dim);
@@ -443,8 +455,8 @@ int paged_decode_plan_host_times(pkv_plan* plan, double* compute_us, double* wai
 /*
  * paged_decode_plan_set_flags — options for the attention calls that use `plan`
  * (this library's own; the pages have no counterpart). Replaces the plan's flags.
- *   PKV_PLAN_EARLY_GATHER: the caller promises that kv_indices and every K/V pool
- *     row that the step's attention calls read were written by work enqueued on
+ *   PKV_PLAN_EARLY_GATHER: the caller promises that kv_indptr, kv_indices and every
+ *     K/V pool row that the step's attention calls read were written by work enqueued on
  *     the stream before this step's paged_decode_plan / paged_decode_plan_shared
  *     call, and that nothing writes them between that call and the step's last
  *     attention call. Exempt are the newest rows that paged_decode_append_attn
@@ -457,6 +469,9 @@ int paged_decode_plan_host_times(pkv_plan* plan, double* compute_us, double* wai
  *     steps and whose new token is appended by paged_decode_append_attn. It does
  *     not fit a step that calls kvpool_append or kvpool_prefetch after the plan.
  *     Off by default; a broken promise gives stale rows, not an error.
+ *   PKV_PLAN_PERSISTENT: a small plan's steps run on the persistent grid with an
+ *     uploaded work list instead of in single-launch mode (paged_decode_plan_create);
+ *     takes effect from the next paged_decode_plan call.
  *   flags : a bitwise OR of PKV_PLAN_* values (0 = none)
  * Returns PKV_ERR_PLAN for a NULL plan and PKV_ERR_INVALID_ARG for unknown bits.
  * Takes effect for attention calls enqueued after it returns.

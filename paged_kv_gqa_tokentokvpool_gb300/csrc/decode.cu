@@ -153,24 +153,26 @@ struct Cfg {
     static_assert(kMBlocks >= 1, "dims per warp");
 };
 
-// Shared memory of the single-launch kernel for small steps: Cfg's layout plus a
-// barrier and its one work unit; its partial result is written over the drained
-// ring as [kQHeads][D] fp32, then the kQHeads base-2 lse values.
+// Shared memory of the single-launch kernel for small steps: Cfg's layout, its one
+// work unit, and its partial result as [kQHeads][D] fp32 then the kQHeads base-2 lse
+// values (a region of its own, so each consumer warp writes its rows as soon as it
+// is done). Two CTAs share an SM where both fit.
 template <int D, int G, int WPH>
 struct SmallCfg {
     using C = Cfg<D, G, WPH, 1>;
-    static constexpr int kOffset = (C::kSmem + 15) / 16 * 16;
-    static constexpr int kSmem = kOffset + 16 + 32;
+    static constexpr int kUnitOffset = (C::kSmem + 15) / 16 * 16;
+    static constexpr int kPartOffset = kUnitOffset + 32;
     static constexpr int kPartBytes = C::kQHeads * D * 4 + C::kQHeads * 4;
-    static_assert(kPartBytes <= C::kStages * C::kStage, "a partial result fits the ring");
+    static constexpr int kSmem = kPartOffset + kPartBytes;
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
 
 struct Shared {
     uint64_t* full;
     uint64_t* empty;
-    uint64_t* cdone;      // single-launch steps: every consumer warp has consumed its unit
     volatile int* flags;  // [0] abort
     const Unit* units;    // the CTA's work units (the plan's list, or one built on the device)
+    int part_offset;      // single-launch steps: shared-memory offset of the partial result
 };
 
 __device__ __forceinline__ int unit_stages(const Unit& un, int stage_tokens) {
@@ -332,36 +334,52 @@ __device__ void producer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                 }
             } else {
                 // Host KV tier: a negative slot id -1 - h names row h of the pinned host
-                // pools. Those rows come over NVLink-C2C by 16-byte cp.async from this
-                // lane, whose completion the barrier tracks (one arrival per lane and
-                // stage); the rest are bulk copies counted in transaction bytes.
-                bool host[C::kCopiesPerLane];
-                int n_host = 0;
+                // pools, read over NVLink-C2C by the warp's lanes together with 16-byte
+                // cp.async (each row 16 bytes a lane); the other rows are bulk copies.
+                // The barrier tracks the lanes' copies (one .noinc arrival per lane and
+                // stage) and the bulk bytes.
+                bool by_lanes[C::kCopiesPerLane];
+                int n_by_lanes = 0;
 #pragma unroll
                 for (int i = 0; i < C::kCopiesPerLane; ++i) {
-                    host[i] = n > 0 && row[i] && slot[i] < 0;
-                    n_host += host[i] ? 1 : 0;
+                    by_lanes[i] = n > 0 && has[i] && row[i] && slot[i] < 0;
+                    n_by_lanes += by_lanes[i] ? 1 : 0;
                 }
-                const int warp_host = __reduce_add_sync(kFull, n_host);
+                const int warp_by_lanes = __reduce_add_sync(kFull, n_by_lanes);
                 if (lane == 0)
-                    mbar_arrive_expect_tx(full_bar, n > 0 ? C::kStageTx / P - uint32_t(warp_host) * C::kRow : 0u);
+                    mbar_arrive_expect_tx(full_bar,
+                                          n > 0 ? C::kStageTx / P - uint32_t(warp_by_lanes) * C::kRow : 0u);
                 __syncwarp();
                 if (n > 0) {
 #pragma unroll
                     for (int i = 0; i < C::kCopiesPerLane; ++i) {
-                        if (!has[i]) continue;
-                        if (host[i]) {
-                            const char* src = static_cast<const char*>(is_v[i] ? a.v_host : a.k_host) +
-                                              int64_t(-1 - slot[i]) * slot_bytes + group_off;
-                            const uint32_t d = dst[i] + stage * C::kStage;
-#pragma unroll 8
-                            for (int c = 0; c < C::kRow / 16; ++c) cp_async16(d + 16 * c, src + 16 * c, true);
-                            continue;
+                        const char* src = nullptr;
+                        if (has[i]) {
+                            if (tiered && row[i] && slot[i] < 0) {
+                                src = static_cast<const char*>(is_v[i] ? a.v_host : a.k_host) +
+                                      int64_t(-1 - slot[i]) * slot_bytes + group_off;
+                            } else {
+                                const char* pool = static_cast<const char*>(is_v[i] ? a.v_pool : a.k_pool);
+                                src = row[i] ? pool + slot[i] * slot_bytes + group_off
+                                             : static_cast<const char*>(a.zero_row);
+                                // fused append: the request's newest token comes from its new row
+                                if (fused && first + tok[i] == un.len - 1)
+                                    src = static_cast<const char*>(is_v[i] ? a.v_new : a.k_new) +
+                                          un.b * slot_bytes + group_off;
+                            }
                         }
-                        const char* pool = static_cast<const char*>(is_v[i] ? a.v_pool : a.k_pool);
-                        const void* src = row[i] ? static_cast<const void*>(pool + slot[i] * slot_bytes + group_off)
-                                                 : a.zero_row;
-                        bulk_g2s_hint(dst[i] + stage * C::kStage, src, C::kRow, full_bar, policy);
+                        const uint32_t d_mine = dst[i] + stage * C::kStage;
+                        if (has[i] && !by_lanes[i]) bulk_g2s_hint(d_mine, src, C::kRow, full_bar, policy);
+                        // the rows of copy i of every lane, one after another, 16 bytes a lane
+                        unsigned todo = __ballot_sync(kFull, by_lanes[i]);
+                        while (todo) {
+                            const int l = __ffs(todo) - 1;
+                            todo &= todo - 1;
+                            const char* s = reinterpret_cast<const char*>(
+                                __shfl_sync(kFull, reinterpret_cast<unsigned long long>(src), l));
+                            const uint32_t d = __shfl_sync(kFull, d_mine, l);
+                            for (int c = lane; c < C::kRow / 16; c += 32) cp_async16(d + 16 * c, s + 16 * c, true);
+                        }
                     }
                 }
                 cp_async_arrive_noinc(full_bar);  // fires once this lane's copies have landed
@@ -441,7 +459,7 @@ __device__ __forceinline__ void store_new_rows(const DecodeArgs& a, const Unit& 
 }
 
 // kSmall: the single-launch kernel for small steps, whose one unit writes its partial
-// result over the CTA's drained ring for the cluster's merge.
+// result to the CTA's shared memory for the cluster's merge.
 template <int D, int G, int WPH, int NB, bool kSmall = false>
 __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& sh, int u_begin,
                               int u_end) {
@@ -599,13 +617,6 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
             }
         }
 
-        if constexpr (kSmall) {
-            // the ring is reused for the partial result once every consumer warp has
-            // consumed its last stage (bounded wait, like every other)
-            if (lane == 0) mbar_arrive(smem_u32(sh.cdone));
-            const bool ok = mbar_wait(smem_u32(sh.cdone), 0, a.status, sh.flags);
-            if (!__all_sync(kFull, ok)) return;
-        }
         // ---- epilogue: o[nb][mb][0..3] = (dim 16*mb' + g (+8), rows r0 + 8nb + 2t4, +1)
         if (!active) continue;
         const int dim0 = part * C::kDimsPerWarp + g;
@@ -634,8 +645,8 @@ __device__ void consumer_warp(const DecodeArgs& a, uint8_t* smem, const Shared& 
                 } else {
                     const int64_t prow = kSmall ? hh * G + h
                                                 : int64_t(un.partial + req) * C::kQHeads + hh * G + h;
-                    float* part_o = kSmall ? reinterpret_cast<float*>(smem) : a.ws_o;
-                    float* part_lse = kSmall ? reinterpret_cast<float*>(smem) + C::kQHeads * D : a.ws_lse;
+                    float* part_o = kSmall ? reinterpret_cast<float*>(smem + sh.part_offset) : a.ws_o;
+                    float* part_lse = kSmall ? part_o + C::kQHeads * D : a.ws_lse;
                     float* dst = part_o + prow * D + dim0;
 #pragma unroll
                     for (int mb = 0; mb < C::kMBlocks; ++mb) {
@@ -657,9 +668,9 @@ __global__ void __launch_bounds__(Cfg<D, G, WPH, NB>::kThreads, Cfg<D, G, WPH, N
     Shared sh;
     sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
     sh.empty = sh.full + C::kStages;
-    sh.cdone = nullptr;
     sh.flags = reinterpret_cast<volatile int*>(sh.full + 2 * C::kStages);
     sh.units = a.units;
+    sh.part_offset = 0;
     if (threadIdx.x == 0) {
         // a stage completes on one arrival per producer warp (plus, with the host KV
         // tier, one per producer lane for its cp.async copies) and the bulk bytes
@@ -716,28 +727,19 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
-__device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-
 template <int D, int G, int WPH>
-__global__ void __launch_bounds__(Cfg<D, G, WPH, 1>::kThreads, 1)
+__global__ void __launch_bounds__(SmallCfg<D, G, WPH>::C::kThreads, 2)
     paged_decode_small_kernel(const DecodeArgs a) {
-    using C = Cfg<D, G, WPH, 1>;
+    using C = typename SmallCfg<D, G, WPH>::C;
     extern __shared__ __align__(128) uint8_t smem[];
     Shared sh;
     sh.full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
     sh.empty = sh.full + C::kStages;
     sh.flags = reinterpret_cast<volatile int*>(sh.full + 2 * C::kStages);
-    sh.cdone = reinterpret_cast<uint64_t*>(smem + SmallCfg<D, G, WPH>::kOffset);
-    Unit* unit = reinterpret_cast<Unit*>(smem + SmallCfg<D, G, WPH>::kOffset + 16);
+    using SC = SmallCfg<D, G, WPH>;
+    Unit* unit = reinterpret_cast<Unit*>(smem + SC::kUnitOffset);
     sh.units = unit;
+    sh.part_offset = SC::kPartOffset;
     constexpr int cs = kSmallCluster;
     const uint32_t rank = cluster_rank();
     const int item = blockIdx.x / cs;
@@ -750,7 +752,6 @@ __global__ void __launch_bounds__(Cfg<D, G, WPH, 1>::kThreads, 1)
             mbar_init(smem_u32(&sh.full[s]), full_arrivals);
             mbar_init(smem_u32(&sh.empty[s]), C::kConsumerWarps);
         }
-        mbar_init(smem_u32(sh.cdone), C::kConsumerWarps);
         sh.flags[0] = 0;
         if (has_item) {
             // with early gather kv_indptr was final before the step's plan call
@@ -775,20 +776,23 @@ __global__ void __launch_bounds__(Cfg<D, G, WPH, 1>::kThreads, 1)
     __syncwarp();
     cluster_sync_all();  // every CTA's partial result is in its shared memory
     if (has_item && warp < C::kConsumerWarps) {
-        constexpr int kVD = D / 32;  // dims per lane
+        // CTA r merges query heads r, r + cs, ...; its consumer warps split head_dim,
+        // kDL dims per lane
+        constexpr int kDL = D / (32 * C::kConsumerWarps);
         const Unit un = *unit;
-        const uint32_t part_base = smem_u32(smem);
-        for (int qh = int(rank) * C::kConsumerWarps + warp; qh < C::kQHeads;
-             qh += C::kConsumerWarps * cs) {
-            // lane p < cs holds part p's base-2 lse
-            const float lp =
-                lane < cs ? dsmem_ld_f32(dsmem_addr(part_base + (C::kQHeads * D + qh) * 4, lane)) : neg_inf();
-            float4 x[cs][kVD / 4];
+        const uint32_t part_base = smem_u32(smem + SC::kPartOffset);
+        const int dim0 = warp * 32 * kDL + lane * kDL;
+        for (int qh = int(rank); qh < C::kQHeads; qh += cs) {
+            // lane p < cs holds part p's base-2 lse (the other lanes read part 0's and drop it)
+            const float lv = dsmem_ld_f32(dsmem_addr(part_base + (C::kQHeads * D + qh) * 4,
+                                                     lane < cs ? lane : 0));
+            const float lp = lane < cs ? lv : neg_inf();
+            float x[cs][kDL];
 #pragma unroll
             for (int p = 0; p < cs; ++p)
 #pragma unroll
-                for (int i = 0; i < kVD / 4; ++i)
-                    x[p][i] = dsmem_ld_f32x4(dsmem_addr(part_base + (qh * D + lane * kVD + 4 * i) * 4, p));
+                for (int i = 0; i < kDL; ++i)
+                    x[p][i] = dsmem_ld_f32(dsmem_addr(part_base + (qh * D + dim0 + i) * 4, p));
             float mx = lp;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
@@ -796,32 +800,27 @@ __global__ void __launch_bounds__(Cfg<D, G, WPH, 1>::kThreads, 1)
             float sm = e;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(kFull, sm, off);
-            float acc[kVD];
+            float acc[kDL];
 #pragma unroll
-            for (int i = 0; i < kVD; ++i) acc[i] = 0.f;
+            for (int i = 0; i < kDL; ++i) acc[i] = 0.f;
 #pragma unroll
             for (int p = 0; p < cs; ++p) {
                 const float w = __shfl_sync(kFull, e, p);
 #pragma unroll
-                for (int i = 0; i < kVD / 4; ++i) {
-                    acc[4 * i] = fmaf(w, x[p][i].x, acc[4 * i]);
-                    acc[4 * i + 1] = fmaf(w, x[p][i].y, acc[4 * i + 1]);
-                    acc[4 * i + 2] = fmaf(w, x[p][i].z, acc[4 * i + 2]);
-                    acc[4 * i + 3] = fmaf(w, x[p][i].w, acc[4 * i + 3]);
-                }
+                for (int i = 0; i < kDL; ++i) acc[i] = fmaf(w, x[p][i], acc[i]);
             }
             const float inv = sm > 0.f ? 1.f / sm : 0.f;
             const int h = (un.hg * C::kHeadsPerCta) * G + qh;  // query head index
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                                 (int64_t(un.b) * a.n_qo_heads + h) * D + lane * kVD;
+                                 (int64_t(un.b) * a.n_qo_heads + h) * D + dim0;
+            if constexpr (kDL == 1) {
+                dst[0] = __float2bfloat16_rn(acc[0] * inv);
+            } else {
 #pragma unroll
-            for (int i = 0; i < kVD; i += 4) {
-                uint2 packed;
-                packed.x = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
-                packed.y = pack_bf16x2(acc[i + 2] * inv, acc[i + 3] * inv);
-                *reinterpret_cast<uint2*>(dst + i) = packed;
+                for (int i = 0; i < kDL; i += 2)
+                    *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
             }
-            if (a.lse != nullptr && lane == 0)
+            if (a.lse != nullptr && warp == 0 && lane == 0)
                 a.lse[int64_t(un.b) * a.n_qo_heads + h] = sm > 0.f ? (mx + __log2f(sm)) * kLn2 : neg_inf();
         }
     }
@@ -1024,7 +1023,7 @@ template <int D, int G, int WPH>
 cudaLaunchConfig_t small_config(int grid, cudaStream_t stream, cudaLaunchAttribute (&attr)[2]) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(Cfg<D, G, WPH, 1>::kThreads);
+    cfg.blockDim = dim3(SmallCfg<D, G, WPH>::C::kThreads);
     cfg.dynamicSmemBytes = SmallCfg<D, G, WPH>::kSmem;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -63,9 +63,10 @@ def oracle_reference(wl, t, layer_pools=None):
                          wl.n_qo_heads, wl.n_kv_heads, wl.head_dim, wl.sm_scale)
 
 
-def run_small(pkv, wl, layer=0, debug=False):
+def run_small(pkv, wl, layer=0, debug=False, persistent=False):
     """Append + plan + attention for one layer of a small workload; returns GPU
-    results, generated tensors and the GPU pools after append."""
+    results, generated tensors and the GPU pools after append. persistent: keep the
+    persistent grid even when the plan is small enough for single-launch mode."""
     t = workloads.layer_tensors(wl, layer, device="cpu", poison_unreferenced=True)
     dev = torch.device("cuda")
     k_pool, v_pool = t.k_pool.to(dev), t.v_pool.to(dev)
@@ -83,6 +84,8 @@ def run_small(pkv, wl, layer=0, debug=False):
         pkv.kvpool_append(k_pool, v_pool, slots, t.k_new.to(dev), t.v_new.to(dev))
         plan = pkv.paged_decode_plan_create(max(wl.batch, 1), max(wl.total_tokens, 1),
                                             wl.n_qo_heads, wl.n_kv_heads, wl.head_dim)
+        if persistent:
+            plan.set_flags(pkv.PKV_PLAN_PERSISTENT)
         pkv.paged_decode_plan(plan, wl.kv_indptr)
         pkv.paged_decode_attn(q, k_pool, v_pool, indptr, indices, wl.batch, wl.n_qo_heads,
                               wl.n_kv_heads, wl.head_dim, wl.sm_scale, out, lse, plan)
@@ -119,12 +122,15 @@ SMALL_CASES = [
 ]
 
 
+@pytest.mark.parametrize("persistent", [False, True], ids=["auto", "persistent"])
 @pytest.mark.parametrize("case", range(len(SMALL_CASES)))
-def test_decode_small_cases(pkv, case):
+def test_decode_small_cases(pkv, case, persistent):
+    """Every case planned by default (single launch where the plan is small enough)
+    and on the persistent grid."""
     lengths, hq, hkv, d = SMALL_CASES[case]
     wl = workloads.scattered_workload(lengths, n_qo_heads=hq, n_kv_heads=hkv, head_dim=d,
                                       seed=100 + case, k_scale=1.0)
-    out, lse, t, _, _, plan = run_small(pkv, wl, debug=(case % 2 == 0))
+    out, lse, t, _, _, plan = run_small(pkv, wl, debug=(case % 2 == 0), persistent=persistent)
     ref_out, ref_lse = oracle_reference(wl, t)
     assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what=f"case {case}")
     assert plan.status() == 0
@@ -557,6 +563,7 @@ def test_shared_prefix_plan(pkv, case, fused):
     idx = torch.from_numpy(wl.kv_indices).to(dev)
     slots = torch.from_numpy(wl.append_slots).to(dev)
     plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, hq, hkv, d)
+    plan.set_flags(pkv.PKV_PLAN_PERSISTENT)  # the shared-prefix kernel runs on the persistent grid
     shared_indptr = np.arange(0, gsize * len(prefixes) + 1, gsize, dtype=np.int32)
     pkv.paged_decode_plan_shared(plan, wl.kv_indptr, shared_indptr, np.array(prefixes, np.int32))
     if fused:
@@ -588,6 +595,7 @@ def test_false_sharing_description_is_rejected_with_debug_checks(pkv):
     idx = torch.from_numpy(wl.kv_indices).to(dev)
     slots = torch.from_numpy(wl.append_slots).to(dev)
     plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, 32, 8, 128)
+    plan.set_flags(pkv.PKV_PLAN_PERSISTENT)  # the shared-prefix kernel runs on the persistent grid
     # claims requests 0-3 share their first 200 slots
     pkv.paged_decode_plan_shared(plan, wl.kv_indptr, np.array([0, 4], np.int32),
                                  np.array([200], np.int32))
