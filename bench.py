@@ -160,10 +160,10 @@ class StepState:
         else:
             self.layers(attn_events)
         if self.launches_per_step is None:
-            info = self.plan.info()
-            # append (unless fused), decode kernel, merge kernel (launched even when
-            # nothing is split)
-            per_layer = (0 if self.fused or not len(self.wl.append_slots) else 1) + 2
+            # append (unless fused), then the decode kernel and the merge kernel (launched
+            # even when nothing is split), or the one single-launch kernel of a small plan
+            attn = 1 if self.plan.single_launch() else 2
+            per_layer = (0 if self.fused or not len(self.wl.append_slots) else 1) + attn
             self.launches_per_step = per_layer * len(self.layer_ids)
 
     def capture(self):
@@ -792,6 +792,9 @@ def measure_decode(config_no: int, args, world=1, pg=None, local=0, cpu_budget=N
     achieved = nbytes["step"] / n_layers / (layer_ms * 1e-3) / 1e9
     eager_gbs = nbytes["attn_per_layer"] / (attn_avg_ms * 1e-3) / 1e9
     info = st.plan.info()
+    attn_kernels = ("paged_decode_attn (single-launch cluster kernel, merge in distributed "
+                    "shared memory): " if st.plan.single_launch() else
+                    "paged_decode_attn (split-KV decode kernel + LSE merge kernel): ")
     traffic = _profiled_traffic(config_no) if layers is None else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -834,7 +837,7 @@ def measure_decode(config_no: int, args, world=1, pg=None, local=0, cpu_budget=N
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "paged_decode_attn (split-KV decode kernel + LSE merge kernel): "
+                     "kernel": attn_kernels +
                                f"{layer_ms * 1e3:.1f} us per call in the timed graph replay "
                                f"(step time over {n_layers} layers), "
                                f"{nbytes['step'] / n_layers / 1e6:.1f} MB algorithmic per call",
