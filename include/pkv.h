@@ -196,7 +196,9 @@ int paged_decode_plan_shared(pkv_plan* plan, const int32_t* kv_indptr_host, int 
  *   plan       : built by paged_decode_plan for this step with the same batch and
  *                created for the same (n_qo_heads, n_kv_heads, head_dim)
  * Launches the split-KV kernel and then the LSE-merge kernel (the latter exits at
- * once when no context was split). A plan serves one stream at a time.
+ * once when no context was split); a plan in single-launch mode (small plans, see
+ * paged_decode_plan_create) launches one cluster kernel instead. A plan serves one
+ * stream at a time.
  */
 int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
                       const int32_t* kv_indptr, const int32_t* kv_indices, int batch,

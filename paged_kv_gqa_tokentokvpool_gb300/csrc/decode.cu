@@ -52,6 +52,13 @@
 //  * Every wait on an mbarrier is bounded (1 s); on expiry the kernel sets the
 //    plan's status word, stops, and waits (again bounded) for its own copies in
 //    flight before exiting.
+//  * Host KV tier: a negative slot id names a row of pinned host pools, which the
+//    producer warp's lanes copy together over NVLink-C2C with 16-byte cp.async (the
+//    stage barrier counts one arrival per lane for them).
+//  * Small steps run as one launch of a second kernel on thread-block clusters of 16
+//    CTAs (one cluster per request and head group, no work list): each CTA reads
+//    kv_indptr, takes a share of the slot list, and the cluster merges its parts
+//    through distributed shared memory (see paged_decode_small_kernel).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

@@ -85,6 +85,21 @@ def test_errors_are_reported_before_any_launch(pkv):
                                   None, None) == pkv.PKV_ERR_PLAN
     lib.paged_prefill_plan_destroy(None)  # no-op
     lib.paged_decode_plan_destroy(None)  # no-op
+    # the plan's mode, host times and the static entry's status need their out arguments
+    one = ctypes.c_int(7)
+    assert lib.paged_decode_plan_mode(None, ctypes.byref(one)) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.paged_decode_plan_host_times(None, None, None, None, 0) == pkv.PKV_ERR_PLAN
+    assert lib.paged_decode_attn_static_status(None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.paged_decode_plan_set_flags(None, pkv.PKV_PLAN_PERSISTENT) == pkv.PKV_ERR_PLAN
+    # host KV tier reads: both host pools and pool sizes are required before anything else
+    f = ctypes.c_float(0.1)
+    assert lib.paged_decode_attn_tiered(p, p, p, 16, None, p, 4, p, p, 1, 32, 8, 128, f, p, p,
+                                        None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert "k_host and v_host" in pkv.pkv_last_error()
+    assert lib.paged_decode_attn_tiered(p, p, p, 0, p, p, 4, p, p, 1, 32, 8, 128, f, p, p,
+                                        None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.paged_decode_attn_tiered(p, p, p, 16, p, p, 4, p, p, 1, 32, 8, 128, f, p, p,
+                                        None, None) == pkv.PKV_ERR_PLAN
 
 
 def test_header_constants_match_the_binding(pkv):
