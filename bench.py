@@ -953,14 +953,20 @@ def main(argv=None):
 
 
 def kernel_source_sha() -> str:
-    """sha256 of the sources that decide a decode call's DRAM traffic: the kernel
+    """sha256 of the code that decides a decode call's DRAM traffic: the kernel
     (csrc/decode.cu, then csrc/ptx.cuh) and the planner that splits the contexts
-    (csrc/plan_host.cpp: the split parts' partial results are part of the traffic)."""
+    (csrc/plan_host.cpp: the split parts' partial results are part of the traffic).
+    Line comments and blank lines are left out, so that an edit of comments alone keeps
+    a recorded capture valid, while any change of code does not."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in ("decode.cu", "ptx.cuh", "plan_host.cpp"):
-        with open(os.path.join(ROOT, "paged_kv_gqa_tokentokvpool_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_gqa_tokentokvpool_gb300", "csrc", name)) as f:
+            for line in f:
+                code = re.sub(r"//.*$", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()
 
 
