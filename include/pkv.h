@@ -270,7 +270,9 @@ int paged_decode_append_attn(const void* q, void* k_pool, void* v_pool, const in
  *   device when it loads the library's code there (with lazy module loading, at
  *   the first call). The first call on a device (with that device current) looks
  *   the array up with cudaGetSymbolAddress and zeroes its status word and zero row
- *   on `stream`, waiting for that; make it before any stream capture. Steps needing
+ *   on `stream`, waiting for that. A call on a stream that is being captured returns
+ *   PKV_ERR_UNSUPPORTED without enqueuing anything: its work list is staged in one
+ *   shared host array, which a graph would read again at every replay. Steps needing
  *   more than 32 MiB of scratch (or more than 1024 CTAs, 4096 (request, head
  *   group) pairs or 8192 work units) return PKV_ERR_PLAN with the size in the
  *   message.

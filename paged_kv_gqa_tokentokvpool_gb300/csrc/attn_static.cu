@@ -85,9 +85,18 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
         return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn_static: lse must be 4-byte aligned");
 
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &capturing);
+    if (e != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "paged_decode_attn_static: stream query: %s", cudaGetErrorString(e));
+    if (capturing != cudaStreamCaptureStatusNone)
+        return fail(PKV_ERR_UNSUPPORTED,
+                    "paged_decode_attn_static: the stream is being captured (the work list is "
+                    "staged in one shared host array, which a graph would replay)");
+
     std::lock_guard<std::mutex> lock(g_mutex);
     int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "paged_decode_attn_static: device query: %s", cudaGetErrorString(e));

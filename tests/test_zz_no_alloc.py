@@ -6,7 +6,8 @@ It is checked through the C ABI against the planned entry point, paged_decode_at
 and against the fp64 oracle, on two calls in a row whose work lists and split
 workspaces differ, so a second call that read stale scratch left by the first would
 show up; then on calls queued back to back on one stream with no host wait between
-them; then for its status word (an injected stall must be reported and cleared); and
+them; then that a call under stream capture is refused; then for its status word (an
+injected stall must be reported and cleared); and
 for allocation: in a fresh process, calls after the first leave the device's free
 memory unchanged, and with eager module loading so does the first. Tolerances are the
 ones of the parity tests: |out - ref| <= 1e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3, and
@@ -143,6 +144,33 @@ def test_static_calls_queued_back_to_back(pkv, orc):
     for i, (c, (o, l)) in enumerate(zip(cases + cases, outs + outs2)):
         c.check(o, l, f"queued call {i}")
     assert pkv.paged_decode_attn_static_status() == 0
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
+def test_static_call_refuses_stream_capture(pkv, orc):
+    """A call on a stream being captured returns PKV_ERR_UNSUPPORTED and enqueues
+    nothing (its work list lives in one shared host array, which a graph would replay);
+    the capture then ends with an empty graph, and the next eager call is correct."""
+    lib = pkv.library()
+    c = Case(pkv, orc, *CALLS[0])
+    out, lse = c.fresh_outputs()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    rc = None
+    with torch.cuda.stream(side):
+        g.capture_begin()
+        try:
+            rc = c.call_static(lib, out, lse, ctypes.c_void_p(side.cuda_stream))
+            message = pkv.pkv_last_error()
+        finally:
+            g.capture_end()
+    torch.cuda.current_stream().wait_stream(side)
+    assert rc == pkv.PKV_ERR_UNSUPPORTED and "captured" in message
+    assert c.call_static(lib, out, lse, _stream()) == 0, pkv.pkv_last_error()
+    torch.cuda.synchronize()
+    c.check(out, lse, "after the refused capture")
 
 
 def test_static_status_reports_an_expired_wait(pkv, orc):
