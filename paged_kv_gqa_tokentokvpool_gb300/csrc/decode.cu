@@ -77,7 +77,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
-constexpr int kProducersPerBlock = 2;  // producer warps per row block of consumer warps
+constexpr int kProducersPerBlock = 2;  // producer warps per CTA
 
 // ---------------------------------------------------------------------------
 // bounded waits (PTX ISA: mbarrier.try_wait, %globaltimer)
