@@ -119,6 +119,9 @@ SMALL_CASES = [
     ([300, 4000, 1], 4, 2, 128),
     ([2500, 9, 700], 8, 1, 128),
     ([5000, 33], 4, 1, 256),
+    # large batches of short contexts: many whole units per CTA, empty ones among them
+    ([1] * 4096, 32, 8, 128),
+    ([(7 * i) % 65 for i in range(2000)], 16, 4, 256),
 ]
 
 
