@@ -856,6 +856,55 @@ def test_tiered_attention_reads_host_rows_in_place(pkv, case):
     assert plan.status() == 0
 
 
+@pytest.mark.parametrize("case", range(2))
+def test_tiered_attention_with_shared_prefixes(pkv, case):
+    """paged_decode_attn_tiered with a paged_decode_plan_shared plan: a third of the
+    listed slots (shared prefix rows and private rows alike) live in the host pools,
+    their HBM copies NaN, and every member names a moved slot by the same host row, so
+    the prefix lists still agree."""
+    prefixes, gsize, suffixes = [([2000], 8, [1 + 97 * i for i in range(8)]),
+                                 ([700, 3100], 9, [1 + 31 * i for i in range(18)])][case]
+    wl = workloads.prefix_shared_workload(prefixes, suffixes, gsize, seed=660 + case)
+    t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
+    k_bits = oracle.append(bits(t.k_pool), wl.append_slots, bits(t.k_new))
+    v_bits = oracle.append(bits(t.v_pool), wl.append_slots, bits(t.v_new))
+    ref_out, ref_lse = oracle.decode(bits(t.q), k_bits, v_bits, wl.kv_indptr, wl.kv_indices,
+                                     32, 8, 128, wl.sm_scale)
+    rng = np.random.default_rng(case)
+    slots = np.unique(wl.kv_indices)
+    moved = np.sort(rng.choice(slots, size=len(slots) // 3, replace=False))
+    host_row = {int(s): i for i, s in enumerate(rng.permutation(moved))}
+    as_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    rows = np.array([host_row[int(s)] for s in moved])
+    k_host = torch.full((len(moved), 8, 128), float("nan"), dtype=torch.bfloat16).pin_memory()
+    v_host = torch.full((len(moved), 8, 128), float("nan"), dtype=torch.bfloat16).pin_memory()
+    k_host[torch.from_numpy(rows)] = as_bf16(k_bits[moved])
+    v_host[torch.from_numpy(rows)] = as_bf16(v_bits[moved])
+    k_dev, v_dev = k_bits.copy(), v_bits.copy()
+    k_dev[moved] = workloads.BF16_NAN_BITS
+    v_dev[moved] = workloads.BF16_NAN_BITS
+    indices = np.array([-1 - host_row[int(s)] if int(s) in host_row else int(s)
+                        for s in wl.kv_indices], np.int32)
+    dev = torch.device("cuda")
+    out = torch.full((wl.batch, 32, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((wl.batch, 32), float("nan"), dtype=torch.float32, device=dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, 32, 8, 128)
+    plan.set_flags(pkv.PKV_PLAN_PERSISTENT)  # the shared-prefix kernel runs on the persistent grid
+    shared_indptr = np.arange(0, gsize * len(prefixes) + 1, gsize, dtype=np.int32)
+    pkv.paged_decode_plan_shared(plan, wl.kv_indptr, shared_indptr, np.array(prefixes, np.int32))
+    pkv.pkv_set_debug_checks(True)  # also checks that the members' prefix ids agree
+    try:
+        pkv.paged_decode_attn_tiered(t.q.to(dev), as_bf16(k_dev).to(dev), as_bf16(v_dev).to(dev),
+                                     k_host, v_host, torch.from_numpy(wl.kv_indptr).to(dev),
+                                     torch.from_numpy(indices).to(dev), wl.batch, 32, 8, 128,
+                                     wl.sm_scale, out, lse, plan)
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_set_debug_checks(False)
+    assert plan.status() == 0
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what=f"tiered shared {case}")
+
+
 def test_tiered_attention_rejects_bad_host_arguments(pkv):
     wl = workloads.scattered_workload([50, 60], seed=5)
     dev = torch.device("cuda")
