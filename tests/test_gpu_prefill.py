@@ -238,3 +238,54 @@ def test_prefill_graph_replay_steps(pkv):
         ref_out, ref_lse = oracle_prefill(pw, layers[layer])
         assert_parity(to_f64(outs[layer]), lses[layer].cpu().numpy(), ref_out, ref_lse,
                       what=f"graph layer {layer}")
+
+
+def test_prefill_and_decode_overlap_on_two_streams(pkv):
+    """A mixed batch's two paths at once: decode steps of one model's layers on one
+    stream and chunked-prefill steps of another's on a second stream, enqueued
+    alternately with no host wait, so the kernels overlap on the GPU (each with its
+    own plan). Both results must equal the oracle's and both status words stay 0."""
+    dev = torch.device("cuda")
+    # decode: 16 requests of 300-5000 tokens
+    wl = workloads.scattered_workload([300 + 311 * i for i in range(16)], seed=71)
+    t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
+    kp_dec, vp_dec = t.k_pool.to(dev), t.v_pool.to(dev)
+    q_dec = t.q.to(dev)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx = torch.from_numpy(wl.kv_indices).to(dev)
+    slots = torch.from_numpy(wl.append_slots).to(dev)
+    k_new, v_new = t.k_new.to(dev), t.v_new.to(dev)
+    out_dec = torch.full((wl.batch, 32, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse_dec = torch.full((wl.batch, 32), float("nan"), dtype=torch.float32, device=dev)
+    dplan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, 32, 8, 128)
+    # prefill: two chunks of 200 and 64 tokens over contexts of 3000 and 900
+    pw = workloads.prefill_workload([200, 64], [3000, 900], seed=72)
+    q, kp, vp, kn, vn = workloads.prefill_tensors(pw, 0, device="cpu", poison_unreferenced=True)
+    kp_pf, vp_pf = kp.to(dev), vp.to(dev)
+    pslots = torch.from_numpy(pw.chunk_slots).to(dev)
+    kn_d, vn_d, q_pf = kn.to(dev), vn.to(dev), q.to(dev)
+    out_pf = torch.full((pw.total_q, 32, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse_pf = torch.full((pw.total_q, 32), float("nan"), dtype=torch.float32, device=dev)
+    pplan = pkv.paged_prefill_plan_create(pw.batch, pw.total_q, 32, 8, 128)
+    qo_d = torch.from_numpy(pw.qo_indptr).to(dev)
+    kv_d = torch.from_numpy(pw.kv_indptr).to(dev)
+    pidx = torch.from_numpy(pw.kv_indices).to(dev)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(6):  # repeated steps (the appends rewrite the same rows)
+        pkv.paged_decode_plan(dplan, wl.kv_indptr, stream=s1)
+        pkv.paged_prefill_plan(pplan, pw.qo_indptr, pw.kv_indptr, stream=s2)
+        for _layer in range(4):
+            pkv.paged_decode_append_attn(q_dec, kp_dec, vp_dec, ip, idx, slots, k_new, v_new,
+                                         wl.batch, 32, 8, 128, wl.sm_scale, out_dec, lse_dec,
+                                         dplan, stream=s1)
+            pkv.kvpool_append(kp_pf, vp_pf, pslots, kn_d, vn_d, stream=s2)
+            pkv.paged_prefill_attn(q_pf, kp_pf, vp_pf, qo_d, kv_d, pidx, pw.batch, 32, 8, 128,
+                                   pw.sm_scale, out_pf, lse_pf, pplan, stream=s2)
+    torch.cuda.synchronize()
+    assert dplan.status() == 0 and pplan.status() == 0
+    from test_gpu_parity import oracle_reference
+    ref_out, ref_lse = oracle_reference(wl, t)
+    assert_parity(to_f64(out_dec), lse_dec.cpu().numpy(), ref_out, ref_lse, what="decode beside prefill")
+    ref_out, ref_lse = oracle_prefill(pw, (q, kp, vp, kn, vn))
+    assert_parity(to_f64(out_pf), lse_pf.cpu().numpy(), ref_out, ref_lse, what="prefill beside decode")
