@@ -77,6 +77,7 @@ void pkv_inject_stall(int n_launches) { g_stalls_to_inject.store(n_launches > 0 
 int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const void* k_new,
                   const void* v_new, int64_t n, int n_kv_heads, int head_dim,
                   int64_t pool_slots, pkv_stream_t stream) {
+    TraceRange trace("kvpool_append");
     clear_error();
     if (n < 0) return fail(PKV_ERR_INVALID_ARG, "kvpool_append: n = %lld < 0", (long long)n);
     if (n_kv_heads <= 0 || head_dim <= 0 || pool_slots <= 0)
@@ -208,6 +209,7 @@ int tier_copy(const char* who, bool to_host, const void* k_dev, const void* v_de
 int kvpool_offload(const void* k_pool, const void* v_pool, const int32_t* dev_slots, void* k_host,
                    void* v_host, const int32_t* host_slots, int64_t n, int n_kv_heads,
                    int head_dim, int64_t pool_slots, int64_t host_slots_cap, pkv_stream_t stream) {
+    TraceRange trace("kvpool_offload");
     clear_error();
     return tier_copy("kvpool_offload", true, k_pool, v_pool, dev_slots, k_host, v_host,
                      host_slots, n, n_kv_heads, head_dim, pool_slots, host_slots_cap, stream);
@@ -216,6 +218,7 @@ int kvpool_offload(const void* k_pool, const void* v_pool, const int32_t* dev_sl
 int kvpool_prefetch(void* k_pool, void* v_pool, const int32_t* dev_slots, const void* k_host,
                     const void* v_host, const int32_t* host_slots, int64_t n, int n_kv_heads,
                     int head_dim, int64_t pool_slots, int64_t host_slots_cap, pkv_stream_t stream) {
+    TraceRange trace("kvpool_prefetch");
     clear_error();
     return tier_copy("kvpool_prefetch", false, k_pool, v_pool, dev_slots, k_host, v_host,
                      host_slots, n, n_kv_heads, head_dim, pool_slots, host_slots_cap, stream);
@@ -512,6 +515,7 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
 }  // namespace
 
 int paged_decode_plan(pkv_plan* p, const int32_t* kv_indptr_host, int batch, pkv_stream_t stream) {
+    TraceRange trace("paged_decode_plan");
     clear_error();
     return plan_impl("paged_decode_plan", p, kv_indptr_host, batch, nullptr, 0, nullptr, stream);
 }
@@ -519,6 +523,7 @@ int paged_decode_plan(pkv_plan* p, const int32_t* kv_indptr_host, int batch, pkv
 int paged_decode_plan_shared(pkv_plan* p, const int32_t* kv_indptr_host, int batch,
                              const int32_t* shared_indptr_host, int n_shared,
                              const int32_t* shared_len_host, pkv_stream_t stream) {
+    TraceRange trace("paged_decode_plan_shared");
     clear_error();
     return plan_impl("paged_decode_plan_shared", p, kv_indptr_host, batch, shared_indptr_host,
                      n_shared, shared_len_host, stream);
@@ -725,6 +730,7 @@ int paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
                       const int32_t* kv_indptr, const int32_t* kv_indices, int batch,
                       int n_qo_heads, int n_kv_heads, int head_dim, float sm_scale, void* out,
                       float* lse, const pkv_plan* p, pkv_stream_t stream) {
+    TraceRange trace("paged_decode_attn");
     clear_error();
     return attn_impl("paged_decode_attn", q, k_pool, v_pool, kv_indptr, kv_indices, batch,
                      n_qo_heads, n_kv_heads, head_dim, sm_scale, out, lse, p, stream, nullptr,
@@ -737,6 +743,7 @@ int paged_decode_attn_tiered(const void* q, const void* k_pool, const void* v_po
                              const int32_t* kv_indices, int batch, int n_qo_heads, int n_kv_heads,
                              int head_dim, float sm_scale, void* out, float* lse,
                              const pkv_plan* p, pkv_stream_t stream) {
+    TraceRange trace("paged_decode_attn_tiered");
     clear_error();
     if (!k_host || !v_host)
         return fail(PKV_ERR_INVALID_ARG, "paged_decode_attn_tiered: k_host and v_host are required");
@@ -752,6 +759,7 @@ int paged_decode_append_attn(const void* q, void* k_pool, void* v_pool, const in
                              const void* v_new, int batch, int n_qo_heads, int n_kv_heads,
                              int head_dim, int64_t pool_slots, float sm_scale, void* out,
                              float* lse, const pkv_plan* p, pkv_stream_t stream) {
+    TraceRange trace("paged_decode_append_attn");
     clear_error();
     if (!slot_ids) return fail(PKV_ERR_INVALID_ARG, "paged_decode_append_attn: slot_ids is NULL");
     if (pool_slots <= 0)

@@ -66,6 +66,7 @@ extern "C" int paged_decode_attn_static(const void* q, const void* k_pool, const
                                         const int32_t* kv_indices, int batch, int n_qo_heads,
                                         int n_kv_heads, int head_dim, float sm_scale, void* out,
                                         float* lse, pkv_stream_t stream) {
+    TraceRange trace("paged_decode_attn_static");
     clear_error();
     if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim))
         return fail(PKV_ERR_UNSUPPORTED,

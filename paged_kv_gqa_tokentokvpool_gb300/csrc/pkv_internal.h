@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
 #include <vector>
@@ -9,6 +10,18 @@
 #include "pkv.h"
 
 namespace pkv {
+
+// ---- tracing ------------------------------------------------------------
+// Every C entry point that enqueues GPU work runs inside an NVTX range of its name
+// (NVTX v3, header only), so profiler timelines show the library's calls and their
+// kernels, and ncu can select kernels by call (--nvtx --nvtx-include "name/"). With
+// no profiling tool attached a range costs a check of a function pointer.
+struct TraceRange {
+    explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange&) = delete;
+    TraceRange& operator=(const TraceRange&) = delete;
+};
 
 // ---- launches -----------------------------------------------------------
 // Kernels are launched with programmatic stream serialisation (PDL) unless the

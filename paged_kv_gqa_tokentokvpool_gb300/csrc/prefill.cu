@@ -949,6 +949,7 @@ void paged_prefill_plan_destroy(pkv_prefill_plan* p) {
 
 int paged_prefill_plan(pkv_prefill_plan* p, const int32_t* qo_indptr_host,
                        const int32_t* kv_indptr_host, int batch, pkv_stream_t stream) {
+    TraceRange trace("paged_prefill_plan");
     clear_error();
     const char* who = "paged_prefill_plan";
     if (!p) return fail(PKV_ERR_PLAN, "%s: plan is NULL", who);
@@ -1031,6 +1032,7 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
                        const int32_t* kv_indices, int batch, int n_qo_heads, int n_kv_heads,
                        int head_dim, float sm_scale, void* out, float* lse,
                        const pkv_prefill_plan* p, pkv_stream_t stream) {
+    TraceRange trace("paged_prefill_attn");
     clear_error();
     const char* who = "paged_prefill_attn";
     if (!p || !p->planned) return fail(PKV_ERR_PLAN, "%s: plan is NULL or not planned", who);
