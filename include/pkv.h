@@ -110,7 +110,8 @@ int kvpool_prefetch(void* k_pool, void* v_pool, const int32_t* dev_slots, const 
  *   max_batch  : largest batch any step will use (>= 1)
  *   max_tokens : largest kv_indptr[batch] any step will use (>= 0)
  *   n_qo_heads, n_kv_heads, head_dim : the attention shape the plan serves
- * Uses the current CUDA device; the plan must be used on that device.
+ * Uses the current CUDA device; the plan must be used on that device: every call that
+ * takes the plan returns PKV_ERR_INVALID_ARG when another device is current.
  * Synchronous. Returns PKV_ERR_UNSUPPORTED for shapes outside the supported set.
  *
  * Small plans (max_batch x KV-head groups within the thread-block clusters the
@@ -371,7 +372,8 @@ typedef struct pkv_prefill_plan pkv_prefill_plan; /* opaque, library-owned */
  *   max_q_tokens : largest qo_indptr[batch] of any step (>= 0)
  *   n_qo_heads, n_kv_heads, head_dim : head_dim 128 or 256; group size
  *                  n_qo_heads / n_kv_heads in {1, 2, 4, 8}
- * Uses the current device. Synchronous. PKV_ERR_UNSUPPORTED for other shapes.
+ * Uses the current device, which must be current for every call that takes the plan
+ * (PKV_ERR_INVALID_ARG otherwise). Synchronous. PKV_ERR_UNSUPPORTED for other shapes.
  */
 int paged_prefill_plan_create(pkv_prefill_plan** plan, int max_batch, int64_t max_q_tokens,
                               int n_qo_heads, int n_kv_heads, int head_dim);

@@ -54,6 +54,18 @@ bool take_injected_stall() {
     return stalls > 0;
 }
 
+// A plan's buffers live on the device it was created on: calls that use it must run
+// with that device current, or its kernels would address another GPU's memory.
+int check_plan_device(const char* who, int plan_device) {
+    int dev = -1;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "%s: cudaGetDevice: %s", who, cudaGetErrorString(e));
+    if (dev != plan_device)
+        return fail(PKV_ERR_INVALID_ARG, "%s: the plan belongs to device %d but device %d is current",
+                    who, plan_device, dev);
+    return PKV_OK;
+}
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char* env = std::getenv("PKV_PDL");
@@ -420,6 +432,7 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
               pkv_stream_t stream) {
     if (!p) return fail(PKV_ERR_PLAN, "%s: plan is NULL", who);
     p->planned = false;
+    if (int rc = check_plan_device(who, p->device); rc != PKV_OK) return rc;
     if (batch < 0 || batch > p->max_batch)
         return fail(PKV_ERR_PLAN, "%s: batch %d outside [0, %d]", who, batch, p->max_batch);
     if (!kv_indptr_host) return fail(PKV_ERR_INVALID_ARG, "%s: kv_indptr_host is NULL", who);
@@ -597,6 +610,7 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
               const void* v_host = nullptr, int64_t host_slots = 0) {
     if (!p) return fail(PKV_ERR_PLAN, "%s: plan is NULL", who);
     if (!p->planned) return fail(PKV_ERR_PLAN, "%s: paged_decode_plan was not run", who);
+    if (int rc = check_plan_device(who, p->device); rc != PKV_OK) return rc;
     if (n_qo_heads != p->n_qo_heads || n_kv_heads != p->n_kv_heads || head_dim != p->head_dim)
         return fail(PKV_ERR_PLAN, "%s: shape (%d, %d, %d) differs from the plan's (%d, %d, %d)", who,
                     n_qo_heads, n_kv_heads, head_dim, p->n_qo_heads, p->n_kv_heads, p->head_dim);

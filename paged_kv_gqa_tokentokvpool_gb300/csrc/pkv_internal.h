@@ -30,6 +30,8 @@ struct TraceRange {
 // predecessor on the stream is still running, and does only plan reads and
 // barrier set-up before its griddepcontrol.wait.
 bool pdl_enabled();
+// PKV_OK when the current device is plan_device, else PKV_ERR_INVALID_ARG (message set).
+int check_plan_device(const char* who, int plan_device);
 
 // ---- errors -------------------------------------------------------------
 int fail(int code, const char* fmt, ...);  // records the message, returns code

@@ -954,6 +954,7 @@ int paged_prefill_plan(pkv_prefill_plan* p, const int32_t* qo_indptr_host,
     const char* who = "paged_prefill_plan";
     if (!p) return fail(PKV_ERR_PLAN, "%s: plan is NULL", who);
     p->planned = false;
+    if (int rc = check_plan_device(who, p->device); rc != PKV_OK) return rc;
     if (batch < 0 || batch > p->max_batch)
         return fail(PKV_ERR_PLAN, "%s: batch %d outside [0, %d]", who, batch, p->max_batch);
     if (!qo_indptr_host || !kv_indptr_host)
@@ -1036,6 +1037,7 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
     clear_error();
     const char* who = "paged_prefill_attn";
     if (!p || !p->planned) return fail(PKV_ERR_PLAN, "%s: plan is NULL or not planned", who);
+    if (int rc = check_plan_device(who, p->device); rc != PKV_OK) return rc;
     if (batch != p->batch)
         return fail(PKV_ERR_PLAN, "%s: batch %d differs from the plan's %d", who, batch, p->batch);
     if (n_qo_heads != p->n_qo_heads || n_kv_heads != p->n_kv_heads || head_dim != p->head_dim)
