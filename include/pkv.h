@@ -500,10 +500,12 @@ int paged_decode_plan_mode(const pkv_plan* plan, int* single_launch);
 int paged_decode_plan_status(pkv_plan* plan, int* status);
 
 /*
- * pkv_set_debug_checks — when on (nonzero), kvpool_append and paged_decode_attn
- * also copy slot ids / indptr / indices to the host and check them (range, and
- * agreement with the plan) before launching; this synchronises the stream.
- * Off by default. Process-wide.
+ * pkv_set_debug_checks — when on (nonzero), kvpool_append, the decode attention
+ * calls and paged_prefill_attn also check, before launching, that each device array
+ * is device (or managed) memory of the right device (PKV_ERR_INVALID_ARG naming the
+ * array; a host pointer would fault the kernel instead), and copy slot ids / indptr /
+ * indices to the host and check them (range, and agreement with the plan,
+ * PKV_ERR_INDEX); this synchronises the stream. Off by default. Process-wide.
  */
 void pkv_set_debug_checks(int on);
 

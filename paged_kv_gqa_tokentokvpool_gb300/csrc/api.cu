@@ -66,6 +66,24 @@ int check_plan_device(const char* who, int plan_device) {
     return PKV_OK;
 }
 
+int check_on_device(const char* who, int device, std::initializer_list<NamedPtr> arrays) {
+    for (const NamedPtr& a : arrays) {
+        if (a.ptr == nullptr) continue;
+        cudaPointerAttributes attr{};
+        const cudaError_t e = cudaPointerGetAttributes(&attr, a.ptr);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(PKV_ERR_INVALID_ARG, "%s: %s is not memory CUDA knows (%s)", who, a.name,
+                        cudaGetErrorString(e));
+        }
+        if (attr.type == cudaMemoryTypeManaged) continue;
+        if (attr.type != cudaMemoryTypeDevice || attr.device != device)
+            return fail(PKV_ERR_INVALID_ARG, "%s: %s is not device memory of device %d", who, a.name,
+                        device);
+    }
+    return PKV_OK;
+}
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char* env = std::getenv("PKV_PDL");
@@ -107,6 +125,13 @@ int kvpool_append(void* k_pool, void* v_pool, const int32_t* slot_ids, const voi
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new))
         return fail(PKV_ERR_INVALID_ARG, "kvpool_append: pools and new rows must be 16-byte aligned");
     if (debug_checks()) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (int rc = check_on_device("kvpool_append", dev,
+                                     {{"k_pool", k_pool}, {"v_pool", v_pool}, {"slot_ids", slot_ids},
+                                      {"k_new", k_new}, {"v_new", v_new}});
+            rc != PKV_OK)
+            return rc;
         std::vector<int32_t> ids(n);
         cudaError_t e = cudaMemcpyAsync(ids.data(), slot_ids, n * sizeof(int32_t),
                                         cudaMemcpyDeviceToHost, stream);
@@ -649,6 +674,13 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
                             "%s: request %d has an empty context, so it has no newest token", who, b);
     }
     if (debug_checks()) {
+        if (int rc = check_on_device(who, p->device,
+                                     {{"q", q}, {"k_pool", k_pool}, {"v_pool", v_pool},
+                                      {"kv_indptr", kv_indptr}, {"kv_indices", kv_indices},
+                                      {"out", out}, {"lse", lse}, {"slot_ids", slot_ids},
+                                      {"k_new", k_new}, {"v_new", v_new}});
+            rc != PKV_OK)
+            return rc;
         std::vector<int32_t> ip(batch + 1);
         cudaError_t e = cudaMemcpyAsync(ip.data(), kv_indptr, ip.size() * sizeof(int32_t),
                                         cudaMemcpyDeviceToHost, stream);

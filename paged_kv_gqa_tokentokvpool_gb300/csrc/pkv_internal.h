@@ -5,6 +5,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
+#include <initializer_list>
 #include <vector>
 
 #include "pkv.h"
@@ -32,6 +33,14 @@ struct TraceRange {
 bool pdl_enabled();
 // PKV_OK when the current device is plan_device, else PKV_ERR_INVALID_ARG (message set).
 int check_plan_device(const char* who, int plan_device);
+// Debug checks: every named array (NULL ones skipped) is device or managed memory of
+// `device`, else PKV_ERR_INVALID_ARG naming it (a host or foreign pointer would fault
+// the kernel instead).
+struct NamedPtr {
+    const char* name;
+    const void* ptr;
+};
+int check_on_device(const char* who, int device, std::initializer_list<NamedPtr> arrays);
 
 // ---- errors -------------------------------------------------------------
 int fail(int code, const char* fmt, ...);  // records the message, returns code

@@ -1052,6 +1052,12 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
         return fail(PKV_ERR_INVALID_ARG, "%s: lse must be 4-byte aligned", who);
     if (debug_checks()) {
+        if (int rc = check_on_device(who, p->device,
+                                     {{"q", q}, {"k_pool", k_pool}, {"v_pool", v_pool},
+                                      {"qo_indptr", qo_indptr}, {"kv_indptr", kv_indptr},
+                                      {"kv_indices", kv_indices}, {"out", out}, {"lse", lse}});
+            rc != PKV_OK)
+            return rc;
         std::vector<int32_t> qo(batch + 1), kv(batch + 1);
         cudaError_t e = cudaMemcpyAsync(qo.data(), qo_indptr, qo.size() * 4, cudaMemcpyDeviceToHost, stream);
         if (e == cudaSuccess)

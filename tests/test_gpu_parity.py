@@ -237,6 +237,31 @@ def test_errors_do_not_launch(pkv):
             pkv.kvpool_append(pool, pool, torch.tensor([3, 3], dtype=torch.int32, device=dev),
                               pool[:2], pool[:2])
         assert e.value.code == pkv.PKV_ERR_INDEX
+        # a host array where device memory belongs (it would fault the kernel); the
+        # binding refuses CPU tensors itself, so these go through the C ABI directly
+        import ctypes
+        lib = pkv.library()
+        vp = lambda t: ctypes.c_void_p(t.data_ptr())
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        q_host = torch.zeros(2, 32, 128, dtype=torch.bfloat16)
+        rc = lib.paged_decode_attn(vp(q_host), vp(pool), vp(pool), vp(ip), vp(idx), 2, 32, 8, 128,
+                                   ctypes.c_float(0.1), vp(out), None, plan.handle, stream)
+        assert rc == pkv.PKV_ERR_INVALID_ARG and "q is not device memory" in pkv.pkv_last_error()
+        pool_host = pool.cpu()
+        rc = lib.kvpool_append(vp(pool_host), vp(pool), vp(idx), vp(pool), vp(pool), 1, 8, 128, 64,
+                               stream)
+        assert rc == pkv.PKV_ERR_INVALID_ARG and "k_pool" in pkv.pkv_last_error()
+        pw = workloads.prefill_workload([5], [9], seed=3)
+        pplan = pkv.paged_prefill_plan_create(1, 5, 32, 8, 128)
+        pkv.paged_prefill_plan(pplan, pw.qo_indptr, pw.kv_indptr)
+        pout = torch.zeros(5, 32, 128, dtype=torch.bfloat16, device=dev)
+        qo_d = torch.from_numpy(pw.qo_indptr).to(dev)
+        kv_d = torch.from_numpy(pw.kv_indptr).to(dev)
+        rc = lib.paged_prefill_attn(vp(torch.zeros(5, 32, 128, dtype=torch.bfloat16)), vp(pool),
+                                    vp(pool), vp(qo_d), vp(kv_d), vp(idx), 1, 32, 8, 128,
+                                    ctypes.c_float(0.1), vp(pout), None, pplan.handle, stream)
+        assert rc == pkv.PKV_ERR_INVALID_ARG and "q is not device memory" in pkv.pkv_last_error()
+        assert torch.all(pout == 0)
     finally:
         pkv.pkv_set_debug_checks(False)
     torch.cuda.synchronize()
