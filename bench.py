@@ -599,6 +599,87 @@ def measure_prefill(pf_no: int, steps: int, warmup: int, layers=None, cpu_budget
     return line
 
 
+def run_curve(args):
+    """Decode attention over a grid of batch sizes and context lengths (the Qwen3-4B
+    attention shape, scattered slots, two layers per step, fused append, graph replay):
+    where the path reaches the HBM roofline. One JSON line with every point."""
+    import paged_kv_gqa_tokentokvpool_gb300 as pkv
+    torch.cuda.set_device(0)
+    peak, peak_kind = measured_hbm_peak()
+    points = []
+    for ctx in (512, 4096, 32768):
+        for batch in (1, 4, 8, 16, 32, 64, 128):
+            wl = workloads.scattered_workload([ctx] * batch, layers=2, seed=3000 + batch,
+                                              name="curve", description="")
+            st = StepState(wl)
+            st.capture()
+            nbytes = step_bytes(wl)
+            stream = torch.cuda.current_stream()
+            for _ in range(args.warmup):
+                st.run()
+            torch.cuda.synchronize()
+            # steps that fit in L2 twice are timed one by one after an L2 flush
+            flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=stream.device)
+                     if nbytes["step"] < 2 * L2_BYTES else None)
+            total_ms = 0.0
+            with ClockSampler(0) as clocks:
+                for _ in range(args.steps):
+                    if flush is not None:
+                        flush.fill_(1)
+                    t0 = torch.cuda.Event(enable_timing=True)
+                    t1 = torch.cuda.Event(enable_timing=True)
+                    t0.record(stream)
+                    st.run()
+                    t1.record(stream)
+                    t1.synchronize()
+                    total_ms += t0.elapsed_time(t1)
+            if st.plan.status() != 0:
+                raise RuntimeError("a decode pipeline wait exceeded its bound")
+            us_layer = total_ms / args.steps / wl.layers * 1e3
+            gbs = nbytes["step"] / wl.layers / (us_layer * 1e-6) / 1e9
+            point = {"batch": batch, "context": ctx, "us_per_layer": us_layer, "gbs": gbs,
+                     "frac_of_measured": gbs / peak, "single_launch": st.plan.single_launch(),
+                     "l2_flushed": flush is not None, "clocks": clocks.summary()}
+            # the other mode where the plan can run it (PKV_PLAN_SINGLE_LAUNCH /
+            # PKV_PLAN_PERSISTENT), timed the same way
+            other = pkv.PKV_PLAN_PERSISTENT if point["single_launch"] else pkv.PKV_PLAN_SINGLE_LAUNCH
+            try:
+                st.plan.set_flags((pkv.PKV_PLAN_EARLY_GATHER if st.early else 0) | other)
+            except pkv.PkvError:
+                other = None
+            if other is not None:
+                st.graph = None  # the next step plans in the other mode: capture it anew
+                st.capture()
+                for _ in range(args.warmup):
+                    st.run()
+                total_ms = 0.0
+                for _ in range(args.steps):
+                    if flush is not None:
+                        flush.fill_(1)
+                    t0 = torch.cuda.Event(enable_timing=True)
+                    t1 = torch.cuda.Event(enable_timing=True)
+                    t0.record(stream)
+                    st.run()
+                    t1.record(stream)
+                    t1.synchronize()
+                    total_ms += t0.elapsed_time(t1)
+                if st.plan.status() != 0:
+                    raise RuntimeError("a decode pipeline wait exceeded its bound")
+                point["us_per_layer_other_mode"] = total_ms / args.steps / wl.layers * 1e3
+            points.append(point)
+            del st, flush
+            torch.cuda.empty_cache()
+    line = {"metric": "paged GQA decode attention, batch x context curve (us per layer, GB/s)",
+            "unit": "GB/s", "data": "synthetic", "dtype": "bf16", "steps": args.steps,
+            "warmup": args.warmup, "peak_gbs": peak, "peak_kind": peak_kind,
+            "config": {"workload": "Qwen3-4B attention shape (32Q/8KV, head_dim 128), scattered "
+                                   "slots, 2 layers per step, fused append, CUDA graph of the "
+                                   "layers, plan per step"},
+            "points": points}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_prefill_bench(args):
     line = measure_prefill(args.prefill, args.steps, args.warmup, args.layers,
                            None if args.no_cpu_baseline else args.cpu_budget)
@@ -909,6 +990,9 @@ def main(argv=None):
                          "workloads and record them under config.sweep (default on one GPU "
                          "for the default workload)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--curve", action="store_true",
+                    help="time decode attention over a grid of batch sizes and context lengths "
+                         "instead of the step (one JSON line of points)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
@@ -917,6 +1001,8 @@ def main(argv=None):
         return run_reference(args, world, rank)
     if args.tier_bench:
         return run_tier_bench(args)
+    if args.curve:
+        return run_curve(args)
     if args.prefill is not None:
         return run_prefill_bench(args)
 

@@ -457,6 +457,7 @@ int paged_decode_plan_host_times(pkv_plan* plan, double* compute_us, double* wai
 /* Flags for paged_decode_plan_set_flags. */
 #define PKV_PLAN_EARLY_GATHER 1u
 #define PKV_PLAN_PERSISTENT 2u
+#define PKV_PLAN_SINGLE_LAUNCH 4u
 
 /*
  * paged_decode_plan_set_flags — options for the attention calls that use `plan`
@@ -478,8 +479,18 @@ int paged_decode_plan_host_times(pkv_plan* plan, double* compute_us, double* wai
  *   PKV_PLAN_PERSISTENT: a small plan's steps run on the persistent grid with an
  *     uploaded work list instead of in single-launch mode (paged_decode_plan_create);
  *     takes effect from the next paged_decode_plan call.
+ *   PKV_PLAN_SINGLE_LAUNCH: every step runs in single-launch mode (as a small plan's
+ *     do) whatever max_tokens, for callers whose requests are short: the mode splits
+ *     each request 16 ways on its own cluster, so a step of a few requests of up to a
+ *     few thousand tokens takes one launch with no upload, while a step with one long
+ *     context streams it on only 8 SMs and is slower than on the persistent grid.
+ *     Results are the same either way. Returns PKV_ERR_UNSUPPORTED when max_batch x
+ *     KV-head groups exceed the clusters the device holds at once, and
+ *     PKV_ERR_INVALID_ARG together with PKV_PLAN_PERSISTENT. Takes effect from the
+ *     next paged_decode_plan call; graphs then follow the single-launch rule above.
  *   flags : a bitwise OR of PKV_PLAN_* values (0 = none)
- * Returns PKV_ERR_PLAN for a NULL plan and PKV_ERR_INVALID_ARG for unknown bits.
+ * Returns PKV_ERR_PLAN for a NULL plan and PKV_ERR_INVALID_ARG for unknown bits (the
+ * plan's flags are then unchanged).
  * Takes effect for attention calls enqueued after it returns.
  */
 int paged_decode_plan_set_flags(pkv_plan* plan, unsigned flags);

@@ -35,6 +35,7 @@ PKV_ERR_CUDA = -4
 PKV_ERR_INDEX = -5
 PKV_PLAN_EARLY_GATHER = 1
 PKV_PLAN_PERSISTENT = 2
+PKV_PLAN_SINGLE_LAUNCH = 4
 
 EXPORTED = ("kvpool_append", "paged_decode_plan_create", "paged_decode_plan",
             "paged_decode_attn", "paged_decode_plan_destroy", "paged_decode_plan_host",

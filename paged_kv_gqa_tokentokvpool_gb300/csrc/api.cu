@@ -84,6 +84,13 @@ int check_on_device(const char* who, int device, std::initializer_list<NamedPtr>
     return PKV_OK;
 }
 
+// The plan's steps run as single launches of the cluster kernel: small plans unless
+// PKV_PLAN_PERSISTENT, and any plan whose clusters fit with PKV_PLAN_SINGLE_LAUNCH.
+bool single_launch_mode(const pkv_plan* p) {
+    if (p->flags & PKV_PLAN_PERSISTENT) return false;
+    return p->small || ((p->flags & PKV_PLAN_SINGLE_LAUNCH) && p->small_fits);
+}
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char* env = std::getenv("PKV_PDL");
@@ -399,8 +406,8 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     {
         const int64_t items = int64_t(max_batch) * (n_kv_heads / hpg);
         const int64_t max_share = int64_t(kSmallCluster) * kSmallMaxStages * decode_stage_tokens(hpg, head_dim);
-        p->small = max_tokens <= max_share &&
-                   items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim);
+        p->small_fits = items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim);
+        p->small = max_tokens <= max_share && p->small_fits;
     }
     p->ctas_max = std::max(p->ctas, p->ctas_shared);
     p->max_batch = max_batch;
@@ -472,7 +479,7 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
     int rc = check_sharing(who, kv_indptr_host, batch, shared_indptr_host, n_shared,
                            shared_len_host);
     if (rc != PKV_OK) return rc;
-    const bool small = p->small && !(p->flags & PKV_PLAN_PERSISTENT);
+    const bool small = single_launch_mode(p);
     bool share = false;
     if (p->share_rows > 0 && !small)
         for (int s = 0; s < n_shared; ++s)
@@ -596,10 +603,19 @@ int paged_decode_plan_host_times(pkv_plan* p, double* compute_us, double* wait_u
 int paged_decode_plan_set_flags(pkv_plan* p, unsigned flags) {
     clear_error();
     if (!p) return fail(PKV_ERR_PLAN, "paged_decode_plan_set_flags: plan is NULL");
-    constexpr unsigned kKnown = PKV_PLAN_EARLY_GATHER | PKV_PLAN_PERSISTENT;
+    constexpr unsigned kKnown = PKV_PLAN_EARLY_GATHER | PKV_PLAN_PERSISTENT | PKV_PLAN_SINGLE_LAUNCH;
     if (flags & ~kKnown)
         return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_set_flags: unknown flags 0x%x",
                     flags & ~kKnown);
+    if ((flags & PKV_PLAN_PERSISTENT) && (flags & PKV_PLAN_SINGLE_LAUNCH))
+        return fail(PKV_ERR_INVALID_ARG,
+                    "paged_decode_plan_set_flags: PKV_PLAN_PERSISTENT and PKV_PLAN_SINGLE_LAUNCH "
+                    "exclude each other");
+    if ((flags & PKV_PLAN_SINGLE_LAUNCH) && !p->small_fits)
+        return fail(PKV_ERR_UNSUPPORTED,
+                    "paged_decode_plan_set_flags: max_batch x KV-head groups (%d) exceed the "
+                    "thread-block clusters the device holds at once",
+                    p->max_batch * p->n_groups);
     p->flags = flags;
     return PKV_OK;
 }
@@ -607,7 +623,7 @@ int paged_decode_plan_set_flags(pkv_plan* p, unsigned flags) {
 int paged_decode_plan_mode(const pkv_plan* p, int* single_launch) {
     clear_error();
     if (!p || !single_launch) return fail(PKV_ERR_INVALID_ARG, "paged_decode_plan_mode: NULL argument");
-    *single_launch = p->small && !(p->flags & PKV_PLAN_PERSISTENT) ? 1 : 0;
+    *single_launch = single_launch_mode(p) ? 1 : 0;
     return PKV_OK;
 }
 

@@ -31,6 +31,8 @@ struct TraceRange {
 // predecessor on the stream is still running, and does only plan reads and
 // barrier set-up before its griddepcontrol.wait.
 bool pdl_enabled();
+// Whether the plan's steps run in single-launch mode (see paged_decode_plan_set_flags).
+bool single_launch_mode(const pkv_plan* p);
 // PKV_OK when the current device is plan_device, else PKV_ERR_INVALID_ARG (message set).
 int check_plan_device(const char* who, int plan_device);
 // Debug checks: every named array (NULL ones skipped) is device or managed memory of
@@ -235,6 +237,9 @@ struct pkv_plan {
     // Small-step mode (fixed at creation): every step runs as one launch of the
     // cluster kernel, which reads kv_indptr on the device; nothing is uploaded.
     bool small = false;
+    // every step of the plan could run in that mode: max_batch x groups clusters fit the
+    // device at once (PKV_PLAN_SINGLE_LAUNCH selects the mode whatever max_tokens)
+    bool small_fits = false;
     bool step_small = false;  // the current step runs in that mode
     std::vector<int32_t> indptr_host;
     // the current step's sharing description (checked against kv_indices when

@@ -774,6 +774,53 @@ def test_small_step_modes(pkv, case, fused, persistent):
     assert np.array_equal(bits(kp), k_after)
 
 
+@pytest.mark.parametrize("lengths", [[1024] * 4, [9000, 5], [1, 2048, 0, 700]],
+                         ids=["four_1k", "one_long", "mixed"])
+def test_single_launch_flag(pkv, lengths):
+    """PKV_PLAN_SINGLE_LAUNCH: a plan whose max_tokens is beyond the automatic
+    single-launch limit runs its steps in that mode all the same (each request split 16
+    ways, a CTA's share of 9000 tokens is 36 stages); results equal the oracle's."""
+    wl = workloads.scattered_workload(lengths, seed=81)
+    t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
+    dev = torch.device("cuda")
+    kp, vp = t.k_pool.to(dev), t.v_pool.to(dev)
+    plan = pkv.paged_decode_plan_create(wl.batch, wl.total_tokens, 32, 8, 128)
+    assert not plan.single_launch()  # more than 2048 tokens
+    with pytest.raises(pkv.PkvError) as e:
+        plan.set_flags(pkv.PKV_PLAN_SINGLE_LAUNCH | pkv.PKV_PLAN_PERSISTENT)
+    assert e.value.code == pkv.PKV_ERR_INVALID_ARG
+    plan.set_flags(pkv.PKV_PLAN_SINGLE_LAUNCH)
+    assert plan.single_launch()
+    pkv.paged_decode_plan(plan, wl.kv_indptr)
+    out = torch.full((wl.batch, 32, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((wl.batch, 32), float("nan"), dtype=torch.float32, device=dev)
+    ip = torch.from_numpy(wl.kv_indptr).to(dev)
+    idx = torch.from_numpy(wl.kv_indices).to(dev)
+    slots = torch.from_numpy(wl.append_slots).to(dev)
+    if all(L > 0 for L in lengths):
+        pkv.paged_decode_append_attn(t.q.to(dev), kp, vp, ip, idx, slots, t.k_new.to(dev),
+                                     t.v_new.to(dev), wl.batch, 32, 8, 128, wl.sm_scale, out, lse,
+                                     plan)
+    else:
+        pkv.kvpool_append(kp, vp, slots, t.k_new.to(dev), t.v_new.to(dev))
+        pkv.paged_decode_attn(t.q.to(dev), kp, vp, ip, idx, wl.batch, 32, 8, 128, wl.sm_scale,
+                              out, lse, plan)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    ref_out, ref_lse = oracle_reference(wl, t)
+    assert_parity(to_f64(out), lse.cpu().numpy(), ref_out, ref_lse, what=f"single launch {lengths}")
+
+
+def test_single_launch_flag_needs_the_clusters(pkv):
+    """A plan whose max_batch x KV-head groups exceed the resident clusters refuses the
+    flag and keeps its mode."""
+    plan = pkv.paged_decode_plan_create(128, 1 << 16, 32, 8, 128)
+    with pytest.raises(pkv.PkvError) as e:
+        plan.set_flags(pkv.PKV_PLAN_SINGLE_LAUNCH)
+    assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
+    assert not plan.single_launch()
+
+
 def test_single_launch_graph_steps(pkv):
     """Small-step mode under CUDA-graph replay: three layers captured once, replayed
     for several steps, each step re-planned on the host (nothing uploaded); every

@@ -106,7 +106,8 @@ def test_header_constants_match_the_binding(pkv):
     text = open(os.path.join(ROOT, "include", "pkv.h")).read()
     flags = dict(re.findall(r"#define\s+(PKV_PLAN_\w+)\s+(\d+)u", text))
     assert flags == {"PKV_PLAN_EARLY_GATHER": str(pkv.PKV_PLAN_EARLY_GATHER),
-                     "PKV_PLAN_PERSISTENT": str(pkv.PKV_PLAN_PERSISTENT)}
+                     "PKV_PLAN_PERSISTENT": str(pkv.PKV_PLAN_PERSISTENT),
+                     "PKV_PLAN_SINGLE_LAUNCH": str(pkv.PKV_PLAN_SINGLE_LAUNCH)}
     codes = dict(re.findall(r"(PKV_(?:OK|ERR_\w+))\s*=\s*(-?\d+)", text))
     assert codes and all(getattr(pkv, k) == int(v) for k, v in codes.items())
 
