@@ -601,7 +601,7 @@ def measure_prefill(pf_no: int, steps: int, warmup: int, layers=None, cpu_budget
 
 def run_curve(args):
     """Decode attention over a grid of batch sizes and context lengths (the Qwen3-4B
-    attention shape, scattered slots, two layers per step, fused append, graph replay):
+    attention shape, scattered slots, 2-8 layers per step, fused append, graph replay):
     where the path reaches the HBM roofline. One JSON line with every point."""
     import paged_kv_gqa_tokentokvpool_gb300 as pkv
     torch.cuda.set_device(0)
@@ -609,8 +609,13 @@ def run_curve(args):
     points = []
     for ctx in (512, 4096, 32768):
         for batch in (1, 4, 8, 16, 32, 64, 128):
-            wl = workloads.scattered_workload([ctx] * batch, layers=2, seed=3000 + batch,
-                                              name="curve", description="")
+            # pools a little larger than the listed slots, and as many layers (2-8) as
+            # fit in about 48 GB, so the per-step plan and graph launch weigh little
+            pool_slots = batch * ctx + batch * ctx // 20 + 1024
+            layer_bytes = pool_slots * 8 * 128 * 2 * 2
+            layers = int(max(2, min(8, 48e9 // layer_bytes)))
+            wl = workloads.scattered_workload([ctx] * batch, layers=layers, pool_slots=pool_slots,
+                                              seed=3000 + batch, name="curve", description="")
             st = StepState(wl)
             st.capture()
             nbytes = step_bytes(wl)
@@ -618,26 +623,40 @@ def run_curve(args):
             for _ in range(args.warmup):
                 st.run()
             torch.cuda.synchronize()
-            # steps that fit in L2 twice are timed one by one after an L2 flush
+            # steps that fit in L2 twice are timed one by one after an L2 flush; larger
+            # ones back to back between two events
             flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=stream.device)
                      if nbytes["step"] < 2 * L2_BYTES else None)
-            total_ms = 0.0
-            with ClockSampler(0) as clocks:
+
+            def time_steps():
+                if flush is None:
+                    t0 = torch.cuda.Event(enable_timing=True)
+                    t1 = torch.cuda.Event(enable_timing=True)
+                    t0.record(stream)
+                    for _ in range(args.steps):
+                        st.run()
+                    t1.record(stream)
+                    t1.synchronize()
+                    return t0.elapsed_time(t1)
+                total = 0.0
                 for _ in range(args.steps):
-                    if flush is not None:
-                        flush.fill_(1)
+                    flush.fill_(1)
                     t0 = torch.cuda.Event(enable_timing=True)
                     t1 = torch.cuda.Event(enable_timing=True)
                     t0.record(stream)
                     st.run()
                     t1.record(stream)
                     t1.synchronize()
-                    total_ms += t0.elapsed_time(t1)
+                    total += t0.elapsed_time(t1)
+                return total
+
+            with ClockSampler(0) as clocks:
+                total_ms = time_steps()
             if st.plan.status() != 0:
                 raise RuntimeError("a decode pipeline wait exceeded its bound")
             us_layer = total_ms / args.steps / wl.layers * 1e3
             gbs = nbytes["step"] / wl.layers / (us_layer * 1e-6) / 1e9
-            point = {"batch": batch, "context": ctx, "us_per_layer": us_layer, "gbs": gbs,
+            point = {"batch": batch, "context": ctx, "layers": layers, "us_per_layer": us_layer, "gbs": gbs,
                      "frac_of_measured": gbs / peak, "single_launch": st.plan.single_launch(),
                      "l2_flushed": flush is not None, "clocks": clocks.summary()}
             # the other mode where the plan can run it (PKV_PLAN_SINGLE_LAUNCH /
@@ -652,17 +671,7 @@ def run_curve(args):
                 st.capture()
                 for _ in range(args.warmup):
                     st.run()
-                total_ms = 0.0
-                for _ in range(args.steps):
-                    if flush is not None:
-                        flush.fill_(1)
-                    t0 = torch.cuda.Event(enable_timing=True)
-                    t1 = torch.cuda.Event(enable_timing=True)
-                    t0.record(stream)
-                    st.run()
-                    t1.record(stream)
-                    t1.synchronize()
-                    total_ms += t0.elapsed_time(t1)
+                total_ms = time_steps()
                 if st.plan.status() != 0:
                     raise RuntimeError("a decode pipeline wait exceeded its bound")
                 point["us_per_layer_other_mode"] = total_ms / args.steps / wl.layers * 1e3
@@ -673,8 +682,8 @@ def run_curve(args):
             "unit": "GB/s", "data": "synthetic", "dtype": "bf16", "steps": args.steps,
             "warmup": args.warmup, "peak_gbs": peak, "peak_kind": peak_kind,
             "config": {"workload": "Qwen3-4B attention shape (32Q/8KV, head_dim 128), scattered "
-                                   "slots, 2 layers per step, fused append, CUDA graph of the "
-                                   "layers, plan per step"},
+                                   "slots, 2-8 layers per step (as fit in about 48 GB), fused "
+                                   "append, CUDA graph of the layers, plan per step"},
             "points": points}
     print(json.dumps(line), flush=True)
     return 0
