@@ -25,7 +25,10 @@
 //    layout (K-major for q and K; V's rows are the same bytes read as an MN-major
 //    operand). A thread's arrival on a stage's barrier rides on its copies, and a
 //    relay thread fences the landed stage (generic to async proxy) for the tensor
-//    core.
+//    core. At head_dim 256 two more warps copy the first 20 tokens of every K and V
+//    tile with 4-row TMA gathers (cp.async.bulk.tensor .tile::gather4) through tensor
+//    maps of the pools in that 128-byte swizzled layout, their bytes counted on the
+//    same barrier: the SMs then take in the tiles by both paths at once.
 //  * An MMA warp issues, from one lane, S = Q K^T (128 x kKv, K = head_dim, operands
 //    in shared memory) into one of two TMEM buffers, and O += P V (128 x head_dim,
 //    K = kKv) with P read from TMEM as the A operand, each signalled on an mbarrier
@@ -41,6 +44,7 @@
 //    flight are drained (again bounded) and the tensor memory is freed. Barriers a
 //    reader could fall two phases behind on are split per buffer, so that no parity
 //    test can alias.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -66,7 +70,7 @@ constexpr int kPfProducerThreads = 32 * kPfProducerWarps;
 constexpr int kPfHalfThreads = kPfProducerThreads / 2;  // K rows by one half, V rows by the other
 constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfProducerWarps;  // also owns the TMEM allocation
 constexpr int kPfRelayWarp = kPfMmaWarp + 1;
-constexpr int kPfThreads = 32 * (kPfRelayWarp + 1);
+constexpr int kPfTmaWarp = kPfRelayWarp + 1;  // head_dim 256: two more warps (K rows, V rows)
 constexpr uint32_t kPfTmemCols = 512;
 constexpr int kPfOCol = 256;                // TMEM columns of O: 256 .. 256 + head_dim
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -94,7 +98,15 @@ struct PfMerge {
 };
 static_assert(sizeof(PfMerge) == 32, "merge record");
 
+// Tensor maps of one head_dim-256 call (cuTensorMapEncodeTiled): each pool as a 2D
+// array [slots, n_kv_heads x head_dim] with 64 x 1 element boxes and the 128-byte
+// swizzle, for 4-row gathers.
+struct PfMaps {
+    CUtensorMap k, v;
+};
+
 struct PfArgs {
+    PfMaps maps;  // head_dim 256 only
     const void* q;
     const void* k_pool;
     const void* v_pool;
@@ -144,11 +156,17 @@ struct PfCfg {
     static constexpr int kAbortOff = kTmemOff + 4;
     static constexpr int kSmem = kAbortOff + 4 + 1024;      // + slack to align the base
     static constexpr int kChunks = D / 8;                   // 16-byte pieces per row
-    static constexpr int kTilePieces = kKv * kChunks / kPfHalfThreads;   // per thread, K or V
+    // At head_dim 256 two more warps copy the first kTmaTok tokens of every K and V
+    // tile by the tensor memory accelerator's gather form, the producer threads the
+    // rest; measured best at 20 of 64 (no share helped at head_dim 128).
+    static constexpr int kTmaTok = D == 256 ? 20 : 0;
+    static constexpr int kThreads = 32 * (kPfRelayWarp + 1 + (kTmaTok > 0 ? 2 : 0));
+    static constexpr int kTilePieces = (kKv - kTmaTok) * kChunks / kPfHalfThreads;  // per thread, K or V
     static constexpr int kQPieces = kPfRows * kChunks / kPfHalfThreads;   // q, by the K half
     static constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kPfRows, kKv, false, false);
     static constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kPfRows, D, false, true);
-    static_assert(kTilePieces * kPfHalfThreads == kKv * kChunks, "ring pieces");
+    static_assert(kTilePieces * kPfHalfThreads == (kKv - kTmaTok) * kChunks, "ring pieces");
+    static_assert(kTmaTok % 4 == 0 && kTmaTok / 4 <= 32, "4-row gathers, one lane each");
     static_assert(kPfKvTile % kKv == 0, "split cuts fall on ring tiles");
     static_assert(kQPieces * kPfHalfThreads == kPfRows * kChunks, "q pieces");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
@@ -213,7 +231,7 @@ __device__ __forceinline__ void load_tile_slots(const PfArgs& a, const PfUnit& u
     using C = PfCfg<D, G>;
 #pragma unroll
     for (int i = 0; i < C::kTilePieces; ++i) {
-        const int tok = (pt + i * kPfHalfThreads) / C::kChunks;
+        const int tok = C::kTmaTok + (pt + i * kPfHalfThreads) / C::kChunks;
         const int j = tile * C::kKv + tok;
         slot[i] = j < un.kv_hi ? __ldg(a.kv_indices + un.kv_begin + j) : -1;
     }
@@ -229,15 +247,28 @@ __device__ __forceinline__ void issue_tile(const PfArgs& a, const PfUnit& un, co
 #pragma unroll
     for (int i = 0; i < C::kTilePieces; ++i) {
         const int c = pt + i * kPfHalfThreads;
-        const int tok = c / C::kChunks, part = c % C::kChunks;
+        const int tok = C::kTmaTok + c / C::kChunks, part = c % C::kChunks;
         const bool valid = slot[i] >= 0;
         const int64_t off = (int64_t(valid ? slot[i] : 0) * a.n_kv_heads + un.g) * D + part * 8;
         cp_async16(dst + sw128_off(tok, part, C::kKv), pool + off, valid);
     }
 }
 
+// Four rows of a 2D tensor map (row indices r0..r3, columns col .. col + 63) into 512
+// consecutive bytes of shared memory at dst, completing their bytes on mbarrier bar
+// (PTX ISA: cp.async.bulk.tensor, .tile::gather4). col * 2 bytes is a multiple of 16.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfArgs a) {
+__global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
+    paged_prefill_kernel(const __grid_constant__ PfArgs a) {
     using C = PfCfg<D, G>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the swizzled operands need 1024-byte aligned atoms
@@ -265,7 +296,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
     if (tid == 0) {
         for (int v = 0; v < 2; ++v)
             for (int s = 0; s < C::kStages; ++s) {
-                mbar_init(landed(v, s), kPfHalfThreads);
+                // the producer threads' cp.async arrivals (and the TMA warp's byte count)
+                mbar_init(landed(v, s), kPfHalfThreads + (C::kTmaTok > 0 ? 1 : 0));
                 mbar_init(full(v, s), 1);
                 mbar_init(empty(v, s), 1);
             }
@@ -418,6 +450,61 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const PfAr
             }
         }
         __syncwarp();
+    } else if (warp >= kPfTmaWarp) {
+        // ================= TMA gather (head_dim 256) =================
+        // Tokens 0 .. kTmaTok - 1 of every K (warp kPfTmaWarp) or V tile: lane l copies
+        // tokens 4l .. 4l + 3, one 4-row gather per 64-element panel, counted in bytes
+        // on the stage's `landed` barrier beside the producer threads' arrivals. Rows
+        // past the range repeat the range's last slot (finite rows the softmax masks).
+        if constexpr (C::kTmaTok > 0) {
+            const int half = warp - kPfTmaWarp;  // 0: K, 1: V
+            const CUtensorMap* map = half ? &a.maps.v : &a.maps.k;
+            const uint32_t ring = base + (half ? C::kVOff : C::kKOff);
+            const int n_copy = a.withhold ? 0 : n_tiles;
+            int sl[4] = {0, 0, 0, 0};
+            const auto load_ids = [&](int t) {
+                if (lane < C::kTmaTok / 4) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        sl[j] = __ldg(a.kv_indices + un.kv_begin +
+                                      min(t * C::kKv + 4 * lane + j, un.kv_hi - 1));
+                }
+            };
+            if (n_copy > 0) load_ids(t0);
+            int issued = 0;
+            for (int n = 0; n < n_copy; ++n) {
+                const int st = n % C::kStages;
+                if (n >= C::kStages) {
+                    bool ok = true;
+                    if (lane == 0)
+                        ok = pf_wait(empty(half, st), uint32_t((n / C::kStages - 1) & 1), a.status, abort_flag);
+                    if (!__shfl_sync(kFullMask, ok, 0)) break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(landed(half, st), uint32_t(C::kTmaTok * D * 2));
+                __syncwarp();
+                if (lane < C::kTmaTok / 4) {
+                    const uint32_t dst = ring + st * C::kKvBytes + lane * 512;
+#pragma unroll
+                    for (int pn = 0; pn < C::kPanels; ++pn)
+                        tma_gather4(dst + pn * C::kKvPanel, map, un.g * D + 64 * pn, sl[0], sl[1], sl[2],
+                                    sl[3], landed(half, st));
+                }
+                ++issued;
+                if (n + 1 < n_copy) load_ids(t0 + n + 1);
+            }
+            // nothing may still write this CTA's shared memory at exit: wait (bounded)
+            // for the last fill of every stage
+            if (lane == 0) {
+                for (int k = issued - C::kStages; k < issued; ++k) {
+                    if (k < 0) continue;
+                    const uint32_t bar = landed(half, k % C::kStages), par = uint32_t((k / C::kStages) & 1);
+                    const unsigned long long t_wait = pf_global_ns();
+                    while (!mbar_try_wait(bar, par) && pf_global_ns() - t_wait < kPfWaitNs) {
+                    }
+                }
+            }
+            __syncwarp();
+        }
     } else if (warp == kPfRelayWarp) {
         // ================= relay: landed stage -> tensor core =================
         // The rows came by cp.async (generic proxy); the tensor core reads them
@@ -672,7 +759,7 @@ int prefill_occupancy() {
     if (prefill_prepare<D, G>() != cudaSuccess) return 0;
     int blocks = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_prefill_kernel<D, G>,
-                                                      kPfThreads, PfCfg<D, G>::kSmem) != cudaSuccess)
+                                                      PfCfg<D, G>::kThreads, PfCfg<D, G>::kSmem) != cudaSuccess)
         return 0;
     return blocks;
 }
@@ -698,7 +785,7 @@ cudaError_t launch_prefill(const PfArgs& a, int n_units, cudaStream_t stream) {
     cudaError_t e = prefill_prepare<D, G>();
     if (e != cudaSuccess || n_units == 0) return e;
     e = launch_pdl(reinterpret_cast<const void*>(&paged_prefill_kernel<D, G>), dim3(n_units),
-                   dim3(kPfThreads), PfCfg<D, G>::kSmem, a, stream);
+                   dim3(PfCfg<D, G>::kThreads), PfCfg<D, G>::kSmem, a, stream);
     if (e != cudaSuccess || a.n_merges == 0) return e;
     const int warps = a.n_merges * kPfRows;
     return launch_pdl(reinterpret_cast<const void*>(&prefill_merge_kernel<D, G>),
@@ -744,6 +831,40 @@ bool prefill_shape_supported(int n_qo_heads, int n_kv_heads, int head_dim) {
 
 int pf_cuda_fail(cudaError_t e, const char* what) {
     return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime (no link against the driver
+// library); NULL when the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult found{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &found) != cudaSuccess ||
+            found != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// Tensor map of a pool, [slots, cols] bf16 (every int32 slot id addressable; the
+// kernel reads only listed slots), for 4-row gathers of 64-element panels: box
+// 64 x 1, 128-byte swizzle.
+bool encode_pool(CUtensorMap* map, const void* pool, uint64_t cols) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, uint64_t(INT32_MAX)};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
+              elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct PfPlanCounts {
@@ -1083,6 +1204,11 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
     a.merges = p->dev_merges;
     a.n_merges = p->n_merges;
     a.status = p->dev_status;
+    if (head_dim == 256) {
+        const uint64_t cols = uint64_t(n_kv_heads) * uint64_t(head_dim);
+        if (!encode_pool(&a.maps.k, k_pool, cols) || !encode_pool(&a.maps.v, v_pool, cols))
+            return fail(PKV_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed for the pools", who);
+    }
     a.withhold = take_injected_stall();
     const cudaError_t e = prefill_dispatch<PfLaunchFn>(head_dim, n_qo_heads / n_kv_heads, a,
                                                        p->n_units, stream);
