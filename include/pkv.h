@@ -481,11 +481,13 @@ int paged_decode_plan_host_times(pkv_plan* plan, double* compute_us, double* wai
  *     takes effect from the next paged_decode_plan call.
  *   PKV_PLAN_SINGLE_LAUNCH: every step runs in single-launch mode (as a small plan's
  *     do) whatever max_tokens, for callers whose requests are short: the mode splits
- *     each request 16 ways on its own cluster, so a step of a few requests of up to a
- *     few thousand tokens takes one launch with no upload, while a step with one long
- *     context streams it on only 8 SMs and is slower than on the persistent grid.
- *     Results are the same either way. Returns PKV_ERR_UNSUPPORTED when max_batch x
- *     KV-head groups exceed the clusters the device holds at once, and
+ *     each request 16 ways on its own cluster (8 ways on clusters of 8 when clusters of
+ *     16 for max_batch x KV-head groups do not all fit the device at once), so a step
+ *     of a few requests of up to a few thousand tokens takes one launch with no
+ *     upload, while a step with one long context streams it on only 4-8 SMs and is
+ *     slower than on the persistent grid. Results are the same either way. Returns
+ *     PKV_ERR_UNSUPPORTED when max_batch x KV-head groups exceed even the clusters of
+ *     8 the device holds at once, and
  *     PKV_ERR_INVALID_ARG together with PKV_PLAN_PERSISTENT. Takes effect from the
  *     next paged_decode_plan call; graphs then follow the single-launch rule above.
  *   flags : a bitwise OR of PKV_PLAN_* values (0 = none)

@@ -406,8 +406,12 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     {
         const int64_t items = int64_t(max_batch) * (n_kv_heads / hpg);
         const int64_t max_share = int64_t(kSmallCluster) * kSmallMaxStages * decode_stage_tokens(hpg, head_dim);
-        p->small_fits = items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim);
-        p->small = max_tokens <= max_share && p->small_fits;
+        const bool fits16 = items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim, kSmallCluster);
+        const bool fits8 =
+            !fits16 && items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim, kSmallClusterMin);
+        p->small_fits = fits16 || fits8;
+        p->small_cs = fits16 ? kSmallCluster : fits8 ? kSmallClusterMin : 0;
+        p->small = max_tokens <= max_share && fits16;
     }
     p->ctas_max = std::max(p->ctas, p->ctas_shared);
     p->max_batch = max_batch;
@@ -493,12 +497,12 @@ int plan_impl(const char* who, pkv_plan* p, const int32_t* kv_indptr_host, int b
         int longest = 0;
         for (int b = 0; b < batch; ++b)
             longest = std::max(longest, kv_indptr_host[b + 1] - kv_indptr_host[b]);
-        p->counts = PlanCounts{items * kSmallCluster, items * kSmallCluster, items,
-                               items * kSmallCluster,
-                               ((longest + kSmallCluster - 1) / kSmallCluster + st - 1) / st * st};
+        const int cs = p->small_cs;
+        p->counts = PlanCounts{items * cs, items * cs, items, items * cs,
+                               ((longest + cs - 1) / cs + st - 1) / st * st};
         p->batch = batch;
         p->shared = false;
-        p->launch_ctas = items * kSmallCluster;
+        p->launch_ctas = items * cs;
         p->shared_indptr_host.clear();
         p->shared_len_host.clear();
         p->indptr_host.assign(kv_indptr_host, kv_indptr_host + batch + 1);
@@ -778,7 +782,7 @@ int attn_impl(const char* who, const void* q, const void* k_pool, const void* v_
     a.slot_ids = fused ? slot_ids : nullptr;
     a.k_host = tiered ? kh : nullptr;
     a.v_host = tiered ? vh : nullptr;
-    a.small = p->step_small ? 1 : 0;
+    a.small = p->step_small ? p->small_cs : 0;
     a.batch = batch;
     a.kv_indptr = kv_indptr;
     cudaError_t e = launch_decode(a, stream);

@@ -734,7 +734,7 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int CS>
 __global__ void __launch_bounds__(SmallCfg<D, G, WPH>::C::kThreads, 2)
     paged_decode_small_kernel(const DecodeArgs a) {
     using C = typename SmallCfg<D, G, WPH>::C;
@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(SmallCfg<D, G, WPH>::C::kThreads, 2)
     Unit* unit = reinterpret_cast<Unit*>(smem + SC::kUnitOffset);
     sh.units = unit;
     sh.part_offset = SC::kPartOffset;
-    constexpr int cs = kSmallCluster;
+    constexpr int cs = CS;  // CTAs of a cluster: the ways each request is split
     const uint32_t rank = cluster_rank();
     const int item = blockIdx.x / cs;
     const int n_groups = a.n_kv_heads / C::kHeadsPerCta;
@@ -1014,10 +1014,10 @@ cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, WPH, NB>, a);
 }
 
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int CS>
 cudaError_t prepare_small() {
     static cudaError_t status = [] {
-        auto k = paged_decode_small_kernel<D, G, WPH>;
+        auto k = paged_decode_small_kernel<D, G, WPH, CS>;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SmallCfg<D, G, WPH>::kSmem);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1026,7 +1026,7 @@ cudaError_t prepare_small() {
     return status;
 }
 
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int CS>
 cudaLaunchConfig_t small_config(int grid, cudaStream_t stream, cudaLaunchAttribute (&attr)[2]) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -1034,7 +1034,7 @@ cudaLaunchConfig_t small_config(int grid, cudaStream_t stream, cudaLaunchAttribu
     cfg.dynamicSmemBytes = SmallCfg<D, G, WPH>::kSmem;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kSmallCluster;
+    attr[0].val.clusterDim.x = CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1046,30 +1046,30 @@ cudaLaunchConfig_t small_config(int grid, cudaStream_t stream, cudaLaunchAttribu
 
 // Clusters of the single-launch kernel that fit on the device at once (0: the kernel
 // cannot run, e.g. no 16-CTA clusters).
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int CS>
 int small_clusters() {
-    if (prepare_small<D, G, WPH>() != cudaSuccess) {
+    if (prepare_small<D, G, WPH, CS>() != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = small_config<D, G, WPH>(kSmallCluster, nullptr, attr);
+    cudaLaunchConfig_t cfg = small_config<D, G, WPH, CS>(CS, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, paged_decode_small_kernel<D, G, WPH>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, paged_decode_small_kernel<D, G, WPH, CS>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-template <int D, int G, int WPH>
+template <int D, int G, int WPH, int CS>
 cudaError_t launch_small(const DecodeArgs& a, cudaStream_t stream) {
-    cudaError_t e = prepare_small<D, G, WPH>();
+    cudaError_t e = prepare_small<D, G, WPH, CS>();
     if (e != cudaSuccess) return e;
     if (a.n_ctas == 0) return cudaSuccess;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = small_config<D, G, WPH>(a.n_ctas, stream, attr);
-    return cudaLaunchKernelEx(&cfg, paged_decode_small_kernel<D, G, WPH>, a);
+    cudaLaunchConfig_t cfg = small_config<D, G, WPH, CS>(a.n_ctas, stream, attr);
+    return cudaLaunchKernelEx(&cfg, paged_decode_small_kernel<D, G, WPH, CS>, a);
 }
 
 // Calls FN<D, G, WPH, NB>::run(args...) for the runtime shape. `shared` selects
@@ -1116,12 +1116,19 @@ struct LaunchFn {
 };
 template <int D, int G, int WPH, int NB>
 struct SmallClustersFn {
-    static int run() { return NB == 1 ? small_clusters<D, G, WPH>() : 0; }
+    static int run(int cs) {
+        if constexpr (NB != 1) return 0;
+        else return cs == kSmallCluster ? small_clusters<D, G, WPH, kSmallCluster>()
+                                        : small_clusters<D, G, WPH, kSmallClusterMin>();
+    }
     static int unsupported() { return 0; }
 };
 template <int D, int G, int WPH, int NB>
 struct SmallLaunchFn {
-    static cudaError_t run(const DecodeArgs& a, cudaStream_t s) { return launch_small<D, G, WPH>(a, s); }
+    static cudaError_t run(const DecodeArgs& a, cudaStream_t s) {
+        return a.small == kSmallCluster ? launch_small<D, G, WPH, kSmallCluster>(a, s)
+                                        : launch_small<D, G, WPH, kSmallClusterMin>(a, s);
+    }
     static cudaError_t unsupported() { return cudaErrorInvalidValue; }
 };
 template <int D, int G, int WPH, int NB>
@@ -1159,10 +1166,11 @@ int decode_ctas_per_sm(int n_qo_heads, int n_kv_heads, int head_dim, int heads_p
                                  shared);
 }
 
-int decode_small_clusters(int n_qo_heads, int n_kv_heads, int head_dim) {
+int decode_small_clusters(int n_qo_heads, int n_kv_heads, int head_dim, int cluster_size) {
     if (!decode_shape_supported(n_qo_heads, n_kv_heads, head_dim)) return 0;
     const int hpc = heads_per_group(n_kv_heads, head_dim);
-    return dispatch<SmallClustersFn>(head_dim, n_qo_heads / n_kv_heads, warps_per_head(hpc), false);
+    return dispatch<SmallClustersFn>(head_dim, n_qo_heads / n_kv_heads, warps_per_head(hpc), false,
+                                     cluster_size);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {

@@ -161,8 +161,9 @@ struct DecodeArgs {
     // addresses of pinned host pools; a negative slot id -1 - h names host row h.
     const void* k_host;
     const void* v_host;
-    // Single-launch small steps (small != 0): no work list; the kernel reads the step's
-    // kv_indptr ([batch + 1], on the device) and merges split parts in each cluster.
+    // Single-launch small steps (small != 0: the cluster size, 16 or 8): no work list;
+    // the kernel reads the step's kv_indptr ([batch + 1], on the device) and merges
+    // split parts in each cluster.
     int small;
     int batch;
     const int32_t* kv_indptr;
@@ -182,10 +183,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // CTAs of one thread-block cluster of the single-launch kernel (a non-portable
 // cluster size): each (request, head group) of a small step is split 16 ways.
 constexpr int kSmallCluster = 16;
+// The smaller cluster (portable size) that PKV_PLAN_SINGLE_LAUNCH falls back to when a
+// plan's clusters of 16 do not all fit the device at once: each request split 8 ways.
+constexpr int kSmallClusterMin = 8;
 // A small-step plan's longest context gives each CTA at most this many stages.
 constexpr int kSmallMaxStages = 8;
 // Clusters of that kernel resident at once for this shape (0: it cannot run here).
-int decode_small_clusters(int n_qo_heads, int n_kv_heads, int head_dim);
+int decode_small_clusters(int n_qo_heads, int n_kv_heads, int head_dim, int cluster_size);
 
 // Row scatter between two pools (either may be pinned host memory mapped for the GPU):
 // dst[dst_slots[i]] = src[src_slots[i]] for K and V, i < n.
@@ -240,6 +244,8 @@ struct pkv_plan {
     // every step of the plan could run in that mode: max_batch x groups clusters fit the
     // device at once (PKV_PLAN_SINGLE_LAUNCH selects the mode whatever max_tokens)
     bool small_fits = false;
+    // the cluster size of the mode: 16, or 8 when only clusters of 8 all fit (flag only)
+    int small_cs = 0;
     bool step_small = false;  // the current step runs in that mode
     std::vector<int32_t> indptr_host;
     // the current step's sharing description (checked against kv_indices when
