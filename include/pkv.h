@@ -116,11 +116,12 @@ int kvpool_prefetch(void* k_pool, void* v_pool, const int32_t* dev_slots, const 
  *
  * Small plans (max_batch x KV-head groups within the thread-block clusters the
  * device holds at once, and max_tokens at most 16 x 8 pipeline stages, 2048 tokens
- * at head_dim 128 with 8 KV heads) run their steps in single-launch mode, the
+ * at head_dim 128 with 8 KV heads; or, where only clusters of 8 all fit, at most
+ * 8 x 8 stages, 1024 tokens) run their steps in single-launch mode, the
  * latency-bound decode of one or a few requests: paged_decode_plan uploads
  * nothing, and each attention call is one launch of a cluster kernel in which 16
- * CTAs split each (request, head group), read kv_indptr on the device, and merge
- * their parts through distributed shared memory. In this mode each attention
+ * (or 8) CTAs split each (request, head group), read kv_indptr on the device, and
+ * merge their parts through distributed shared memory. In this mode each attention
  * launch carries the step's batch: a CUDA graph of attention calls is valid only
  * for steps with the batch it was captured with (PKV_PLAN_PERSISTENT keeps the
  * persistent grid, whose graphs serve any batch). paged_decode_plan_mode reports

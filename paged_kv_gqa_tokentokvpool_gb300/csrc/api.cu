@@ -401,8 +401,9 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     p->ctas = p->num_sms * p->ctas_per_sm;
     p->ctas_shared = p->share_rows > 0 ? p->num_sms * shared_per_sm : 0;
     // A plan whose every step is small runs its steps as single launches of the
-    // cluster kernel: all (request, head group) clusters resident at once, and a CTA's
-    // share of the longest context the plan allows at most kSmallMaxStages stages.
+    // cluster kernel: all (request, head group) clusters resident at once (clusters of
+    // 16, else of 8), and a CTA's share of the longest context the plan allows at most
+    // kSmallMaxStages stages.
     {
         const int64_t items = int64_t(max_batch) * (n_kv_heads / hpg);
         const int64_t max_share = int64_t(kSmallCluster) * kSmallMaxStages * decode_stage_tokens(hpg, head_dim);
@@ -411,7 +412,8 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
             !fits16 && items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim, kSmallClusterMin);
         p->small_fits = fits16 || fits8;
         p->small_cs = fits16 ? kSmallCluster : fits8 ? kSmallClusterMin : 0;
-        p->small = max_tokens <= max_share && fits16;
+        // automatic: no CTA's share of any request can exceed kSmallMaxStages stages
+        p->small = p->small_fits && max_tokens <= max_share / kSmallCluster * p->small_cs;
     }
     p->ctas_max = std::max(p->ctas, p->ctas_shared);
     p->max_batch = max_batch;
