@@ -22,11 +22,13 @@ def pkv():
     return m
 
 
-@pytest.mark.parametrize("lengths", [[3000, 17, 900, 1], [500, 17, 900, 1]],
-                         ids=["persistent_grid", "single_launch"])
+@pytest.mark.parametrize("lengths", [[3000, 17, 900, 1], [500, 17, 900, 1], [100] * 8],
+                         ids=["persistent_grid", "single_launch", "single_launch_8"])
 def test_expired_waits_set_the_status_word_and_the_context_survives(pkv, lengths):
-    """The second workload's plan is small enough for the single-launch cluster kernel,
-    whose CTAs also meet at cluster barriers after the bounded waits have run out."""
+    """The second and third workloads' plans are small enough for the single-launch
+    cluster kernel (the third, 8 requests, on clusters of 8 where clusters of 16 for
+    all of them do not fit), whose CTAs also meet at cluster barriers after the bounded
+    waits have run out."""
     wl = workloads.scattered_workload(lengths, seed=61)
     t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
     dev = torch.device("cuda")
