@@ -116,12 +116,12 @@ int kvpool_prefetch(void* k_pool, void* v_pool, const int32_t* dev_slots, const 
  *
  * Small plans (max_batch x KV-head groups within the thread-block clusters the
  * device holds at once, and max_tokens at most 16 x 8 pipeline stages, 2048 tokens
- * at head_dim 128 with 8 KV heads; or, where only clusters of 8 all fit, at most
- * 8 x 8 stages, 1024 tokens) run their steps in single-launch mode, the
+ * at head_dim 128 with 8 KV heads; or, where only clusters of 8 (4) all fit, at most
+ * 8 (4) x 8 stages) run their steps in single-launch mode, the
  * latency-bound decode of one or a few requests: paged_decode_plan uploads
  * nothing, and each attention call is one launch of a cluster kernel in which 16
- * (or 8) CTAs split each (request, head group), read kv_indptr on the device, and
- * merge their parts through distributed shared memory. In this mode each attention
+ * (or 8, or 4) CTAs split each (request, head group), read kv_indptr on the device,
+ * and merge their parts through distributed shared memory. In this mode each attention
  * launch carries the step's batch: a CUDA graph of attention calls is valid only
  * for steps with the batch it was captured with (PKV_PLAN_PERSISTENT keeps the
  * persistent grid, whose graphs serve any batch). paged_decode_plan_mode reports
@@ -482,13 +482,13 @@ int paged_decode_plan_host_times(pkv_plan* plan, double* compute_us, double* wai
  *     takes effect from the next paged_decode_plan call.
  *   PKV_PLAN_SINGLE_LAUNCH: every step runs in single-launch mode (as a small plan's
  *     do) whatever max_tokens, for callers whose requests are short: the mode splits
- *     each request 16 ways on its own cluster (8 ways on clusters of 8 when clusters of
- *     16 for max_batch x KV-head groups do not all fit the device at once), so a step
- *     of a few requests of up to a few thousand tokens takes one launch with no
- *     upload, while a step with one long context streams it on only 4-8 SMs and is
- *     slower than on the persistent grid. Results are the same either way. Returns
- *     PKV_ERR_UNSUPPORTED when max_batch x KV-head groups exceed even the clusters of
- *     8 the device holds at once, and
+ *     each request 16 ways on its own cluster (8 or 4 ways on clusters of 8 or 4 when
+ *     larger clusters for max_batch x KV-head groups do not all fit the device at
+ *     once), so a step of requests of a few hundred to a few thousand tokens takes one
+ *     launch with no upload and no merge kernel, while a step with one long context
+ *     streams it on only 2-8 SMs and is slower than on the persistent grid. Results
+ *     are the same either way. Returns PKV_ERR_UNSUPPORTED when max_batch x KV-head
+ *     groups exceed even the clusters of 4 the device holds at once, and
  *     PKV_ERR_INVALID_ARG together with PKV_PLAN_PERSISTENT. Takes effect from the
  *     next paged_decode_plan call; graphs then follow the single-launch rule above.
  *   flags : a bitwise OR of PKV_PLAN_* values (0 = none)

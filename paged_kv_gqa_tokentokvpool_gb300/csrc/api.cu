@@ -407,11 +407,13 @@ int paged_decode_plan_create(pkv_plan** out_plan, int max_batch, int64_t max_tok
     {
         const int64_t items = int64_t(max_batch) * (n_kv_heads / hpg);
         const int64_t max_share = int64_t(kSmallCluster) * kSmallMaxStages * decode_stage_tokens(hpg, head_dim);
-        const bool fits16 = items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim, kSmallCluster);
-        const bool fits8 =
-            !fits16 && items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim, kSmallClusterMin);
-        p->small_fits = fits16 || fits8;
-        p->small_cs = fits16 ? kSmallCluster : fits8 ? kSmallClusterMin : 0;
+        p->small_cs = 0;
+        for (int cs : kSmallClusterSizes)
+            if (items <= decode_small_clusters(n_qo_heads, n_kv_heads, head_dim, cs)) {
+                p->small_cs = cs;
+                break;
+            }
+        p->small_fits = p->small_cs > 0;
         // automatic: no CTA's share of any request can exceed kSmallMaxStages stages
         p->small = p->small_fits && max_tokens <= max_share / kSmallCluster * p->small_cs;
     }

@@ -1117,17 +1117,28 @@ struct LaunchFn {
 template <int D, int G, int WPH, int NB>
 struct SmallClustersFn {
     static int run(int cs) {
-        if constexpr (NB != 1) return 0;
-        else return cs == kSmallCluster ? small_clusters<D, G, WPH, kSmallCluster>()
-                                        : small_clusters<D, G, WPH, kSmallClusterMin>();
+        if constexpr (NB != 1) {
+            return 0;
+        } else {
+            switch (cs) {
+                case 16: return small_clusters<D, G, WPH, 16>();
+                case 8: return small_clusters<D, G, WPH, 8>();
+                case 4: return small_clusters<D, G, WPH, 4>();
+                default: return 0;
+            }
+        }
     }
     static int unsupported() { return 0; }
 };
 template <int D, int G, int WPH, int NB>
 struct SmallLaunchFn {
     static cudaError_t run(const DecodeArgs& a, cudaStream_t s) {
-        return a.small == kSmallCluster ? launch_small<D, G, WPH, kSmallCluster>(a, s)
-                                        : launch_small<D, G, WPH, kSmallClusterMin>(a, s);
+        switch (a.small) {
+            case 16: return launch_small<D, G, WPH, 16>(a, s);
+            case 8: return launch_small<D, G, WPH, 8>(a, s);
+            case 4: return launch_small<D, G, WPH, 4>(a, s);
+            default: return cudaErrorInvalidValue;
+        }
     }
     static cudaError_t unsupported() { return cudaErrorInvalidValue; }
 };

@@ -183,9 +183,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // CTAs of one thread-block cluster of the single-launch kernel (a non-portable
 // cluster size): each (request, head group) of a small step is split 16 ways.
 constexpr int kSmallCluster = 16;
-// The smaller cluster (portable size) that PKV_PLAN_SINGLE_LAUNCH falls back to when a
-// plan's clusters of 16 do not all fit the device at once: each request split 8 ways.
-constexpr int kSmallClusterMin = 8;
+// The smaller clusters (portable sizes) the mode falls back to when a plan's clusters of
+// 16 do not all fit the device at once: each request split 8, then 4 ways.
+constexpr int kSmallClusterSizes[3] = {16, 8, 4};
 // A small-step plan's longest context gives each CTA at most this many stages.
 constexpr int kSmallMaxStages = 8;
 // Clusters of that kernel resident at once for this shape (0: it cannot run here).
@@ -244,7 +244,7 @@ struct pkv_plan {
     // every step of the plan could run in that mode: max_batch x groups clusters fit the
     // device at once (PKV_PLAN_SINGLE_LAUNCH selects the mode whatever max_tokens)
     bool small_fits = false;
-    // the cluster size of the mode: 16, or 8 when only clusters of 8 all fit (flag only)
+    // the cluster size of the mode: the largest of 16, 8, 4 whose clusters all fit
     int small_cs = 0;
     bool step_small = false;  // the current step runs in that mode
     std::vector<int32_t> indptr_host;

@@ -775,13 +775,15 @@ def test_small_step_modes(pkv, case, fused, persistent):
 
 
 @pytest.mark.parametrize("lengths", [[1024] * 4, [9000, 5], [1, 2048, 0, 700], [512] * 8,
-                                     [300 + 97 * i for i in range(12)]],
-                         ids=["four_1k", "one_long", "mixed", "eight_short", "twelve"])
+                                     [300 + 97 * i for i in range(12)],
+                                     [200 + 37 * i for i in range(24)]],
+                         ids=["four_1k", "one_long", "mixed", "eight_short", "twelve",
+                              "twenty_four"])
 def test_single_launch_flag(pkv, lengths):
     """PKV_PLAN_SINGLE_LAUNCH: a plan whose max_tokens is beyond the automatic
     single-launch limit runs its steps in that mode all the same (each request split 16
-    ways, a CTA's share of 9000 tokens is 36 stages; 8 ways on clusters of 8 for the
-    batches whose clusters of 16 do not all fit); results equal the oracle's."""
+    ways, a CTA's share of 9000 tokens is 36 stages; 8 or 4 ways on clusters of 8 or 4
+    for the batches whose clusters of 16 do not all fit); results equal the oracle's."""
     wl = workloads.scattered_workload(lengths, seed=81)
     t = workloads.layer_tensors(wl, 0, device="cpu", poison_unreferenced=True)
     dev = torch.device("cuda")
