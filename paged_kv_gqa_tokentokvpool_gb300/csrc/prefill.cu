@@ -30,12 +30,16 @@
 //    maps of the pools in that 128-byte swizzled layout, their bytes counted on the
 //    same barrier: the SMs then take in the tiles by both paths at once.
 //  * An MMA warp issues, from one lane, S = Q K^T (128 x kKv, K = head_dim, operands
-//    in shared memory) into one of two TMEM buffers, and O += P V (128 x head_dim,
+//    in shared memory) into one of three TMEM buffers, and O += P V (128 x head_dim,
 //    K = kKv) with P read from TMEM as the A operand, each signalled on an mbarrier
-//    by tcgen05.commit. S runs up to two tiles ahead of the softmax.
+//    by tcgen05.commit. P is written over the upper half of its own S buffer once the
+//    softmax has read it, so S of tile n + 3 waits for P V of tile n to complete; S
+//    runs up to two tiles ahead of the softmax, and the softmax never waits for a
+//    buffer to write P into.
 //  * Four softmax warps own one query row per thread: they read the row of S from
 //    TMEM, apply the causal mask (list position <= the row's query position) and an
-//    online softmax in base 2 with fp32 state, write P as bf16 pairs back to TMEM, and
+//    online softmax in base 2 with fp32 state, write P as bf16 pairs over the upper half
+//    of the same S buffer, and
 //    rescale O in TMEM when a row's running maximum grows by more than 2^8 (between
 //    rescales the probabilities stay below 2^8, exact enough for bf16 P and fp32
 //    sums). At the end they read O back, divide by the row sum and store out and lse.
@@ -72,7 +76,7 @@ constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfProducerWarps;  // also owns the
 constexpr int kPfRelayWarp = kPfMmaWarp + 1;
 constexpr int kPfTmaWarp = kPfRelayWarp + 1;  // head_dim 256: two more warps (K rows, V rows)
 constexpr uint32_t kPfTmemCols = 512;
-constexpr int kPfOCol = 256;                // TMEM columns of O: 256 .. 256 + head_dim
+constexpr int kPfSBufs = 3;                 // S buffers in TMEM (P over their upper halves)
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -136,9 +140,9 @@ struct PfCfg {
     // tensor core, so the MMAs are made as large as shared memory allows.
     static constexpr int kKv = D == 128 ? 128 : 64;
     static constexpr int kStages = D == 128 ? 3 : 2;
-    // TMEM columns: S buffers at 0 and kKv (fp32), O at kPfOCol, and two P buffers
-    // of kKv / 2 columns (bf16 pairs) at kPCol, the A operand of P V
-    static constexpr int kPCol = D == 128 ? kPfOCol + D : 2 * kKv;
+    // TMEM columns: S buffer b at b * kKv (fp32; P of its tile, kKv / 2 columns of
+    // bf16 pairs, the A operand of P V, over its upper half), O in the last D columns
+    static constexpr int kOCol = int(kPfTmemCols) - D;
     static constexpr int kPanels = D / 64;
     static constexpr int kQPanel = kPfRows * 128;           // bytes of one q panel
     static constexpr int kKvPanel = kKv * 128;              // bytes of one K (or V) panel
@@ -149,9 +153,9 @@ struct PfCfg {
     static constexpr int kVOff = kKOff + kStages * kKvBytes;
     static constexpr int kBarOff = kVOff + kStages * kKvBytes;
     // mbarriers: for K and for V rings each landed / full / empty [kStages];
-    // s_full[2], s_empty[2], p_full[2], o_done[2], drain; then the TMEM address and
-    // the abort flag
-    static constexpr int kNumBars = 6 * kStages + 9;
+    // s_full, p_full and o_done per S buffer, drain; then the TMEM address and the
+    // abort flag
+    static constexpr int kNumBars = 6 * kStages + 3 * kPfSBufs + 1;
     static constexpr int kTmemOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemOff + 4;
     static constexpr int kSmem = kAbortOff + 4 + 1024;      // + slack to align the base
@@ -170,9 +174,7 @@ struct PfCfg {
     static_assert(kPfKvTile % kKv == 0, "split cuts fall on ring tiles");
     static_assert(kQPieces * kPfHalfThreads == kPfRows * kChunks, "q pieces");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-    static_assert(2 * kKv <= kPfOCol && kPfOCol + D <= int(kPfTmemCols), "TMEM columns");
-    static_assert(kPCol + kKv <= int(kPfTmemCols) && (kPCol >= kPfOCol + D || kPCol + kKv <= kPfOCol),
-                  "P columns");
+    static_assert(kPfSBufs * kKv <= kOCol, "TMEM columns");
 };
 
 // Byte offset of 16-byte chunk c of row n in a panel-major swizzled operand whose
@@ -282,14 +284,14 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
     const auto full = [&](int v, int s) { return bars + 8u * ((2 + v) * C::kStages + s); };
     const auto empty = [&](int v, int s) { return bars + 8u * ((4 + v) * C::kStages + s); };
     const uint32_t bars2 = bars + 8u * 6 * C::kStages;
-    const auto s_full = [&](int b) { return bars2 + 8u * b; };
-    const auto s_empty = [&](int b) { return bars2 + 8u * (2 + b); };
-    // P of tile n written / P V of tile n done: one barrier per P buffer (tiles of
-    // one parity), so that a barrier's next phase always waits for its reader to
-    // have seen the previous one
-    const auto p_full = [&](int n) { return bars2 + 8u * (4 + (n & 1)); };
-    const auto o_done = [&](int n) { return bars2 + 8u * (6 + (n & 1)); };
-    const uint32_t drain = bars2 + 8u * 8;
+    // S of tile n written / P of tile n written / P V of tile n done: one barrier per
+    // S buffer (tiles n, n + 3, ...; phase parity (n / 3) & 1). No role can run three
+    // tiles ahead of a barrier's other side, so no parity test can alias.
+    const auto s_full = [&](int n) { return bars2 + 8u * (n % kPfSBufs); };
+    const auto p_full = [&](int n) { return bars2 + 8u * (kPfSBufs + n % kPfSBufs); };
+    const auto o_done = [&](int n) { return bars2 + 8u * (2 * kPfSBufs + n % kPfSBufs); };
+    const auto ph = [](int n) { return uint32_t((n / kPfSBufs) & 1); };
+    const uint32_t drain = bars2 + 8u * 3 * kPfSBufs;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -301,11 +303,8 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
                 mbar_init(full(v, s), 1);
                 mbar_init(empty(v, s), 1);
             }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kPfSBufs; ++b) {
             mbar_init(s_full(b), 1);
-            mbar_init(s_empty(b), 32 * kPfSoftmaxWarps);
-        }
-        for (int b = 0; b < 2; ++b) {
             mbar_init(p_full(b), 32 * kPfSoftmaxWarps);
             mbar_init(o_done(b), 1);
         }
@@ -372,13 +371,13 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
         // ================= MMA issuer (one warp, one lane issues) =================
         // Two streams of work, each issued as soon as its inputs are ready (polled,
         // so that neither waits behind the other): S of tile ns once its K stage has
-        // been announced and the softmax has read the S buffer's previous tile (so S
-        // runs up to two tiles ahead of the softmax), and
+        // been announced and P V of tile ns - 3, which read P from the same S buffer,
+        // has completed (so S runs up to two tiles ahead of the softmax), and
         // P V of tile npv once its P is in TMEM (and O rescaled) and its V stage has
         // been announced. The whole warp runs the loop with lane 0's view of the
         // barriers, so the descriptors stay warp-uniform; lane 0 alone issues.
         const bool leader = lane == 0;
-        const uint32_t o_tmem = tmem + uint32_t(kPfOCol);
+        const uint32_t o_tmem = tmem + uint32_t(C::kOCol);
         const uint64_t q_desc = tc::sdesc_sw128(base + C::kQOff, 16, 1024);
         const uint64_t k_desc = tc::sdesc_sw128(base + C::kKOff, 16, 1024);
         const uint64_t v_desc = tc::sdesc_sw128(base + C::kVOff, C::kKvPanel, 1024);
@@ -390,31 +389,31 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
             bool go = false;
             if (leader && ns < n_tiles)
                 go = mbar_test(full(0, ns % C::kStages), uint32_t((ns / C::kStages) & 1)) &&
-                     (ns < 2 || mbar_test(s_empty(ns & 1), uint32_t((ns / 2 - 1) & 1)));
+                     (ns < kPfSBufs || mbar_test(o_done(ns), ph(ns - kPfSBufs)));
             if (__shfl_sync(kFullMask, go, 0)) {
                 tc::fence_after_sync();
                 // descriptor start addresses advance in 16-byte units (low bits)
                 const uint64_t kd = k_desc + uint64_t(((ns % C::kStages) * C::kKvBytes) >> 4);
-                const uint32_t s_tmem = tmem + uint32_t((ns & 1) * C::kKv);
+                const uint32_t s_tmem = tmem + uint32_t((ns % kPfSBufs) * C::kKv);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = uint32_t(((ks >> 2) * C::kQPanel + (ks & 3) * 32) >> 4);
                     const uint32_t koff = uint32_t(((ks >> 2) * C::kKvPanel + (ks & 3) * 32) >> 4);
                     tc::mma_bf16_ss_if(leader, s_tmem, q_desc + off, kd + koff, C::kIdescS, ks > 0);
                 }
-                tc::commit_if(leader, s_full(ns & 1));
+                tc::commit_if(leader, s_full(ns));
                 tc::commit_if(leader, empty(0, ns % C::kStages));
                 ++ns;
                 progress = true;
             }
             go = false;
             if (leader && npv < ns)
-                go = mbar_test(p_full(npv), uint32_t((npv >> 1) & 1)) &&
+                go = mbar_test(p_full(npv), ph(npv)) &&
                      mbar_test(full(1, npv % C::kStages), uint32_t((npv / C::kStages) & 1));
             if (__shfl_sync(kFullMask, go, 0)) {
                 tc::fence_after_sync();
                 const uint64_t vd = v_desc + uint64_t(((npv % C::kStages) * C::kKvBytes) >> 4);
-                const uint32_t p_tmem = tmem + uint32_t(C::kPCol + (npv & 1) * (C::kKv / 2));
+                const uint32_t p_tmem = tmem + uint32_t((npv % kPfSBufs) * C::kKv + C::kKv / 2);
 #pragma unroll
                 for (int ks = 0; ks < C::kKv / 16; ++ks)
                     tc::mma_bf16_ts_if(leader, o_tmem, p_tmem + uint32_t(8 * ks),
@@ -551,22 +550,20 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
         float m = neg_inf(), l = 0.f;
         bool ok = true;
         for (int n = 0; n < n_tiles; ++n) {
-            const int b = n & 1;
-            ok = pf_wait(s_full(b), uint32_t((n / 2) & 1), a.status, abort_flag);
+            const uint32_t s_tmem = tmem + lane_base + uint32_t((n % kPfSBufs) * C::kKv);
+            ok = pf_wait(s_full(n), ph(n), a.status, abort_flag);
             if (!__all_sync(kFullMask, ok)) { ok = false; break; }
             tc::fence_after_sync();
             float x[C::kKv];
-            {   // the row of S in one load
+            {   // the row of S in one load (complete before P is written over it)
                 uint32_t v[C::kKv];
                 if constexpr (C::kKv == 128)
-                    tc::tmem_ld128(tmem + lane_base + uint32_t(b * C::kKv), v);
+                    tc::tmem_ld128(s_tmem, v);
                 else
-                    tc::tmem_ld64(tmem + lane_base + uint32_t(b * C::kKv), v);
+                    tc::tmem_ld64(s_tmem, v);
 #pragma unroll
                 for (int i = 0; i < C::kKv; ++i) x[i] = __uint_as_float(v[i]);
             }
-            tc::fence_before_sync();
-            mbar_arrive(s_empty(b));  // S buffer b may be overwritten
             // causal mask: entry e is seen by this row iff e <= qpos and e < kv_hi
             // (raw scores; sm_scale > 0 is applied in the exponent below)
             const int e0 = (t0 + n) * C::kKv;
@@ -592,14 +589,10 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
             const float alpha = grow ? ex2(m - m_new) : 1.f;  // 0 on the first tile
             m = m_new;
             const float neg_m = -m;
-            // TMEM P buffer n & 1 was last read by P V of tile n - 2
-            if (n > 1) {
-                ok = pf_wait(o_done(n), uint32_t(((n - 2) >> 1) & 1), a.status, abort_flag);
-                if (!__all_sync(kFullMask, ok)) { ok = false; break; }
-            }
             // P = 2^(s * scale - m) as bf16 pairs into this row's TMEM lane (the A
-            // operand of P V), 64 entries (32 columns) at a time
-            const uint32_t p_tmem = tmem + lane_base + uint32_t(C::kPCol + (n & 1) * (C::kKv / 2));
+            // operand of P V) over the upper half of the S buffer, 64 entries (32
+            // columns) at a time
+            const uint32_t p_tmem = s_tmem + uint32_t(C::kKv / 2);
             float sums[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < C::kKv / 64; ++c) {
@@ -619,14 +612,14 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
             // a row maximum moved: O (complete up to P V of tile n - 1) is rescaled
             // before P V of tile n accumulates into it
             if (n > 0 && __any_sync(kFullMask, grow)) {
-                ok = pf_wait(o_done(n - 1), uint32_t(((n - 1) >> 1) & 1), a.status, abort_flag);
+                ok = pf_wait(o_done(n - 1), ph(n - 1), a.status, abort_flag);
                 if (!__all_sync(kFullMask, ok)) { ok = false; break; }
                 tc::fence_after_sync();
                 {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
-                        const uint32_t ta = tmem + lane_base + uint32_t(kPfOCol + 32 * c);
+                        const uint32_t ta = tmem + lane_base + uint32_t(C::kOCol + 32 * c);
                         tc::tmem_ld32(ta, v);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
@@ -641,7 +634,7 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
         }
         // ---- epilogue: O of the last tile, divided by the row sum
         if (ok && n_tiles > 0) {
-            ok = pf_wait(o_done(n_tiles - 1), uint32_t(((n_tiles - 1) >> 1) & 1), a.status, abort_flag);
+            ok = pf_wait(o_done(n_tiles - 1), ph(n_tiles - 1), a.status, abort_flag);
             ok = __all_sync(kFullMask, ok);
         }
         if (ok && n_tiles > 0) {
@@ -653,7 +646,7 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
-                tc::tmem_ld32(tmem + lane_base + uint32_t(kPfOCol + 32 * c), v);
+                tc::tmem_ld32(tmem + lane_base + uint32_t(C::kOCol + 32 * c), v);
                 if (!store) continue;
                 if (un.part >= 0) {  // a piece of a split range: fp32 partial result
                     float4* dst = reinterpret_cast<float4*>(
