@@ -25,10 +25,11 @@
 //    layout (K-major for q and K; V's rows are the same bytes read as an MN-major
 //    operand). A thread's arrival on a stage's barrier rides on its copies, and a
 //    relay thread fences the landed stage (generic to async proxy) for the tensor
-//    core. At head_dim 256 two more warps copy the first 20 tokens of every K and V
-//    tile with 4-row TMA gathers (cp.async.bulk.tensor .tile::gather4) through tensor
-//    maps of the pools in that 128-byte swizzled layout, their bytes counted on the
-//    same barrier: the SMs then take in the tiles by both paths at once.
+//    core. Two more warps copy the first tokens of every K and V tile (32 of 128 at
+//    head_dim 128, 20 of 64 at 256) with 4-row TMA gathers (cp.async.bulk.tensor
+//    .tile::gather4) through tensor maps of the pools in that 128-byte swizzled
+//    layout, their bytes counted on the same barrier: the SMs then take in the tiles
+//    by both paths at once.
 //  * An MMA warp issues, from one lane, S = Q K^T (128 x kKv, K = head_dim, operands
 //    in shared memory) into one of three TMEM buffers, and O += P V (128 x head_dim,
 //    K = kKv) with P read from TMEM as the A operand, each signalled on an mbarrier
@@ -74,7 +75,7 @@ constexpr int kPfProducerThreads = 32 * kPfProducerWarps;
 constexpr int kPfHalfThreads = kPfProducerThreads / 2;  // K rows by one half, V rows by the other
 constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfProducerWarps;  // also owns the TMEM allocation
 constexpr int kPfRelayWarp = kPfMmaWarp + 1;
-constexpr int kPfTmaWarp = kPfRelayWarp + 1;  // head_dim 256: two more warps (K rows, V rows)
+constexpr int kPfTmaWarp = kPfRelayWarp + 1;  // two more warps (K rows, V rows)
 constexpr uint32_t kPfTmemCols = 512;
 constexpr int kPfSBufs = 3;                 // S buffers in TMEM (P over their upper halves)
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -102,7 +103,7 @@ struct PfMerge {
 };
 static_assert(sizeof(PfMerge) == 32, "merge record");
 
-// Tensor maps of one head_dim-256 call (cuTensorMapEncodeTiled): each pool as a 2D
+// Tensor maps of one call (cuTensorMapEncodeTiled): each pool as a 2D
 // array [slots, n_kv_heads x head_dim] with 64 x 1 element boxes and the 128-byte
 // swizzle, for 4-row gathers.
 struct PfMaps {
@@ -110,7 +111,7 @@ struct PfMaps {
 };
 
 struct PfArgs {
-    PfMaps maps;  // head_dim 256 only
+    PfMaps maps;  // the pools, for the TMA gathers
     const void* q;
     const void* k_pool;
     const void* v_pool;
@@ -128,6 +129,11 @@ struct PfArgs {
     int* status;       // nonzero: a wait of some CTA exceeded its bound
     bool withhold;     // injected stall (pkv_inject_stall): the producers issue no copies
 };
+
+// Tokens of every K and V tile copied by the tensor memory accelerator's gather form
+// (two more warps), the rest by the producer threads' cp.async: measured best at 20
+// of 64 at head_dim 256 and 32 of 128 at head_dim 128.
+constexpr int pf_tma_tokens(int head_dim) { return head_dim == 256 ? 20 : 32; }
 
 // Shared memory of one CTA (offsets from a 1024-byte aligned base). Every operand
 // is stored as 64-element panels of 128-byte rows in the 128-byte swizzled layout:
@@ -160,10 +166,9 @@ struct PfCfg {
     static constexpr int kAbortOff = kTmemOff + 4;
     static constexpr int kSmem = kAbortOff + 4 + 1024;      // + slack to align the base
     static constexpr int kChunks = D / 8;                   // 16-byte pieces per row
-    // At head_dim 256 two more warps copy the first kTmaTok tokens of every K and V
-    // tile by the tensor memory accelerator's gather form, the producer threads the
-    // rest; measured best at 20 of 64 (no share helped at head_dim 128).
-    static constexpr int kTmaTok = D == 256 ? 20 : 0;
+    // Two more warps copy the first kTmaTok tokens of every K and V tile by the
+    // tensor memory accelerator's gather form, the producer threads the rest.
+    static constexpr int kTmaTok = pf_tma_tokens(D);
     static constexpr int kThreads = 32 * (kPfRelayWarp + 1 + (kTmaTok > 0 ? 2 : 0));
     static constexpr int kTilePieces = (kKv - kTmaTok) * kChunks / kPfHalfThreads;  // per thread, K or V
     static constexpr int kQPieces = kPfRows * kChunks / kPfHalfThreads;   // q, by the K half
@@ -450,7 +455,7 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
         }
         __syncwarp();
     } else if (warp >= kPfTmaWarp) {
-        // ================= TMA gather (head_dim 256) =================
+        // ================= TMA gather =================
         // Tokens 0 .. kTmaTok - 1 of every K (warp kPfTmaWarp) or V tile: lane l copies
         // tokens 4l .. 4l + 3, one 4-row gather per 64-element panel, counted in bytes
         // on the stage's `landed` barrier beside the producer threads' arrivals. Rows
@@ -1197,7 +1202,7 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
     a.merges = p->dev_merges;
     a.n_merges = p->n_merges;
     a.status = p->dev_status;
-    if (head_dim == 256) {
+    if (pf_tma_tokens(head_dim) > 0) {
         const uint64_t cols = uint64_t(n_kv_heads) * uint64_t(head_dim);
         if (!encode_pool(&a.maps.k, k_pool, cols) || !encode_pool(&a.maps.v, v_pool, cols))
             return fail(PKV_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed for the pools", who);
