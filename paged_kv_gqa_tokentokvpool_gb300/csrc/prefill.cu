@@ -577,16 +577,16 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < C::kKv; ++i) x[i] = i < lim ? x[i] : neg_inf();
             }
-            // row maximum: eight independent chains, then a tree
+            // row maximum: eight independent chains of three-input maxima, then a tree
             float mxv[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) mxv[j] = x[j];
 #pragma unroll
-            for (int i = 8; i < C::kKv; i += 8)
+            for (int i = 8; i < C::kKv; i += 16)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) mxv[j] = fmaxf(mxv[j], x[i + j]);
-            const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
-                                   fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7]))) * sl2;
+                for (int j = 0; j < 8; ++j) mxv[j] = fmax3(mxv[j], x[i + j], x[i + 8 + j]);
+            const float mx = fmax3(fmax3(mxv[0], mxv[1], mxv[2]), fmax3(mxv[3], mxv[4], mxv[5]),
+                                   fmaxf(mxv[6], mxv[7])) * sl2;
             // running maximum (base 2, scaled): moves when a row's maximum grows by more
             // than 2^8 (the first tile always sets it: every row sees entry kv_lo)
             const bool grow = mx > m + kRescaleLog2;
@@ -598,22 +598,25 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
             // operand of P V) over the upper half of the S buffer, 64 entries (32
             // columns) at a time
             const uint32_t p_tmem = s_tmem + uint32_t(C::kKv / 2);
-            float sums[4] = {0.f, 0.f, 0.f, 0.f};
+            // (the exponent arguments and the row sum two entries to an instruction:
+            // the paired fp32 FMA and add of sm_100 and later)
+            const float2 sl2x2 = make_float2(sl2, sl2), neg_mx2 = make_float2(neg_m, neg_m);
+            float2 sums[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < C::kKv / 64; ++c) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2(fmaf(x[64 * c + 2 * i], sl2, neg_m));
-                    const float p1 = ex2(fmaf(x[64 * c + 2 * i + 1], sl2, neg_m));
-                    sums[(2 * i) & 3] += p0;
-                    sums[(2 * i + 1) & 3] += p1;
-                    pk[i] = pack_bf16x2(p0, p1);
+                    const float2 e = __ffma2_rn(make_float2(x[64 * c + 2 * i], x[64 * c + 2 * i + 1]),
+                                                sl2x2, neg_mx2);
+                    const float2 p = make_float2(ex2(e.x), ex2(e.y));
+                    sums[i & 1] = __fadd2_rn(sums[i & 1], p);
+                    pk[i] = pack_bf16x2(p.x, p.y);
                 }
                 tc::tmem_st32(p_tmem + uint32_t(32 * c), pk);
             }
-            const float sum0 = sums[0] + sums[2], sum1 = sums[1] + sums[3];
-            l = fmaf(l, alpha, sum0 + sum1);
+            const float2 s2 = __fadd2_rn(sums[0], sums[1]);
+            l = fmaf(l, alpha, s2.x + s2.y);
             // a row maximum moved: O (complete up to P V of tile n - 1) is rescaled
             // before P V of tile n accumulates into it
             if (n > 0 && __any_sync(kFullMask, grow)) {

@@ -131,6 +131,13 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     return y;
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, PTX ISA 8.8, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // 2^x on the hardware's approximate exponential unit (ex2.approx, PTX ISA).
 __device__ __forceinline__ float ex2(float x) {
     float y;
