@@ -230,34 +230,33 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Slot ids of the rows this producer thread copies for KV tile `tile` (-1 past
-// the range): piece i is token (pt + i * kPfHalfThreads) / kChunks.
+// Slot ids of the rows this producer thread copies for KV tile `tile`: piece i is
+// token (pt + i * kPfHalfThreads) / kChunks. Tokens past the range repeat the range's
+// last row (finite rows that the softmax masks), so every copy is a full one.
 template <int D, int G>
 __device__ __forceinline__ void load_tile_slots(const PfArgs& a, const PfUnit& un, int tile, int pt,
                                                 int (&slot)[PfCfg<D, G>::kTilePieces]) {
     using C = PfCfg<D, G>;
+    const int32_t* ids = a.kv_indices + un.kv_begin;
 #pragma unroll
     for (int i = 0; i < C::kTilePieces; ++i) {
         const int tok = C::kTmaTok + (pt + i * kPfHalfThreads) / C::kChunks;
-        const int j = tile * C::kKv + tok;
-        slot[i] = j < un.kv_hi ? __ldg(a.kv_indices + un.kv_begin + j) : -1;
+        slot[i] = __ldg(ids + min(tile * C::kKv + tok, un.kv_hi - 1));
     }
 }
 
-// cp.async of this thread's pieces of a K (or V) tile from `pool` into the stage at
-// shared address `dst` (zero past the range).
+// cp.async of this thread's pieces of a K (or V) tile into the stage at shared address
+// `dst`. `src` is this thread's 16 bytes of the row of slot 0 (its KV head and its
+// 16-byte column, the same for every piece), `row_bytes` the pool's bytes per slot.
 template <int D, int G>
-__device__ __forceinline__ void issue_tile(const PfArgs& a, const PfUnit& un, const __nv_bfloat16* pool,
-                                           uint32_t dst, int pt,
+__device__ __forceinline__ void issue_tile(const char* src, uint32_t row_bytes, uint32_t dst, int pt,
                                            const int (&slot)[PfCfg<D, G>::kTilePieces]) {
     using C = PfCfg<D, G>;
 #pragma unroll
     for (int i = 0; i < C::kTilePieces; ++i) {
         const int c = pt + i * kPfHalfThreads;
         const int tok = C::kTmaTok + c / C::kChunks, part = c % C::kChunks;
-        const bool valid = slot[i] >= 0;
-        const int64_t off = (int64_t(valid ? slot[i] : 0) * a.n_kv_heads + un.g) * D + part * 8;
-        cp_async16(dst + sw128_off(tok, part, C::kKv), pool + off, valid);
+        cp_async16(dst + sw128_off(tok, part, C::kKv), src + size_t(uint32_t(slot[i])) * row_bytes);
     }
 }
 
@@ -358,7 +357,10 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
                 cp_async16(base + C::kQOff + sw128_off(r, part, kPfRows), q + off, valid);
             }
         }
-        const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(half ? a.v_pool : a.k_pool);
+        static_assert(kPfHalfThreads % C::kChunks == 0, "a thread's 16-byte column is fixed");
+        const uint32_t row_bytes = uint32_t(a.n_kv_heads) * D * 2;
+        const char* src = static_cast<const char*>(half ? a.v_pool : a.k_pool) +
+                          (size_t(un.g) * D + (pt % C::kChunks) * 8) * 2;
         const uint32_t ring = base + (half ? C::kVOff : C::kKOff);
         int slot[C::kTilePieces];
         if (n_copy_tiles > 0) load_tile_slots<D, G>(a, un, t0, pt, slot);
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
             if (n >= C::kStages &&
                 !pf_wait(empty(half, st), uint32_t((n / C::kStages - 1) & 1), a.status, abort_flag))
                 break;
-            issue_tile<D, G>(a, un, pool, ring + st * C::kKvBytes, pt, slot);
+            issue_tile<D, G>(src, row_bytes, ring + st * C::kKvBytes, pt, slot);
             cp_async_arrive(landed(half, st));
             if (n + 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + n + 1, pt, slot);
         }

@@ -86,6 +86,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
                  "r"(valid ? 16 : 0)
                  : "memory");
 }
+// 16-byte asynchronous copy, always a full one.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 // Arrive on an mbarrier once every cp.async this thread issued so far has landed;
 // the barrier's expected count already includes this arrival (.noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
