@@ -211,6 +211,18 @@ __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, int* stat
     }
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, PTX ISA 8.8, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 16-byte asynchronous copy, always a full one.
+__device__ __forceinline__ void cp_async16_full(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // Non-blocking test of the phase of `bar` with the given parity.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -256,7 +268,7 @@ __device__ __forceinline__ void issue_tile(const char* src, uint32_t row_bytes, 
     for (int i = 0; i < C::kTilePieces; ++i) {
         const int c = pt + i * kPfHalfThreads;
         const int tok = C::kTmaTok + c / C::kChunks, part = c % C::kChunks;
-        cp_async16(dst + sw128_off(tok, part, C::kKv), src + size_t(uint32_t(slot[i])) * row_bytes);
+        cp_async16_full(dst + sw128_off(tok, part, C::kKv), src + size_t(uint32_t(slot[i])) * row_bytes);
     }
 }
 

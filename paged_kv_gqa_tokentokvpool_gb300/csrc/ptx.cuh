@@ -86,10 +86,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
                  "r"(valid ? 16 : 0)
                  : "memory");
 }
-// 16-byte asynchronous copy, always a full one.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
 // Arrive on an mbarrier once every cp.async this thread issued so far has landed;
 // the barrier's expected count already includes this arrival (.noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
@@ -133,13 +129,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
-}
-
-// max(a, b, c) in one instruction (three-input max.f32, PTX ISA 8.8, sm_100 and later).
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
 }
 
 // 2^x on the hardware's approximate exponential unit (ex2.approx, PTX ISA).
