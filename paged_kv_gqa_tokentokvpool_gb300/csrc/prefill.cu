@@ -702,62 +702,75 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
     }
 }
 
-// Log-sum-exp merge of split units: one warp per (merge record, row of its 128),
-// lanes over head_dim, every piece's loads issued before any is used:
+// Log-sum-exp merge of split units: half a warp per (merge record, row of its 128),
+// its 16 lanes over head_dim (D / 16 dims each), the pieces folded in chunks of
+// kPfMergeChunk with every load of a chunk issued before any is used:
 //     lse = log2 sum_c 2^lse_c,   out = sum_c 2^(lse_c - lse) out_c
+// kept as a running maximum m, sum s = sum_c 2^(lse_c - m) and accumulator
+// a = sum_c 2^(lse_c - m) out_c, rescaled when m grows. Few registers a thread, so a
+// step's merges run in about one wave.
 constexpr int kPfMergeWarps = 4;
 constexpr int kPfMaxPieces = 16;  // pieces per split unit (the planner's cap)
+constexpr int kPfMergeChunk = 4;  // pieces whose loads are in flight together
 
 template <int D, int G>
 __global__ void __launch_bounds__(32 * kPfMergeWarps) prefill_merge_kernel(const PfArgs a) {
     pdl_launch_dependents();
-    constexpr int kVD = D / 32;  // dims per lane
+    constexpr int kVD = D / 16;  // dims per lane
     const int lane = threadIdx.x & 31;
-    const int w = blockIdx.x * kPfMergeWarps + (threadIdx.x >> 5);
-    if (w >= a.n_merges * kPfRows) return;
-    const PfMerge mg = a.merges[w / kPfRows];  // plan data
-    const int r = w % kPfRows, t = r / G, h = r % G;
+    const int hw = (blockIdx.x * kPfMergeWarps + (threadIdx.x >> 5)) * 2 + (lane >> 4);  // half-warp
+    if (hw >= a.n_merges * kPfRows) return;  // no warp-wide operation follows
+    const PfMerge mg = a.merges[hw / kPfRows];  // plan data
+    const int r = hw % kPfRows, t = r / G, h = r % G;
     if (t >= mg.n_q) return;
+    const int d0 = (lane & 15) * kVD;
     pdl_wait();  // the pieces come from the kernel before
-    float x[kPfMaxPieces][kVD], xl[kPfMaxPieces];
-#pragma unroll
-    for (int c = 0; c < kPfMaxPieces; ++c) {
-        if (c < mg.count) {
-            const int64_t wrow = int64_t(mg.first + c) * kPfRows + r;
-            xl[c] = __ldcg(a.ws_lse + wrow);
-#pragma unroll
-            for (int i = 0; i < kVD; i += 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_o + wrow * D + lane * kVD + i));
-                x[c][i] = v.x;
-                x[c][i + 1] = v.y;
-                x[c][i + 2] = v.z;
-                x[c][i + 3] = v.w;
-            }
-        }
-    }
-    float mx = neg_inf();
-#pragma unroll
-    for (int c = 0; c < kPfMaxPieces; ++c)
-        if (c < mg.count) mx = fmaxf(mx, xl[c]);
-    float sum = 0.f, acc[kVD];
+    float m = neg_inf(), sum = 0.f, acc[kVD];
 #pragma unroll
     for (int i = 0; i < kVD; ++i) acc[i] = 0.f;
+    for (int c0 = 0; c0 < mg.count; c0 += kPfMergeChunk) {
+        float xl[kPfMergeChunk];
+        float4 x[kPfMergeChunk][kVD / 4];
 #pragma unroll
-    for (int c = 0; c < kPfMaxPieces; ++c) {
-        if (c < mg.count) {
-            const float wgt = ex2(xl[c] - mx);
+        for (int c = 0; c < kPfMergeChunk; ++c) {
+            const bool in = c0 + c < mg.count;
+            const int64_t wrow = int64_t(mg.first + (in ? c0 + c : 0)) * kPfRows + r;
+            xl[c] = in ? __ldcg(a.ws_lse + wrow) : neg_inf();
+#pragma unroll
+            for (int i = 0; i < kVD / 4; ++i)
+                x[c][i] = in ? __ldcg(reinterpret_cast<const float4*>(a.ws_o + wrow * D + d0) + i)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float mc = m;
+#pragma unroll
+        for (int c = 0; c < kPfMergeChunk; ++c) mc = fmaxf(mc, xl[c]);
+        const float scale = m == neg_inf() ? 0.f : ex2(m - mc);  // every piece has a finite lse
+        sum *= scale;
+#pragma unroll
+        for (int i = 0; i < kVD; ++i) acc[i] *= scale;
+#pragma unroll
+        for (int c = 0; c < kPfMergeChunk; ++c) {
+            const float wgt = ex2(xl[c] - mc);  // 0 for the chunk's padding
             sum += wgt;
 #pragma unroll
-            for (int i = 0; i < kVD; ++i) acc[i] = fmaf(wgt, x[c][i], acc[i]);
+            for (int i = 0; i < kVD / 4; ++i) {
+                acc[4 * i] = fmaf(wgt, x[c][i].x, acc[4 * i]);
+                acc[4 * i + 1] = fmaf(wgt, x[c][i].y, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(wgt, x[c][i].z, acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(wgt, x[c][i].w, acc[4 * i + 3]);
+            }
         }
+        m = mc;
     }
     const float inv = 1.f / sum;
     const int64_t row = int64_t(mg.q_row0 + t) * a.n_qo_heads + mg.g * G + h;
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + row * D + lane * kVD;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + row * D + d0;
 #pragma unroll
-    for (int i = 0; i < kVD; i += 2)
-        *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
-    if (a.lse != nullptr && lane == 0) a.lse[row] = (mx + __log2f(sum)) * kLn2;
+    for (int i = 0; i < kVD; i += 8)
+        *reinterpret_cast<uint4*>(dst + i) =
+            make_uint4(pack_bf16x2(acc[i] * inv, acc[i + 1] * inv), pack_bf16x2(acc[i + 2] * inv, acc[i + 3] * inv),
+                       pack_bf16x2(acc[i + 4] * inv, acc[i + 5] * inv), pack_bf16x2(acc[i + 6] * inv, acc[i + 7] * inv));
+    if (a.lse != nullptr && (lane & 15) == 0) a.lse[row] = (m + __log2f(sum)) * kLn2;
 }
 
 template <int D, int G>
@@ -802,7 +815,7 @@ cudaError_t launch_prefill(const PfArgs& a, int n_units, cudaStream_t stream) {
     e = launch_pdl(reinterpret_cast<const void*>(&paged_prefill_kernel<D, G>), dim3(n_units),
                    dim3(PfCfg<D, G>::kThreads), PfCfg<D, G>::kSmem, a, stream);
     if (e != cudaSuccess || a.n_merges == 0) return e;
-    const int warps = a.n_merges * kPfRows;
+    const int warps = (a.n_merges * kPfRows + 1) / 2;  // half a warp per row
     return launch_pdl(reinterpret_cast<const void*>(&prefill_merge_kernel<D, G>),
                       dim3((warps + kPfMergeWarps - 1) / kPfMergeWarps), dim3(32 * kPfMergeWarps),
                       0, a, stream);
