@@ -419,7 +419,8 @@ int paged_prefill_attn(const void* q, const void* k_pool, const void* v_pool,
  * paged_prefill_plan_host — the prefill planner alone, on the host, with no CUDA call
  * (for inspection and tests). Same offset checks as paged_prefill_plan.
  *   split_target : a step with fewer tile units than this has its long ranges split
- *                  (paged_prefill_plan uses two waves of the device's grid); 0 = never
+ *                  (paged_prefill_plan uses two waves of the device's grid, three at
+ *                  head_dim 256); 0 = never
  *   units_out    : [max_units * 8] int32 — per unit {workspace block or -1, KV head,
  *                  first query row, query rows, kv_indptr[b], list position of the
  *                  first query, first list entry, end list entry (exclusive)}

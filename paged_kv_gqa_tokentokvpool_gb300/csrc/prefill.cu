@@ -1044,9 +1044,11 @@ int paged_prefill_plan_create(pkv_prefill_plan** out_plan, int max_batch, int64_
         delete p;
         return fail(PKV_ERR_CUDA, "paged_prefill_plan_create: device or occupancy query failed");
     }
-    // Steps with fewer tile units than two waves of the grid split long causal
-    // ranges into pieces; a split step has at most 2 x target pieces.
-    p->split_target = 2 * sms * per_sm;
+    // Steps with fewer tile units than two waves of the grid (three at head_dim 256,
+    // whose K/V tiles cost about twice as much per entry, so finer pieces pay for
+    // their start-up; both measured best) split long causal ranges into pieces; a
+    // split step has at most 2 x target pieces.
+    p->split_target = (head_dim == 256 ? 3 : 2) * sms * per_sm;
     p->max_merges = p->split_target;
     p->max_blocks = 2 * p->split_target;
     const int64_t units = (max_q_tokens / p->tile_tokens + max_batch) * int64_t(n_kv_heads) +
