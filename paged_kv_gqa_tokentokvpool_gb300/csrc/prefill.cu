@@ -23,9 +23,10 @@
 //    128, 64 at 256), with 16-byte cp.async into separate K and V rings of
 //    shared-memory stages. Each row is stored in the tensor core's 128-byte swizzled
 //    layout (K-major for q and K; V's rows are the same bytes read as an MN-major
-//    operand). A thread's arrival on a stage's barrier rides on its copies, and a
-//    relay thread fences the landed stage (generic to async proxy) for the tensor
-//    core. Two more warps copy the first tokens of every K and V tile (32 of 128 at
+//    operand). Tokens past a range repeat its last row (finite rows the softmax masks),
+//    so every copy is a full one from a per-unit base address. A thread's arrival on a
+//    stage's barrier rides on its copies, and a relay thread fences the landed stage
+//    (generic to async proxy) for the tensor core. Two more warps copy the first tokens of every K and V tile (32 of 128 at
 //    head_dim 128, 20 of 64 at 256) with 4-row TMA gathers (cp.async.bulk.tensor
 //    .tile::gather4) through tensor maps of the pools in that 128-byte swizzled
 //    layout, their bytes counted on the same barrier: the SMs then take in the tiles
@@ -39,16 +40,17 @@
 //    buffer to write P into.
 //  * Four softmax warps own one query row per thread: they read the row of S from
 //    TMEM, apply the causal mask (list position <= the row's query position) and an
-//    online softmax in base 2 with fp32 state, write P as bf16 pairs over the upper half
-//    of the same S buffer, and
-//    rescale O in TMEM when a row's running maximum grows by more than 2^8 (between
-//    rescales the probabilities stay below 2^8, exact enough for bf16 P and fp32
-//    sums). At the end they read O back, divide by the row sum and store out and lse.
+//    online softmax in base 2 with fp32 state (three-input maxima, and the exponent
+//    arguments and row sums two entries to an instruction), write P as bf16 pairs over
+//    the upper half of the same S buffer, and rescale O in TMEM when a row's running
+//    maximum grows by more than 2^8 (between rescales the probabilities stay below
+//    2^8, exact enough for bf16 P and fp32 sums). At the end they read O back, divide
+//    by the row sum and store out and lse.
 //  * Every wait is an mbarrier wait bounded by 1 s; on expiry the CTA records it in
 //    the plan's status word, every role leaves its loop, the MMA and copies in
 //    flight are drained (again bounded) and the tensor memory is freed. Barriers a
-//    reader could fall two phases behind on are split per buffer, so that no parity
-//    test can alias.
+//    reader could fall behind on are split per buffer, so that no parity test can
+//    alias.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
