@@ -244,34 +244,52 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Slot ids of the rows this producer thread copies for KV tile `tile`: piece i is
-// token (pt + i * kPfHalfThreads) / kChunks. Tokens past the range repeat the range's
-// last row (finite rows that the softmax masks), so every copy is a full one.
+// A producer thread's pieces of a K (or V) tile: piece i is token kTmaTok + tokA +
+// i * kStep (tokA = pt / kChunks < kStep), in its 16-byte column pt % kChunks.
 template <int D, int G>
-__device__ __forceinline__ void load_tile_slots(const PfArgs& a, const PfUnit& un, int tile, int pt,
+struct PfPieces {
+    using C = PfCfg<D, G>;
+    static constexpr int kStep = kPfHalfThreads / C::kChunks;
+    static constexpr int kPeriod = 8 / kStep;  // pieces per 8-row swizzle atom
+    static_assert(kPfHalfThreads % C::kChunks == 0 && 8 % kStep == 0, "piece layout");
+};
+
+// Slot ids of the rows this producer thread copies for KV tile `tile`. Tokens past the
+// range repeat the range's last row (finite rows that the softmax masks), so every copy
+// is a full one; on a tile wholly inside the range (all but a range's last) no entry
+// needs that clamp and each id is one load at a fixed offset.
+template <int D, int G>
+__device__ __forceinline__ void load_tile_slots(const int32_t* ids, int kv_hi, int tile, int tokA,
                                                 int (&slot)[PfCfg<D, G>::kTilePieces]) {
     using C = PfCfg<D, G>;
-    const int32_t* ids = a.kv_indices + un.kv_begin;
+    constexpr int kStep = PfPieces<D, G>::kStep;
+    const int first = tile * C::kKv + C::kTmaTok + tokA;  // this thread's first token
+    const int32_t* p = ids + first;
+    if ((tile + 1) * C::kKv <= kv_hi) {
 #pragma unroll
-    for (int i = 0; i < C::kTilePieces; ++i) {
-        const int tok = C::kTmaTok + (pt + i * kPfHalfThreads) / C::kChunks;
-        slot[i] = __ldg(ids + min(tile * C::kKv + tok, un.kv_hi - 1));
+        for (int i = 0; i < C::kTilePieces; ++i) slot[i] = __ldg(p + i * kStep);
+    } else {
+        const int last = kv_hi - 1 - first;  // the range's last entry, from the first token
+#pragma unroll
+        for (int i = 0; i < C::kTilePieces; ++i) slot[i] = __ldg(p + min(i * kStep, last));
     }
 }
 
 // cp.async of this thread's pieces of a K (or V) tile into the stage at shared address
 // `dst`. `src` is this thread's 16 bytes of the row of slot 0 (its KV head and its
 // 16-byte column, the same for every piece), `row_bytes` the pool's bytes per slot.
+// lo[r] is the swizzled offset of piece r; piece r + kPeriod * q lies 1024 q bytes
+// (q atoms of 8 rows) further.
 template <int D, int G>
-__device__ __forceinline__ void issue_tile(const char* src, uint32_t row_bytes, uint32_t dst, int pt,
+__device__ __forceinline__ void issue_tile(const char* src, uint32_t row_bytes, uint32_t dst,
+                                           const uint32_t (&lo)[PfPieces<D, G>::kPeriod],
                                            const int (&slot)[PfCfg<D, G>::kTilePieces]) {
     using C = PfCfg<D, G>;
+    constexpr int kPeriod = PfPieces<D, G>::kPeriod;
 #pragma unroll
-    for (int i = 0; i < C::kTilePieces; ++i) {
-        const int c = pt + i * kPfHalfThreads;
-        const int tok = C::kTmaTok + c / C::kChunks, part = c % C::kChunks;
-        cp_async16_full(dst + sw128_off(tok, part, C::kKv), src + size_t(uint32_t(slot[i])) * row_bytes);
-    }
+    for (int i = 0; i < C::kTilePieces; ++i)
+        cp_async16_full(dst + lo[i % kPeriod] + uint32_t(1024 * (i / kPeriod)),
+                        src + size_t(uint32_t(slot[i])) * row_bytes);
 }
 
 // Four rows of a 2D tensor map (row indices r0..r3, columns col .. col + 63) into 512
@@ -371,21 +389,27 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
                 cp_async16(base + C::kQOff + sw128_off(r, part, kPfRows), q + off, valid);
             }
         }
-        static_assert(kPfHalfThreads % C::kChunks == 0, "a thread's 16-byte column is fixed");
         const uint32_t row_bytes = uint32_t(a.n_kv_heads) * D * 2;
         const char* src = static_cast<const char*>(half ? a.v_pool : a.k_pool) +
                           (size_t(un.g) * D + (pt % C::kChunks) * 8) * 2;
         const uint32_t ring = base + (half ? C::kVOff : C::kKOff);
+        using PP = PfPieces<D, G>;
+        const int tokA = pt / C::kChunks, col = pt % C::kChunks;
+        uint32_t lo[PP::kPeriod];
+#pragma unroll
+        for (int r = 0; r < PP::kPeriod; ++r)
+            lo[r] = sw128_off(C::kTmaTok + tokA + r * PP::kStep, col, C::kKv);
+        const int32_t* ids = a.kv_indices + un.kv_begin;
         int slot[C::kTilePieces];
-        if (n_copy_tiles > 0) load_tile_slots<D, G>(a, un, t0, pt, slot);
+        if (n_copy_tiles > 0) load_tile_slots<D, G>(ids, un.kv_hi, t0, tokA, slot);
         for (int n = 0; n < n_copy_tiles; ++n) {
             const int st = n % C::kStages;
             if (n >= C::kStages &&
                 !pf_wait(empty(half, st), uint32_t((n / C::kStages - 1) & 1), a.status, abort_flag))
                 break;
-            issue_tile<D, G>(src, row_bytes, ring + st * C::kKvBytes, pt, slot);
+            issue_tile<D, G>(src, row_bytes, ring + st * C::kKvBytes, lo, slot);
             cp_async_arrive(landed(half, st));
-            if (n + 1 < n_tiles) load_tile_slots<D, G>(a, un, t0 + n + 1, pt, slot);
+            if (n + 1 < n_tiles) load_tile_slots<D, G>(ids, un.kv_hi, t0 + n + 1, tokA, slot);
         }
         cp_async_wait<0>();  // nothing may still write this CTA's shared memory at exit
     } else if (warp == kPfMmaWarp) {
