@@ -147,7 +147,12 @@ struct PfCfg {
     // its issuing thread about as much time as a 128 x 128 x 16 step takes the
     // tensor core, so the MMAs are made as large as shared memory allows.
     static constexpr int kKv = D == 128 ? 128 : 64;
-    static constexpr int kStages = D == 128 ? 3 : 2;
+    static constexpr int kKStages = D == 128 ? 3 : 2;  // K ring stages
+    static constexpr int kVStages = D == 128 ? 3 : 2;  // V ring stages
+    static constexpr int kRingStages = kKStages + kVStages;
+    // stages of ring v (0: K, 1: V) and the index of its stage s among both rings
+    __host__ __device__ static constexpr int stages(int v) { return v ? kVStages : kKStages; }
+    __host__ __device__ static constexpr int ring_slot(int v, int s) { return (v ? kKStages : 0) + s; }
     // TMEM columns: S buffer b at b * kKv (fp32; P of its tile, kKv / 2 columns of
     // bf16 pairs, the A operand of P V, over its upper half), O in the last D columns
     static constexpr int kOCol = int(kPfTmemCols) - D;
@@ -158,12 +163,12 @@ struct PfCfg {
     static constexpr int kKvBytes = kPanels * kKvPanel;     // K (or V) of one stage
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + kQBytes;
-    static constexpr int kVOff = kKOff + kStages * kKvBytes;
-    static constexpr int kBarOff = kVOff + kStages * kKvBytes;
-    // mbarriers: for K and for V rings each landed / full / empty [kStages];
+    static constexpr int kVOff = kKOff + kKStages * kKvBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kKvBytes;
+    // mbarriers: landed / full / empty per stage of the K and V rings;
     // s_full, p_full and o_done per S buffer, drain; then the TMEM address and the
     // abort flag
-    static constexpr int kNumBars = 6 * kStages + 3 * kPfSBufs + 1;
+    static constexpr int kNumBars = 3 * kRingStages + 3 * kPfSBufs + 1;
     static constexpr int kTmemOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemOff + 4;
     static constexpr int kSmem = kAbortOff + 4 + 1024;      // + slack to align the base
@@ -316,10 +321,10 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
     const uint32_t bars = base + C::kBarOff;
     // ring barriers of K (v = 0) and V (v = 1): landed (the producers' copies are in
     // shared memory), full (announced to the tensor core), empty (read by it)
-    const auto landed = [&](int v, int s) { return bars + 8u * ((0 + v) * C::kStages + s); };
-    const auto full = [&](int v, int s) { return bars + 8u * ((2 + v) * C::kStages + s); };
-    const auto empty = [&](int v, int s) { return bars + 8u * ((4 + v) * C::kStages + s); };
-    const uint32_t bars2 = bars + 8u * 6 * C::kStages;
+    const auto landed = [&](int v, int s) { return bars + 8u * C::ring_slot(v, s); };
+    const auto full = [&](int v, int s) { return bars + 8u * (C::kRingStages + C::ring_slot(v, s)); };
+    const auto empty = [&](int v, int s) { return bars + 8u * (2 * C::kRingStages + C::ring_slot(v, s)); };
+    const uint32_t bars2 = bars + 8u * 3 * C::kRingStages;
     // S of tile n written / P of tile n written / P V of tile n done: one barrier per
     // S buffer (tiles n, n + 3, ...; phase parity (n / 3) & 1). No role can run three
     // tiles ahead of a barrier's other side, so no parity test can alias.
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
 
     if (tid == 0) {
         for (int v = 0; v < 2; ++v)
-            for (int s = 0; s < C::kStages; ++s) {
+            for (int s = 0; s < C::stages(v); ++s) {
                 // the producer threads' cp.async arrivals (and the TMA warp's byte count)
                 mbar_init(landed(v, s), kPfHalfThreads + (C::kTmaTok > 0 ? 1 : 0));
                 mbar_init(full(v, s), 1);
@@ -367,8 +372,9 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
     if (warp >= kPfSoftmaxWarps && warp < kPfMmaWarp) {
         // ================= producers =================
         // Two halves: one gathers K tiles (and the unit's q rows), the other V tiles.
-        // K tile n goes to K stage n % kStages once S of tile n - kStages has read it,
-        // V tile n once P V of tile n - kStages has, so the next K tiles are not held
+        // K tile n goes to K stage n % kKStages once S of tile n - kKStages has read it,
+        // V tile n to V stage n % kVStages once P V of tile n - kVStages has, so the
+        // next K tiles are not held
         // back by the P V products. Each thread's arrival on the stage's `landed`
         // barrier is attached to its copies, so it completes the moment the rows are
         // in shared memory; the relay warp then announces the stage to the tensor core.
@@ -403,9 +409,10 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
         int slot[C::kTilePieces];
         if (n_copy_tiles > 0) load_tile_slots<D, G>(ids, un.kv_hi, t0, tokA, slot);
         for (int n = 0; n < n_copy_tiles; ++n) {
-            const int st = n % C::kStages;
-            if (n >= C::kStages &&
-                !pf_wait(empty(half, st), uint32_t((n / C::kStages - 1) & 1), a.status, abort_flag))
+            const int stages = C::stages(half);
+            const int st = n % stages;
+            if (n >= stages &&
+                !pf_wait(empty(half, st), uint32_t((n / stages - 1) & 1), a.status, abort_flag))
                 break;
             issue_tile<D, G>(src, row_bytes, ring + st * C::kKvBytes, lo, slot);
             cp_async_arrive(landed(half, st));
@@ -433,12 +440,12 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
             bool progress = false;
             bool go = false;
             if (leader && ns < n_tiles)
-                go = mbar_test(full(0, ns % C::kStages), uint32_t((ns / C::kStages) & 1)) &&
+                go = mbar_test(full(0, ns % C::kKStages), uint32_t((ns / C::kKStages) & 1)) &&
                      (ns < kPfSBufs || mbar_test(o_done(ns), ph(ns - kPfSBufs)));
             if (__shfl_sync(kFullMask, go, 0)) {
                 tc::fence_after_sync();
                 // descriptor start addresses advance in 16-byte units (low bits)
-                const uint64_t kd = k_desc + uint64_t(((ns % C::kStages) * C::kKvBytes) >> 4);
+                const uint64_t kd = k_desc + uint64_t(((ns % C::kKStages) * C::kKvBytes) >> 4);
                 const uint32_t s_tmem = tmem + uint32_t((ns % kPfSBufs) * C::kKv);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -447,24 +454,24 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
                     tc::mma_bf16_ss_if(leader, s_tmem, q_desc + off, kd + koff, C::kIdescS, ks > 0);
                 }
                 tc::commit_if(leader, s_full(ns));
-                tc::commit_if(leader, empty(0, ns % C::kStages));
+                tc::commit_if(leader, empty(0, ns % C::kKStages));
                 ++ns;
                 progress = true;
             }
             go = false;
             if (leader && npv < ns)
                 go = mbar_test(p_full(npv), ph(npv)) &&
-                     mbar_test(full(1, npv % C::kStages), uint32_t((npv / C::kStages) & 1));
+                     mbar_test(full(1, npv % C::kVStages), uint32_t((npv / C::kVStages) & 1));
             if (__shfl_sync(kFullMask, go, 0)) {
                 tc::fence_after_sync();
-                const uint64_t vd = v_desc + uint64_t(((npv % C::kStages) * C::kKvBytes) >> 4);
+                const uint64_t vd = v_desc + uint64_t(((npv % C::kVStages) * C::kKvBytes) >> 4);
                 const uint32_t p_tmem = tmem + uint32_t((npv % kPfSBufs) * C::kKv + C::kKv / 2);
 #pragma unroll
                 for (int ks = 0; ks < C::kKv / 16; ++ks)
                     tc::mma_bf16_ts_if(leader, o_tmem, p_tmem + uint32_t(8 * ks),
                                        vd + uint64_t((ks * 16 * 128) >> 4), C::kIdescO, npv > 0 || ks > 0);
                 tc::commit_if(leader, o_done(npv));
-                tc::commit_if(leader, empty(1, npv % C::kStages));
+                tc::commit_if(leader, empty(1, npv % C::kVStages));
                 ++npv;
                 progress = true;
             }
@@ -517,11 +524,12 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
             if (n_copy > 0) load_ids(t0);
             int issued = 0;
             for (int n = 0; n < n_copy; ++n) {
-                const int st = n % C::kStages;
-                if (n >= C::kStages) {
+                const int stages = C::stages(half);
+                const int st = n % stages;
+                if (n >= stages) {
                     bool ok = true;
                     if (lane == 0)
-                        ok = pf_wait(empty(half, st), uint32_t((n / C::kStages - 1) & 1), a.status, abort_flag);
+                        ok = pf_wait(empty(half, st), uint32_t((n / stages - 1) & 1), a.status, abort_flag);
                     if (!__shfl_sync(kFullMask, ok, 0)) break;
                 }
                 if (lane == 0) mbar_arrive_expect_tx(landed(half, st), uint32_t(C::kTmaTok * D * 2));
@@ -539,9 +547,10 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
             // nothing may still write this CTA's shared memory at exit: wait (bounded)
             // for the last fill of every stage
             if (lane == 0) {
-                for (int k = issued - C::kStages; k < issued; ++k) {
+                for (int k = issued - C::stages(half); k < issued; ++k) {
                     if (k < 0) continue;
-                    const uint32_t bar = landed(half, k % C::kStages), par = uint32_t((k / C::kStages) & 1);
+                    const uint32_t bar = landed(half, k % C::stages(half)),
+                                   par = uint32_t((k / C::stages(half)) & 1);
                     const unsigned long long t_wait = pf_global_ns();
                     while (!mbar_try_wait(bar, par) && pf_global_ns() - t_wait < kPfWaitNs) {
                     }
@@ -564,9 +573,10 @@ __global__ void __launch_bounds__(PfCfg<D, G>::kThreads, 1)
 #pragma unroll
                 for (int v = 0; v < 2; ++v) {
                     const int n = nr[v];
-                    if (n < n_tiles && mbar_test(landed(v, n % C::kStages), uint32_t((n / C::kStages) & 1))) {
+                    if (n < n_tiles &&
+                        mbar_test(landed(v, n % C::stages(v)), uint32_t((n / C::stages(v)) & 1))) {
                         tc::fence_proxy_async_smem();
-                        mbar_arrive(full(v, n % C::kStages));
+                        mbar_arrive(full(v, n % C::stages(v)));
                         nr[v] = n + 1;
                         progress = true;
                     }
