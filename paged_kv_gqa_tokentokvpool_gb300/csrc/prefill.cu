@@ -27,7 +27,7 @@
 //    so every copy is a full one from a per-unit base address. A thread's arrival on a
 //    stage's barrier rides on its copies, and a relay thread fences the landed stage
 //    (generic to async proxy) for the tensor core. Two more warps copy the first tokens of every K and V tile (32 of 128 at
-//    head_dim 128, 20 of 64 at 256) with 4-row TMA gathers (cp.async.bulk.tensor
+//    head_dim 128, 16 of 64 at 256) with 4-row TMA gathers (cp.async.bulk.tensor
 //    .tile::gather4) through tensor maps of the pools in that 128-byte swizzled
 //    layout, their bytes counted on the same barrier: the SMs then take in the tiles
 //    by both paths at once.
@@ -133,9 +133,9 @@ struct PfArgs {
 };
 
 // Tokens of every K and V tile copied by the tensor memory accelerator's gather form
-// (two more warps), the rest by the producer threads' cp.async: measured best at 20
+// (two more warps), the rest by the producer threads' cp.async: measured best at 16
 // of 64 at head_dim 256 and 32 of 128 at head_dim 128.
-constexpr int pf_tma_tokens(int head_dim) { return head_dim == 256 ? 20 : 32; }
+constexpr int pf_tma_tokens(int head_dim) { return head_dim == 256 ? 16 : 32; }
 
 // Shared memory of one CTA (offsets from a 1024-byte aligned base). Every operand
 // is stored as 64-element panels of 128-byte rows in the 128-byte swizzled layout:
